@@ -1,0 +1,543 @@
+"""Throughput benchmark: 4K -> 1080p RGB uint8 bilinear resize on one GB300.
+
+One step = one bilinear resize of a 3840x2160 RGB u8 frame to 1920x1080
+through the C ABI (resize_u8), the whole hot path (tables come from the plan,
+built once per geometry, outside the timed region).  The frames are the
+smooth synthetic content (sum of sinusoids + noise) in a ring of 16 device
+frames (498 MB of source + output, over 3x the 129 MB L2), so every step
+reads its input from HBM.  Steps are replayed from CUDA graphs of 96 launches
+(one launch per step, back to back on one stream); K steps are timed with
+CUDA events after W warm-up steps, with a barrier and device synchronise on
+both sides.
+
+Printed (one JSON line): output Gpix/s (`value`), the dominant kernel's
+roofline (algorithmic bytes per launch / average launch duration, against the
+measured HBM copy peak), the end-to-end figure through resize_u8_host from
+page-locked host buffers, the oracle timed on the host cores, and the SM
+clocks sampled during the timed region.
+
+`--impl reference` times the CPU oracle (the only other implementation of the
+method) on the same workload instead, each step a bounded band of output rows.
+`--workload` selects one of the other resize workloads for local studies; the
+default is the headline one.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+MB = 1e6
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCE = os.path.join(ROOT, "bilinear_image_resize_gb300", "csrc", "kernels.cu")
+
+# name -> (description, kind, H, W, OH, OW, C, mode, batch)
+WORKLOADS = {
+    "4k_to_1080p": ("4K->1080p RGB u8 bilinear (3840x2160 -> 1920x1080, smooth synthetic)",
+                    "u8", 2160, 3840, 1080, 1920, 3, "linear", 1),
+    "1080p_to_4k": ("1080p->4K RGB u8 bilinear upscale (1920x1080 -> 3840x2160)", "u8", 1080, 1920, 2160, 3840, 3,
+                    "linear", 1),
+    "4k_to_1080p_nearest": ("4K->1080p RGB u8 nearest", "u8", 2160, 3840, 1080, 1920, 3, "nearest", 1),
+    "1080p_to_540p": ("1080p->960x540 RGB u8 bilinear", "u8", 1080, 1920, 540, 960, 3, "linear", 1),
+    "1080p_to_720p": ("1080p->1280x720 RGB u8 bilinear", "u8", 1080, 1920, 720, 1280, 3, "linear", 1),
+    "batch64_720p_to_224_norm": ("64x 1280x720 RGB u8 -> 224x224 bilinear + normalise, f32 NCHW", "norm", 720, 1280,
+                                 224, 224, 3, "linear", 64),
+    "f32_8192_to_5980_filter3x3": ("f32 8192x8192 -> 5980x5980 bilinear + 3x3 filter", "filt", 8192, 8192, 5980,
+                                   5980, 1, "linear", 1),
+    "tiny_64x48_to_128x96": ("u8 64x48 -> 128x96 bilinear", "u8", 48, 64, 96, 128, 1, "linear", 1),
+}
+DEFAULT_WORKLOAD = "4k_to_1080p"
+METRIC = "output Gpix/s and achieved HBM GB/s (% of GB300 peak), 4K->1080p RGB u8 bilinear"
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def algorithmic_bytes(kind, H, W, OH, OW, C, mode, batch):
+    """Bytes the method must move per launch: every source row a tap reads
+    (whole rows: every 32-byte sector of a tapped row holds a tap at these
+    ratios) plus the output."""
+    import bilinear_image_resize_gb300 as rz
+    m = rz.RZ_LINEAR if mode == "linear" else rz.RZ_NEAREST
+    yofs, _, _ = rz.resize_axis_table(H, OH, m)
+    rows = set(int(r) for r in yofs)
+    if m == rz.RZ_LINEAR:
+        rows |= set(min(int(r) + 1, H - 1) for r in yofs)
+    in_es = 4 if kind == "filt" else 1
+    out_es = 1 if kind == "u8" else 4
+    read = len(rows) * W * C * in_es
+    write = OH * OW * C * out_es
+    return batch * read, batch * write
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms in a thread."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for (t, line) in self.samples:
+            if not (t0 <= t <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm.append(float(parts[2]))
+                smax = float(parts[3])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def profile_traffic(workload: str):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, or None when the summary is missing or the kernel source has
+    changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", f"ncu_{workload}.md")
+    try:
+        with open(path) as f:
+            text = f.read()
+        with open(KERNEL_SOURCE, "rb") as f:
+            src_hash = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m_hash = re.search(r"kernels\.cu sha256\[:16\]:\s*`?([0-9a-f]{16})", text)
+    m_bytes = re.search(r"dram bytes per launch:\s*`?([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != src_hash:
+        return None
+    return int(m_bytes.group(1))
+
+
+# ------------------------------------------------------------------ the GPU arm
+
+def make_frames(kind, H, W, C, batch, count, dev):
+    import numpy as np
+    import torch
+
+    from bilinear_image_resize_gb300 import synth
+    if kind == "u8":
+        base = synth.smooth_rgb(W, H, 3) if (C == 3 and W >= 1920) else synth.random_u8((H, W, C), seed=3)
+        if base.shape != (H, W, C):
+            base = synth.random_u8((H, W, C), seed=3)
+        t = torch.from_numpy(np.ascontiguousarray(base)).to(dev)
+        frames = [t.clone() for _ in range(count)]
+        for i, f in enumerate(frames):        # distinct content per frame, same statistics
+            if i:
+                f.copy_(torch.roll(t, shifts=7 * i, dims=1))
+        return frames
+    if kind == "norm":
+        base = torch.from_numpy(synth.frames_rgb(batch, W, H, 4)).to(dev)
+        return [base.clone() if i else base for i in range(count)]
+    base = torch.from_numpy(synth.float_gray(W, H, 5)).to(dev)
+    return [base.clone() if i else base for i in range(count)]
+
+
+def make_outputs(kind, OH, OW, C, batch, count, dev):
+    import torch
+    if kind == "u8":
+        shape, dt = (OH, OW, C), torch.uint8
+    elif kind == "norm":
+        shape, dt = (batch, C, OH, OW), torch.float32
+    else:
+        shape, dt = (OH, OW), torch.float32
+    return [torch.empty(shape, dtype=dt, device=dev) for _ in range(count)]
+
+
+def gpu_arm(args, rank, local_rank, world):
+    import numpy as np
+    import torch
+
+    import bilinear_image_resize_gb300 as rz
+    from bilinear_image_resize_gb300 import synth
+
+    desc, kind, H, W, OH, OW, C, mode_s, batch = WORKLOADS[args.workload]
+    mode = rz.RZ_LINEAR if mode_s == "linear" else rz.RZ_NEAREST
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    rd, wr = algorithmic_bytes(kind, H, W, OH, OW, C, mode_s, batch)
+    step_bytes = rd + wr
+    in_bytes = batch * H * W * C * (4 if kind == "filt" else 1)
+    out_bytes = wr
+    ring = max(2, min(64, int(3 * L2_BYTES // (in_bytes + out_bytes)) + 1))
+    frames = make_frames(kind, H, W, C, batch, ring, dev)
+    outs = make_outputs(kind, OH, OW, C, batch, ring, dev)
+    plan = rz.resize_plan_create(H, W, OH, OW, mode)
+    if args.tile:
+        tr, tw = (int(v) for v in args.tile.split("x"))
+        fam = {"u8": rz.KIND_U8, "norm": rz.KIND_NORMALIZE, "filt": rz.KIND_FILTER3X3}[kind]
+        rz.resize_plan_set_tile(plan, fam, tr, tw)
+    epi = None
+    if kind == "norm":
+        epi = rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=synth.NORM_MEAN, std=synth.NORM_STD)
+    elif kind == "filt":
+        epi = rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=synth.filter_weights())
+
+    def step(i):
+        s, d = frames[i % ring], outs[i % ring]
+        if kind == "u8":
+            rz.resize_u8(plan, s, d, stream=stream)
+        else:
+            rz.resize_fused(plan, s, d, epi, stream=stream)
+
+    torch.cuda.synchronize()
+    # warm-up, eager (also sets kernel attributes before any capture)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize()
+
+    G = min(96, max(1, args.steps))
+    G -= G % ring if G >= ring else 0
+    G = max(G, 1)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i)
+        return g
+
+    g_full = capture(G)
+    rem = args.steps % G
+    g_rem = capture(rem) if rem else None
+    reps = args.steps // G
+    # graph warm-up replays
+    g_full.replay()
+    torch.cuda.synchronize()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    sampler = ClockSampler(visible[local_rank] if local_rank < len(visible) else local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    # keep the GPU busy for a moment before the timed region so clocks settle
+    for _ in range(max(1, int(0.3 / max(1e-6, G * 10e-6)))):
+        g_full.replay()
+    torch.cuda.synchronize()
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    ev0.record(stream)
+    for _ in range(reps):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    if dist:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    time.sleep(0.1)
+    sampler.stop()
+    clocks = sampler.summary(t_host0 - 0.02, t_host1 + 0.02)
+
+    ms_max = ms
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+
+    # eager (per-call launch) rate, for reference
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        n_eager = min(args.steps, 2000)
+        for i in range(n_eager):
+            step(i)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = ev0.elapsed_time(ev1) / n_eager
+
+    # end to end through resize_u8_host (u8 workloads): pinned host frames,
+    # H2D + kernel + D2H every step, three streams in rotation
+    e2e = None
+    if kind == "u8":
+        e2e = e2e_u8(rz, plan, frames[0], H, W, OH, OW, C, dev, n=max(10, min(args.steps, 200)))
+
+    px = OH * OW * batch
+    value = px * args.steps * world / (ms_max / 1e3) / 1e9
+    launch_ms = ms / args.steps
+    achieved = step_bytes / (launch_ms / 1e3) / 1e9
+    peaks, src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    res = {
+        "value": value, "ms": ms_max, "launch_ms": launch_ms, "eager_ms_per_step": eager_ms,
+        "achieved_gbs": achieved, "peak_gbs": peak, "peak_src": src, "step_bytes": step_bytes,
+        "read_bytes": rd, "write_bytes": wr, "ring": ring, "graph_steps": G, "clocks": clocks, "e2e": e2e,
+        "desc": desc, "px": px,
+    }
+    plan.destroy()
+    return res
+
+
+def e2e_u8(rz, plan, dev_frame, H, W, OH, OW, C, dev, n):
+    import torch
+    host_src = [dev_frame.cpu().pin_memory() for _ in range(2)]
+    host_dst = [torch.empty((OH, OW, C), dtype=torch.uint8).pin_memory() for _ in range(3)]
+    streams = [torch.cuda.Stream(device=dev) for _ in range(3)]
+    dsrc = [torch.empty((H, W, C), dtype=torch.uint8, device=dev) for _ in range(3)]
+    ddst = [torch.empty((OH, OW, C), dtype=torch.uint8, device=dev) for _ in range(3)]
+    for i in range(3):     # warm-up
+        rz.resize_u8_host(plan, host_src[i % 2], host_dst[i], dsrc[i], ddst[i], stream=streams[i])
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    main = torch.cuda.current_stream(dev)
+    start.record(main)
+    for s in streams:
+        s.wait_event(start)
+    for i in range(n):
+        k = i % 3
+        rz.resize_u8_host(plan, host_src[i % 2], host_dst[k], dsrc[k], ddst[k], stream=streams[k])
+    for k in range(3):
+        ends[k].record(streams[k])
+    torch.cuda.synchronize()
+    ms = max(start.elapsed_time(e) for e in ends)
+    return {"value": OH * OW * n / (ms / 1e3) / 1e9, "unit": "Gpix/s",
+            "h2d_bytes_per_step": H * W * C, "d2h_bytes_per_step": OH * OW * C,
+            "ms_per_step": ms / n, "streams": 3, "steps": n}
+
+
+# ------------------------------------------------------------------ the oracle on the host
+
+def oracle_rate(workload, budget_s):
+    """Gpix/s of the oracle over a bounded sample: whole output bands of the
+    workload, repeated until `budget_s` of single-threaded CPU time."""
+    import numpy as np
+
+    import oracle
+    from bilinear_image_resize_gb300 import synth
+    desc, kind, H, W, OH, OW, C, mode, batch = WORKLOADS[workload]
+    if kind == "u8":
+        img = synth.smooth_rgb(W, H, 3) if (C == 3 and W >= 1920) else synth.random_u8((H, W, C), seed=3)
+        if mode == "linear":
+            def run(rows):
+                return oracle.linear_u8_rows(img, OH, OW, 0, rows)
+        else:
+            def run(rows):
+                return oracle.nearest_u8(img, OH, OW)
+    elif kind == "norm":
+        frames = synth.frames_rgb(batch, W, H, 4)
+
+        def run(rows):
+            return oracle.linear_u8_normalize(frames[0], OH, OW, synth.NORM_MEAN, synth.NORM_STD)
+    else:
+        img = synth.float_gray(W, H, 5)
+        w = synth.filter_weights()
+
+        def run(rows):
+            return oracle.linear_f32_filter3x3(img, OH, OW, w)
+    t0 = time.perf_counter()
+    run(min(OH, 8))
+    probe = time.perf_counter() - t0
+    rows_full = OH if (kind == "u8" and mode == "linear") else None
+    n_px = 0
+    calls = 0
+    t0 = time.perf_counter()
+    while True:
+        if rows_full:
+            run(rows_full)
+            n_px += OH * OW
+        else:
+            run(None)
+            n_px += OH * OW
+        calls += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return n_px / dt / 1e9, calls, dt, probe
+
+
+def reference_arm(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    desc, kind, H, W, OH, OW, C, mode, batch = WORKLOADS[args.workload]
+    import oracle
+    from bilinear_image_resize_gb300 import synth
+    import numpy as np
+    img = synth.smooth_rgb(W, H, 3) if (kind == "u8" and C == 3 and W >= 1920) else None
+    if kind != "u8" or mode != "linear" or img is None:
+        value, calls, dt, _ = oracle_rate(args.workload, 10.0)
+        total_s = dt
+        steps_px = None
+    else:
+        # each step: a band of output rows sized so that W + K steps take about a minute
+        t0 = time.perf_counter()
+        oracle.linear_u8_rows(img, OH, OW, 0, OH)
+        per_frame = time.perf_counter() - t0
+        budget = 60.0 / max(1, args.steps + args.warmup)
+        rows = int(max(1, min(OH, OH * budget / max(per_frame, 1e-6))))
+        for _ in range(args.warmup):
+            oracle.linear_u8_rows(img, OH, OW, 0, rows)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle.linear_u8_rows(img, OH, OW, 0, rows)
+        total_s = time.perf_counter() - t0
+        value = rows * OW * args.steps / total_s / 1e9
+        steps_px = rows * OW
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "Gpix/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s * 1e3 / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": desc, "sample": f"{steps_px} output pixels (a band of rows) per step"
+                   if steps_px else "whole outputs, 10 s", "threads": 1},
+        "cpu_baseline": {"value": value, "unit": "Gpix/s", "cores": 1, "kind": "oracle",
+                         "sample": f"bands of {steps_px} output pixels per step, single-threaded C oracle"},
+        "e2e": {"value": value, "unit": "Gpix/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--tile", default="", help="override tile as ROWSxCOLS (tuning only)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+
+    import __graft_entry__
+    __graft_entry__.build()
+
+    r = gpu_arm(args, rank, local_rank, world)
+
+    if rank == 0:
+        cpu = None
+        if world == 1:
+            v, calls, dt, _ = oracle_rate(args.workload, args.cpu_budget)
+            cpu = {"value": v, "unit": "Gpix/s", "cores": 1, "kind": "oracle",
+                   "sample": f"{calls} whole outputs of this workload in {dt:.1f} s, single-threaded C oracle"}
+        traffic = profile_traffic(args.workload)
+        desc = r["desc"]
+        line = {
+            "metric": METRIC,
+            "value": r["value"],
+            "unit": "Gpix/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": r["ms"] / args.steps,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "u8" if WORKLOADS[args.workload][1] == "u8" else "f32",
+            "data": "synthetic",
+            "config": {
+                "workload": desc,
+                "l2": f"ring of {r['ring']} distinct input/output sets "
+                      f"({r['ring'] * (r['read_bytes'] + r['write_bytes']) / MB:.0f} MB) > 3x L2; every step L2-cold",
+                "launch": f"CUDA graphs of {r['graph_steps']} resize_u8 launches, one stream",
+                "algorithmic_bytes_per_step": r["step_bytes"],
+                "parallelism": f"{world} independent replica(s)",
+            },
+            "hbm_gbs": r["achieved_gbs"],
+            "roofline": {
+                "bound": "hbm",
+                "achieved": r["achieved_gbs"],
+                "peak": r["peak_gbs"],
+                "unit": "GB/s",
+                "frac": r["achieved_gbs"] / r["peak_gbs"],
+                "peak_source": f"{r['peak_src']} HBM copy (MEASURED_PEAKS.json hbm_gbs)",
+                "traffic": traffic,
+            },
+            "cpu_baseline": cpu,
+            "e2e": r["e2e"],
+            "gpu_launches": args.steps,
+            "eager_ms_per_step": r["eager_ms_per_step"],
+            "clocks": r["clocks"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,231 @@
-"""GB300-native image resize (placeholder; the binding is added with the library)."""
+"""GB300-native image resize: Python binding of the C ABI (include/gbresize.h).
+
+Every function here only marshals arguments (torch tensors -> device pointers,
+byte pitches, the current CUDA stream) and calls the C entry point of the
+same name; all computation runs in the library's CUDA kernels.  A non-zero
+status raises ``ResizeError``.
+
+Images are torch tensors laid out HWC (or HW for one channel) with the last
+two dimensions packed; the row pitch is taken from ``stride(0)``, so row
+padding (a view into a wider buffer) is allowed.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _native
+from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_EPI_FILTER3X3,
+                      RZ_EPI_NORMALIZE_NCHW, RZ_ERR_ARG, RZ_ERR_CUDA, RZ_ERR_NOMEM, RZ_ERR_TIMEOUT,
+                      RZ_ERR_UNSUPPORTED, RZ_F32, RZ_LINEAR, RZ_MAX_DIM, RZ_NEAREST, RZ_OK, RZ_U8, RzEpilogue)
+
+__all__ = [
+    "ResizeError", "Plan", "resize_plan_create", "resize_plan_destroy", "resize_plan_status",
+    "resize_plan_set_tile", "resize_u8", "resize_f32", "resize_fused", "resize_u8_host",
+    "resize_axis_table", "resize_strerror", "resize_last_cuda_error", "make_epilogue",
+    "RZ_LINEAR", "RZ_NEAREST", "RZ_U8", "RZ_F32", "RZ_EPI_NORMALIZE_NCHW", "RZ_EPI_FILTER3X3",
+    "RZ_OK", "RZ_ERR_ARG", "RZ_ERR_UNSUPPORTED", "RZ_ERR_CUDA", "RZ_ERR_NOMEM", "RZ_ERR_TIMEOUT",
+    "RZ_MAX_DIM", "KIND_U8", "KIND_F32", "KIND_NORMALIZE", "KIND_FILTER3X3",
+]
+
+
+class ResizeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        lib = _native.load()
+        msg = lib.resize_strerror(code).decode()
+        if code == RZ_ERR_CUDA:
+            msg += f" (cudaError {lib.resize_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [status {code}]")
+        self.code = code
+
+
+def _check(code: int, where: str) -> None:
+    if code != RZ_OK:
+        raise ResizeError(code, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Plan:
+    """Owns an ``rz_plan`` handle; freed by ``resize_plan_destroy`` or on collection."""
+
+    def __init__(self, handle: int, in_h: int, in_w: int, out_h: int, out_w: int, mode: int):
+        self.handle = handle
+        self.in_h, self.in_w, self.out_h, self.out_w, self.mode = in_h, in_w, out_h, out_w, mode
+
+    def destroy(self) -> None:
+        if self.handle:
+            h, self.handle = self.handle, None
+            _check(_native.load().resize_plan_destroy(h), "resize_plan_destroy")
+
+    def __del__(self):
+        try:
+            if self.handle:
+                _native.load().resize_plan_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.destroy()
+
+
+def resize_plan_create(in_h: int, in_w: int, out_h: int, out_w: int, mode: int = RZ_LINEAR, stream=None) -> Plan:
+    h = ctypes.c_void_p()
+    _check(_native.load().resize_plan_create(ctypes.byref(h), in_h, in_w, out_h, out_w, mode, _stream(stream)),
+           "resize_plan_create")
+    return Plan(h.value, in_h, in_w, out_h, out_w, mode)
+
+
+def resize_plan_destroy(plan: Plan) -> None:
+    plan.destroy()
+
+
+def resize_plan_status(plan: Plan) -> int:
+    st = ctypes.c_int(-1)
+    _check(_native.load().resize_plan_status(plan.handle, ctypes.byref(st)), "resize_plan_status")
+    return st.value
+
+
+def resize_plan_set_tile(plan: Plan, kind: int, tile_rows: int, tile_cols: int) -> None:
+    _check(_native.load().resize_plan_set_tile(plan.handle, kind, tile_rows, tile_cols), "resize_plan_set_tile")
+
+
+def _hwc(t, name):
+    """(H, W, C, pitch_bytes) of an HWC/HW tensor whose pixels are packed."""
+    if t.dim() == 2:
+        H, W = t.shape
+        C = 1
+        if t.stride(1) != 1:
+            raise ValueError(f"{name}: columns must be contiguous")
+    elif t.dim() == 3:
+        H, W, C = t.shape
+        if t.stride(2) != 1 or t.stride(1) != C:
+            raise ValueError(f"{name}: pixels must be packed (stride(1) == C, stride(2) == 1)")
+    else:
+        raise ValueError(f"{name}: expected HxW or HxWxC, got shape {tuple(t.shape)}")
+    return H, W, C, t.stride(0) * t.element_size()
+
+
+def resize_u8(plan: Plan, src, dst, mode: int | None = None, stream=None) -> None:
+    """dst[:] = resize(src) for uint8 tensors (H, W[, C]) -> (OH, OW[, C])."""
+    H, W, C, sp = _hwc(src, "src")
+    OH, OW, C2, dp = _hwc(dst, "dst")
+    if C2 != C:
+        raise ValueError("src and dst channel counts differ")
+    _check(_native.load().resize_u8(plan.handle, src.data_ptr(), sp, dst.data_ptr(), dp, H, W, C, OH, OW,
+                                    plan.mode if mode is None else mode, _stream(stream)), "resize_u8")
+
+
+def resize_f32(plan: Plan, src, dst, mode: int | None = None, stream=None) -> None:
+    """dst[:] = resize(src) for float32 tensors (H, W[, C]) -> (OH, OW[, C])."""
+    H, W, C, sp = _hwc(src, "src")
+    OH, OW, C2, dp = _hwc(dst, "dst")
+    if C2 != C:
+        raise ValueError("src and dst channel counts differ")
+    _check(_native.load().resize_f32(plan.handle, src.data_ptr(), sp, dst.data_ptr(), dp, H, W, C, OH, OW,
+                                     plan.mode if mode is None else mode, _stream(stream)), "resize_f32")
+
+
+def make_epilogue(kind: int, batch: int = 1, src_batch_stride: int = 0, dst_batch_stride: int = 0,
+                  mean=(0.0, 0.0, 0.0, 0.0), std=(1.0, 1.0, 1.0, 1.0), w3x3=None) -> RzEpilogue:
+    e = RzEpilogue()
+    e.kind, e.batch = kind, batch
+    e.src_batch_stride, e.dst_batch_stride = src_batch_stride, dst_batch_stride
+    for i in range(4):
+        e.mean[i] = float(mean[i]) if i < len(mean) else 0.0
+        e.std[i] = float(std[i]) if i < len(std) else 1.0
+    if w3x3 is not None:
+        for i in range(9):
+            e.w3x3[i] = float(w3x3[i])
+    return e
+
+
+def resize_fused(plan: Plan, src, dst, epilogue: RzEpilogue, stream=None) -> None:
+    """Bilinear resize with a fused epilogue.
+
+    RZ_EPI_NORMALIZE_NCHW: src uint8 (N, H, W, C) or (H, W, C); dst float32
+    (N, C, OH, OW) or (C, OH, OW).  RZ_EPI_FILTER3X3: src and dst float32
+    (N, H, W, C) / (H, W, C) / (H, W).  The epilogue's batch and batch strides
+    are filled in from the tensors.
+    """
+    import torch
+    e = RzEpilogue.from_buffer_copy(epilogue)
+    batched = src.dim() == 4
+    s = src if batched else src.unsqueeze(0)
+    if e.kind == RZ_EPI_NORMALIZE_NCHW:
+        d = dst if dst.dim() == 4 else dst.unsqueeze(0)
+        N, C, OH, OW = d.shape
+        if d.stride(3) != 1 or d.stride(1) != OH * d.stride(2):
+            raise ValueError("dst planes must be rows of contiguous floats with planes stacked by rows")
+        dp = d.stride(2) * 4
+        dtype_code = RZ_U8
+        if s.dtype != torch.uint8 or d.dtype != torch.float32:
+            raise ValueError("normalise epilogue takes uint8 src and float32 dst")
+    elif e.kind == RZ_EPI_FILTER3X3:
+        if not batched and src.dim() == 2:
+            s = src.unsqueeze(0).unsqueeze(-1)
+            d = dst.unsqueeze(0).unsqueeze(-1)
+        else:
+            d = dst if dst.dim() == 4 else dst.unsqueeze(0)
+        N, OH, OW, C = d.shape
+        dp = d.stride(1) * 4
+        dtype_code = RZ_F32
+        if s.dtype != torch.float32 or d.dtype != torch.float32:
+            raise ValueError("3x3 epilogue takes float32 src and dst")
+    else:
+        raise ValueError(f"unknown epilogue kind {e.kind}")
+    Nb, H, W, Cs = s.shape
+    if Nb != N or Cs != C:
+        raise ValueError("src and dst batch or channel counts differ")
+    if s.stride(3) != 1 or s.stride(2) != C:
+        raise ValueError("src pixels must be packed")
+    e.batch = N
+    e.src_batch_stride = s.stride(0) * s.element_size()
+    e.dst_batch_stride = d.stride(0) * d.element_size()
+    _check(_native.load().resize_fused(plan.handle, s.data_ptr(), dtype_code, s.stride(1) * s.element_size(),
+                                       d.data_ptr(), dp, H, W, C, OH, OW, RZ_LINEAR, ctypes.byref(e),
+                                       _stream(stream)), "resize_fused")
+
+
+def resize_u8_host(plan: Plan, host_src, host_dst, dev_src, dev_dst, stream=None) -> None:
+    """Host -> device copy, resize, device -> host copy, queued on one stream.
+
+    host_src/host_dst are CPU tensors (page-locked for asynchronous copies);
+    dev_src/dev_dst are the caller's device buffers of the same shapes.
+    """
+    H, W, C, hsp = _hwc(host_src, "host_src")
+    OH, OW, _, hdp = _hwc(host_dst, "host_dst")
+    _, _, _, dsp = _hwc(dev_src, "dev_src")
+    _, _, _, ddp = _hwc(dev_dst, "dev_dst")
+    _check(_native.load().resize_u8_host(plan.handle, host_src.data_ptr(), hsp, host_dst.data_ptr(), hdp,
+                                         dev_src.data_ptr(), dsp, dev_dst.data_ptr(), ddp, H, W, C, OH, OW,
+                                         plan.mode, _stream(stream)), "resize_u8_host")
+
+
+def resize_axis_table(n_in: int, n_out: int, mode: int = RZ_LINEAR):
+    """Host-only sampling table of one axis: (ofs int32, w_q11 int32, u float32) numpy arrays."""
+    import numpy as np
+    ofs = np.zeros(n_out, np.int32)
+    w = np.zeros(n_out, np.int32)
+    u = np.zeros(n_out, np.float32)
+    _check(_native.load().resize_axis_table(n_in, n_out, mode, ofs.ctypes.data, w.ctypes.data, u.ctypes.data),
+           "resize_axis_table")
+    return ofs, w, u
+
+
+def resize_strerror(code: int) -> str:
+    return _native.load().resize_strerror(code).decode()
+
+
+def resize_last_cuda_error() -> int:
+    return _native.load().resize_last_cuda_error()

@@ -1,0 +1,83 @@
+"""ctypes declarations of the C ABI in include/gbresize.h.
+
+Loading fails loudly (``RuntimeError``) when ``libgbresize.so`` has not been
+built; there is no other implementation to fall back on.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import library_path
+
+RZ_NEAREST = 0
+RZ_LINEAR = 1
+RZ_U8 = 0
+RZ_F32 = 1
+RZ_EPI_NORMALIZE_NCHW = 1
+RZ_EPI_FILTER3X3 = 2
+RZ_OK = 0
+RZ_ERR_ARG = 1
+RZ_ERR_UNSUPPORTED = 2
+RZ_ERR_CUDA = 3
+RZ_ERR_NOMEM = 4
+RZ_ERR_TIMEOUT = 5
+RZ_MAX_DIM = 65536
+
+# kernel families for resize_plan_set_tile
+KIND_U8 = 0
+KIND_F32 = 1
+KIND_NORMALIZE = 2 + RZ_EPI_NORMALIZE_NCHW
+KIND_FILTER3X3 = 2 + RZ_EPI_FILTER3X3
+
+
+class RzEpilogue(ctypes.Structure):
+    _fields_ = [
+        ("kind", ctypes.c_int),
+        ("batch", ctypes.c_int),
+        ("src_batch_stride", ctypes.c_size_t),
+        ("dst_batch_stride", ctypes.c_size_t),
+        ("mean", ctypes.c_float * 4),
+        ("std", ctypes.c_float * 4),
+        ("w3x3", ctypes.c_float * 9),
+    ]
+
+
+_p = ctypes.c_void_p
+_sz = ctypes.c_size_t
+_i = ctypes.c_int
+
+# name -> (restype, argtypes); every symbol include/gbresize.h declares
+SIGNATURES = {
+    "resize_plan_create": (_i, [ctypes.POINTER(_p), _i, _i, _i, _i, _i, _p]),
+    "resize_plan_destroy": (_i, [_p]),
+    "resize_plan_status": (_i, [_p, ctypes.POINTER(_i)]),
+    "resize_plan_set_tile": (_i, [_p, _i, _i, _i]),
+    "resize_u8": (_i, [_p, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
+    "resize_f32": (_i, [_p, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
+    "resize_fused": (_i, [_p, _p, _i, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, ctypes.POINTER(RzEpilogue), _p]),
+    "resize_u8_host": (_i, [_p, _p, _sz, _p, _sz, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
+    "resize_axis_table": (_i, [_i, _i, _i, _p, _p, _p]),
+    "resize_strerror": (ctypes.c_char_p, [_i]),
+    "resize_last_cuda_error": (_i, []),
+}
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib

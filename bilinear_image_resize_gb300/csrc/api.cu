@@ -1,0 +1,532 @@
+// C ABI of the resize library: plans (exact sampling tables), argument
+// validation, tile selection and kernel launch.  See include/gbresize.h for
+// the contract of every entry point.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "gbresize.h"
+#include "rz_internal.h"
+
+using rz::KArgs;
+using rz::SmemLayout;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e)
+{
+    g_last_cuda_error = static_cast<int>(e);
+    if (e == cudaErrorMemoryAllocation)
+        return RZ_ERR_NOMEM;
+    return RZ_ERR_CUDA;
+}
+
+int64_t floor_div(int64_t a, int64_t b)  // b > 0
+{
+    int64_t q = a / b;
+    if ((a % b) != 0 && a < 0)
+        q -= 1;
+    return q;
+}
+
+// Bilinear sampling table of one axis.  Output index d samples
+// x = (d + 1/2) n_in / n_out - 1/2 = num / den, num = (2d+1) n_in - n_out,
+// den = 2 n_out (Volcanic resize page, "Naive resize with linear sampling").
+// ofs = floor(x); the far tap's weight is u = r / den with r = num - ofs*den:
+// as 11-bit fixed point round-half-up(2048 u) (CUDA interpolation page §6.2),
+// as float rounded once from double.  A left tap left of 0, or a left tap at
+// n_in - 1, is folded to one clamped tap with weight 0: both taps would read
+// the same clamped sample (§6.1), so the value is unchanged.
+void axis_linear(int n_in, int n_out, int32_t *ofs, int32_t *q11, float *u)
+{
+    const int64_t den = 2 * static_cast<int64_t>(n_out);
+    for (int64_t d = 0; d < n_out; d++) {
+        const int64_t num = (2 * d + 1) * n_in - n_out;
+        int64_t s = floor_div(num, den);
+        const int64_t r = num - s * den;
+        int64_t w = floor_div(4096 * r + den, 2 * den);
+        float uf = static_cast<float>(static_cast<double>(r) / static_cast<double>(den));
+        if (s < 0) {
+            s = 0;
+            w = 0;
+            uf = 0.0f;
+        } else if (s >= n_in - 1) {
+            s = n_in - 1;
+            w = 0;
+            uf = 0.0f;
+        }
+        if (ofs) ofs[d] = static_cast<int32_t>(s);
+        if (q11) q11[d] = static_cast<int32_t>(w);
+        if (u) u[d] = uf;
+    }
+}
+
+// Nearest table: floor(d n_in / n_out), OpenCV INTER_NEAREST (CUDA
+// interpolation page §2.1 read as the floor rule).
+void axis_nearest(int n_in, int n_out, int32_t *ofs)
+{
+    for (int64_t d = 0; d < n_out; d++) {
+        int64_t s = floor_div(d * n_in, n_out);
+        if (s > n_in - 1) s = n_in - 1;
+        ofs[d] = static_cast<int32_t>(s);
+    }
+}
+
+struct TileCfg {
+    int TR = 0, TW = 0, tiles_x = 0, tiles_y = 0, max_rows = 0, slot_bytes = 0;
+    size_t smem = 0;
+};
+
+}  // namespace
+
+struct rz_plan_s {
+    int H, W, OH, OW, mode, device;
+    std::vector<int32_t> xofs, xq, yofs, yq;
+    std::vector<float> xu, yu;
+    void *dmem = nullptr;
+    int2 *d_xq = nullptr, *d_xf = nullptr, *d_yq = nullptr, *d_yf = nullptr;
+    int *d_status = nullptr;
+    std::mutex mu;
+    struct Entry { int fam, C, batch_log; TileCfg cfg; };
+    std::vector<Entry> cache;
+    int over_tr[rz::FAM_COUNT] = {}, over_tw[rz::FAM_COUNT] = {};
+};
+
+namespace {
+
+bool valid_mode(int m) { return m == RZ_LINEAR || m == RZ_NEAREST; }
+
+// Upper bound on the bytes of one staged source row of the tile column
+// starting at output column dx0: the tap span rounded out to 16 bytes.
+int span_bytes(const rz_plan_s &p, int fam, int C, int dx0, int dx1)
+{
+    const int halo = rz::fam_halo(fam);
+    const int es = rz::fam_in_es(fam);
+    const int cx0 = std::clamp(dx0 - halo, 0, p.OW - 1);
+    const int cx1 = std::clamp(dx1 - 1 + halo, 0, p.OW - 1);
+    const int xs0 = p.xofs[cx0];
+    const int xs1 = p.mode == RZ_LINEAR ? std::min(p.xofs[cx1] + 1, p.W - 1) : p.xofs[cx1];
+    const int lo = (xs0 * C * es) & ~15;
+    const int hi = ((xs1 + 1) * C * es + 15) & ~15;
+    return hi - lo;
+}
+
+int max_slot_bytes(const rz_plan_s &p, int fam, int C, int TW)
+{
+    int m = 0;
+    for (int dx0 = 0; dx0 < p.OW; dx0 += TW)
+        m = std::max(m, span_bytes(p, fam, C, dx0, std::min(dx0 + TW, p.OW)));
+    return m;
+}
+
+// Largest number of distinct source rows a tile of TR output rows stages,
+// counted exactly as the kernel lists them.
+int max_tile_rows(const rz_plan_s &p, int fam, int TR)
+{
+    const int halo = rz::fam_halo(fam);
+    const bool lin = p.mode == RZ_LINEAR;
+    int m = 0;
+    for (int dy0 = 0; dy0 < p.OH; dy0 += TR) {
+        const int dy1 = std::min(dy0 + TR, p.OH);
+        int n = 0, last = -1;
+        for (int k = 0; k < dy1 - dy0 + 2 * halo; k++) {
+            const int dy = std::clamp(dy0 - halo + k, 0, p.OH - 1);
+            const int r0 = p.yofs[dy];
+            const int r1 = lin ? std::min(r0 + 1, p.H - 1) : r0;
+            if (r0 > last) { n++; last = r0; }
+            if (r1 > last) { n++; last = r1; }
+        }
+        m = std::max(m, n);
+    }
+    return m;
+}
+
+bool eval_tile(const rz_plan_s &p, int fam, int C, int TR, int TW, TileCfg *out)
+{
+    TileCfg t;
+    t.TR = std::max(1, std::min(TR, p.OH));
+    t.TW = std::max(1, std::min(TW, p.OW));
+    t.tiles_x = (p.OW + t.TW - 1) / t.TW;
+    t.tiles_y = (p.OH + t.TR - 1) / t.TR;
+    t.slot_bytes = max_slot_bytes(p, fam, C, t.TW);
+    t.max_rows = max_tile_rows(p, fam, t.TR);
+    const SmemLayout L = rz::smem_layout(fam, C, t.TR, t.TW, t.max_rows, t.slot_bytes);
+    t.smem = static_cast<size_t>(L.total);
+    *out = t;
+    return L.total <= rz::kMaxSmem;
+}
+
+constexpr int kSms = 152;
+constexpr int kSoftSmem = 48 * 1024;     // keeps >= 4 CTAs resident per SM
+constexpr int kFilterSmem = 96 * 1024;   // the 3x3 tile trades occupancy for less halo
+
+// Automatic tile choice.  Plain resize and normalise: rows as wide as the
+// output (or the widest power-of-two strip whose staged row stays within
+// 16 KB), then as many output rows per tile as keep the CTA under 48 KB of
+// shared memory while still giving every SM about eight CTAs.  3x3 filter:
+// 128-column strips of up to 32 rows, so that the one-pixel halo costs a
+// few per cent.
+TileCfg choose_tile(const rz_plan_s &p, int fam, int C, int batch)
+{
+    const int out_es = rz::fam_out_es(fam);
+    std::vector<int> tws;
+    tws.push_back(p.OW);
+    for (int w = 4096; w >= 1; w >>= 1)
+        if (w < p.OW) tws.push_back(w);
+    TileCfg best;
+    if (fam == rz::FAM_FILT) {
+        for (int TW : {128, 64, 32, 16, 8, 4, 2, 1}) {
+            for (int TR : {32, 16, 8, 4, 2, 1}) {
+                TileCfg t;
+                if (eval_tile(p, fam, C, TR, TW, &t) && t.smem <= static_cast<size_t>(kFilterSmem))
+                    return t;
+            }
+        }
+        for (int TW : {16, 8, 4, 2, 1})
+            if (eval_tile(p, fam, C, 1, TW, &best)) return best;
+        return best;
+    }
+    int TW = 1;
+    for (int w : tws) {
+        const int px_bytes = fam == rz::FAM_NORM ? 4 : C * out_es;
+        const int row_out = px_bytes * std::min(w, p.OW);
+        const bool aligned = (w >= p.OW) || ((w * px_bytes) % 16 == 0);
+        if (!aligned) continue;
+        if (max_slot_bytes(p, fam, C, w) <= 16384 && row_out <= 16384) { TW = w; break; }
+    }
+    TileCfg t1;
+    if (!eval_tile(p, fam, C, 1, TW, &t1)) {
+        // a single row of this width does not fit: fall back to narrow strips
+        for (int w = TW / 2; w >= 1; w /= 2)
+            if (eval_tile(p, fam, C, 1, w, &t1)) return t1;
+        return t1;
+    }
+    best = t1;
+    const long long want = std::min<long long>(8LL * kSms, static_cast<long long>(batch) * t1.tiles_x * t1.tiles_y);
+    for (int TR = 2; TR <= 64; TR *= 2) {
+        TileCfg t;
+        if (!eval_tile(p, fam, C, TR, TW, &t) || t.smem > static_cast<size_t>(kSoftSmem)) break;
+        if (static_cast<long long>(batch) * t.tiles_x * t.tiles_y < want) break;
+        best = t;
+        if (TR >= p.OH) break;
+    }
+    return best;
+}
+
+int batch_log(int batch)
+{
+    int l = 0;
+    while ((1 << l) < batch && l < 30) l++;
+    return l;
+}
+
+// Tile for this call: the override if one is set, else the cached automatic
+// choice.  Returns false if an override does not fit in shared memory.
+bool get_tile(rz_plan_s *p, int fam, int C, int batch, TileCfg *out)
+{
+    std::lock_guard<std::mutex> lk(p->mu);
+    if (p->over_tr[fam] > 0 && p->over_tw[fam] > 0)
+        return eval_tile(*p, fam, C, p->over_tr[fam], p->over_tw[fam], out);
+    const int bl = batch_log(batch);
+    for (const auto &e : p->cache)
+        if (e.fam == fam && e.C == C && e.batch_log == bl) { *out = e.cfg; return true; }
+    TileCfg t = choose_tile(*p, fam, C, 1 << bl);
+    p->cache.push_back({fam, C, bl, t});
+    *out = t;
+    return true;
+}
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+size_t image_extent(int rows, size_t pitch, size_t row_bytes)
+{
+    return rows <= 0 ? 0 : static_cast<size_t>(rows - 1) * pitch + row_bytes;
+}
+
+int check_device(const rz_plan_s *p)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return dev == p->device ? RZ_OK : RZ_ERR_ARG;
+}
+
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
+// Shared body of every resize entry point.  `planes` > 0 selects the planar
+// (NCHW) output of the normalise epilogue.
+int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bstride, void *dst, size_t dst_pitch,
+        size_t dst_bstride, int H, int W, int C, int OH, int OW, int mode, int batch, const rz::KArgs &extra,
+        void *stream, bool do_launch = true)
+{
+    if (!p) return RZ_ERR_ARG;
+    if (H != p->H || W != p->W || OH != p->OH || OW != p->OW || mode != p->mode) return RZ_ERR_ARG;
+    if (C <= 0 || batch < 0) return RZ_ERR_ARG;
+    if (C != 1 && C != 3 && C != 4) return RZ_ERR_UNSUPPORTED;
+    if (OH == 0 || OW == 0 || batch == 0) return RZ_OK;
+    if (!src || !dst) return RZ_ERR_ARG;
+    const int in_es = rz::fam_in_es(fam), out_es = rz::fam_out_es(fam);
+    const bool nchw = fam == rz::FAM_NORM;
+    const size_t in_row = static_cast<size_t>(W) * C * in_es;
+    const size_t out_row = static_cast<size_t>(OW) * (nchw ? 1 : C) * out_es;
+    if (src_pitch < in_row || dst_pitch < out_row) return RZ_ERR_ARG;
+    if (in_es == 4 && ((src_pitch & 3) || (reinterpret_cast<uintptr_t>(src) & 3))) return RZ_ERR_ARG;
+    if (out_es == 4 && ((dst_pitch & 3) || (reinterpret_cast<uintptr_t>(dst) & 3))) return RZ_ERR_ARG;
+    const size_t src_img = image_extent(H, src_pitch, in_row);
+    const size_t dst_img = nchw ? static_cast<size_t>(C) * OH * dst_pitch : image_extent(OH, dst_pitch, out_row);
+    if (batch > 1) {
+        if (src_bstride < src_img || dst_bstride < dst_img) return RZ_ERR_ARG;
+        if (in_es == 4 && (src_bstride & 3)) return RZ_ERR_ARG;
+        if (out_es == 4 && (dst_bstride & 3)) return RZ_ERR_ARG;
+    }
+    const size_t src_all = batch > 1 ? (batch - 1) * src_bstride + src_img : src_img;
+    const size_t dst_all = batch > 1 ? (batch - 1) * dst_bstride + dst_img : dst_img;
+    if (overlap(src, src_all, dst, dst_all)) return RZ_ERR_ARG;
+    int rc = check_device(p);
+    if (rc != RZ_OK) return rc;
+
+    TileCfg t;
+    if (!get_tile(p, fam, C, batch, &t)) return RZ_ERR_ARG;
+
+    KArgs a = extra;
+    a.src = static_cast<const uint8_t *>(src);
+    a.src_pitch = static_cast<long long>(src_pitch);
+    a.src_bstride = batch > 1 ? static_cast<long long>(src_bstride) : 0;
+    a.dst = static_cast<uint8_t *>(dst);
+    a.dst_pitch = static_cast<long long>(dst_pitch);
+    a.dst_bstride = batch > 1 ? static_cast<long long>(dst_bstride) : 0;
+    a.dst_plane = nchw ? static_cast<long long>(OH) * static_cast<long long>(dst_pitch) : 0;
+    a.H = H; a.W = W; a.OH = OH; a.OW = OW; a.C = C;
+    a.TR = t.TR; a.TW = t.TW; a.tiles_x = t.tiles_x; a.tiles_y = t.tiles_y;
+    a.max_rows = t.max_rows; a.slot_bytes = t.slot_bytes;
+    a.tma_in = aligned16(src) && (src_pitch % 16 == 0) && (in_row % 16 == 0) &&
+               (a.src_bstride % 16 == 0);
+    const int strip_bytes = t.TW * (nchw ? 1 : C) * out_es;
+    a.tma_out = aligned16(dst) && (dst_pitch % 16 == 0) && (a.dst_bstride % 16 == 0) &&
+                (a.dst_plane % 16 == 0) && (t.tiles_x == 1 || strip_bytes % 16 == 0);
+    const bool fl = (fam == rz::FAM_F32 || fam == rz::FAM_FILT);
+    a.xt = fl ? p->d_xf : p->d_xq;
+    a.yt = fl ? p->d_yf : p->d_yq;
+    a.status = p->d_status;
+    if (!do_launch) return RZ_OK;
+    const int e = rz::launch_resize(fam, mode, a, batch, t.smem, stream);
+    if (e != 0) return cuda_fail(static_cast<cudaError_t>(e));
+    return RZ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int resize_axis_table(int n_in, int n_out, int mode, int32_t *ofs, int32_t *w_q11, float *u)
+{
+    if (n_in < 1 || n_out < 0 || n_in > RZ_MAX_DIM || n_out > RZ_MAX_DIM || !valid_mode(mode)) return RZ_ERR_ARG;
+    if (mode == RZ_LINEAR) {
+        axis_linear(n_in, n_out, ofs, w_q11, u);
+    } else {
+        std::vector<int32_t> tmp(static_cast<size_t>(n_out));
+        axis_nearest(n_in, n_out, tmp.data());
+        if (ofs) std::memcpy(ofs, tmp.data(), tmp.size() * sizeof(int32_t));
+    }
+    return RZ_OK;
+}
+
+int resize_plan_create(rz_plan *out, int in_h, int in_w, int out_h, int out_w, int mode, void *stream)
+{
+    if (!out) return RZ_ERR_ARG;
+    *out = nullptr;
+    if (in_h < 1 || in_w < 1 || out_h < 0 || out_w < 0 || in_h > RZ_MAX_DIM || in_w > RZ_MAX_DIM ||
+        out_h > RZ_MAX_DIM || out_w > RZ_MAX_DIM || !valid_mode(mode))
+        return RZ_ERR_ARG;
+    rz_plan_s *p = new (std::nothrow) rz_plan_s();
+    if (!p) return RZ_ERR_NOMEM;
+    p->H = in_h; p->W = in_w; p->OH = out_h; p->OW = out_w; p->mode = mode;
+    try {
+        p->xofs.resize(out_w); p->xq.resize(out_w); p->xu.resize(out_w);
+        p->yofs.resize(out_h); p->yq.resize(out_h); p->yu.resize(out_h);
+    } catch (...) {
+        delete p;
+        return RZ_ERR_NOMEM;
+    }
+    if (mode == RZ_LINEAR) {
+        axis_linear(in_w, out_w, p->xofs.data(), p->xq.data(), p->xu.data());
+        axis_linear(in_h, out_h, p->yofs.data(), p->yq.data(), p->yu.data());
+    } else {
+        axis_nearest(in_w, out_w, p->xofs.data());
+        axis_nearest(in_h, out_h, p->yofs.data());
+    }
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e != cudaSuccess) { delete p; return cuda_fail(e); }
+
+    // one device block: x tables (q11 and float weights), y tables, status word
+    const size_t nx = static_cast<size_t>(out_w), ny = static_cast<size_t>(out_h);
+    const size_t off_xf = nx * sizeof(int2), off_yq = 2 * off_xf, off_yf = off_yq + ny * sizeof(int2);
+    const size_t off_st = off_yf + ny * sizeof(int2);
+    const size_t total = off_st + 16;
+    std::vector<uint8_t> host(total, 0);
+    int2 *hxq = reinterpret_cast<int2 *>(host.data()), *hxf = reinterpret_cast<int2 *>(host.data() + off_xf);
+    int2 *hyq = reinterpret_cast<int2 *>(host.data() + off_yq), *hyf = reinterpret_cast<int2 *>(host.data() + off_yf);
+    for (size_t i = 0; i < nx; i++) {
+        int32_t ubits;
+        std::memcpy(&ubits, &p->xu[i], 4);
+        hxq[i] = make_int2(p->xofs[i], p->xq[i]);
+        hxf[i] = make_int2(p->xofs[i], ubits);
+    }
+    for (size_t i = 0; i < ny; i++) {
+        int32_t vbits;
+        std::memcpy(&vbits, &p->yu[i], 4);
+        hyq[i] = make_int2(p->yofs[i], p->yq[i]);
+        hyf[i] = make_int2(p->yofs[i], vbits);
+    }
+    e = cudaMalloc(&p->dmem, total);
+    if (e != cudaSuccess) { p->dmem = nullptr; delete p; return cuda_fail(e); }
+    uint8_t *d = static_cast<uint8_t *>(p->dmem);
+    p->d_xq = reinterpret_cast<int2 *>(d);
+    p->d_xf = reinterpret_cast<int2 *>(d + off_xf);
+    p->d_yq = reinterpret_cast<int2 *>(d + off_yq);
+    p->d_yf = reinterpret_cast<int2 *>(d + off_yf);
+    p->d_status = reinterpret_cast<int *>(d + off_st);
+    // pageable source: the call returns once the bytes are staged, so `host`
+    // may be freed on return
+    e = cudaMemcpyAsync(p->dmem, host.data(), total, cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { cudaFree(p->dmem); delete p; return cuda_fail(e); }
+    *out = p;
+    return RZ_OK;
+}
+
+int resize_plan_destroy(rz_plan p)
+{
+    if (!p) return RZ_OK;
+    int rc = RZ_OK;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device) cudaSetDevice(p->device);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) rc = cuda_fail(e);
+    e = cudaFree(p->dmem);
+    if (e != cudaSuccess && rc == RZ_OK) rc = cuda_fail(e);
+    if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
+    delete p;
+    return rc;
+}
+
+int resize_plan_status(rz_plan p, int *status)
+{
+    if (!p) return RZ_ERR_ARG;
+    int rc = check_device(p);
+    if (rc != RZ_OK) return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    int v = 0;
+    e = cudaMemcpy(&v, p->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaMemset(p->d_status, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (status) *status = v;
+    return RZ_OK;
+}
+
+int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_cols)
+{
+    if (!p || kind < 0 || kind >= rz::FAM_COUNT || kind == 2 || tile_rows < 0 || tile_cols < 0) return RZ_ERR_ARG;
+    if ((tile_rows == 0) != (tile_cols == 0)) return RZ_ERR_ARG;
+    std::lock_guard<std::mutex> lk(p->mu);
+    p->over_tr[kind] = tile_rows;
+    p->over_tw[kind] = tile_cols;
+    return RZ_OK;
+}
+
+int resize_u8(rz_plan p, const uint8_t *src, size_t src_pitch, uint8_t *dst, size_t dst_pitch, int H, int W, int C,
+              int out_h, int out_w, int mode, void *stream)
+{
+    KArgs extra = {};
+    return run(p, rz::FAM_U8, src, src_pitch, 0, dst, dst_pitch, 0, H, W, C, out_h, out_w, mode, 1, extra, stream);
+}
+
+int resize_f32(rz_plan p, const float *src, size_t src_pitch, float *dst, size_t dst_pitch, int H, int W, int C,
+               int out_h, int out_w, int mode, void *stream)
+{
+    KArgs extra = {};
+    return run(p, rz::FAM_F32, src, src_pitch, 0, dst, dst_pitch, 0, H, W, C, out_h, out_w, mode, 1, extra, stream);
+}
+
+int resize_fused(rz_plan p, const void *src, int src_dtype, size_t src_pitch, void *dst, size_t dst_pitch, int H,
+                 int W, int C, int out_h, int out_w, int mode, const rz_epilogue *e, void *stream)
+{
+    if (!e || mode != RZ_LINEAR) return RZ_ERR_ARG;
+    KArgs extra = {};
+    int fam;
+    if (e->kind == RZ_EPI_NORMALIZE_NCHW) {
+        if (src_dtype != RZ_U8) return RZ_ERR_ARG;
+        fam = rz::FAM_NORM;
+        if (C < 1 || C > 4) return C < 1 ? RZ_ERR_ARG : RZ_ERR_UNSUPPORTED;
+        for (int c = 0; c < C; c++) {
+            const double sd = e->std[c], mu = e->mean[c];
+            if (!(sd != 0.0) || sd != sd || sd - sd != 0.0 || mu != mu || mu - mu != 0.0) return RZ_ERR_ARG;
+            extra.scale[c] = static_cast<float>(1.0 / (255.0 * sd));
+            extra.shift[c] = static_cast<float>(-mu / sd);
+        }
+    } else if (e->kind == RZ_EPI_FILTER3X3) {
+        if (src_dtype != RZ_F32) return RZ_ERR_ARG;
+        fam = rz::FAM_FILT;
+        for (int i = 0; i < 9; i++) extra.w[i] = e->w3x3[i];
+    } else {
+        return RZ_ERR_ARG;
+    }
+    return run(p, fam, src, src_pitch, e->src_batch_stride, dst, dst_pitch, e->dst_batch_stride, H, W, C, out_h,
+               out_w, mode, e->batch, extra, stream);
+}
+
+int resize_u8_host(rz_plan p, const uint8_t *host_src, size_t host_src_pitch, uint8_t *host_dst, size_t host_dst_pitch,
+                   uint8_t *dev_src, size_t dev_src_pitch, uint8_t *dev_dst, size_t dev_dst_pitch, int H, int W,
+                   int C, int out_h, int out_w, int mode, void *stream)
+{
+    if (!p || !host_src || !host_dst || !dev_src || !dev_dst) return RZ_ERR_ARG;
+    if (C <= 0 || H != p->H || W != p->W || out_h != p->OH || out_w != p->OW) return RZ_ERR_ARG;
+    const size_t in_row = static_cast<size_t>(W) * C, out_row = static_cast<size_t>(out_w) * C;
+    if (host_src_pitch < in_row || host_dst_pitch < out_row) return RZ_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // validate the device-side call before queuing any copy
+    int rc = run(p, rz::FAM_U8, dev_src, dev_src_pitch, 0, dev_dst, dev_dst_pitch, 0, H, W, C, out_h, out_w, mode, 1,
+                 KArgs{}, stream, false);
+    if (rc != RZ_OK) return rc;
+    cudaError_t e = cudaMemcpy2DAsync(dev_src, dev_src_pitch, host_src, host_src_pitch, in_row, H,
+                                      cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    rc = resize_u8(p, dev_src, dev_src_pitch, dev_dst, dev_dst_pitch, H, W, C, out_h, out_w, mode, stream);
+    if (rc != RZ_OK) return rc;
+    if (out_h > 0 && out_w > 0) {
+        e = cudaMemcpy2DAsync(host_dst, host_dst_pitch, dev_dst, dev_dst_pitch, out_row, out_h,
+                              cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return RZ_OK;
+}
+
+const char *resize_strerror(int code)
+{
+    switch (code) {
+    case RZ_OK: return "ok";
+    case RZ_ERR_ARG: return "invalid argument";
+    case RZ_ERR_UNSUPPORTED: return "unsupported parameter";
+    case RZ_ERR_CUDA: return "CUDA runtime error";
+    case RZ_ERR_NOMEM: return "out of memory";
+    case RZ_ERR_TIMEOUT: return "kernel timed out waiting for a bulk copy";
+    default: return "unknown status";
+    }
+}
+
+int resize_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

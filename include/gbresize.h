@@ -1,0 +1,223 @@
+/*
+ * gbresize — image resize for NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * Operations (the method these calls implement):
+ *  - bilinear resize, OpenCV INTER_LINEAR style: output pixel (dx, dy) samples
+ *    the input at x = (dx + 1/2) * W / OW - 1/2, y = (dy + 1/2) * H / OH - 1/2
+ *    ("From Prototype to Performance: Optimizing OpenCV Resize on Volcanic
+ *    GPUs", section "Naive resize with linear sampling": the output coordinate
+ *    plus 0.5 times the inverse scale, fed to a linear sampler whose texel
+ *    centres sit at +0.5), with weights (1-u)(1-v), u(1-v), (1-u)v, uv on the
+ *    four neighbours (CUDA interpolation page, hnwysp.cn/news/129086, §2.2)
+ *    and neighbour indices clamped into the image (same page, §6.1);
+ *  - nearest resize, OpenCV INTER_NEAREST: source index floor(dx * W / OW)
+ *    (CUDA interpolation page §2.1, read as OpenCV's floor rule);
+ *  - two epilogues fused into the bilinear kernel (CUDA interpolation page
+ *    §4.2, operator fusion): per-channel normalisation to float32 planar
+ *    (NCHW), and a 3x3 float filter (correlation, replicate border on the
+ *    output grid; "OpenCL image convolution", §2).
+ *
+ * Numerics:
+ *  - uint8 bilinear is exact integer arithmetic: 11-bit weights
+ *    A1 = round-half-up(2048 u), A0 = 2048 - A1 (and B0/B1 for v), the four
+ *    products summed in int32 and rounded half-up once, (sum + 2^21) >> 22
+ *    (CUDA interpolation page §6.2, fixed point).  The result is bit-exact
+ *    and independent of evaluation order.
+ *  - float32 bilinear uses weights u = r / den computed exactly in double on
+ *    the host and rounded once to float; max abs error about 5e-5 on values
+ *    in [0, 255].
+ *  - nearest is a copy (bit-exact for both types).
+ *
+ * Layout: images are row-major, interleaved HWC, with an explicit row pitch in
+ * BYTES (pitch >= W * C * sizeof(element); any value, odd pitches included).
+ * C is 1, 3 or 4.  All image pointers are DEVICE pointers unless a call says
+ * otherwise; the caller owns them.  Sizes follow OpenCV's dsize convention
+ * only in spirit: every call takes heights and widths separately.
+ *
+ * Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ * default stream).  Every resize call is asynchronous on that stream, does
+ * not allocate, and does not synchronise the host.
+ *
+ * Errors: every call returns an RZ_* status.  Arguments are validated before
+ * anything is launched; a rejected call has no effect.  RZ_ERR_CUDA means a
+ * CUDA runtime call failed; resize_last_cuda_error() gives its cudaError_t
+ * (per host thread).  The library never aborts, prints or throws.
+ *
+ * Threads: a plan may be used from several host threads and streams at once;
+ * calls on different streams that write the same output race, as any CUDA
+ * work would.
+ */
+#ifndef GBRESIZE_H
+#define GBRESIZE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of the C ABI keep default visibility; everything else in the
+ * library is hidden. */
+#if defined(__GNUC__)
+#define RZ_API __attribute__((visibility("default")))
+#else
+#define RZ_API
+#endif
+
+#define RZ_NEAREST 0
+#define RZ_LINEAR 1
+
+#define RZ_U8 0
+#define RZ_F32 1
+
+#define RZ_EPI_NORMALIZE_NCHW 1
+#define RZ_EPI_FILTER3X3 2
+
+#define RZ_OK 0
+#define RZ_ERR_ARG 1          /* bad pointer, size, pitch, mode or overlap     */
+#define RZ_ERR_UNSUPPORTED 2  /* valid but not implemented (e.g. C = 2)        */
+#define RZ_ERR_CUDA 3         /* a CUDA runtime call failed                    */
+#define RZ_ERR_NOMEM 4        /* host or device allocation failed (plans only) */
+#define RZ_ERR_TIMEOUT 5      /* a kernel gave up waiting on a bulk copy       */
+
+/* Largest accepted height or width, input or output. */
+#define RZ_MAX_DIM 65536
+
+/* Opaque plan: per-column and per-row sampling tables for one geometry
+ * (H x W -> OH x OW) and one mode, resident in device memory. */
+typedef struct rz_plan_s *rz_plan;
+
+/*
+ * Build the sampling tables of one geometry and mode.
+ *
+ * For RZ_LINEAR, per output column dx:  num = (2dx + 1) W - OW,  den = 2 OW,
+ * xofs = floor(num / den),  r = num - xofs * den,  u = r / den; the uint8
+ * weight a1 = round-half-up(2048 r / den); columns whose left tap falls left
+ * of 0 or whose right tap falls right of W-1 are folded onto one clamped tap
+ * (a1 = 0, u = 0), which gives exactly the values of clamping both taps.
+ * The same per output row (yofs, b1, v).  For RZ_NEAREST, xn = floor(dx W / OW)
+ * and yn = floor(dy H / OH).  Sampling position: Volcanic resize page,
+ * "Naive resize with linear sampling"; weights: CUDA interpolation page §2.2
+ * and §6.2; nearest: §2.1; output size int(in * scale) is the caller's
+ * choice (Volcanic page, "Step 2").
+ *
+ * in_h, in_w >= 1; out_h, out_w >= 0; all <= RZ_MAX_DIM; mode RZ_LINEAR or
+ * RZ_NEAREST.  Allocates device memory for the tables and a status word and
+ * copies them on `stream` (asynchronously); the plan may be used on any stream
+ * once that copy has completed (synchronise `stream` first, or use the same
+ * stream).  On success *out receives the plan; on failure *out is NULL.
+ */
+RZ_API int resize_plan_create(rz_plan *out, int in_h, int in_w, int out_h, int out_w, int mode, void *stream);
+
+/* Free a plan (NULL is accepted).  Synchronises the device first so that no
+ * queued kernel still reads the tables. */
+RZ_API int resize_plan_destroy(rz_plan p);
+
+/*
+ * Read and clear the plan's device status word (RZ_OK, or RZ_ERR_TIMEOUT if a
+ * kernel using this plan gave up waiting on a bulk copy).  Synchronises the
+ * device.  *status may be NULL.
+ */
+RZ_API int resize_plan_status(rz_plan p, int *status);
+
+/*
+ * uint8 resize of one interleaved image.
+ *   src, dst: device pointers; src_pitch, dst_pitch: bytes between rows.
+ *   H, W, out_h, out_w and mode must equal the plan's; C in {1, 3, 4}.
+ *   src_pitch >= W*C, dst_pitch >= out_w*C; the source and destination byte
+ *   ranges must not overlap.
+ * Output (dx, dy, c) is written at dst + dy*dst_pitch + dx*C + c; bytes of a
+ * row beyond out_w*C are not touched.  Bilinear is bit-exact with the
+ * definition above; nearest is a byte copy.
+ */
+RZ_API int resize_u8(rz_plan p, const uint8_t *src, size_t src_pitch, uint8_t *dst, size_t dst_pitch,
+              int H, int W, int C, int out_h, int out_w, int mode, void *stream);
+
+/* float32 resize; as resize_u8 with 4-byte elements (pitches still in bytes,
+ * multiples of 4). */
+RZ_API int resize_f32(rz_plan p, const float *src, size_t src_pitch, float *dst, size_t dst_pitch,
+               int H, int W, int C, int out_h, int out_w, int mode, void *stream);
+
+/*
+ * Epilogue fused into the bilinear kernel (CUDA interpolation page §4.2;
+ * kernel merging leaves results unchanged, "Performance Optimization of Object
+ * Tracking Algorithms in OpenCV on GPUs", §4.2 and Table 10).
+ *
+ * RZ_EPI_NORMALIZE_NCHW: src uint8 HWC, dst float32 planar.  The uint8
+ *   bilinear result q is computed exactly as resize_u8 does and written as
+ *   y = (q / 255 - mean[c]) / std[c], evaluated in float32 as
+ *   fmaf(q, 1 / (255 std[c]), -mean[c] / std[c]) with both constants rounded
+ *   once from double on the host.  Element (c, dy, dx) of image n lands at
+ *   dst + n*dst_batch_stride + c*out_h*dst_pitch + dy*dst_pitch + dx*4, so
+ *   dst_pitch is the byte pitch of one plane row (>= out_w*4, multiple of 4).
+ *   Images are `batch` frames src + n*src_batch_stride.
+ * RZ_EPI_FILTER3X3: src and dst float32 HWC.  z = sum_{a,b in -1..1}
+ *   w3x3[(a+1)*3 + (b+1)] * r[clamp(dy+a)][clamp(dx+b)] where r is the float32
+ *   bilinear result on the output grid and clamp keeps rows in [0, out_h-1]
+ *   and columns in [0, out_w-1] (replicate border).  Each channel is filtered
+ *   on its own.  Batch as above (plane layout is HWC here).
+ *
+ * batch >= 0 (0 is a no-op); batch strides are bytes and must keep the frames
+ * from overlapping when batch > 1.
+ */
+typedef struct {
+    int kind;
+    int batch;
+    size_t src_batch_stride;
+    size_t dst_batch_stride;
+    float mean[4];
+    float std[4];
+    float w3x3[9];
+} rz_epilogue;
+
+/*
+ * Bilinear resize with an epilogue.  src_dtype is RZ_U8 for
+ * RZ_EPI_NORMALIZE_NCHW and RZ_F32 for RZ_EPI_FILTER3X3; mode must be
+ * RZ_LINEAR.  Other arguments as resize_u8/resize_f32.  std[c] must be
+ * non-zero and finite.
+ */
+RZ_API int resize_fused(rz_plan p, const void *src, int src_dtype, size_t src_pitch, void *dst, size_t dst_pitch,
+                 int H, int W, int C, int out_h, int out_w, int mode, const rz_epilogue *e, void *stream);
+
+/*
+ * End-to-end uint8 resize from HOST memory: copies the image from
+ * host_src (pitch host_src_pitch) into the caller's device buffer dev_src
+ * (pitch dev_src_pitch), resizes it into dev_dst (pitch dev_dst_pitch) and
+ * copies the result back to host_dst (pitch host_dst_pitch), all queued on
+ * `stream` (asynchronous; page-locked host memory makes the copies overlap
+ * other work).  Allocates nothing; the caller provides both device buffers.
+ * The host buffers must stay valid until the stream reaches the end of the
+ * call's work.
+ */
+RZ_API int resize_u8_host(rz_plan p, const uint8_t *host_src, size_t host_src_pitch, uint8_t *host_dst,
+                   size_t host_dst_pitch, uint8_t *dev_src, size_t dev_src_pitch, uint8_t *dev_dst,
+                   size_t dev_dst_pitch, int H, int W, int C, int out_h, int out_w, int mode, void *stream);
+
+/*
+ * Host-only: fill the tables resize_plan_create would upload, for tests and
+ * tools.  Any output pointer may be NULL.  For RZ_LINEAR: ofs[n_out] (int32),
+ * w_q11[n_out] (int32, 0..2048), u[n_out] (float).  For RZ_NEAREST only ofs is
+ * written.  n_in >= 1, 0 <= n_out, both <= RZ_MAX_DIM.  No CUDA call is made.
+ */
+RZ_API int resize_axis_table(int n_in, int n_out, int mode, int32_t *ofs, int32_t *w_q11, float *u);
+
+/* Human-readable name of a status code (static string). */
+RZ_API const char *resize_strerror(int code);
+
+/* cudaError_t of the last RZ_ERR_CUDA returned on this host thread (0 if none). */
+RZ_API int resize_last_cuda_error(void);
+
+/*
+ * Tile override for tuning (0 = automatic): output rows and output columns
+ * per CTA for kernel family `kind` (RZ_U8, RZ_F32, or 2 + RZ_EPI_* for the
+ * fused kernels) of this plan.  Results do not depend on it; only speed does.
+ * Rejected (RZ_ERR_ARG) if the tile would not fit in shared memory.
+ */
+RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_cols);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBRESIZE_H */

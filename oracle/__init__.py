@@ -11,11 +11,10 @@ bytes.  See ``oracle.c`` for the definitions and the passages they follow.
 from __future__ import annotations
 
 import ctypes
-import os
 
 import numpy as np
 
-from ._build import build, library_path
+from ._build import build
 
 _lib = None
 
@@ -28,9 +27,7 @@ def _load():
     global _lib
     if _lib is not None:
         return _lib
-    path = library_path()
-    if not os.path.exists(path):
-        build()
+    path = build()          # compiles only when oracle.c is newer than the library
     lib = ctypes.CDLL(path)
     lib.oracle_linear_coord.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_i64),
                                         ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
@@ -43,6 +40,8 @@ def _load():
         f = getattr(lib, name)
         f.argtypes = [_p, _i64, _int, _int, _int, _p, _i64, _int, _int]
         f.restype = None
+    lib.oracle_linear_u8_rows.argtypes = [_p, _i64, _int, _int, _int, _p, _i64, _int, _int, _int, _int]
+    lib.oracle_linear_u8_rows.restype = None
     lib.oracle_linear_f32.argtypes = [_p, _i64, _int, _int, _int, _p, _int, _int]
     lib.oracle_linear_f32.restype = None
     lib.oracle_nearest_f32.argtypes = [_p, _i64, _int, _int, _int, _p, _int, _int]
@@ -94,6 +93,18 @@ def linear_u8(src: np.ndarray, out_h: int, out_w: int) -> np.ndarray:
     dst = np.empty((out_h, out_w, C), np.uint8)
     _load().oracle_linear_u8(_ptr(s), s.strides[0], H, W, C, _ptr(dst), dst.strides[0], out_h, out_w)
     return dst
+
+
+def linear_u8_rows(src: np.ndarray, out_h: int, out_w: int, dy0: int, dy1: int) -> np.ndarray:
+    """Output rows [dy0, dy1) of the u8 bilinear resize to (out_h, out_w); shape (dy1-dy0, out_w, C)."""
+    s = _as_hwc(np.asarray(src))
+    assert s.dtype == np.uint8 and 0 <= dy0 <= dy1 <= out_h
+    H, W, C = s.shape
+    full = np.empty((dy1 - dy0, out_w, C), np.uint8)
+    # rows dy0.. land at the start of `full`: shift the destination base back by dy0 rows
+    base = full.ctypes.data - dy0 * full.strides[0]
+    _load().oracle_linear_u8_rows(_ptr(s), s.strides[0], H, W, C, base, full.strides[0], out_h, out_w, dy0, dy1)
+    return full
 
 
 def nearest_u8(src: np.ndarray, out_h: int, out_w: int) -> np.ndarray:

@@ -101,10 +101,10 @@ int64_t oracle_nearest_index(int64_t n_in, int64_t n_out, int64_t d)
  *           + 2^21 ) >> 22
  * where s(i, j) is column i, row j, and A/B are the 11-bit weights of u/v.
  */
-void oracle_linear_u8(const uint8_t *src, int64_t src_pitch, int H, int W, int C,
-                      uint8_t *dst, int64_t dst_pitch, int OH, int OW)
+void oracle_linear_u8_rows(const uint8_t *src, int64_t src_pitch, int H, int W, int C,
+                           uint8_t *dst, int64_t dst_pitch, int OH, int OW, int dy0, int dy1)
 {
-    for (int64_t dy = 0; dy < OH; dy++) {
+    for (int64_t dy = dy0; dy < dy1 && dy < OH; dy++) {
         int64_t j, rv, dv;
         oracle_linear_coord(H, OH, dy, &j, &rv, &dv);
         int64_t B1 = oracle_weight_q11(rv, dv);
@@ -126,6 +126,13 @@ void oracle_linear_u8(const uint8_t *src, int64_t src_pitch, int H, int W, int C
             }
         }
     }
+}
+
+/* All output rows; the row-range form above lets a caller time a bounded sample. */
+void oracle_linear_u8(const uint8_t *src, int64_t src_pitch, int H, int W, int C,
+                      uint8_t *dst, int64_t dst_pitch, int OH, int OW)
+{
+    oracle_linear_u8_rows(src, src_pitch, H, W, C, dst, dst_pitch, OH, OW, 0, OH);
 }
 
 /* u8 nearest, [INTERP] §2.1 read as OpenCV INTER_NEAREST (floor). */

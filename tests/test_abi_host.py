@@ -1,0 +1,137 @@
+"""Host-side tests of the C ABI: no GPU needed, no kernel launched.
+
+* the library loads and exports every symbol include/gbresize.h declares;
+* the plan's sampling tables (resize_axis_table, the same code the plan
+  uploads) match an independent computation in exact rationals;
+* argument validation rejects bad calls before touching CUDA.
+"""
+import ctypes
+import math
+import os
+import re
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bilinear_image_resize_gb300 import _build, _native
+    _build.build()
+    return _native.load()
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "gbresize.h")) as f:
+        text = f.read()
+    return re.findall(r"^RZ_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from bilinear_image_resize_gb300 import _native
+    names = declared_symbols()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _native.SIGNATURES, f"binding lacks {n}"
+    assert set(_native.SIGNATURES) == set(names)
+
+
+def test_epilogue_struct_layout_matches_header():
+    from bilinear_image_resize_gb300 import RzEpilogue
+    # int, int, size_t, size_t, float[4], float[4], float[9] on LP64
+    assert ctypes.sizeof(RzEpilogue) == 4 + 4 + 8 + 8 + 16 + 16 + 36 + 4  # trailing pad to 8
+
+
+def exact_linear(n_in, n_out):
+    ofs, q, u = [], [], []
+    for d in range(n_out):
+        x = Fraction(2 * d + 1, 2) * Fraction(n_in, n_out) - Fraction(1, 2)
+        i = math.floor(x)
+        frac = x - i
+        if i < 0 or i >= n_in - 1:       # one clamped tap
+            ofs.append(min(max(i, 0), n_in - 1))
+            q.append(0)
+            u.append(0.0)
+        else:
+            ofs.append(i)
+            q.append(math.floor(2048 * frac + Fraction(1, 2)))
+            u.append(float(np.float32(float(frac))))
+    return np.array(ofs), np.array(q), np.array(u, np.float32)
+
+
+GEOMS = [(64, 128), (48, 96), (64, 32), (3840, 1920), (1920, 3840), (1280, 224), (720, 224), (8192, 5980),
+         (1, 1), (1, 9), (9, 1), (3, 4096), (4096, 3), (7, 5), (5, 7), (1920, 1280), (1080, 720)]
+
+
+@pytest.mark.parametrize("geom", GEOMS)
+def test_linear_tables_match_exact_rationals(lib, geom):
+    import bilinear_image_resize_gb300 as rz
+    n_in, n_out = geom
+    ofs, q, u = rz.resize_axis_table(n_in, n_out, rz.RZ_LINEAR)
+    eo, eq, eu = exact_linear(n_in, n_out)
+    np.testing.assert_array_equal(ofs, eo)
+    np.testing.assert_array_equal(q, eq)
+    np.testing.assert_array_equal(u, eu)
+    assert np.all((q >= 0) & (q <= 2048))
+    assert np.all(np.diff(ofs) >= 0)            # rows are visited in order
+    assert np.all((ofs >= 0) & (ofs <= n_in - 1))
+
+
+@pytest.mark.parametrize("geom", GEOMS)
+def test_nearest_tables_match_floor(lib, geom):
+    import bilinear_image_resize_gb300 as rz
+    n_in, n_out = geom
+    ofs, _, _ = rz.resize_axis_table(n_in, n_out, rz.RZ_NEAREST)
+    expect = [min((d * n_in) // n_out, n_in - 1) for d in range(n_out)]
+    np.testing.assert_array_equal(ofs, expect)
+
+
+def test_axis_table_rejects_bad_args(lib):
+    assert lib.resize_axis_table(0, 5, 1, None, None, None) == 1
+    assert lib.resize_axis_table(5, -1, 1, None, None, None) == 1
+    assert lib.resize_axis_table(5, 5, 7, None, None, None) == 1
+    assert lib.resize_axis_table(65537, 5, 1, None, None, None) == 1
+    assert lib.resize_axis_table(5, 0, 1, None, None, None) == 0
+
+
+def test_calls_validate_before_cuda(lib):
+    RZ_ERR_ARG = 1
+    h = ctypes.c_void_p()
+    # bad geometry / mode: rejected before any CUDA call
+    assert lib.resize_plan_create(ctypes.byref(h), 0, 5, 5, 5, 1, None) == RZ_ERR_ARG
+    assert h.value is None
+    assert lib.resize_plan_create(ctypes.byref(h), 5, 5, 5, 5, 9, None) == RZ_ERR_ARG
+    assert lib.resize_plan_create(None, 5, 5, 5, 5, 1, None) == RZ_ERR_ARG
+    # null plan
+    assert lib.resize_u8(None, 16, 3, 32, 3, 1, 1, 1, 1, 1, 1, None) == RZ_ERR_ARG
+    assert lib.resize_f32(None, 16, 12, 32, 12, 1, 1, 3, 1, 1, 1, None) == RZ_ERR_ARG
+    assert lib.resize_fused(None, 16, 0, 3, 32, 4, 1, 1, 3, 1, 1, 1, None, None) == RZ_ERR_ARG
+    assert lib.resize_u8_host(None, 16, 3, 32, 3, 48, 3, 64, 3, 1, 1, 3, 1, 1, 1, None) == RZ_ERR_ARG
+    assert lib.resize_plan_status(None, None) == RZ_ERR_ARG
+    assert lib.resize_plan_set_tile(None, 0, 1, 1) == RZ_ERR_ARG
+    assert lib.resize_plan_destroy(None) == 0
+
+
+def test_plan_create_without_gpu_reports_cuda_error():
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+    except ImportError:
+        pass
+    from bilinear_image_resize_gb300 import _native
+    lib = _native.load()
+    h = ctypes.c_void_p()
+    rc = lib.resize_plan_create(ctypes.byref(h), 10, 10, 5, 5, 1, None)
+    assert rc == 3 and h.value is None
+    assert lib.resize_last_cuda_error() != 0
+
+
+def test_strerror(lib):
+    for code in range(6):
+        assert lib.resize_strerror(code)
+    assert lib.resize_strerror(99) == b"unknown status"

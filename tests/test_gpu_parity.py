@@ -1,0 +1,309 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+uint8 results must be bit-exact; float32 results within 1e-4 absolute on
+values in [0, 255] (the bound the float32 path is specified to); nearest is
+a copy and must be exact for both types.  The five workloads run at full
+size and are compared on every output element; a seeded sweep of small
+geometries covers ragged tiles, every channel count, odd pitches, unaligned
+pointers, extreme ratios and the degenerate sizes.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from bilinear_image_resize_gb300 import synth
+from gpu_util import Canvas, device_image, max_abs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+F32_TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def rz():
+    import __graft_entry__
+    __graft_entry__.build()
+    import bilinear_image_resize_gb300 as m
+    torch.cuda.set_device(0)
+    return m
+
+
+def gpu_u8(rz, img, OH, OW, mode, src_pitch=None, src_off=0, dst_pad=0, dst_off=0, tile=None, stream=None):
+    if img.ndim == 2:
+        img = img[:, :, None]
+    H, W, C = img.shape
+    src, _keep = device_image(img, src_pitch, src_off)
+    out = Canvas(OH, OW, C, torch.uint8, dst_pad, dst_off)
+    with rz.resize_plan_create(H, W, OH, OW, mode) as plan:
+        if tile:
+            rz.resize_plan_set_tile(plan, rz.KIND_U8, *tile)
+        rz.resize_u8(plan, src, out.view, stream=stream)
+        torch.cuda.synchronize()
+        assert rz.resize_plan_status(plan) == rz.RZ_OK
+    out.check_canary()
+    return out.result()
+
+
+def gpu_f32(rz, img, OH, OW, mode, src_pitch=None, src_off=0, dst_pad=0, dst_off=0, tile=None):
+    if img.ndim == 2:
+        img = img[:, :, None]
+    H, W, C = img.shape
+    src, _keep = device_image(img, src_pitch, src_off)
+    out = Canvas(OH, OW, C, torch.float32, dst_pad, dst_off)
+    with rz.resize_plan_create(H, W, OH, OW, mode) as plan:
+        if tile:
+            rz.resize_plan_set_tile(plan, rz.KIND_F32, *tile)
+        rz.resize_f32(plan, src, out.view)
+        torch.cuda.synchronize()
+        assert rz.resize_plan_status(plan) == rz.RZ_OK
+    out.check_canary()
+    return out.result()
+
+
+def check_u8(rz, img, OH, OW, mode, **kw):
+    got = gpu_u8(rz, img, OH, OW, mode, **kw)
+    want = (oracle.linear_u8 if mode == rz.RZ_LINEAR else oracle.nearest_u8)(img, OH, OW)
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)
+        raise AssertionError(f"{len(bad)} u8 mismatches, first at {bad[0].tolist()}: "
+                             f"gpu {got[tuple(bad[0])]} oracle {want[tuple(bad[0])]}")
+
+
+def check_f32(rz, img, OH, OW, mode, **kw):
+    got = gpu_f32(rz, img, OH, OW, mode, **kw)
+    if mode == rz.RZ_LINEAR:
+        err = max_abs(got, oracle.linear_f32(img, OH, OW))
+        assert err <= F32_TOL, err
+        return err
+    np.testing.assert_array_equal(got, oracle.nearest_f32(img, OH, OW))
+    return 0.0
+
+
+# ------------------------------------------------------------------ the five workloads, full size
+
+def test_tiny_gray_64x48(rz):
+    img = synth.tiny_gray()
+    check_u8(rz, img, 96, 128, rz.RZ_LINEAR)
+    check_u8(rz, img, 24, 32, rz.RZ_NEAREST)
+
+
+def test_smooth_rgb_1080p(rz):
+    img = synth.smooth_rgb(1920, 1080, 2)
+    check_u8(rz, img, 540, 960, rz.RZ_LINEAR)
+    check_u8(rz, img, 720, 1280, rz.RZ_LINEAR)
+
+
+def test_smooth_rgb_4k(rz):
+    img4k = synth.smooth_rgb(3840, 2160, 3)
+    check_u8(rz, img4k, 1080, 1920, rz.RZ_LINEAR)
+    check_u8(rz, img4k, 1080, 1920, rz.RZ_NEAREST)
+    img1080 = synth.smooth_rgb(1920, 1080, 2)
+    check_u8(rz, img1080, 2160, 3840, rz.RZ_LINEAR)
+
+
+def test_batch_normalize_nchw(rz):
+    frames = synth.frames_rgb()                       # (64, 720, 1280, 3)
+    src = torch.from_numpy(frames).cuda()
+    dst = torch.full((64, 3, 224, 224), -7.0, dtype=torch.float32, device="cuda")
+    with rz.resize_plan_create(720, 1280, 224, 224, rz.RZ_LINEAR) as plan:
+        rz.resize_fused(plan, src, dst, rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=synth.NORM_MEAN,
+                                                         std=synth.NORM_STD))
+        torch.cuda.synchronize()
+        assert rz.resize_plan_status(plan) == rz.RZ_OK
+    got = dst.cpu().numpy()
+    worst = 0.0
+    for n in range(64):
+        want = oracle.linear_u8_normalize(frames[n], 224, 224, synth.NORM_MEAN, synth.NORM_STD)
+        worst = max(worst, max_abs(got[n], want))
+    assert worst <= F32_TOL, worst
+
+
+def test_float_gray_8192_filter3x3(rz):
+    img = synth.float_gray()                          # 8192 x 8192 f32
+    w = synth.filter_weights()
+    OH = OW = int(8192 * 0.73)
+    assert OH == 5980
+    src = torch.from_numpy(img).cuda()
+    dst = torch.empty((OH, OW), dtype=torch.float32, device="cuda")
+    with rz.resize_plan_create(8192, 8192, OH, OW, rz.RZ_LINEAR) as plan:
+        rz.resize_fused(plan, src, dst, rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=w))
+        torch.cuda.synchronize()
+        assert rz.resize_plan_status(plan) == rz.RZ_OK
+    want = oracle.linear_f32_filter3x3(img, OH, OW, w)
+    err = max_abs(dst.cpu().numpy(), want)
+    assert err <= F32_TOL, err
+
+
+def test_float_gray_8192_plain_bilinear(rz):
+    img = synth.float_gray()
+    check_f32(rz, img, 5980, 5980, rz.RZ_LINEAR)
+
+
+# ------------------------------------------------------------------ seeded sweeps
+
+def sweep_cases(seed, n):
+    rng = np.random.default_rng(seed)
+    for _ in range(n):
+        H, W = int(rng.integers(1, 68)), int(rng.integers(1, 68))
+        OH, OW = int(rng.integers(1, 68)), int(rng.integers(1, 68))
+        C = int(rng.choice([1, 3, 4]))
+        pad = int(rng.choice([0, 0, 1, 3, 16, 29]))
+        off = int(rng.choice([0, 0, 1, 5, 16]))
+        yield H, W, OH, OW, C, pad, off
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_sweep_u8(rz, seed):
+    for (H, W, OH, OW, C, pad, off) in sweep_cases(100 + seed, 40):
+        img = synth.random_u8((H, W, C), seed=H * 1000 + W)
+        for mode in (rz.RZ_LINEAR, rz.RZ_NEAREST):
+            check_u8(rz, img, OH, OW, mode, src_pitch=W * C + pad, src_off=off, dst_pad=pad, dst_off=off)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_sweep_f32(rz, seed):
+    for (H, W, OH, OW, C, pad, off) in sweep_cases(200 + seed, 30):
+        img = synth.random_f32((H, W, C), seed=H * 1000 + W)
+        for mode in (rz.RZ_LINEAR, rz.RZ_NEAREST):
+            check_f32(rz, img, OH, OW, mode, src_pitch=W * C + pad, src_off=off, dst_pad=pad, dst_off=off)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_sweep_fused_filter(rz, seed):
+    rng = np.random.default_rng(300 + seed)
+    for _ in range(12):
+        H, W, OH, OW = (int(v) for v in rng.integers(1, 90, size=4))
+        C = int(rng.choice([1, 3, 4]))
+        N = int(rng.integers(1, 4))
+        img = synth.random_f32((N, H, W, C), seed=H * 7 + W)
+        w = (rng.random(9) - 0.3).astype(np.float32)
+        src = torch.from_numpy(img).cuda()
+        dst = torch.empty((N, OH, OW, C), dtype=torch.float32, device="cuda")
+        with rz.resize_plan_create(H, W, OH, OW, rz.RZ_LINEAR) as plan:
+            rz.resize_fused(plan, src, dst, rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=w))
+            torch.cuda.synchronize()
+        got = dst.cpu().numpy()
+        for n in range(N):
+            for c in range(C):
+                want = oracle.filter3x3(oracle.linear_f32(img[n][:, :, c:c + 1].copy(), OH, OW), w)
+                err = max_abs(got[n, :, :, c], want)
+                assert err <= F32_TOL * np.abs(w).sum(), (H, W, OH, OW, C, n, c, err)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_sweep_fused_normalize(rz, seed):
+    rng = np.random.default_rng(400 + seed)
+    for _ in range(12):
+        H, W, OH, OW = (int(v) for v in rng.integers(1, 90, size=4))
+        C = int(rng.choice([1, 3, 4]))
+        N = int(rng.integers(1, 5))
+        frames = synth.random_u8((N, H, W, C), seed=H * 13 + W)
+        mean = rng.random(4) * 0.8
+        std = 0.1 + rng.random(4) * 0.5
+        src = torch.from_numpy(frames).cuda()
+        dst = torch.empty((N, C, OH, OW), dtype=torch.float32, device="cuda")
+        with rz.resize_plan_create(H, W, OH, OW, rz.RZ_LINEAR) as plan:
+            e = rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=np.float32(mean), std=np.float32(std))
+            rz.resize_fused(plan, src, dst, e)
+            torch.cuda.synchronize()
+        got = dst.cpu().numpy()
+        for n in range(N):
+            want = oracle.linear_u8_normalize(frames[n], OH, OW, np.float32(mean).astype(np.float64),
+                                              np.float32(std).astype(np.float64))
+            err = max_abs(got[n], want)
+            assert err <= F32_TOL, (H, W, OH, OW, C, err)
+
+
+# ------------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("geom", [(1, 1, 1, 1), (1, 1, 7, 5), (7, 5, 1, 1), (1, 64, 3, 1), (64, 1, 1, 3),
+                                  (2, 3, 2, 4096), (2, 4096, 3, 2), (4096, 2, 2, 3), (3, 2, 4096, 2),
+                                  (2, 65536, 2, 5), (1, 65536, 1, 65536), (9, 9, 9, 9)])
+def test_degenerate_and_extreme_geometries(rz, geom):
+    H, W, OH, OW = geom
+    for C in (1, 3):
+        img = synth.random_u8((H, W, C), seed=OH + OW)
+        check_u8(rz, img, OH, OW, rz.RZ_LINEAR)
+        check_u8(rz, img, OH, OW, rz.RZ_NEAREST)
+    check_f32(rz, synth.random_f32((H, W, 1), seed=3), OH, OW, rz.RZ_LINEAR)
+
+
+def test_identity_is_a_copy(rz):
+    img = synth.random_u8((33, 47, 3), seed=9)
+    np.testing.assert_array_equal(gpu_u8(rz, img, 33, 47, rz.RZ_LINEAR), img)
+    f = synth.random_f32((33, 47, 4), seed=9)
+    np.testing.assert_array_equal(gpu_f32(rz, f, 33, 47, rz.RZ_LINEAR), f)
+
+
+def test_empty_output_is_a_no_op(rz):
+    img = synth.random_u8((8, 8, 3), seed=1)
+    src, _k = device_image(img)
+    with rz.resize_plan_create(8, 8, 0, 5, rz.RZ_LINEAR) as plan:
+        dst = torch.empty((0, 5, 3), dtype=torch.uint8, device="cuda")
+        rz.resize_u8(plan, src, dst)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("tile", [(1, 1), (1, 16), (3, 7), (5, 64), (16, 128), (64, 4096), (2, 33)])
+def test_tile_shapes_do_not_change_results(rz, tile):
+    img = synth.random_u8((97, 131, 3), seed=77)
+    for (OH, OW) in [(41, 59), (200, 263), (97, 131)]:
+        check_u8(rz, img, OH, OW, rz.RZ_LINEAR, tile=tile)
+        check_u8(rz, img, OH, OW, rz.RZ_NEAREST, tile=tile)
+    f = synth.random_f32((97, 131, 1), seed=78)
+    check_f32(rz, f, 53, 211, rz.RZ_LINEAR, tile=tile)
+
+
+def test_filter_tile_shapes_do_not_change_results(rz):
+    img = synth.random_f32((150, 170), seed=79)
+    w = synth.filter_weights()
+    want = oracle.linear_f32_filter3x3(img, 109, 124, w)
+    src = torch.from_numpy(img).cuda()
+    for tile in [(1, 1), (2, 3), (7, 16), (32, 128), (109, 124), (13, 200)]:
+        dst = torch.empty((109, 124), dtype=torch.float32, device="cuda")
+        with rz.resize_plan_create(150, 170, 109, 124, rz.RZ_LINEAR) as plan:
+            rz.resize_plan_set_tile(plan, rz.KIND_FILTER3X3, *tile)
+            rz.resize_fused(plan, src, dst, rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=w))
+            torch.cuda.synchronize()
+        assert max_abs(dst.cpu().numpy(), want) <= F32_TOL, tile
+
+
+def test_non_default_stream(rz):
+    img = synth.smooth_rgb(1920, 1080, 2)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        got = gpu_u8(rz, img, 540, 960, rz.RZ_LINEAR, stream=s)
+    np.testing.assert_array_equal(got, oracle.linear_u8(img, 540, 960))
+
+
+def test_host_buffers_entry_point(rz):
+    img = synth.smooth_rgb(1920, 1080, 2)
+    hsrc = torch.from_numpy(np.ascontiguousarray(img)).pin_memory()
+    hdst = torch.empty((540, 960, 3), dtype=torch.uint8).pin_memory()
+    dsrc = torch.empty((1080, 1920, 3), dtype=torch.uint8, device="cuda")
+    ddst = torch.empty((540, 960, 3), dtype=torch.uint8, device="cuda")
+    with rz.resize_plan_create(1080, 1920, 540, 960, rz.RZ_LINEAR) as plan:
+        rz.resize_u8_host(plan, hsrc, hdst, dsrc, ddst)
+        torch.cuda.synchronize()
+    np.testing.assert_array_equal(hdst.numpy(), oracle.linear_u8(img, 540, 960))
+
+
+def test_invalid_calls_raise(rz):
+    img = synth.random_u8((8, 8, 3), seed=1)
+    src, _k = device_image(img)
+    with rz.resize_plan_create(8, 8, 4, 4, rz.RZ_LINEAR) as plan:
+        dst = torch.empty((4, 4, 3), dtype=torch.uint8, device="cuda")
+        with pytest.raises(rz.ResizeError):          # wrong geometry
+            rz.resize_u8(plan, src, torch.empty((5, 4, 3), dtype=torch.uint8, device="cuda"))
+        with pytest.raises(rz.ResizeError):          # wrong mode for this plan
+            rz.resize_u8(plan, src, dst, mode=rz.RZ_NEAREST)
+        with pytest.raises(rz.ResizeError):          # C = 2
+            rz.resize_u8(plan, torch.zeros((8, 8, 2), dtype=torch.uint8, device="cuda"),
+                         torch.zeros((4, 4, 2), dtype=torch.uint8, device="cuda"))
+        flat = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+        a = torch.as_strided(flat, (8, 8, 3), (24, 3, 1), 0)
+        b = torch.as_strided(flat, (4, 4, 3), (12, 3, 1), 100)
+        with pytest.raises(rz.ResizeError):          # overlapping source and destination
+            rz.resize_u8(plan, a, b)
+        assert rz.resize_plan_status(plan) == rz.RZ_OK
