@@ -261,11 +261,26 @@ def gpu_arm(args, rank, local_rank, world):
         return g
 
     g_full = capture(G)
+    # the graph must do the work: its output for frame 0 equals an eager call's
+    ref0 = torch.empty_like(outs[0])
+    with torch.cuda.stream(stream):
+        if kind == "u8":
+            rz.resize_u8(plan, frames[0], ref0, stream=stream)
+        else:
+            rz.resize_fused(plan, frames[0], ref0, epi, stream=stream)
+        outs[0].zero_()
+        g_full.replay()
+    torch.cuda.synchronize()
+    if not torch.equal(outs[0], ref0):
+        raise RuntimeError("captured graph did not reproduce the eager result")
+    del ref0
     rem = args.steps % G
     g_rem = capture(rem) if rem else None
     reps = args.steps // G
-    # graph warm-up replays
-    g_full.replay()
+    # graph warm-up replays; replay() launches on torch's current stream, so
+    # every replay below runs with `stream` current
+    with torch.cuda.stream(stream):
+        g_full.replay()
     torch.cuda.synchronize()
 
     dist = None
@@ -276,8 +291,9 @@ def gpu_arm(args, rank, local_rank, world):
     sampler.start()
     time.sleep(0.3)
     # keep the GPU busy for a moment before the timed region so clocks settle
-    for _ in range(max(1, int(0.3 / max(1e-6, G * 10e-6)))):
-        g_full.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, int(0.3 / max(1e-6, G * 10e-6)))):
+            g_full.replay()
     torch.cuda.synchronize()
 
     ev0 = torch.cuda.Event(enable_timing=True)
@@ -286,12 +302,13 @@ def gpu_arm(args, rank, local_rank, world):
         dist.barrier()
     torch.cuda.synchronize()
     t_host0 = time.time()
-    ev0.record(stream)
-    for _ in range(reps):
-        g_full.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    ev1.record(stream)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
     torch.cuda.synchronize()
     t_host1 = time.time()
     if dist:
