@@ -229,6 +229,12 @@ def gpu_arm(args, rank, local_rank, world):
         tr, tw = (int(v) for v in args.tile.split("x"))
         fam = {"u8": rz.KIND_U8, "norm": rz.KIND_NORMALIZE, "filt": rz.KIND_FILTER3X3}[kind]
         rz.resize_plan_set_tile(plan, fam, tr, tw)
+    if args.stages:
+        rz.resize_plan_set_option(plan, rz.RZ_OPT_STAGES, args.stages)
+    if args.generic:
+        rz.resize_plan_set_option(plan, rz.RZ_OPT_GENERIC_ONLY, 1)
+    if args.ctas_per_sm:
+        rz.resize_plan_set_option(plan, rz.RZ_OPT_CTAS_PER_SM, args.ctas_per_sm)
     epi = None
     if kind == "norm":
         epi = rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=synth.NORM_MEAN, std=synth.NORM_STD)
@@ -485,6 +491,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--tile", default="", help="override tile as ROWSxCOLS (tuning only)")
+    ap.add_argument("--stages", type=int, default=0, help="staged-tile ring depth (tuning only)")
+    ap.add_argument("--generic", action="store_true", help="disable the exact 2x path (tuning only)")
+    ap.add_argument("--ctas-per-sm", type=int, default=0, help="cap resident CTAs per SM (tuning only)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -532,6 +541,9 @@ def main():
                 "launch": f"CUDA graphs of {r['graph_steps']} resize_u8 launches, one stream",
                 "algorithmic_bytes_per_step": r["step_bytes"],
                 "parallelism": f"{world} independent replica(s)",
+                "tuning": {k: v for k, v in (("tile", args.tile), ("stages", args.stages),
+                                             ("generic_only", args.generic), ("ctas_per_sm", args.ctas_per_sm))
+                           if v} or "automatic",
             },
             "hbm_gbs": r["achieved_gbs"],
             "roofline": {

@@ -16,15 +16,17 @@ import ctypes
 from . import _native
 from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_EPI_FILTER3X3,
                       RZ_EPI_NORMALIZE_NCHW, RZ_ERR_ARG, RZ_ERR_CUDA, RZ_ERR_NOMEM, RZ_ERR_TIMEOUT,
-                      RZ_ERR_UNSUPPORTED, RZ_F32, RZ_LINEAR, RZ_MAX_DIM, RZ_NEAREST, RZ_OK, RZ_U8, RzEpilogue)
+                      RZ_ERR_UNSUPPORTED, RZ_F32, RZ_LINEAR, RZ_MAX_DIM, RZ_NEAREST, RZ_OK, RZ_OPT_CTAS_PER_SM,
+                      RZ_OPT_GENERIC_ONLY, RZ_OPT_STAGES, RZ_U8, RzEpilogue)
 
 __all__ = [
     "ResizeError", "Plan", "resize_plan_create", "resize_plan_destroy", "resize_plan_status",
-    "resize_plan_set_tile", "resize_u8", "resize_f32", "resize_fused", "resize_u8_host",
+    "resize_plan_set_tile", "resize_plan_set_option", "resize_u8", "resize_f32", "resize_fused", "resize_u8_host",
     "resize_axis_table", "resize_strerror", "resize_last_cuda_error", "make_epilogue",
     "RZ_LINEAR", "RZ_NEAREST", "RZ_U8", "RZ_F32", "RZ_EPI_NORMALIZE_NCHW", "RZ_EPI_FILTER3X3",
     "RZ_OK", "RZ_ERR_ARG", "RZ_ERR_UNSUPPORTED", "RZ_ERR_CUDA", "RZ_ERR_NOMEM", "RZ_ERR_TIMEOUT",
     "RZ_MAX_DIM", "KIND_U8", "KIND_F32", "KIND_NORMALIZE", "KIND_FILTER3X3",
+    "RZ_OPT_STAGES", "RZ_OPT_GENERIC_ONLY", "RZ_OPT_CTAS_PER_SM",
 ]
 
 
@@ -98,6 +100,10 @@ def resize_plan_status(plan: Plan) -> int:
 
 def resize_plan_set_tile(plan: Plan, kind: int, tile_rows: int, tile_cols: int) -> None:
     _check(_native.load().resize_plan_set_tile(plan.handle, kind, tile_rows, tile_cols), "resize_plan_set_tile")
+
+
+def resize_plan_set_option(plan: Plan, option: int, value: int) -> None:
+    _check(_native.load().resize_plan_set_option(plan.handle, option, value), "resize_plan_set_option")
 
 
 def _hwc(t, name):

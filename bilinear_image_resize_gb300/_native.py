@@ -24,6 +24,10 @@ RZ_ERR_NOMEM = 4
 RZ_ERR_TIMEOUT = 5
 RZ_MAX_DIM = 65536
 
+RZ_OPT_STAGES = 1
+RZ_OPT_GENERIC_ONLY = 2
+RZ_OPT_CTAS_PER_SM = 3
+
 # kernel families for resize_plan_set_tile
 KIND_U8 = 0
 KIND_F32 = 1
@@ -53,6 +57,7 @@ SIGNATURES = {
     "resize_plan_destroy": (_i, [_p]),
     "resize_plan_status": (_i, [_p, ctypes.POINTER(_i)]),
     "resize_plan_set_tile": (_i, [_p, _i, _i, _i]),
+    "resize_plan_set_option": (_i, [_p, _i, _i]),
     "resize_u8": (_i, [_p, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
     "resize_f32": (_i, [_p, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
     "resize_fused": (_i, [_p, _p, _i, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, ctypes.POINTER(RzEpilogue), _p]),

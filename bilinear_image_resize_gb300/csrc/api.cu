@@ -80,8 +80,9 @@ void axis_nearest(int n_in, int n_out, int32_t *ofs)
 }
 
 struct TileCfg {
-    int TR = 0, TW = 0, tiles_x = 0, tiles_y = 0, max_rows = 0, slot_bytes = 0;
+    int TR = 0, TW = 0, tiles_x = 0, tiles_y = 0, max_rows = 0, slot_bytes = 0, stages = 0, variant = 0;
     size_t smem = 0;
+    int grid = 0;
 };
 
 }  // namespace
@@ -94,9 +95,12 @@ struct rz_plan_s {
     int2 *d_xq = nullptr, *d_xf = nullptr, *d_yq = nullptr, *d_yf = nullptr;
     int *d_status = nullptr;
     std::mutex mu;
-    struct Entry { int fam, C, batch_log; TileCfg cfg; };
+    struct Entry { int fam, C, batch; TileCfg cfg; };
     std::vector<Entry> cache;
     int over_tr[rz::FAM_COUNT] = {}, over_tw[rz::FAM_COUNT] = {};
+    int opt_stages = 0;        // 0: automatic
+    int opt_generic = 0;       // 1: never use an exact-ratio specialisation
+    int opt_ctas_per_sm = 0;   // 0: as many as fit
 };
 
 namespace {
@@ -148,7 +152,7 @@ int max_tile_rows(const rz_plan_s &p, int fam, int TR)
     return m;
 }
 
-bool eval_tile(const rz_plan_s &p, int fam, int C, int TR, int TW, TileCfg *out)
+bool eval_tile(const rz_plan_s &p, int fam, int C, int TR, int TW, int stages, TileCfg *out)
 {
     TileCfg t;
     t.TR = std::max(1, std::min(TR, p.OH));
@@ -157,90 +161,148 @@ bool eval_tile(const rz_plan_s &p, int fam, int C, int TR, int TW, TileCfg *out)
     t.tiles_y = (p.OH + t.TR - 1) / t.TR;
     t.slot_bytes = max_slot_bytes(p, fam, C, t.TW);
     t.max_rows = max_tile_rows(p, fam, t.TR);
-    const SmemLayout L = rz::smem_layout(fam, C, t.TR, t.TW, t.max_rows, t.slot_bytes);
+    t.stages = stages;
+    const SmemLayout L = rz::smem_layout(fam, C, t.TR, t.TW, t.max_rows, t.slot_bytes, stages);
     t.smem = static_cast<size_t>(L.total);
     *out = t;
     return L.total <= rz::kMaxSmem;
 }
 
-constexpr int kSms = 152;
-constexpr int kSoftSmem = 48 * 1024;     // keeps >= 4 CTAs resident per SM
+constexpr int kSms = 152;                // GB300; the launch itself asks the device
+constexpr int kSoftSmem = 48 * 1024;     // keeps several CTAs resident per SM
 constexpr int kFilterSmem = 96 * 1024;   // the 3x3 tile trades occupancy for less halo
+constexpr int kDefaultStages = 3;
 
-// Automatic tile choice.  Plain resize and normalise: rows as wide as the
-// output (or the widest power-of-two strip whose staged row stays within
-// 16 KB), then as many output rows per tile as keep the CTA under 48 KB of
-// shared memory while still giving every SM about eight CTAs.  3x3 filter:
-// 128-column strips of up to 32 rows, so that the one-pixel halo costs a
-// few per cent.
-TileCfg choose_tile(const rz_plan_s &p, int fam, int C, int batch)
+// True when the plan is an exact 2x downscale on both axes: every column and
+// row samples x = 2d + 1/2 (weight 1024 on taps 2d and 2d + 1).
+bool is_down2(const rz_plan_s &p)
+{
+    if (p.mode != RZ_LINEAR || p.W != 2 * p.OW || p.H != 2 * p.OH) return false;
+    for (int d = 0; d < p.OW; d++)
+        if (p.xofs[d] != 2 * d || p.xq[d] != 1024) return false;
+    for (int d = 0; d < p.OH; d++)
+        if (p.yofs[d] != 2 * d || p.yq[d] != 1024) return false;
+    return true;
+}
+
+// Automatic tile choice for persistent CTAs.  Plain resize and normalise:
+// rows as wide as the output (or the widest power-of-two strip whose staged
+// row stays within 16 KB), narrowed while there are fewer than about twelve
+// tiles per SM (for balance across SMs), then as many output rows per tile as
+// keep the staged ring under 48 KB with that many tiles.  3x3 filter: strips
+// of 128 columns and up to 32 rows, so the one-pixel halo costs a few per cent.
+TileCfg choose_tile(const rz_plan_s &p, int fam, int C, int batch, int stages, bool down2)
 {
     const int out_es = rz::fam_out_es(fam);
+    const int px_bytes = fam == rz::FAM_NORM ? 4 : C * out_es;
+    TileCfg best;
+    if (fam == rz::FAM_FILT) {
+        for (int TW : {128, 64, 32, 16, 8, 4, 2, 1})
+            for (int TR : {32, 16, 8, 4, 2, 1}) {
+                TileCfg t;
+                if (eval_tile(p, fam, C, TR, TW, stages, &t) && t.smem <= static_cast<size_t>(kFilterSmem))
+                    return t;
+            }
+        for (int TW : {16, 8, 4, 2, 1})
+            if (eval_tile(p, fam, C, 1, TW, 1, &best)) return best;
+        return best;
+    }
     std::vector<int> tws;
     tws.push_back(p.OW);
     for (int w = 4096; w >= 1; w >>= 1)
         if (w < p.OW) tws.push_back(w);
-    TileCfg best;
-    if (fam == rz::FAM_FILT) {
-        for (int TW : {128, 64, 32, 16, 8, 4, 2, 1}) {
-            for (int TR : {32, 16, 8, 4, 2, 1}) {
-                TileCfg t;
-                if (eval_tile(p, fam, C, TR, TW, &t) && t.smem <= static_cast<size_t>(kFilterSmem))
-                    return t;
-            }
-        }
-        for (int TW : {16, 8, 4, 2, 1})
-            if (eval_tile(p, fam, C, 1, TW, &best)) return best;
-        return best;
-    }
-    int TW = 1;
+    auto ok_width = [&](int w) {
+        if (w >= p.OW) return true;
+        if ((w * px_bytes) % 16 != 0) return false;
+        return !down2 || (w % 8) == 0;
+    };
+    const long long want_tiles = 12LL * kSms;
+    int TW = 0;
     for (int w : tws) {
-        const int px_bytes = fam == rz::FAM_NORM ? 4 : C * out_es;
+        if (!ok_width(w)) continue;
         const int row_out = px_bytes * std::min(w, p.OW);
-        const bool aligned = (w >= p.OW) || ((w * px_bytes) % 16 == 0);
-        if (!aligned) continue;
-        if (max_slot_bytes(p, fam, C, w) <= 16384 && row_out <= 16384) { TW = w; break; }
+        if (max_slot_bytes(p, fam, C, w) > 16384 || row_out > 16384) continue;
+        if (TW == 0) TW = w;
+        const long long tiles = static_cast<long long>(batch) * p.OH * ((p.OW + w - 1) / w);
+        TW = w;
+        if (tiles >= want_tiles || w <= 64) break;
+    }
+    if (TW == 0) {
+        // no strip of 16 KB: fall back to the narrowest widths that fit
+        for (int w = 32; w >= 1; w >>= 1)
+            if (ok_width(w) || w == 1) { TW = w; break; }
     }
     TileCfg t1;
-    if (!eval_tile(p, fam, C, 1, TW, &t1)) {
-        // a single row of this width does not fit: fall back to narrow strips
-        for (int w = TW / 2; w >= 1; w /= 2)
-            if (eval_tile(p, fam, C, 1, w, &t1)) return t1;
-        return t1;
+    int st = stages;
+    while (!eval_tile(p, fam, C, 1, TW, st, &t1)) {
+        if (st > 1) { st--; continue; }
+        if (TW == 1) return t1;
+        TW = std::max(1, TW / 2);
     }
     best = t1;
-    const long long want = std::min<long long>(8LL * kSms, static_cast<long long>(batch) * t1.tiles_x * t1.tiles_y);
     for (int TR = 2; TR <= 64; TR *= 2) {
         TileCfg t;
-        if (!eval_tile(p, fam, C, TR, TW, &t) || t.smem > static_cast<size_t>(kSoftSmem)) break;
-        if (static_cast<long long>(batch) * t.tiles_x * t.tiles_y < want) break;
+        if (!eval_tile(p, fam, C, TR, TW, st, &t) || t.smem > static_cast<size_t>(kSoftSmem)) break;
+        if (static_cast<long long>(batch) * t.tiles_x * t.tiles_y < want_tiles) break;
         best = t;
         if (TR >= p.OH) break;
     }
     return best;
 }
 
-int batch_log(int batch)
+std::mutex g_attr_mu;
+std::vector<std::pair<int, const void *>> g_attr_done;  // (device, kernel) with the smem opt-in applied
+
+int ensure_smem_attr(int dev, const void *fn)
 {
-    int l = 0;
-    while ((1 << l) < batch && l < 30) l++;
-    return l;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    for (const auto &e : g_attr_done)
+        if (e.first == dev && e.second == fn) return 0;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, rz::kMaxSmem);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    g_attr_done.push_back({dev, fn});
+    return 0;
 }
 
-// Tile for this call: the override if one is set, else the cached automatic
-// choice.  Returns false if an override does not fit in shared memory.
-bool get_tile(rz_plan_s *p, int fam, int C, int batch, TileCfg *out)
+// Tile and grid for this call: the override if one is set, else the cached
+// automatic choice.  Returns an RZ_* status.
+int get_tile(rz_plan_s *p, int fam, int C, int batch, TileCfg *out, const void **fn_out)
 {
     std::lock_guard<std::mutex> lk(p->mu);
-    if (p->over_tr[fam] > 0 && p->over_tw[fam] > 0)
-        return eval_tile(*p, fam, C, p->over_tr[fam], p->over_tw[fam], out);
-    const int bl = batch_log(batch);
     for (const auto &e : p->cache)
-        if (e.fam == fam && e.C == C && e.batch_log == bl) { *out = e.cfg; return true; }
-    TileCfg t = choose_tile(*p, fam, C, 1 << bl);
-    p->cache.push_back({fam, C, bl, t});
+        if (e.fam == fam && e.C == C && e.batch == batch) {
+            *out = e.cfg;
+            *fn_out = rz::kernel_for(fam, p->mode, e.cfg.variant, C);
+            return RZ_OK;
+        }
+    const int stages = p->opt_stages > 0 ? p->opt_stages : kDefaultStages;
+    const bool down2 = fam == rz::FAM_U8 && !p->opt_generic && is_down2(*p);
+    TileCfg t;
+    if (p->over_tr[fam] > 0 && p->over_tw[fam] > 0) {
+        if (!eval_tile(*p, fam, C, p->over_tr[fam], p->over_tw[fam], stages, &t)) return RZ_ERR_ARG;
+    } else {
+        t = choose_tile(*p, fam, C, batch, stages, down2);
+    }
+    t.variant = rz::VAR_GENERIC;
+    if (down2 && (t.tiles_x == 1 || t.TW % 8 == 0)) t.variant = rz::VAR_DOWN2;
+    const void *fn = rz::kernel_for(fam, p->mode, t.variant, C);
+    if (!fn) return RZ_ERR_UNSUPPORTED;
+    int e = ensure_smem_attr(p->device, fn);
+    if (e != 0) return cuda_fail(static_cast<cudaError_t>(e));
+    int per_sm = 0, sms = 0;
+    cudaError_t ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, rz::kThreads, t.smem);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    if (per_sm < 1) return RZ_ERR_ARG;
+    if (p->opt_ctas_per_sm > 0) per_sm = std::min(per_sm, p->opt_ctas_per_sm);
+    const long long ntiles = static_cast<long long>(batch) * t.tiles_x * t.tiles_y;
+    if (ntiles > 0x7fffffffLL) return RZ_ERR_UNSUPPORTED;
+    t.grid = static_cast<int>(std::min<long long>(ntiles, static_cast<long long>(per_sm) * sms));
+    p->cache.push_back({fam, C, batch, t});
     *out = t;
-    return true;
+    *fn_out = fn;
+    return RZ_OK;
 }
 
 bool overlap(const void *a, size_t na, const void *b, size_t nb)
@@ -297,7 +359,9 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     if (rc != RZ_OK) return rc;
 
     TileCfg t;
-    if (!get_tile(p, fam, C, batch, &t)) return RZ_ERR_ARG;
+    const void *fn = nullptr;
+    rc = get_tile(p, fam, C, batch, &t, &fn);
+    if (rc != RZ_OK) return rc;
 
     KArgs a = extra;
     a.src = static_cast<const uint8_t *>(src);
@@ -309,7 +373,8 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     a.dst_plane = nchw ? static_cast<long long>(OH) * static_cast<long long>(dst_pitch) : 0;
     a.H = H; a.W = W; a.OH = OH; a.OW = OW; a.C = C;
     a.TR = t.TR; a.TW = t.TW; a.tiles_x = t.tiles_x; a.tiles_y = t.tiles_y;
-    a.max_rows = t.max_rows; a.slot_bytes = t.slot_bytes;
+    a.batch = batch;
+    a.max_rows = t.max_rows; a.slot_bytes = t.slot_bytes; a.stages = t.stages;
     a.tma_in = aligned16(src) && (src_pitch % 16 == 0) && (in_row % 16 == 0) &&
                (a.src_bstride % 16 == 0);
     const int strip_bytes = t.TW * (nchw ? 1 : C) * out_es;
@@ -320,7 +385,7 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     a.yt = fl ? p->d_yf : p->d_yq;
     a.status = p->d_status;
     if (!do_launch) return RZ_OK;
-    const int e = rz::launch_resize(fam, mode, a, batch, t.smem, stream);
+    const int e = rz::launch_resize(fn, a, t.grid, t.smem, stream);
     if (e != 0) return cuda_fail(static_cast<cudaError_t>(e));
     return RZ_OK;
 }
@@ -444,6 +509,31 @@ int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_cols)
     std::lock_guard<std::mutex> lk(p->mu);
     p->over_tr[kind] = tile_rows;
     p->over_tw[kind] = tile_cols;
+    p->cache.clear();
+    return RZ_OK;
+}
+
+int resize_plan_set_option(rz_plan p, int option, int value)
+{
+    if (!p) return RZ_ERR_ARG;
+    std::lock_guard<std::mutex> lk(p->mu);
+    switch (option) {
+    case RZ_OPT_STAGES:
+        if (value < 0 || value > rz::kMaxStages) return RZ_ERR_ARG;
+        p->opt_stages = value;
+        break;
+    case RZ_OPT_GENERIC_ONLY:
+        if (value != 0 && value != 1) return RZ_ERR_ARG;
+        p->opt_generic = value;
+        break;
+    case RZ_OPT_CTAS_PER_SM:
+        if (value < 0 || value > 32) return RZ_ERR_ARG;
+        p->opt_ctas_per_sm = value;
+        break;
+    default:
+        return RZ_ERR_ARG;
+    }
+    p->cache.clear();
     return RZ_OK;
 }
 

@@ -1,18 +1,20 @@
 // Resize kernels for sm_103a.
 //
-// One CTA owns a tile of TR output rows x TW output columns.  It
-//   1. lists the distinct source rows its output rows sample (two per row for
-//      bilinear, one for nearest, plus a one-row halo for the 3x3 epilogue),
-//   2. stages the needed column span of each of those rows in shared memory
-//      with one bulk (TMA) copy per row, completing on an mbarrier (plain
-//      loads when the addresses are not 16-byte aligned),
-//   3. computes its outputs from shared memory (bilinear as the exact 11-bit
-//      fixed-point sum for uint8, as two lerps for float32), applies the
-//      fused epilogue, and writes the tile into shared memory,
-//   4. stores each output row with one bulk (TMA) copy.
-// HBM is touched once per needed source byte and once per output byte; the
-// staged rows are reused by every output row and column of the tile that
-// samples them.
+// Persistent CTAs (as many as fit on the GPU at once) walk the output tiles
+// of TR rows x TW columns in a static round-robin.  Each CTA keeps a ring of
+// `stages` staged tiles in shared memory:
+//   1. thread 0 lists the distinct source rows the tile's output rows sample
+//      (two per row for bilinear, one for nearest, plus a one-row halo for
+//      the 3x3 epilogue) and issues one bulk (TMA) copy per row for the
+//      needed column span, completing on the stage's mbarrier — `stages`
+//      tiles ahead of the tile being computed (plain loads by all threads
+//      when the source is not 16-byte aligned);
+//   2. all threads compute the tile from shared memory into one of two
+//      output buffers: uint8 bilinear as the exact 11-bit fixed-point sum,
+//      float32 as two lerps, then the fused epilogue;
+//   3. thread 0 writes each output row with one bulk (TMA) store and, while
+//      that store drains, the ring moves on.
+// HBM is read once per needed source byte and written once per output byte.
 //
 // Sampling: CUDA interpolation page (hnwysp.cn/news/129086) §2.1 nearest,
 // §2.2 bilinear weights, §6.1 clamp, §6.2 fixed point, §4.2 fused epilogue;
@@ -22,7 +24,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "rz_internal.h"
 
@@ -73,7 +74,7 @@ __device__ __forceinline__ uint64_t global_ns()
 }
 
 // Wait for phase `parity` of the barrier, at most kWaitLimitNs.  On time-out
-// the status word records RZ_ERR_TIMEOUT and false is returned.
+// the status word (if given) records RZ_ERR_TIMEOUT and false is returned.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status)
 {
     if (mbar_try_wait(bar, parity))
@@ -110,208 +111,226 @@ __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until at most N committed bulk-store groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 
 // Make this thread's generic-proxy shared-memory writes visible to the bulk-copy (async) proxy.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
-__device__ __forceinline__ int ceil_log2(int v)
-{
-    return v <= 1 ? 0 : 32 - __clz(v - 1);
-}
+__device__ __forceinline__ int ceil_log2(int v) { return v <= 1 ? 0 : 32 - __clz(v - 1); }
 
-// ------------------------------------------------------------------ tile set-up
+// ------------------------------------------------------------------ tiles and stages
 
-struct Tile {
-    int b;              // image index within the batch
+struct TileGeom {
     int dy0, dy1;       // output rows [dy0, dy1)
     int dx0, dx1;       // output columns [dx0, dx1)
-    const uint8_t *src; // this image's first source row
-    uint8_t *dst;       // this image's output base
+    const uint8_t *src; // this tile's source image
+    uint8_t *dst;       // this tile's output image
 };
 
-__device__ __forceinline__ Tile decode_tile(const KArgs &a)
+__device__ __forceinline__ TileGeom tile_geom(const KArgs &a, int tile)
 {
-    Tile t;
+    TileGeom g;
     const int per_img = a.tiles_x * a.tiles_y;
-    const int bid = blockIdx.x;
-    t.b = bid / per_img;
-    const int r = bid - t.b * per_img;
+    const int b = tile / per_img;
+    const int r = tile - b * per_img;
     const int ty = r / a.tiles_x;
     const int tx = r - ty * a.tiles_x;
-    t.dy0 = ty * a.TR;
-    t.dy1 = min(t.dy0 + a.TR, a.OH);
-    t.dx0 = tx * a.TW;
-    t.dx1 = min(t.dx0 + a.TW, a.OW);
-    t.src = a.src + (long long)t.b * a.src_bstride;
-    t.dst = a.dst + (long long)t.b * a.dst_bstride;
-    return t;
+    g.dy0 = ty * a.TR;
+    g.dy1 = min(g.dy0 + a.TR, a.OH);
+    g.dx0 = tx * a.TW;
+    g.dx1 = min(g.dx0 + a.TW, a.OW);
+    g.src = a.src + (long long)b * a.src_bstride;
+    g.dst = a.dst + (long long)b * a.dst_bstride;
+    return g;
 }
 
-// Stage the source rows of the tile.  Thread 0 builds the list of distinct
-// source rows for the computed rows dy0-halo .. dy1-1+halo (clamped into the
-// image; rows are non-decreasing in dy, so a row already listed is one of the
-// last two entries), records for each computed row the slots of its two tap
-// rows, and issues one bulk copy per listed row.  Returns false if the copies
-// did not arrive in time (status word set) — the caller then leaves the tile.
+// Stage header, at the start of each stage.
+struct StageHdr {
+    int nrows;   // staged rows (-1: tile rejected)
+    int b_lo;    // byte offset, within a source row, of slot byte 0
+    int nbytes;  // bytes staged per row
+    int pad;
+};
+
+// Thread 0: list the tile's source rows into stage `st`, record for each
+// computed row the slots of its two tap rows, and (bulk path) issue the
+// copies on `bar`.  Source rows are visited in non-decreasing order, so a
+// row already listed is one of the last two entries.
 template <int LINEAR>
-__device__ bool stage_rows(const KArgs &a, const Tile &t, int halo, int in_es, uint8_t *smem, const SmemLayout &L)
+__device__ void prepare_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, uint64_t *bar, int tile, int halo,
+                              int in_es)
 {
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
-    int *hdr = reinterpret_cast<int *>(smem + 8);
-    int *rows = reinterpret_cast<int *>(smem + L.off_rows);
-    int *map = reinterpret_cast<int *>(smem + L.off_map);
-    uint8_t *slots = smem + L.off_slots;
+    StageHdr *h = reinterpret_cast<StageHdr *>(st);
+    int *rows = reinterpret_cast<int *>(st + L.rows_off);
+    int *map = reinterpret_cast<int *>(st + L.map_off);
+    uint8_t *slots = st + L.slots_off;
+    const TileGeom g = tile_geom(a, tile);
 
-    if (threadIdx.x == 0) {
-        // column span of the computed columns, in bytes of a source row
-        const int cx0 = clampi(t.dx0 - halo, 0, a.OW - 1);
-        const int cx1 = clampi(t.dx1 - 1 + halo, 0, a.OW - 1);
-        const int xs0 = a.xt[cx0].x;
-        const int xs1 = LINEAR ? min(a.xt[cx1].x + 1, a.W - 1) : a.xt[cx1].x;
-        int b_lo = xs0 * a.C * in_es;
-        int b_hi = (xs1 + 1) * a.C * in_es;
-        if (a.tma_in) {
-            b_lo &= ~15;
-            b_hi = (b_hi + 15) & ~15;
-        }
-        const int nbytes = b_hi - b_lo;
-
-        int n = 0;
-        bool overflow = nbytes > a.slot_bytes;
-        const int nrc = (t.dy1 - t.dy0) + 2 * halo;
-        for (int k = 0; k < nrc && !overflow; k++) {
-            const int dy = clampi(t.dy0 - halo + k, 0, a.OH - 1);
-            const int r0 = a.yt[dy].x;
-            const int r1 = LINEAR ? min(r0 + 1, a.H - 1) : r0;
-            int s0, s1;
-            if (n > 0 && rows[n - 1] == r0)
-                s0 = n - 1;
-            else if (n > 1 && rows[n - 2] == r0)
-                s0 = n - 2;
-            else {
-                if (n == a.max_rows) { overflow = true; break; }
-                rows[n] = r0;
-                s0 = n++;
-            }
-            if (rows[n - 1] == r1)
-                s1 = n - 1;
-            else {
-                if (n == a.max_rows) { overflow = true; break; }
-                rows[n] = r1;
-                s1 = n++;
-            }
-            map[2 * k] = s0;
-            map[2 * k + 1] = s1;
-        }
-        if (overflow) {
-            // the host sizes max_rows and slot_bytes from the same tables, so
-            // this is unreachable; it guards shared memory all the same
-            atomicExch(a.status, RZ_ERR_ARG);
-            n = -1;
-        }
-        hdr[0] = n;
-        hdr[1] = b_lo;
-        hdr[2] = nbytes;
-        if (n > 0 && a.tma_in) {
-            mbar_init(bar, 1);
-            fence_mbar_init();
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * nbytes));
-            for (int s = 0; s < n; s++)
-                bulk_load(slots + s * a.slot_bytes, t.src + (long long)rows[s] * a.src_pitch + b_lo,
-                          static_cast<uint32_t>(nbytes), bar);
-        }
-    }
-    __syncthreads();
-    const int n = hdr[0];
-    if (n < 0)
-        return false;
+    const int cx0 = clampi(g.dx0 - halo, 0, a.OW - 1);
+    const int cx1 = clampi(g.dx1 - 1 + halo, 0, a.OW - 1);
+    const int xs0 = a.xt[cx0].x;
+    const int xs1 = LINEAR ? min(a.xt[cx1].x + 1, a.W - 1) : a.xt[cx1].x;
+    int b_lo = xs0 * a.C * in_es;
+    int b_hi = (xs1 + 1) * a.C * in_es;
     if (a.tma_in) {
-        const bool ok = mbar_wait_bounded(bar, 0, a.status);
-        // every thread leaves together if any timed out, so no barrier below
-        // is left waiting for threads that returned
-        if (__syncthreads_or(!ok)) {
-            // give copies still in flight a second bounded wait before leaving
-            if (!ok)
-                mbar_wait_bounded(bar, 0, nullptr);
-            return false;
-        }
-    } else {
-        const int b_lo = hdr[1], nbytes = hdr[2];
-        for (int s = 0; s < n; s++) {
-            const uint8_t *g = t.src + (long long)rows[s] * a.src_pitch + b_lo;
-            uint8_t *d = slots + s * a.slot_bytes;
-            for (int k = threadIdx.x; k < nbytes; k += kThreads)
-                d[k] = __ldg(g + k);
-        }
-        __syncthreads();
+        b_lo &= ~15;
+        b_hi = (b_hi + 15) & ~15;
     }
-    return true;
+    const int nbytes = b_hi - b_lo;
+
+    int n = 0;
+    bool overflow = nbytes > a.slot_bytes;
+    const int nrc = (g.dy1 - g.dy0) + 2 * halo;
+    for (int k = 0; k < nrc && !overflow; k++) {
+        const int dy = clampi(g.dy0 - halo + k, 0, a.OH - 1);
+        const int r0 = a.yt[dy].x;
+        const int r1 = LINEAR ? min(r0 + 1, a.H - 1) : r0;
+        int s0, s1;
+        if (n > 0 && rows[n - 1] == r0)
+            s0 = n - 1;
+        else if (n > 1 && rows[n - 2] == r0)
+            s0 = n - 2;
+        else if (n == a.max_rows) {
+            overflow = true;
+            break;
+        } else {
+            rows[n] = r0;
+            s0 = n++;
+        }
+        if (rows[n - 1] == r1)
+            s1 = n - 1;
+        else if (n == a.max_rows) {
+            overflow = true;
+            break;
+        } else {
+            rows[n] = r1;
+            s1 = n++;
+        }
+        map[2 * k] = s0;
+        map[2 * k + 1] = s1;
+    }
+    if (overflow) {
+        // the host sizes max_rows and slot_bytes from the same tables, so this
+        // is unreachable; it guards shared memory all the same
+        atomicExch(a.status, RZ_ERR_ARG);
+        n = -1;
+    }
+    h->nrows = n;
+    h->b_lo = b_lo;
+    h->nbytes = nbytes;
+    h->pad = tile;
+    if (a.tma_in) {
+        // the barrier completes its phase even for a rejected tile
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n > 0 ? n * nbytes : 0));
+        for (int s = 0; s < n; s++)
+            bulk_load(slots + s * a.slot_bytes, g.src + (long long)rows[s] * a.src_pitch + b_lo,
+                      static_cast<uint32_t>(nbytes), bar);
+    }
 }
 
-// Write the output tile from shared memory: `nrow` rows of `row_bytes` bytes,
-// row i from obuf + i*obuf_pitch to gdst + i*gpitch.  Bulk copies when
-// allowed (16-byte aligned start and pitch); the ragged tail of each row,
-// under 16 bytes, and the whole row otherwise, by plain stores.
-__device__ __forceinline__ void store_rows(const KArgs &a, uint8_t *gdst, long long gpitch, const uint8_t *obuf,
-                                           int obuf_pitch, int nrow, int row_bytes)
+// All threads: copy a prepared stage's rows with plain loads (unaligned sources).
+__device__ void load_stage_plain(const KArgs &a, const SmemLayout &L, uint8_t *st, int tile)
 {
-    const int bulk = a.tma_out ? (row_bytes & ~15) : 0;
+    const StageHdr *h = reinterpret_cast<const StageHdr *>(st);
+    const int *rows = reinterpret_cast<const int *>(st + L.rows_off);
+    uint8_t *slots = st + L.slots_off;
+    const TileGeom g = tile_geom(a, tile);
+    for (int s = 0; s < h->nrows; s++) {
+        const uint8_t *src = g.src + (long long)rows[s] * a.src_pitch + h->b_lo;
+        uint8_t *d = slots + s * a.slot_bytes;
+        for (int k = threadIdx.x; k < h->nbytes; k += kThreads)
+            d[k] = __ldg(src + k);
+    }
+}
+
+// Thread 0: one bulk store per output row of the tile (the 16-byte multiple
+// of each row; the ragged tail goes through store_tail).
+__device__ void issue_stores(const KArgs &a, const SmemLayout &L, const uint8_t *ob, const TileGeom &g, int planes,
+                             int px_bytes)
+{
+    const int nr = g.dy1 - g.dy0;
+    const int row_bytes = (g.dx1 - g.dx0) * px_bytes;
+    const int bulk = row_bytes & ~15;
     if (bulk > 0) {
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            for (int i = 0; i < nrow; i++)
-                bulk_store(gdst + i * gpitch, obuf + i * obuf_pitch, static_cast<uint32_t>(bulk));
-            bulk_commit();
-        }
-    } else {
-        __syncthreads();
+        uint8_t *base = g.dst + (long long)g.dy0 * a.dst_pitch + (long long)g.dx0 * px_bytes;
+        for (int c = 0; c < planes; c++)
+            for (int i = 0; i < nr; i++)
+                bulk_store(base + c * a.dst_plane + i * a.dst_pitch, ob + (c * a.TR + i) * L.out_row_bytes,
+                           static_cast<uint32_t>(bulk));
     }
-    const int tail = row_bytes - bulk;
-    if (tail > 0) {
-        for (int i = 0; i < nrow; i++)
-            for (int k = threadIdx.x; k < tail; k += kThreads)
-                gdst[i * gpitch + bulk + k] = obuf[i * obuf_pitch + bulk + k];
-    }
-    if (bulk > 0 && threadIdx.x == 0)
-        bulk_wait_read_all();
+    bulk_commit();
 }
 
-// ------------------------------------------------------------------ plain resize
-
-template <typename T, int C, int LINEAR>
-__global__ void __launch_bounds__(kThreads) k_resize(const KArgs a)
+// All threads: write the bytes of each output row that the bulk stores do
+// not cover (all of them when bulk stores are not allowed).
+__device__ void store_tail(const KArgs &a, const SmemLayout &L, const uint8_t *ob, const TileGeom &g, int planes,
+                           int px_bytes)
 {
-    extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int ES = sizeof(T);
-    constexpr int FAM = (ES == 1) ? FAM_U8 : FAM_F32;
-    const Tile t = decode_tile(a);
-    const SmemLayout L = smem_layout(FAM, C, a.TR, a.TW, a.max_rows, a.slot_bytes);
-    if (!stage_rows<LINEAR>(a, t, 0, ES, smem, L))
+    const int nr = g.dy1 - g.dy0;
+    const int row_bytes = (g.dx1 - g.dx0) * px_bytes;
+    const int bulk = a.tma_out ? (row_bytes & ~15) : 0;
+    const int tail = row_bytes - bulk;
+    if (tail <= 0)
         return;
+    uint8_t *base = g.dst + (long long)g.dy0 * a.dst_pitch + (long long)g.dx0 * px_bytes + bulk;
+    const int n = planes * nr * tail;
+    for (int k = threadIdx.x; k < n; k += kThreads) {
+        const int row = k / tail, j = k - row * tail;
+        const int c = row / nr, i = row - c * nr;
+        base[c * a.dst_plane + i * a.dst_pitch + j] = ob[(c * a.TR + i) * L.out_row_bytes + bulk + j];
+    }
+}
 
-    const int *hdr = reinterpret_cast<const int *>(smem + 8);
-    const int *map = reinterpret_cast<const int *>(smem + L.off_map);
-    const T *slots = reinterpret_cast<const T *>(smem + L.off_slots);
-    T *obuf = reinterpret_cast<T *>(smem + L.off_out);
-    const int lo = hdr[1] / ES;              // element index of slot element 0
-    const int slot_el = a.slot_bytes / ES;
-    const int orow_el = L.out_row_bytes / ES;
+// ------------------------------------------------------------------ compute: one tile
 
-    const int nr = t.dy1 - t.dy0, nc = t.dx1 - t.dx0;
+struct StageView {
+    const uint8_t *slots;
+    const int *map;
+    int b_lo, slot_bytes;
+};
+
+__device__ __forceinline__ StageView stage_view(const KArgs &a, const SmemLayout &L, const uint8_t *st)
+{
+    StageView v;
+    v.slots = st + L.slots_off;
+    v.map = reinterpret_cast<const int *>(st + L.map_off);
+    v.b_lo = reinterpret_cast<const StageHdr *>(st)->b_lo;
+    v.slot_bytes = a.slot_bytes;
+    return v;
+}
+
+// Generic bilinear / nearest, any ratio.  Pixel-per-thread gather from the
+// staged rows; uint8 bilinear is
+//   out = (B0 (A0 t0 + A1 t1) + B1 (A0 b0 + A1 b1) + 2^21) >> 22
+// with A1 = 11-bit weight of the right tap, B1 of the lower row — exact in
+// int32 (at most 2048 * 2048 * 255 + 2^21 < 2^31).
+template <typename T, int C, int LINEAR>
+__device__ void compute_generic(const KArgs &a, const StageView &sv, const TileGeom &g, uint8_t *ob_bytes,
+                                int orow_bytes)
+{
+    constexpr int ES = sizeof(T);
+    const T *slots = reinterpret_cast<const T *>(sv.slots);
+    T *ob = reinterpret_cast<T *>(ob_bytes);
+    const int lo = sv.b_lo / ES;
+    const int slot_el = sv.slot_bytes / ES;
+    const int orow_el = orow_bytes / ES;
+    const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
     const int lg = min(8, ceil_log2(nc));
     const int tpr = 1 << lg, rpp = kThreads >> lg;
     for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
-        const int dy = t.dy0 + rl;
-        const int2 yw = a.yt[dy];
-        const T *top = slots + map[2 * rl] * slot_el - lo;
-        const T *bot = slots + map[2 * rl + 1] * slot_el - lo;
-        T *orow = obuf + rl * orow_el;
+        const int2 yw = __ldg(&a.yt[g.dy0 + rl]);
+        const T *top = slots + sv.map[2 * rl] * slot_el - lo;
+        const T *bot = slots + sv.map[2 * rl + 1] * slot_el - lo;
+        T *orow = ob + rl * orow_el;
         for (int cl = threadIdx.x & (tpr - 1); cl < nc; cl += tpr) {
-            const int2 xw = __ldg(&a.xt[t.dx0 + cl]);
+            const int2 xw = __ldg(&a.xt[g.dx0 + cl]);
             const int o0 = xw.x * C;
             if (!LINEAR) {
 #pragma unroll
@@ -342,39 +361,137 @@ __global__ void __launch_bounds__(kThreads) k_resize(const KArgs a)
             }
         }
     }
-    uint8_t *gdst = t.dst + (long long)t.dy0 * a.dst_pitch + (long long)t.dx0 * C * ES;
-    store_rows(a, gdst, a.dst_pitch, reinterpret_cast<const uint8_t *>(obuf), L.out_row_bytes, nr, nc * C * ES);
 }
 
-// ------------------------------------------------------------------ bilinear + normalise (u8 HWC -> f32 NCHW)
+// Exact 2x downscale of uint8 (W = 2 OW, H = 2 OH).  Every column and row then
+// samples x = 2d + 1/2, so A0 = A1 = B0 = B1 = 1024 and the generic sum
+// reduces to out = (t0 + t1 + b0 + b1 + 2) >> 2: the same value, bit for bit.
+// The four taps are summed with dp4a; weights of 64 and a start of 128 put
+// 64 (sum + 2) in the accumulator, whose byte 1 is the rounded result, so a
+// byte permute packs it.  The tile's staged span starts at the tile's first
+// source byte, 16-byte aligned (the host keeps TW a multiple of 8 columns).
+__device__ __forceinline__ uint32_t pick_byte1(uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    return __byte_perm(__byte_perm(a, b, 0x0051), __byte_perm(c, d, 0x0051), 0x5410);
+}
 
 template <int C>
-__global__ void __launch_bounds__(kThreads) k_resize_normalize(const KArgs a)
+__device__ void compute_down2(const KArgs &a, const StageView &sv, const TileGeom &g, uint8_t *ob, int orow_bytes)
 {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const Tile t = decode_tile(a);
-    const SmemLayout L = smem_layout(FAM_NORM, C, a.TR, a.TW, a.max_rows, a.slot_bytes);
-    if (!stage_rows<1>(a, t, 0, 1, smem, L))
-        return;
+    const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
+    const int ofs0 = 2 * g.dx0 * C - sv.b_lo;    // 0 or a multiple of 16
+    // pixels per thread: 8 (C=1), 4 (C=3), 2 (C=4) -> 8, 12, 8 output bytes
+    constexpr int PX = (C == 1) ? 8 : (C == 3 ? 4 : 2);
+    const int ngrp = nc / PX;
+    const int lg = min(8, ceil_log2(ngrp + 1));
+    const int tpr = 1 << lg, rpp = kThreads >> lg;
+    for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
+        const uint8_t *top = sv.slots + sv.map[2 * rl] * sv.slot_bytes + ofs0;
+        const uint8_t *bot = sv.slots + sv.map[2 * rl + 1] * sv.slot_bytes + ofs0;
+        uint8_t *orow = ob + rl * orow_bytes;
+        for (int j = threadIdx.x & (tpr - 1); j < ngrp; j += tpr) {
+            if constexpr (C == 1) {
+                const uint4 t = *reinterpret_cast<const uint4 *>(top + 16 * j);
+                const uint4 b = *reinterpret_cast<const uint4 *>(bot + 16 * j);
+                const uint32_t tw[4] = {t.x, t.y, t.z, t.w}, bw[4] = {b.x, b.y, b.z, b.w};
+                uint32_t s[8];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    s[2 * k] = __dp4a(tw[k], 0x00004040u, __dp4a(bw[k], 0x00004040u, 128u));
+                    s[2 * k + 1] = __dp4a(tw[k], 0x40400000u, __dp4a(bw[k], 0x40400000u, 128u));
+                }
+                uint2 o;
+                o.x = pick_byte1(s[0], s[1], s[2], s[3]);
+                o.y = pick_byte1(s[4], s[5], s[6], s[7]);
+                *reinterpret_cast<uint2 *>(orow + 8 * j) = o;
+            } else if constexpr (C == 3) {
+                // 24 source bytes per row = words w0..w5; output pixel q covers
+                // source bytes [6q, 6q + 6): channel c sums bytes 6q+c and 6q+3+c
+                const uint2 *tp = reinterpret_cast<const uint2 *>(top + 24 * j);
+                const uint2 *bp = reinterpret_cast<const uint2 *>(bot + 24 * j);
+                const uint2 t0 = tp[0], t1 = tp[1], t2 = tp[2];
+                const uint2 b0 = bp[0], b1 = bp[1], b2 = bp[2];
+                const uint32_t tw[6] = {t0.x, t0.y, t1.x, t1.y, t2.x, t2.y};
+                const uint32_t bw[6] = {b0.x, b0.y, b1.x, b1.y, b2.x, b2.y};
+                uint32_t s[12];
+#pragma unroll
+                for (int q = 0; q < 4; q += 2) {
+                    // even pixel: bytes 0..5 of words (k, k+1) with k = 3q/2
+                    const int k = 3 * q / 2;
+                    s[3 * q + 0] = __dp4a(tw[k], 0x40000040u, __dp4a(bw[k], 0x40000040u, 128u));
+                    s[3 * q + 1] = __dp4a(tw[k], 0x00004000u,
+                                          __dp4a(tw[k + 1], 0x00000040u,
+                                                 __dp4a(bw[k], 0x00004000u, __dp4a(bw[k + 1], 0x00000040u, 128u))));
+                    s[3 * q + 2] = __dp4a(tw[k], 0x00400000u,
+                                          __dp4a(tw[k + 1], 0x00004000u,
+                                                 __dp4a(bw[k], 0x00400000u, __dp4a(bw[k + 1], 0x00004000u, 128u))));
+                    // odd pixel: bytes 2..7 of words (k+1, k+2)
+                    s[3 * q + 3] = __dp4a(tw[k + 1], 0x00400000u,
+                                          __dp4a(tw[k + 2], 0x00004000u,
+                                                 __dp4a(bw[k + 1], 0x00400000u, __dp4a(bw[k + 2], 0x00004000u, 128u))));
+                    s[3 * q + 4] = __dp4a(tw[k + 1], 0x40000000u,
+                                          __dp4a(tw[k + 2], 0x00400000u,
+                                                 __dp4a(bw[k + 1], 0x40000000u, __dp4a(bw[k + 2], 0x00400000u, 128u))));
+                    s[3 * q + 5] = __dp4a(tw[k + 2], 0x40000040u, __dp4a(bw[k + 2], 0x40000040u, 128u));
+                }
+                uint32_t *o = reinterpret_cast<uint32_t *>(orow + 12 * j);
+                o[0] = pick_byte1(s[0], s[1], s[2], s[3]);
+                o[1] = pick_byte1(s[4], s[5], s[6], s[7]);
+                o[2] = pick_byte1(s[8], s[9], s[10], s[11]);
+            } else {
+                // C == 4: per output pixel four words; sum byte lanes in two
+                // 16-bit-lane halves (each sum <= 1022 fits)
+                const uint4 t = *reinterpret_cast<const uint4 *>(top + 16 * j);
+                const uint4 b = *reinterpret_cast<const uint4 *>(bot + 16 * j);
+                const uint32_t w[2][4] = {{t.x, t.y, b.x, b.y}, {t.z, t.w, b.z, b.w}};
+                uint2 o;
+                uint32_t r[2];
+#pragma unroll
+                for (int p = 0; p < 2; p++) {
+                    const uint32_t l = __byte_perm(w[p][0], 0, 0x4240) + __byte_perm(w[p][1], 0, 0x4240) +
+                                       __byte_perm(w[p][2], 0, 0x4240) + __byte_perm(w[p][3], 0, 0x4240) +
+                                       0x00020002u;
+                    const uint32_t h = __byte_perm(w[p][0], 0, 0x4341) + __byte_perm(w[p][1], 0, 0x4341) +
+                                       __byte_perm(w[p][2], 0, 0x4341) + __byte_perm(w[p][3], 0, 0x4341) +
+                                       0x00020002u;
+                    r[p] = ((l >> 2) & 0x00ff00ffu) | ((h << 6) & 0xff00ff00u);
+                }
+                o.x = r[0];
+                o.y = r[1];
+                *reinterpret_cast<uint2 *>(orow + 8 * j) = o;
+            }
+        }
+        // columns left over after whole groups
+        for (int p = ngrp * PX + (threadIdx.x & (tpr - 1)); p < nc; p += tpr) {
+#pragma unroll
+            for (int c = 0; c < C; c++) {
+                const int o = 2 * p * C + c;
+                const int s = top[o] + top[o + C] + bot[o] + bot[o + C] + 2;
+                orow[p * C + c] = static_cast<uint8_t>(s >> 2);
+            }
+        }
+    }
+}
 
-    const int *hdr = reinterpret_cast<const int *>(smem + 8);
-    const int *map = reinterpret_cast<const int *>(smem + L.off_map);
-    const uint8_t *slots = smem + L.off_slots;
-    float *obuf = reinterpret_cast<float *>(smem + L.off_out);
-    const int lo = hdr[1];
-    const int orow_el = L.out_row_bytes / 4;
+// Bilinear + normalise: the uint8 result q of the generic sum, then
+// y = q * scale[c] + shift[c] written planar.
+template <int C>
+__device__ void compute_normalize(const KArgs &a, const StageView &sv, const TileGeom &g, uint8_t *ob_bytes,
+                                  int orow_bytes)
+{
+    float *ob = reinterpret_cast<float *>(ob_bytes);
+    const int orow_el = orow_bytes / 4;
     const int plane_el = a.TR * orow_el;
-
-    const int nr = t.dy1 - t.dy0, nc = t.dx1 - t.dx0;
+    const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
     const int lg = min(8, ceil_log2(nc));
     const int tpr = 1 << lg, rpp = kThreads >> lg;
     for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
-        const int2 yw = a.yt[t.dy0 + rl];
+        const int2 yw = __ldg(&a.yt[g.dy0 + rl]);
         const int B1 = yw.y, B0 = 2048 - B1;
-        const uint8_t *top = slots + map[2 * rl] * a.slot_bytes - lo;
-        const uint8_t *bot = slots + map[2 * rl + 1] * a.slot_bytes - lo;
+        const uint8_t *top = sv.slots + sv.map[2 * rl] * sv.slot_bytes - sv.b_lo;
+        const uint8_t *bot = sv.slots + sv.map[2 * rl + 1] * sv.slot_bytes - sv.b_lo;
         for (int cl = threadIdx.x & (tpr - 1); cl < nc; cl += tpr) {
-            const int2 xw = __ldg(&a.xt[t.dx0 + cl]);
+            const int2 xw = __ldg(&a.xt[g.dx0 + cl]);
             const int o0 = xw.x * C, o1 = min(xw.x + 1, a.W - 1) * C;
             const int A1 = xw.y, A0 = 2048 - A1;
 #pragma unroll
@@ -382,73 +499,37 @@ __global__ void __launch_bounds__(kThreads) k_resize_normalize(const KArgs a)
                 const int hT = A0 * top[o0 + c] + A1 * top[o1 + c];
                 const int hB = A0 * bot[o0 + c] + A1 * bot[o1 + c];
                 const int q = (B0 * hT + B1 * hB + (1 << 21)) >> 22;
-                obuf[c * plane_el + rl * orow_el + cl] = fmaf(static_cast<float>(q), a.scale[c], a.shift[c]);
+                ob[c * plane_el + rl * orow_el + cl] = fmaf(static_cast<float>(q), a.scale[c], a.shift[c]);
             }
         }
     }
-    // one bulk store per (plane, row): plane c of image b at dst + c*dst_plane
-    const int row_bytes = nc * 4;
-    const int bulk = a.tma_out ? (row_bytes & ~15) : 0;
-    uint8_t *gbase = t.dst + (long long)t.dy0 * a.dst_pitch + (long long)t.dx0 * 4;
-    const uint8_t *ob = reinterpret_cast<const uint8_t *>(obuf);
-    if (bulk > 0) {
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            for (int c = 0; c < C; c++)
-                for (int i = 0; i < nr; i++)
-                    bulk_store(gbase + c * a.dst_plane + i * a.dst_pitch,
-                               ob + (c * plane_el + i * orow_el) * 4, static_cast<uint32_t>(bulk));
-            bulk_commit();
-        }
-    } else {
-        __syncthreads();
-    }
-    const int tail = row_bytes - bulk;
-    if (tail > 0)
-        for (int c = 0; c < C; c++)
-            for (int i = 0; i < nr; i++)
-                for (int k = threadIdx.x; k < tail; k += kThreads)
-                    gbase[c * a.dst_plane + i * a.dst_pitch + bulk + k] = ob[(c * plane_el + i * orow_el) * 4 + bulk + k];
-    if (bulk > 0 && threadIdx.x == 0)
-        bulk_wait_read_all();
 }
 
-// ------------------------------------------------------------------ bilinear + 3x3 filter (f32)
-
+// Bilinear + 3x3: resized float values of the tile and a one-pixel ring
+// (rows and columns clamped into the output grid: replicate border) go to
+// `mid`; then z = sum w[i*3+j] * mid[row+i][col+j].
 template <int C>
-__global__ void __launch_bounds__(kThreads) k_resize_filter3x3(const KArgs a)
+__device__ void compute_filter3x3(const KArgs &a, const StageView &sv, const TileGeom &g, uint8_t *ob_bytes,
+                                  int orow_bytes, float *mid)
 {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const Tile t = decode_tile(a);
-    const SmemLayout L = smem_layout(FAM_FILT, C, a.TR, a.TW, a.max_rows, a.slot_bytes);
-    if (!stage_rows<1>(a, t, 1, 4, smem, L))
-        return;
-
-    const int *hdr = reinterpret_cast<const int *>(smem + 8);
-    const int *map = reinterpret_cast<const int *>(smem + L.off_map);
-    const float *slots = reinterpret_cast<const float *>(smem + L.off_slots);
-    float *mid = reinterpret_cast<float *>(smem + L.off_mid);
-    float *obuf = reinterpret_cast<float *>(smem + L.off_out);
-    const int lo = hdr[1] / 4;
-    const int slot_el = a.slot_bytes / 4;
-    const int orow_el = L.out_row_bytes / 4;
-    const int mid_w = a.TW + 2;  // row pitch of mid, in pixels
-
-    const int nr = t.dy1 - t.dy0, nc = t.dx1 - t.dx0;
-    // 1. resized values on the tile plus a one-pixel ring, rows and columns
-    //    clamped into the output grid (replicate border)
+    const float *slots = reinterpret_cast<const float *>(sv.slots);
+    float *ob = reinterpret_cast<float *>(ob_bytes);
+    const int lo = sv.b_lo / 4;
+    const int slot_el = sv.slot_bytes / 4;
+    const int orow_el = orow_bytes / 4;
+    const int mid_w = a.TW + 2;
+    const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
     {
         const int hr = nr + 2, hc = nc + 2;
         const int lg = min(8, ceil_log2(hc));
         const int tpr = 1 << lg, rpp = kThreads >> lg;
         for (int k = threadIdx.x >> lg; k < hr; k += rpp) {
-            const int dy = clampi(t.dy0 - 1 + k, 0, a.OH - 1);
-            const float v = __int_as_float(a.yt[dy].y);
-            const float *top = slots + map[2 * k] * slot_el - lo;
-            const float *bot = slots + map[2 * k + 1] * slot_el - lo;
+            const int dy = clampi(g.dy0 - 1 + k, 0, a.OH - 1);
+            const float v = __int_as_float(__ldg(&a.yt[dy]).y);
+            const float *top = slots + sv.map[2 * k] * slot_el - lo;
+            const float *bot = slots + sv.map[2 * k + 1] * slot_el - lo;
             for (int j = threadIdx.x & (tpr - 1); j < hc; j += tpr) {
-                const int dx = clampi(t.dx0 - 1 + j, 0, a.OW - 1);
+                const int dx = clampi(g.dx0 - 1 + j, 0, a.OW - 1);
                 const int2 xw = __ldg(&a.xt[dx]);
                 const float u = __int_as_float(xw.y);
                 const int o0 = xw.x * C, o1 = min(xw.x + 1, a.W - 1) * C;
@@ -464,7 +545,6 @@ __global__ void __launch_bounds__(kThreads) k_resize_filter3x3(const KArgs a)
         }
     }
     __syncthreads();
-    // 2. 3x3 correlation over the ring-extended tile
     {
         const int lg = min(8, ceil_log2(nc));
         const int tpr = 1 << lg, rpp = kThreads >> lg;
@@ -478,81 +558,148 @@ __global__ void __launch_bounds__(kThreads) k_resize_filter3x3(const KArgs a)
 #pragma unroll
                         for (int j = 0; j < 3; j++)
                             z = fmaf(a.w[i * 3 + j], mid[((rl + i) * mid_w + (cl + j)) * C + c], z);
-                    obuf[rl * orow_el + cl * C + c] = z;
+                    ob[rl * orow_el + cl * C + c] = z;
                 }
             }
         }
     }
-    uint8_t *gdst = t.dst + (long long)t.dy0 * a.dst_pitch + (long long)t.dx0 * C * 4;
-    store_rows(a, gdst, a.dst_pitch, reinterpret_cast<const uint8_t *>(obuf), L.out_row_bytes, nr, nc * C * 4);
 }
 
-// ------------------------------------------------------------------ dispatch
+// ------------------------------------------------------------------ the persistent kernel
 
-using KernelFn = void (*)(const KArgs);
-
-KernelFn pick(int fam, int mode, int C)
+// OP: 0 plain resize (T, C, LINEAR, VAR), 1 normalise, 2 3x3 filter.
+template <int OP, typename T, int C, int LINEAR, int VAR>
+__global__ void __launch_bounds__(kThreads) k_resize(const KArgs a)
 {
-    const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
-    if (ci < 0)
-        return nullptr;
-    static const KernelFn u8[2][3] = {
-        {k_resize<uint8_t, 1, 0>, k_resize<uint8_t, 3, 0>, k_resize<uint8_t, 4, 0>},
-        {k_resize<uint8_t, 1, 1>, k_resize<uint8_t, 3, 1>, k_resize<uint8_t, 4, 1>}};
-    static const KernelFn f32[2][3] = {
-        {k_resize<float, 1, 0>, k_resize<float, 3, 0>, k_resize<float, 4, 0>},
-        {k_resize<float, 1, 1>, k_resize<float, 3, 1>, k_resize<float, 4, 1>}};
-    static const KernelFn norm[3] = {k_resize_normalize<1>, k_resize_normalize<3>, k_resize_normalize<4>};
-    static const KernelFn filt[3] = {k_resize_filter3x3<1>, k_resize_filter3x3<3>, k_resize_filter3x3<4>};
-    const int m = mode == RZ_LINEAR ? 1 : 0;
-    switch (fam) {
-    case FAM_U8: return u8[m][ci];
-    case FAM_F32: return f32[m][ci];
-    case FAM_NORM: return m ? norm[ci] : nullptr;
-    case FAM_FILT: return m ? filt[ci] : nullptr;
-    default: return nullptr;
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int FAM = OP == 1 ? FAM_NORM : (OP == 2 ? FAM_FILT : (sizeof(T) == 1 ? FAM_U8 : FAM_F32));
+    constexpr int HALO = OP == 2 ? 1 : 0;
+    constexpr int IN_ES = fam_in_es(FAM);
+    constexpr int PLANES = OP == 1 ? C : 1;
+    constexpr int PX_BYTES = OP == 1 ? 4 : C * fam_out_es(FAM);
+    const SmemLayout L = smem_layout(FAM, C, a.TR, a.TW, a.max_rows, a.slot_bytes, a.stages);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    const int ntiles = a.batch * a.tiles_x * a.tiles_y;
+    const int NS = a.stages;
+    const int G = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        if (a.tma_in) {
+            for (int s = 0; s < NS; s++)
+                mbar_init(&bars[s], 1);
+            fence_mbar_init();
+        }
+        for (int s = 0; s < NS; s++) {
+            const int t = blockIdx.x + s * G;
+            if (t < ntiles)
+                prepare_stage<LINEAR>(a, L, smem + L.stage_off + s * L.stage_bytes, &bars[s], t, HALO, IN_ES);
+        }
+    }
+    __syncthreads();
+
+    int it = 0;
+    bool failed = false;
+    for (int t = blockIdx.x; t < ntiles; t += G, ++it) {
+        const int s = it % NS;
+        uint8_t *st = smem + L.stage_off + s * L.stage_bytes;
+        uint8_t *ob = smem + L.out_off + (it & 1) * L.out_bytes;
+        // the output buffer is free once the store issued two tiles ago has read it
+        if (threadIdx.x == 0 && it >= 2)
+            bulk_wait_read<1>();
+        if (a.tma_in) {
+            const bool ok = mbar_wait_bounded(&bars[s], (it / NS) & 1, a.status);
+            if (__syncthreads_or(!ok)) {
+                failed = true;
+                break;
+            }
+        } else {
+            __syncthreads();    // the stage header written by thread 0 is visible
+            load_stage_plain(a, L, st, t);
+            __syncthreads();
+        }
+        if (reinterpret_cast<const StageHdr *>(st)->nrows < 0) {
+            failed = true;
+            break;
+        }
+        const TileGeom g = tile_geom(a, t);
+        const StageView sv = stage_view(a, L, st);
+        if constexpr (OP == 0) {
+            if constexpr (VAR == VAR_DOWN2)
+                compute_down2<C>(a, sv, g, ob, L.out_row_bytes);
+            else
+                compute_generic<T, C, LINEAR>(a, sv, g, ob, L.out_row_bytes);
+        } else if constexpr (OP == 1) {
+            compute_normalize<C>(a, sv, g, ob, L.out_row_bytes);
+        } else {
+            compute_filter3x3<C>(a, sv, g, ob, L.out_row_bytes, reinterpret_cast<float *>(smem + L.mid_off));
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            if (a.tma_out)
+                issue_stores(a, L, ob, g, PLANES, PX_BYTES);
+            const int tn = t + NS * G;
+            if (tn < ntiles)
+                prepare_stage<LINEAR>(a, L, st, &bars[s], tn, HALO, IN_ES);
+        }
+        store_tail(a, L, ob, g, PLANES, PX_BYTES);
+    }
+    if (threadIdx.x == 0) {
+        bulk_wait_read<0>();
+        if (failed && a.tma_in) {
+            // let bulk loads still in flight land before the CTA leaves
+            for (int k = 0; k < NS; k++) {
+                const int j = it + k;
+                if (blockIdx.x + j * G < ntiles)
+                    mbar_wait_bounded(&bars[j % NS], (j / NS) & 1, nullptr);
+            }
+        }
     }
 }
 
 }  // namespace
 
-int launch_resize(int fam, int mode, const KArgs &a, int batch, size_t smem, void *stream)
+const void *kernel_for(int fam, int mode, int variant, int C)
 {
-    KernelFn fn = pick(fam, mode, a.C);
-    if (!fn)
-        return static_cast<int>(cudaErrorInvalidValue);
-    // opt every kernel in to the full shared-memory carve-out once per process
-    // (per device the attribute is applied lazily by the runtime)
-    static std::mutex mu;
-    static int done_dev[64][FAM_COUNT * 2 * 3] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return static_cast<int>(e);
-    const int ci = (a.C == 1) ? 0 : (a.C == 3 ? 1 : 2);
-    const int slot = (fam * 2 + (mode == RZ_LINEAR ? 1 : 0)) * 3 + ci;
-    if (dev >= 0 && dev < 64) {
-        std::lock_guard<std::mutex> lk(mu);
-        if (!done_dev[dev][slot]) {
-            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kMaxSmem);
-            if (e != cudaSuccess)
-                return static_cast<int>(e);
-            done_dev[dev][slot] = 1;
-        }
+    const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
+    if (ci < 0)
+        return nullptr;
+    using Fn = void (*)(const KArgs);
+    static const Fn u8[2][3] = {
+        {k_resize<0, uint8_t, 1, 0, 0>, k_resize<0, uint8_t, 3, 0, 0>, k_resize<0, uint8_t, 4, 0, 0>},
+        {k_resize<0, uint8_t, 1, 1, 0>, k_resize<0, uint8_t, 3, 1, 0>, k_resize<0, uint8_t, 4, 1, 0>}};
+    static const Fn u8_down2[3] = {k_resize<0, uint8_t, 1, 1, VAR_DOWN2>, k_resize<0, uint8_t, 3, 1, VAR_DOWN2>,
+                                   k_resize<0, uint8_t, 4, 1, VAR_DOWN2>};
+    static const Fn f32[2][3] = {
+        {k_resize<0, float, 1, 0, 0>, k_resize<0, float, 3, 0, 0>, k_resize<0, float, 4, 0, 0>},
+        {k_resize<0, float, 1, 1, 0>, k_resize<0, float, 3, 1, 0>, k_resize<0, float, 4, 1, 0>}};
+    static const Fn norm[3] = {k_resize<1, uint8_t, 1, 1, 0>, k_resize<1, uint8_t, 3, 1, 0>,
+                               k_resize<1, uint8_t, 4, 1, 0>};
+    static const Fn filt[3] = {k_resize<2, float, 1, 1, 0>, k_resize<2, float, 3, 1, 0>, k_resize<2, float, 4, 1, 0>};
+    const int m = mode == RZ_LINEAR ? 1 : 0;
+    switch (fam) {
+    case FAM_U8:
+        if (variant == VAR_DOWN2)
+            return m ? reinterpret_cast<const void *>(u8_down2[ci]) : nullptr;
+        return reinterpret_cast<const void *>(u8[m][ci]);
+    case FAM_F32: return reinterpret_cast<const void *>(f32[m][ci]);
+    case FAM_NORM: return m ? reinterpret_cast<const void *>(norm[ci]) : nullptr;
+    case FAM_FILT: return m ? reinterpret_cast<const void *>(filt[ci]) : nullptr;
+    default: return nullptr;
     }
-    const long long nblk = (long long)batch * a.tiles_x * a.tiles_y;
-    if (nblk <= 0)
+}
+
+int launch_resize(const void *fn, const KArgs &a, int grid, size_t smem, void *stream)
+{
+    if (grid <= 0)
         return 0;
-    if (nblk > 0x7fffffffLL)
-        return static_cast<int>(cudaErrorInvalidConfiguration);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(nblk), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
-    e = cudaLaunchKernelEx(&cfg, fn, a);
-    return static_cast<int>(e);
+    return static_cast<int>(
+        cudaLaunchKernelEx(&cfg, reinterpret_cast<void (*)(const KArgs)>(const_cast<void *>(fn)), a));
 }
 
 }  // namespace rz

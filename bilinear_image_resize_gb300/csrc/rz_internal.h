@@ -11,49 +11,61 @@ namespace rz {
 
 constexpr int kThreads = 256;           // threads per CTA, every kernel
 constexpr int kMaxSmem = 227 * 1024;    // opt-in dynamic shared memory per CTA on sm_103a
+constexpr int kMaxStages = 4;           // staged-tile ring depth limit
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded mbarrier waits: 1 s
 
 // Kernel families.  The numbering matches resize_plan_set_tile's `kind`.
 enum Family { FAM_U8 = 0, FAM_F32 = 1, FAM_NORM = 3, FAM_FILT = 4, FAM_COUNT = 5 };
 
-__host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
+// Compute variants of the uint8 bilinear family.
+enum Variant { VAR_GENERIC = 0, VAR_DOWN2 = 1 };
 
-__host__ __device__ inline int fam_in_es(int fam) { return (fam == FAM_U8 || fam == FAM_NORM) ? 1 : 4; }
-__host__ __device__ inline int fam_out_es(int fam) { return fam == FAM_U8 ? 1 : 4; }
-__host__ __device__ inline int fam_halo(int fam) { return fam == FAM_FILT ? 1 : 0; }
+__host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ constexpr int fam_in_es(int fam) { return (fam == FAM_U8 || fam == FAM_NORM) ? 1 : 4; }
+__host__ __device__ constexpr int fam_out_es(int fam) { return fam == FAM_U8 ? 1 : 4; }
+__host__ __device__ constexpr int fam_halo(int fam) { return fam == FAM_FILT ? 1 : 0; }
 
 // Byte offsets of the pieces of a CTA's dynamic shared memory.  Host and
 // device compute them with this one function.
+//
+//   [0, 64)                       one mbarrier per stage
+//   stages x stage_bytes          per stage: header {nrows, b_lo, nbytes, tile},
+//                                 int rows[max_rows], int map[2 * computed rows],
+//                                 then max_rows staged row segments of slot_bytes
+//   mid                           float[(TR+2) * (TW+2) * C] resized values with
+//                                 their one-pixel ring (3x3 epilogue only)
+//   2 x out_bytes                 double-buffered output tile
 struct SmemLayout {
-    int off_rows;   // int[max_rows]: staged source row indices
-    int off_map;    // int[2 * computed rows]: slot of the top / bottom tap row
-    int off_slots;  // max_rows staged row segments of slot_bytes each
-    int off_mid;    // float[(TR+2) * (TW+2) * C]: resized values incl. halo (3x3 only)
-    int off_out;    // output tile, rows of out_row_bytes (planes for NCHW)
-    int out_row_bytes;
+    int stage_off, stage_bytes;
+    int rows_off, map_off, slots_off;   // within a stage
+    int mid_off;
+    int out_off, out_bytes, out_row_bytes;
     int total;
 };
-// header at offset 0: u64 mbarrier, then int nrows, int b_lo, int nbytes
-constexpr int kHdrBytes = 32;
 
-__host__ __device__ inline SmemLayout smem_layout(int fam, int C, int TR, int TW, int max_rows, int slot_bytes)
+__host__ __device__ inline SmemLayout smem_layout(int fam, int C, int TR, int TW, int max_rows, int slot_bytes,
+                                                  int stages)
 {
     SmemLayout L;
     const int halo = fam_halo(fam);
     const int nrc = TR + 2 * halo;
-    L.off_rows = kHdrBytes;
-    L.off_map = align_up(L.off_rows + 4 * max_rows, 16);
-    L.off_slots = align_up(L.off_map + 8 * nrc, 128);
-    L.off_mid = L.off_slots + max_rows * slot_bytes;
-    const int mid = halo ? (TR + 2) * (TW + 2) * C * 4 : 0;
-    L.off_out = align_up(L.off_mid + mid, 128);
+    L.rows_off = 16;
+    L.map_off = align_up(L.rows_off + 4 * max_rows, 16);
+    L.slots_off = align_up(L.map_off + 8 * nrc, 128);
+    L.stage_bytes = align_up(L.slots_off + max_rows * slot_bytes, 128);
+    L.stage_off = 128;
+    L.mid_off = L.stage_off + stages * L.stage_bytes;
+    const int mid = halo ? align_up((TR + 2) * (TW + 2) * C * 4, 128) : 0;
+    L.out_off = L.mid_off + mid;
     if (fam == FAM_NORM) {
         L.out_row_bytes = align_up(TW * 4, 16);
-        L.total = L.off_out + C * TR * L.out_row_bytes;
+        L.out_bytes = align_up(C * TR * L.out_row_bytes, 128);
     } else {
         L.out_row_bytes = align_up(TW * C * fam_out_es(fam), 16);
-        L.total = L.off_out + TR * L.out_row_bytes;
+        L.out_bytes = align_up(TR * L.out_row_bytes, 128);
     }
+    L.total = L.out_off + 2 * L.out_bytes;
     return L;
 }
 
@@ -69,8 +81,10 @@ struct KArgs {
     int H, W, OH, OW, C;
     int TR, TW;             // output rows / columns per tile
     int tiles_x, tiles_y;   // tiles per image
+    int batch;              // images
     int max_rows;           // staged source rows reserved per tile
     int slot_bytes;         // bytes reserved per staged row
+    int stages;             // depth of the staged-tile ring (1..kMaxStages)
     int tma_in, tma_out;    // bulk copies allowed for loads / stores
     const int2 *xt;         // per output column {source column, weight}
     const int2 *yt;         // per output row    {source row, weight}
@@ -79,7 +93,10 @@ struct KArgs {
     float w[9];                // 3x3 epilogue weights, row-major
 };
 
-// Launch one resize kernel (asynchronous).  Returns a cudaError_t value.
-int launch_resize(int fam, int mode, const KArgs &a, int batch, size_t smem, void *stream);
+// Kernel entry for (family, mode, variant, C); nullptr if none.
+const void *kernel_for(int fam, int mode, int variant, int C);
+
+// Launch it on `grid` persistent CTAs (asynchronous).  Returns a cudaError_t value.
+int launch_resize(const void *fn, const KArgs &a, int grid, size_t smem, void *stream);
 
 }  // namespace rz

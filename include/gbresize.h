@@ -216,6 +216,22 @@ RZ_API int resize_last_cuda_error(void);
  */
 RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_cols);
 
+/*
+ * Tuning and testing options of a plan (results never depend on them):
+ *   RZ_OPT_STAGES       value 0 (automatic) or 1..4: source tiles each CTA
+ *                       keeps in flight ahead of the one it computes;
+ *   RZ_OPT_GENERIC_ONLY value 0 or 1: 1 disables the exact-ratio fast path
+ *                       (uint8 2x downscale, used only when every table entry
+ *                       is the 2x pattern, where it is bit-identical);
+ *   RZ_OPT_CTAS_PER_SM  value 0 (as many as fit) or 1..32: caps the resident
+ *                       CTAs per SM of the persistent grid.
+ * Returns RZ_ERR_ARG for an unknown option or value.
+ */
+#define RZ_OPT_STAGES 1
+#define RZ_OPT_GENERIC_ONLY 2
+#define RZ_OPT_CTAS_PER_SM 3
+RZ_API int resize_plan_set_option(rz_plan p, int option, int value);
+
 #ifdef __cplusplus
 }
 #endif

@@ -307,3 +307,61 @@ def test_invalid_calls_raise(rz):
         with pytest.raises(rz.ResizeError):          # overlapping source and destination
             rz.resize_u8(plan, a, b)
         assert rz.resize_plan_status(plan) == rz.RZ_OK
+
+
+# ------------------------------------------------------------------ pipeline depth and the exact 2x path
+
+def run_u8_opts(rz, img, OH, OW, mode, opts, tile=None):
+    H, W, C = img.shape
+    src, _k = device_image(img)
+    out = Canvas(OH, OW, C, torch.uint8)
+    with rz.resize_plan_create(H, W, OH, OW, mode) as plan:
+        for k, v in opts.items():
+            rz.resize_plan_set_option(plan, k, v)
+        if tile:
+            rz.resize_plan_set_tile(plan, rz.KIND_U8, *tile)
+        rz.resize_u8(plan, src, out.view)
+        torch.cuda.synchronize()
+        assert rz.resize_plan_status(plan) == rz.RZ_OK
+    out.check_canary()
+    return out.result()
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3, 4])
+@pytest.mark.parametrize("ctas", [1, 2, 0])
+def test_ring_depth_and_grid_do_not_change_results(rz, stages, ctas):
+    # one or two CTAs per SM make every CTA walk many tiles, so each stage's
+    # barrier goes through many phases
+    img = synth.smooth_rgb(1920, 1080, 2)
+    opts = {rz.RZ_OPT_STAGES: stages, rz.RZ_OPT_CTAS_PER_SM: ctas}
+    for (OH, OW) in [(540, 960), (720, 1280), (2160, 3840)]:
+        got = run_u8_opts(rz, img, OH, OW, rz.RZ_LINEAR, opts)
+        np.testing.assert_array_equal(got, oracle.linear_u8(img, OH, OW))
+    got = run_u8_opts(rz, img, 270, 480, rz.RZ_NEAREST, opts)
+    np.testing.assert_array_equal(got, oracle.nearest_u8(img, 270, 480))
+
+
+@pytest.mark.parametrize("C", [1, 3, 4])
+@pytest.mark.parametrize("geom", [(2160, 3840), (48, 64), (2, 2), (6, 34), (1080, 1922), (30, 18)])
+def test_exact_2x_path_is_bit_identical_to_generic(rz, C, geom):
+    H, W = geom
+    img = synth.random_u8((H, W, C), seed=H + W + C)
+    fast = run_u8_opts(rz, img, H // 2, W // 2, rz.RZ_LINEAR, {})
+    slow = run_u8_opts(rz, img, H // 2, W // 2, rz.RZ_LINEAR, {rz.RZ_OPT_GENERIC_ONLY: 1})
+    np.testing.assert_array_equal(fast, slow)
+    np.testing.assert_array_equal(fast, oracle.linear_u8(img, H // 2, W // 2))
+
+
+@pytest.mark.parametrize("tile", [(1, 8), (1, 16), (2, 24), (3, 64), (1, 960), (4, 1920)])
+def test_exact_2x_path_tiles(rz, tile):
+    img = synth.smooth_rgb(3840, 2160, 3)
+    got = run_u8_opts(rz, img, 1080, 1920, rz.RZ_LINEAR, {rz.RZ_OPT_STAGES: 2}, tile=tile)
+    np.testing.assert_array_equal(got, oracle.linear_u8(img, 1080, 1920))
+
+
+def test_options_reject_bad_values(rz):
+    with rz.resize_plan_create(8, 8, 4, 4, rz.RZ_LINEAR) as plan:
+        for opt, val in [(rz.RZ_OPT_STAGES, 5), (rz.RZ_OPT_STAGES, -1), (rz.RZ_OPT_GENERIC_ONLY, 2),
+                         (rz.RZ_OPT_CTAS_PER_SM, 33), (99, 0)]:
+            with pytest.raises(rz.ResizeError):
+                rz.resize_plan_set_option(plan, opt, val)
