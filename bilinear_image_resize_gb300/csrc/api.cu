@@ -171,7 +171,7 @@ bool eval_tile(const rz_plan_s &p, int fam, int C, int TR, int TW, int stages, T
 constexpr int kSms = 152;                // GB300; the launch itself asks the device
 constexpr int kSoftSmem = 48 * 1024;     // keeps several CTAs resident per SM
 constexpr int kFilterSmem = 96 * 1024;   // the 3x3 tile trades occupancy for less halo
-constexpr int kDefaultStages = 3;
+constexpr int kDefaultStages = 2;
 
 // True when the plan is an exact 2x downscale on both axes: every column and
 // row samples x = 2d + 1/2 (weight 1024 on taps 2d and 2d + 1).
@@ -216,7 +216,7 @@ TileCfg choose_tile(const rz_plan_s &p, int fam, int C, int batch, int stages, b
         if ((w * px_bytes) % 16 != 0) return false;
         return !down2 || (w % 8) == 0;
     };
-    const long long want_tiles = 12LL * kSms;
+    const long long want_tiles = 6LL * kSms;
     int TW = 0;
     for (int w : tws) {
         if (!ok_width(w)) continue;
@@ -279,7 +279,12 @@ int get_tile(rz_plan_s *p, int fam, int C, int batch, TileCfg *out, const void *
     const bool down2 = fam == rz::FAM_U8 && !p->opt_generic && is_down2(*p);
     TileCfg t;
     if (p->over_tr[fam] > 0 && p->over_tw[fam] > 0) {
-        if (!eval_tile(*p, fam, C, p->over_tr[fam], p->over_tw[fam], stages, &t)) return RZ_ERR_ARG;
+        // an explicit ring depth must fit as asked; an automatic one shrinks
+        int st = stages;
+        while (!eval_tile(*p, fam, C, p->over_tr[fam], p->over_tw[fam], st, &t)) {
+            if (p->opt_stages > 0 || st == 1) return RZ_ERR_ARG;
+            st--;
+        }
     } else {
         t = choose_tile(*p, fam, C, batch, stages, down2);
     }

@@ -1,19 +1,21 @@
 // Resize kernels for sm_103a.
 //
 // Persistent CTAs (as many as fit on the GPU at once) walk the output tiles
-// of TR rows x TW columns in a static round-robin.  Each CTA keeps a ring of
-// `stages` staged tiles in shared memory:
-//   1. thread 0 lists the distinct source rows the tile's output rows sample
-//      (two per row for bilinear, one for nearest, plus a one-row halo for
-//      the 3x3 epilogue) and issues one bulk (TMA) copy per row for the
-//      needed column span, completing on the stage's mbarrier — `stages`
-//      tiles ahead of the tile being computed (plain loads by all threads
-//      when the source is not 16-byte aligned);
-//   2. all threads compute the tile from shared memory into one of two
-//      output buffers: uint8 bilinear as the exact 11-bit fixed-point sum,
-//      float32 as two lerps, then the fused epilogue;
-//   3. thread 0 writes each output row with one bulk (TMA) store and, while
-//      that store drains, the ring moves on.
+// of TR rows x TW columns in a static round-robin.  Each CTA is warp
+// specialised:
+//   * one producer warp keeps a ring of `stages` tiles of source rows in
+//     shared memory.  For each tile it loads the tile's row table entries
+//     with all 32 lanes in one round trip, lists the distinct source rows the
+//     tile's output rows sample (two per row for bilinear, one for nearest,
+//     plus a one-row halo for the 3x3 epilogue) and issues one bulk (TMA)
+//     copy per row, from several lanes, for the needed column span,
+//     completing on the stage's "full" mbarrier.  It refills a stage as soon
+//     as the consumers release it on the stage's "empty" mbarrier.  When the
+//     source is not 16-byte aligned the warp copies the rows itself;
+//   * eight consumer warps compute each tile from shared memory into one of
+//     two output buffers (uint8 bilinear as the exact 11-bit fixed-point sum,
+//     float32 as two lerps, then the fused epilogue), and one consumer thread
+//     writes each output row with one bulk (TMA) store.
 // HBM is read once per needed source byte and written once per output byte.
 //
 // Sampling: CUDA interpolation page (hnwysp.cn/news/129086) §2.1 nearest,
@@ -51,6 +53,29 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Barrier among the consumer warps only (the producer warp never joins it).
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+// Consumer barrier that also returns whether `v` held on any consumer thread.
+__device__ __forceinline__ bool consumer_any(bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "n"(kConsumers)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
@@ -159,14 +184,19 @@ struct StageHdr {
     int pad;
 };
 
-// Thread 0: list the tile's source rows into stage `st`, record for each
-// computed row the slots of its two tap rows, and (bulk path) issue the
-// copies on `bar`.  Source rows are visited in non-decreasing order, so a
-// row already listed is one of the last two entries.
+// Producer warp: stage the source rows of `tile` into stage `st`.  All lanes
+// load the tile's row-table entries (one round trip); every lane then walks
+// the same list of distinct source rows (non-decreasing in the output row, so
+// a row already listed is one of the last two entries); lane 0 records the
+// list, the per-row slot map and the header; the row copies are spread over
+// the lanes.  Bulk path: lane 0 arms `full` with the byte count before any
+// copy is issued.  Plain path: the lanes copy the bytes and each arrives on
+// `full` (initialised for 32 arrivals).
 template <int LINEAR>
-__device__ void prepare_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, uint64_t *bar, int tile, int halo,
+__device__ void produce_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, uint64_t *full, int tile, int halo,
                               int in_es)
 {
+    const int lane = threadIdx.x & 31;
     StageHdr *h = reinterpret_cast<StageHdr *>(st);
     int *rows = reinterpret_cast<int *>(st + L.rows_off);
     int *map = reinterpret_cast<int *>(st + L.map_off);
@@ -175,8 +205,17 @@ __device__ void prepare_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, 
 
     const int cx0 = clampi(g.dx0 - halo, 0, a.OW - 1);
     const int cx1 = clampi(g.dx1 - 1 + halo, 0, a.OW - 1);
-    const int xs0 = a.xt[cx0].x;
-    const int xs1 = LINEAR ? min(a.xt[cx1].x + 1, a.W - 1) : a.xt[cx1].x;
+    const int nrc = (g.dy1 - g.dy0) + 2 * halo;
+    // one round trip: lanes 0/1 fetch the column span ends, lane k a row entry
+    int xv = 0;
+    if (lane < 2)
+        xv = __ldg(&a.xt[lane == 0 ? cx0 : cx1]).x;
+    int yv = 0;
+    if (lane < nrc)
+        yv = __ldg(&a.yt[clampi(g.dy0 - halo + lane, 0, a.OH - 1)]).x;
+    const int xs0 = __shfl_sync(0xffffffffu, xv, 0);
+    const int xs1r = __shfl_sync(0xffffffffu, xv, 1);
+    const int xs1 = LINEAR ? min(xs1r + 1, a.W - 1) : xs1r;
     int b_lo = xs0 * a.C * in_es;
     int b_hi = (xs1 + 1) * a.C * in_es;
     if (a.tma_in) {
@@ -185,73 +224,77 @@ __device__ void prepare_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, 
     }
     const int nbytes = b_hi - b_lo;
 
-    int n = 0;
+    // every lane builds the same list; lane 0 stores it
+    int n = 0, last = -1, prev = -1;   // last two listed rows
     bool overflow = nbytes > a.slot_bytes;
-    const int nrc = (g.dy1 - g.dy0) + 2 * halo;
-    for (int k = 0; k < nrc && !overflow; k++) {
-        const int dy = clampi(g.dy0 - halo + k, 0, a.OH - 1);
-        const int r0 = a.yt[dy].x;
+    for (int k = 0; k < nrc; k++) {
+        int r0;
+        if (k < 32) {
+            r0 = __shfl_sync(0xffffffffu, yv, k);
+        } else {
+            r0 = __ldg(&a.yt[clampi(g.dy0 - halo + k, 0, a.OH - 1)]).x;   // tiles of over 32 rows
+        }
         const int r1 = LINEAR ? min(r0 + 1, a.H - 1) : r0;
         int s0, s1;
-        if (n > 0 && rows[n - 1] == r0)
+        if (n > 0 && last == r0)
             s0 = n - 1;
-        else if (n > 1 && rows[n - 2] == r0)
+        else if (n > 1 && prev == r0)
             s0 = n - 2;
-        else if (n == a.max_rows) {
-            overflow = true;
-            break;
-        } else {
-            rows[n] = r0;
+        else {
+            if (n == a.max_rows) { overflow = true; break; }
+            if (lane == 0) rows[n] = r0;
+            prev = last; last = r0;
             s0 = n++;
         }
-        if (rows[n - 1] == r1)
+        if (last == r1)
             s1 = n - 1;
-        else if (n == a.max_rows) {
-            overflow = true;
-            break;
-        } else {
-            rows[n] = r1;
+        else {
+            if (n == a.max_rows) { overflow = true; break; }
+            if (lane == 0) rows[n] = r1;
+            prev = last; last = r1;
             s1 = n++;
         }
-        map[2 * k] = s0;
-        map[2 * k + 1] = s1;
+        if (lane == 0) {
+            map[2 * k] = s0;
+            map[2 * k + 1] = s1;
+        }
     }
     if (overflow) {
         // the host sizes max_rows and slot_bytes from the same tables, so this
         // is unreachable; it guards shared memory all the same
-        atomicExch(a.status, RZ_ERR_ARG);
+        if (lane == 0)
+            atomicExch(a.status, RZ_ERR_ARG);
         n = -1;
     }
-    h->nrows = n;
-    h->b_lo = b_lo;
-    h->nbytes = nbytes;
-    h->pad = tile;
+    if (lane == 0) {
+        h->nrows = n;
+        h->b_lo = b_lo;
+        h->nbytes = nbytes;
+        h->pad = tile;
+    }
+    __syncwarp();
     if (a.tma_in) {
-        // the barrier completes its phase even for a rejected tile
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n > 0 ? n * nbytes : 0));
-        for (int s = 0; s < n; s++)
-            bulk_load(slots + s * a.slot_bytes, g.src + (long long)rows[s] * a.src_pitch + b_lo,
-                      static_cast<uint32_t>(nbytes), bar);
+        // arm the barrier for every byte before any copy can land; a rejected
+        // tile completes the phase with no bytes
+        if (lane == 0)
+            mbar_arrive_expect_tx(full, static_cast<uint32_t>(n > 0 ? n * nbytes : 0));
+        __syncwarp();
+        for (int r = lane; r < n; r += 32)
+            bulk_load(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch + b_lo,
+                      static_cast<uint32_t>(nbytes), full);
+    } else {
+        for (int r = 0; r < n; r++) {
+            const uint8_t *src = g.src + (long long)rows[r] * a.src_pitch + b_lo;
+            uint8_t *d = slots + r * a.slot_bytes;
+            for (int k = lane; k < nbytes; k += 32)
+                d[k] = __ldg(src + k);
+        }
+        mbar_arrive(full);   // each lane releases its own copies
     }
 }
 
-// All threads: copy a prepared stage's rows with plain loads (unaligned sources).
-__device__ void load_stage_plain(const KArgs &a, const SmemLayout &L, uint8_t *st, int tile)
-{
-    const StageHdr *h = reinterpret_cast<const StageHdr *>(st);
-    const int *rows = reinterpret_cast<const int *>(st + L.rows_off);
-    uint8_t *slots = st + L.slots_off;
-    const TileGeom g = tile_geom(a, tile);
-    for (int s = 0; s < h->nrows; s++) {
-        const uint8_t *src = g.src + (long long)rows[s] * a.src_pitch + h->b_lo;
-        uint8_t *d = slots + s * a.slot_bytes;
-        for (int k = threadIdx.x; k < h->nbytes; k += kThreads)
-            d[k] = __ldg(src + k);
-    }
-}
-
-// Thread 0: one bulk store per output row of the tile (the 16-byte multiple
-// of each row; the ragged tail goes through store_tail).
+// One consumer thread: one bulk store per output row of the tile (the
+// 16-byte multiple of each row; the ragged tail goes through store_tail).
 __device__ void issue_stores(const KArgs &a, const SmemLayout &L, const uint8_t *ob, const TileGeom &g, int planes,
                              int px_bytes)
 {
@@ -268,8 +311,8 @@ __device__ void issue_stores(const KArgs &a, const SmemLayout &L, const uint8_t 
     bulk_commit();
 }
 
-// All threads: write the bytes of each output row that the bulk stores do
-// not cover (all of them when bulk stores are not allowed).
+// Consumer threads: write the bytes of each output row that the bulk stores
+// do not cover (all of them when bulk stores are not allowed).
 __device__ void store_tail(const KArgs &a, const SmemLayout &L, const uint8_t *ob, const TileGeom &g, int planes,
                            int px_bytes)
 {
@@ -281,7 +324,7 @@ __device__ void store_tail(const KArgs &a, const SmemLayout &L, const uint8_t *o
         return;
     uint8_t *base = g.dst + (long long)g.dy0 * a.dst_pitch + (long long)g.dx0 * px_bytes + bulk;
     const int n = planes * nr * tail;
-    for (int k = threadIdx.x; k < n; k += kThreads) {
+    for (int k = threadIdx.x; k < n; k += kConsumers) {
         const int row = k / tail, j = k - row * tail;
         const int c = row / nr, i = row - c * nr;
         base[c * a.dst_plane + i * a.dst_pitch + j] = ob[(c * a.TR + i) * L.out_row_bytes + bulk + j];
@@ -323,7 +366,7 @@ __device__ void compute_generic(const KArgs &a, const StageView &sv, const TileG
     const int orow_el = orow_bytes / ES;
     const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
     const int lg = min(8, ceil_log2(nc));
-    const int tpr = 1 << lg, rpp = kThreads >> lg;
+    const int tpr = 1 << lg, rpp = kConsumers >> lg;
     for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
         const int2 yw = __ldg(&a.yt[g.dy0 + rl]);
         const T *top = slots + sv.map[2 * rl] * slot_el - lo;
@@ -384,7 +427,7 @@ __device__ void compute_down2(const KArgs &a, const StageView &sv, const TileGeo
     constexpr int PX = (C == 1) ? 8 : (C == 3 ? 4 : 2);
     const int ngrp = nc / PX;
     const int lg = min(8, ceil_log2(ngrp + 1));
-    const int tpr = 1 << lg, rpp = kThreads >> lg;
+    const int tpr = 1 << lg, rpp = kConsumers >> lg;
     for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
         const uint8_t *top = sv.slots + sv.map[2 * rl] * sv.slot_bytes + ofs0;
         const uint8_t *bot = sv.slots + sv.map[2 * rl + 1] * sv.slot_bytes + ofs0;
@@ -484,7 +527,7 @@ __device__ void compute_normalize(const KArgs &a, const StageView &sv, const Til
     const int plane_el = a.TR * orow_el;
     const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
     const int lg = min(8, ceil_log2(nc));
-    const int tpr = 1 << lg, rpp = kThreads >> lg;
+    const int tpr = 1 << lg, rpp = kConsumers >> lg;
     for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
         const int2 yw = __ldg(&a.yt[g.dy0 + rl]);
         const int B1 = yw.y, B0 = 2048 - B1;
@@ -522,7 +565,7 @@ __device__ void compute_filter3x3(const KArgs &a, const StageView &sv, const Til
     {
         const int hr = nr + 2, hc = nc + 2;
         const int lg = min(8, ceil_log2(hc));
-        const int tpr = 1 << lg, rpp = kThreads >> lg;
+        const int tpr = 1 << lg, rpp = kConsumers >> lg;
         for (int k = threadIdx.x >> lg; k < hr; k += rpp) {
             const int dy = clampi(g.dy0 - 1 + k, 0, a.OH - 1);
             const float v = __int_as_float(__ldg(&a.yt[dy]).y);
@@ -544,10 +587,10 @@ __device__ void compute_filter3x3(const KArgs &a, const StageView &sv, const Til
             }
         }
     }
-    __syncthreads();
+    consumer_sync();
     {
         const int lg = min(8, ceil_log2(nc));
-        const int tpr = 1 << lg, rpp = kThreads >> lg;
+        const int tpr = 1 << lg, rpp = kConsumers >> lg;
         for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
             for (int cl = threadIdx.x & (tpr - 1); cl < nc; cl += tpr) {
 #pragma unroll
@@ -569,7 +612,7 @@ __device__ void compute_filter3x3(const KArgs &a, const StageView &sv, const Til
 
 // OP: 0 plain resize (T, C, LINEAR, VAR), 1 normalise, 2 3x3 filter.
 template <int OP, typename T, int C, int LINEAR, int VAR>
-__global__ void __launch_bounds__(kThreads) k_resize(const KArgs a)
+__global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int FAM = OP == 1 ? FAM_NORM : (OP == 2 ? FAM_FILT : (sizeof(T) == 1 ? FAM_U8 : FAM_F32));
@@ -578,25 +621,40 @@ __global__ void __launch_bounds__(kThreads) k_resize(const KArgs a)
     constexpr int PLANES = OP == 1 ? C : 1;
     constexpr int PX_BYTES = OP == 1 ? 4 : C * fam_out_es(FAM);
     const SmemLayout L = smem_layout(FAM, C, a.TR, a.TW, a.max_rows, a.slot_bytes, a.stages);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + kMaxStages;
     const int ntiles = a.batch * a.tiles_x * a.tiles_y;
     const int NS = a.stages;
     const int G = gridDim.x;
 
     if (threadIdx.x == 0) {
-        if (a.tma_in) {
-            for (int s = 0; s < NS; s++)
-                mbar_init(&bars[s], 1);
-            fence_mbar_init();
-        }
         for (int s = 0; s < NS; s++) {
-            const int t = blockIdx.x + s * G;
-            if (t < ntiles)
-                prepare_stage<LINEAR>(a, L, smem + L.stage_off + s * L.stage_bytes, &bars[s], t, HALO, IN_ES);
+            mbar_init(&full[s], a.tma_in ? 1 : 32);
+            mbar_init(&empty[s], 1);
         }
+        fence_mbar_init();
     }
     __syncthreads();
 
+    if (threadIdx.x >= kConsumers) {
+        // ---------------- producer warp
+        int it = 0;
+        for (int t = blockIdx.x; t < ntiles; t += G, ++it) {
+            const int s = it % NS;
+            if (it >= NS) {
+                // wait until the consumers have released this stage's previous tile
+                bool ok = true;
+                if ((threadIdx.x & 31) == 0)
+                    ok = mbar_wait_bounded(&empty[s], ((it / NS) - 1) & 1, a.status);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0))
+                    break;
+            }
+            produce_stage<LINEAR>(a, L, smem + L.stage_off + s * L.stage_bytes, &full[s], t, HALO, IN_ES);
+        }
+        return;
+    }
+
+    // ---------------- consumer warps
     int it = 0;
     bool failed = false;
     for (int t = blockIdx.x; t < ntiles; t += G, ++it) {
@@ -606,18 +664,10 @@ __global__ void __launch_bounds__(kThreads) k_resize(const KArgs a)
         // the output buffer is free once the store issued two tiles ago has read it
         if (threadIdx.x == 0 && it >= 2)
             bulk_wait_read<1>();
-        if (a.tma_in) {
-            const bool ok = mbar_wait_bounded(&bars[s], (it / NS) & 1, a.status);
-            if (__syncthreads_or(!ok)) {
-                failed = true;
-                break;
-            }
-        } else {
-            __syncthreads();    // the stage header written by thread 0 is visible
-            load_stage_plain(a, L, st, t);
-            __syncthreads();
-        }
-        if (reinterpret_cast<const StageHdr *>(st)->nrows < 0) {
+        const bool ok = mbar_wait_bounded(&full[s], (it / NS) & 1, a.status);
+        // all consumers leave together if any timed out (the header is only
+        // read once the stage is known to be full)
+        if (consumer_any(!ok) || reinterpret_cast<const StageHdr *>(st)->nrows < 0) {
             failed = true;
             break;
         }
@@ -634,13 +684,11 @@ __global__ void __launch_bounds__(kThreads) k_resize(const KArgs a)
             compute_filter3x3<C>(a, sv, g, ob, L.out_row_bytes, reinterpret_cast<float *>(smem + L.mid_off));
         }
         fence_proxy_async_smem();
-        __syncthreads();
+        consumer_sync();
         if (threadIdx.x == 0) {
+            mbar_arrive(&empty[s]);          // the stage may be refilled
             if (a.tma_out)
                 issue_stores(a, L, ob, g, PLANES, PX_BYTES);
-            const int tn = t + NS * G;
-            if (tn < ntiles)
-                prepare_stage<LINEAR>(a, L, st, &bars[s], tn, HALO, IN_ES);
         }
         store_tail(a, L, ob, g, PLANES, PX_BYTES);
     }
@@ -651,7 +699,7 @@ __global__ void __launch_bounds__(kThreads) k_resize(const KArgs a)
             for (int k = 0; k < NS; k++) {
                 const int j = it + k;
                 if (blockIdx.x + j * G < ntiles)
-                    mbar_wait_bounded(&bars[j % NS], (j / NS) & 1, nullptr);
+                    mbar_wait_bounded(&full[j % NS], (j / NS) & 1, nullptr);
             }
         }
     }

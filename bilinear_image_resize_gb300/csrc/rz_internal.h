@@ -9,7 +9,8 @@
 
 namespace rz {
 
-constexpr int kThreads = 256;           // threads per CTA, every kernel
+constexpr int kConsumers = 256;         // compute threads per CTA (warps 0..7)
+constexpr int kThreads = kConsumers + 32;  // plus one producer warp that stages tiles
 constexpr int kMaxSmem = 227 * 1024;    // opt-in dynamic shared memory per CTA on sm_103a
 constexpr int kMaxStages = 4;           // staged-tile ring depth limit
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded mbarrier waits: 1 s
@@ -29,7 +30,7 @@ __host__ __device__ constexpr int fam_halo(int fam) { return fam == FAM_FILT ? 1
 // Byte offsets of the pieces of a CTA's dynamic shared memory.  Host and
 // device compute them with this one function.
 //
-//   [0, 64)                       one mbarrier per stage
+//   [0, 64)                       per stage: a "full" and an "empty" mbarrier
 //   stages x stage_bytes          per stage: header {nrows, b_lo, nbytes, tile},
 //                                 int rows[max_rows], int map[2 * computed rows],
 //                                 then max_rows staged row segments of slot_bytes
