@@ -235,6 +235,10 @@ def gpu_arm(args, rank, local_rank, world):
         rz.resize_plan_set_option(plan, rz.RZ_OPT_GENERIC_ONLY, 1)
     if args.ctas_per_sm:
         rz.resize_plan_set_option(plan, rz.RZ_OPT_CTAS_PER_SM, args.ctas_per_sm)
+    if args.grid_per_tile:
+        rz.resize_plan_set_option(plan, rz.RZ_OPT_GRID_MODE, 1)
+    if args.no_pdl:
+        rz.resize_plan_set_option(plan, rz.RZ_OPT_PDL, 0)
     epi = None
     if kind == "norm":
         epi = rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=synth.NORM_MEAN, std=synth.NORM_STD)
@@ -481,6 +485,42 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ short run for profilers
+
+def profile_run(args):
+    """A few eager launches of the workload and nothing else (no graphs, no
+    clock sampling, no CPU baseline): the command the ncu captures run."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import torch
+
+    import bilinear_image_resize_gb300 as rz
+    from bilinear_image_resize_gb300 import synth
+    desc, kind, H, W, OH, OW, C, mode_s, batch = WORKLOADS[args.workload]
+    mode = rz.RZ_LINEAR if mode_s == "linear" else rz.RZ_NEAREST
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    in_bytes = batch * H * W * C * (4 if kind == "filt" else 1)
+    ring = max(2, min(64, int(3 * L2_BYTES // max(1, in_bytes)) + 1))
+    frames = make_frames(kind, H, W, C, batch, ring, dev)
+    outs = make_outputs(kind, OH, OW, C, batch, ring, dev)
+    plan = rz.resize_plan_create(H, W, OH, OW, mode)
+    epi = None
+    if kind == "norm":
+        epi = rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=synth.NORM_MEAN, std=synth.NORM_STD)
+    elif kind == "filt":
+        epi = rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=synth.filter_weights())
+    for i in range(args.warmup + args.profile):
+        if kind == "u8":
+            rz.resize_u8(plan, frames[i % ring], outs[i % ring])
+        else:
+            rz.resize_fused(plan, frames[i % ring], outs[i % ring], epi)
+    torch.cuda.synchronize()
+    assert rz.resize_plan_status(plan) == rz.RZ_OK
+    plan.destroy()
+    print(f"profile run: {args.warmup} + {args.profile} launches of {desc}")
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -494,13 +534,20 @@ def main():
     ap.add_argument("--stages", type=int, default=0, help="staged-tile ring depth (tuning only)")
     ap.add_argument("--generic", action="store_true", help="disable the exact 2x path (tuning only)")
     ap.add_argument("--ctas-per-sm", type=int, default=0, help="cap resident CTAs per SM (tuning only)")
+    ap.add_argument("--grid-per-tile", action="store_true", help="one CTA per tile (tuning only)")
+    ap.add_argument("--no-pdl", action="store_true", help="plain stream-ordered launches (tuning only)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--profile", type=int, default=0,
+                    help="only run W + N eager launches (for ncu captures); prints no JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
 
     if args.impl == "reference":
         reference_arm(args)
+        return
+    if args.profile:
+        profile_run(args)
         return
 
     rank, local_rank, world = dist_env()
@@ -542,7 +589,8 @@ def main():
                 "algorithmic_bytes_per_step": r["step_bytes"],
                 "parallelism": f"{world} independent replica(s)",
                 "tuning": {k: v for k, v in (("tile", args.tile), ("stages", args.stages),
-                                             ("generic_only", args.generic), ("ctas_per_sm", args.ctas_per_sm))
+                                             ("generic_only", args.generic), ("ctas_per_sm", args.ctas_per_sm),
+                                             ("grid_per_tile", args.grid_per_tile), ("no_pdl", args.no_pdl))
                            if v} or "automatic",
             },
             "hbm_gbs": r["achieved_gbs"],

@@ -27,6 +27,8 @@ RZ_MAX_DIM = 65536
 RZ_OPT_STAGES = 1
 RZ_OPT_GENERIC_ONLY = 2
 RZ_OPT_CTAS_PER_SM = 3
+RZ_OPT_GRID_MODE = 4
+RZ_OPT_PDL = 5
 
 # kernel families for resize_plan_set_tile
 KIND_U8 = 0

@@ -101,6 +101,8 @@ struct rz_plan_s {
     int opt_stages = 0;        // 0: automatic
     int opt_generic = 0;       // 1: never use an exact-ratio specialisation
     int opt_ctas_per_sm = 0;   // 0: as many as fit
+    int opt_grid_mode = 0;     // 0: persistent CTAs; 1: one CTA per tile
+    int opt_pdl = 1;           // programmatic dependent launch
 };
 
 namespace {
@@ -303,7 +305,9 @@ int get_tile(rz_plan_s *p, int fam, int C, int batch, TileCfg *out, const void *
     if (p->opt_ctas_per_sm > 0) per_sm = std::min(per_sm, p->opt_ctas_per_sm);
     const long long ntiles = static_cast<long long>(batch) * t.tiles_x * t.tiles_y;
     if (ntiles > 0x7fffffffLL) return RZ_ERR_UNSUPPORTED;
-    t.grid = static_cast<int>(std::min<long long>(ntiles, static_cast<long long>(per_sm) * sms));
+    t.grid = p->opt_grid_mode == 1
+                 ? static_cast<int>(ntiles)
+                 : static_cast<int>(std::min<long long>(ntiles, static_cast<long long>(per_sm) * sms));
     p->cache.push_back({fam, C, batch, t});
     *out = t;
     *fn_out = fn;
@@ -390,7 +394,7 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     a.yt = fl ? p->d_yf : p->d_yq;
     a.status = p->d_status;
     if (!do_launch) return RZ_OK;
-    const int e = rz::launch_resize(fn, a, t.grid, t.smem, stream);
+    const int e = rz::launch_resize(fn, a, t.grid, t.smem, p->opt_pdl != 0, stream);
     if (e != 0) return cuda_fail(static_cast<cudaError_t>(e));
     return RZ_OK;
 }
@@ -534,6 +538,14 @@ int resize_plan_set_option(rz_plan p, int option, int value)
     case RZ_OPT_CTAS_PER_SM:
         if (value < 0 || value > 32) return RZ_ERR_ARG;
         p->opt_ctas_per_sm = value;
+        break;
+    case RZ_OPT_GRID_MODE:
+        if (value != 0 && value != 1) return RZ_ERR_ARG;
+        p->opt_grid_mode = value;
+        break;
+    case RZ_OPT_PDL:
+        if (value != 0 && value != 1) return RZ_ERR_ARG;
+        p->opt_pdl = value;
         break;
     default:
         return RZ_ERR_ARG;

@@ -115,16 +115,33 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return true;
 }
 
-// Bulk copy global -> this CTA's shared memory, completing on `bar`.
-// Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar)
+// Bulk copy global -> this CTA's shared memory, completing on `bar`, with an
+// L2 cache policy (createpolicy) attached.  Both addresses 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load_hint(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar,
+                                               uint64_t policy)
 {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(sdst)),
-        "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_addr(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
 }
+
+// L2 policy for data read once: evicted first, so that the small sampling
+// tables (read by every launch) stay resident.
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Programmatic dependent launch: wait until the grids this launch depends on
+// have completed and their memory is visible; allow the next grid in the
+// stream to start launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
 // Bulk copy shared -> global (bulk-group completion).
 __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
@@ -279,9 +296,10 @@ __device__ void produce_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, 
         if (lane == 0)
             mbar_arrive_expect_tx(full, static_cast<uint32_t>(n > 0 ? n * nbytes : 0));
         __syncwarp();
+        const uint64_t pol = policy_evict_first();
         for (int r = lane; r < n; r += 32)
-            bulk_load(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch + b_lo,
-                      static_cast<uint32_t>(nbytes), full);
+            bulk_load_hint(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch + b_lo,
+                           static_cast<uint32_t>(nbytes), full, pol);
     } else {
         for (int r = 0; r < n; r++) {
             const uint8_t *src = g.src + (long long)rows[r] * a.src_pitch + b_lo;
@@ -635,6 +653,10 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a)
         fence_mbar_init();
     }
     __syncthreads();
+    // the next launch in the stream may begin its set-up; nothing of this
+    // grid touches global memory before the grids it depends on are done
+    grid_launch_dependents();
+    grid_dependency_wait();
 
     if (threadIdx.x >= kConsumers) {
         // ---------------- producer warp
@@ -737,7 +759,7 @@ const void *kernel_for(int fam, int mode, int variant, int C)
     }
 }
 
-int launch_resize(const void *fn, const KArgs &a, int grid, size_t smem, void *stream)
+int launch_resize(const void *fn, const KArgs &a, int grid, size_t smem, bool pdl, void *stream)
 {
     if (grid <= 0)
         return 0;
@@ -746,6 +768,15 @@ int launch_resize(const void *fn, const KArgs &a, int grid, size_t smem, void *s
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        // overlap this launch's start with the previous kernel's tail; the
+        // kernel waits (griddepcontrol.wait) before touching global memory
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     return static_cast<int>(
         cudaLaunchKernelEx(&cfg, reinterpret_cast<void (*)(const KArgs)>(const_cast<void *>(fn)), a));
 }

@@ -97,7 +97,8 @@ struct KArgs {
 // Kernel entry for (family, mode, variant, C); nullptr if none.
 const void *kernel_for(int fam, int mode, int variant, int C);
 
-// Launch it on `grid` persistent CTAs (asynchronous).  Returns a cudaError_t value.
-int launch_resize(const void *fn, const KArgs &a, int grid, size_t smem, void *stream);
+// Launch it on `grid` CTAs (asynchronous), optionally as a programmatic
+// dependent launch.  Returns a cudaError_t value.
+int launch_resize(const void *fn, const KArgs &a, int grid, size_t smem, bool pdl, void *stream);
 
 }  // namespace rz

@@ -224,12 +224,21 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  *                       (uint8 2x downscale, used only when every table entry
  *                       is the 2x pattern, where it is bit-identical);
  *   RZ_OPT_CTAS_PER_SM  value 0 (as many as fit) or 1..32: caps the resident
- *                       CTAs per SM of the persistent grid.
+ *                       CTAs per SM of the persistent grid;
+ *   RZ_OPT_GRID_MODE    value 0 (persistent CTAs, the default) or 1 (one CTA
+ *                       per output tile);
+ *   RZ_OPT_PDL          value 1 (default) or 0: launch as a programmatic
+ *                       dependent launch, so that a resize queued right after
+ *                       another kernel on the same stream starts its set-up
+ *                       while that kernel finishes (it still reads and writes
+ *                       memory only after that kernel has completed).
  * Returns RZ_ERR_ARG for an unknown option or value.
  */
 #define RZ_OPT_STAGES 1
 #define RZ_OPT_GENERIC_ONLY 2
 #define RZ_OPT_CTAS_PER_SM 3
+#define RZ_OPT_GRID_MODE 4
+#define RZ_OPT_PDL 5
 RZ_API int resize_plan_set_option(rz_plan p, int option, int value);
 
 #ifdef __cplusplus

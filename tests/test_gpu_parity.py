@@ -328,12 +328,15 @@ def run_u8_opts(rz, img, OH, OW, mode, opts, tile=None):
 
 
 @pytest.mark.parametrize("stages", [1, 2, 3, 4])
-@pytest.mark.parametrize("ctas", [1, 2, 0])
+@pytest.mark.parametrize("ctas", [1, 2, 0, "per_tile"])
 def test_ring_depth_and_grid_do_not_change_results(rz, stages, ctas):
     # one or two CTAs per SM make every CTA walk many tiles, so each stage's
-    # barrier goes through many phases
+    # barrier goes through many phases; "per_tile" launches one CTA per tile
     img = synth.smooth_rgb(1920, 1080, 2)
-    opts = {rz.RZ_OPT_STAGES: stages, rz.RZ_OPT_CTAS_PER_SM: ctas}
+    if ctas == "per_tile":
+        opts = {rz.RZ_OPT_STAGES: stages, rz.RZ_OPT_GRID_MODE: 1, rz.RZ_OPT_PDL: 0}
+    else:
+        opts = {rz.RZ_OPT_STAGES: stages, rz.RZ_OPT_CTAS_PER_SM: ctas}
     for (OH, OW) in [(540, 960), (720, 1280), (2160, 3840)]:
         got = run_u8_opts(rz, img, OH, OW, rz.RZ_LINEAR, opts)
         np.testing.assert_array_equal(got, oracle.linear_u8(img, OH, OW))
@@ -362,6 +365,31 @@ def test_exact_2x_path_tiles(rz, tile):
 def test_options_reject_bad_values(rz):
     with rz.resize_plan_create(8, 8, 4, 4, rz.RZ_LINEAR) as plan:
         for opt, val in [(rz.RZ_OPT_STAGES, 5), (rz.RZ_OPT_STAGES, -1), (rz.RZ_OPT_GENERIC_ONLY, 2),
-                         (rz.RZ_OPT_CTAS_PER_SM, 33), (99, 0)]:
+                         (rz.RZ_OPT_CTAS_PER_SM, 33), (rz.RZ_OPT_GRID_MODE, 2), (rz.RZ_OPT_PDL, 3), (99, 0)]:
             with pytest.raises(rz.ResizeError):
                 rz.resize_plan_set_option(plan, opt, val)
+
+
+def test_back_to_back_dependent_resizes(rz):
+    # a chain where each resize reads the previous one's output, queued with
+    # programmatic dependent launches: every link must see its input complete
+    img = synth.smooth_rgb(1920, 1080, 2)
+    a = torch.from_numpy(np.ascontiguousarray(img)).cuda()
+    b = torch.empty((540, 960, 3), dtype=torch.uint8, device="cuda")
+    c = torch.empty((270, 480, 3), dtype=torch.uint8, device="cuda")
+    d = torch.empty((540, 960, 3), dtype=torch.uint8, device="cuda")
+    p1 = rz.resize_plan_create(1080, 1920, 540, 960, rz.RZ_LINEAR)
+    p2 = rz.resize_plan_create(540, 960, 270, 480, rz.RZ_LINEAR)
+    p3 = rz.resize_plan_create(270, 480, 540, 960, rz.RZ_LINEAR)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        rz.resize_u8(p1, a, b)
+        rz.resize_u8(p2, b, c)
+        rz.resize_u8(p3, c, d)
+    torch.cuda.synchronize()
+    e1 = oracle.linear_u8(img, 540, 960)
+    e2 = oracle.linear_u8(e1, 270, 480)
+    np.testing.assert_array_equal(d.cpu().numpy(), oracle.linear_u8(e2, 540, 960))
+    for p in (p1, p2, p3):
+        assert rz.resize_plan_status(p) == rz.RZ_OK
+        p.destroy()
