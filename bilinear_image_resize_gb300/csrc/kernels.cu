@@ -167,6 +167,36 @@ __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? l
 
 __device__ __forceinline__ int ceil_log2(int v) { return v <= 1 ? 0 : 32 - __clz(v - 1); }
 
+// floor(num / den) for 0 < den <= 2^17 and |num / den| < 2^17 + 1, exactly:
+// the float quotient has absolute error below 2^-6 there, so its floor is
+// within one of the true floor, and 64-bit integer checks correct it.
+__device__ __forceinline__ int floor_div_exact(long long num, int den)
+{
+    int q = __float2int_rd(static_cast<float>(num) / static_cast<float>(den));
+    const long long qd = static_cast<long long>(q) * den;
+    if (qd > num)
+        q -= 1;
+    else if (qd + den <= num)
+        q += 1;
+    return q;
+}
+
+// Source row/column sampled by output index d, exactly as the plan's tables
+// hold it: bilinear floor(((2d+1) n_in - n_out) / (2 n_out)) folded into
+// [0, n_in - 1]; nearest floor(d n_in / n_out) kept below n_in.  The
+// producer needs only these indices (not the weights) to stage a tile, so it
+// derives them without touching global memory.
+template <int LINEAR>
+__device__ __forceinline__ int sample_index(int n_in, int n_out, int d)
+{
+    int s;
+    if (LINEAR)
+        s = floor_div_exact((2LL * d + 1) * n_in - n_out, 2 * n_out);
+    else
+        s = floor_div_exact(static_cast<long long>(d) * n_in, n_out);
+    return s < 0 ? 0 : (s > n_in - 1 ? n_in - 1 : s);
+}
+
 // ------------------------------------------------------------------ tiles and stages
 
 struct TileGeom {
@@ -201,35 +231,30 @@ struct StageHdr {
     int pad;
 };
 
-// Producer warp: stage the source rows of `tile` into stage `st`.  All lanes
-// load the tile's row-table entries (one round trip); every lane then walks
-// the same list of distinct source rows (non-decreasing in the output row, so
-// a row already listed is one of the last two entries); lane 0 records the
-// list, the per-row slot map and the header; the row copies are spread over
-// the lanes.  Bulk path: lane 0 arms `full` with the byte count before any
-// copy is issued.  Plain path: the lanes copy the bytes and each arrives on
-// `full` (initialised for 32 arrivals).
+// Producer warp, part 1 (no global memory access): list the source rows of
+// `tile` into stage `st`.  Lanes derive the tile's column span and row
+// indices in parallel; every lane then walks the same list of distinct
+// source rows (non-decreasing in the output row, so a row already listed is
+// one of the last two entries); lane 0 records the list, the per-row slot
+// map and the header.
 template <int LINEAR>
-__device__ void produce_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, uint64_t *full, int tile, int halo,
-                              int in_es)
+__device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, int tile, int halo, int in_es)
 {
     const int lane = threadIdx.x & 31;
     StageHdr *h = reinterpret_cast<StageHdr *>(st);
     int *rows = reinterpret_cast<int *>(st + L.rows_off);
     int *map = reinterpret_cast<int *>(st + L.map_off);
-    uint8_t *slots = st + L.slots_off;
     const TileGeom g = tile_geom(a, tile);
 
     const int cx0 = clampi(g.dx0 - halo, 0, a.OW - 1);
     const int cx1 = clampi(g.dx1 - 1 + halo, 0, a.OW - 1);
     const int nrc = (g.dy1 - g.dy0) + 2 * halo;
-    // one round trip: lanes 0/1 fetch the column span ends, lane k a row entry
     int xv = 0;
     if (lane < 2)
-        xv = __ldg(&a.xt[lane == 0 ? cx0 : cx1]).x;
+        xv = sample_index<LINEAR>(a.W, a.OW, lane == 0 ? cx0 : cx1);
     int yv = 0;
     if (lane < nrc)
-        yv = __ldg(&a.yt[clampi(g.dy0 - halo + lane, 0, a.OH - 1)]).x;
+        yv = sample_index<LINEAR>(a.H, a.OH, clampi(g.dy0 - halo + lane, 0, a.OH - 1));
     const int xs0 = __shfl_sync(0xffffffffu, xv, 0);
     const int xs1r = __shfl_sync(0xffffffffu, xv, 1);
     const int xs1 = LINEAR ? min(xs1r + 1, a.W - 1) : xs1r;
@@ -241,16 +266,11 @@ __device__ void produce_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, 
     }
     const int nbytes = b_hi - b_lo;
 
-    // every lane builds the same list; lane 0 stores it
     int n = 0, last = -1, prev = -1;   // last two listed rows
     bool overflow = nbytes > a.slot_bytes;
-    for (int k = 0; k < nrc; k++) {
-        int r0;
-        if (k < 32) {
-            r0 = __shfl_sync(0xffffffffu, yv, k);
-        } else {
-            r0 = __ldg(&a.yt[clampi(g.dy0 - halo + k, 0, a.OH - 1)]).x;   // tiles of over 32 rows
-        }
+    for (int k = 0; k < nrc && !overflow; k++) {
+        const int r0 = k < 32 ? __shfl_sync(0xffffffffu, yv, k)
+                              : sample_index<LINEAR>(a.H, a.OH, clampi(g.dy0 - halo + k, 0, a.OH - 1));
         const int r1 = LINEAR ? min(r0 + 1, a.H - 1) : r0;
         int s0, s1;
         if (n > 0 && last == r0)
@@ -276,30 +296,39 @@ __device__ void produce_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, 
             map[2 * k + 1] = s1;
         }
     }
-    if (overflow) {
-        // the host sizes max_rows and slot_bytes from the same tables, so this
-        // is unreachable; it guards shared memory all the same
-        if (lane == 0)
-            atomicExch(a.status, RZ_ERR_ARG);
-        n = -1;
-    }
     if (lane == 0) {
-        h->nrows = n;
+        // the host sizes max_rows and slot_bytes from the same indices, so an
+        // overflow is unreachable; it guards shared memory all the same
+        h->nrows = overflow ? -1 : n;
         h->b_lo = b_lo;
         h->nbytes = nbytes;
         h->pad = tile;
     }
     __syncwarp();
+}
+
+// Producer warp, part 2: fetch the planned rows.  Bulk path: lane 0 arms
+// `full` with the byte count before any copy is issued, and the copies are
+// spread over the lanes.  Plain path (unaligned source): the lanes copy the
+// bytes and each arrives on `full` (initialised for 32 arrivals).
+__device__ void fetch_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, uint64_t *full, uint64_t policy)
+{
+    const int lane = threadIdx.x & 31;
+    const StageHdr *h = reinterpret_cast<const StageHdr *>(st);
+    const int *rows = reinterpret_cast<const int *>(st + L.rows_off);
+    uint8_t *slots = st + L.slots_off;
+    const TileGeom g = tile_geom(a, h->pad);
+    const int n = h->nrows, nbytes = h->nbytes, b_lo = h->b_lo;
+    if (n < 0 && lane == 0)
+        atomicExch(a.status, RZ_ERR_ARG);
     if (a.tma_in) {
-        // arm the barrier for every byte before any copy can land; a rejected
-        // tile completes the phase with no bytes
+        // a rejected tile completes the phase with no bytes
         if (lane == 0)
             mbar_arrive_expect_tx(full, static_cast<uint32_t>(n > 0 ? n * nbytes : 0));
         __syncwarp();
-        const uint64_t pol = policy_evict_first();
         for (int r = lane; r < n; r += 32)
             bulk_load_hint(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch + b_lo,
-                           static_cast<uint32_t>(nbytes), full, pol);
+                           static_cast<uint32_t>(nbytes), full, policy);
     } else {
         for (int r = 0; r < n; r++) {
             const uint8_t *src = g.src + (long long)rows[r] * a.src_pitch + b_lo;
@@ -653,16 +682,24 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a)
         fence_mbar_init();
     }
     __syncthreads();
-    // the next launch in the stream may begin its set-up; nothing of this
-    // grid touches global memory before the grids it depends on are done
+    // the next launch in the stream may begin its set-up now
     grid_launch_dependents();
-    grid_dependency_wait();
 
     if (threadIdx.x >= kConsumers) {
         // ---------------- producer warp
+        const uint64_t policy = policy_evict_first();
+        // plan the first stages before waiting for the grids this launch
+        // depends on: planning reads no global memory
+        for (int k = 0; k < NS; k++) {
+            const int t = blockIdx.x + k * G;
+            if (t < ntiles)
+                plan_stage<LINEAR>(a, L, smem + L.stage_off + k * L.stage_bytes, t, HALO, IN_ES);
+        }
+        grid_dependency_wait();
         int it = 0;
         for (int t = blockIdx.x; t < ntiles; t += G, ++it) {
             const int s = it % NS;
+            uint8_t *st = smem + L.stage_off + s * L.stage_bytes;
             if (it >= NS) {
                 // wait until the consumers have released this stage's previous tile
                 bool ok = true;
@@ -670,11 +707,15 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a)
                     ok = mbar_wait_bounded(&empty[s], ((it / NS) - 1) & 1, a.status);
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0))
                     break;
+                plan_stage<LINEAR>(a, L, st, t, HALO, IN_ES);
             }
-            produce_stage<LINEAR>(a, L, smem + L.stage_off + s * L.stage_bytes, &full[s], t, HALO, IN_ES);
+            fetch_stage(a, L, st, &full[s], policy);
         }
         return;
     }
+    // consumers touch global memory only after the grids this launch depends
+    // on are complete
+    grid_dependency_wait();
 
     // ---------------- consumer warps
     int it = 0;
