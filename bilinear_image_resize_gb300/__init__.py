@@ -17,12 +17,14 @@ from . import _native
 from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_EPI_FILTER3X3,
                       RZ_EPI_NORMALIZE_NCHW, RZ_ERR_ARG, RZ_ERR_CUDA, RZ_ERR_NOMEM, RZ_ERR_TIMEOUT,
                       RZ_ERR_UNSUPPORTED, RZ_F32, RZ_LINEAR, RZ_MAX_DIM, RZ_NEAREST, RZ_OK, RZ_OPT_CTAS_PER_SM,
-                      RZ_OPT_GENERIC_ONLY, RZ_OPT_GRID_MODE, RZ_OPT_PDL, RZ_OPT_STAGES, RZ_U8, RzEpilogue)
+                      RZ_OPT_GENERIC_ONLY, RZ_OPT_GRID_MODE, RZ_OPT_PDL, RZ_OPT_STAGES, RZ_U8, RZ_NOALLOC_MAX_DIM,
+                      RzEpilogue)
 
 __all__ = [
     "ResizeError", "Plan", "resize_plan_create", "resize_plan_destroy", "resize_plan_status",
     "resize_plan_set_tile", "resize_plan_set_option", "resize_u8", "resize_f32", "resize_fused", "resize_u8_host",
-    "resize_axis_table", "resize_strerror", "resize_last_cuda_error", "make_epilogue",
+    "resize_axis_table", "resize_strerror", "resize_last_cuda_error", "make_epilogue", "resize_u8_noalloc",
+    "RZ_NOALLOC_MAX_DIM",
     "RZ_LINEAR", "RZ_NEAREST", "RZ_U8", "RZ_F32", "RZ_EPI_NORMALIZE_NCHW", "RZ_EPI_FILTER3X3",
     "RZ_OK", "RZ_ERR_ARG", "RZ_ERR_UNSUPPORTED", "RZ_ERR_CUDA", "RZ_ERR_NOMEM", "RZ_ERR_TIMEOUT",
     "RZ_MAX_DIM", "KIND_U8", "KIND_F32", "KIND_NORMALIZE", "KIND_FILTER3X3",
@@ -130,6 +132,18 @@ def resize_u8(plan: Plan, src, dst, mode: int | None = None, stream=None) -> Non
         raise ValueError("src and dst channel counts differ")
     _check(_native.load().resize_u8(plan.handle, src.data_ptr(), sp, dst.data_ptr(), dp, H, W, C, OH, OW,
                                     plan.mode if mode is None else mode, _stream(stream)), "resize_u8")
+
+
+def resize_u8_noalloc(src, dst, mode: int = RZ_LINEAR, stream=None) -> None:
+    """dst[:] = resize(src) for uint8 tensors without a plan and without any
+    device allocation (tables in the library's static device array; see
+    include/gbresize.h for the size limit and the sharing rules)."""
+    H, W, C, sp = _hwc(src, "src")
+    OH, OW, C2, dp = _hwc(dst, "dst")
+    if C2 != C:
+        raise ValueError("src and dst channel counts differ")
+    _check(_native.load().resize_u8_noalloc(src.data_ptr(), sp, dst.data_ptr(), dp, H, W, C, OH, OW, mode,
+                                            _stream(stream)), "resize_u8_noalloc")
 
 
 def resize_f32(plan: Plan, src, dst, mode: int | None = None, stream=None) -> None:

@@ -23,6 +23,7 @@ RZ_ERR_CUDA = 3
 RZ_ERR_NOMEM = 4
 RZ_ERR_TIMEOUT = 5
 RZ_MAX_DIM = 65536
+RZ_NOALLOC_MAX_DIM = 8192
 
 RZ_OPT_STAGES = 1
 RZ_OPT_GENERIC_ONLY = 2
@@ -67,6 +68,7 @@ SIGNATURES = {
     "resize_axis_table": (_i, [_i, _i, _i, _p, _p, _p]),
     "resize_strerror": (ctypes.c_char_p, [_i]),
     "resize_last_cuda_error": (_i, []),
+    "resize_u8_noalloc": (_i, [_p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
 }
 
 _lib = None

@@ -401,6 +401,10 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
 
 }  // namespace
 
+namespace rz {
+void record_cuda_error(int e) { g_last_cuda_error = e; }
+}  // namespace rz
+
 extern "C" {
 
 int resize_axis_table(int n_in, int n_out, int mode, int32_t *ofs, int32_t *w_q11, float *u)

@@ -94,6 +94,9 @@ struct KArgs {
     float w[9];                // 3x3 epilogue weights, row-major
 };
 
+// Record a cudaError_t for resize_last_cuda_error (this host thread).
+void record_cuda_error(int e);
+
 // Kernel entry for (family, mode, variant, C); nullptr if none.
 const void *kernel_for(int fam, int mode, int variant, int C);
 

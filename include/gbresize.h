@@ -241,6 +241,34 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
 #define RZ_OPT_PDL 5
 RZ_API int resize_plan_set_option(rz_plan p, int option, int value);
 
+/*
+ * uint8 resize that allocates nothing, for callers that may not allocate
+ * device memory themselves: a plugin whose device memory belongs to its host
+ * framework's pooling allocator (a stray cudaMalloc there can fail under a
+ * tight budget or wait on the device), or a real-time pipeline that forbids
+ * allocation once it runs.  The pages have no counterpart; it is an addition
+ * to the resize_plan_create / resize_u8 pair.
+ *
+ * Arguments, layout and results are those of resize_u8 (bit-identical
+ * output), without a plan: src and dst are the caller's device buffers.  The
+ * sampling tables and the kernel's status word live in one static device
+ * array of about 128 KB that every GPU loading the library keeps until the
+ * process exits; a small kernel rebuilds the tables on the device at the
+ * start of each call.  No cudaMalloc, cudaFree or other allocating routine
+ * is called.
+ *   - out_h and out_w must not exceed RZ_NOALLOC_MAX_DIM: larger sizes return
+ *     RZ_ERR_UNSUPPORTED before anything is queued.
+ *   - All calls share the array.  Calls queued on one stream are ordered and
+ *     safe; calls that overlap on the GPU (different streams running at the
+ *     same time) race on the tables and may produce wrong results.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Kernel time-outs are not reported (there is no plan to hold a status).
+ */
+#define RZ_NOALLOC_MAX_DIM 8192
+RZ_API int resize_u8_noalloc(const uint8_t *src, size_t src_pitch, uint8_t *dst, size_t dst_pitch, int H, int W,
+                             int C, int out_h, int out_w, int mode, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
