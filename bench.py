@@ -300,9 +300,9 @@ def gpu_arm(args, rank, local_rank, world):
     sampler = ClockSampler(visible[local_rank] if local_rank < len(visible) else local_rank)
     sampler.start()
     time.sleep(0.3)
-    # keep the GPU busy for a moment before the timed region so clocks settle
+    # a short busy period before the timed region so clocks settle
     with torch.cuda.stream(stream):
-        for _ in range(max(1, int(0.3 / max(1e-6, G * 10e-6)))):
+        for _ in range(20):
             g_full.replay()
     torch.cuda.synchronize()
 
