@@ -124,12 +124,16 @@ int span_bytes(const rz_plan_s &p, int fam, int C, int dx0, int dx1)
     return hi - lo;
 }
 
-int max_slot_bytes(const rz_plan_s &p, int fam, int C, int TW)
+// Bytes reserved per staged row: the widest span, plus 16 bytes of padding
+// for the uint8 bilinear kernels, whose 32-bit tap reads may run up to 11
+// bytes past a span (onto taps of weight 0).  `pad` = false for the exact 2x
+// path, which reads only inside each span.
+int max_slot_bytes(const rz_plan_s &p, int fam, int C, int TW, bool pad = true)
 {
     int m = 0;
     for (int dx0 = 0; dx0 < p.OW; dx0 += TW)
         m = std::max(m, span_bytes(p, fam, C, dx0, std::min(dx0 + TW, p.OW)));
-    return m;
+    return m + (pad ? rz::fam_slot_pad(fam) : 0);
 }
 
 // Largest number of distinct source rows a tile of TR output rows stages,
@@ -154,14 +158,14 @@ int max_tile_rows(const rz_plan_s &p, int fam, int TR)
     return m;
 }
 
-bool eval_tile(const rz_plan_s &p, int fam, int C, int TR, int TW, int stages, TileCfg *out)
+bool eval_tile(const rz_plan_s &p, int fam, int C, int TR, int TW, int stages, TileCfg *out, bool pad = true)
 {
     TileCfg t;
     t.TR = std::max(1, std::min(TR, p.OH));
     t.TW = std::max(1, std::min(TW, p.OW));
     t.tiles_x = (p.OW + t.TW - 1) / t.TW;
     t.tiles_y = (p.OH + t.TR - 1) / t.TR;
-    t.slot_bytes = max_slot_bytes(p, fam, C, t.TW);
+    t.slot_bytes = max_slot_bytes(p, fam, C, t.TW, pad);
     t.max_rows = max_tile_rows(p, fam, t.TR);
     t.stages = stages;
     const SmemLayout L = rz::smem_layout(fam, C, t.TR, t.TW, t.max_rows, t.slot_bytes, stages);
@@ -215,7 +219,7 @@ TileCfg choose_tile(const rz_plan_s &p, int fam, int C, int batch, int stages, b
         // rows, one contiguous span) per tile and a ring of two tiles measured
         // best for 4K -> 1080p RGB (8.9 us against 10.4 us for one-row tiles)
         TileCfg t;
-        if (max_slot_bytes(p, fam, C, p.OW) <= 24576 && eval_tile(p, fam, C, 2, p.OW, stages, &t) &&
+        if (max_slot_bytes(p, fam, C, p.OW, false) <= 24576 && eval_tile(p, fam, C, 2, p.OW, stages, &t, false) &&
             t.smem <= static_cast<size_t>(rz::kMaxSmem) / 2)
             return t;
     }

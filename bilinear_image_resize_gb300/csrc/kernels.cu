@@ -78,15 +78,18 @@ __device__ __forceinline__ bool consumer_any(bool v)
     return r != 0;
 }
 
+// One bounded wait attempt: the thread may be suspended in hardware until the
+// phase completes or about 0.5 ms pass (suspend-time hint), so waiting warps
+// do not spin through issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(500000u)
         : "memory");
     return ok != 0;
 }
@@ -396,8 +399,57 @@ __device__ __forceinline__ StageView stage_view(const KArgs &a, const SmemLayout
     return v;
 }
 
-// Generic bilinear / nearest, any ratio.  Pixel-per-thread gather from the
-// staged rows; uint8 bilinear is
+// uint8 bilinear of one output pixel from two staged rows.  `o0` is the
+// byte offset (within the staged rows) of the left tap's first channel; the
+// right tap follows C bytes later (at the right image edge the plan gives the
+// right tap weight 0, and the bytes read past the row are padding, so the
+// product is 0).  The 2C tap bytes of each row are fetched as 32-bit words,
+// each channel's pair (left, right) is gathered into one 16-bit lane with a
+// byte permute, and dp2a forms A0 * left + A1 * right exactly in int32:
+//   q = (B0 hT + B1 hB + 2^21) >> 22.
+template <int C>
+__device__ __forceinline__ void bilinear_u8_px(const uint8_t *top, const uint8_t *bot, int o0, uint32_t aw, int B0,
+                                               int B1, int (&q)[C])
+{
+    const uint8_t *rowp[2] = {top, bot};
+    int h[2][C];
+#pragma unroll
+    for (int r = 0; r < 2; r++) {
+        if constexpr (C == 4) {
+            const uint32_t t0 = *reinterpret_cast<const uint32_t *>(rowp[r] + o0);
+            const uint32_t t1 = *reinterpret_cast<const uint32_t *>(rowp[r] + o0 + 4);
+            const uint32_t p01 = __byte_perm(t0, t1, 0x5140);   // c0 pair, c1 pair
+            const uint32_t p23 = __byte_perm(t0, t1, 0x7362);   // c2 pair, c3 pair
+            h[r][0] = static_cast<int>(__dp2a_lo(aw, p01, 0u));
+            h[r][1] = static_cast<int>(__dp2a_hi(aw, p01, 0u));
+            h[r][2] = static_cast<int>(__dp2a_lo(aw, p23, 0u));
+            h[r][3] = static_cast<int>(__dp2a_hi(aw, p23, 0u));
+        } else {
+            const int base = o0 & ~3;
+            const uint32_t sel = 0x3210u + 0x1111u * static_cast<uint32_t>(o0 & 3);
+            const uint32_t *w = reinterpret_cast<const uint32_t *>(rowp[r] + base);
+            const uint32_t w0 = w[0], w1 = w[1];
+            const uint32_t lo4 = __byte_perm(w0, w1, sel);      // bytes o0 .. o0+3
+            if constexpr (C == 1) {
+                h[r][0] = static_cast<int>(__dp2a_lo(aw, lo4, 0u));
+            } else {
+                const uint32_t hi4 = __byte_perm(w1, w[2], sel);  // bytes o0+4 .. o0+7
+                const uint32_t p01 = __byte_perm(lo4, hi4, 0x4130);  // t0c0 t1c0 t0c1 t1c1
+                const uint32_t p2 = __byte_perm(lo4, hi4, 0x0052);   // t0c2 t1c2
+                h[r][0] = static_cast<int>(__dp2a_lo(aw, p01, 0u));
+                h[r][1] = static_cast<int>(__dp2a_hi(aw, p01, 0u));
+                h[r][2] = static_cast<int>(__dp2a_lo(aw, p2, 0u));
+            }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < C; c++)
+        q[c] = (B0 * h[0][c] + B1 * h[1][c] + (1 << 21)) >> 22;
+}
+
+// Generic bilinear / nearest, any ratio.  Each thread takes four output
+// pixels of a row per step (stride = threads per row) so that their table
+// and shared-memory loads are in flight together; uint8 bilinear is
 //   out = (B0 (A0 t0 + A1 t1) + B1 (A0 b0 + A1 b1) + 2^21) >> 22
 // with A1 = 11-bit weight of the right tap, B1 of the lower row — exact in
 // int32 (at most 2048 * 2048 * 255 + 2^21 < 2^31).
@@ -406,39 +458,49 @@ __device__ void compute_generic(const KArgs &a, const StageView &sv, const TileG
                                 int orow_bytes)
 {
     constexpr int ES = sizeof(T);
+    constexpr int U = 4;
     const T *slots = reinterpret_cast<const T *>(sv.slots);
     T *ob = reinterpret_cast<T *>(ob_bytes);
     const int lo = sv.b_lo / ES;
     const int slot_el = sv.slot_bytes / ES;
     const int orow_el = orow_bytes / ES;
     const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
-    const int lg = min(8, ceil_log2(nc));
+    const int lg = min(8, ceil_log2((nc + U - 1) / U));
     const int tpr = 1 << lg, rpp = kConsumers >> lg;
     for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
         const int2 yw = __ldg(&a.yt[g.dy0 + rl]);
-        const T *top = slots + sv.map[2 * rl] * slot_el - lo;
-        const T *bot = slots + sv.map[2 * rl + 1] * slot_el - lo;
+        const T *top = slots + sv.map[2 * rl] * slot_el;       // element 0 = source element lo
+        const T *bot = slots + sv.map[2 * rl + 1] * slot_el;
         T *orow = ob + rl * orow_el;
-        for (int cl = threadIdx.x & (tpr - 1); cl < nc; cl += tpr) {
-            const int2 xw = __ldg(&a.xt[g.dx0 + cl]);
-            const int o0 = xw.x * C;
-            if (!LINEAR) {
+        for (int c0 = threadIdx.x & (tpr - 1); c0 < nc; c0 += U * tpr) {
+            int2 xw[U];
 #pragma unroll
-                for (int c = 0; c < C; c++)
-                    orow[cl * C + c] = top[o0 + c];
-            } else {
-                const int o1 = min(xw.x + 1, a.W - 1) * C;
-                if constexpr (ES == 1) {
-                    const int A1 = xw.y, A0 = 2048 - A1;
-                    const int B1 = yw.y, B0 = 2048 - B1;
+            for (int k = 0; k < U; k++) {
+                const int cl = c0 + k * tpr;
+                xw[k] = cl < nc ? __ldg(&a.xt[g.dx0 + cl]) : make_int2(0, 0);
+            }
 #pragma unroll
-                    for (int c = 0; c < C; c++) {
-                        const int hT = A0 * top[o0 + c] + A1 * top[o1 + c];
-                        const int hB = A0 * bot[o0 + c] + A1 * bot[o1 + c];
-                        orow[cl * C + c] = static_cast<T>((B0 * hT + B1 * hB + (1 << 21)) >> 22);
-                    }
+            for (int k = 0; k < U; k++) {
+                const int cl = c0 + k * tpr;
+                if (cl >= nc)
+                    break;
+                const int o0 = xw[k].x * C - lo;
+                if (!LINEAR) {
+#pragma unroll
+                    for (int c = 0; c < C; c++)
+                        orow[cl * C + c] = top[o0 + c];
+                } else if constexpr (ES == 1) {
+                    const uint32_t aw =
+                        static_cast<uint32_t>(2048 - xw[k].y) | (static_cast<uint32_t>(xw[k].y) << 16);
+                    int q[C];
+                    bilinear_u8_px<C>(reinterpret_cast<const uint8_t *>(top), reinterpret_cast<const uint8_t *>(bot),
+                                      o0, aw, 2048 - yw.y, yw.y, q);
+#pragma unroll
+                    for (int c = 0; c < C; c++)
+                        orow[cl * C + c] = static_cast<T>(q[c]);
                 } else {
-                    const float u = __int_as_float(xw.y), v = __int_as_float(yw.y);
+                    const int o1 = min(xw[k].x + 1, a.W - 1) * C - lo;
+                    const float u = __int_as_float(xw[k].y), v = __int_as_float(yw.y);
 #pragma unroll
                     for (int c = 0; c < C; c++) {
                         const float t0 = top[o0 + c], t1 = top[o1 + c];
@@ -564,32 +626,41 @@ __device__ void compute_down2(const KArgs &a, const StageView &sv, const TileGeo
 }
 
 // Bilinear + normalise: the uint8 result q of the generic sum, then
-// y = q * scale[c] + shift[c] written planar.
+// y = q * scale[c] + shift[c] written planar.  Four pixels per thread step.
 template <int C>
 __device__ void compute_normalize(const KArgs &a, const StageView &sv, const TileGeom &g, uint8_t *ob_bytes,
                                   int orow_bytes)
 {
+    constexpr int U = 4;
     float *ob = reinterpret_cast<float *>(ob_bytes);
     const int orow_el = orow_bytes / 4;
     const int plane_el = a.TR * orow_el;
     const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
-    const int lg = min(8, ceil_log2(nc));
+    const int lg = min(8, ceil_log2((nc + U - 1) / U));
     const int tpr = 1 << lg, rpp = kConsumers >> lg;
     for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
         const int2 yw = __ldg(&a.yt[g.dy0 + rl]);
         const int B1 = yw.y, B0 = 2048 - B1;
-        const uint8_t *top = sv.slots + sv.map[2 * rl] * sv.slot_bytes - sv.b_lo;
-        const uint8_t *bot = sv.slots + sv.map[2 * rl + 1] * sv.slot_bytes - sv.b_lo;
-        for (int cl = threadIdx.x & (tpr - 1); cl < nc; cl += tpr) {
-            const int2 xw = __ldg(&a.xt[g.dx0 + cl]);
-            const int o0 = xw.x * C, o1 = min(xw.x + 1, a.W - 1) * C;
-            const int A1 = xw.y, A0 = 2048 - A1;
+        const uint8_t *top = sv.slots + sv.map[2 * rl] * sv.slot_bytes;
+        const uint8_t *bot = sv.slots + sv.map[2 * rl + 1] * sv.slot_bytes;
+        for (int c0 = threadIdx.x & (tpr - 1); c0 < nc; c0 += U * tpr) {
+            int2 xw[U];
 #pragma unroll
-            for (int c = 0; c < C; c++) {
-                const int hT = A0 * top[o0 + c] + A1 * top[o1 + c];
-                const int hB = A0 * bot[o0 + c] + A1 * bot[o1 + c];
-                const int q = (B0 * hT + B1 * hB + (1 << 21)) >> 22;
-                ob[c * plane_el + rl * orow_el + cl] = fmaf(static_cast<float>(q), a.scale[c], a.shift[c]);
+            for (int k = 0; k < U; k++) {
+                const int cl = c0 + k * tpr;
+                xw[k] = cl < nc ? __ldg(&a.xt[g.dx0 + cl]) : make_int2(0, 0);
+            }
+#pragma unroll
+            for (int k = 0; k < U; k++) {
+                const int cl = c0 + k * tpr;
+                if (cl >= nc)
+                    break;
+                const uint32_t aw = static_cast<uint32_t>(2048 - xw[k].y) | (static_cast<uint32_t>(xw[k].y) << 16);
+                int q[C];
+                bilinear_u8_px<C>(top, bot, xw[k].x * C - sv.b_lo, aw, B0, B1, q);
+#pragma unroll
+                for (int c = 0; c < C; c++)
+                    ob[c * plane_el + rl * orow_el + cl] = fmaf(static_cast<float>(q[c]), a.scale[c], a.shift[c]);
             }
         }
     }
@@ -597,7 +668,10 @@ __device__ void compute_normalize(const KArgs &a, const StageView &sv, const Til
 
 // Bilinear + 3x3: resized float values of the tile and a one-pixel ring
 // (rows and columns clamped into the output grid: replicate border) go to
-// `mid`; then z = sum w[i*3+j] * mid[row+i][col+j].
+// `mid`; then z = sum w[i*3+j] * mid[row+i][col+j].  Both phases walk a
+// flattened index space so every consumer thread has work; the second phase
+// gives each thread four vertically adjacent outputs of one column, whose
+// 3x3 windows share their rows in registers (18 shared loads for 4 outputs).
 template <int C>
 __device__ void compute_filter3x3(const KArgs &a, const StageView &sv, const TileGeom &g, uint8_t *ob_bytes,
                                   int orow_bytes, float *mid)
@@ -611,45 +685,70 @@ __device__ void compute_filter3x3(const KArgs &a, const StageView &sv, const Til
     const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
     {
         const int hr = nr + 2, hc = nc + 2;
-        const int lg = min(8, ceil_log2(hc));
-        const int tpr = 1 << lg, rpp = kConsumers >> lg;
-        for (int k = threadIdx.x >> lg; k < hr; k += rpp) {
+        const int total = hr * hc;
+        const int step_k = kConsumers / hc, step_j = kConsumers - step_k * hc;
+        int k = threadIdx.x / hc, j = threadIdx.x - k * hc;
+        for (int e = threadIdx.x; e < total; e += kConsumers) {
             const int dy = clampi(g.dy0 - 1 + k, 0, a.OH - 1);
             const float v = __int_as_float(__ldg(&a.yt[dy]).y);
             const float *top = slots + sv.map[2 * k] * slot_el - lo;
             const float *bot = slots + sv.map[2 * k + 1] * slot_el - lo;
-            for (int j = threadIdx.x & (tpr - 1); j < hc; j += tpr) {
-                const int dx = clampi(g.dx0 - 1 + j, 0, a.OW - 1);
-                const int2 xw = __ldg(&a.xt[dx]);
-                const float u = __int_as_float(xw.y);
-                const int o0 = xw.x * C, o1 = min(xw.x + 1, a.W - 1) * C;
+            const int dx = clampi(g.dx0 - 1 + j, 0, a.OW - 1);
+            const int2 xw = __ldg(&a.xt[dx]);
+            const float u = __int_as_float(xw.y);
+            const int o0 = xw.x * C, o1 = min(xw.x + 1, a.W - 1) * C;
 #pragma unroll
-                for (int c = 0; c < C; c++) {
-                    const float t0 = top[o0 + c], t1 = top[o1 + c];
-                    const float b0 = bot[o0 + c], b1 = bot[o1 + c];
-                    const float hT = fmaf(u, t1 - t0, t0);
-                    const float hB = fmaf(u, b1 - b0, b0);
-                    mid[(k * mid_w + j) * C + c] = fmaf(v, hB - hT, hT);
-                }
+            for (int c = 0; c < C; c++) {
+                const float t0 = top[o0 + c], t1 = top[o1 + c];
+                const float b0 = bot[o0 + c], b1 = bot[o1 + c];
+                const float hT = fmaf(u, t1 - t0, t0);
+                const float hB = fmaf(u, b1 - b0, b0);
+                mid[(k * mid_w + j) * C + c] = fmaf(v, hB - hT, hT);
+            }
+            j += step_j;
+            k += step_k;
+            if (j >= hc) {
+                j -= hc;
+                k += 1;
             }
         }
     }
     consumer_sync();
     {
-        const int lg = min(8, ceil_log2(nc));
-        const int tpr = 1 << lg, rpp = kConsumers >> lg;
-        for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
-            for (int cl = threadIdx.x & (tpr - 1); cl < nc; cl += tpr) {
+        constexpr int R = 4;                       // outputs per thread, down one column
+        const int groups = (nr + R - 1) / R;
+        const int total = groups * nc;
+        const int step_q = kConsumers / nc, step_c = kConsumers - step_q * nc;
+        int q = threadIdx.x / nc, cl = threadIdx.x - q * nc;
+        for (int e = threadIdx.x; e < total; e += kConsumers) {
+            const int r0 = q * R;
+            const int rows = min(R, nr - r0);
 #pragma unroll
-                for (int c = 0; c < C; c++) {
-                    float z = 0.0f;
+            for (int c = 0; c < C; c++) {
+                float win[R + 2][3];
 #pragma unroll
-                    for (int i = 0; i < 3; i++)
+                for (int i = 0; i < R + 2; i++)
 #pragma unroll
-                        for (int j = 0; j < 3; j++)
-                            z = fmaf(a.w[i * 3 + j], mid[((rl + i) * mid_w + (cl + j)) * C + c], z);
-                    ob[rl * orow_el + cl * C + c] = z;
+                    for (int jj = 0; jj < 3; jj++)
+                        win[i][jj] = (i < rows + 2) ? mid[((r0 + i) * mid_w + (cl + jj)) * C + c] : 0.0f;
+#pragma unroll
+                for (int r = 0; r < R; r++) {
+                    if (r < rows) {
+                        float z = 0.0f;
+#pragma unroll
+                        for (int i = 0; i < 3; i++)
+#pragma unroll
+                            for (int jj = 0; jj < 3; jj++)
+                                z = fmaf(a.w[i * 3 + jj], win[r + i][jj], z);
+                        ob[(r0 + r) * orow_el + cl * C + c] = z;
+                    }
                 }
+            }
+            cl += step_c;
+            q += step_q;
+            if (cl >= nc) {
+                cl -= nc;
+                q += 1;
             }
         }
     }
@@ -727,9 +826,13 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a)
         // the output buffer is free once the store issued two tiles ago has read it
         if (threadIdx.x == 0 && it >= 2)
             bulk_wait_read<1>();
-        const bool ok = mbar_wait_bounded(&full[s], (it / NS) & 1, a.status);
-        // all consumers leave together if any timed out (the header is only
-        // read once the stage is known to be full)
+        // one consumer thread waits for the stage (acquiring the bulk-copied
+        // bytes); the other warps wait in the hardware barrier, which issues
+        // nothing, and leave it ordered after that thread's acquire.  All
+        // consumers leave the loop together if the wait timed out.
+        bool ok = true;
+        if (threadIdx.x == 0)
+            ok = mbar_wait_bounded(&full[s], (it / NS) & 1, a.status);
         if (consumer_any(!ok) || reinterpret_cast<const StageHdr *>(st)->nrows < 0) {
             failed = true;
             break;

@@ -143,7 +143,7 @@ extern "C" int resize_u8_noalloc(const uint8_t *src, size_t src_pitch, uint8_t *
             span = std::max(span, (((xs1 + 1) * C + 15) & ~15) - ((xs0 * C) & ~15));
         }
         TW = w;
-        slot_bytes = span;
+        slot_bytes = span + rz::fam_slot_pad(rz::FAM_U8);
         if (span <= 16384 && w * C <= 16384) break;
     }
     // the kernel: the exact 2x path when every table entry is the 2x pattern

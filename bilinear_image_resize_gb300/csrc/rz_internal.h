@@ -26,6 +26,9 @@ __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / 
 __host__ __device__ constexpr int fam_in_es(int fam) { return (fam == FAM_U8 || fam == FAM_NORM) ? 1 : 4; }
 __host__ __device__ constexpr int fam_out_es(int fam) { return fam == FAM_U8 ? 1 : 4; }
 __host__ __device__ constexpr int fam_halo(int fam) { return fam == FAM_FILT ? 1 : 0; }
+// Padding after each staged row: the uint8 bilinear tap reads are 32-bit
+// words and may pass the end of a row's span by up to 11 bytes.
+__host__ __device__ constexpr int fam_slot_pad(int fam) { return (fam == FAM_U8 || fam == FAM_NORM) ? 16 : 0; }
 
 // Byte offsets of the pieces of a CTA's dynamic shared memory.  Host and
 // device compute them with this one function.
