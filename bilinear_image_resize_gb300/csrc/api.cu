@@ -81,9 +81,31 @@ void axis_nearest(int n_in, int n_out, int32_t *ofs)
 
 struct TileCfg {
     int TR = 0, TW = 0, tiles_x = 0, tiles_y = 0, max_rows = 0, slot_bytes = 0, stages = 0, variant = 0;
+    int tensor = 0, box_granules = 0, box_rows = 0;   // tensor-map staging (one box per tile)
     size_t smem = 0;
     int grid = 0;
 };
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime (the
+// library links no driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tensor_encoder()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
 
 }  // namespace
 
@@ -158,15 +180,45 @@ int max_tile_rows(const rz_plan_s &p, int fam, int TR)
     return m;
 }
 
+// Largest source row range (last row - first row + 1) a tile samples: the
+// height of the box that stages a tile with one tensor-map copy.
+int max_tile_row_range(const rz_plan_s &p, int fam, int TR)
+{
+    const int halo = rz::fam_halo(fam);
+    const bool lin = p.mode == RZ_LINEAR;
+    int m = 0;
+    for (int dy0 = 0; dy0 < p.OH; dy0 += TR) {
+        const int dy1 = std::min(dy0 + TR, p.OH);
+        const int first = p.yofs[std::clamp(dy0 - halo, 0, p.OH - 1)];
+        const int rl = p.yofs[std::clamp(dy1 - 1 + halo, 0, p.OH - 1)];
+        const int last = lin ? std::min(rl + 1, p.H - 1) : rl;
+        m = std::max(m, last - first + 1);
+    }
+    return m;
+}
+
 bool eval_tile(const rz_plan_s &p, int fam, int C, int TR, int TW, int stages, TileCfg *out, bool pad = true)
 {
     TileCfg t;
+    if (fam == rz::FAM_FILT)
+        TW = std::min(TW, 240);   // eight warps x 30 columns per tile
     t.TR = std::max(1, std::min(TR, p.OH));
     t.TW = std::max(1, std::min(TW, p.OW));
     t.tiles_x = (p.OW + t.TW - 1) / t.TW;
     t.tiles_y = (p.OH + t.TR - 1) / t.TR;
     t.slot_bytes = max_slot_bytes(p, fam, C, t.TW, pad);
     t.max_rows = max_tile_rows(p, fam, t.TR);
+    if (fam == rz::FAM_FILT) {
+        // the 3x3 tiles are narrow and tall: stage each with one tensor-map
+        // box when it fits the box limits (256 granules by 256 rows)
+        const int range = max_tile_row_range(p, fam, t.TR);
+        if (t.slot_bytes / 16 <= 256 && range <= 256) {
+            t.tensor = 1;
+            t.box_granules = t.slot_bytes / 16;
+            t.box_rows = range;
+            t.max_rows = std::max(t.max_rows, range);
+        }
+    }
     t.stages = stages;
     const SmemLayout L = rz::smem_layout(fam, C, t.TR, t.TW, t.max_rows, t.slot_bytes, stages);
     t.smem = static_cast<size_t>(L.total);
@@ -176,7 +228,7 @@ bool eval_tile(const rz_plan_s &p, int fam, int C, int TR, int TW, int stages, T
 
 constexpr int kSms = 152;                // GB300; the launch itself asks the device
 constexpr int kSoftSmem = 48 * 1024;     // keeps several CTAs resident per SM
-constexpr int kFilterSmem = 96 * 1024;   // the 3x3 tile trades occupancy for less halo
+constexpr int kFilterSmem = 112 * 1024;  // two CTAs per SM for the 3x3 epilogue
 constexpr int kDefaultStages = 2;
 
 // True when the plan is an exact 2x downscale on both axes: every column and
@@ -203,14 +255,17 @@ TileCfg choose_tile(const rz_plan_s &p, int fam, int C, int batch, int stages, b
     const int px_bytes = fam == rz::FAM_NORM ? 4 : C * out_es;
     TileCfg best;
     if (fam == rz::FAM_FILT) {
-        for (int TW : {128, 64, 32, 16, 8, 4, 2, 1})
-            for (int TR : {32, 16, 8, 4, 2, 1}) {
-                TileCfg t;
-                if (eval_tile(p, fam, C, TR, TW, stages, &t) && t.smem <= static_cast<size_t>(kFilterSmem))
-                    return t;
-            }
-        for (int TW : {16, 8, 4, 2, 1})
-            if (eval_tile(p, fam, C, 1, TW, 1, &best)) return best;
+        // the kernel's eight consumer warps emit 30 columns each: tiles are
+        // 240 columns wide (the whole output when narrower), as many rows as
+        // keep two CTAs per SM
+        const int TW = std::min(p.OW, 240);
+        for (int TR : {32, 24, 16, 8, 4, 2, 1}) {
+            TileCfg t;
+            if (eval_tile(p, fam, C, TR, TW, stages, &t) && t.smem <= static_cast<size_t>(kFilterSmem))
+                return t;
+        }
+        for (int TR : {4, 2, 1})
+            if (eval_tile(p, fam, C, TR, TW, 1, &best)) return best;
         return best;
     }
     if (down2) {
@@ -407,8 +462,28 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     a.xt = fl ? p->d_xf : p->d_xq;
     a.yt = fl ? p->d_yf : p->d_yq;
     a.status = p->d_status;
+    CUtensorMap tmap;
+    std::memset(&tmap, 0, sizeof(tmap));
+    a.tensor_in = 0;
+    if (t.tensor && a.tma_in) {
+        // the image as {16-byte granule, granules per row, rows, images}
+        EncodeTiledFn enc = tensor_encoder();
+        const cuuint64_t dims[4] = {16, in_row / 16, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(batch)};
+        const cuuint64_t bstride = batch > 1 ? a.src_bstride : static_cast<long long>(src_pitch) * H;
+        const cuuint64_t strides[3] = {16, static_cast<cuuint64_t>(src_pitch), bstride};
+        const cuuint32_t box[4] = {16, static_cast<cuuint32_t>(t.box_granules), static_cast<cuuint32_t>(t.box_rows),
+                                   1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (enc && enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(src), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+            a.tensor_in = 1;
+            a.box_granules = t.box_granules;
+            a.box_rows = t.box_rows;
+        }
+    }
     if (!do_launch) return RZ_OK;
-    const int e = rz::launch_resize(fn, a, t.grid, t.smem, p->opt_pdl != 0, stream);
+    const int e = rz::launch_resize(fn, a, tmap, t.grid, t.smem, p->opt_pdl != 0, stream);
     if (e != 0) return cuda_fail(static_cast<cudaError_t>(e));
     return RZ_OK;
 }
@@ -463,8 +538,12 @@ int resize_plan_create(rz_plan *out, int in_h, int in_w, int out_h, int out_w, i
 
     // one device block: x tables (q11 and float weights), y tables, status word
     const size_t nx = static_cast<size_t>(out_w), ny = static_cast<size_t>(out_h);
-    const size_t off_xf = nx * sizeof(int2), off_yq = 2 * off_xf, off_yf = off_yq + ny * sizeof(int2);
-    const size_t off_st = off_yf + ny * sizeof(int2);
+    // each table starts on a 16-byte boundary and is followed by at least
+    // four spare entries, so kernels may read entries in 16-byte pairs
+    const size_t xbytes = ((nx + 4) * sizeof(int2) + 15) & ~size_t(15);
+    const size_t ybytes = ((ny + 4) * sizeof(int2) + 15) & ~size_t(15);
+    const size_t off_xf = xbytes, off_yq = 2 * xbytes, off_yf = off_yq + ybytes;
+    const size_t off_st = off_yf + ybytes;
     const size_t total = off_st + 16;
     std::vector<uint8_t> host(total, 0);
     int2 *hxq = reinterpret_cast<int2 *>(host.data()), *hxf = reinterpret_cast<int2 *>(host.data() + off_xf);

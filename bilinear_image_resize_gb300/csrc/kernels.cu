@@ -55,6 +55,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
@@ -101,19 +107,26 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-// Wait for phase `parity` of the barrier, at most kWaitLimitNs.  On time-out
-// the status word (if given) records RZ_ERR_TIMEOUT and false is returned.
+// Wait for phase `parity` of the barrier, at most kWaitLimitNs.  Between
+// attempts the waiting warp sleeps (32 ns, doubling up to 256 ns) so that it
+// leaves the issue slots to the warps computing on the same scheduler.  On
+// time-out the status word (if given) records RZ_ERR_TIMEOUT and false is
+// returned.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = global_ns();
+    unsigned int nap = 32;
     while (!mbar_try_wait(bar, parity)) {
         if (global_ns() - t0 > kWaitLimitNs) {
             if (status)
                 atomicExch(status, RZ_ERR_TIMEOUT);
             return false;
         }
+        __nanosleep(nap);
+        if (nap < 256)
+            nap <<= 1;
     }
     return true;
 }
@@ -128,6 +141,21 @@ __device__ __forceinline__ void bulk_load_hint(void *sdst, const void *gsrc, uin
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
         "%4;" ::"r"(smem_addr(sdst)),
         "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Tensor-map copy of one box {16 bytes, granules, rows, 1} at coordinates
+// {0, granule, row, image} into shared memory, completing on `bar`.  The
+// innermost coordinate is 0, so the copy starts on a 16-byte boundary; parts
+// of the box outside the image are zero-filled, not read.
+__device__ __forceinline__ void tensor_load_4d(void *sdst, const CUtensorMap *map, int granule, int row, int image,
+                                               uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(sdst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(granule), "r"(row), "r"(image), "r"(smem_addr(bar)),
+        "l"(policy)
         : "memory");
 }
 
@@ -231,7 +259,10 @@ struct StageHdr {
     int nrows;   // staged rows (-1: tile rejected)
     int b_lo;    // byte offset, within a source row, of slot byte 0
     int nbytes;  // bytes staged per row
-    int pad;
+    int tile;    // tile index
+    int row0;    // first staged source row (tensor-map staging)
+    int image;   // image index within the batch
+    int pad[2];
 };
 
 // Producer warp, part 1 (no global memory access): list the source rows of
@@ -299,13 +330,28 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, int
             map[2 * k + 1] = s1;
         }
     }
+    int row0 = 0;
+    if (a.tensor_in && !overflow && n > 0) {
+        // one box holds the whole row range: slot = row - first row
+        __syncwarp();
+        row0 = rows[0];
+        const int range = rows[n - 1] - row0 + 1;
+        if (range > a.box_rows)
+            overflow = true;
+        else if (lane == 0)
+            for (int k = 0; k < 2 * nrc; k++)
+                map[k] = rows[map[k]] - row0;
+        n = range;
+    }
     if (lane == 0) {
-        // the host sizes max_rows and slot_bytes from the same indices, so an
-        // overflow is unreachable; it guards shared memory all the same
+        // the host sizes max_rows, slot_bytes and the box from the same
+        // indices, so an overflow is unreachable; it guards shared memory
         h->nrows = overflow ? -1 : n;
         h->b_lo = b_lo;
         h->nbytes = nbytes;
-        h->pad = tile;
+        h->tile = tile;
+        h->row0 = row0;
+        h->image = tile / (a.tiles_x * a.tiles_y);
     }
     __syncwarp();
 }
@@ -314,24 +360,92 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, int
 // `full` with the byte count before any copy is issued, and the copies are
 // spread over the lanes.  Plain path (unaligned source): the lanes copy the
 // bytes and each arrives on `full` (initialised for 32 arrivals).
-__device__ void fetch_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, uint64_t *full, uint64_t policy)
+__device__ void fetch_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, uint64_t *full, uint64_t policy,
+                            const CUtensorMap *tmap, bool tables, int halo)
 {
     const int lane = threadIdx.x & 31;
     const StageHdr *h = reinterpret_cast<const StageHdr *>(st);
     const int *rows = reinterpret_cast<const int *>(st + L.rows_off);
     uint8_t *slots = st + L.slots_off;
-    const TileGeom g = tile_geom(a, h->pad);
+    const TileGeom g = tile_geom(a, h->tile);
     const int n = h->nrows, nbytes = h->nbytes, b_lo = h->b_lo;
     if (n < 0 && lane == 0)
         atomicExch(a.status, RZ_ERR_ARG);
-    if (a.tma_in) {
+    if (tables) {
+        // bytes first (armed without arriving), then the table entries, then
+        // the one arrival: the stage completes with copies and tables in place
+        if (a.tensor_in) {
+            if (lane == 0 && n > 0) {
+                mbar_expect_tx(full, static_cast<uint32_t>(a.box_rows * a.box_granules * 16));
+                tensor_load_4d(slots, tmap, b_lo / 16, h->row0, h->image, full, policy);
+            }
+        } else if (a.tma_in) {
+            if (lane == 0 && n > 0)
+                mbar_expect_tx(full, static_cast<uint32_t>(n * nbytes));
+            __syncwarp();
+            for (int r = lane; r < n; r += 32)
+                bulk_load_hint(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch + b_lo,
+                               static_cast<uint32_t>(nbytes), full, policy);
+        } else {
+            for (int r = 0; r < n; r++) {
+                const uint8_t *src = g.src + (long long)rows[r] * a.src_pitch + b_lo;
+                uint8_t *d = slots + r * a.slot_bytes;
+                for (int k = lane; k < nbytes; k += 32)
+                    d[k] = __ldg(src + k);
+            }
+        }
+        // x entries of the computed columns dx0 - halo .. (clamped into the
+        // tile's staged span), y entries of the computed rows (clamped)
+        int2 *tx = reinterpret_cast<int2 *>(st + L.tab_off);
+        int2 *ty = tx + tab_x_entries(a.TW, halo);
+        const int nx = (g.dx1 - g.dx0) + 2 * halo, ny = (g.dy1 - g.dy0) + 2 * halo;
+        const int xhi = min(g.dx1 - 1 + halo, a.OW - 1);
+        for (int k = lane; k < nx; k += 32)
+            tx[k] = __ldg(&a.xt[clampi(g.dx0 - halo + k, 0, xhi)]);
+        for (int k = lane; k < ny; k += 32)
+            ty[k] = __ldg(&a.yt[clampi(g.dy0 - halo + k, 0, a.OH - 1)]);
+        __syncwarp();
+        if (a.tma_in || a.tensor_in) {
+            if (lane == 0)
+                mbar_arrive(full);
+        } else {
+            mbar_arrive(full);   // 32 arrivals: each lane releases its own writes
+        }
+    } else if (a.tensor_in) {
+        // one tensor-map copy of the box {granules x box_rows} at the tile's
+        // first row; the box is what the barrier counts, whatever part of it
+        // the tile uses
+        if (lane == 0) {
+            const uint32_t box = static_cast<uint32_t>(a.box_rows * a.box_granules * 16);
+            mbar_arrive_expect_tx(full, n > 0 ? box : 0u);
+            if (n > 0)
+                tensor_load_4d(slots, tmap, b_lo / 16, h->row0, h->image, full, policy);
+        }
+    } else if (a.tma_in) {
         // a rejected tile completes the phase with no bytes
         if (lane == 0)
             mbar_arrive_expect_tx(full, static_cast<uint32_t>(n > 0 ? n * nbytes : 0));
         __syncwarp();
-        for (int r = lane; r < n; r += 32)
-            bulk_load_hint(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch + b_lo,
-                           static_cast<uint32_t>(nbytes), full, policy);
+        if (b_lo == 0 && nbytes == a.src_pitch && nbytes == a.slot_bytes) {
+            // whole rows that sit back to back in memory and in the slots:
+            // one bulk copy per run of consecutive source rows (a bulk copy
+            // has a fixed cost, so fewer, larger copies stream faster)
+            if (lane == 0) {
+                int r = 0;
+                while (r < n) {
+                    int e = r + 1;
+                    while (e < n && rows[e] == rows[e - 1] + 1)
+                        e++;
+                    bulk_load_hint(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch,
+                                   static_cast<uint32_t>((e - r) * nbytes), full, policy);
+                    r = e;
+                }
+            }
+        } else {
+            for (int r = lane; r < n; r += 32)
+                bulk_load_hint(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch + b_lo,
+                               static_cast<uint32_t>(nbytes), full, policy);
+        }
     } else {
         for (int r = 0; r < n; r++) {
             const uint8_t *src = g.src + (long long)rows[r] * a.src_pitch + b_lo;
@@ -386,12 +500,16 @@ __device__ void store_tail(const KArgs &a, const SmemLayout &L, const uint8_t *o
 struct StageView {
     const uint8_t *slots;
     const int *map;
+    const int2 *tx;   // staged x entries (narrow-tile families)
+    const int2 *ty;   // staged y entries (narrow-tile families)
     int b_lo, slot_bytes;
 };
 
-__device__ __forceinline__ StageView stage_view(const KArgs &a, const SmemLayout &L, const uint8_t *st)
+__device__ __forceinline__ StageView stage_view(const KArgs &a, const SmemLayout &L, const uint8_t *st, int halo)
 {
     StageView v;
+    v.tx = reinterpret_cast<const int2 *>(st + L.tab_off);
+    v.ty = v.tx + tab_x_entries(a.TW, halo);
     v.slots = st + L.slots_off;
     v.map = reinterpret_cast<const int *>(st + L.map_off);
     v.b_lo = reinterpret_cast<const StageHdr *>(st)->b_lo;
@@ -447,9 +565,18 @@ __device__ __forceinline__ void bilinear_u8_px(const uint8_t *top, const uint8_t
         q[c] = (B0 * h[0][c] + B1 * h[1][c] + (1 << 21)) >> 22;
 }
 
-// Generic bilinear / nearest, any ratio.  Each thread takes four output
-// pixels of a row per step (stride = threads per row) so that their table
-// and shared-memory loads are in flight together; uint8 bilinear is
+// Pack the low bytes of four ints into one word (first int in byte 0).
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
+{
+    return __byte_perm(__byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040),
+                       __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040), 0x5410);
+}
+
+// Generic bilinear / nearest, any ratio.  Each thread takes runs of four
+// consecutive output pixels: their column-table entries arrive in two 16-byte
+// loads (the tables are 16-byte aligned and carry spare entries past the last
+// column), and their outputs leave in 32-bit (uint8) or 128-bit (float)
+// shared-memory stores.  uint8 bilinear is
 //   out = (B0 (A0 t0 + A1 t1) + B1 (A0 b0 + A1 b1) + 2^21) >> 22
 // with A1 = 11-bit weight of the right tap, B1 of the lower row — exact in
 // int32 (at most 2048 * 2048 * 255 + 2^21 < 2^31).
@@ -458,57 +585,126 @@ __device__ void compute_generic(const KArgs &a, const StageView &sv, const TileG
                                 int orow_bytes)
 {
     constexpr int ES = sizeof(T);
-    constexpr int U = 4;
-    const T *slots = reinterpret_cast<const T *>(sv.slots);
-    T *ob = reinterpret_cast<T *>(ob_bytes);
-    const int lo = sv.b_lo / ES;
-    const int slot_el = sv.slot_bytes / ES;
-    const int orow_el = orow_bytes / ES;
+    constexpr int RUN = 4;
     const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
-    const int lg = min(8, ceil_log2((nc + U - 1) / U));
+    const int nruns = (nc + RUN - 1) / RUN;
+    const int lg = min(8, ceil_log2(nruns));
     const int tpr = 1 << lg, rpp = kConsumers >> lg;
+    const bool pair_ok = (g.dx0 & 1) == 0;   // 16-byte table loads start on an even column
     for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
         const int2 yw = __ldg(&a.yt[g.dy0 + rl]);
-        const T *top = slots + sv.map[2 * rl] * slot_el;       // element 0 = source element lo
-        const T *bot = slots + sv.map[2 * rl + 1] * slot_el;
-        T *orow = ob + rl * orow_el;
-        for (int c0 = threadIdx.x & (tpr - 1); c0 < nc; c0 += U * tpr) {
-            int2 xw[U];
+        const uint8_t *top = sv.slots + sv.map[2 * rl] * sv.slot_bytes;
+        const uint8_t *bot = sv.slots + sv.map[2 * rl + 1] * sv.slot_bytes;
+        uint8_t *orow = ob_bytes + rl * orow_bytes;
+        for (int j = threadIdx.x & (tpr - 1); j < nruns; j += tpr) {
+            const int p0 = j * RUN;
+            const int npx = min(RUN, nc - p0);
+            int2 xw[RUN];
+            if (pair_ok) {
+                const int4 v0 = __ldg(reinterpret_cast<const int4 *>(a.xt + g.dx0 + p0));
+                const int4 v1 = __ldg(reinterpret_cast<const int4 *>(a.xt + g.dx0 + p0 + 2));
+                xw[0] = make_int2(v0.x, v0.y);
+                xw[1] = make_int2(v0.z, v0.w);
+                xw[2] = make_int2(v1.x, v1.y);
+                xw[3] = make_int2(v1.z, v1.w);
+            } else {
 #pragma unroll
-            for (int k = 0; k < U; k++) {
-                const int cl = c0 + k * tpr;
-                xw[k] = cl < nc ? __ldg(&a.xt[g.dx0 + cl]) : make_int2(0, 0);
+                for (int k = 0; k < RUN; k++)
+                    xw[k] = p0 + k < nc ? __ldg(&a.xt[g.dx0 + p0 + k]) : make_int2(0, 0);
             }
+            if constexpr (ES == 1) {
+                int q[RUN][C];
 #pragma unroll
-            for (int k = 0; k < U; k++) {
-                const int cl = c0 + k * tpr;
-                if (cl >= nc)
-                    break;
-                const int o0 = xw[k].x * C - lo;
-                if (!LINEAR) {
+                for (int k = 0; k < RUN; k++) {
+                    if (k < npx) {
+                        const int o0 = xw[k].x * C - sv.b_lo;
+                        if (!LINEAR) {
 #pragma unroll
-                    for (int c = 0; c < C; c++)
-                        orow[cl * C + c] = top[o0 + c];
-                } else if constexpr (ES == 1) {
-                    const uint32_t aw =
-                        static_cast<uint32_t>(2048 - xw[k].y) | (static_cast<uint32_t>(xw[k].y) << 16);
-                    int q[C];
-                    bilinear_u8_px<C>(reinterpret_cast<const uint8_t *>(top), reinterpret_cast<const uint8_t *>(bot),
-                                      o0, aw, 2048 - yw.y, yw.y, q);
+                            for (int c = 0; c < C; c++)
+                                q[k][c] = top[o0 + c];
+                        } else {
+                            const uint32_t aw = static_cast<uint32_t>(2048 - xw[k].y) |
+                                                (static_cast<uint32_t>(xw[k].y) << 16);
+                            bilinear_u8_px<C>(top, bot, o0, aw, 2048 - yw.y, yw.y, q[k]);
+                        }
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < C; c++)
-                        orow[cl * C + c] = static_cast<T>(q[c]);
-                } else {
-                    const int o1 = min(xw[k].x + 1, a.W - 1) * C - lo;
-                    const float u = __int_as_float(xw[k].y), v = __int_as_float(yw.y);
-#pragma unroll
-                    for (int c = 0; c < C; c++) {
-                        const float t0 = top[o0 + c], t1 = top[o1 + c];
-                        const float b0 = bot[o0 + c], b1 = bot[o1 + c];
-                        const float hT = fmaf(u, t1 - t0, t0);
-                        const float hB = fmaf(u, b1 - b0, b0);
-                        orow[cl * C + c] = fmaf(v, hB - hT, hT);
+                        for (int c = 0; c < C; c++)
+                            q[k][c] = 0;
                     }
+                }
+                uint8_t *o = orow + p0 * C;
+                if (npx == RUN) {
+                    if constexpr (C == 1) {
+                        *reinterpret_cast<uint32_t *>(o) = pack4(q[0][0], q[1][0], q[2][0], q[3][0]);
+                    } else if constexpr (C == 3) {
+                        uint32_t *w = reinterpret_cast<uint32_t *>(o);
+                        w[0] = pack4(q[0][0], q[0][1], q[0][2], q[1][0]);
+                        w[1] = pack4(q[1][1], q[1][2], q[2][0], q[2][1]);
+                        w[2] = pack4(q[2][2], q[3][0], q[3][1], q[3][2]);
+                    } else {
+                        *reinterpret_cast<uint4 *>(o) = make_uint4(pack4(q[0][0], q[0][1], q[0][2], q[0][3]),
+                                                                   pack4(q[1][0], q[1][1], q[1][2], q[1][3]),
+                                                                   pack4(q[2][0], q[2][1], q[2][2], q[2][3]),
+                                                                   pack4(q[3][0], q[3][1], q[3][2], q[3][3]));
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < RUN; k++)
+                        if (k < npx)
+#pragma unroll
+                            for (int c = 0; c < C; c++)
+                                o[k * C + c] = static_cast<uint8_t>(q[k][c]);
+                }
+            } else {
+                const float *ft = reinterpret_cast<const float *>(top);
+                const float *fb = reinterpret_cast<const float *>(bot);
+                const int lo = sv.b_lo / 4;
+                const float v = __int_as_float(yw.y);
+                float r[RUN][C];
+#pragma unroll
+                for (int k = 0; k < RUN; k++) {
+                    if (k < npx) {
+                        const int o0 = xw[k].x * C - lo;
+                        if (!LINEAR) {
+#pragma unroll
+                            for (int c = 0; c < C; c++)
+                                r[k][c] = ft[o0 + c];
+                        } else {
+                            const int o1 = min(xw[k].x + 1, a.W - 1) * C - lo;
+                            const float u = __int_as_float(xw[k].y);
+#pragma unroll
+                            for (int c = 0; c < C; c++) {
+                                const float t0 = ft[o0 + c], t1 = ft[o1 + c];
+                                const float b0 = fb[o0 + c], b1 = fb[o1 + c];
+                                const float hT = fmaf(u, t1 - t0, t0);
+                                const float hB = fmaf(u, b1 - b0, b0);
+                                r[k][c] = fmaf(v, hB - hT, hT);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < C; c++)
+                            r[k][c] = 0.0f;
+                    }
+                }
+                float *o = reinterpret_cast<float *>(orow) + p0 * C;
+                if (npx == RUN) {
+                    // RUN * C floats from a 16-byte aligned start: C float4 stores
+                    float4 *o4 = reinterpret_cast<float4 *>(o);
+#pragma unroll
+                    for (int m = 0; m < C; m++) {
+                        const int e = 4 * m;
+                        o4[m] = make_float4(r[(e + 0) / C][(e + 0) % C], r[(e + 1) / C][(e + 1) % C],
+                                            r[(e + 2) / C][(e + 2) % C], r[(e + 3) / C][(e + 3) % C]);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < RUN; k++)
+                        if (k < npx)
+#pragma unroll
+                            for (int c = 0; c < C; c++)
+                                o[k * C + c] = r[k][c];
                 }
             }
         }
@@ -639,7 +835,7 @@ __device__ void compute_normalize(const KArgs &a, const StageView &sv, const Til
     const int lg = min(8, ceil_log2((nc + U - 1) / U));
     const int tpr = 1 << lg, rpp = kConsumers >> lg;
     for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
-        const int2 yw = __ldg(&a.yt[g.dy0 + rl]);
+        const int2 yw = sv.ty[rl];
         const int B1 = yw.y, B0 = 2048 - B1;
         const uint8_t *top = sv.slots + sv.map[2 * rl] * sv.slot_bytes;
         const uint8_t *bot = sv.slots + sv.map[2 * rl + 1] * sv.slot_bytes;
@@ -648,7 +844,7 @@ __device__ void compute_normalize(const KArgs &a, const StageView &sv, const Til
 #pragma unroll
             for (int k = 0; k < U; k++) {
                 const int cl = c0 + k * tpr;
-                xw[k] = cl < nc ? __ldg(&a.xt[g.dx0 + cl]) : make_int2(0, 0);
+                xw[k] = cl < nc ? sv.tx[cl] : make_int2(0, 0);
             }
 #pragma unroll
             for (int k = 0; k < U; k++) {
@@ -666,89 +862,74 @@ __device__ void compute_normalize(const KArgs &a, const StageView &sv, const Til
     }
 }
 
-// Bilinear + 3x3: resized float values of the tile and a one-pixel ring
-// (rows and columns clamped into the output grid: replicate border) go to
-// `mid`; then z = sum w[i*3+j] * mid[row+i][col+j].  Both phases walk a
-// flattened index space so every consumer thread has work; the second phase
-// gives each thread four vertically adjacent outputs of one column, whose
-// 3x3 windows share their rows in registers (18 shared loads for 4 outputs).
+// Bilinear + 3x3 filter, as a sliding window in registers.  Warp w owns
+// the output columns dx0 + 30w .. dx0 + 30w + 29; lane l resizes the column
+// dx0 + 30w + l - 1 (clamped into the output grid: replicate border), one
+// output row after another from row dy0 - 1 to dy1 (also clamped).  Each
+// lane keeps its column's last three resized rows and its two neighbours'
+// (taken with warp shuffles) in registers, so every output is nine fmaf on
+// registers:  z = sum w[i*3+j] * r[row-1+i][col-1+j].  Lanes 0 and 31 only
+// supply the neighbours of lanes 1 and 30.
 template <int C>
 __device__ void compute_filter3x3(const KArgs &a, const StageView &sv, const TileGeom &g, uint8_t *ob_bytes,
-                                  int orow_bytes, float *mid)
+                                  int orow_bytes)
 {
+    constexpr int COLS = 30;                       // output columns per warp
     const float *slots = reinterpret_cast<const float *>(sv.slots);
     float *ob = reinterpret_cast<float *>(ob_bytes);
     const int lo = sv.b_lo / 4;
     const int slot_el = sv.slot_bytes / 4;
     const int orow_el = orow_bytes / 4;
-    const int mid_w = a.TW + 2;
     const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
-    {
-        const int hr = nr + 2, hc = nc + 2;
-        const int total = hr * hc;
-        const int step_k = kConsumers / hc, step_j = kConsumers - step_k * hc;
-        int k = threadIdx.x / hc, j = threadIdx.x - k * hc;
-        for (int e = threadIdx.x; e < total; e += kConsumers) {
-            const int dy = clampi(g.dy0 - 1 + k, 0, a.OH - 1);
-            const float v = __int_as_float(__ldg(&a.yt[dy]).y);
-            const float *top = slots + sv.map[2 * k] * slot_el - lo;
-            const float *bot = slots + sv.map[2 * k + 1] * slot_el - lo;
-            const int dx = clampi(g.dx0 - 1 + j, 0, a.OW - 1);
-            const int2 xw = __ldg(&a.xt[dx]);
-            const float u = __int_as_float(xw.y);
-            const int o0 = xw.x * C, o1 = min(xw.x + 1, a.W - 1) * C;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int col = warp * COLS + lane - 1;        // output column of this lane, relative to dx0
+    if (warp * COLS >= nc)
+        return;                                    // no output column for this warp (narrow tile)
+    // the staged x entries cover columns dx0 - 1 .. dx1 (clamped); lanes past
+    // the last output column of a narrow tile reuse the last entry and emit
+    // nothing
+    const int2 xw = sv.tx[min(col + 1, nc + 1)];
+    const float u = __int_as_float(xw.y);
+    const int o0 = xw.x * C - lo, o1 = min(xw.x + 1, a.W - 1) * C - lo;
+    const bool emit = lane >= 1 && lane <= COLS && col < nc;
+    float m[3][C], l[3][C], r[3][C];               // rows k-2, k-1, k of own column and neighbours
 #pragma unroll
-            for (int c = 0; c < C; c++) {
-                const float t0 = top[o0 + c], t1 = top[o1 + c];
-                const float b0 = bot[o0 + c], b1 = bot[o1 + c];
-                const float hT = fmaf(u, t1 - t0, t0);
-                const float hB = fmaf(u, b1 - b0, b0);
-                mid[(k * mid_w + j) * C + c] = fmaf(v, hB - hT, hT);
-            }
-            j += step_j;
-            k += step_k;
-            if (j >= hc) {
-                j -= hc;
-                k += 1;
-            }
+    for (int i = 0; i < 3; i++)
+#pragma unroll
+        for (int c = 0; c < C; c++)
+            m[i][c] = l[i][c] = r[i][c] = 0.0f;
+    for (int k = 0; k < nr + 2; k++) {
+        const float v = __int_as_float(sv.ty[k].y);
+        const float *top = slots + sv.map[2 * k] * slot_el;
+        const float *bot = slots + sv.map[2 * k + 1] * slot_el;
+#pragma unroll
+        for (int c = 0; c < C; c++) {
+            m[0][c] = m[1][c];
+            m[1][c] = m[2][c];
+            l[0][c] = l[1][c];
+            l[1][c] = l[2][c];
+            r[0][c] = r[1][c];
+            r[1][c] = r[2][c];
+            const float t0 = top[o0 + c], t1 = top[o1 + c];
+            const float b0 = bot[o0 + c], b1 = bot[o1 + c];
+            const float hT = fmaf(u, t1 - t0, t0);
+            const float hB = fmaf(u, b1 - b0, b0);
+            const float val = fmaf(v, hB - hT, hT);
+            m[2][c] = val;
+            l[2][c] = __shfl_up_sync(0xffffffffu, val, 1);
+            r[2][c] = __shfl_down_sync(0xffffffffu, val, 1);
         }
-    }
-    consumer_sync();
-    {
-        constexpr int R = 4;                       // outputs per thread, down one column
-        const int groups = (nr + R - 1) / R;
-        const int total = groups * nc;
-        const int step_q = kConsumers / nc, step_c = kConsumers - step_q * nc;
-        int q = threadIdx.x / nc, cl = threadIdx.x - q * nc;
-        for (int e = threadIdx.x; e < total; e += kConsumers) {
-            const int r0 = q * R;
-            const int rows = min(R, nr - r0);
+        if (k >= 2 && emit) {
 #pragma unroll
             for (int c = 0; c < C; c++) {
-                float win[R + 2][3];
+                float z = 0.0f;
 #pragma unroll
-                for (int i = 0; i < R + 2; i++)
-#pragma unroll
-                    for (int jj = 0; jj < 3; jj++)
-                        win[i][jj] = (i < rows + 2) ? mid[((r0 + i) * mid_w + (cl + jj)) * C + c] : 0.0f;
-#pragma unroll
-                for (int r = 0; r < R; r++) {
-                    if (r < rows) {
-                        float z = 0.0f;
-#pragma unroll
-                        for (int i = 0; i < 3; i++)
-#pragma unroll
-                            for (int jj = 0; jj < 3; jj++)
-                                z = fmaf(a.w[i * 3 + jj], win[r + i][jj], z);
-                        ob[(r0 + r) * orow_el + cl * C + c] = z;
-                    }
+                for (int i = 0; i < 3; i++) {
+                    z = fmaf(a.w[i * 3 + 0], l[i][c], z);
+                    z = fmaf(a.w[i * 3 + 1], m[i][c], z);
+                    z = fmaf(a.w[i * 3 + 2], r[i][c], z);
                 }
-            }
-            cl += step_c;
-            q += step_q;
-            if (cl >= nc) {
-                cl -= nc;
-                q += 1;
+                ob[(k - 2) * orow_el + col * C + c] = z;
             }
         }
     }
@@ -758,7 +939,7 @@ __device__ void compute_filter3x3(const KArgs &a, const StageView &sv, const Til
 
 // OP: 0 plain resize (T, C, LINEAR, VAR), 1 normalise, 2 3x3 filter.
 template <int OP, typename T, int C, int LINEAR, int VAR>
-__global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a)
+__global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a, const __grid_constant__ CUtensorMap tmap)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int FAM = OP == 1 ? FAM_NORM : (OP == 2 ? FAM_FILT : (sizeof(T) == 1 ? FAM_U8 : FAM_F32));
@@ -808,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a)
                     break;
                 plan_stage<LINEAR>(a, L, st, t, HALO, IN_ES);
             }
-            fetch_stage(a, L, st, &full[s], policy);
+            fetch_stage(a, L, st, &full[s], policy, &tmap, fam_tables_in_stage(FAM), HALO);
         }
         return;
     }
@@ -838,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a)
             break;
         }
         const TileGeom g = tile_geom(a, t);
-        const StageView sv = stage_view(a, L, st);
+        const StageView sv = stage_view(a, L, st, HALO);
         if constexpr (OP == 0) {
             if constexpr (VAR == VAR_DOWN2)
                 compute_down2<C>(a, sv, g, ob, L.out_row_bytes);
@@ -847,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a)
         } else if constexpr (OP == 1) {
             compute_normalize<C>(a, sv, g, ob, L.out_row_bytes);
         } else {
-            compute_filter3x3<C>(a, sv, g, ob, L.out_row_bytes, reinterpret_cast<float *>(smem + L.mid_off));
+            compute_filter3x3<C>(a, sv, g, ob, L.out_row_bytes);
         }
         fence_proxy_async_smem();
         consumer_sync();
@@ -878,7 +1059,7 @@ const void *kernel_for(int fam, int mode, int variant, int C)
     const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
     if (ci < 0)
         return nullptr;
-    using Fn = void (*)(const KArgs);
+    using Fn = void (*)(const KArgs, const CUtensorMap);
     static const Fn u8[2][3] = {
         {k_resize<0, uint8_t, 1, 0, 0>, k_resize<0, uint8_t, 3, 0, 0>, k_resize<0, uint8_t, 4, 0, 0>},
         {k_resize<0, uint8_t, 1, 1, 0>, k_resize<0, uint8_t, 3, 1, 0>, k_resize<0, uint8_t, 4, 1, 0>}};
@@ -903,7 +1084,8 @@ const void *kernel_for(int fam, int mode, int variant, int C)
     }
 }
 
-int launch_resize(const void *fn, const KArgs &a, int grid, size_t smem, bool pdl, void *stream)
+int launch_resize(const void *fn, const KArgs &a, const CUtensorMap &tmap, int grid, size_t smem, bool pdl,
+                  void *stream)
 {
     if (grid <= 0)
         return 0;
@@ -921,8 +1103,8 @@ int launch_resize(const void *fn, const KArgs &a, int grid, size_t smem, bool pd
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return static_cast<int>(
-        cudaLaunchKernelEx(&cfg, reinterpret_cast<void (*)(const KArgs)>(const_cast<void *>(fn)), a));
+    return static_cast<int>(cudaLaunchKernelEx(
+        &cfg, reinterpret_cast<void (*)(const KArgs, const CUtensorMap)>(const_cast<void *>(fn)), a, tmap));
 }
 
 }  // namespace rz

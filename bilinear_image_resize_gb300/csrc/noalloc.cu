@@ -208,7 +208,9 @@ extern "C" int resize_u8_noalloc(const uint8_t *src, size_t src_pitch, uint8_t *
     k_noalloc_tables<<<(n + 255) / 256, 256, 0, s>>>(sc, H, W, out_h, out_w, linear ? 1 : 0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(e);
-    const int le = rz::launch_resize(fn, a, grid, static_cast<size_t>(L.total), true, stream);
+    CUtensorMap unused;   // row copies only: the kernel ignores the map
+    for (size_t i = 0; i < sizeof(unused.opaque) / sizeof(unused.opaque[0]); i++) unused.opaque[i] = 0;
+    const int le = rz::launch_resize(fn, a, unused, grid, static_cast<size_t>(L.total), true, stream);
     if (le != 0) return fail(static_cast<cudaError_t>(le));
     return RZ_OK;
 }

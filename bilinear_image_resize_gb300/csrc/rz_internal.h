@@ -2,6 +2,8 @@
 // (kernels.cu).  Nothing here is part of the C ABI.
 #pragma once
 
+#include <cuda.h>   // CUtensorMap (a plain struct; no driver library is linked)
+
 #include <cstddef>
 #include <cstdint>
 
@@ -26,6 +28,10 @@ __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / 
 __host__ __device__ constexpr int fam_in_es(int fam) { return (fam == FAM_U8 || fam == FAM_NORM) ? 1 : 4; }
 __host__ __device__ constexpr int fam_out_es(int fam) { return fam == FAM_U8 ? 1 : 4; }
 __host__ __device__ constexpr int fam_halo(int fam) { return fam == FAM_FILT ? 1 : 0; }
+// Families whose producer also stages the tile's sampling-table entries.
+__host__ __device__ constexpr bool fam_tables_in_stage(int fam) { return fam == FAM_NORM || fam == FAM_FILT; }
+__host__ __device__ constexpr int tab_x_entries(int TW, int halo) { return TW + 2 * halo + 8; }
+
 // Padding after each staged row: the uint8 bilinear tap reads are 32-bit
 // words and may pass the end of a row's span by up to 11 bytes.
 __host__ __device__ constexpr int fam_slot_pad(int fam) { return (fam == FAM_U8 || fam == FAM_NORM) ? 16 : 0; }
@@ -34,15 +40,13 @@ __host__ __device__ constexpr int fam_slot_pad(int fam) { return (fam == FAM_U8 
 // device compute them with this one function.
 //
 //   [0, 64)                       per stage: a "full" and an "empty" mbarrier
-//   stages x stage_bytes          per stage: header {nrows, b_lo, nbytes, tile},
+//   stages x stage_bytes          per stage: header {nrows, b_lo, nbytes, tile, first row, image},
 //                                 int rows[max_rows], int map[2 * computed rows],
 //                                 then max_rows staged row segments of slot_bytes
-//   mid                           float[(TR+2) * (TW+2) * C] resized values with
-//                                 their one-pixel ring (3x3 epilogue only)
 //   2 x out_bytes                 double-buffered output tile
 struct SmemLayout {
     int stage_off, stage_bytes;
-    int rows_off, map_off, slots_off;   // within a stage
+    int rows_off, map_off, tab_off, slots_off;   // within a stage
     int mid_off;
     int out_off, out_bytes, out_row_bytes;
     int total;
@@ -54,13 +58,17 @@ __host__ __device__ inline SmemLayout smem_layout(int fam, int C, int TR, int TW
     SmemLayout L;
     const int halo = fam_halo(fam);
     const int nrc = TR + 2 * halo;
-    L.rows_off = 16;
+    L.rows_off = 32;
     L.map_off = align_up(L.rows_off + 4 * max_rows, 16);
-    L.slots_off = align_up(L.map_off + 8 * nrc, 128);
+    L.tab_off = align_up(L.map_off + 8 * nrc, 16);
+    // the narrow-tile families stage the tile's table entries too:
+    // x entries for the computed columns (+ slack), then y entries for the computed rows
+    const int tab = fam_tables_in_stage(fam) ? 8 * ((TW + 2 * halo + 8) + nrc) : 0;
+    L.slots_off = align_up(L.tab_off + tab, 128);
     L.stage_bytes = align_up(L.slots_off + max_rows * slot_bytes, 128);
     L.stage_off = 128;
     L.mid_off = L.stage_off + stages * L.stage_bytes;
-    const int mid = halo ? align_up((TR + 2) * (TW + 2) * C * 4, 128) : 0;
+    const int mid = 0;   // the 3x3 epilogue keeps its window in registers
     L.out_off = L.mid_off + mid;
     if (fam == FAM_NORM) {
         L.out_row_bytes = align_up(TW * 4, 16);
@@ -90,6 +98,9 @@ struct KArgs {
     int slot_bytes;         // bytes reserved per staged row
     int stages;             // depth of the staged-tile ring (1..kMaxStages)
     int tma_in, tma_out;    // bulk copies allowed for loads / stores
+    int tensor_in;          // stage each tile with one tensor-map copy (box below)
+    int box_granules;       // box width in 16-byte granules
+    int box_rows;           // box height in rows
     const int2 *xt;         // per output column {source column, weight}
     const int2 *yt;         // per output row    {source row, weight}
     int *status;            // device status word (RZ_OK or RZ_ERR_TIMEOUT)
@@ -104,7 +115,9 @@ void record_cuda_error(int e);
 const void *kernel_for(int fam, int mode, int variant, int C);
 
 // Launch it on `grid` CTAs (asynchronous), optionally as a programmatic
-// dependent launch.  Returns a cudaError_t value.
-int launch_resize(const void *fn, const KArgs &a, int grid, size_t smem, bool pdl, void *stream);
+// dependent launch.  `tmap` describes the source when a.tensor_in is set
+// (otherwise its contents are ignored).  Returns a cudaError_t value.
+int launch_resize(const void *fn, const KArgs &a, const CUtensorMap &tmap, int grid, size_t smem, bool pdl,
+                  void *stream);
 
 }  // namespace rz
