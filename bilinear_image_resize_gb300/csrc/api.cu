@@ -81,7 +81,7 @@ void axis_nearest(int n_in, int n_out, int32_t *ofs)
 
 struct TileCfg {
     int TR = 0, TW = 0, tiles_x = 0, tiles_y = 0, max_rows = 0, slot_bytes = 0, stages = 0, variant = 0;
-    int tensor = 0, box_granules = 0, box_rows = 0;   // tensor-map staging (one box per tile)
+    int tensor = 0, box_words = 0, box_rows = 0;   // tensor-map staging (one box per tile)
     size_t smem = 0;
     int grid = 0;
 };
@@ -210,11 +210,11 @@ bool eval_tile(const rz_plan_s &p, int fam, int C, int TR, int TW, int stages, T
     t.max_rows = max_tile_rows(p, fam, t.TR);
     if (fam == rz::FAM_FILT) {
         // the 3x3 tiles are narrow and tall: stage each with one tensor-map
-        // box when it fits the box limits (256 granules by 256 rows)
+        // box when it fits the box limits (256 eight-byte words by 256 rows)
         const int range = max_tile_row_range(p, fam, t.TR);
-        if (t.slot_bytes / 16 <= 256 && range <= 256) {
+        if (t.slot_bytes % 16 == 0 && t.slot_bytes / 8 <= 256 && range <= 256) {
             t.tensor = 1;
-            t.box_granules = t.slot_bytes / 16;
+            t.box_words = t.slot_bytes / 8;
             t.box_rows = range;
             t.max_rows = std::max(t.max_rows, range);
         }
@@ -466,19 +466,19 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     std::memset(&tmap, 0, sizeof(tmap));
     a.tensor_in = 0;
     if (t.tensor && a.tma_in) {
-        // the image as {16-byte granule, granules per row, rows, images}
+        // the image as {8-byte words per row, rows, images}: a box row is
+        // the tile's whole column span, so it moves as one long transfer
         EncodeTiledFn enc = tensor_encoder();
-        const cuuint64_t dims[4] = {16, in_row / 16, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(batch)};
+        const cuuint64_t dims[3] = {in_row / 8, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(batch)};
         const cuuint64_t bstride = batch > 1 ? a.src_bstride : static_cast<long long>(src_pitch) * H;
-        const cuuint64_t strides[3] = {16, static_cast<cuuint64_t>(src_pitch), bstride};
-        const cuuint32_t box[4] = {16, static_cast<cuuint32_t>(t.box_granules), static_cast<cuuint32_t>(t.box_rows),
-                                   1};
-        const cuuint32_t estr[4] = {1, 1, 1, 1};
-        if (enc && enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(src), dims, strides, box, estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(src_pitch), bstride};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(t.box_words), static_cast<cuuint32_t>(t.box_rows), 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (enc && enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void *>(src), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
             a.tensor_in = 1;
-            a.box_granules = t.box_granules;
+            a.box_words = t.box_words;
             a.box_rows = t.box_rows;
         }
     }
@@ -538,35 +538,41 @@ int resize_plan_create(rz_plan *out, int in_h, int in_w, int out_h, int out_w, i
 
     // one device block: x tables (q11 and float weights), y tables, status word
     const size_t nx = static_cast<size_t>(out_w), ny = static_cast<size_t>(out_h);
-    // each table starts on a 16-byte boundary and is followed by at least
-    // four spare entries, so kernels may read entries in 16-byte pairs
-    const size_t xbytes = ((nx + 4) * sizeof(int2) + 15) & ~size_t(15);
-    const size_t ybytes = ((ny + 4) * sizeof(int2) + 15) & ~size_t(15);
+    // each table is kTabPad entries (a 16-byte multiple) after the start of
+    // its block, which starts on a 16-byte boundary; the kTabPad entries
+    // before and the kTabPad (or more) after it repeat its first and last
+    // entry, so kernels may read entries in 16-byte pairs and copy a tile's
+    // clamped range of entries in one piece
+    constexpr size_t kPad = rz::kTabPad;
+    const size_t xbytes = ((nx + 2 * kPad) * sizeof(int2) + 15) & ~size_t(15);
+    const size_t ybytes = ((ny + 2 * kPad) * sizeof(int2) + 15) & ~size_t(15);
     const size_t off_xf = xbytes, off_yq = 2 * xbytes, off_yf = off_yq + ybytes;
     const size_t off_st = off_yf + ybytes;
     const size_t total = off_st + 16;
     std::vector<uint8_t> host(total, 0);
     int2 *hxq = reinterpret_cast<int2 *>(host.data()), *hxf = reinterpret_cast<int2 *>(host.data() + off_xf);
     int2 *hyq = reinterpret_cast<int2 *>(host.data() + off_yq), *hyf = reinterpret_cast<int2 *>(host.data() + off_yf);
-    for (size_t i = 0; i < nx; i++) {
+    for (size_t k = 0; nx > 0 && k < xbytes / sizeof(int2); k++) {
+        const size_t i = std::min(k < kPad ? 0 : k - kPad, nx - 1);
         int32_t ubits;
         std::memcpy(&ubits, &p->xu[i], 4);
-        hxq[i] = make_int2(p->xofs[i], p->xq[i]);
-        hxf[i] = make_int2(p->xofs[i], ubits);
+        hxq[k] = make_int2(p->xofs[i], p->xq[i]);
+        hxf[k] = make_int2(p->xofs[i], ubits);
     }
-    for (size_t i = 0; i < ny; i++) {
+    for (size_t k = 0; ny > 0 && k < ybytes / sizeof(int2); k++) {
+        const size_t i = std::min(k < kPad ? 0 : k - kPad, ny - 1);
         int32_t vbits;
         std::memcpy(&vbits, &p->yu[i], 4);
-        hyq[i] = make_int2(p->yofs[i], p->yq[i]);
-        hyf[i] = make_int2(p->yofs[i], vbits);
+        hyq[k] = make_int2(p->yofs[i], p->yq[i]);
+        hyf[k] = make_int2(p->yofs[i], vbits);
     }
     e = cudaMalloc(&p->dmem, total);
     if (e != cudaSuccess) { p->dmem = nullptr; delete p; return cuda_fail(e); }
     uint8_t *d = static_cast<uint8_t *>(p->dmem);
-    p->d_xq = reinterpret_cast<int2 *>(d);
-    p->d_xf = reinterpret_cast<int2 *>(d + off_xf);
-    p->d_yq = reinterpret_cast<int2 *>(d + off_yq);
-    p->d_yf = reinterpret_cast<int2 *>(d + off_yf);
+    p->d_xq = reinterpret_cast<int2 *>(d) + kPad;
+    p->d_xf = reinterpret_cast<int2 *>(d + off_xf) + kPad;
+    p->d_yq = reinterpret_cast<int2 *>(d + off_yq) + kPad;
+    p->d_yf = reinterpret_cast<int2 *>(d + off_yf) + kPad;
     p->d_status = reinterpret_cast<int *>(d + off_st);
     // pageable source: the call returns once the bytes are staged, so `host`
     // may be freed on return

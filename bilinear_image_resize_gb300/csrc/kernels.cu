@@ -144,18 +144,28 @@ __device__ __forceinline__ void bulk_load_hint(void *sdst, const void *gsrc, uin
         : "memory");
 }
 
-// Tensor-map copy of one box {16 bytes, granules, rows, 1} at coordinates
-// {0, granule, row, image} into shared memory, completing on `bar`.  The
-// innermost coordinate is 0, so the copy starts on a 16-byte boundary; parts
-// of the box outside the image are zero-filled, not read.
-__device__ __forceinline__ void tensor_load_4d(void *sdst, const CUtensorMap *map, int granule, int row, int image,
+// Tensor-map copy of one box {words, rows, 1} at coordinates {word, row,
+// image} into shared memory, completing on `bar`.  The map's elements are
+// 8-byte words and `word` is even, so the copy starts on a 16-byte boundary;
+// parts of the box outside the image are zero-filled, not read.
+__device__ __forceinline__ void tensor_load_3d(void *sdst, const CUtensorMap *map, int word, int row, int image,
                                                uint64_t *bar, uint64_t policy)
 {
     asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(sdst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(granule), "r"(row), "r"(image), "r"(smem_addr(bar)),
-        "l"(policy)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(sdst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(word), "r"(row), "r"(image), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Bulk copy global -> this CTA's shared memory with the default L2 policy
+// (for the sampling tables, which every tile row reads again).
+__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
 }
 
@@ -199,11 +209,12 @@ __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? l
 __device__ __forceinline__ int ceil_log2(int v) { return v <= 1 ? 0 : 32 - __clz(v - 1); }
 
 // floor(num / den) for 0 < den <= 2^17 and |num / den| < 2^17 + 1, exactly:
-// the float quotient has absolute error below 2^-6 there, so its floor is
-// within one of the true floor, and 64-bit integer checks correct it.
+// the fast float quotient (num rounded to float, a division within 2 ulp)
+// is off by less than 2^-4 there, so its floor is within one of the true
+// floor, and 64-bit integer checks correct it.
 __device__ __forceinline__ int floor_div_exact(long long num, int den)
 {
-    int q = __float2int_rd(static_cast<float>(num) / static_cast<float>(den));
+    int q = __float2int_rd(__fdividef(static_cast<float>(num), static_cast<float>(den)));
     const long long qd = static_cast<long long>(q) * den;
     if (qd > num)
         q -= 1;
@@ -262,15 +273,15 @@ struct StageHdr {
     int tile;    // tile index
     int row0;    // first staged source row (tensor-map staging)
     int image;   // image index within the batch
-    int pad[2];
+    int xsh;     // staged x (y) table entries start this many entries
+    int ysh;     //   before the tile's first computed column (row): 0 or 1
 };
 
 // Producer warp, part 1 (no global memory access): list the source rows of
 // `tile` into stage `st`.  Lanes derive the tile's column span and row
-// indices in parallel; every lane then walks the same list of distinct
-// source rows (non-decreasing in the output row, so a row already listed is
-// one of the last two entries); lane 0 records the list, the per-row slot
-// map and the header.
+// indices in parallel, one computed output row per lane; which rows are new
+// and where each lands in the list follow from warp votes (the sampled rows
+// never decrease along the output rows); lane 0 records the header.
 template <int LINEAR>
 __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, int tile, int halo, int in_es)
 {
@@ -300,47 +311,53 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, int
     }
     const int nbytes = b_hi - b_lo;
 
-    int n = 0, last = -1, prev = -1;   // last two listed rows
+    // Distinct source rows.  Lane k takes computed row k (32 rows per pass)
+    // with taps r0 <= r1 <= r0 + 1.  Taps never decrease along k, so r0 is
+    // already listed exactly when r0 <= r1 of row k - 1, and is then the last
+    // or the one-before-last entry listed before row k; r1 is new exactly
+    // when it exceeds both.  Counts of new taps on lower lanes (ballots) give
+    // each tap its slot.
+    int n = 0, r1_before = -1, row0 = 0;
     bool overflow = nbytes > a.slot_bytes;
-    for (int k = 0; k < nrc && !overflow; k++) {
-        const int r0 = k < 32 ? __shfl_sync(0xffffffffu, yv, k)
-                              : sample_index<LINEAR>(a.H, a.OH, clampi(g.dy0 - halo + k, 0, a.OH - 1));
-        const int r1 = LINEAR ? min(r0 + 1, a.H - 1) : r0;
-        int s0, s1;
-        if (n > 0 && last == r0)
-            s0 = n - 1;
-        else if (n > 1 && prev == r0)
-            s0 = n - 2;
-        else {
-            if (n == a.max_rows) { overflow = true; break; }
-            if (lane == 0) rows[n] = r0;
-            prev = last; last = r0;
-            s0 = n++;
+    const unsigned lower = (1u << lane) - 1u;
+    for (int base = 0; base < nrc; base += 32) {
+        const int k = base + lane;
+        const bool act = k < nrc;
+        int r0 = 0x7fffffff, r1 = 0x7fffffff;
+        if (act) {
+            r0 = k < 32 ? yv : sample_index<LINEAR>(a.H, a.OH, clampi(g.dy0 - halo + k, 0, a.OH - 1));
+            r1 = LINEAR ? min(r0 + 1, a.H - 1) : r0;
         }
-        if (last == r1)
-            s1 = n - 1;
-        else {
-            if (n == a.max_rows) { overflow = true; break; }
-            if (lane == 0) rows[n] = r1;
-            prev = last; last = r1;
-            s1 = n++;
-        }
-        if (lane == 0) {
+        int prev_r1 = __shfl_up_sync(0xffffffffu, r1, 1);
+        if (lane == 0)
+            prev_r1 = r1_before;
+        const bool new0 = act && r0 > prev_r1;
+        const bool new1 = act && r1 > max(r0, prev_r1);
+        const unsigned b0 = __ballot_sync(0xffffffffu, new0), b1 = __ballot_sync(0xffffffffu, new1);
+        const int c = n + __popc(b0 & lower) + __popc(b1 & lower);   // entries listed before row k
+        const int s0 = new0 ? c : c - 1 - (prev_r1 - r0);
+        const int s1 = new1 ? c + (new0 ? 1 : 0) : (r1 == r0 ? s0 : c - 1);
+        if (act) {
+            if (new0 && s0 < a.max_rows) rows[s0] = r0;
+            if (new1 && s1 < a.max_rows) rows[s1] = r1;
             map[2 * k] = s0;
             map[2 * k + 1] = s1;
         }
+        if (base == 0)
+            row0 = __shfl_sync(0xffffffffu, r0, 0);
+        n += __popc(b0) + __popc(b1);
+        r1_before = __shfl_sync(0xffffffffu, r1, min(31, nrc - 1 - base));
     }
-    int row0 = 0;
+    if (n > a.max_rows)
+        overflow = true;
     if (a.tensor_in && !overflow && n > 0) {
         // one box holds the whole row range: slot = row - first row
-        __syncwarp();
-        row0 = rows[0];
-        const int range = rows[n - 1] - row0 + 1;
+        const int range = r1_before - row0 + 1;
         if (range > a.box_rows)
             overflow = true;
-        else if (lane == 0)
-            for (int k = 0; k < 2 * nrc; k++)
-                map[k] = rows[map[k]] - row0;
+        __syncwarp();
+        for (int k = lane; k < 2 * nrc && !overflow; k += 32)
+            map[k] = rows[map[k]] - row0;
         n = range;
     }
     if (lane == 0) {
@@ -352,6 +369,8 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, int
         h->tile = tile;
         h->row0 = row0;
         h->image = tile / (a.tiles_x * a.tiles_y);
+        h->xsh = (g.dx0 - halo) & 1;
+        h->ysh = (g.dy0 - halo) & 1;
     }
     __syncwarp();
 }
@@ -372,54 +391,59 @@ __device__ void fetch_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, ui
     if (n < 0 && lane == 0)
         atomicExch(a.status, RZ_ERR_ARG);
     if (tables) {
-        // bytes first (armed without arriving), then the table entries, then
-        // the one arrival: the stage completes with copies and tables in place
-        if (a.tensor_in) {
-            if (lane == 0 && n > 0) {
-                mbar_expect_tx(full, static_cast<uint32_t>(a.box_rows * a.box_granules * 16));
-                tensor_load_4d(slots, tmap, b_lo / 16, h->row0, h->image, full, policy);
+        // the tile's x entries (computed columns dx0 - halo .. dx1 - 1 + halo)
+        // and y entries (computed rows), each one bulk copy of a range that
+        // starts and ends on an even entry; the plan's tables repeat their
+        // end entries beyond both ends, which is the clamp
+        int2 *tx = reinterpret_cast<int2 *>(st + L.tab_off);
+        int2 *ty = tx + tab_x_entries(a.TW, halo);
+        const int xa = (g.dx0 - halo) & ~1, xb = align_up(g.dx1 + halo, 2);
+        const int ya = (g.dy0 - halo) & ~1, yb = align_up(g.dy1 + halo, 2);
+        const uint32_t tab_bytes = static_cast<uint32_t>(8 * ((xb - xa) + (yb - ya)));
+        if (a.tensor_in || a.tma_in) {
+            uint32_t bytes = tab_bytes;
+            if (n > 0)
+                bytes += static_cast<uint32_t>(a.tensor_in ? a.box_rows * a.box_words * 8 : n * nbytes);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full, bytes);
+                bulk_load(tx, a.xt + xa, static_cast<uint32_t>(8 * (xb - xa)), full);
+                bulk_load(ty, a.yt + ya, static_cast<uint32_t>(8 * (yb - ya)), full);
+                if (a.tensor_in && n > 0)
+                    tensor_load_3d(slots, tmap, b_lo / 8, h->row0, h->image, full, policy);
             }
-        } else if (a.tma_in) {
-            if (lane == 0 && n > 0)
-                mbar_expect_tx(full, static_cast<uint32_t>(n * nbytes));
-            __syncwarp();
-            for (int r = lane; r < n; r += 32)
-                bulk_load_hint(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch + b_lo,
-                               static_cast<uint32_t>(nbytes), full, policy);
+            if (!a.tensor_in) {
+                __syncwarp();
+                for (int r = lane; r < n; r += 32)
+                    bulk_load_hint(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch + b_lo,
+                                   static_cast<uint32_t>(nbytes), full, policy);
+            }
         } else {
+            // the tables still move as bulk copies (armed before any lane
+            // arrives); the unaligned rows are copied by the lanes, each of
+            // which arrives after its own copies
+            if (lane == 0) {
+                mbar_expect_tx(full, tab_bytes);
+                bulk_load(tx, a.xt + xa, static_cast<uint32_t>(8 * (xb - xa)), full);
+                bulk_load(ty, a.yt + ya, static_cast<uint32_t>(8 * (yb - ya)), full);
+            }
             for (int r = 0; r < n; r++) {
                 const uint8_t *src = g.src + (long long)rows[r] * a.src_pitch + b_lo;
                 uint8_t *d = slots + r * a.slot_bytes;
                 for (int k = lane; k < nbytes; k += 32)
                     d[k] = __ldg(src + k);
             }
-        }
-        // x entries of the computed columns dx0 - halo .. (clamped into the
-        // tile's staged span), y entries of the computed rows (clamped)
-        int2 *tx = reinterpret_cast<int2 *>(st + L.tab_off);
-        int2 *ty = tx + tab_x_entries(a.TW, halo);
-        const int nx = (g.dx1 - g.dx0) + 2 * halo, ny = (g.dy1 - g.dy0) + 2 * halo;
-        const int xhi = min(g.dx1 - 1 + halo, a.OW - 1);
-        for (int k = lane; k < nx; k += 32)
-            tx[k] = __ldg(&a.xt[clampi(g.dx0 - halo + k, 0, xhi)]);
-        for (int k = lane; k < ny; k += 32)
-            ty[k] = __ldg(&a.yt[clampi(g.dy0 - halo + k, 0, a.OH - 1)]);
-        __syncwarp();
-        if (a.tma_in || a.tensor_in) {
-            if (lane == 0)
-                mbar_arrive(full);
-        } else {
-            mbar_arrive(full);   // 32 arrivals: each lane releases its own writes
+            __syncwarp();
+            mbar_arrive(full);
         }
     } else if (a.tensor_in) {
         // one tensor-map copy of the box {granules x box_rows} at the tile's
         // first row; the box is what the barrier counts, whatever part of it
         // the tile uses
         if (lane == 0) {
-            const uint32_t box = static_cast<uint32_t>(a.box_rows * a.box_granules * 16);
+            const uint32_t box = static_cast<uint32_t>(a.box_rows * a.box_words * 8);
             mbar_arrive_expect_tx(full, n > 0 ? box : 0u);
             if (n > 0)
-                tensor_load_4d(slots, tmap, b_lo / 16, h->row0, h->image, full, policy);
+                tensor_load_3d(slots, tmap, b_lo / 8, h->row0, h->image, full, policy);
         }
     } else if (a.tma_in) {
         // a rejected tile completes the phase with no bytes
@@ -508,11 +532,12 @@ struct StageView {
 __device__ __forceinline__ StageView stage_view(const KArgs &a, const SmemLayout &L, const uint8_t *st, int halo)
 {
     StageView v;
-    v.tx = reinterpret_cast<const int2 *>(st + L.tab_off);
-    v.ty = v.tx + tab_x_entries(a.TW, halo);
+    const StageHdr *h = reinterpret_cast<const StageHdr *>(st);
+    v.tx = reinterpret_cast<const int2 *>(st + L.tab_off) + h->xsh;
+    v.ty = reinterpret_cast<const int2 *>(st + L.tab_off) + tab_x_entries(a.TW, halo) + h->ysh;
     v.slots = st + L.slots_off;
     v.map = reinterpret_cast<const int *>(st + L.map_off);
-    v.b_lo = reinterpret_cast<const StageHdr *>(st)->b_lo;
+    v.b_lo = h->b_lo;
     v.slot_bytes = a.slot_bytes;
     return v;
 }

@@ -30,7 +30,14 @@ __host__ __device__ constexpr int fam_out_es(int fam) { return fam == FAM_U8 ? 1
 __host__ __device__ constexpr int fam_halo(int fam) { return fam == FAM_FILT ? 1 : 0; }
 // Families whose producer also stages the tile's sampling-table entries.
 __host__ __device__ constexpr bool fam_tables_in_stage(int fam) { return fam == FAM_NORM || fam == FAM_FILT; }
-__host__ __device__ constexpr int tab_x_entries(int TW, int halo) { return TW + 2 * halo + 8; }
+// Staged table entries: a tile's x (y) entries are copied in one bulk copy
+// that starts on an even entry, so one entry of slack at each end.
+__host__ __device__ constexpr int tab_x_entries(int TW, int halo) { return align_up(TW + 2 * halo + 8, 2); }
+__host__ __device__ constexpr int tab_y_entries(int TR, int halo) { return align_up(TR + 2 * halo + 4, 2); }
+// Entries before and after each of the plan's device tables that repeat the
+// first and last entry (the clamp of the 3x3 halo), so that any tile's range
+// of entries is one contiguous copy.
+constexpr int kTabPad = 8;
 
 // Padding after each staged row: the uint8 bilinear tap reads are 32-bit
 // words and may pass the end of a row's span by up to 11 bytes.
@@ -63,7 +70,7 @@ __host__ __device__ inline SmemLayout smem_layout(int fam, int C, int TR, int TW
     L.tab_off = align_up(L.map_off + 8 * nrc, 16);
     // the narrow-tile families stage the tile's table entries too:
     // x entries for the computed columns (+ slack), then y entries for the computed rows
-    const int tab = fam_tables_in_stage(fam) ? 8 * ((TW + 2 * halo + 8) + nrc) : 0;
+    const int tab = fam_tables_in_stage(fam) ? 8 * (tab_x_entries(TW, halo) + tab_y_entries(TR, halo)) : 0;
     L.slots_off = align_up(L.tab_off + tab, 128);
     L.stage_bytes = align_up(L.slots_off + max_rows * slot_bytes, 128);
     L.stage_off = 128;
@@ -99,10 +106,10 @@ struct KArgs {
     int stages;             // depth of the staged-tile ring (1..kMaxStages)
     int tma_in, tma_out;    // bulk copies allowed for loads / stores
     int tensor_in;          // stage each tile with one tensor-map copy (box below)
-    int box_granules;       // box width in 16-byte granules
+    int box_words;          // box width in 8-byte words
     int box_rows;           // box height in rows
-    const int2 *xt;         // per output column {source column, weight}
-    const int2 *yt;         // per output row    {source row, weight}
+    const int2 *xt;         // per output column {source column, weight}; kTabPad clamped entries either side
+    const int2 *yt;         // per output row    {source row, weight}; kTabPad clamped entries either side
     int *status;            // device status word (RZ_OK or RZ_ERR_TIMEOUT)
     float scale[4], shift[4];  // normalise epilogue: y = q * scale[c] + shift[c]
     float w[9];                // 3x3 epilogue weights, row-major

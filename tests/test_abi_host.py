@@ -139,10 +139,11 @@ def test_strerror(lib):
 
 def test_float_quotient_floor_is_within_one():
     # The kernels derive sampling indices as floor(float(num) / float(den))
-    # followed by one integer correction each way; that is exact only if the
-    # float floor is within one of the true floor.  Check the claim with IEEE
-    # single arithmetic over the extremes and a random sample of geometries
-    # (n_in, n_out <= RZ_MAX_DIM).
+    # with a fast division (within 2 ulp of the rounded quotient) followed by
+    # one integer correction each way; that is exact only if the float floor
+    # is within one of the true floor.  Check the claim with IEEE single
+    # arithmetic, the quotient moved 2 ulp either way, over the extremes and a
+    # random sample of geometries (n_in, n_out <= RZ_MAX_DIM).
     rng = np.random.default_rng(123)
     cases = [(65536, 1), (1, 65536), (65536, 65536), (65535, 3), (3, 65535), (8192, 5980), (3840, 1920)]
     cases += [tuple(int(v) for v in rng.integers(1, 65537, size=2)) for _ in range(200)]
@@ -150,6 +151,10 @@ def test_float_quotient_floor_is_within_one():
         d = np.unique(np.concatenate([np.arange(min(n_out, 64)), np.arange(max(0, n_out - 64), n_out),
                                       rng.integers(0, n_out, size=256)])).astype(np.int64)
         for num, den in (((2 * d + 1) * n_in - n_out, 2 * n_out), (d * n_in, n_out)):
-            qf = np.floor(np.float32(num.astype(np.float32)) / np.float32(den)).astype(np.int64)
+            q = np.float32(num.astype(np.float32)) / np.float32(den)
+            lo = np.nextafter(np.nextafter(q, np.float32(-np.inf)), np.float32(-np.inf))
+            hi = np.nextafter(np.nextafter(q, np.float32(np.inf)), np.float32(np.inf))
             exact = np.floor_divide(num, den)
-            assert np.all(np.abs(qf - exact) <= 1), (n_in, n_out)
+            for qv in (lo, q, hi):
+                qf = np.floor(qv).astype(np.int64)
+                assert np.all(np.abs(qf - exact) <= 1), (n_in, n_out)
