@@ -81,7 +81,8 @@ void axis_nearest(int n_in, int n_out, int32_t *ofs)
 
 struct TileCfg {
     int TR = 0, TW = 0, tiles_x = 0, tiles_y = 0, max_rows = 0, slot_bytes = 0, stages = 0, variant = 0;
-    int tensor = 0, box_words = 0, box_rows = 0;   // tensor-map staging (one box per tile)
+    int tensor = 0, box_words = 0, box_rows = 0;   // tensor-map staging (one box per tile or chunk)
+    int ring_chunks = 0, chunk_rows = 0, chunk_boxes = 0, box_bytes = 0;   // streaming 3x3 filter
     size_t smem = 0;
     int grid = 0;
 };
@@ -125,6 +126,7 @@ struct rz_plan_s {
     int opt_ctas_per_sm = 0;   // 0: as many as fit
     int opt_grid_mode = 0;     // 0: persistent CTAs; 1: one CTA per tile
     int opt_pdl = 1;           // programmatic dependent launch
+    int opt_ring_rows = 0;     // 3x3 filter: source rows in the streaming ring (0: automatic)
 };
 
 namespace {
@@ -335,6 +337,83 @@ int ensure_smem_attr(int dev, const void *fn)
     return 0;
 }
 
+constexpr int kFilterCtaSmem = 74 * 1024;   // three streaming-filter CTAs per SM
+constexpr int kFilterMinRows = 16;          // shortest automatic unit: the halo adds 2 resized rows
+
+// Units, ring and grid of the streaming 3x3 filter kernel (filter.cu).
+// Units are strips of up to filter_strip(C) output columns; the automatic unit height
+// splits each strip into as many segments as give every resident CTA about
+// one unit, so a source row is staged once per strip segment.  The ring holds
+// chunks of eight rows (fewer when the option asks for a small ring), as many
+// chunks as keep three CTAs per SM (two at least).
+int get_filter_tile(rz_plan_s *p, int C, int batch, TileCfg *out, const void **fn_out)
+{
+    const void *fn = rz::filter_kernel_for(p->mode, C);
+    if (!fn) return RZ_ERR_UNSUPPORTED;
+    const int fam = rz::FAM_FILT;
+    TileCfg t;
+    // strips as wide as the kernel takes, narrowed to share the columns evenly
+    const int strips = (p->OW + rz::filter_strip(C) - 1) / rz::filter_strip(C);
+    t.TW = (p->OW + strips - 1) / strips;
+    if (p->over_tw[fam] > 0) t.TW = std::min(p->over_tw[fam], rz::filter_strip(C));
+    t.TW = std::min(t.TW, p->OW);
+    t.tiles_x = (p->OW + t.TW - 1) / t.TW;
+    const int span = max_slot_bytes(*p, fam, C, t.TW);   // a multiple of 16
+    const int BW = std::min(span, 2048);                 // a box row: at most 256 eight-byte words
+    const int NB = (span + BW - 1) / BW;
+    int G = rz::kFilterChunkRows, NCH;
+    if (p->opt_ring_rows > 0) {
+        while (G > 1 && 2 * G > p->opt_ring_rows) G /= 2;
+        NCH = p->opt_ring_rows / G;
+    } else {
+        const int chunk = NB * rz::filter_block_bytes(G, BW);
+        NCH = std::max(2, std::min(rz::kFilterRingMax / G, kFilterCtaSmem / (chunk + 16)));
+    }
+    while (rz::filter_smem(NCH, G, NB, BW) > rz::kMaxSmem) {
+        if (NCH > 2) NCH--;
+        else if (G > 1) G /= 2;
+        else return RZ_ERR_UNSUPPORTED;
+    }
+    t.ring_chunks = NCH;
+    t.chunk_rows = G;
+    t.chunk_boxes = NB;
+    t.box_bytes = BW;
+    t.slot_bytes = span;
+    t.tensor = 1;            // used when the source allows bulk copies
+    t.box_words = BW / 8;
+    t.box_rows = G;
+    t.smem = static_cast<size_t>(rz::filter_smem(NCH, G, NB, BW));
+    t.stages = 0;
+    t.variant = rz::VAR_GENERIC;
+    int e = ensure_smem_attr(p->device, fn);
+    if (e != 0) return cuda_fail(static_cast<cudaError_t>(e));
+    int per_sm = 0, sms = 0;
+    cudaError_t ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, rz::kThreads, t.smem);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    if (per_sm < 1) return RZ_ERR_ARG;
+    if (p->opt_ctas_per_sm > 0) per_sm = std::min(per_sm, p->opt_ctas_per_sm);
+    const long long cap = static_cast<long long>(per_sm) * sms;
+    int TR;
+    if (p->over_tr[fam] > 0) {
+        TR = p->over_tr[fam];
+    } else {
+        const long long segs = std::max<long long>(1, cap / (static_cast<long long>(batch) * t.tiles_x));
+        TR = static_cast<int>((p->OH + segs - 1) / segs);
+        TR = std::max(TR, std::min(p->OH, kFilterMinRows));
+    }
+    t.TR = std::max(1, std::min(TR, p->OH));
+    t.tiles_y = (p->OH + t.TR - 1) / t.TR;
+    const long long units = static_cast<long long>(batch) * t.tiles_x * t.tiles_y;
+    if (units > 0x7fffffffLL) return RZ_ERR_UNSUPPORTED;
+    t.grid = p->opt_grid_mode == 1 ? static_cast<int>(units) : static_cast<int>(std::min(units, cap));
+    p->cache.push_back({fam, C, batch, t});
+    *out = t;
+    *fn_out = fn;
+    return RZ_OK;
+}
+
 // Tile and grid for this call: the override if one is set, else the cached
 // automatic choice.  Returns an RZ_* status.
 int get_tile(rz_plan_s *p, int fam, int C, int batch, TileCfg *out, const void **fn_out)
@@ -343,9 +422,11 @@ int get_tile(rz_plan_s *p, int fam, int C, int batch, TileCfg *out, const void *
     for (const auto &e : p->cache)
         if (e.fam == fam && e.C == C && e.batch == batch) {
             *out = e.cfg;
-            *fn_out = rz::kernel_for(fam, p->mode, e.cfg.variant, C);
+            *fn_out = fam == rz::FAM_FILT ? rz::filter_kernel_for(p->mode, C)
+                                          : rz::kernel_for(fam, p->mode, e.cfg.variant, C);
             return RZ_OK;
         }
+    if (fam == rz::FAM_FILT) return get_filter_tile(p, C, batch, out, fn_out);
     const int stages = p->opt_stages > 0 ? p->opt_stages : kDefaultStages;
     const bool down2 = fam == rz::FAM_U8 && !p->opt_generic && is_down2(*p);
     TileCfg t;
@@ -453,6 +534,8 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     a.TR = t.TR; a.TW = t.TW; a.tiles_x = t.tiles_x; a.tiles_y = t.tiles_y;
     a.batch = batch;
     a.max_rows = t.max_rows; a.slot_bytes = t.slot_bytes; a.stages = t.stages;
+    a.ring_chunks = t.ring_chunks; a.chunk_rows = t.chunk_rows; a.chunk_boxes = t.chunk_boxes;
+    a.box_bytes = t.box_bytes;
     a.tma_in = aligned16(src) && (src_pitch % 16 == 0) && (in_row % 16 == 0) &&
                (a.src_bstride % 16 == 0);
     const int strip_bytes = t.TW * (nchw ? 1 : C) * out_es;
@@ -649,6 +732,10 @@ int resize_plan_set_option(rz_plan p, int option, int value)
     case RZ_OPT_PDL:
         if (value != 0 && value != 1) return RZ_ERR_ARG;
         p->opt_pdl = value;
+        break;
+    case RZ_OPT_RING_ROWS:
+        if (value != 0 && (value < 2 || value > rz::kFilterRingMax)) return RZ_ERR_ARG;
+        p->opt_ring_rows = value;
         break;
     default:
         return RZ_ERR_ARG;

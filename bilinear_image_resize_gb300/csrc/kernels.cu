@@ -27,217 +27,13 @@
 
 #include <cstdint>
 
+#include "rz_device.h"
 #include "rz_internal.h"
 
 namespace rz {
 namespace {
 
-// ------------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init()
-{
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// Barrier among the consumer warps only (the producer warp never joins it).
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
-
-// Consumer barrier that also returns whether `v` held on any consumer thread.
-__device__ __forceinline__ bool consumer_any(bool v)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "n"(kConsumers)
-        : "memory");
-    return r != 0;
-}
-
-// One bounded wait attempt: the thread may be suspended in hardware until the
-// phase completes or about 0.5 ms pass (suspend-time hint), so waiting warps
-// do not spin through issue slots.
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity), "r"(500000u)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for phase `parity` of the barrier, at most kWaitLimitNs.  Between
-// attempts the waiting warp sleeps (32 ns, doubling up to 256 ns) so that it
-// leaves the issue slots to the warps computing on the same scheduler.  On
-// time-out the status word (if given) records RZ_ERR_TIMEOUT and false is
-// returned.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const uint64_t t0 = global_ns();
-    unsigned int nap = 32;
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) {
-            if (status)
-                atomicExch(status, RZ_ERR_TIMEOUT);
-            return false;
-        }
-        __nanosleep(nap);
-        if (nap < 256)
-            nap <<= 1;
-    }
-    return true;
-}
-
-// Bulk copy global -> this CTA's shared memory, completing on `bar`, with an
-// L2 cache policy (createpolicy) attached.  Both addresses 16-byte aligned,
-// bytes a multiple of 16.
-__device__ __forceinline__ void bulk_load_hint(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar,
-                                               uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
-        "%4;" ::"r"(smem_addr(sdst)),
-        "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
-// Tensor-map copy of one box {words, rows, 1} at coordinates {word, row,
-// image} into shared memory, completing on `bar`.  The map's elements are
-// 8-byte words and `word` is even, so the copy starts on a 16-byte boundary;
-// parts of the box outside the image are zero-filled, not read.
-__device__ __forceinline__ void tensor_load_3d(void *sdst, const CUtensorMap *map, int word, int row, int image,
-                                               uint64_t *bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(sdst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(word), "r"(row), "r"(image), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
-// Bulk copy global -> this CTA's shared memory with the default L2 policy
-// (for the sampling tables, which every tile row reads again).
-__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(sdst)),
-        "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
-// L2 policy for data read once: evicted first, so that the small sampling
-// tables (read by every launch) stay resident.
-__device__ __forceinline__ uint64_t policy_evict_first()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-// Programmatic dependent launch: wait until the grids this launch depends on
-// have completed and their memory is visible; allow the next grid in the
-// stream to start launching.
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
-
-// Bulk copy shared -> global (bulk-group completion).
-__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(ssrc)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// Wait until at most N committed bulk-store groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// Make this thread's generic-proxy shared-memory writes visible to the bulk-copy (async) proxy.
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-__device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
-
-__device__ __forceinline__ int ceil_log2(int v) { return v <= 1 ? 0 : 32 - __clz(v - 1); }
-
-// floor(num / den) for 0 < den <= 2^17 and |num / den| < 2^17 + 1, exactly:
-// the fast float quotient (num rounded to float, a division within 2 ulp)
-// is off by less than 2^-4 there, so its floor is within one of the true
-// floor, and 64-bit integer checks correct it.
-__device__ __forceinline__ int floor_div_exact(long long num, int den)
-{
-    int q = __float2int_rd(__fdividef(static_cast<float>(num), static_cast<float>(den)));
-    const long long qd = static_cast<long long>(q) * den;
-    if (qd > num)
-        q -= 1;
-    else if (qd + den <= num)
-        q += 1;
-    return q;
-}
-
-// Source row/column sampled by output index d, exactly as the plan's tables
-// hold it: bilinear floor(((2d+1) n_in - n_out) / (2 n_out)) folded into
-// [0, n_in - 1]; nearest floor(d n_in / n_out) kept below n_in.  The
-// producer needs only these indices (not the weights) to stage a tile, so it
-// derives them without touching global memory.
-template <int LINEAR>
-__device__ __forceinline__ int sample_index(int n_in, int n_out, int d)
-{
-    int s;
-    if (LINEAR)
-        s = floor_div_exact((2LL * d + 1) * n_in - n_out, 2 * n_out);
-    else
-        s = floor_div_exact(static_cast<long long>(d) * n_in, n_out);
-    return s < 0 ? 0 : (s > n_in - 1 ? n_in - 1 : s);
-}
+using namespace dev;
 
 // ------------------------------------------------------------------ tiles and stages
 
@@ -265,7 +61,8 @@ __device__ __forceinline__ TileGeom tile_geom(const KArgs &a, int tile)
     return g;
 }
 
-// Stage header, at the start of each stage.
+// Tile plan header, at the start of each plan entry: everything the copies
+// and the consumers need beyond the row list and slot map.
 struct StageHdr {
     int nrows;   // staged rows (-1: tile rejected)
     int b_lo;    // byte offset, within a source row, of slot byte 0
@@ -275,20 +72,24 @@ struct StageHdr {
     int image;   // image index within the batch
     int xsh;     // staged x (y) table entries start this many entries
     int ysh;     //   before the tile's first computed column (row): 0 or 1
+    int xa, xn;  // x table entries copied: [xa, xa + xn), even bounds
+    int ya, yn;  // y table entries copied: [ya, ya + yn), even bounds
+    int pad[4];
 };
+static_assert(sizeof(StageHdr) == 64, "plan header size");
 
 // Producer warp, part 1 (no global memory access): list the source rows of
-// `tile` into stage `st`.  Lanes derive the tile's column span and row
+// `tile` into plan entry `pl`.  Lanes derive the tile's column span and row
 // indices in parallel, one computed output row per lane; which rows are new
 // and where each lands in the list follow from warp votes (the sampled rows
 // never decrease along the output rows); lane 0 records the header.
 template <int LINEAR>
-__device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, int tile, int halo, int in_es)
+__device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *pl, int tile, int halo, int in_es)
 {
     const int lane = threadIdx.x & 31;
-    StageHdr *h = reinterpret_cast<StageHdr *>(st);
-    int *rows = reinterpret_cast<int *>(st + L.rows_off);
-    int *map = reinterpret_cast<int *>(st + L.map_off);
+    StageHdr *h = reinterpret_cast<StageHdr *>(pl);
+    int *rows = reinterpret_cast<int *>(pl + L.rows_off);
+    int *map = reinterpret_cast<int *>(pl + L.map_off);
     const TileGeom g = tile_geom(a, tile);
 
     const int cx0 = clampi(g.dx0 - halo, 0, a.OW - 1);
@@ -371,6 +172,12 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, int
         h->image = tile / (a.tiles_x * a.tiles_y);
         h->xsh = (g.dx0 - halo) & 1;
         h->ysh = (g.dy0 - halo) & 1;
+        // table entries of the computed columns dx0 - halo .. dx1 - 1 + halo
+        // and rows, widened to even bounds (16-byte copies)
+        h->xa = (g.dx0 - halo) & ~1;
+        h->xn = align_up(g.dx1 + halo, 2) - h->xa;
+        h->ya = (g.dy0 - halo) & ~1;
+        h->yn = align_up(g.dy1 + halo, 2) - h->ya;
     }
     __syncwarp();
 }
@@ -379,14 +186,14 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, int
 // `full` with the byte count before any copy is issued, and the copies are
 // spread over the lanes.  Plain path (unaligned source): the lanes copy the
 // bytes and each arrives on `full` (initialised for 32 arrivals).
-__device__ void fetch_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, uint64_t *full, uint64_t policy,
-                            const CUtensorMap *tmap, bool tables, int halo)
+__device__ void fetch_stage(const KArgs &a, const SmemLayout &L, const uint8_t *pl, uint8_t *st, uint64_t *full,
+                            uint64_t policy, const CUtensorMap *tmap, bool tables, int halo)
 {
     const int lane = threadIdx.x & 31;
-    const StageHdr *h = reinterpret_cast<const StageHdr *>(st);
-    const int *rows = reinterpret_cast<const int *>(st + L.rows_off);
+    const StageHdr *h = reinterpret_cast<const StageHdr *>(pl);
+    const int *rows = reinterpret_cast<const int *>(pl + L.rows_off);
     uint8_t *slots = st + L.slots_off;
-    const TileGeom g = tile_geom(a, h->tile);
+    const uint8_t *img = a.src + (long long)h->image * a.src_bstride;   // this tile's source image
     const int n = h->nrows, nbytes = h->nbytes, b_lo = h->b_lo;
     if (n < 0 && lane == 0)
         atomicExch(a.status, RZ_ERR_ARG);
@@ -397,8 +204,8 @@ __device__ void fetch_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, ui
         // end entries beyond both ends, which is the clamp
         int2 *tx = reinterpret_cast<int2 *>(st + L.tab_off);
         int2 *ty = tx + tab_x_entries(a.TW, halo);
-        const int xa = (g.dx0 - halo) & ~1, xb = align_up(g.dx1 + halo, 2);
-        const int ya = (g.dy0 - halo) & ~1, yb = align_up(g.dy1 + halo, 2);
+        const int xa = h->xa, xb = h->xa + h->xn;
+        const int ya = h->ya, yb = h->ya + h->yn;
         const uint32_t tab_bytes = static_cast<uint32_t>(8 * ((xb - xa) + (yb - ya)));
         if (a.tensor_in || a.tma_in) {
             uint32_t bytes = tab_bytes;
@@ -414,7 +221,7 @@ __device__ void fetch_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, ui
             if (!a.tensor_in) {
                 __syncwarp();
                 for (int r = lane; r < n; r += 32)
-                    bulk_load_hint(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch + b_lo,
+                    bulk_load_hint(slots + r * a.slot_bytes, img + (long long)rows[r] * a.src_pitch + b_lo,
                                    static_cast<uint32_t>(nbytes), full, policy);
             }
         } else {
@@ -427,7 +234,7 @@ __device__ void fetch_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, ui
                 bulk_load(ty, a.yt + ya, static_cast<uint32_t>(8 * (yb - ya)), full);
             }
             for (int r = 0; r < n; r++) {
-                const uint8_t *src = g.src + (long long)rows[r] * a.src_pitch + b_lo;
+                const uint8_t *src = img + (long long)rows[r] * a.src_pitch + b_lo;
                 uint8_t *d = slots + r * a.slot_bytes;
                 for (int k = lane; k < nbytes; k += 32)
                     d[k] = __ldg(src + k);
@@ -460,19 +267,19 @@ __device__ void fetch_stage(const KArgs &a, const SmemLayout &L, uint8_t *st, ui
                     int e = r + 1;
                     while (e < n && rows[e] == rows[e - 1] + 1)
                         e++;
-                    bulk_load_hint(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch,
+                    bulk_load_hint(slots + r * a.slot_bytes, img + (long long)rows[r] * a.src_pitch,
                                    static_cast<uint32_t>((e - r) * nbytes), full, policy);
                     r = e;
                 }
             }
         } else {
             for (int r = lane; r < n; r += 32)
-                bulk_load_hint(slots + r * a.slot_bytes, g.src + (long long)rows[r] * a.src_pitch + b_lo,
+                bulk_load_hint(slots + r * a.slot_bytes, img + (long long)rows[r] * a.src_pitch + b_lo,
                                static_cast<uint32_t>(nbytes), full, policy);
         }
     } else {
         for (int r = 0; r < n; r++) {
-            const uint8_t *src = g.src + (long long)rows[r] * a.src_pitch + b_lo;
+            const uint8_t *src = img + (long long)rows[r] * a.src_pitch + b_lo;
             uint8_t *d = slots + r * a.slot_bytes;
             for (int k = lane; k < nbytes; k += 32)
                 d[k] = __ldg(src + k);
@@ -529,14 +336,15 @@ struct StageView {
     int b_lo, slot_bytes;
 };
 
-__device__ __forceinline__ StageView stage_view(const KArgs &a, const SmemLayout &L, const uint8_t *st, int halo)
+__device__ __forceinline__ StageView stage_view(const KArgs &a, const SmemLayout &L, const uint8_t *pl,
+                                                const uint8_t *st, int halo)
 {
     StageView v;
-    const StageHdr *h = reinterpret_cast<const StageHdr *>(st);
+    const StageHdr *h = reinterpret_cast<const StageHdr *>(pl);
     v.tx = reinterpret_cast<const int2 *>(st + L.tab_off) + h->xsh;
     v.ty = reinterpret_cast<const int2 *>(st + L.tab_off) + tab_x_entries(a.TW, halo) + h->ysh;
     v.slots = st + L.slots_off;
-    v.map = reinterpret_cast<const int *>(st + L.map_off);
+    v.map = reinterpret_cast<const int *>(pl + L.map_off);
     v.b_lo = h->b_lo;
     v.slot_bytes = a.slot_bytes;
     return v;
@@ -995,10 +803,11 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a, const __g
         const uint64_t policy = policy_evict_first();
         // plan the first stages before waiting for the grids this launch
         // depends on: planning reads no global memory
+        const int NP = NS + 1;
         for (int k = 0; k < NS; k++) {
             const int t = blockIdx.x + k * G;
             if (t < ntiles)
-                plan_stage<LINEAR>(a, L, smem + L.stage_off + k * L.stage_bytes, t, HALO, IN_ES);
+                plan_stage<LINEAR>(a, L, smem + L.plan_off + k * L.plan_bytes, t, HALO, IN_ES);
         }
         grid_dependency_wait();
         int it = 0;
@@ -1012,9 +821,14 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a, const __g
                     ok = mbar_wait_bounded(&empty[s], ((it / NS) - 1) & 1, a.status);
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0))
                     break;
-                plan_stage<LINEAR>(a, L, st, t, HALO, IN_ES);
             }
-            fetch_stage(a, L, st, &full[s], policy, &tmap, fam_tables_in_stage(FAM), HALO);
+            fetch_stage(a, L, smem + L.plan_off + (it % NP) * L.plan_bytes, st, &full[s], policy, &tmap,
+                        fam_tables_in_stage(FAM), HALO);
+            // plan the next tile while the consumers work.  Tiles it - NS + 1
+            // .. it may still be in use; with NS + 1 plan entries the next
+            // tile's entry is none of theirs.
+            if (it + 1 >= NS && t + G < ntiles)
+                plan_stage<LINEAR>(a, L, smem + L.plan_off + ((it + 1) % NP) * L.plan_bytes, t + G, HALO, IN_ES);
         }
         return;
     }
@@ -1028,6 +842,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a, const __g
     for (int t = blockIdx.x; t < ntiles; t += G, ++it) {
         const int s = it % NS;
         uint8_t *st = smem + L.stage_off + s * L.stage_bytes;
+        const uint8_t *pl = smem + L.plan_off + (it % (NS + 1)) * L.plan_bytes;
         uint8_t *ob = smem + L.out_off + (it & 1) * L.out_bytes;
         // the output buffer is free once the store issued two tiles ago has read it
         if (threadIdx.x == 0 && it >= 2)
@@ -1039,12 +854,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a, const __g
         bool ok = true;
         if (threadIdx.x == 0)
             ok = mbar_wait_bounded(&full[s], (it / NS) & 1, a.status);
-        if (consumer_any(!ok) || reinterpret_cast<const StageHdr *>(st)->nrows < 0) {
+        if (consumer_any(!ok) || reinterpret_cast<const StageHdr *>(pl)->nrows < 0) {
             failed = true;
             break;
         }
         const TileGeom g = tile_geom(a, t);
-        const StageView sv = stage_view(a, L, st, HALO);
+        const StageView sv = stage_view(a, L, pl, st, HALO);
         if constexpr (OP == 0) {
             if constexpr (VAR == VAR_DOWN2)
                 compute_down2<C>(a, sv, g, ob, L.out_row_bytes);

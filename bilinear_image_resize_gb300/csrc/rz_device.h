@@ -1,0 +1,225 @@
+// Device helpers shared by the resize kernels (kernels.cu) and the 3x3
+// filter kernel (filter.cu): inline PTX for mbarriers, bulk (TMA) copies,
+// programmatic dependent launch and cache policies, and the exact sampling
+// index the producers derive without touching the tables.  Nothing here is
+// part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "rz_internal.h"
+
+namespace rz {
+namespace dev {
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Barrier among the consumer warps only (the producer warp never joins it).
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+// Consumer barrier that also returns whether `v` held on any consumer thread.
+__device__ __forceinline__ bool consumer_any(bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "n"(kConsumers)
+        : "memory");
+    return r != 0;
+}
+
+// One bounded wait attempt: the thread may be suspended in hardware until the
+// phase completes or about 0.5 ms pass (suspend-time hint), so waiting warps
+// do not spin through issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(500000u)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of the barrier, at most kWaitLimitNs.  Between
+// attempts the waiting warp sleeps (32 ns, doubling up to 256 ns) so that it
+// leaves the issue slots to the warps computing on the same scheduler.  On
+// time-out the status word (if given) records RZ_ERR_TIMEOUT and false is
+// returned.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    unsigned int nap = 32;
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+            if (status)
+                atomicExch(status, RZ_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(nap);
+        if (nap < 256)
+            nap <<= 1;
+    }
+    return true;
+}
+
+// Bulk copy global -> this CTA's shared memory, completing on `bar`, with an
+// L2 cache policy (createpolicy) attached.  Both addresses 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load_hint(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar,
+                                               uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_addr(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Tensor-map copy of one box {words, rows, 1} at coordinates {word, row,
+// image} into shared memory, completing on `bar`.  The map's elements are
+// 8-byte words and `word` is even, so the copy starts on a 16-byte boundary;
+// parts of the box outside the image are zero-filled, not read.
+__device__ __forceinline__ void tensor_load_3d(void *sdst, const CUtensorMap *map, int word, int row, int image,
+                                               uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(sdst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(word), "r"(row), "r"(image), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Bulk copy global -> this CTA's shared memory with the default L2 policy
+// (for the sampling tables, which every tile row reads again).
+__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// L2 policy for data read once: evicted first, so that the small sampling
+// tables (read by every launch) stay resident.
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Programmatic dependent launch: wait until the grids this launch depends on
+// have completed and their memory is visible; allow the next grid in the
+// stream to start launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// Bulk copy shared -> global (bulk-group completion).
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(ssrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N committed bulk-store groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the bulk-copy (async) proxy.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+__device__ __forceinline__ int ceil_log2(int v) { return v <= 1 ? 0 : 32 - __clz(v - 1); }
+
+// floor(num / den) for 0 < den <= 2^17 and |num / den| < 2^17 + 1, exactly:
+// the fast float quotient (num rounded to float, a division within 2 ulp)
+// is off by less than 2^-4 there, so its floor is within one of the true
+// floor, and 64-bit integer checks correct it.
+__device__ __forceinline__ int floor_div_exact(long long num, int den)
+{
+    int q = __float2int_rd(__fdividef(static_cast<float>(num), static_cast<float>(den)));
+    const long long qd = static_cast<long long>(q) * den;
+    if (qd > num)
+        q -= 1;
+    else if (qd + den <= num)
+        q += 1;
+    return q;
+}
+
+// Source row/column sampled by output index d, exactly as the plan's tables
+// hold it: bilinear floor(((2d+1) n_in - n_out) / (2 n_out)) folded into
+// [0, n_in - 1]; nearest floor(d n_in / n_out) kept below n_in.  The
+// producer needs only these indices (not the weights) to stage a tile, so it
+// derives them without touching global memory.
+template <int LINEAR>
+__device__ __forceinline__ int sample_index(int n_in, int n_out, int d)
+{
+    int s;
+    if (LINEAR)
+        s = floor_div_exact((2LL * d + 1) * n_in - n_out, 2 * n_out);
+    else
+        s = floor_div_exact(static_cast<long long>(d) * n_in, n_out);
+    return s < 0 ? 0 : (s > n_in - 1 ? n_in - 1 : s);
+}
+
+}  // namespace dev
+}  // namespace rz

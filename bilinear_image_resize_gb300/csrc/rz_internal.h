@@ -46,14 +46,19 @@ __host__ __device__ constexpr int fam_slot_pad(int fam) { return (fam == FAM_U8 
 // Byte offsets of the pieces of a CTA's dynamic shared memory.  Host and
 // device compute them with this one function.
 //
-//   [0, 64)                       per stage: a "full" and an "empty" mbarrier
-//   stages x stage_bytes          per stage: header {nrows, b_lo, nbytes, tile, first row, image},
-//                                 int rows[max_rows], int map[2 * computed rows],
-//                                 then max_rows staged row segments of slot_bytes
+//   [0, 128)                      per stage: a "full" and an "empty" mbarrier
+//   (stages + 1) x plan_bytes     tile plans: header {nrows, b_lo, nbytes, tile, first row, image,
+//                                 table ranges}, int rows[max_rows], int map[2 * computed rows]
+//   stages x stage_bytes          staged tiles: table entries (narrow-tile families), then
+//                                 max_rows staged row segments of slot_bytes
 //   2 x out_bytes                 double-buffered output tile
+// The plan ring has one entry more than the stage ring, so the producer can
+// plan the next tile while every stage is still in use.
 struct SmemLayout {
+    int plan_off, plan_bytes;
+    int rows_off, map_off;       // within a plan
     int stage_off, stage_bytes;
-    int rows_off, map_off, tab_off, slots_off;   // within a stage
+    int tab_off, slots_off;      // within a stage
     int mid_off;
     int out_off, out_bytes, out_row_bytes;
     int total;
@@ -65,15 +70,17 @@ __host__ __device__ inline SmemLayout smem_layout(int fam, int C, int TR, int TW
     SmemLayout L;
     const int halo = fam_halo(fam);
     const int nrc = TR + 2 * halo;
-    L.rows_off = 32;
+    L.plan_off = 128;
+    L.rows_off = 64;
     L.map_off = align_up(L.rows_off + 4 * max_rows, 16);
-    L.tab_off = align_up(L.map_off + 8 * nrc, 16);
+    L.plan_bytes = align_up(L.map_off + 8 * nrc, 16);
+    L.stage_off = align_up(L.plan_off + (stages + 1) * L.plan_bytes, 128);
     // the narrow-tile families stage the tile's table entries too:
     // x entries for the computed columns (+ slack), then y entries for the computed rows
     const int tab = fam_tables_in_stage(fam) ? 8 * (tab_x_entries(TW, halo) + tab_y_entries(TR, halo)) : 0;
-    L.slots_off = align_up(L.tab_off + tab, 128);
+    L.tab_off = 0;
+    L.slots_off = align_up(tab, 128);
     L.stage_bytes = align_up(L.slots_off + max_rows * slot_bytes, 128);
-    L.stage_off = 128;
     L.mid_off = L.stage_off + stages * L.stage_bytes;
     const int mid = 0;   // the 3x3 epilogue keeps its window in registers
     L.out_off = L.mid_off + mid;
@@ -86,6 +93,28 @@ __host__ __device__ inline SmemLayout smem_layout(int fam, int C, int TR, int TW
     }
     L.total = L.out_off + 2 * L.out_bytes;
     return L;
+}
+
+// 3x3 filter family (filter.cu): units of TW <= filter_strip(C) output columns
+// by TR output rows, whose source rows stream through a ring of chunks.  A
+// chunk holds up to chunk_rows rows; each row's span is cut into chunk_boxes
+// blocks of box_bytes (<= 2048, a multiple of 16), stored block-major: block
+// k of row i at k * block_bytes + i * box_bytes, block_bytes = chunk_rows *
+// box_bytes rounded up to 128.  Shared memory: ring_chunks "full" and
+// ring_chunks "empty" mbarriers, the producer's list window, then the chunks.
+// resized columns per consumer lane: two for one channel, else one
+__host__ __device__ constexpr int filter_lane_cols(int C) { return C == 1 ? 2 : 1; }
+// widest strip: eight consumer warps x (32 x lane columns - 2) output columns
+__host__ __device__ constexpr int filter_strip(int C) { return 8 * (32 * filter_lane_cols(C) - 2); }
+constexpr int kFilterChunkRows = 8;   // rows per chunk (a power of two)
+constexpr int kFilterRingMax = 128;   // ring rows (chunks x rows per chunk)
+__host__ __device__ constexpr int filter_block_bytes(int rows, int box_bytes) { return align_up(rows * box_bytes, 128); }
+// after the barriers: the producer's window of listed rows (kFilterListWindow ints)
+constexpr int kFilterListWindow = 128;
+__host__ __device__ constexpr int filter_chunks_off(int chunks) { return align_up(16 * chunks + 4 * kFilterListWindow, 128); }
+__host__ __device__ constexpr int filter_smem(int chunks, int rows, int boxes, int box_bytes)
+{
+    return filter_chunks_off(chunks) + chunks * boxes * filter_block_bytes(rows, box_bytes);
 }
 
 // Everything a resize kernel reads, passed by value in the parameter bank.
@@ -108,6 +137,10 @@ struct KArgs {
     int tensor_in;          // stage each tile with one tensor-map copy (box below)
     int box_words;          // box width in 8-byte words
     int box_rows;           // box height in rows
+    int ring_chunks;        // 3x3 filter: chunks in the ring (>= 2)
+    int chunk_rows;         // 3x3 filter: rows per chunk (1, 2, 4 or 8)
+    int chunk_boxes;        // 3x3 filter: blocks per row span
+    int box_bytes;          // 3x3 filter: bytes per block of a row
     const int2 *xt;         // per output column {source column, weight}; kTabPad clamped entries either side
     const int2 *yt;         // per output row    {source row, weight}; kTabPad clamped entries either side
     int *status;            // device status word (RZ_OK or RZ_ERR_TIMEOUT)
@@ -120,6 +153,9 @@ void record_cuda_error(int e);
 
 // Kernel entry for (family, mode, variant, C); nullptr if none.
 const void *kernel_for(int fam, int mode, int variant, int C);
+
+// The streaming 3x3 filter kernel for (mode, C); nullptr if none.
+const void *filter_kernel_for(int mode, int C);
 
 // Launch it on `grid` CTAs (asynchronous), optionally as a programmatic
 // dependent launch.  `tmap` describes the source when a.tensor_in is set

@@ -212,14 +212,18 @@ RZ_API int resize_last_cuda_error(void);
  * Tile override for tuning (0 = automatic): output rows and output columns
  * per CTA for kernel family `kind` (RZ_U8, RZ_F32, or 2 + RZ_EPI_* for the
  * fused kernels) of this plan.  Results do not depend on it; only speed does.
- * Rejected (RZ_ERR_ARG) if the tile would not fit in shared memory.
+ * For the 3x3 filter family a tile is one streamed unit: tile_rows output rows
+ * of a strip of tile_cols (at most 240) output columns.  A tile that does not
+ * fit in shared memory makes the next call of that family fail with
+ * RZ_ERR_ARG (RZ_ERR_UNSUPPORTED for the 3x3 filter family).
  */
 RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_cols);
 
 /*
  * Tuning and testing options of a plan (results never depend on them):
  *   RZ_OPT_STAGES       value 0 (automatic) or 1..4: source tiles each CTA
- *                       keeps in flight ahead of the one it computes;
+ *                       keeps in flight ahead of the one it computes (all
+ *                       families but the 3x3 filter, which streams rows);
  *   RZ_OPT_GENERIC_ONLY value 0 or 1: 1 disables the exact-ratio fast path
  *                       (uint8 2x downscale, used only when every table entry
  *                       is the 2x pattern, where it is bit-identical);
@@ -231,7 +235,10 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  *                       dependent launch, so that a resize queued right after
  *                       another kernel on the same stream starts its set-up
  *                       while that kernel finishes (it still reads and writes
- *                       memory only after that kernel has completed).
+ *                       memory only after that kernel has completed);
+ *   RZ_OPT_RING_ROWS    value 0 (automatic) or 2..128: source rows in the
+ *                       shared-memory ring through which each CTA of the 3x3
+ *                       filter family streams its strip.
  * Returns RZ_ERR_ARG for an unknown option or value.
  */
 #define RZ_OPT_STAGES 1
@@ -239,6 +246,7 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
 #define RZ_OPT_CTAS_PER_SM 3
 #define RZ_OPT_GRID_MODE 4
 #define RZ_OPT_PDL 5
+#define RZ_OPT_RING_ROWS 6
 RZ_API int resize_plan_set_option(rz_plan p, int option, int value);
 
 /*

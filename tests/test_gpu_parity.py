@@ -269,6 +269,62 @@ def test_filter_tile_shapes_do_not_change_results(rz):
         assert max_abs(dst.cpu().numpy(), want) <= F32_TOL, tile
 
 
+def run_filter(rz, img, OH, OW, w, opts=(), tile=None, src_pitch=None, src_off=0):
+    H, W, C = img.shape
+    src, _keep = device_image(img, src_pitch, src_off)
+    out = Canvas(OH, OW, C, torch.float32)
+    with rz.resize_plan_create(H, W, OH, OW, rz.RZ_LINEAR) as plan:
+        for k, v in opts:
+            rz.resize_plan_set_option(plan, k, v)
+        if tile:
+            rz.resize_plan_set_tile(plan, rz.KIND_FILTER3X3, *tile)
+        rz.resize_fused(plan, src, out.view, rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=w))
+        torch.cuda.synchronize()
+        assert rz.resize_plan_status(plan) == rz.RZ_OK
+    out.check_canary()
+    return out.result()
+
+
+def want_filter(img, OH, OW, w):
+    return np.stack([oracle.filter3x3(oracle.linear_f32(img[:, :, c:c + 1].copy(), OH, OW), w)
+                     for c in range(img.shape[2])], axis=-1)
+
+
+@pytest.mark.parametrize("ring", [2, 3, 5, 0])
+@pytest.mark.parametrize("ctas", [1, 0, "per_unit"])
+def test_filter_ring_and_grid_do_not_change_results(rz, ring, ctas):
+    # rings of two or three rows wrap every few rows and one CTA per SM makes
+    # each CTA walk many units, carrying ring slots and barrier phases across
+    # them; "per_unit" launches one CTA per unit
+    w = synth.filter_weights()
+    opts = [(rz.RZ_OPT_RING_ROWS, ring)]
+    if ctas == "per_unit":
+        opts += [(rz.RZ_OPT_GRID_MODE, 1), (rz.RZ_OPT_PDL, 0)]
+    else:
+        opts += [(rz.RZ_OPT_CTAS_PER_SM, ctas)]
+    for (H, W, C, OH, OW, tile) in [(300, 410, 1, 211, 173, None), (300, 410, 1, 211, 173, (7, 30)),
+                                    (97, 130, 3, 260, 333, (19, 64)), (640, 480, 4, 150, 170, (5, 240)),
+                                    (1500, 1200, 1, 1099, 877, None)]:
+        img = synth.random_f32((H, W, C), seed=H + W + C)
+        got = run_filter(rz, img, OH, OW, w, opts, tile)
+        err = max_abs(got, want_filter(img, OH, OW, w))
+        assert err <= F32_TOL * np.abs(w).sum(), (H, W, C, OH, OW, tile, err)
+
+
+def test_filter_unaligned_source_rows(rz):
+    # a source that is not 16-byte aligned (start or pitch) is copied by the
+    # producer warp's lanes instead of bulk copies
+    w = synth.filter_weights()
+    for (H, W, C, OH, OW, pitch, off) in [(120, 97, 1, 80, 61, 101, 1), (64, 75, 3, 99, 140, 75 * 3, 3),
+                                          (50, 33, 4, 40, 29, 33 * 4 + 2, 2)]:
+        img = synth.random_f32((H, W, C), seed=H * 3 + W)
+        for ring in (2, 0):
+            got = run_filter(rz, img, OH, OW, w, [(rz.RZ_OPT_RING_ROWS, ring), (rz.RZ_OPT_CTAS_PER_SM, 1)],
+                             src_pitch=pitch, src_off=off)
+            err = max_abs(got, want_filter(img, OH, OW, w))
+            assert err <= F32_TOL * np.abs(w).sum(), (H, W, C, OH, OW, ring, err)
+
+
 def test_non_default_stream(rz):
     img = synth.smooth_rgb(1920, 1080, 2)
     s = torch.cuda.Stream()
@@ -365,7 +421,8 @@ def test_exact_2x_path_tiles(rz, tile):
 def test_options_reject_bad_values(rz):
     with rz.resize_plan_create(8, 8, 4, 4, rz.RZ_LINEAR) as plan:
         for opt, val in [(rz.RZ_OPT_STAGES, 5), (rz.RZ_OPT_STAGES, -1), (rz.RZ_OPT_GENERIC_ONLY, 2),
-                         (rz.RZ_OPT_CTAS_PER_SM, 33), (rz.RZ_OPT_GRID_MODE, 2), (rz.RZ_OPT_PDL, 3), (99, 0)]:
+                         (rz.RZ_OPT_CTAS_PER_SM, 33), (rz.RZ_OPT_GRID_MODE, 2), (rz.RZ_OPT_PDL, 3),
+                         (rz.RZ_OPT_RING_ROWS, 1), (rz.RZ_OPT_RING_ROWS, 129), (99, 0)]:
             with pytest.raises(rz.ResizeError):
                 rz.resize_plan_set_option(plan, opt, val)
 
