@@ -162,16 +162,14 @@ int max_slot_bytes(const rz_plan_s &p, int fam, int C, int TW, bool pad = true)
 
 // Largest number of distinct source rows a tile of TR output rows stages,
 // counted exactly as the kernel lists them.
-int max_tile_rows(const rz_plan_s &p, int fam, int TR)
+int max_tile_rows(const rz_plan_s &p, int TR)
 {
-    const int halo = rz::fam_halo(fam);
     const bool lin = p.mode == RZ_LINEAR;
     int m = 0;
     for (int dy0 = 0; dy0 < p.OH; dy0 += TR) {
         const int dy1 = std::min(dy0 + TR, p.OH);
         int n = 0, last = -1;
-        for (int k = 0; k < dy1 - dy0 + 2 * halo; k++) {
-            const int dy = std::clamp(dy0 - halo + k, 0, p.OH - 1);
+        for (int dy = dy0; dy < dy1; dy++) {
             const int r0 = p.yofs[dy];
             const int r1 = lin ? std::min(r0 + 1, p.H - 1) : r0;
             if (r0 > last) { n++; last = r0; }
@@ -182,45 +180,15 @@ int max_tile_rows(const rz_plan_s &p, int fam, int TR)
     return m;
 }
 
-// Largest source row range (last row - first row + 1) a tile samples: the
-// height of the box that stages a tile with one tensor-map copy.
-int max_tile_row_range(const rz_plan_s &p, int fam, int TR)
-{
-    const int halo = rz::fam_halo(fam);
-    const bool lin = p.mode == RZ_LINEAR;
-    int m = 0;
-    for (int dy0 = 0; dy0 < p.OH; dy0 += TR) {
-        const int dy1 = std::min(dy0 + TR, p.OH);
-        const int first = p.yofs[std::clamp(dy0 - halo, 0, p.OH - 1)];
-        const int rl = p.yofs[std::clamp(dy1 - 1 + halo, 0, p.OH - 1)];
-        const int last = lin ? std::min(rl + 1, p.H - 1) : rl;
-        m = std::max(m, last - first + 1);
-    }
-    return m;
-}
-
 bool eval_tile(const rz_plan_s &p, int fam, int C, int TR, int TW, int stages, TileCfg *out, bool pad = true)
 {
     TileCfg t;
-    if (fam == rz::FAM_FILT)
-        TW = std::min(TW, 240);   // eight warps x 30 columns per tile
     t.TR = std::max(1, std::min(TR, p.OH));
     t.TW = std::max(1, std::min(TW, p.OW));
     t.tiles_x = (p.OW + t.TW - 1) / t.TW;
     t.tiles_y = (p.OH + t.TR - 1) / t.TR;
     t.slot_bytes = max_slot_bytes(p, fam, C, t.TW, pad);
-    t.max_rows = max_tile_rows(p, fam, t.TR);
-    if (fam == rz::FAM_FILT) {
-        // the 3x3 tiles are narrow and tall: stage each with one tensor-map
-        // box when it fits the box limits (256 eight-byte words by 256 rows)
-        const int range = max_tile_row_range(p, fam, t.TR);
-        if (t.slot_bytes % 16 == 0 && t.slot_bytes / 8 <= 256 && range <= 256) {
-            t.tensor = 1;
-            t.box_words = t.slot_bytes / 8;
-            t.box_rows = range;
-            t.max_rows = std::max(t.max_rows, range);
-        }
-    }
+    t.max_rows = max_tile_rows(p, t.TR);
     t.stages = stages;
     const SmemLayout L = rz::smem_layout(fam, C, t.TR, t.TW, t.max_rows, t.slot_bytes, stages);
     t.smem = static_cast<size_t>(L.total);
@@ -230,7 +198,6 @@ bool eval_tile(const rz_plan_s &p, int fam, int C, int TR, int TW, int stages, T
 
 constexpr int kSms = 152;                // GB300; the launch itself asks the device
 constexpr int kSoftSmem = 48 * 1024;     // keeps several CTAs resident per SM
-constexpr int kFilterSmem = 112 * 1024;  // two CTAs per SM for the 3x3 epilogue
 constexpr int kDefaultStages = 2;
 
 // True when the plan is an exact 2x downscale on both axes: every column and
@@ -249,27 +216,13 @@ bool is_down2(const rz_plan_s &p)
 // rows as wide as the output (or the widest power-of-two strip whose staged
 // row stays within 16 KB), narrowed while there are fewer than about twelve
 // tiles per SM (for balance across SMs), then as many output rows per tile as
-// keep the staged ring under 48 KB with that many tiles.  3x3 filter: strips
-// of 128 columns and up to 32 rows, so the one-pixel halo costs a few per cent.
+// keep the staged ring under 48 KB with that many tiles.  (The 3x3 filter
+// family streams strips instead: get_filter_tile.)
 TileCfg choose_tile(const rz_plan_s &p, int fam, int C, int batch, int stages, bool down2)
 {
     const int out_es = rz::fam_out_es(fam);
     const int px_bytes = fam == rz::FAM_NORM ? 4 : C * out_es;
     TileCfg best;
-    if (fam == rz::FAM_FILT) {
-        // the kernel's eight consumer warps emit 30 columns each: tiles are
-        // 240 columns wide (the whole output when narrower), as many rows as
-        // keep two CTAs per SM
-        const int TW = std::min(p.OW, 240);
-        for (int TR : {32, 24, 16, 8, 4, 2, 1}) {
-            TileCfg t;
-            if (eval_tile(p, fam, C, TR, TW, stages, &t) && t.smem <= static_cast<size_t>(kFilterSmem))
-                return t;
-        }
-        for (int TR : {4, 2, 1})
-            if (eval_tile(p, fam, C, TR, TW, 1, &best)) return best;
-        return best;
-    }
     if (down2) {
         // the exact 2x path computes little per byte, so the kernel is bound
         // by the source stream: two output rows (four consecutive source

@@ -296,96 +296,109 @@ __global__ void __launch_bounds__(kThreads, 3) k_filter_stream(const KArgs a, co
                 acc1[i][c] = acc2[i][c] = 0.0f;
         const int ncomp = g.dy1 - g.dy0 + 2;
         int n = 0, r1_before = -1;
-        unsigned bpk = 0, binfo = 0;   // lane j of the batch: packed row offsets, chunk info of row base + j
-        float bv = 0.0f;
+        // chunks of the previous row's taps (none yet: one below the unit's first)
+        unsigned c0_before = ucb - 1, c1_before = ucb - 1;
         int2 ye_next = a.yt[clampi(g.dy0 - 1 + lane, 0, a.OH - 1)];
-        for (int k = 0; k < ncomp; k++) {
-            if ((k & 31) == 0) {
-                // the next 32 resized rows: list positions of their taps, the
-                // ring chunks and shared-memory rows those land in (16-byte
-                // units: shared memory is below 2^20 bytes), and the chunks
-                // to hold; the table entries for the batch after are fetched
-                // meanwhile
-                const int nact = min(32, ncomp - k);
-                const int2 ye = ye_next;
-                ye_next = a.yt[clampi(g.dy0 - 1 + k + 32 + lane, 0, a.OH - 1)];
-                const int r1 = LINEAR ? min(ye.x + 1, a.H - 1) : ye.x;
-                const ListBatch lb = list_batch(ye.x, r1, lane < nact, n, r1_before, nact);
-                const unsigned c0 = ucb + (lb.s0 >> LG), c1 = ucb + (lb.s1 >> LG);
-                const unsigned top = ((c0 % NCH) * CB + (lb.s0 & (G - 1)) * BW) >> 4;
-                const unsigned bot = ((c1 % NCH) * CB + (lb.s1 & (G - 1)) * BW) >> 4;
-                bpk = top | (bot << 16);
-                binfo = (c1 << 1) | (c1 - c0);
-                bv = __int_as_float(ye.y);
+        for (int base = 0; base < ncomp && ok; base += 32) {
+            // the next 32 resized rows: list positions of their taps, the ring
+            // chunks and shared-memory rows those land in (16-byte units:
+            // shared memory is below 2^20 bytes), and which rows move to a new
+            // chunk; the table entries of the batch after are fetched meanwhile
+            const int nact = min(32, ncomp - base);
+            const int2 ye = ye_next;
+            ye_next = a.yt[clampi(g.dy0 - 1 + base + 32 + lane, 0, a.OH - 1)];
+            const int r1 = LINEAR ? min(ye.x + 1, a.H - 1) : ye.x;
+            const ListBatch lb = list_batch(ye.x, r1, lane < nact, n, r1_before, nact);
+            const unsigned bc0 = ucb + (lb.s0 >> LG), bc1 = ucb + (lb.s1 >> LG);
+            const unsigned top16 = ((bc0 % NCH) * CB + (lb.s0 & (G - 1)) * BW) >> 4;
+            const unsigned bot16 = ((bc1 % NCH) * CB + (lb.s1 & (G - 1)) * BW) >> 4;
+            const unsigned bpk = top16 | (bot16 << 16);
+            const float bv = __int_as_float(ye.y);
+            unsigned prev_c0 = __shfl_up_sync(0xffffffffu, bc0, 1);
+            unsigned prev_c1 = __shfl_up_sync(0xffffffffu, bc1, 1);
+            if (lane == 0) {
+                prev_c0 = c0_before;
+                prev_c1 = c1_before;
             }
-            const unsigned pk = __shfl_sync(0xffffffffu, bpk, k & 31);
-            const unsigned info = __shfl_sync(0xffffffffu, binfo, k & 31);
-            const float v = __shfl_sync(0xffffffffu, bv, k & 31);
-            const unsigned c1 = info >> 1, c0 = c1 - (info & 1u);
-            // release the chunks before this resized row's first tap (the
-            // previous step's reads are complete: their values were shuffled)
-            while (static_cast<int>(c0 - rch) > 0) {
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&empty[rslot]);
-                ++rch;
-                if (++rslot == NCH)
-                    rslot = 0;
-            }
-            // wait for every chunk up to the last tap's
-            if (static_cast<int>(c1 - wch) >= 0) {
-                do {
-                    if (!mbar_wait_bounded(&full[wslot], static_cast<uint32_t>(wphase), a.status))
-                        ok = false;
-                    ++wch;
-                    if (++wslot == NCH) {
-                        wslot = 0;
-                        wphase ^= 1;
+            // rows whose taps move to a later chunk: the first tap's move
+            // releases chunks, the second tap's waits for one
+            const unsigned events = __ballot_sync(0xffffffffu, lane < nact && (bc0 != prev_c0 || bc1 != prev_c1));
+            c0_before = __shfl_sync(0xffffffffu, bc0, nact - 1);
+            c1_before = __shfl_sync(0xffffffffu, bc1, nact - 1);
+            for (int j = 0; j < nact; j++) {
+                const int k = base + j;
+                const unsigned pk = __shfl_sync(0xffffffffu, bpk, j);
+                const float v = __shfl_sync(0xffffffffu, bv, j);
+                if ((events >> j) & 1u) {
+                    const unsigned c0 = __shfl_sync(0xffffffffu, bc0, j);
+                    const unsigned c1 = __shfl_sync(0xffffffffu, bc1, j);
+                    // release the chunks before this row's first tap (the
+                    // previous rows' reads are complete: their values were
+                    // shuffled)
+                    while (static_cast<int>(c0 - rch) > 0) {
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(&empty[rslot]);
+                        ++rch;
+                        if (++rslot == NCH)
+                            rslot = 0;
                     }
-                } while (static_cast<int>(c1 - wch) >= 0);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
+                    // wait for every chunk up to the second tap's
+                    while (static_cast<int>(c1 - wch) >= 0) {
+                        if (!mbar_wait_bounded(&full[wslot], static_cast<uint32_t>(wphase), a.status))
+                            ok = false;
+                        ++wch;
+                        if (++wslot == NCH) {
+                            wslot = 0;
+                            wphase ^= 1;
+                        }
+                    }
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        ok = false;
+                        break;
+                    }
                 }
+                const float *top = fchunks + (pk & 0xffffu) * 4;
+                const float *bot = fchunks + (pk >> 16) * 4;
+                const bool store = k >= 2;
+#pragma unroll
+                for (int c = 0; c < C; c++) {
+                    float m[NCOL], l[NCOL], r[NCOL];
+#pragma unroll
+                    for (int i = 0; i < NCOL; i++) {
+                        const float t0 = top[off0[i][c]], t1 = top[off1[i][c]];
+                        const float b0 = bot[off0[i][c]], b1 = bot[off1[i][c]];
+                        const float hT = fmaf(uw[i], t1 - t0, t0);
+                        const float hB = fmaf(uw[i], b1 - b0, b0);
+                        m[i] = fmaf(v, hB - hT, hT);
+                    }
+                    if constexpr (NCOL == 1) {
+                        l[0] = __shfl_up_sync(0xffffffffu, m[0], 1);
+                        r[0] = __shfl_down_sync(0xffffffffu, m[0], 1);
+                    } else {
+                        // e = lane and e = lane + 32: the two halves meet
+                        // between lane 31's first column and lane 0's second
+                        l[0] = __shfl_up_sync(0xffffffffu, m[0], 1);
+                        r[0] = __shfl_sync(0xffffffffu, lane == 0 ? m[1] : m[0], (lane + 1) & 31);
+                        l[1] = __shfl_sync(0xffffffffu, lane == 31 ? m[0] : m[1], (lane + 31) & 31);
+                        r[1] = __shfl_down_sync(0xffffffffu, m[1], 1);
+                    }
+#pragma unroll
+                    for (int i = 0; i < NCOL; i++) {
+                        // this row is row a = -1 of output k, a = 0 of k - 1,
+                        // a = +1 of k - 2
+                        const float a0 = fmaf(a.w[2], r[i], fmaf(a.w[1], m[i], a.w[0] * l[i]));
+                        const float a1 = fmaf(a.w[5], r[i], fmaf(a.w[4], m[i], fmaf(a.w[3], l[i], acc1[i][c])));
+                        const float a2 = fmaf(a.w[8], r[i], fmaf(a.w[7], m[i], fmaf(a.w[6], l[i], acc2[i][c])));
+                        if (store && emit[i])
+                            __stcs(reinterpret_cast<float *>(op) + (rel0 + 32 * i) * C + c, a2);
+                        acc2[i][c] = a1;
+                        acc1[i][c] = a0;
+                    }
+                }
+                if (store)
+                    op += a.dst_pitch;
             }
-            const float *top = fchunks + (pk & 0xffffu) * 4;
-            const float *bot = fchunks + (pk >> 16) * 4;
-#pragma unroll
-            for (int c = 0; c < C; c++) {
-                float m[NCOL], l[NCOL], r[NCOL];
-#pragma unroll
-                for (int i = 0; i < NCOL; i++) {
-                    const float t0 = top[off0[i][c]], t1 = top[off1[i][c]];
-                    const float b0 = bot[off0[i][c]], b1 = bot[off1[i][c]];
-                    const float hT = fmaf(uw[i], t1 - t0, t0);
-                    const float hB = fmaf(uw[i], b1 - b0, b0);
-                    m[i] = fmaf(v, hB - hT, hT);
-                }
-                if constexpr (NCOL == 1) {
-                    l[0] = __shfl_up_sync(0xffffffffu, m[0], 1);
-                    r[0] = __shfl_down_sync(0xffffffffu, m[0], 1);
-                } else {
-                    // e = lane and e = lane + 32: the two halves meet between
-                    // lane 31's first column and lane 0's second
-                    l[0] = __shfl_up_sync(0xffffffffu, m[0], 1);
-                    r[0] = __shfl_sync(0xffffffffu, lane == 0 ? m[1] : m[0], (lane + 1) & 31);
-                    l[1] = __shfl_sync(0xffffffffu, lane == 31 ? m[0] : m[1], (lane + 31) & 31);
-                    r[1] = __shfl_down_sync(0xffffffffu, m[1], 1);
-                }
-#pragma unroll
-                for (int i = 0; i < NCOL; i++) {
-                    // this row is row a = -1 of output k, a = 0 of k - 1, a = +1 of k - 2
-                    const float a0 = fmaf(a.w[2], r[i], fmaf(a.w[1], m[i], a.w[0] * l[i]));
-                    const float a1 = fmaf(a.w[5], r[i], fmaf(a.w[4], m[i], fmaf(a.w[3], l[i], acc1[i][c])));
-                    const float a2 = fmaf(a.w[8], r[i], fmaf(a.w[7], m[i], fmaf(a.w[6], l[i], acc2[i][c])));
-                    if (k >= 2 && emit[i])
-                        __stcs(reinterpret_cast<float *>(op) + (rel0 + 32 * i) * C + c, a2);
-                    acc2[i][c] = a1;
-                    acc1[i][c] = a0;
-                }
-            }
-            if (k >= 2)
-                op += a.dst_pitch;
         }
         if (!ok)
             break;

@@ -1,17 +1,19 @@
-// Resize kernels for sm_103a.
+// Resize kernels for sm_103a: uint8 and float32 resize and the normalise
+// epilogue (the 3x3 filter epilogue streams strips instead: filter.cu).
 //
 // Persistent CTAs (as many as fit on the GPU at once) walk the output tiles
 // of TR rows x TW columns in a static round-robin.  Each CTA is warp
 // specialised:
 //   * one producer warp keeps a ring of `stages` tiles of source rows in
-//     shared memory.  For each tile it loads the tile's row table entries
-//     with all 32 lanes in one round trip, lists the distinct source rows the
-//     tile's output rows sample (two per row for bilinear, one for nearest,
-//     plus a one-row halo for the 3x3 epilogue) and issues one bulk (TMA)
-//     copy per row, from several lanes, for the needed column span,
-//     completing on the stage's "full" mbarrier.  It refills a stage as soon
-//     as the consumers release it on the stage's "empty" mbarrier.  When the
-//     source is not 16-byte aligned the warp copies the rows itself;
+//     shared memory.  It plans each tile in a ring of stages + 1 plan
+//     entries one tile ahead: the tile's column span and the distinct source
+//     rows its output rows sample (two per row for bilinear, one for
+//     nearest), derived exactly from the sampling formula with warp votes,
+//     without reading memory.  When the consumers release a stage (its
+//     "empty" mbarrier) it issues one bulk (TMA) copy per row, or per run of
+//     whole consecutive rows, completing on the stage's "full" mbarrier; the
+//     normalise family's table entries come along as two more bulk copies.
+//     When the source is not 16-byte aligned the warp copies the rows itself;
 //   * eight consumer warps compute each tile from shared memory into one of
 //     two output buffers (uint8 bilinear as the exact 11-bit fixed-point sum,
 //     float32 as two lerps, then the fused epilogue), and one consumer thread
@@ -68,13 +70,12 @@ struct StageHdr {
     int b_lo;    // byte offset, within a source row, of slot byte 0
     int nbytes;  // bytes staged per row
     int tile;    // tile index
-    int row0;    // first staged source row (tensor-map staging)
     int image;   // image index within the batch
     int xsh;     // staged x (y) table entries start this many entries
-    int ysh;     //   before the tile's first computed column (row): 0 or 1
+    int ysh;     //   before the tile's first column (row): 0 or 1
     int xa, xn;  // x table entries copied: [xa, xa + xn), even bounds
     int ya, yn;  // y table entries copied: [ya, ya + yn), even bounds
-    int pad[4];
+    int pad[5];
 };
 static_assert(sizeof(StageHdr) == 64, "plan header size");
 
@@ -84,7 +85,7 @@ static_assert(sizeof(StageHdr) == 64, "plan header size");
 // and where each lands in the list follow from warp votes (the sampled rows
 // never decrease along the output rows); lane 0 records the header.
 template <int LINEAR>
-__device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *pl, int tile, int halo, int in_es)
+__device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *pl, int tile, int in_es)
 {
     const int lane = threadIdx.x & 31;
     StageHdr *h = reinterpret_cast<StageHdr *>(pl);
@@ -92,15 +93,13 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *pl, int
     int *map = reinterpret_cast<int *>(pl + L.map_off);
     const TileGeom g = tile_geom(a, tile);
 
-    const int cx0 = clampi(g.dx0 - halo, 0, a.OW - 1);
-    const int cx1 = clampi(g.dx1 - 1 + halo, 0, a.OW - 1);
-    const int nrc = (g.dy1 - g.dy0) + 2 * halo;
+    const int nrc = g.dy1 - g.dy0;   // output rows of the tile
     int xv = 0;
     if (lane < 2)
-        xv = sample_index<LINEAR>(a.W, a.OW, lane == 0 ? cx0 : cx1);
+        xv = sample_index<LINEAR>(a.W, a.OW, lane == 0 ? g.dx0 : g.dx1 - 1);
     int yv = 0;
     if (lane < nrc)
-        yv = sample_index<LINEAR>(a.H, a.OH, clampi(g.dy0 - halo + lane, 0, a.OH - 1));
+        yv = sample_index<LINEAR>(a.H, a.OH, g.dy0 + lane);
     const int xs0 = __shfl_sync(0xffffffffu, xv, 0);
     const int xs1r = __shfl_sync(0xffffffffu, xv, 1);
     const int xs1 = LINEAR ? min(xs1r + 1, a.W - 1) : xs1r;
@@ -112,13 +111,13 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *pl, int
     }
     const int nbytes = b_hi - b_lo;
 
-    // Distinct source rows.  Lane k takes computed row k (32 rows per pass)
+    // Distinct source rows.  Lane k takes output row k (32 rows per pass)
     // with taps r0 <= r1 <= r0 + 1.  Taps never decrease along k, so r0 is
     // already listed exactly when r0 <= r1 of row k - 1, and is then the last
     // or the one-before-last entry listed before row k; r1 is new exactly
     // when it exceeds both.  Counts of new taps on lower lanes (ballots) give
     // each tap its slot.
-    int n = 0, r1_before = -1, row0 = 0;
+    int n = 0, r1_before = -1;
     bool overflow = nbytes > a.slot_bytes;
     const unsigned lower = (1u << lane) - 1u;
     for (int base = 0; base < nrc; base += 32) {
@@ -126,7 +125,7 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *pl, int
         const bool act = k < nrc;
         int r0 = 0x7fffffff, r1 = 0x7fffffff;
         if (act) {
-            r0 = k < 32 ? yv : sample_index<LINEAR>(a.H, a.OH, clampi(g.dy0 - halo + k, 0, a.OH - 1));
+            r0 = k < 32 ? yv : sample_index<LINEAR>(a.H, a.OH, g.dy0 + k);
             r1 = LINEAR ? min(r0 + 1, a.H - 1) : r0;
         }
         int prev_r1 = __shfl_up_sync(0xffffffffu, r1, 1);
@@ -144,40 +143,27 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *pl, int
             map[2 * k] = s0;
             map[2 * k + 1] = s1;
         }
-        if (base == 0)
-            row0 = __shfl_sync(0xffffffffu, r0, 0);
         n += __popc(b0) + __popc(b1);
         r1_before = __shfl_sync(0xffffffffu, r1, min(31, nrc - 1 - base));
     }
     if (n > a.max_rows)
         overflow = true;
-    if (a.tensor_in && !overflow && n > 0) {
-        // one box holds the whole row range: slot = row - first row
-        const int range = r1_before - row0 + 1;
-        if (range > a.box_rows)
-            overflow = true;
-        __syncwarp();
-        for (int k = lane; k < 2 * nrc && !overflow; k += 32)
-            map[k] = rows[map[k]] - row0;
-        n = range;
-    }
     if (lane == 0) {
-        // the host sizes max_rows, slot_bytes and the box from the same
-        // indices, so an overflow is unreachable; it guards shared memory
+        // the host sizes max_rows and slot_bytes from the same indices, so
+        // an overflow is unreachable; it guards shared memory
         h->nrows = overflow ? -1 : n;
         h->b_lo = b_lo;
         h->nbytes = nbytes;
         h->tile = tile;
-        h->row0 = row0;
         h->image = tile / (a.tiles_x * a.tiles_y);
-        h->xsh = (g.dx0 - halo) & 1;
-        h->ysh = (g.dy0 - halo) & 1;
-        // table entries of the computed columns dx0 - halo .. dx1 - 1 + halo
-        // and rows, widened to even bounds (16-byte copies)
-        h->xa = (g.dx0 - halo) & ~1;
-        h->xn = align_up(g.dx1 + halo, 2) - h->xa;
-        h->ya = (g.dy0 - halo) & ~1;
-        h->yn = align_up(g.dy1 + halo, 2) - h->ya;
+        h->xsh = g.dx0 & 1;
+        h->ysh = g.dy0 & 1;
+        // table entries of the tile's columns and rows, widened to even
+        // bounds (16-byte copies)
+        h->xa = g.dx0 & ~1;
+        h->xn = align_up(g.dx1, 2) - h->xa;
+        h->ya = g.dy0 & ~1;
+        h->yn = align_up(g.dy1, 2) - h->ya;
     }
     __syncwarp();
 }
@@ -187,7 +173,7 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *pl, int
 // spread over the lanes.  Plain path (unaligned source): the lanes copy the
 // bytes and each arrives on `full` (initialised for 32 arrivals).
 __device__ void fetch_stage(const KArgs &a, const SmemLayout &L, const uint8_t *pl, uint8_t *st, uint64_t *full,
-                            uint64_t policy, const CUtensorMap *tmap, bool tables, int halo)
+                            uint64_t policy, bool tables)
 {
     const int lane = threadIdx.x & 31;
     const StageHdr *h = reinterpret_cast<const StageHdr *>(pl);
@@ -198,32 +184,25 @@ __device__ void fetch_stage(const KArgs &a, const SmemLayout &L, const uint8_t *
     if (n < 0 && lane == 0)
         atomicExch(a.status, RZ_ERR_ARG);
     if (tables) {
-        // the tile's x entries (computed columns dx0 - halo .. dx1 - 1 + halo)
-        // and y entries (computed rows), each one bulk copy of a range that
-        // starts and ends on an even entry; the plan's tables repeat their
-        // end entries beyond both ends, which is the clamp
+        // the tile's x entries and y entries, each one bulk copy of a range
+        // that starts and ends on an even entry (the plan's tables repeat
+        // their end entries past both ends)
         int2 *tx = reinterpret_cast<int2 *>(st + L.tab_off);
-        int2 *ty = tx + tab_x_entries(a.TW, halo);
+        int2 *ty = tx + tab_x_entries(a.TW);
         const int xa = h->xa, xb = h->xa + h->xn;
         const int ya = h->ya, yb = h->ya + h->yn;
         const uint32_t tab_bytes = static_cast<uint32_t>(8 * ((xb - xa) + (yb - ya)));
-        if (a.tensor_in || a.tma_in) {
-            uint32_t bytes = tab_bytes;
-            if (n > 0)
-                bytes += static_cast<uint32_t>(a.tensor_in ? a.box_rows * a.box_words * 8 : n * nbytes);
+        if (a.tma_in) {
+            const uint32_t bytes = tab_bytes + static_cast<uint32_t>(n > 0 ? n * nbytes : 0);
             if (lane == 0) {
                 mbar_arrive_expect_tx(full, bytes);
                 bulk_load(tx, a.xt + xa, static_cast<uint32_t>(8 * (xb - xa)), full);
                 bulk_load(ty, a.yt + ya, static_cast<uint32_t>(8 * (yb - ya)), full);
-                if (a.tensor_in && n > 0)
-                    tensor_load_3d(slots, tmap, b_lo / 8, h->row0, h->image, full, policy);
             }
-            if (!a.tensor_in) {
-                __syncwarp();
-                for (int r = lane; r < n; r += 32)
-                    bulk_load_hint(slots + r * a.slot_bytes, img + (long long)rows[r] * a.src_pitch + b_lo,
-                                   static_cast<uint32_t>(nbytes), full, policy);
-            }
+            __syncwarp();
+            for (int r = lane; r < n; r += 32)
+                bulk_load_hint(slots + r * a.slot_bytes, img + (long long)rows[r] * a.src_pitch + b_lo,
+                               static_cast<uint32_t>(nbytes), full, policy);
         } else {
             // the tables still move as bulk copies (armed before any lane
             // arrives); the unaligned rows are copied by the lanes, each of
@@ -241,16 +220,6 @@ __device__ void fetch_stage(const KArgs &a, const SmemLayout &L, const uint8_t *
             }
             __syncwarp();
             mbar_arrive(full);
-        }
-    } else if (a.tensor_in) {
-        // one tensor-map copy of the box {granules x box_rows} at the tile's
-        // first row; the box is what the barrier counts, whatever part of it
-        // the tile uses
-        if (lane == 0) {
-            const uint32_t box = static_cast<uint32_t>(a.box_rows * a.box_words * 8);
-            mbar_arrive_expect_tx(full, n > 0 ? box : 0u);
-            if (n > 0)
-                tensor_load_3d(slots, tmap, b_lo / 8, h->row0, h->image, full, policy);
         }
     } else if (a.tma_in) {
         // a rejected tile completes the phase with no bytes
@@ -337,12 +306,12 @@ struct StageView {
 };
 
 __device__ __forceinline__ StageView stage_view(const KArgs &a, const SmemLayout &L, const uint8_t *pl,
-                                                const uint8_t *st, int halo)
+                                                const uint8_t *st)
 {
     StageView v;
     const StageHdr *h = reinterpret_cast<const StageHdr *>(pl);
     v.tx = reinterpret_cast<const int2 *>(st + L.tab_off) + h->xsh;
-    v.ty = reinterpret_cast<const int2 *>(st + L.tab_off) + tab_x_entries(a.TW, halo) + h->ysh;
+    v.ty = reinterpret_cast<const int2 *>(st + L.tab_off) + tab_x_entries(a.TW) + h->ysh;
     v.slots = st + L.slots_off;
     v.map = reinterpret_cast<const int *>(pl + L.map_off);
     v.b_lo = h->b_lo;
@@ -703,80 +672,14 @@ __device__ void compute_normalize(const KArgs &a, const StageView &sv, const Til
 // (taken with warp shuffles) in registers, so every output is nine fmaf on
 // registers:  z = sum w[i*3+j] * r[row-1+i][col-1+j].  Lanes 0 and 31 only
 // supply the neighbours of lanes 1 and 30.
-template <int C>
-__device__ void compute_filter3x3(const KArgs &a, const StageView &sv, const TileGeom &g, uint8_t *ob_bytes,
-                                  int orow_bytes)
-{
-    constexpr int COLS = 30;                       // output columns per warp
-    const float *slots = reinterpret_cast<const float *>(sv.slots);
-    float *ob = reinterpret_cast<float *>(ob_bytes);
-    const int lo = sv.b_lo / 4;
-    const int slot_el = sv.slot_bytes / 4;
-    const int orow_el = orow_bytes / 4;
-    const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int col = warp * COLS + lane - 1;        // output column of this lane, relative to dx0
-    if (warp * COLS >= nc)
-        return;                                    // no output column for this warp (narrow tile)
-    // the staged x entries cover columns dx0 - 1 .. dx1 (clamped); lanes past
-    // the last output column of a narrow tile reuse the last entry and emit
-    // nothing
-    const int2 xw = sv.tx[min(col + 1, nc + 1)];
-    const float u = __int_as_float(xw.y);
-    const int o0 = xw.x * C - lo, o1 = min(xw.x + 1, a.W - 1) * C - lo;
-    const bool emit = lane >= 1 && lane <= COLS && col < nc;
-    float m[3][C], l[3][C], r[3][C];               // rows k-2, k-1, k of own column and neighbours
-#pragma unroll
-    for (int i = 0; i < 3; i++)
-#pragma unroll
-        for (int c = 0; c < C; c++)
-            m[i][c] = l[i][c] = r[i][c] = 0.0f;
-    for (int k = 0; k < nr + 2; k++) {
-        const float v = __int_as_float(sv.ty[k].y);
-        const float *top = slots + sv.map[2 * k] * slot_el;
-        const float *bot = slots + sv.map[2 * k + 1] * slot_el;
-#pragma unroll
-        for (int c = 0; c < C; c++) {
-            m[0][c] = m[1][c];
-            m[1][c] = m[2][c];
-            l[0][c] = l[1][c];
-            l[1][c] = l[2][c];
-            r[0][c] = r[1][c];
-            r[1][c] = r[2][c];
-            const float t0 = top[o0 + c], t1 = top[o1 + c];
-            const float b0 = bot[o0 + c], b1 = bot[o1 + c];
-            const float hT = fmaf(u, t1 - t0, t0);
-            const float hB = fmaf(u, b1 - b0, b0);
-            const float val = fmaf(v, hB - hT, hT);
-            m[2][c] = val;
-            l[2][c] = __shfl_up_sync(0xffffffffu, val, 1);
-            r[2][c] = __shfl_down_sync(0xffffffffu, val, 1);
-        }
-        if (k >= 2 && emit) {
-#pragma unroll
-            for (int c = 0; c < C; c++) {
-                float z = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 3; i++) {
-                    z = fmaf(a.w[i * 3 + 0], l[i][c], z);
-                    z = fmaf(a.w[i * 3 + 1], m[i][c], z);
-                    z = fmaf(a.w[i * 3 + 2], r[i][c], z);
-                }
-                ob[(k - 2) * orow_el + col * C + c] = z;
-            }
-        }
-    }
-}
-
 // ------------------------------------------------------------------ the persistent kernel
 
-// OP: 0 plain resize (T, C, LINEAR, VAR), 1 normalise, 2 3x3 filter.
+// OP: 0 plain resize (T, C, LINEAR, VAR), 1 normalise.
 template <int OP, typename T, int C, int LINEAR, int VAR>
-__global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a, const __grid_constant__ CUtensorMap tmap)
+__global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a, const __grid_constant__ CUtensorMap)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int FAM = OP == 1 ? FAM_NORM : (OP == 2 ? FAM_FILT : (sizeof(T) == 1 ? FAM_U8 : FAM_F32));
-    constexpr int HALO = OP == 2 ? 1 : 0;
+    constexpr int FAM = OP == 1 ? FAM_NORM : (sizeof(T) == 1 ? FAM_U8 : FAM_F32);
     constexpr int IN_ES = fam_in_es(FAM);
     constexpr int PLANES = OP == 1 ? C : 1;
     constexpr int PX_BYTES = OP == 1 ? 4 : C * fam_out_es(FAM);
@@ -807,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a, const __g
         for (int k = 0; k < NS; k++) {
             const int t = blockIdx.x + k * G;
             if (t < ntiles)
-                plan_stage<LINEAR>(a, L, smem + L.plan_off + k * L.plan_bytes, t, HALO, IN_ES);
+                plan_stage<LINEAR>(a, L, smem + L.plan_off + k * L.plan_bytes, t, IN_ES);
         }
         grid_dependency_wait();
         int it = 0;
@@ -822,13 +725,13 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a, const __g
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0))
                     break;
             }
-            fetch_stage(a, L, smem + L.plan_off + (it % NP) * L.plan_bytes, st, &full[s], policy, &tmap,
-                        fam_tables_in_stage(FAM), HALO);
+            fetch_stage(a, L, smem + L.plan_off + (it % NP) * L.plan_bytes, st, &full[s], policy,
+                        fam_tables_in_stage(FAM));
             // plan the next tile while the consumers work.  Tiles it - NS + 1
             // .. it may still be in use; with NS + 1 plan entries the next
             // tile's entry is none of theirs.
             if (it + 1 >= NS && t + G < ntiles)
-                plan_stage<LINEAR>(a, L, smem + L.plan_off + ((it + 1) % NP) * L.plan_bytes, t + G, HALO, IN_ES);
+                plan_stage<LINEAR>(a, L, smem + L.plan_off + ((it + 1) % NP) * L.plan_bytes, t + G, IN_ES);
         }
         return;
     }
@@ -859,16 +762,14 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a, const __g
             break;
         }
         const TileGeom g = tile_geom(a, t);
-        const StageView sv = stage_view(a, L, pl, st, HALO);
+        const StageView sv = stage_view(a, L, pl, st);
         if constexpr (OP == 0) {
             if constexpr (VAR == VAR_DOWN2)
                 compute_down2<C>(a, sv, g, ob, L.out_row_bytes);
             else
                 compute_generic<T, C, LINEAR>(a, sv, g, ob, L.out_row_bytes);
-        } else if constexpr (OP == 1) {
-            compute_normalize<C>(a, sv, g, ob, L.out_row_bytes);
         } else {
-            compute_filter3x3<C>(a, sv, g, ob, L.out_row_bytes);
+            compute_normalize<C>(a, sv, g, ob, L.out_row_bytes);
         }
         fence_proxy_async_smem();
         consumer_sync();
@@ -910,7 +811,6 @@ const void *kernel_for(int fam, int mode, int variant, int C)
         {k_resize<0, float, 1, 1, 0>, k_resize<0, float, 3, 1, 0>, k_resize<0, float, 4, 1, 0>}};
     static const Fn norm[3] = {k_resize<1, uint8_t, 1, 1, 0>, k_resize<1, uint8_t, 3, 1, 0>,
                                k_resize<1, uint8_t, 4, 1, 0>};
-    static const Fn filt[3] = {k_resize<2, float, 1, 1, 0>, k_resize<2, float, 3, 1, 0>, k_resize<2, float, 4, 1, 0>};
     const int m = mode == RZ_LINEAR ? 1 : 0;
     switch (fam) {
     case FAM_U8:
@@ -919,7 +819,6 @@ const void *kernel_for(int fam, int mode, int variant, int C)
         return reinterpret_cast<const void *>(u8[m][ci]);
     case FAM_F32: return reinterpret_cast<const void *>(f32[m][ci]);
     case FAM_NORM: return m ? reinterpret_cast<const void *>(norm[ci]) : nullptr;
-    case FAM_FILT: return m ? reinterpret_cast<const void *>(filt[ci]) : nullptr;
     default: return nullptr;
     }
 }

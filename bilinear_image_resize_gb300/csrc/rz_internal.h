@@ -29,14 +29,14 @@ __host__ __device__ constexpr int fam_in_es(int fam) { return (fam == FAM_U8 || 
 __host__ __device__ constexpr int fam_out_es(int fam) { return fam == FAM_U8 ? 1 : 4; }
 __host__ __device__ constexpr int fam_halo(int fam) { return fam == FAM_FILT ? 1 : 0; }
 // Families whose producer also stages the tile's sampling-table entries.
-__host__ __device__ constexpr bool fam_tables_in_stage(int fam) { return fam == FAM_NORM || fam == FAM_FILT; }
+__host__ __device__ constexpr bool fam_tables_in_stage(int fam) { return fam == FAM_NORM; }
 // Staged table entries: a tile's x (y) entries are copied in one bulk copy
 // that starts on an even entry, so one entry of slack at each end.
-__host__ __device__ constexpr int tab_x_entries(int TW, int halo) { return align_up(TW + 2 * halo + 8, 2); }
-__host__ __device__ constexpr int tab_y_entries(int TR, int halo) { return align_up(TR + 2 * halo + 4, 2); }
+__host__ __device__ constexpr int tab_x_entries(int TW) { return align_up(TW + 8, 2); }
+__host__ __device__ constexpr int tab_y_entries(int TR) { return align_up(TR + 4, 2); }
 // Entries before and after each of the plan's device tables that repeat the
-// first and last entry (the clamp of the 3x3 halo), so that any tile's range
-// of entries is one contiguous copy.
+// first and last entry, so that a tile's range of entries widened to even
+// bounds (one bulk copy) stays inside the allocation and reads as the clamp.
 constexpr int kTabPad = 8;
 
 // Padding after each staged row: the uint8 bilinear tap reads are 32-bit
@@ -47,9 +47,9 @@ __host__ __device__ constexpr int fam_slot_pad(int fam) { return (fam == FAM_U8 
 // device compute them with this one function.
 //
 //   [0, 128)                      per stage: a "full" and an "empty" mbarrier
-//   (stages + 1) x plan_bytes     tile plans: header {nrows, b_lo, nbytes, tile, first row, image,
-//                                 table ranges}, int rows[max_rows], int map[2 * computed rows]
-//   stages x stage_bytes          staged tiles: table entries (narrow-tile families), then
+//   (stages + 1) x plan_bytes     tile plans: header {nrows, b_lo, nbytes, tile, image,
+//                                 table ranges}, int rows[max_rows], int map[2 * output rows]
+//   stages x stage_bytes          staged tiles: table entries (normalise family), then
 //                                 max_rows staged row segments of slot_bytes
 //   2 x out_bytes                 double-buffered output tile
 // The plan ring has one entry more than the stage ring, so the producer can
@@ -59,7 +59,6 @@ struct SmemLayout {
     int rows_off, map_off;       // within a plan
     int stage_off, stage_bytes;
     int tab_off, slots_off;      // within a stage
-    int mid_off;
     int out_off, out_bytes, out_row_bytes;
     int total;
 };
@@ -68,22 +67,18 @@ __host__ __device__ inline SmemLayout smem_layout(int fam, int C, int TR, int TW
                                                   int stages)
 {
     SmemLayout L;
-    const int halo = fam_halo(fam);
-    const int nrc = TR + 2 * halo;
     L.plan_off = 128;
     L.rows_off = 64;
     L.map_off = align_up(L.rows_off + 4 * max_rows, 16);
-    L.plan_bytes = align_up(L.map_off + 8 * nrc, 16);
+    L.plan_bytes = align_up(L.map_off + 8 * TR, 16);
     L.stage_off = align_up(L.plan_off + (stages + 1) * L.plan_bytes, 128);
-    // the narrow-tile families stage the tile's table entries too:
-    // x entries for the computed columns (+ slack), then y entries for the computed rows
-    const int tab = fam_tables_in_stage(fam) ? 8 * (tab_x_entries(TW, halo) + tab_y_entries(TR, halo)) : 0;
+    // the normalise family stages the tile's table entries too: x entries
+    // for its columns (+ slack), then y entries for its rows
+    const int tab = fam_tables_in_stage(fam) ? 8 * (tab_x_entries(TW) + tab_y_entries(TR)) : 0;
     L.tab_off = 0;
     L.slots_off = align_up(tab, 128);
     L.stage_bytes = align_up(L.slots_off + max_rows * slot_bytes, 128);
-    L.mid_off = L.stage_off + stages * L.stage_bytes;
-    const int mid = 0;   // the 3x3 epilogue keeps its window in registers
-    L.out_off = L.mid_off + mid;
+    L.out_off = L.stage_off + stages * L.stage_bytes;
     if (fam == FAM_NORM) {
         L.out_row_bytes = align_up(TW * 4, 16);
         L.out_bytes = align_up(C * TR * L.out_row_bytes, 128);
