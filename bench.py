@@ -350,6 +350,11 @@ def gpu_arm(args, rank, local_rank, world):
     if kind == "u8":
         e2e = e2e_u8(rz, plan, frames[0], H, W, OH, OW, C, dev, n=max(10, min(args.steps, 200)))
 
+    # several frames per launch (resize_u8_batch), u8 workloads
+    batched = None
+    if kind == "u8" and args.batch_frames > 0:
+        batched = batched_u8(rz, plan, frames, H, W, OH, OW, C, args.batch_frames, stream, dev, step_bytes)
+
     px = OH * OW * batch
     value = px * args.steps * world / (ms_max / 1e3) / 1e9
     launch_ms = ms / args.steps
@@ -360,10 +365,57 @@ def gpu_arm(args, rank, local_rank, world):
         "value": value, "ms": ms_max, "launch_ms": launch_ms, "eager_ms_per_step": eager_ms,
         "achieved_gbs": achieved, "peak_gbs": peak, "peak_src": src, "step_bytes": step_bytes,
         "read_bytes": rd, "write_bytes": wr, "ring": ring, "graph_steps": G, "clocks": clocks, "e2e": e2e,
-        "desc": desc, "px": px,
+        "desc": desc, "px": px, "batched": batched,
     }
     plan.destroy()
     return res
+
+
+def batched_u8(rz, plan, frames, H, W, OH, OW, C, nf, stream, dev, frame_bytes, launches=48):
+    """Frames per second when `nf` frames go through one resize_u8_batch
+    launch: two distinct batches in rotation (each larger than L2 for 4K
+    frames), graph-replayed launches timed with events on the launching
+    stream, after a check that frame 0 of a batched launch equals the
+    single-frame call's output."""
+    import torch
+    sets = []
+    for b in range(2):
+        src = torch.stack([frames[(b * nf + i) % len(frames)] for i in range(nf)])
+        sets.append((src, torch.empty((nf, OH, OW, C), dtype=torch.uint8, device=dev)))
+    one = torch.empty((OH, OW, C), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        rz.resize_u8(plan, sets[0][0][0], one, stream=stream)
+        for src, dst in sets:
+            rz.resize_u8_batch(plan, src, dst, stream=stream)
+    torch.cuda.synchronize()
+    if not torch.equal(sets[0][1][0], one):
+        raise RuntimeError("batched launch did not reproduce the single-frame result")
+    n = 8
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            src, dst = sets[i % 2]
+            rz.resize_u8_batch(plan, src, dst, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, launches // n)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * n)
+    peaks, _src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    gbs = nf * frame_bytes / (ms / 1e3) / 1e9
+    return {"frames_per_launch": nf, "value": nf * OH * OW / (ms / 1e3) / 1e9, "unit": "Gpix/s",
+            "ms_per_launch": ms, "launches": reps * n, "entry": "resize_u8_batch",
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak},
+            "l2": f"two batches of {nf} frames in rotation, {nf * frame_bytes / MB:.0f} MB each"}
 
 
 def e2e_u8(rz, plan, dev_frame, H, W, OH, OW, C, dev, n):
@@ -510,15 +562,23 @@ def profile_run(args):
         epi = rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=synth.NORM_MEAN, std=synth.NORM_STD)
     elif kind == "filt":
         epi = rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=synth.filter_weights())
+    nf = args.batch_frames if (kind == "u8" and args.profile_batched) else 0
+    if nf:
+        # two batches of nf frames in rotation, one resize_u8_batch launch each
+        sets = [(torch.stack([frames[(b * nf + i) % ring] for i in range(nf)]),
+                 torch.empty((nf, OH, OW, C), dtype=torch.uint8, device=dev)) for b in range(2)]
     for i in range(args.warmup + args.profile):
-        if kind == "u8":
+        if nf:
+            rz.resize_u8_batch(plan, *sets[i % 2])
+        elif kind == "u8":
             rz.resize_u8(plan, frames[i % ring], outs[i % ring])
         else:
             rz.resize_fused(plan, frames[i % ring], outs[i % ring], epi)
     torch.cuda.synchronize()
     assert rz.resize_plan_status(plan) == rz.RZ_OK
     plan.destroy()
-    print(f"profile run: {args.warmup} + {args.profile} launches of {desc}")
+    what = f"batches of {nf} frames of " if nf else ""
+    print(f"profile run: {args.warmup} + {args.profile} launches of {what}{desc}")
 
 
 # ------------------------------------------------------------------ main
@@ -537,8 +597,12 @@ def main():
     ap.add_argument("--grid-per-tile", action="store_true", help="one CTA per tile (tuning only)")
     ap.add_argument("--no-pdl", action="store_true", help="plain stream-ordered launches (tuning only)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--batch-frames", type=int, default=8,
+                    help="uint8 workloads: also time this many frames per resize_u8_batch launch (0: skip)")
     ap.add_argument("--profile", type=int, default=0,
                     help="only run W + N eager launches (for ncu captures); prints no JSON line")
+    ap.add_argument("--profile-batched", action="store_true",
+                    help="with --profile on a uint8 workload: launches of --batch-frames frames each")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -585,7 +649,9 @@ def main():
                 "workload": desc,
                 "l2": f"ring of {r['ring']} distinct input/output sets "
                       f"({r['ring'] * (r['read_bytes'] + r['write_bytes']) / MB:.0f} MB) > 3x L2; every step L2-cold",
-                "launch": f"CUDA graphs of {r['graph_steps']} resize_u8 launches, one stream",
+                "launch": f"CUDA graphs of {r['graph_steps']} "
+                          f"{'resize_u8' if WORKLOADS[args.workload][1] == 'u8' else 'resize_fused'} launches "
+                          f"(one frame or batch each), one stream",
                 "algorithmic_bytes_per_step": r["step_bytes"],
                 "parallelism": f"{world} independent replica(s)",
                 "tuning": {k: v for k, v in (("tile", args.tile), ("stages", args.stages),
@@ -608,6 +674,7 @@ def main():
             "gpu_launches": args.steps,
             "eager_ms_per_step": r["eager_ms_per_step"],
             "clocks": r["clocks"],
+            "batched": r["batched"],
         }
         print(json.dumps(line), flush=True)
     if world > 1:

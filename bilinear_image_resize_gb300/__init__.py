@@ -23,7 +23,8 @@ from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_EPI_
 
 __all__ = [
     "ResizeError", "Plan", "resize_plan_create", "resize_plan_destroy", "resize_plan_status",
-    "resize_plan_set_tile", "resize_plan_set_option", "resize_u8", "resize_f32", "resize_fused", "resize_u8_host",
+    "resize_plan_set_tile", "resize_plan_set_option", "resize_u8", "resize_f32", "resize_u8_batch",
+    "resize_f32_batch", "resize_fused", "resize_u8_host",
     "resize_axis_table", "resize_strerror", "resize_last_cuda_error", "make_epilogue", "resize_u8_noalloc",
     "RZ_NOALLOC_MAX_DIM",
     "RZ_LINEAR", "RZ_NEAREST", "RZ_U8", "RZ_F32", "RZ_EPI_NORMALIZE_NCHW", "RZ_EPI_FILTER3X3",
@@ -156,6 +157,36 @@ def resize_f32(plan: Plan, src, dst, mode: int | None = None, stream=None) -> No
         raise ValueError("src and dst channel counts differ")
     _check(_native.load().resize_f32(plan.handle, src.data_ptr(), sp, dst.data_ptr(), dp, H, W, C, OH, OW,
                                      plan.mode if mode is None else mode, _stream(stream)), "resize_f32")
+
+
+def _nhwc(t, name):
+    """(N, H, W, C, pitch_bytes, batch_stride_bytes) of an NHWC tensor whose pixels are packed."""
+    if t.dim() != 4:
+        raise ValueError(f"{name}: expected NxHxWxC, got shape {tuple(t.shape)}")
+    N, H, W, C = t.shape
+    if t.stride(3) != 1 or t.stride(2) != C:
+        raise ValueError(f"{name}: pixels must be packed (stride(2) == C, stride(3) == 1)")
+    es = t.element_size()
+    return N, H, W, C, t.stride(1) * es, t.stride(0) * es
+
+
+def _batch(fn_name, plan, src, dst, mode, stream):
+    N, H, W, C, sp, sb = _nhwc(src, "src")
+    N2, OH, OW, C2, dp, db = _nhwc(dst, "dst")
+    if N2 != N or C2 != C:
+        raise ValueError("src and dst batch or channel counts differ")
+    _check(getattr(_native.load(), fn_name)(plan.handle, src.data_ptr(), sp, sb, dst.data_ptr(), dp, db, N, H, W, C,
+                                            OH, OW, plan.mode if mode is None else mode, _stream(stream)), fn_name)
+
+
+def resize_u8_batch(plan: Plan, src, dst, mode: int | None = None, stream=None) -> None:
+    """dst[n] = resize(src[n]) for uint8 tensors (N, H, W, C) -> (N, OH, OW, C), one launch."""
+    _batch("resize_u8_batch", plan, src, dst, mode, stream)
+
+
+def resize_f32_batch(plan: Plan, src, dst, mode: int | None = None, stream=None) -> None:
+    """dst[n] = resize(src[n]) for float32 tensors (N, H, W, C) -> (N, OH, OW, C), one launch."""
+    _batch("resize_f32_batch", plan, src, dst, mode, stream)
 
 
 def make_epilogue(kind: int, batch: int = 1, src_batch_stride: int = 0, dst_batch_stride: int = 0,

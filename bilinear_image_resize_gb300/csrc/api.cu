@@ -711,6 +711,24 @@ int resize_f32(rz_plan p, const float *src, size_t src_pitch, float *dst, size_t
     return run(p, rz::FAM_F32, src, src_pitch, 0, dst, dst_pitch, 0, H, W, C, out_h, out_w, mode, 1, extra, stream);
 }
 
+int resize_u8_batch(rz_plan p, const uint8_t *src, size_t src_pitch, size_t src_batch_stride, uint8_t *dst,
+                    size_t dst_pitch, size_t dst_batch_stride, int batch, int H, int W, int C, int out_h, int out_w,
+                    int mode, void *stream)
+{
+    KArgs extra = {};
+    return run(p, rz::FAM_U8, src, src_pitch, src_batch_stride, dst, dst_pitch, dst_batch_stride, H, W, C, out_h,
+               out_w, mode, batch, extra, stream);
+}
+
+int resize_f32_batch(rz_plan p, const float *src, size_t src_pitch, size_t src_batch_stride, float *dst,
+                     size_t dst_pitch, size_t dst_batch_stride, int batch, int H, int W, int C, int out_h, int out_w,
+                     int mode, void *stream)
+{
+    KArgs extra = {};
+    return run(p, rz::FAM_F32, src, src_pitch, src_batch_stride, dst, dst_pitch, dst_batch_stride, H, W, C, out_h,
+               out_w, mode, batch, extra, stream);
+}
+
 int resize_fused(rz_plan p, const void *src, int src_dtype, size_t src_pitch, void *dst, size_t dst_pitch, int H,
                  int W, int C, int out_h, int out_w, int mode, const rz_epilogue *e, void *stream)
 {

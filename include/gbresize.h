@@ -140,6 +140,25 @@ RZ_API int resize_f32(rz_plan p, const float *src, size_t src_pitch, float *dst,
                int H, int W, int C, int out_h, int out_w, int mode, void *stream);
 
 /*
+ * Batched forms: `batch` images of the plan's geometry in one launch (one
+ * kernel walks the tiles of all of them, so a stream of frames pays the
+ * launch's fixed start-up and drain once per batch instead of once per
+ * frame).  Image n starts at src + n*src_batch_stride and
+ * dst + n*dst_batch_stride (bytes); with batch > 1 the strides must cover an
+ * image (src_batch_stride >= (H-1)*src_pitch + W*C*element size, likewise
+ * dst) and the float32 strides must be multiples of 4.  No source image may
+ * overlap any destination image.  batch = 0 does nothing; batch = 1 is the
+ * single-image call (strides ignored).  Results per image equal the
+ * single-image call's.
+ */
+RZ_API int resize_u8_batch(rz_plan p, const uint8_t *src, size_t src_pitch, size_t src_batch_stride, uint8_t *dst,
+                           size_t dst_pitch, size_t dst_batch_stride, int batch, int H, int W, int C, int out_h,
+                           int out_w, int mode, void *stream);
+RZ_API int resize_f32_batch(rz_plan p, const float *src, size_t src_pitch, size_t src_batch_stride, float *dst,
+                            size_t dst_pitch, size_t dst_batch_stride, int batch, int H, int W, int C, int out_h,
+                            int out_w, int mode, void *stream);
+
+/*
  * Epilogue fused into the bilinear kernel (CUDA interpolation page §4.2;
  * kernel merging leaves results unchanged, "Performance Optimization of Object
  * Tracking Algorithms in OpenCV on GPUs", §4.2 and Table 10).

@@ -111,6 +111,8 @@ def test_calls_validate_before_cuda(lib):
     assert lib.resize_f32(None, 16, 12, 32, 12, 1, 1, 3, 1, 1, 1, None) == RZ_ERR_ARG
     assert lib.resize_fused(None, 16, 0, 3, 32, 4, 1, 1, 3, 1, 1, 1, None, None) == RZ_ERR_ARG
     assert lib.resize_u8_host(None, 16, 3, 32, 3, 48, 3, 64, 3, 1, 1, 3, 1, 1, 1, None) == RZ_ERR_ARG
+    assert lib.resize_u8_batch(None, 16, 3, 3, 32, 3, 3, 2, 1, 1, 3, 1, 1, 1, None) == RZ_ERR_ARG
+    assert lib.resize_f32_batch(None, 16, 12, 12, 32, 12, 12, 2, 1, 1, 3, 1, 1, 1, None) == RZ_ERR_ARG
     assert lib.resize_plan_status(None, None) == RZ_ERR_ARG
     assert lib.resize_plan_set_tile(None, 0, 1, 1) == RZ_ERR_ARG
     assert lib.resize_plan_destroy(None) == 0

@@ -325,6 +325,87 @@ def test_filter_unaligned_source_rows(rz):
             assert err <= F32_TOL * np.abs(w).sum(), (H, W, C, OH, OW, ring, err)
 
 
+def batch_canvas(N, H, W, C, dtype, pitch, bstride, off=0):
+    """An (N, H, W, C) view with the given row pitch, batch stride and start offset (elements)."""
+    flat = torch.zeros(off + (N - 1) * bstride + (H - 1) * pitch + W * C + 64, dtype=dtype, device="cuda")
+    return torch.as_strided(flat, (N, H, W, C), (bstride, pitch, C, 1), off), flat
+
+
+@pytest.mark.parametrize("kind", ["u8", "f32"])
+@pytest.mark.parametrize("layout", ["packed", "padded", "unaligned"])
+def test_batch_matches_per_image_oracle(rz, kind, layout):
+    # one launch over N images equals N single-image resizes; padding between
+    # rows and images, and unaligned strides (plain copies), change nothing
+    N, H, W, C, OH, OW = 3, 270, 480, 3, 181, 317
+    rng = np.random.default_rng(91)
+    if kind == "u8":
+        imgs = rng.integers(0, 256, size=(N, H, W, C), dtype=np.uint8)
+        dt, fn = torch.uint8, rz.resize_u8_batch
+    else:
+        imgs = (rng.random((N, H, W, C)) * 255).astype(np.float32)
+        dt, fn = torch.float32, rz.resize_f32_batch
+    pad, opad, off = {"packed": (0, 0, 0), "padded": (16, 32, 0), "unaligned": (5, 7, 3)}[layout]
+    if kind == "f32" and layout == "unaligned":
+        pad, opad, off = 1, 3, 1
+    sp = W * C + pad
+    src, _ks = batch_canvas(N, H, W, C, dt, sp, H * sp + opad, off)
+    src.copy_(torch.from_numpy(imgs).cuda())
+    dp = OW * C + pad
+    dst, dflat = batch_canvas(N, OH, OW, C, dt, dp, OH * dp + opad, off)
+    for mode in (rz.RZ_LINEAR, rz.RZ_NEAREST):
+        dflat.fill_(0)
+        with rz.resize_plan_create(H, W, OH, OW, mode) as plan:
+            fn(plan, src, dst)
+            torch.cuda.synchronize()
+            assert rz.resize_plan_status(plan) == rz.RZ_OK
+        got = dst.cpu().numpy()
+        for n in range(N):
+            if kind == "u8":
+                want = (oracle.linear_u8 if mode == rz.RZ_LINEAR else oracle.nearest_u8)(imgs[n], OH, OW)
+                np.testing.assert_array_equal(got[n], want, err_msg=f"image {n}")
+            else:
+                want = (oracle.linear_f32 if mode == rz.RZ_LINEAR else oracle.nearest_f32)(imgs[n], OH, OW)
+                assert max_abs(got[n], want) <= F32_TOL, n
+
+
+def test_batch_of_4k_frames_is_bit_exact(rz):
+    # the exact 2x path over a batch of frames, as the bench runs it
+    N = 3
+    frames = np.stack([synth.smooth_rgb(3840, 2160, 10 + n) for n in range(N)])
+    src = torch.from_numpy(frames).cuda()
+    dst = torch.empty((N, 1080, 1920, 3), dtype=torch.uint8, device="cuda")
+    with rz.resize_plan_create(2160, 3840, 1080, 1920, rz.RZ_LINEAR) as plan:
+        rz.resize_u8_batch(plan, src, dst)
+        torch.cuda.synchronize()
+    got = dst.cpu().numpy()
+    for n in range(N):
+        np.testing.assert_array_equal(got[n], oracle.linear_u8(frames[n], 1080, 1920))
+
+
+def test_batch_argument_checks(rz):
+    with rz.resize_plan_create(8, 8, 4, 4, rz.RZ_LINEAR) as plan:
+        lib = rz._native.load()
+        src = torch.zeros((2, 8, 8, 3), dtype=torch.uint8, device="cuda")
+        dst = torch.zeros((2, 4, 4, 3), dtype=torch.uint8, device="cuda")
+        s, d = src.data_ptr(), dst.data_ptr()
+        # batch stride smaller than an image
+        assert lib.resize_u8_batch(plan.handle, s, 24, 100, d, 12, 48, 2, 8, 8, 3, 4, 4, 1, None) == rz.RZ_ERR_ARG
+        assert lib.resize_u8_batch(plan.handle, s, 24, 192, d, 12, 40, 2, 8, 8, 3, 4, 4, 1, None) == rz.RZ_ERR_ARG
+        # negative batch; zero is a no-op
+        assert lib.resize_u8_batch(plan.handle, s, 24, 192, d, 12, 48, -1, 8, 8, 3, 4, 4, 1, None) == rz.RZ_ERR_ARG
+        assert lib.resize_u8_batch(plan.handle, s, 24, 192, d, 12, 48, 0, 8, 8, 3, 4, 4, 1, None) == rz.RZ_OK
+        # a destination image overlapping a source image
+        assert lib.resize_u8_batch(plan.handle, s, 24, 192, s + 192, 12, 48, 2, 8, 8, 3, 4, 4, 1,
+                                   None) == rz.RZ_ERR_ARG
+        # float32 batch strides must be multiples of 4
+        f = torch.zeros((2 * 8 * 8 * 3 + 8,), dtype=torch.float32, device="cuda")
+        g = torch.zeros((2 * 4 * 4 * 3 + 8,), dtype=torch.float32, device="cuda")
+        assert lib.resize_f32_batch(plan.handle, f.data_ptr(), 96, 770, g.data_ptr(), 48, 192, 2, 8, 8, 3, 4, 4, 1,
+                                    None) == rz.RZ_ERR_ARG
+        torch.cuda.synchronize()
+        assert not dst.any()
+
+
 def test_non_default_stream(rz):
     img = synth.smooth_rgb(1920, 1080, 2)
     s = torch.cuda.Stream()
