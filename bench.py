@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 
 MB = 1e6
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_SOURCE = os.path.join(ROOT, "bilinear_image_resize_gb300", "csrc", "kernels.cu")
+CSRC = os.path.join(ROOT, "bilinear_image_resize_gb300", "csrc")
 
 # name -> (description, kind, H, W, OH, OW, C, mode, batch)
 WORKLOADS = {
@@ -150,21 +150,29 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def kernel_sources_hash(cu: str) -> str:
+    """sha256[:16] over a kernel's .cu file and the two headers it includes:
+    the key that ties a committed ncu summary to the code it measured."""
+    h = hashlib.sha256()
+    for name in (cu, "rz_device.h", "rz_internal.h"):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def profile_traffic(workload: str):
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu
-    summary, or None when the summary is missing or the kernel source has
+    summary, or None when the summary is missing or the kernel's sources have
     changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", f"ncu_{workload}.md")
     try:
         with open(path) as f:
             text = f.read()
-        with open(KERNEL_SOURCE, "rb") as f:
-            src_hash = hashlib.sha256(f.read()).hexdigest()[:16]
+        m_hash = re.search(r"kernel sources \((\w+\.cu) \+ headers\) sha256\[:16\]:\s*`([0-9a-f]{16})`", text)
+        m_bytes = re.search(r"dram bytes per launch:\s*`?([0-9]+)", text)
+        if not m_hash or not m_bytes or kernel_sources_hash(m_hash.group(1)) != m_hash.group(2):
+            return None
     except OSError:
-        return None
-    m_hash = re.search(r"kernels\.cu sha256\[:16\]:\s*`?([0-9a-f]{16})", text)
-    m_bytes = re.search(r"dram bytes per launch:\s*`?([0-9]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != src_hash:
         return None
     return int(m_bytes.group(1))
 
