@@ -81,8 +81,9 @@ void axis_nearest(int n_in, int n_out, int32_t *ofs)
 
 struct TileCfg {
     int TR = 0, TW = 0, tiles_x = 0, tiles_y = 0, max_rows = 0, slot_bytes = 0, stages = 0, variant = 0;
-    int tensor = 0, box_words = 0, box_rows = 0;   // tensor-map staging (one box per tile or chunk)
-    int ring_chunks = 0, chunk_rows = 0, chunk_boxes = 0, box_bytes = 0;   // streaming 3x3 filter
+    int tensor = 0, box_words = 0, box_rows = 0;   // tensor-map staging (one box per chunk)
+    int stream = 0;   // 0: staged-tile kernel; 1: streaming 3x3 filter; 2: streaming uint8 bilinear
+    int ring_chunks = 0, chunk_rows = 0, chunk_boxes = 0, box_bytes = 0;   // streaming kernels
     size_t smem = 0;
     int grid = 0;
 };
@@ -126,7 +127,8 @@ struct rz_plan_s {
     int opt_ctas_per_sm = 0;   // 0: as many as fit
     int opt_grid_mode = 0;     // 0: persistent CTAs; 1: one CTA per tile
     int opt_pdl = 1;           // programmatic dependent launch
-    int opt_ring_rows = 0;     // 3x3 filter: source rows in the streaming ring (0: automatic)
+    int opt_ring_rows = 0;     // streaming kernels: source rows in the ring (0: automatic)
+    int opt_stream = 0;        // uint8 bilinear: 0 automatic, 1 staged tiles only, 2 streaming where it fits
 };
 
 namespace {
@@ -217,7 +219,7 @@ bool is_down2(const rz_plan_s &p)
 // row stays within 16 KB), narrowed while there are fewer than about twelve
 // tiles per SM (for balance across SMs), then as many output rows per tile as
 // keep the staged ring under 48 KB with that many tiles.  (The 3x3 filter
-// family streams strips instead: get_filter_tile.)
+// family and uint8 upscales stream strips instead: get_stream_tile.)
 TileCfg choose_tile(const rz_plan_s &p, int fam, int C, int batch, int stages, bool down2)
 {
     const int out_es = rz::fam_out_es(fam);
@@ -290,39 +292,51 @@ int ensure_smem_attr(int dev, const void *fn)
     return 0;
 }
 
-constexpr int kFilterCtaSmem = 74 * 1024;   // three streaming-filter CTAs per SM
-constexpr int kFilterMinRows = 16;          // shortest automatic unit: the halo adds 2 resized rows
+constexpr int kStreamCtaSmem = 74 * 1024;   // three streaming CTAs per SM
+constexpr int kStreamMinRows = 16;          // shortest automatic unit (the filter's halo adds 2 rows)
 
-// Units, ring and grid of the streaming 3x3 filter kernel (filter.cu).
-// Units are strips of up to filter_strip(C) output columns; the automatic unit height
+// Units, ring and grid of a streaming kernel (stream.cu).  Units are strips
+// of up to the kernel's widest strip (filter_strip / stream_u8_strip),
+// narrowed to share the columns evenly; the uint8 form needs each strip's
+// source span plus 16 bytes of padding (its 32-bit tap reads) in one 2 KB
+// block and narrows the strips until it fits.  The automatic unit height
 // splits each strip into as many segments as give every resident CTA about
 // one unit, so a source row is staged once per strip segment.  The ring holds
 // chunks of eight rows (fewer when the option asks for a small ring), as many
-// chunks as keep three CTAs per SM (two at least).
-int get_filter_tile(rz_plan_s *p, int C, int batch, TileCfg *out, const void **fn_out)
+// chunks as keep three CTAs per SM (two at least).  Returns
+// RZ_ERR_UNSUPPORTED when the uint8 form does not fit (the caller then uses
+// the staged-tile kernel).
+int get_stream_tile(rz_plan_s *p, int op, int C, int batch, TileCfg *out, const void **fn_out)
 {
-    const void *fn = rz::filter_kernel_for(p->mode, C);
+    const void *fn = rz::stream_kernel_for(op, p->mode, C);
     if (!fn) return RZ_ERR_UNSUPPORTED;
-    const int fam = rz::FAM_FILT;
+    const bool u8 = op == rz::STREAM_U8;
+    const int fam = u8 ? rz::FAM_U8 : rz::FAM_FILT;
+    const int widest = u8 ? rz::stream_u8_strip(C) : rz::filter_strip(C);
     TileCfg t;
-    // strips as wide as the kernel takes, narrowed to share the columns evenly
-    const int strips = (p->OW + rz::filter_strip(C) - 1) / rz::filter_strip(C);
-    t.TW = (p->OW + strips - 1) / strips;
-    if (p->over_tw[fam] > 0) t.TW = std::min(p->over_tw[fam], rz::filter_strip(C));
-    t.TW = std::min(t.TW, p->OW);
+    int strips = (p->OW + widest - 1) / widest;
+    int span = 0;
+    for (;;) {
+        t.TW = (p->OW + strips - 1) / strips;
+        if (u8 && t.TW < p->OW) t.TW = std::min(p->OW, (t.TW + 31) / 32 * 32);   // word-aligned output runs
+        if (p->over_tw[fam] > 0) t.TW = std::min({p->over_tw[fam], widest, p->OW});
+        span = max_slot_bytes(*p, fam, C, t.TW, u8);   // a multiple of 16 (+16 of padding for uint8)
+        if (!u8 || span <= 2048) break;
+        if (p->over_tw[fam] > 0 || t.TW <= 32) return RZ_ERR_UNSUPPORTED;
+        strips++;
+    }
     t.tiles_x = (p->OW + t.TW - 1) / t.TW;
-    const int span = max_slot_bytes(*p, fam, C, t.TW);   // a multiple of 16
-    const int BW = std::min(span, 2048);                 // a box row: at most 256 eight-byte words
+    const int BW = std::min(span, 2048);   // a box row: at most 256 eight-byte words
     const int NB = (span + BW - 1) / BW;
-    int G = rz::kFilterChunkRows, NCH;
+    int G = rz::kStreamChunkRows, NCH;
     if (p->opt_ring_rows > 0) {
         while (G > 1 && 2 * G > p->opt_ring_rows) G /= 2;
         NCH = p->opt_ring_rows / G;
     } else {
-        const int chunk = NB * rz::filter_block_bytes(G, BW);
-        NCH = std::max(2, std::min(rz::kFilterRingMax / G, kFilterCtaSmem / (chunk + 16)));
+        const int chunk = NB * rz::stream_block_bytes(G, BW);
+        NCH = std::max(2, std::min(rz::kStreamRingMax / G, kStreamCtaSmem / (chunk + 16)));
     }
-    while (rz::filter_smem(NCH, G, NB, BW) > rz::kMaxSmem) {
+    while (rz::stream_smem(NCH, G, NB, BW) > rz::kMaxSmem) {
         if (NCH > 2) NCH--;
         else if (G > 1) G /= 2;
         else return RZ_ERR_UNSUPPORTED;
@@ -335,9 +349,10 @@ int get_filter_tile(rz_plan_s *p, int C, int batch, TileCfg *out, const void **f
     t.tensor = 1;            // used when the source allows bulk copies
     t.box_words = BW / 8;
     t.box_rows = G;
-    t.smem = static_cast<size_t>(rz::filter_smem(NCH, G, NB, BW));
+    t.smem = static_cast<size_t>(rz::stream_smem(NCH, G, NB, BW));
     t.stages = 0;
     t.variant = rz::VAR_GENERIC;
+    t.stream = u8 ? 2 : 1;
     int e = ensure_smem_attr(p->device, fn);
     if (e != 0) return cuda_fail(static_cast<cudaError_t>(e));
     int per_sm = 0, sms = 0;
@@ -354,7 +369,7 @@ int get_filter_tile(rz_plan_s *p, int C, int batch, TileCfg *out, const void **f
     } else {
         const long long segs = std::max<long long>(1, cap / (static_cast<long long>(batch) * t.tiles_x));
         TR = static_cast<int>((p->OH + segs - 1) / segs);
-        TR = std::max(TR, std::min(p->OH, kFilterMinRows));
+        TR = std::max(TR, std::min(p->OH, kStreamMinRows));
     }
     t.TR = std::max(1, std::min(TR, p->OH));
     t.tiles_y = (p->OH + t.TR - 1) / t.TR;
@@ -367,6 +382,15 @@ int get_filter_tile(rz_plan_s *p, int C, int batch, TileCfg *out, const void **f
     return RZ_OK;
 }
 
+// The uint8 bilinear resize takes the streaming form for vertical upscales,
+// where each source row feeds several output rows (or when the option asks
+// for it), unless the exact 2x path applies.
+bool want_u8_stream(const rz_plan_s &p, bool down2)
+{
+    if (p.mode != RZ_LINEAR || down2 || p.opt_stream == 1) return false;
+    return p.opt_stream == 2 || p.OH > p.H;
+}
+
 // Tile and grid for this call: the override if one is set, else the cached
 // automatic choice.  Returns an RZ_* status.
 int get_tile(rz_plan_s *p, int fam, int C, int batch, TileCfg *out, const void **fn_out)
@@ -375,13 +399,18 @@ int get_tile(rz_plan_s *p, int fam, int C, int batch, TileCfg *out, const void *
     for (const auto &e : p->cache)
         if (e.fam == fam && e.C == C && e.batch == batch) {
             *out = e.cfg;
-            *fn_out = fam == rz::FAM_FILT ? rz::filter_kernel_for(p->mode, C)
-                                          : rz::kernel_for(fam, p->mode, e.cfg.variant, C);
+            *fn_out = e.cfg.stream ? rz::stream_kernel_for(e.cfg.stream == 2 ? rz::STREAM_U8 : rz::STREAM_FILTER,
+                                                           p->mode, C)
+                                   : rz::kernel_for(fam, p->mode, e.cfg.variant, C);
             return RZ_OK;
         }
-    if (fam == rz::FAM_FILT) return get_filter_tile(p, C, batch, out, fn_out);
+    if (fam == rz::FAM_FILT) return get_stream_tile(p, rz::STREAM_FILTER, C, batch, out, fn_out);
     const int stages = p->opt_stages > 0 ? p->opt_stages : kDefaultStages;
     const bool down2 = fam == rz::FAM_U8 && !p->opt_generic && is_down2(*p);
+    if (fam == rz::FAM_U8 && want_u8_stream(*p, down2)) {
+        const int rc = get_stream_tile(p, rz::STREAM_U8, C, batch, out, fn_out);
+        if (rc != RZ_ERR_UNSUPPORTED) return rc;   // else the staged-tile kernel below
+    }
     TileCfg t;
     if (p->over_tr[fam] > 0 && p->over_tw[fam] > 0) {
         // an explicit ring depth must fit as asked; an automatic one shrinks
@@ -687,8 +716,12 @@ int resize_plan_set_option(rz_plan p, int option, int value)
         p->opt_pdl = value;
         break;
     case RZ_OPT_RING_ROWS:
-        if (value != 0 && (value < 2 || value > rz::kFilterRingMax)) return RZ_ERR_ARG;
+        if (value != 0 && (value < 2 || value > rz::kStreamRingMax)) return RZ_ERR_ARG;
         p->opt_ring_rows = value;
+        break;
+    case RZ_OPT_STREAM:
+        if (value < 0 || value > 2) return RZ_ERR_ARG;
+        p->opt_stream = value;
         break;
     default:
         return RZ_ERR_ARG;

@@ -323,55 +323,18 @@ __device__ __forceinline__ StageView stage_view(const KArgs &a, const SmemLayout
 // byte offset (within the staged rows) of the left tap's first channel; the
 // right tap follows C bytes later (at the right image edge the plan gives the
 // right tap weight 0, and the bytes read past the row are padding, so the
-// product is 0).  The 2C tap bytes of each row are fetched as 32-bit words,
-// each channel's pair (left, right) is gathered into one 16-bit lane with a
-// byte permute, and dp2a forms A0 * left + A1 * right exactly in int32:
+// product is 0).  Each row's pair of taps is summed exactly by hsum_u8:
 //   q = (B0 hT + B1 hB + 2^21) >> 22.
 template <int C>
 __device__ __forceinline__ void bilinear_u8_px(const uint8_t *top, const uint8_t *bot, int o0, uint32_t aw, int B0,
                                                int B1, int (&q)[C])
 {
-    const uint8_t *rowp[2] = {top, bot};
-    int h[2][C];
-#pragma unroll
-    for (int r = 0; r < 2; r++) {
-        if constexpr (C == 4) {
-            const uint32_t t0 = *reinterpret_cast<const uint32_t *>(rowp[r] + o0);
-            const uint32_t t1 = *reinterpret_cast<const uint32_t *>(rowp[r] + o0 + 4);
-            const uint32_t p01 = __byte_perm(t0, t1, 0x5140);   // c0 pair, c1 pair
-            const uint32_t p23 = __byte_perm(t0, t1, 0x7362);   // c2 pair, c3 pair
-            h[r][0] = static_cast<int>(__dp2a_lo(aw, p01, 0u));
-            h[r][1] = static_cast<int>(__dp2a_hi(aw, p01, 0u));
-            h[r][2] = static_cast<int>(__dp2a_lo(aw, p23, 0u));
-            h[r][3] = static_cast<int>(__dp2a_hi(aw, p23, 0u));
-        } else {
-            const int base = o0 & ~3;
-            const uint32_t sel = 0x3210u + 0x1111u * static_cast<uint32_t>(o0 & 3);
-            const uint32_t *w = reinterpret_cast<const uint32_t *>(rowp[r] + base);
-            const uint32_t w0 = w[0], w1 = w[1];
-            const uint32_t lo4 = __byte_perm(w0, w1, sel);      // bytes o0 .. o0+3
-            if constexpr (C == 1) {
-                h[r][0] = static_cast<int>(__dp2a_lo(aw, lo4, 0u));
-            } else {
-                const uint32_t hi4 = __byte_perm(w1, w[2], sel);  // bytes o0+4 .. o0+7
-                const uint32_t p01 = __byte_perm(lo4, hi4, 0x4130);  // t0c0 t1c0 t0c1 t1c1
-                const uint32_t p2 = __byte_perm(lo4, hi4, 0x0052);   // t0c2 t1c2
-                h[r][0] = static_cast<int>(__dp2a_lo(aw, p01, 0u));
-                h[r][1] = static_cast<int>(__dp2a_hi(aw, p01, 0u));
-                h[r][2] = static_cast<int>(__dp2a_lo(aw, p2, 0u));
-            }
-        }
-    }
+    int hT[C], hB[C];
+    hsum_u8<C>(top, o0, aw, hT);
+    hsum_u8<C>(bot, o0, aw, hB);
 #pragma unroll
     for (int c = 0; c < C; c++)
-        q[c] = (B0 * h[0][c] + B1 * h[1][c] + (1 << 21)) >> 22;
-}
-
-// Pack the low bytes of four ints into one word (first int in byte 0).
-__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
-{
-    return __byte_perm(__byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040),
-                       __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040), 0x5410);
+        q[c] = (B0 * hT[c] + B1 * hB[c] + (1 << 21)) >> 22;
 }
 
 // Generic bilinear / nearest, any ratio.  Each thread takes runs of four

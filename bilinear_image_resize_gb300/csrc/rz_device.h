@@ -221,5 +221,49 @@ __device__ __forceinline__ int sample_index(int n_in, int n_out, int d)
     return s < 0 ? 0 : (s > n_in - 1 ? n_in - 1 : s);
 }
 
+// Exact horizontal tap sum of one staged uint8 row for one output pixel:
+// h[c] = A0 * row[o0 + c] + A1 * row[o0 + C + c] (at most 2048 * 255), with
+// aw = A0 | A1 << 16.  The 2C tap bytes are fetched as 32-bit words (up to
+// 11 bytes past the taps: the staged rows carry 16 bytes of padding), each
+// channel's pair is gathered into one 16-bit lane pair by a byte permute, and
+// dp2a forms the sum.  For C = 4, o0 must be a multiple of 4.
+template <int C>
+__device__ __forceinline__ void hsum_u8(const uint8_t *row, int o0, uint32_t aw, int (&h)[C])
+{
+    if constexpr (C == 4) {
+        const uint32_t t0 = *reinterpret_cast<const uint32_t *>(row + o0);
+        const uint32_t t1 = *reinterpret_cast<const uint32_t *>(row + o0 + 4);
+        const uint32_t p01 = __byte_perm(t0, t1, 0x5140);   // c0 pair, c1 pair
+        const uint32_t p23 = __byte_perm(t0, t1, 0x7362);   // c2 pair, c3 pair
+        h[0] = static_cast<int>(__dp2a_lo(aw, p01, 0u));
+        h[1] = static_cast<int>(__dp2a_hi(aw, p01, 0u));
+        h[2] = static_cast<int>(__dp2a_lo(aw, p23, 0u));
+        h[3] = static_cast<int>(__dp2a_hi(aw, p23, 0u));
+    } else {
+        const int base = o0 & ~3;
+        const uint32_t sel = 0x3210u + 0x1111u * static_cast<uint32_t>(o0 & 3);
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(row + base);
+        const uint32_t w0 = w[0], w1 = w[1];
+        const uint32_t lo4 = __byte_perm(w0, w1, sel);      // bytes o0 .. o0+3
+        if constexpr (C == 1) {
+            h[0] = static_cast<int>(__dp2a_lo(aw, lo4, 0u));
+        } else {
+            const uint32_t hi4 = __byte_perm(w1, w[2], sel);  // bytes o0+4 .. o0+7
+            const uint32_t p01 = __byte_perm(lo4, hi4, 0x4130);  // t0c0 t1c0 t0c1 t1c1
+            const uint32_t p2 = __byte_perm(lo4, hi4, 0x0052);   // t0c2 t1c2
+            h[0] = static_cast<int>(__dp2a_lo(aw, p01, 0u));
+            h[1] = static_cast<int>(__dp2a_hi(aw, p01, 0u));
+            h[2] = static_cast<int>(__dp2a_lo(aw, p2, 0u));
+        }
+    }
+}
+
+// Pack the low bytes of four ints into one word (first int in byte 0).
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
+{
+    return __byte_perm(__byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040),
+                       __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040), 0x5410);
+}
+
 }  // namespace dev
 }  // namespace rz

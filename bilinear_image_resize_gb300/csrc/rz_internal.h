@@ -90,26 +90,30 @@ __host__ __device__ inline SmemLayout smem_layout(int fam, int C, int TR, int TW
     return L;
 }
 
-// 3x3 filter family (filter.cu): units of TW <= filter_strip(C) output columns
-// by TR output rows, whose source rows stream through a ring of chunks.  A
-// chunk holds up to chunk_rows rows; each row's span is cut into chunk_boxes
-// blocks of box_bytes (<= 2048, a multiple of 16), stored block-major: block
-// k of row i at k * block_bytes + i * box_bytes, block_bytes = chunk_rows *
+// Streaming kernels (stream.cu): the 3x3 filter family and the uint8
+// bilinear resize in row-separable form.  Units of TW output columns by TR
+// output rows, whose source rows stream through a ring of chunks.  A chunk
+// holds up to chunk_rows rows; each row's span is cut into chunk_boxes blocks
+// of box_bytes (<= 2048, a multiple of 16), stored block-major: block k of
+// row i at k * block_bytes + i * box_bytes, block_bytes = chunk_rows *
 // box_bytes rounded up to 128.  Shared memory: ring_chunks "full" and
 // ring_chunks "empty" mbarriers, the producer's list window, then the chunks.
-// resized columns per consumer lane: two for one channel, else one
+enum StreamOp { STREAM_FILTER = 0, STREAM_U8 = 1 };
+constexpr int kStreamChunkRows = 8;     // rows per chunk (a power of two)
+constexpr int kStreamRingMax = 128;     // ring rows (chunks x rows per chunk)
+constexpr int kStreamListWindow = 128;  // listed rows the producer keeps (ints)
+// 3x3 filter: resized columns per consumer lane (two for one channel, else
+// one); widest strip = eight consumer warps x (32 x lane columns - 2) outputs
 __host__ __device__ constexpr int filter_lane_cols(int C) { return C == 1 ? 2 : 1; }
-// widest strip: eight consumer warps x (32 x lane columns - 2) output columns
 __host__ __device__ constexpr int filter_strip(int C) { return 8 * (32 * filter_lane_cols(C) - 2); }
-constexpr int kFilterChunkRows = 8;   // rows per chunk (a power of two)
-constexpr int kFilterRingMax = 128;   // ring rows (chunks x rows per chunk)
-__host__ __device__ constexpr int filter_block_bytes(int rows, int box_bytes) { return align_up(rows * box_bytes, 128); }
-// after the barriers: the producer's window of listed rows (kFilterListWindow ints)
-constexpr int kFilterListWindow = 128;
-__host__ __device__ constexpr int filter_chunks_off(int chunks) { return align_up(16 * chunks + 4 * kFilterListWindow, 128); }
-__host__ __device__ constexpr int filter_smem(int chunks, int rows, int boxes, int box_bytes)
+// uint8 bilinear: consecutive output pixels per consumer lane; widest strip
+__host__ __device__ constexpr int stream_u8_run(int C) { return C == 4 ? 2 : 4; }
+__host__ __device__ constexpr int stream_u8_strip(int C) { return 8 * 32 * stream_u8_run(C); }
+__host__ __device__ constexpr int stream_block_bytes(int rows, int box_bytes) { return align_up(rows * box_bytes, 128); }
+__host__ __device__ constexpr int stream_chunks_off(int chunks) { return align_up(16 * chunks + 4 * kStreamListWindow, 128); }
+__host__ __device__ constexpr int stream_smem(int chunks, int rows, int boxes, int box_bytes)
 {
-    return filter_chunks_off(chunks) + chunks * boxes * filter_block_bytes(rows, box_bytes);
+    return stream_chunks_off(chunks) + chunks * boxes * stream_block_bytes(rows, box_bytes);
 }
 
 // Everything a resize kernel reads, passed by value in the parameter bank.
@@ -132,10 +136,10 @@ struct KArgs {
     int tensor_in;          // stage each tile with one tensor-map copy (box below)
     int box_words;          // box width in 8-byte words
     int box_rows;           // box height in rows
-    int ring_chunks;        // 3x3 filter: chunks in the ring (>= 2)
-    int chunk_rows;         // 3x3 filter: rows per chunk (1, 2, 4 or 8)
-    int chunk_boxes;        // 3x3 filter: blocks per row span
-    int box_bytes;          // 3x3 filter: bytes per block of a row
+    int ring_chunks;        // streaming kernels: chunks in the ring (>= 2)
+    int chunk_rows;         // streaming kernels: rows per chunk (1, 2, 4 or 8)
+    int chunk_boxes;        // streaming kernels: blocks per row span
+    int box_bytes;          // streaming kernels: bytes per block of a row
     const int2 *xt;         // per output column {source column, weight}; kTabPad clamped entries either side
     const int2 *yt;         // per output row    {source row, weight}; kTabPad clamped entries either side
     int *status;            // device status word (RZ_OK or RZ_ERR_TIMEOUT)
@@ -149,8 +153,8 @@ void record_cuda_error(int e);
 // Kernel entry for (family, mode, variant, C); nullptr if none.
 const void *kernel_for(int fam, int mode, int variant, int C);
 
-// The streaming 3x3 filter kernel for (mode, C); nullptr if none.
-const void *filter_kernel_for(int mode, int C);
+// The streaming kernel for (StreamOp, mode, C); nullptr if none.
+const void *stream_kernel_for(int op, int mode, int C);
 
 // Launch it on `grid` CTAs (asynchronous), optionally as a programmatic
 // dependent launch.  `tmap` describes the source when a.tensor_in is set

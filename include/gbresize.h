@@ -231,8 +231,9 @@ RZ_API int resize_last_cuda_error(void);
  * Tile override for tuning (0 = automatic): output rows and output columns
  * per CTA for kernel family `kind` (RZ_U8, RZ_F32, or 2 + RZ_EPI_* for the
  * fused kernels) of this plan.  Results do not depend on it; only speed does.
- * For the 3x3 filter family a tile is one streamed unit: tile_rows output rows
- * of a strip of tile_cols (at most 240) output columns.  A tile that does not
+ * For the streaming kernels (the 3x3 filter family, uint8 bilinear upscales)
+ * a tile is one streamed unit: tile_rows output rows of a strip of tile_cols
+ * output columns (at most the kernel's widest strip).  A tile that does not
  * fit in shared memory makes the next call of that family fail with
  * RZ_ERR_ARG (RZ_ERR_UNSUPPORTED for the 3x3 filter family).
  */
@@ -256,8 +257,16 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  *                       while that kernel finishes (it still reads and writes
  *                       memory only after that kernel has completed);
  *   RZ_OPT_RING_ROWS    value 0 (automatic) or 2..128: source rows in the
- *                       shared-memory ring through which each CTA of the 3x3
- *                       filter family streams its strip.
+ *                       shared-memory ring through which each CTA of a
+ *                       streaming kernel (the 3x3 filter family; uint8
+ *                       bilinear upscales) streams its strip;
+ *   RZ_OPT_STREAM       value 0 (automatic), 1 or 2: how uint8 bilinear
+ *                       resizes run.  0 streams vertical upscales (each source
+ *                       row's horizontal sums computed once, kept in
+ *                       registers) and stages tiles otherwise; 1 always stages
+ *                       tiles; 2 streams whenever a strip's source span fits
+ *                       (the exact 2x path keeps its own kernel).  Bit-exact
+ *                       either way.
  * Returns RZ_ERR_ARG for an unknown option or value.
  */
 #define RZ_OPT_STAGES 1
@@ -266,6 +275,7 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
 #define RZ_OPT_GRID_MODE 4
 #define RZ_OPT_PDL 5
 #define RZ_OPT_RING_ROWS 6
+#define RZ_OPT_STREAM 7
 RZ_API int resize_plan_set_option(rz_plan p, int option, int value);
 
 /*

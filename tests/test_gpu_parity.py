@@ -29,13 +29,15 @@ def rz():
     return m
 
 
-def gpu_u8(rz, img, OH, OW, mode, src_pitch=None, src_off=0, dst_pad=0, dst_off=0, tile=None, stream=None):
+def gpu_u8(rz, img, OH, OW, mode, src_pitch=None, src_off=0, dst_pad=0, dst_off=0, tile=None, stream=None, opts=()):
     if img.ndim == 2:
         img = img[:, :, None]
     H, W, C = img.shape
     src, _keep = device_image(img, src_pitch, src_off)
     out = Canvas(OH, OW, C, torch.uint8, dst_pad, dst_off)
     with rz.resize_plan_create(H, W, OH, OW, mode) as plan:
+        for k, v in opts:
+            rz.resize_plan_set_option(plan, k, v)
         if tile:
             rz.resize_plan_set_tile(plan, rz.KIND_U8, *tile)
         rz.resize_u8(plan, src, out.view, stream=stream)
@@ -159,6 +161,62 @@ def test_sweep_u8(rz, seed):
         img = synth.random_u8((H, W, C), seed=H * 1000 + W)
         for mode in (rz.RZ_LINEAR, rz.RZ_NEAREST):
             check_u8(rz, img, OH, OW, mode, src_pitch=W * C + pad, src_off=off, dst_pad=pad, dst_off=off)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_sweep_u8_streaming(rz, seed):
+    # the row-separable streaming form forced on every geometry (downscales
+    # too), with odd pitches and unaligned pointers
+    for (H, W, OH, OW, C, pad, off) in sweep_cases(700 + seed, 40):
+        img = synth.random_u8((H, W, C), seed=H * 1000 + W + 7)
+        check_u8(rz, img, OH, OW, rz.RZ_LINEAR, src_pitch=W * C + pad, src_off=off, dst_pad=pad, dst_off=off,
+                 opts=[(rz.RZ_OPT_STREAM, 2)])
+
+
+_STREAM_GEOMS = [(1080, 1920, 3, 2160, 3840), (300, 410, 3, 611, 797), (97, 130, 4, 260, 333),
+                 (64, 75, 1, 190, 201), (500, 700, 3, 333, 401), (33, 2000, 1, 70, 4100)]
+_stream_want = {}
+
+
+def stream_case(rz, geom):
+    H, W, C, OH, OW = geom
+    if geom not in _stream_want:
+        img = synth.smooth_rgb(W, H, 2) if C == 3 and W >= 1920 else synth.random_u8((H, W, C), seed=H + W + C)
+        _stream_want[geom] = (img, oracle.linear_u8(img, OH, OW))
+    return _stream_want[geom]
+
+
+@pytest.mark.parametrize("ring", [2, 3, 5, 0])
+@pytest.mark.parametrize("ctas", [1, 0, "per_unit"])
+def test_u8_stream_ring_and_grid_do_not_change_results(rz, ring, ctas):
+    # rings of two or three rows wrap every few rows and one CTA per SM makes
+    # each CTA walk many units; "per_unit" launches one CTA per unit
+    opts = [(rz.RZ_OPT_STREAM, 2), (rz.RZ_OPT_RING_ROWS, ring)]
+    if ctas == "per_unit":
+        opts += [(rz.RZ_OPT_GRID_MODE, 1), (rz.RZ_OPT_PDL, 0)]
+    else:
+        opts += [(rz.RZ_OPT_CTAS_PER_SM, ctas)]
+    for geom in _STREAM_GEOMS:
+        img, want = stream_case(rz, geom)
+        got = gpu_u8(rz, img, geom[3], geom[4], rz.RZ_LINEAR, opts=opts)
+        np.testing.assert_array_equal(got, want, err_msg=str(geom))
+
+
+@pytest.mark.parametrize("tile", [(1, 32), (7, 64), (40, 1024), (3, 100), (2160, 96), (16, 1)])
+def test_u8_stream_unit_shapes(rz, tile):
+    for geom in _STREAM_GEOMS[:3]:
+        img, want = stream_case(rz, geom)
+        got = gpu_u8(rz, img, geom[3], geom[4], rz.RZ_LINEAR, tile=tile, opts=[(rz.RZ_OPT_STREAM, 2)])
+        np.testing.assert_array_equal(got, want, err_msg=str((geom, tile)))
+
+
+def test_u8_stream_and_staged_tiles_agree(rz):
+    # both uint8 kernels on the same upscale: identical bytes
+    img, want = stream_case(rz, _STREAM_GEOMS[1])
+    a = gpu_u8(rz, img, 611, 797, rz.RZ_LINEAR, opts=[(rz.RZ_OPT_STREAM, 1)])
+    b = gpu_u8(rz, img, 611, 797, rz.RZ_LINEAR, opts=[(rz.RZ_OPT_STREAM, 2)])
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(a, want)
 
 
 @pytest.mark.parametrize("seed", range(3))
@@ -503,7 +561,8 @@ def test_options_reject_bad_values(rz):
     with rz.resize_plan_create(8, 8, 4, 4, rz.RZ_LINEAR) as plan:
         for opt, val in [(rz.RZ_OPT_STAGES, 5), (rz.RZ_OPT_STAGES, -1), (rz.RZ_OPT_GENERIC_ONLY, 2),
                          (rz.RZ_OPT_CTAS_PER_SM, 33), (rz.RZ_OPT_GRID_MODE, 2), (rz.RZ_OPT_PDL, 3),
-                         (rz.RZ_OPT_RING_ROWS, 1), (rz.RZ_OPT_RING_ROWS, 129), (99, 0)]:
+                         (rz.RZ_OPT_RING_ROWS, 1), (rz.RZ_OPT_RING_ROWS, 129), (rz.RZ_OPT_STREAM, 3),
+                         (rz.RZ_OPT_STREAM, -1), (99, 0)]:
             with pytest.raises(rz.ResizeError):
                 rz.resize_plan_set_option(plan, opt, val)
 
