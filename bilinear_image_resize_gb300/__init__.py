@@ -18,7 +18,7 @@ from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_EPI_
                       RZ_EPI_NORMALIZE_NCHW, RZ_ERR_ARG, RZ_ERR_CUDA, RZ_ERR_NOMEM, RZ_ERR_TIMEOUT,
                       RZ_ERR_UNSUPPORTED, RZ_F32, RZ_LINEAR, RZ_MAX_DIM, RZ_NEAREST, RZ_NOALLOC_MAX_DIM, RZ_OK,
                       RZ_OPT_CTAS_PER_SM, RZ_OPT_GENERIC_ONLY, RZ_OPT_GRID_MODE, RZ_OPT_PDL, RZ_OPT_RING_ROWS,
-                      RZ_OPT_STAGES, RZ_OPT_STREAM, RZ_U8, RzEpilogue)
+                      RZ_OPT_STAGES, RZ_OPT_U8_KERNEL, RZ_U8, RzEpilogue)
 
 __all__ = [
     "ResizeError", "Plan", "resize_plan_create", "resize_plan_destroy", "resize_plan_status",
@@ -30,7 +30,7 @@ __all__ = [
     "RZ_OK", "RZ_ERR_ARG", "RZ_ERR_UNSUPPORTED", "RZ_ERR_CUDA", "RZ_ERR_NOMEM", "RZ_ERR_TIMEOUT",
     "RZ_MAX_DIM", "KIND_U8", "KIND_F32", "KIND_NORMALIZE", "KIND_FILTER3X3",
     "RZ_OPT_STAGES", "RZ_OPT_GENERIC_ONLY", "RZ_OPT_CTAS_PER_SM", "RZ_OPT_GRID_MODE", "RZ_OPT_PDL",
-    "RZ_OPT_RING_ROWS", "RZ_OPT_STREAM",
+    "RZ_OPT_RING_ROWS", "RZ_OPT_U8_KERNEL",
 ]
 
 

@@ -31,7 +31,7 @@ RZ_OPT_CTAS_PER_SM = 3
 RZ_OPT_GRID_MODE = 4
 RZ_OPT_PDL = 5
 RZ_OPT_RING_ROWS = 6
-RZ_OPT_STREAM = 7
+RZ_OPT_U8_KERNEL = 7
 
 # kernel families for resize_plan_set_tile
 KIND_U8 = 0

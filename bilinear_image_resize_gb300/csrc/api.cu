@@ -128,7 +128,7 @@ struct rz_plan_s {
     int opt_grid_mode = 0;     // 0: persistent CTAs; 1: one CTA per tile
     int opt_pdl = 1;           // programmatic dependent launch
     int opt_ring_rows = 0;     // streaming kernels: source rows in the ring (0: automatic)
-    int opt_stream = 0;        // uint8 bilinear: 0 automatic, 1 staged tiles only, 2 streaming where it fits
+    int opt_u8_kernel = 0;     // uint8 bilinear: 0 automatic, 1 staged tiles, 2 streaming, 3 direct
 };
 
 namespace {
@@ -387,8 +387,8 @@ int get_stream_tile(rz_plan_s *p, int op, int C, int batch, TileCfg *out, const 
 // for it), unless the exact 2x path applies.
 bool want_u8_stream(const rz_plan_s &p, bool down2)
 {
-    if (p.mode != RZ_LINEAR || down2 || p.opt_stream == 1) return false;
-    return p.opt_stream == 2 || p.OH > p.H;
+    if (p.mode != RZ_LINEAR || down2) return false;
+    return p.opt_u8_kernel == 2 || (p.opt_u8_kernel == 0 && p.OH > p.H);
 }
 
 // Tile and grid for this call: the override if one is set, else the cached
@@ -523,6 +523,26 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     const int strip_bytes = t.TW * (nchw ? 1 : C) * out_es;
     a.tma_out = aligned16(dst) && (dst_pitch % 16 == 0) && (a.dst_bstride % 16 == 0) &&
                 (a.dst_plane % 16 == 0) && (t.tiles_x == 1 || strip_bytes % 16 == 0);
+    if (t.variant == rz::VAR_DOWN2 && (p->opt_u8_kernel == 0 || p->opt_u8_kernel == 3)) {
+        // the exact 2x path with direct loads when the layout allows its
+        // vector loads and stores (otherwise the staged-tile kernel below)
+        const uintptr_t lw = C == 3 ? 8 : 16, sw = C == 3 ? 4 : 8;
+        const uintptr_t sa = reinterpret_cast<uintptr_t>(src) | src_pitch | static_cast<uintptr_t>(a.src_bstride);
+        const uintptr_t da = reinterpret_cast<uintptr_t>(dst) | dst_pitch | static_cast<uintptr_t>(a.dst_bstride);
+        const void *dfn = rz::direct_down2_kernel_for(C);
+        if (dfn && sa % lw == 0 && da % sw == 0) {
+            if (!do_launch) return RZ_OK;
+            const int px = rz::down2_px(C);
+            const long long groups = static_cast<long long>(OH) * ((OW + px - 1) / px);
+            const int gx = static_cast<int>((groups + rz::kDirectThreads - 1) / rz::kDirectThreads);
+            CUtensorMap none;
+            std::memset(&none, 0, sizeof(none));
+            const int e = rz::launch_resize(dfn, a, none, gx, 0, p->opt_pdl != 0, stream, rz::kDirectThreads,
+                                            std::min(batch, 65535));
+            if (e != 0) return cuda_fail(static_cast<cudaError_t>(e));
+            return RZ_OK;
+        }
+    }
     const bool fl = (fam == rz::FAM_F32 || fam == rz::FAM_FILT);
     a.xt = fl ? p->d_xf : p->d_xq;
     a.yt = fl ? p->d_yf : p->d_yq;
@@ -719,9 +739,9 @@ int resize_plan_set_option(rz_plan p, int option, int value)
         if (value != 0 && (value < 2 || value > rz::kStreamRingMax)) return RZ_ERR_ARG;
         p->opt_ring_rows = value;
         break;
-    case RZ_OPT_STREAM:
-        if (value < 0 || value > 2) return RZ_ERR_ARG;
-        p->opt_stream = value;
+    case RZ_OPT_U8_KERNEL:
+        if (value < 0 || value > 3) return RZ_ERR_ARG;
+        p->opt_u8_kernel = value;
         break;
     default:
         return RZ_ERR_ARG;

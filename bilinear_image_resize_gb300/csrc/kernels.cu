@@ -476,25 +476,16 @@ __device__ void compute_generic(const KArgs &a, const StageView &sv, const TileG
     }
 }
 
-// Exact 2x downscale of uint8 (W = 2 OW, H = 2 OH).  Every column and row then
-// samples x = 2d + 1/2, so A0 = A1 = B0 = B1 = 1024 and the generic sum
-// reduces to out = (t0 + t1 + b0 + b1 + 2) >> 2: the same value, bit for bit.
-// The four taps are summed with dp4a; weights of 64 and a start of 128 put
-// 64 (sum + 2) in the accumulator, whose byte 1 is the rounded result, so a
-// byte permute packs it.  The tile's staged span starts at the tile's first
-// source byte, 16-byte aligned (the host keeps TW a multiple of 8 columns).
-__device__ __forceinline__ uint32_t pick_byte1(uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    return __byte_perm(__byte_perm(a, b, 0x0051), __byte_perm(c, d, 0x0051), 0x5410);
-}
-
+// Exact 2x downscale of uint8 (W = 2 OW, H = 2 OH): see down2_group.  The
+// tile's staged span starts at the tile's first source byte, 16-byte aligned
+// (the host keeps TW a multiple of 8 columns).
 template <int C>
 __device__ void compute_down2(const KArgs &a, const StageView &sv, const TileGeom &g, uint8_t *ob, int orow_bytes)
 {
     const int nr = g.dy1 - g.dy0, nc = g.dx1 - g.dx0;
     const int ofs0 = 2 * g.dx0 * C - sv.b_lo;    // 0 or a multiple of 16
-    // pixels per thread: 8 (C=1), 4 (C=3), 2 (C=4) -> 8, 12, 8 output bytes
-    constexpr int PX = (C == 1) ? 8 : (C == 3 ? 4 : 2);
+    constexpr int PX = down2_px(C);              // 8, 4, 2 pixels: 8, 12, 8 output bytes
+    constexpr int SW = 2 * PX * C / 4;           // source words per row and group
     const int ngrp = nc / PX;
     const int lg = min(8, ceil_log2(ngrp + 1));
     const int tpr = 1 << lg, rpp = kConsumers >> lg;
@@ -503,75 +494,28 @@ __device__ void compute_down2(const KArgs &a, const StageView &sv, const TileGeo
         const uint8_t *bot = sv.slots + sv.map[2 * rl + 1] * sv.slot_bytes + ofs0;
         uint8_t *orow = ob + rl * orow_bytes;
         for (int j = threadIdx.x & (tpr - 1); j < ngrp; j += tpr) {
-            if constexpr (C == 1) {
-                const uint4 t = *reinterpret_cast<const uint4 *>(top + 16 * j);
-                const uint4 b = *reinterpret_cast<const uint4 *>(bot + 16 * j);
-                const uint32_t tw[4] = {t.x, t.y, t.z, t.w}, bw[4] = {b.x, b.y, b.z, b.w};
-                uint32_t s[8];
-#pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    s[2 * k] = __dp4a(tw[k], 0x00004040u, __dp4a(bw[k], 0x00004040u, 128u));
-                    s[2 * k + 1] = __dp4a(tw[k], 0x40400000u, __dp4a(bw[k], 0x40400000u, 128u));
-                }
-                uint2 o;
-                o.x = pick_byte1(s[0], s[1], s[2], s[3]);
-                o.y = pick_byte1(s[4], s[5], s[6], s[7]);
-                *reinterpret_cast<uint2 *>(orow + 8 * j) = o;
-            } else if constexpr (C == 3) {
-                // 24 source bytes per row = words w0..w5; output pixel q covers
-                // source bytes [6q, 6q + 6): channel c sums bytes 6q+c and 6q+3+c
+            uint32_t tw[SW], bw[SW], o[SW / 2];
+            if constexpr (C == 3) {
                 const uint2 *tp = reinterpret_cast<const uint2 *>(top + 24 * j);
                 const uint2 *bp = reinterpret_cast<const uint2 *>(bot + 24 * j);
-                const uint2 t0 = tp[0], t1 = tp[1], t2 = tp[2];
-                const uint2 b0 = bp[0], b1 = bp[1], b2 = bp[2];
-                const uint32_t tw[6] = {t0.x, t0.y, t1.x, t1.y, t2.x, t2.y};
-                const uint32_t bw[6] = {b0.x, b0.y, b1.x, b1.y, b2.x, b2.y};
-                uint32_t s[12];
 #pragma unroll
-                for (int q = 0; q < 4; q += 2) {
-                    // even pixel: bytes 0..5 of words (k, k+1) with k = 3q/2
-                    const int k = 3 * q / 2;
-                    s[3 * q + 0] = __dp4a(tw[k], 0x40000040u, __dp4a(bw[k], 0x40000040u, 128u));
-                    s[3 * q + 1] = __dp4a(tw[k], 0x00004000u,
-                                          __dp4a(tw[k + 1], 0x00000040u,
-                                                 __dp4a(bw[k], 0x00004000u, __dp4a(bw[k + 1], 0x00000040u, 128u))));
-                    s[3 * q + 2] = __dp4a(tw[k], 0x00400000u,
-                                          __dp4a(tw[k + 1], 0x00004000u,
-                                                 __dp4a(bw[k], 0x00400000u, __dp4a(bw[k + 1], 0x00004000u, 128u))));
-                    // odd pixel: bytes 2..7 of words (k+1, k+2)
-                    s[3 * q + 3] = __dp4a(tw[k + 1], 0x00400000u,
-                                          __dp4a(tw[k + 2], 0x00004000u,
-                                                 __dp4a(bw[k + 1], 0x00400000u, __dp4a(bw[k + 2], 0x00004000u, 128u))));
-                    s[3 * q + 4] = __dp4a(tw[k + 1], 0x40000000u,
-                                          __dp4a(tw[k + 2], 0x00400000u,
-                                                 __dp4a(bw[k + 1], 0x40000000u, __dp4a(bw[k + 2], 0x00400000u, 128u))));
-                    s[3 * q + 5] = __dp4a(tw[k + 2], 0x40000040u, __dp4a(bw[k + 2], 0x40000040u, 128u));
+                for (int k = 0; k < 3; k++) {
+                    const uint2 t = tp[k], b = bp[k];
+                    tw[2 * k] = t.x; tw[2 * k + 1] = t.y;
+                    bw[2 * k] = b.x; bw[2 * k + 1] = b.y;
                 }
-                uint32_t *o = reinterpret_cast<uint32_t *>(orow + 12 * j);
-                o[0] = pick_byte1(s[0], s[1], s[2], s[3]);
-                o[1] = pick_byte1(s[4], s[5], s[6], s[7]);
-                o[2] = pick_byte1(s[8], s[9], s[10], s[11]);
             } else {
-                // C == 4: per output pixel four words; sum byte lanes in two
-                // 16-bit-lane halves (each sum <= 1022 fits)
                 const uint4 t = *reinterpret_cast<const uint4 *>(top + 16 * j);
                 const uint4 b = *reinterpret_cast<const uint4 *>(bot + 16 * j);
-                const uint32_t w[2][4] = {{t.x, t.y, b.x, b.y}, {t.z, t.w, b.z, b.w}};
-                uint2 o;
-                uint32_t r[2];
-#pragma unroll
-                for (int p = 0; p < 2; p++) {
-                    const uint32_t l = __byte_perm(w[p][0], 0, 0x4240) + __byte_perm(w[p][1], 0, 0x4240) +
-                                       __byte_perm(w[p][2], 0, 0x4240) + __byte_perm(w[p][3], 0, 0x4240) +
-                                       0x00020002u;
-                    const uint32_t h = __byte_perm(w[p][0], 0, 0x4341) + __byte_perm(w[p][1], 0, 0x4341) +
-                                       __byte_perm(w[p][2], 0, 0x4341) + __byte_perm(w[p][3], 0, 0x4341) +
-                                       0x00020002u;
-                    r[p] = ((l >> 2) & 0x00ff00ffu) | ((h << 6) & 0xff00ff00u);
-                }
-                o.x = r[0];
-                o.y = r[1];
-                *reinterpret_cast<uint2 *>(orow + 8 * j) = o;
+                tw[0] = t.x; tw[1] = t.y; tw[2] = t.z; tw[3] = t.w;
+                bw[0] = b.x; bw[1] = b.y; bw[2] = b.z; bw[3] = b.w;
+            }
+            down2_group<C>(tw, bw, o);
+            if constexpr (C == 3) {
+                uint32_t *op = reinterpret_cast<uint32_t *>(orow + 12 * j);
+                op[0] = o[0]; op[1] = o[1]; op[2] = o[2];
+            } else {
+                *reinterpret_cast<uint2 *>(orow + 8 * j) = make_uint2(o[0], o[1]);
             }
         }
         // columns left over after whole groups
@@ -635,6 +579,7 @@ __device__ void compute_normalize(const KArgs &a, const StageView &sv, const Til
 // (taken with warp shuffles) in registers, so every output is nine fmaf on
 // registers:  z = sum w[i*3+j] * r[row-1+i][col-1+j].  Lanes 0 and 31 only
 // supply the neighbours of lanes 1 and 30.
+
 // ------------------------------------------------------------------ the persistent kernel
 
 // OP: 0 plain resize (T, C, LINEAR, VAR), 1 normalise.
@@ -787,13 +732,13 @@ const void *kernel_for(int fam, int mode, int variant, int C)
 }
 
 int launch_resize(const void *fn, const KArgs &a, const CUtensorMap &tmap, int grid, size_t smem, bool pdl,
-                  void *stream)
+                  void *stream, int threads, int grid_y)
 {
-    if (grid <= 0)
+    if (grid <= 0 || grid_y <= 0)
         return 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), static_cast<unsigned>(grid_y), 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];

@@ -265,5 +265,77 @@ __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
                        __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040), 0x5410);
 }
 
+// ------------------------------------------------------------------ exact 2x downscale
+
+// Exact 2x downscale of uint8 (W = 2 OW, H = 2 OH).  Every column and row then
+// samples x = 2d + 1/2, so A0 = A1 = B0 = B1 = 1024 and the bilinear sum
+// reduces to out = (t0 + t1 + b0 + b1 + 2) >> 2: the same value, bit for bit.
+// The four taps are summed with dp4a; weights of 64 and a start of 128 put
+// 64 (sum + 2) in the accumulator (at most 65408), whose byte 1 is the
+// rounded result, so byte permutes pack it.
+
+__device__ __forceinline__ uint32_t pick_byte1(uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    return __byte_perm(__byte_perm(a, b, 0x0051), __byte_perm(c, d, 0x0051), 0x5410);
+}
+
+// One group of down2_px(C) output pixels: tw / bw are the group's source
+// words of the upper / lower row
+// (2 down2_px(C) C / 4 words each), o receives the down2_px(C) C / 4 output
+// words.
+template <int C>
+__device__ __forceinline__ void down2_group(const uint32_t *tw, const uint32_t *bw, uint32_t *o)
+{
+    if constexpr (C == 1) {
+        uint32_t s[8];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            s[2 * k] = __dp4a(tw[k], 0x00004040u, __dp4a(bw[k], 0x00004040u, 128u));
+            s[2 * k + 1] = __dp4a(tw[k], 0x40400000u, __dp4a(bw[k], 0x40400000u, 128u));
+        }
+        o[0] = pick_byte1(s[0], s[1], s[2], s[3]);
+        o[1] = pick_byte1(s[4], s[5], s[6], s[7]);
+    } else if constexpr (C == 3) {
+        // 24 source bytes per row = words w0..w5; output pixel q covers source
+        // bytes [6q, 6q + 6): channel c sums bytes 6q+c and 6q+3+c
+        uint32_t s[12];
+#pragma unroll
+        for (int q = 0; q < 4; q += 2) {
+            // even pixel: bytes 0..5 of words (k, k+1) with k = 3q/2
+            const int k = 3 * q / 2;
+            s[3 * q + 0] = __dp4a(tw[k], 0x40000040u, __dp4a(bw[k], 0x40000040u, 128u));
+            s[3 * q + 1] = __dp4a(tw[k], 0x00004000u,
+                                  __dp4a(tw[k + 1], 0x00000040u,
+                                         __dp4a(bw[k], 0x00004000u, __dp4a(bw[k + 1], 0x00000040u, 128u))));
+            s[3 * q + 2] = __dp4a(tw[k], 0x00400000u,
+                                  __dp4a(tw[k + 1], 0x00004000u,
+                                         __dp4a(bw[k], 0x00400000u, __dp4a(bw[k + 1], 0x00004000u, 128u))));
+            // odd pixel: bytes 2..7 of words (k+1, k+2)
+            s[3 * q + 3] = __dp4a(tw[k + 1], 0x00400000u,
+                                  __dp4a(tw[k + 2], 0x00004000u,
+                                         __dp4a(bw[k + 1], 0x00400000u, __dp4a(bw[k + 2], 0x00004000u, 128u))));
+            s[3 * q + 4] = __dp4a(tw[k + 1], 0x40000000u,
+                                  __dp4a(tw[k + 2], 0x00400000u,
+                                         __dp4a(bw[k + 1], 0x40000000u, __dp4a(bw[k + 2], 0x00400000u, 128u))));
+            s[3 * q + 5] = __dp4a(tw[k + 2], 0x40000040u, __dp4a(bw[k + 2], 0x40000040u, 128u));
+        }
+        o[0] = pick_byte1(s[0], s[1], s[2], s[3]);
+        o[1] = pick_byte1(s[4], s[5], s[6], s[7]);
+        o[2] = pick_byte1(s[8], s[9], s[10], s[11]);
+    } else {
+        // C == 4: per output pixel four words; sum byte lanes in two 16-bit-lane
+        // halves (each sum <= 1022 fits)
+        const uint32_t w[2][4] = {{tw[0], tw[1], bw[0], bw[1]}, {tw[2], tw[3], bw[2], bw[3]}};
+#pragma unroll
+        for (int p = 0; p < 2; p++) {
+            const uint32_t l = __byte_perm(w[p][0], 0, 0x4240) + __byte_perm(w[p][1], 0, 0x4240) +
+                               __byte_perm(w[p][2], 0, 0x4240) + __byte_perm(w[p][3], 0, 0x4240) + 0x00020002u;
+            const uint32_t h = __byte_perm(w[p][0], 0, 0x4341) + __byte_perm(w[p][1], 0, 0x4341) +
+                               __byte_perm(w[p][2], 0, 0x4341) + __byte_perm(w[p][3], 0, 0x4341) + 0x00020002u;
+            o[p] = ((l >> 2) & 0x00ff00ffu) | ((h << 6) & 0xff00ff00u);
+        }
+    }
+}
+
 }  // namespace dev
 }  // namespace rz

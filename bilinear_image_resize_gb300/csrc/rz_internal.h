@@ -156,10 +156,21 @@ const void *kernel_for(int fam, int mode, int variant, int C);
 // The streaming kernel for (StreamOp, mode, C); nullptr if none.
 const void *stream_kernel_for(int op, int mode, int C);
 
-// Launch it on `grid` CTAs (asynchronous), optionally as a programmatic
-// dependent launch.  `tmap` describes the source when a.tensor_in is set
-// (otherwise its contents are ignored).  Returns a cudaError_t value.
+// Launch it on grid x grid_y CTAs of `threads` (asynchronous), optionally as
+// a programmatic dependent launch.  `tmap` describes the source when
+// a.tensor_in is set (otherwise its contents are ignored).  Returns a
+// cudaError_t value.
 int launch_resize(const void *fn, const KArgs &a, const CUtensorMap &tmap, int grid, size_t smem, bool pdl,
-                  void *stream);
+                  void *stream, int threads = kThreads, int grid_y = 1);
+
+// Exact 2x uint8 downscale: output pixels per group, 8 (C = 1), 4 (C = 3),
+// 2 (C = 4), i.e. 8, 12, 8 output bytes from 16, 24, 16 source bytes of each
+// of two rows.
+__host__ __device__ constexpr int down2_px(int C) { return C == 1 ? 8 : (C == 3 ? 4 : 2); }
+
+// Direct-load kernels (direct.cu): a thread per output group, no staging.
+constexpr int kDirectThreads = 256;
+// The exact 2x uint8 downscale for C channels; nullptr if none.
+const void *direct_down2_kernel_for(int C);
 
 }  // namespace rz

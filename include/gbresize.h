@@ -260,13 +260,18 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  *                       shared-memory ring through which each CTA of a
  *                       streaming kernel (the 3x3 filter family; uint8
  *                       bilinear upscales) streams its strip;
- *   RZ_OPT_STREAM       value 0 (automatic), 1 or 2: how uint8 bilinear
- *                       resizes run.  0 streams vertical upscales (each source
+ *   RZ_OPT_U8_KERNEL    value 0 (automatic), 1, 2 or 3: which kernel runs
+ *                       uint8 bilinear resizes.  0: the exact 2x case with
+ *                       direct loads when the layout allows (source base,
+ *                       pitch and batch stride multiples of 16 bytes, 8 for
+ *                       three channels; output ones of 8, 4 for three
+ *                       channels), vertical upscales streamed (each source
  *                       row's horizontal sums computed once, kept in
- *                       registers) and stages tiles otherwise; 1 always stages
- *                       tiles; 2 streams whenever a strip's source span fits
- *                       (the exact 2x path keeps its own kernel).  Bit-exact
- *                       either way.
+ *                       registers), other cases in staged tiles; 1: staged
+ *                       tiles always; 2: streamed whenever a strip's source
+ *                       span fits (not the exact 2x case); 3: direct loads
+ *                       for the exact 2x case where the layout allows, staged
+ *                       tiles otherwise.  Bit-exact whichever runs.
  * Returns RZ_ERR_ARG for an unknown option or value.
  */
 #define RZ_OPT_STAGES 1
@@ -275,7 +280,7 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
 #define RZ_OPT_GRID_MODE 4
 #define RZ_OPT_PDL 5
 #define RZ_OPT_RING_ROWS 6
-#define RZ_OPT_STREAM 7
+#define RZ_OPT_U8_KERNEL 7
 RZ_API int resize_plan_set_option(rz_plan p, int option, int value);
 
 /*

@@ -170,7 +170,7 @@ def test_sweep_u8_streaming(rz, seed):
     for (H, W, OH, OW, C, pad, off) in sweep_cases(700 + seed, 40):
         img = synth.random_u8((H, W, C), seed=H * 1000 + W + 7)
         check_u8(rz, img, OH, OW, rz.RZ_LINEAR, src_pitch=W * C + pad, src_off=off, dst_pad=pad, dst_off=off,
-                 opts=[(rz.RZ_OPT_STREAM, 2)])
+                 opts=[(rz.RZ_OPT_U8_KERNEL, 2)])
 
 
 _STREAM_GEOMS = [(1080, 1920, 3, 2160, 3840), (300, 410, 3, 611, 797), (97, 130, 4, 260, 333),
@@ -191,7 +191,7 @@ def stream_case(rz, geom):
 def test_u8_stream_ring_and_grid_do_not_change_results(rz, ring, ctas):
     # rings of two or three rows wrap every few rows and one CTA per SM makes
     # each CTA walk many units; "per_unit" launches one CTA per unit
-    opts = [(rz.RZ_OPT_STREAM, 2), (rz.RZ_OPT_RING_ROWS, ring)]
+    opts = [(rz.RZ_OPT_U8_KERNEL, 2), (rz.RZ_OPT_RING_ROWS, ring)]
     if ctas == "per_unit":
         opts += [(rz.RZ_OPT_GRID_MODE, 1), (rz.RZ_OPT_PDL, 0)]
     else:
@@ -206,15 +206,15 @@ def test_u8_stream_ring_and_grid_do_not_change_results(rz, ring, ctas):
 def test_u8_stream_unit_shapes(rz, tile):
     for geom in _STREAM_GEOMS[:3]:
         img, want = stream_case(rz, geom)
-        got = gpu_u8(rz, img, geom[3], geom[4], rz.RZ_LINEAR, tile=tile, opts=[(rz.RZ_OPT_STREAM, 2)])
+        got = gpu_u8(rz, img, geom[3], geom[4], rz.RZ_LINEAR, tile=tile, opts=[(rz.RZ_OPT_U8_KERNEL, 2)])
         np.testing.assert_array_equal(got, want, err_msg=str((geom, tile)))
 
 
 def test_u8_stream_and_staged_tiles_agree(rz):
     # both uint8 kernels on the same upscale: identical bytes
     img, want = stream_case(rz, _STREAM_GEOMS[1])
-    a = gpu_u8(rz, img, 611, 797, rz.RZ_LINEAR, opts=[(rz.RZ_OPT_STREAM, 1)])
-    b = gpu_u8(rz, img, 611, 797, rz.RZ_LINEAR, opts=[(rz.RZ_OPT_STREAM, 2)])
+    a = gpu_u8(rz, img, 611, 797, rz.RZ_LINEAR, opts=[(rz.RZ_OPT_U8_KERNEL, 1)])
+    b = gpu_u8(rz, img, 611, 797, rz.RZ_LINEAR, opts=[(rz.RZ_OPT_U8_KERNEL, 2)])
     np.testing.assert_array_equal(a, b)
     np.testing.assert_array_equal(a, want)
 
@@ -528,10 +528,11 @@ def test_ring_depth_and_grid_do_not_change_results(rz, stages, ctas):
     # one or two CTAs per SM make every CTA walk many tiles, so each stage's
     # barrier goes through many phases; "per_tile" launches one CTA per tile
     img = synth.smooth_rgb(1920, 1080, 2)
+    # staged tiles everywhere (the options shape that kernel)
     if ctas == "per_tile":
-        opts = {rz.RZ_OPT_STAGES: stages, rz.RZ_OPT_GRID_MODE: 1, rz.RZ_OPT_PDL: 0}
+        opts = {rz.RZ_OPT_STAGES: stages, rz.RZ_OPT_GRID_MODE: 1, rz.RZ_OPT_PDL: 0, rz.RZ_OPT_U8_KERNEL: 1}
     else:
-        opts = {rz.RZ_OPT_STAGES: stages, rz.RZ_OPT_CTAS_PER_SM: ctas}
+        opts = {rz.RZ_OPT_STAGES: stages, rz.RZ_OPT_CTAS_PER_SM: ctas, rz.RZ_OPT_U8_KERNEL: 1}
     for (OH, OW) in [(540, 960), (720, 1280), (2160, 3840)]:
         got = run_u8_opts(rz, img, OH, OW, rz.RZ_LINEAR, opts)
         np.testing.assert_array_equal(got, oracle.linear_u8(img, OH, OW))
@@ -544,16 +545,51 @@ def test_ring_depth_and_grid_do_not_change_results(rz, stages, ctas):
 def test_exact_2x_path_is_bit_identical_to_generic(rz, C, geom):
     H, W = geom
     img = synth.random_u8((H, W, C), seed=H + W + C)
-    fast = run_u8_opts(rz, img, H // 2, W // 2, rz.RZ_LINEAR, {})
+    direct = run_u8_opts(rz, img, H // 2, W // 2, rz.RZ_LINEAR, {})
+    staged = run_u8_opts(rz, img, H // 2, W // 2, rz.RZ_LINEAR, {rz.RZ_OPT_U8_KERNEL: 1})
     slow = run_u8_opts(rz, img, H // 2, W // 2, rz.RZ_LINEAR, {rz.RZ_OPT_GENERIC_ONLY: 1})
-    np.testing.assert_array_equal(fast, slow)
-    np.testing.assert_array_equal(fast, oracle.linear_u8(img, H // 2, W // 2))
+    np.testing.assert_array_equal(direct, slow)
+    np.testing.assert_array_equal(staged, slow)
+    np.testing.assert_array_equal(direct, oracle.linear_u8(img, H // 2, W // 2))
+
+
+@pytest.mark.parametrize("C", [1, 3, 4])
+def test_exact_2x_direct_loads(rz, C):
+    # the direct-load kernel: ragged widths (a row's last pixels fewer than a
+    # group), a one-pixel output, unaligned layouts (which take the staged
+    # kernel) and both paths against the oracle
+    for (H, W) in [(2, 2), (2, 18), (6, 34), (30, 46), (64, 64), (200, 1002), (1080, 1926)]:
+        img = synth.random_u8((H, W, C), seed=H * 7 + W + C)
+        want = oracle.linear_u8(img, H // 2, W // 2)
+        for pad, off in [(0, 0), (16, 0), (3, 1), (8, 4)]:
+            got = gpu_u8(rz, img, H // 2, W // 2, rz.RZ_LINEAR, src_pitch=W * C + pad, src_off=off, dst_pad=pad,
+                         dst_off=off, opts=[(rz.RZ_OPT_U8_KERNEL, 3)])
+            np.testing.assert_array_equal(got, want, err_msg=str((H, W, pad, off)))
+
+
+def test_exact_2x_direct_batch_and_pdl_chain(rz):
+    # a batch through the direct kernel, then a second resize of its output
+    # queued right after it (the dependent launch must wait for the first)
+    N = 4
+    frames = np.stack([synth.random_u8((540, 960, 3), seed=60 + n) for n in range(N)])
+    src = torch.from_numpy(frames).cuda()
+    mid = torch.empty((N, 270, 480, 3), dtype=torch.uint8, device="cuda")
+    out = torch.empty((N, 135, 240, 3), dtype=torch.uint8, device="cuda")
+    with rz.resize_plan_create(540, 960, 270, 480, rz.RZ_LINEAR) as p1, \
+            rz.resize_plan_create(270, 480, 135, 240, rz.RZ_LINEAR) as p2:
+        for _ in range(3):
+            rz.resize_u8_batch(p1, src, mid)
+            rz.resize_u8_batch(p2, mid, out)
+        torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    for n in range(N):
+        np.testing.assert_array_equal(got[n], oracle.linear_u8(oracle.linear_u8(frames[n], 270, 480), 135, 240))
 
 
 @pytest.mark.parametrize("tile", [(1, 8), (1, 16), (2, 24), (3, 64), (1, 960), (4, 1920)])
 def test_exact_2x_path_tiles(rz, tile):
     img = synth.smooth_rgb(3840, 2160, 3)
-    got = run_u8_opts(rz, img, 1080, 1920, rz.RZ_LINEAR, {rz.RZ_OPT_STAGES: 2}, tile=tile)
+    got = run_u8_opts(rz, img, 1080, 1920, rz.RZ_LINEAR, {rz.RZ_OPT_STAGES: 2, rz.RZ_OPT_U8_KERNEL: 1}, tile=tile)
     np.testing.assert_array_equal(got, oracle.linear_u8(img, 1080, 1920))
 
 
@@ -561,8 +597,8 @@ def test_options_reject_bad_values(rz):
     with rz.resize_plan_create(8, 8, 4, 4, rz.RZ_LINEAR) as plan:
         for opt, val in [(rz.RZ_OPT_STAGES, 5), (rz.RZ_OPT_STAGES, -1), (rz.RZ_OPT_GENERIC_ONLY, 2),
                          (rz.RZ_OPT_CTAS_PER_SM, 33), (rz.RZ_OPT_GRID_MODE, 2), (rz.RZ_OPT_PDL, 3),
-                         (rz.RZ_OPT_RING_ROWS, 1), (rz.RZ_OPT_RING_ROWS, 129), (rz.RZ_OPT_STREAM, 3),
-                         (rz.RZ_OPT_STREAM, -1), (99, 0)]:
+                         (rz.RZ_OPT_RING_ROWS, 1), (rz.RZ_OPT_RING_ROWS, 129), (rz.RZ_OPT_U8_KERNEL, 4),
+                         (rz.RZ_OPT_U8_KERNEL, -1), (99, 0)]:
             with pytest.raises(rz.ResizeError):
                 rz.resize_plan_set_option(plan, opt, val)
 
