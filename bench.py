@@ -247,6 +247,8 @@ def gpu_arm(args, rank, local_rank, world):
         rz.resize_plan_set_option(plan, rz.RZ_OPT_GRID_MODE, 1)
     if args.no_pdl:
         rz.resize_plan_set_option(plan, rz.RZ_OPT_PDL, 0)
+    if args.u8_kernel:
+        rz.resize_plan_set_option(plan, rz.RZ_OPT_U8_KERNEL, args.u8_kernel)
     epi = None
     if kind == "norm":
         epi = rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=synth.NORM_MEAN, std=synth.NORM_STD)
@@ -604,6 +606,8 @@ def main():
     ap.add_argument("--ctas-per-sm", type=int, default=0, help="cap resident CTAs per SM (tuning only)")
     ap.add_argument("--grid-per-tile", action="store_true", help="one CTA per tile (tuning only)")
     ap.add_argument("--no-pdl", action="store_true", help="plain stream-ordered launches (tuning only)")
+    ap.add_argument("--u8-kernel", type=int, default=0,
+                    help="RZ_OPT_U8_KERNEL: 1 staged tiles, 2 streaming, 3 direct loads (tuning only)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--batch-frames", type=int, default=8,
                     help="uint8 workloads: also time this many frames per resize_u8_batch launch (0: skip)")
@@ -664,7 +668,8 @@ def main():
                 "parallelism": f"{world} independent replica(s)",
                 "tuning": {k: v for k, v in (("tile", args.tile), ("stages", args.stages),
                                              ("generic_only", args.generic), ("ctas_per_sm", args.ctas_per_sm),
-                                             ("grid_per_tile", args.grid_per_tile), ("no_pdl", args.no_pdl))
+                                             ("grid_per_tile", args.grid_per_tile), ("no_pdl", args.no_pdl),
+                                             ("u8_kernel", args.u8_kernel))
                            if v} or "automatic",
             },
             "hbm_gbs": r["achieved_gbs"],

@@ -546,6 +546,25 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     const bool fl = (fam == rz::FAM_F32 || fam == rz::FAM_FILT);
     a.xt = fl ? p->d_xf : p->d_xq;
     a.yt = fl ? p->d_yf : p->d_yq;
+    // any other uint8-source resize not streamed: direct loads (unless the
+    // option asks for staged tiles, or for streaming that did not fit)
+    const int opt = p->opt_u8_kernel;
+    const bool direct = t.stream == 0 && ((fam == rz::FAM_U8 && (opt == 0 || opt == 3)) ||
+                                          (fam == rz::FAM_NORM && opt != 1));
+    if (direct) {
+        const void *dfn = rz::direct_kernel_for(fam == rz::FAM_NORM ? rz::DIRECT_NORM : rz::DIRECT_U8, mode, C);
+        if (dfn) {
+            if (!do_launch) return RZ_OK;
+            const long long groups = static_cast<long long>(OH) * ((OW + rz::kDirectRun - 1) / rz::kDirectRun);
+            const int gx = static_cast<int>((groups + rz::kDirectThreads - 1) / rz::kDirectThreads);
+            CUtensorMap none;
+            std::memset(&none, 0, sizeof(none));
+            const int e = rz::launch_resize(dfn, a, none, gx, 0, p->opt_pdl != 0, stream, rz::kDirectThreads,
+                                            std::min(batch, 65535));
+            if (e != 0) return cuda_fail(static_cast<cudaError_t>(e));
+            return RZ_OK;
+        }
+    }
     a.status = p->d_status;
     CUtensorMap tmap;
     std::memset(&tmap, 0, sizeof(tmap));

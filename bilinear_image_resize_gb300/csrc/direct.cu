@@ -1,5 +1,6 @@
-// Direct-load kernel for sm_103a: the exact 2x uint8 downscale with every
-// thread loading its own source bytes.
+// Direct-load kernels for sm_103a: every thread loads its own source bytes
+// and writes its own outputs (the exact 2x uint8 downscale; any ratio with a
+// uint8 source, plain or through the normalise epilogue).
 //
 // For one frame per launch the path is bound by how fast HBM requests get in
 // flight after the launch, not by bandwidth: a thread per output group, each
@@ -90,7 +91,138 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_direct(const KArgs a, 
     }
 }
 
+// Any ratio, uint8 source: bilinear (exact 11-bit fixed point, the tiled
+// kernel's arithmetic: hsum_u8 per row, then (B0 hT + B1 hB + 2^21) >> 22)
+// or nearest, written as uint8 HWC (OP = DIRECT_U8) or through the normalise
+// epilogue as float32 planes (OP = DIRECT_NORM: y = q * scale[c] + shift[c],
+// CUDA interpolation page §4.2).  A thread takes four consecutive output
+// pixels of one row: their four table entries in two 16-byte loads, their
+// taps from the two source rows through L1 (neighbouring threads share
+// them), 32-bit words where the row layout allows and the taps lie at least
+// 12 bytes before the row's end (so no load passes the row), bytes otherwise.
+template <int OP, int C, int LINEAR>
+__global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const __grid_constant__ CUtensorMap)
+{
+    constexpr int RUN = 4;
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int gpr = (a.OW + RUN - 1) / RUN;
+    const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
+    if (idx >= a.OH * gpr)
+        return;
+    const int dy = idx / gpr, x0 = (idx - dy * gpr) * RUN;
+    const int npx = min(RUN, a.OW - x0);
+    const int row_bytes = a.W * C;
+    // the tables are 16-byte aligned with spare entries past their end, and
+    // x0 is a multiple of 4
+    const int4 xa = __ldg(reinterpret_cast<const int4 *>(a.xt + x0));
+    const int4 xb = __ldg(reinterpret_cast<const int4 *>(a.xt + x0 + 2));
+    const int xs[RUN] = {xa.x, xa.z, xb.x, xb.z};   // left tap (nearest: the tap)
+    const int xw[RUN] = {xa.y, xa.w, xb.y, xb.w};   // right tap's 11-bit weight
+    const int2 ye = __ldg(a.yt + dy);
+    const int r0 = ye.x, r1 = LINEAR ? min(ye.x + 1, a.H - 1) : ye.x;
+    const int B1 = ye.y, B0 = 2048 - B1;
+    const bool words_in = ((reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
+                            static_cast<uintptr_t>(a.src_bstride)) & 3) == 0;
+    for (int b = blockIdx.y; b < a.batch; b += gridDim.y) {
+        const uint8_t *img = a.src + (long long)b * a.src_bstride;
+        const uint8_t *top = img + (long long)r0 * a.src_pitch;
+        const uint8_t *bot = img + (long long)r1 * a.src_pitch;
+        int q[RUN][C];
+#pragma unroll
+        for (int k = 0; k < RUN; k++) {
+            const int o0 = xs[k] * C;
+            if (k >= npx) {
+#pragma unroll
+                for (int c = 0; c < C; c++)
+                    q[k][c] = 0;
+            } else if (!LINEAR) {
+#pragma unroll
+                for (int c = 0; c < C; c++)
+                    q[k][c] = __ldg(top + o0 + c);
+            } else {
+                int hT[C], hB[C];
+                if (words_in && o0 + 12 <= row_bytes) {
+                    const uint32_t aw = static_cast<uint32_t>(2048 - xw[k]) | (static_cast<uint32_t>(xw[k]) << 16);
+                    hsum_u8<C>(top, o0, aw, hT);
+                    hsum_u8<C>(bot, o0, aw, hB);
+                } else {
+                    const int o1 = min(xs[k] + 1, a.W - 1) * C;
+#pragma unroll
+                    for (int c = 0; c < C; c++) {
+                        hT[c] = (2048 - xw[k]) * __ldg(top + o0 + c) + xw[k] * __ldg(top + o1 + c);
+                        hB[c] = (2048 - xw[k]) * __ldg(bot + o0 + c) + xw[k] * __ldg(bot + o1 + c);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < C; c++)
+                    q[k][c] = (B0 * hT[c] + B1 * hB[c] + (1 << 21)) >> 22;
+            }
+        }
+        if constexpr (OP == DIRECT_U8) {
+            uint8_t *op = a.dst + (long long)b * a.dst_bstride + (long long)dy * a.dst_pitch + (long long)x0 * C;
+            const bool words = npx == RUN && ((reinterpret_cast<uintptr_t>(op)) & 3) == 0;
+            if (words) {
+                uint32_t *o = reinterpret_cast<uint32_t *>(op);
+                if constexpr (C == 1) {
+                    __stcs(o, pack4(q[0][0], q[1][0], q[2][0], q[3][0]));
+                } else if constexpr (C == 3) {
+                    __stcs(o, pack4(q[0][0], q[0][1], q[0][2], q[1][0]));
+                    __stcs(o + 1, pack4(q[1][1], q[1][2], q[2][0], q[2][1]));
+                    __stcs(o + 2, pack4(q[2][2], q[3][0], q[3][1], q[3][2]));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < RUN; k++)
+                        __stcs(o + k, pack4(q[k][0], q[k][1], q[k][2], q[k][3]));
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < RUN; k++)
+                    if (k < npx)
+#pragma unroll
+                        for (int c = 0; c < C; c++)
+                            op[k * C + c] = static_cast<uint8_t>(q[k][c]);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < C; c++) {
+                float *pl = reinterpret_cast<float *>(a.dst + (long long)b * a.dst_bstride + (long long)c * a.dst_plane +
+                                                      (long long)dy * a.dst_pitch) + x0;
+                float f[RUN];
+#pragma unroll
+                for (int k = 0; k < RUN; k++)
+                    f[k] = fmaf(static_cast<float>(q[k][c]), a.scale[c], a.shift[c]);
+                if (npx == RUN && (reinterpret_cast<uintptr_t>(pl) & 15) == 0) {
+                    __stcs(reinterpret_cast<float4 *>(pl), make_float4(f[0], f[1], f[2], f[3]));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < RUN; k++)
+                        if (k < npx)
+                            __stcs(pl + k, f[k]);
+                }
+            }
+        }
+    }
+}
+
 }  // namespace
+
+// Any ratio: op DIRECT_U8 (bilinear or nearest) or DIRECT_NORM (bilinear).
+const void *direct_kernel_for(int op, int mode, int C)
+{
+    using Fn = void (*)(const KArgs, const CUtensorMap);
+    static const Fn u8[2][3] = {{k_direct<DIRECT_U8, 1, 0>, k_direct<DIRECT_U8, 3, 0>, k_direct<DIRECT_U8, 4, 0>},
+                                {k_direct<DIRECT_U8, 1, 1>, k_direct<DIRECT_U8, 3, 1>, k_direct<DIRECT_U8, 4, 1>}};
+    static const Fn norm[3] = {k_direct<DIRECT_NORM, 1, 1>, k_direct<DIRECT_NORM, 3, 1>,
+                               k_direct<DIRECT_NORM, 4, 1>};
+    const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
+    if (ci < 0)
+        return nullptr;
+    const int m = mode == RZ_LINEAR ? 1 : 0;
+    if (op == DIRECT_NORM)
+        return m ? reinterpret_cast<const void *>(norm[ci]) : nullptr;
+    return reinterpret_cast<const void *>(u8[m][ci]);
+}
 
 const void *direct_down2_kernel_for(int C)
 {

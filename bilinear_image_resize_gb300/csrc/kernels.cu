@@ -571,15 +571,6 @@ __device__ void compute_normalize(const KArgs &a, const StageView &sv, const Til
     }
 }
 
-// Bilinear + 3x3 filter, as a sliding window in registers.  Warp w owns
-// the output columns dx0 + 30w .. dx0 + 30w + 29; lane l resizes the column
-// dx0 + 30w + l - 1 (clamped into the output grid: replicate border), one
-// output row after another from row dy0 - 1 to dy1 (also clamped).  Each
-// lane keeps its column's last three resized rows and its two neighbours'
-// (taken with warp shuffles) in registers, so every output is nine fmaf on
-// registers:  z = sum w[i*3+j] * r[row-1+i][col-1+j].  Lanes 0 and 31 only
-// supply the neighbours of lanes 1 and 30.
-
 // ------------------------------------------------------------------ the persistent kernel
 
 // OP: 0 plain resize (T, C, LINEAR, VAR), 1 normalise.

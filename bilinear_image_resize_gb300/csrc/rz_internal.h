@@ -172,5 +172,10 @@ __host__ __device__ constexpr int down2_px(int C) { return C == 1 ? 8 : (C == 3 
 constexpr int kDirectThreads = 256;
 // The exact 2x uint8 downscale for C channels; nullptr if none.
 const void *direct_down2_kernel_for(int C);
+// Any ratio, uint8 source: DIRECT_U8 (uint8 out) or DIRECT_NORM (normalise
+// epilogue, float32 planes) for (mode, C); nullptr if none.
+enum DirectOp { DIRECT_U8 = 0, DIRECT_NORM = 1 };
+constexpr int kDirectRun = 4;   // output pixels per thread
+const void *direct_kernel_for(int op, int mode, int C);
 
 }  // namespace rz

@@ -163,6 +163,27 @@ def test_sweep_u8(rz, seed):
             check_u8(rz, img, OH, OW, mode, src_pitch=W * C + pad, src_off=off, dst_pad=pad, dst_off=off)
 
 
+@pytest.mark.parametrize("seed", range(2))
+def test_sweep_u8_staged_tiles(rz, seed):
+    # the staged-tile kernel forced on every geometry (the default takes
+    # direct loads or streaming)
+    for (H, W, OH, OW, C, pad, off) in sweep_cases(800 + seed, 40):
+        img = synth.random_u8((H, W, C), seed=H * 1000 + W + 9)
+        for mode in (rz.RZ_LINEAR, rz.RZ_NEAREST):
+            check_u8(rz, img, OH, OW, mode, src_pitch=W * C + pad, src_off=off, dst_pad=pad, dst_off=off,
+                     opts=[(rz.RZ_OPT_U8_KERNEL, 1)])
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_sweep_u8_direct(rz, seed):
+    # direct loads forced on every geometry, upscales too
+    for (H, W, OH, OW, C, pad, off) in sweep_cases(900 + seed, 40):
+        img = synth.random_u8((H, W, C), seed=H * 1000 + W + 11)
+        for mode in (rz.RZ_LINEAR, rz.RZ_NEAREST):
+            check_u8(rz, img, OH, OW, mode, src_pitch=W * C + pad, src_off=off, dst_pad=pad, dst_off=off,
+                     opts=[(rz.RZ_OPT_U8_KERNEL, 3)])
+
+
 @pytest.mark.parametrize("seed", range(3))
 def test_sweep_u8_streaming(rz, seed):
     # the row-separable streaming form forced on every geometry (downscales
@@ -250,7 +271,9 @@ def test_sweep_fused_filter(rz, seed):
 
 
 @pytest.mark.parametrize("seed", range(3))
-def test_sweep_fused_normalize(rz, seed):
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_sweep_fused_normalize(rz, seed, kernel):
+    # kernel 0: automatic (direct loads); 1: staged tiles
     rng = np.random.default_rng(400 + seed)
     for _ in range(12):
         H, W, OH, OW = (int(v) for v in rng.integers(1, 90, size=4))
@@ -262,6 +285,7 @@ def test_sweep_fused_normalize(rz, seed):
         src = torch.from_numpy(frames).cuda()
         dst = torch.empty((N, C, OH, OW), dtype=torch.float32, device="cuda")
         with rz.resize_plan_create(H, W, OH, OW, rz.RZ_LINEAR) as plan:
+            rz.resize_plan_set_option(plan, rz.RZ_OPT_U8_KERNEL, kernel)
             e = rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=np.float32(mean), std=np.float32(std))
             rz.resize_fused(plan, src, dst, e)
             torch.cuda.synchronize()
