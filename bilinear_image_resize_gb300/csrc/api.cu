@@ -523,13 +523,16 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     const int strip_bytes = t.TW * (nchw ? 1 : C) * out_es;
     a.tma_out = aligned16(dst) && (dst_pitch % 16 == 0) && (a.dst_bstride % 16 == 0) &&
                 (a.dst_plane % 16 == 0) && (t.tiles_x == 1 || strip_bytes % 16 == 0);
-    if (t.variant == rz::VAR_DOWN2 && (p->opt_u8_kernel == 0 || p->opt_u8_kernel == 3)) {
+    // exact 2x, bilinear (the plan's tables are the 2x pattern) or nearest
+    // (floor(2d) = 2d always)
+    const bool nearest2 = fam == rz::FAM_U8 && mode == RZ_NEAREST && W == 2 * OW && H == 2 * OH && !p->opt_generic;
+    if ((t.variant == rz::VAR_DOWN2 || nearest2) && (p->opt_u8_kernel == 0 || p->opt_u8_kernel == 3)) {
         // the exact 2x path with direct loads when the layout allows its
-        // vector loads and stores (otherwise the staged-tile kernel below)
+        // vector loads and stores (otherwise the kernels below)
         const uintptr_t lw = C == 3 ? 8 : 16, sw = C == 3 ? 4 : 8;
         const uintptr_t sa = reinterpret_cast<uintptr_t>(src) | src_pitch | static_cast<uintptr_t>(a.src_bstride);
         const uintptr_t da = reinterpret_cast<uintptr_t>(dst) | dst_pitch | static_cast<uintptr_t>(a.dst_bstride);
-        const void *dfn = rz::direct_down2_kernel_for(C);
+        const void *dfn = rz::direct_down2_kernel_for(mode, C);
         if (dfn && sa % lw == 0 && da % sw == 0) {
             if (!do_launch) return RZ_OK;
             const int px = rz::down2_px(C);

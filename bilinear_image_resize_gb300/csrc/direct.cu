@@ -34,7 +34,9 @@ using namespace dev;
 // by the host: W = 2 OW, H = 2 OH; source base, pitch and batch stride
 // multiples of the load width (16 bytes for 1 and 4 channels, 8 for 3);
 // output base, pitch and batch stride multiples of the store width (8, 4).
-template <int C>
+// LINEAR = 0 is the exact 2x nearest: every other pixel of every other row
+// (only the upper row is read).
+template <int C, int LINEAR>
 __global__ void __launch_bounds__(kDirectThreads) k_down2_direct(const KArgs a, const __grid_constant__ CUtensorMap)
 {
     constexpr int PX = down2_px(C);       // output pixels per group
@@ -59,17 +61,25 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_direct(const KArgs a, 
                 const uint2 *bp = reinterpret_cast<const uint2 *>(bot + SB * j);
 #pragma unroll
                 for (int k = 0; k < 3; k++) {
-                    const uint2 t = __ldcs(tp + k), u = __ldcs(bp + k);
+                    const uint2 t = __ldcs(tp + k);
                     tw[2 * k] = t.x; tw[2 * k + 1] = t.y;
-                    bw[2 * k] = u.x; bw[2 * k + 1] = u.y;
+                    if (LINEAR) {
+                        const uint2 u = __ldcs(bp + k);
+                        bw[2 * k] = u.x; bw[2 * k + 1] = u.y;
+                    }
                 }
             } else {
                 const uint4 t = __ldcs(reinterpret_cast<const uint4 *>(top + SB * j));
-                const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(bot + SB * j));
                 tw[0] = t.x; tw[1] = t.y; tw[2] = t.z; tw[3] = t.w;
-                bw[0] = u.x; bw[1] = u.y; bw[2] = u.z; bw[3] = u.w;
+                if (LINEAR) {
+                    const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(bot + SB * j));
+                    bw[0] = u.x; bw[1] = u.y; bw[2] = u.z; bw[3] = u.w;
+                }
             }
-            down2_group<C>(tw, bw, o);
+            if (LINEAR)
+                down2_group<C>(tw, bw, o);
+            else
+                down2_nearest_group<C>(tw, o);
             if constexpr (C == 3) {
                 uint32_t *op = reinterpret_cast<uint32_t *>(out + OB * j);
                 __stcs(op, o[0]);
@@ -84,8 +94,12 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_direct(const KArgs a, 
 #pragma unroll
                 for (int c = 0; c < C; c++) {
                     const int o = 2 * p * C + c;
-                    const int s = top[o] + top[o + C] + bot[o] + bot[o + C] + 2;
-                    out[p * C + c] = static_cast<uint8_t>(s >> 2);
+                    if (LINEAR) {
+                        const int s = top[o] + top[o + C] + bot[o] + bot[o + C] + 2;
+                        out[p * C + c] = static_cast<uint8_t>(s >> 2);
+                    } else {
+                        out[p * C + c] = top[o];
+                    }
                 }
         }
     }
@@ -224,12 +238,13 @@ const void *direct_kernel_for(int op, int mode, int C)
     return reinterpret_cast<const void *>(u8[m][ci]);
 }
 
-const void *direct_down2_kernel_for(int C)
+const void *direct_down2_kernel_for(int mode, int C)
 {
     using Fn = void (*)(const KArgs, const CUtensorMap);
-    static const Fn k[3] = {k_down2_direct<1>, k_down2_direct<3>, k_down2_direct<4>};
+    static const Fn k[2][3] = {{k_down2_direct<1, 0>, k_down2_direct<3, 0>, k_down2_direct<4, 0>},
+                               {k_down2_direct<1, 1>, k_down2_direct<3, 1>, k_down2_direct<4, 1>}};
     const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
-    return ci < 0 ? nullptr : reinterpret_cast<const void *>(k[ci]);
+    return ci < 0 ? nullptr : reinterpret_cast<const void *>(k[mode == RZ_LINEAR ? 1 : 0][ci]);
 }
 
 }  // namespace rz

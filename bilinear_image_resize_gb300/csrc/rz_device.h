@@ -337,5 +337,25 @@ __device__ __forceinline__ void down2_group(const uint32_t *tw, const uint32_t *
     }
 }
 
+// Exact 2x nearest: output pixel p is source pixel 2p of row 2 dy (floor(d n_in
+// / n_out) = 2d).  One group from the upper row's words: the first pixel of
+// each source pair, packed by byte permutes (source byte indices in the
+// comments).
+template <int C>
+__device__ __forceinline__ void down2_nearest_group(const uint32_t *tw, uint32_t *o)
+{
+    if constexpr (C == 1) {
+        o[0] = __byte_perm(tw[0], tw[1], 0x6420);   // 0 2 4 6
+        o[1] = __byte_perm(tw[2], tw[3], 0x6420);   // 8 10 12 14
+    } else if constexpr (C == 3) {
+        o[0] = __byte_perm(tw[0], tw[1], 0x6210);                                  // 0 1 2 6
+        o[1] = __byte_perm(__byte_perm(tw[1], tw[2], 0x0043), tw[3], 0x5410);      // 7 8 12 13
+        o[2] = __byte_perm(__byte_perm(tw[3], tw[4], 0x0762), tw[5], 0x4210);      // 14 18 19 20
+    } else {
+        o[0] = tw[0];   // pixel 0
+        o[1] = tw[2];   // pixel 2
+    }
+}
+
 }  // namespace dev
 }  // namespace rz

@@ -170,8 +170,9 @@ __host__ __device__ constexpr int down2_px(int C) { return C == 1 ? 8 : (C == 3 
 
 // Direct-load kernels (direct.cu): a thread per output group, no staging.
 constexpr int kDirectThreads = 256;
-// The exact 2x uint8 downscale for C channels; nullptr if none.
-const void *direct_down2_kernel_for(int C);
+// The exact 2x uint8 downscale (bilinear or nearest) for C channels; nullptr
+// if none.
+const void *direct_down2_kernel_for(int mode, int C);
 // Any ratio, uint8 source: DIRECT_U8 (uint8 out) or DIRECT_NORM (normalise
 // epilogue, float32 planes) for (mode, C); nullptr if none.
 enum DirectOp { DIRECT_U8 = 0, DIRECT_NORM = 1 };

@@ -584,11 +584,12 @@ def test_exact_2x_direct_loads(rz, C):
     # kernel) and both paths against the oracle
     for (H, W) in [(2, 2), (2, 18), (6, 34), (30, 46), (64, 64), (200, 1002), (1080, 1926)]:
         img = synth.random_u8((H, W, C), seed=H * 7 + W + C)
-        want = oracle.linear_u8(img, H // 2, W // 2)
-        for pad, off in [(0, 0), (16, 0), (3, 1), (8, 4)]:
-            got = gpu_u8(rz, img, H // 2, W // 2, rz.RZ_LINEAR, src_pitch=W * C + pad, src_off=off, dst_pad=pad,
-                         dst_off=off, opts=[(rz.RZ_OPT_U8_KERNEL, 3)])
-            np.testing.assert_array_equal(got, want, err_msg=str((H, W, pad, off)))
+        for mode, fn in ((rz.RZ_LINEAR, oracle.linear_u8), (rz.RZ_NEAREST, oracle.nearest_u8)):
+            want = fn(img, H // 2, W // 2)
+            for pad, off in [(0, 0), (16, 0), (3, 1), (8, 4)]:
+                got = gpu_u8(rz, img, H // 2, W // 2, mode, src_pitch=W * C + pad, src_off=off, dst_pad=pad,
+                             dst_off=off, opts=[(rz.RZ_OPT_U8_KERNEL, 3)])
+                np.testing.assert_array_equal(got, want, err_msg=str((mode, H, W, pad, off)))
 
 
 def test_exact_2x_direct_batch_and_pdl_chain(rz):
