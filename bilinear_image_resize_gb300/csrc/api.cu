@@ -383,8 +383,9 @@ int get_stream_tile(rz_plan_s *p, int op, int C, int batch, TileCfg *out, const 
 }
 
 // The uint8 bilinear resize takes the streaming form for vertical upscales,
-// where each source row feeds several output rows (or when the option asks
-// for it), unless the exact 2x path applies.
+// where each source row feeds several output rows (measured faster there than
+// the direct kernels), or when the option asks for it; not for the exact 2x
+// case.
 bool want_u8_stream(const rz_plan_s &p, bool down2)
 {
     if (p.mode != RZ_LINEAR || down2) return false;
@@ -467,6 +468,70 @@ int check_device(const rz_plan_s *p)
 
 bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
 
+// Direct-load kernels (direct.cu) for uint8-source resizes, unless the
+// option asks for staged tiles (1) or streaming (2), and except automatic
+// bilinear vertical upscales (streamed).  Exact 2x (bilinear tables of the
+// 2x pattern, or nearest at W = 2 OW, H = 2 OH) with vector loads where the
+// layout allows; vertical bilinear upscales (option 3) with each thread
+// walking rows; everything else one thread per four output pixels.  Returns
+// true with *rc set when it handled the call.
+bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do_launch, int *rc)
+{
+    const int opt = p->opt_u8_kernel;
+    if (!((fam == rz::FAM_U8 && (opt == 0 || opt == 3)) || (fam == rz::FAM_NORM && opt != 1))) return false;
+    if (fam == rz::FAM_U8 && opt == 0 && mode == RZ_LINEAR && a.OH > a.H && !is_down2(*p)) return false;
+    const int C = a.C, batch = a.batch;
+    a.xt = p->d_xq;
+    a.yt = p->d_yq;
+    const void *fn = nullptr;
+    long long groups = 0;
+    if (fam == rz::FAM_U8 && !p->opt_generic && a.W == 2 * a.OW && a.H == 2 * a.OH &&
+        (mode == RZ_NEAREST || is_down2(*p))) {
+        const uintptr_t lw = C == 3 ? 8 : 16, sw = C == 3 ? 4 : 8;
+        const uintptr_t sa = reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
+                             static_cast<uintptr_t>(a.src_bstride);
+        const uintptr_t da = reinterpret_cast<uintptr_t>(a.dst) | static_cast<uintptr_t>(a.dst_pitch) |
+                             static_cast<uintptr_t>(a.dst_bstride);
+        if (sa % lw == 0 && da % sw == 0) {
+            fn = rz::direct_down2_kernel_for(mode, C);
+            const int px = rz::down2_px(C);
+            groups = static_cast<long long>(a.OH) * ((a.OW + px - 1) / px);
+        }
+    }
+    const long long gpr = (a.OW + rz::kDirectRun - 1) / rz::kDirectRun;
+    if (!fn && fam == rz::FAM_U8 && mode == RZ_LINEAR && a.OH > a.H) {
+        // about 2048 threads per SM, each walking R output rows
+        fn = rz::direct_rows_kernel_for(C);
+        int sms = 0;
+        const cudaError_t ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+        if (ce != cudaSuccess) {
+            *rc = cuda_fail(ce);
+            return true;
+        }
+        int R = p->over_tr[fam];
+        if (R <= 0) {
+            const long long want = static_cast<long long>(sms) * 2048;
+            R = static_cast<int>(std::clamp<long long>((gpr * a.OH * batch + want - 1) / want, 2, 32));
+        }
+        a.TR = std::min(R, a.OH);
+        groups = gpr * ((a.OH + a.TR - 1) / a.TR);
+    }
+    if (!fn) {
+        fn = rz::direct_kernel_for(fam == rz::FAM_NORM ? rz::DIRECT_NORM : rz::DIRECT_U8, mode, C);
+        groups = gpr * a.OH;
+    }
+    if (!fn) return false;
+    *rc = RZ_OK;
+    if (!do_launch) return true;
+    const int gx = static_cast<int>((groups + rz::kDirectThreads - 1) / rz::kDirectThreads);
+    CUtensorMap none;
+    std::memset(&none, 0, sizeof(none));
+    const int e = rz::launch_resize(fn, a, none, gx, 0, p->opt_pdl != 0, stream, rz::kDirectThreads,
+                                    std::min(batch, 65535));
+    if (e != 0) *rc = cuda_fail(static_cast<cudaError_t>(e));
+    return true;
+}
+
 // Shared body of every resize entry point.  `planes` > 0 selects the planar
 // (NCHW) output of the normalise epilogue.
 int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bstride, void *dst, size_t dst_pitch,
@@ -499,11 +564,6 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     int rc = check_device(p);
     if (rc != RZ_OK) return rc;
 
-    TileCfg t;
-    const void *fn = nullptr;
-    rc = get_tile(p, fam, C, batch, &t, &fn);
-    if (rc != RZ_OK) return rc;
-
     KArgs a = extra;
     a.src = static_cast<const uint8_t *>(src);
     a.src_pitch = static_cast<long long>(src_pitch);
@@ -513,8 +573,15 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     a.dst_bstride = batch > 1 ? static_cast<long long>(dst_bstride) : 0;
     a.dst_plane = nchw ? static_cast<long long>(OH) * static_cast<long long>(dst_pitch) : 0;
     a.H = H; a.W = W; a.OH = OH; a.OW = OW; a.C = C;
-    a.TR = t.TR; a.TW = t.TW; a.tiles_x = t.tiles_x; a.tiles_y = t.tiles_y;
     a.batch = batch;
+    a.status = p->d_status;
+    if (run_direct(p, fam, a, mode, stream, do_launch, &rc)) return rc;
+
+    TileCfg t;
+    const void *fn = nullptr;
+    rc = get_tile(p, fam, C, batch, &t, &fn);
+    if (rc != RZ_OK) return rc;
+    a.TR = t.TR; a.TW = t.TW; a.tiles_x = t.tiles_x; a.tiles_y = t.tiles_y;
     a.max_rows = t.max_rows; a.slot_bytes = t.slot_bytes; a.stages = t.stages;
     a.ring_chunks = t.ring_chunks; a.chunk_rows = t.chunk_rows; a.chunk_boxes = t.chunk_boxes;
     a.box_bytes = t.box_bytes;
@@ -523,52 +590,9 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     const int strip_bytes = t.TW * (nchw ? 1 : C) * out_es;
     a.tma_out = aligned16(dst) && (dst_pitch % 16 == 0) && (a.dst_bstride % 16 == 0) &&
                 (a.dst_plane % 16 == 0) && (t.tiles_x == 1 || strip_bytes % 16 == 0);
-    // exact 2x, bilinear (the plan's tables are the 2x pattern) or nearest
-    // (floor(2d) = 2d always)
-    const bool nearest2 = fam == rz::FAM_U8 && mode == RZ_NEAREST && W == 2 * OW && H == 2 * OH && !p->opt_generic;
-    if ((t.variant == rz::VAR_DOWN2 || nearest2) && (p->opt_u8_kernel == 0 || p->opt_u8_kernel == 3)) {
-        // the exact 2x path with direct loads when the layout allows its
-        // vector loads and stores (otherwise the kernels below)
-        const uintptr_t lw = C == 3 ? 8 : 16, sw = C == 3 ? 4 : 8;
-        const uintptr_t sa = reinterpret_cast<uintptr_t>(src) | src_pitch | static_cast<uintptr_t>(a.src_bstride);
-        const uintptr_t da = reinterpret_cast<uintptr_t>(dst) | dst_pitch | static_cast<uintptr_t>(a.dst_bstride);
-        const void *dfn = rz::direct_down2_kernel_for(mode, C);
-        if (dfn && sa % lw == 0 && da % sw == 0) {
-            if (!do_launch) return RZ_OK;
-            const int px = rz::down2_px(C);
-            const long long groups = static_cast<long long>(OH) * ((OW + px - 1) / px);
-            const int gx = static_cast<int>((groups + rz::kDirectThreads - 1) / rz::kDirectThreads);
-            CUtensorMap none;
-            std::memset(&none, 0, sizeof(none));
-            const int e = rz::launch_resize(dfn, a, none, gx, 0, p->opt_pdl != 0, stream, rz::kDirectThreads,
-                                            std::min(batch, 65535));
-            if (e != 0) return cuda_fail(static_cast<cudaError_t>(e));
-            return RZ_OK;
-        }
-    }
     const bool fl = (fam == rz::FAM_F32 || fam == rz::FAM_FILT);
     a.xt = fl ? p->d_xf : p->d_xq;
     a.yt = fl ? p->d_yf : p->d_yq;
-    // any other uint8-source resize not streamed: direct loads (unless the
-    // option asks for staged tiles, or for streaming that did not fit)
-    const int opt = p->opt_u8_kernel;
-    const bool direct = t.stream == 0 && ((fam == rz::FAM_U8 && (opt == 0 || opt == 3)) ||
-                                          (fam == rz::FAM_NORM && opt != 1));
-    if (direct) {
-        const void *dfn = rz::direct_kernel_for(fam == rz::FAM_NORM ? rz::DIRECT_NORM : rz::DIRECT_U8, mode, C);
-        if (dfn) {
-            if (!do_launch) return RZ_OK;
-            const long long groups = static_cast<long long>(OH) * ((OW + rz::kDirectRun - 1) / rz::kDirectRun);
-            const int gx = static_cast<int>((groups + rz::kDirectThreads - 1) / rz::kDirectThreads);
-            CUtensorMap none;
-            std::memset(&none, 0, sizeof(none));
-            const int e = rz::launch_resize(dfn, a, none, gx, 0, p->opt_pdl != 0, stream, rz::kDirectThreads,
-                                            std::min(batch, 65535));
-            if (e != 0) return cuda_fail(static_cast<cudaError_t>(e));
-            return RZ_OK;
-        }
-    }
-    a.status = p->d_status;
     CUtensorMap tmap;
     std::memset(&tmap, 0, sizeof(tmap));
     a.tensor_in = 0;

@@ -219,7 +219,127 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
     }
 }
 
+// uint8 bilinear, rows walked per thread: a thread takes four consecutive
+// output columns of TR consecutive output rows (a.TR) and keeps the exact
+// horizontal sums of the two newest source rows it has sampled in registers
+// (two buffers, a new row written over the older one).  Output rows sample
+// non-decreasing source rows, so each source row's sums are formed once per
+// thread however many output rows use it: an upscale by s forms about 1/s
+// rows per output row instead of two.  Same arithmetic and load rules as
+// k_direct.
+template <int C>
+__global__ void __launch_bounds__(kDirectThreads) k_direct_rows(const KArgs a, const __grid_constant__ CUtensorMap)
+{
+    constexpr int RUN = 4;
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int gpr = (a.OW + RUN - 1) / RUN;
+    const int segs = (a.OH + a.TR - 1) / a.TR;
+    const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
+    if (idx >= segs * gpr)
+        return;
+    const int sg = idx / gpr, x0 = (idx - sg * gpr) * RUN;
+    const int dy0 = sg * a.TR, dy1 = min(dy0 + a.TR, a.OH);
+    const int npx = min(RUN, a.OW - x0);
+    const int row_bytes = a.W * C;
+    const int4 xa = __ldg(reinterpret_cast<const int4 *>(a.xt + x0));
+    const int4 xb = __ldg(reinterpret_cast<const int4 *>(a.xt + x0 + 2));
+    const int xs[RUN] = {xa.x, xa.z, xb.x, xb.z};
+    const int xw[RUN] = {xa.y, xa.w, xb.y, xb.w};
+    uint32_t aw[RUN];
+    int o1[RUN];       // right tap's byte offset (clamped at the row end)
+    bool wok[RUN];     // word loads stay inside the row
+    const bool words_in = ((reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
+                            static_cast<uintptr_t>(a.src_bstride)) & 3) == 0;
+#pragma unroll
+    for (int k = 0; k < RUN; k++) {
+        aw[k] = static_cast<uint32_t>(2048 - xw[k]) | (static_cast<uint32_t>(xw[k]) << 16);
+        o1[k] = min(xs[k] + 1, a.W - 1) * C;
+        wok[k] = words_in && xs[k] * C + 12 <= row_bytes;
+    }
+    // sums of one source row at this thread's four columns
+    auto hrow = [&](const uint8_t *row, int (&h)[RUN][C]) {
+#pragma unroll
+        for (int k = 0; k < RUN; k++) {
+            if (wok[k]) {
+                hsum_u8<C>(row, xs[k] * C, aw[k], h[k]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < C; c++)
+                    h[k][c] = (2048 - xw[k]) * __ldg(row + xs[k] * C + c) + xw[k] * __ldg(row + o1[k] + c);
+            }
+        }
+    };
+    for (int b = blockIdx.y; b < a.batch; b += gridDim.y) {
+        const uint8_t *img = a.src + (long long)b * a.src_bstride;
+        uint8_t *op = a.dst + (long long)b * a.dst_bstride + (long long)dy0 * a.dst_pitch + (long long)x0 * C;
+        const bool words = npx == RUN && ((reinterpret_cast<uintptr_t>(op) | static_cast<uintptr_t>(a.dst_pitch)) &
+                                          3) == 0;
+        int h0[RUN][C], h1[RUN][C];   // the two newest sampled rows' sums
+        bool newer1 = false;          // h1 holds the newer row
+        int last = -1;                // the newest sampled row
+        for (int dy = dy0; dy < dy1; dy++) {
+            const int2 ye = __ldg(a.yt + dy);
+            const int r0 = ye.x, r1 = min(ye.x + 1, a.H - 1);
+            if (r1 > last) {
+                if (r0 > last) {
+                    // both taps new: the upper into h0, the lower into h1
+                    hrow(img + (long long)r0 * a.src_pitch, h0);
+                    hrow(img + (long long)r1 * a.src_pitch, h1);
+                    newer1 = true;
+                } else if (newer1) {
+                    hrow(img + (long long)r1 * a.src_pitch, h0);
+                    newer1 = false;
+                } else {
+                    hrow(img + (long long)r1 * a.src_pitch, h1);
+                    newer1 = true;
+                }
+                last = r1;
+            }
+            // the taps are (last - 1, last), or last twice at the bottom edge
+            const int B1 = r0 == r1 ? 2048 : ye.y;
+            const int w0 = newer1 ? 2048 - B1 : B1, w1 = newer1 ? B1 : 2048 - B1;
+            int q[RUN][C];
+#pragma unroll
+            for (int k = 0; k < RUN; k++)
+#pragma unroll
+                for (int c = 0; c < C; c++)
+                    q[k][c] = (w0 * h0[k][c] + w1 * h1[k][c] + (1 << 21)) >> 22;
+            if (words) {
+                uint32_t *o = reinterpret_cast<uint32_t *>(op);
+                if constexpr (C == 1) {
+                    __stcs(o, pack4(q[0][0], q[1][0], q[2][0], q[3][0]));
+                } else if constexpr (C == 3) {
+                    __stcs(o, pack4(q[0][0], q[0][1], q[0][2], q[1][0]));
+                    __stcs(o + 1, pack4(q[1][1], q[1][2], q[2][0], q[2][1]));
+                    __stcs(o + 2, pack4(q[2][2], q[3][0], q[3][1], q[3][2]));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < RUN; k++)
+                        __stcs(o + k, pack4(q[k][0], q[k][1], q[k][2], q[k][3]));
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < RUN; k++)
+                    if (k < npx)
+#pragma unroll
+                        for (int c = 0; c < C; c++)
+                            op[k * C + c] = static_cast<uint8_t>(q[k][c]);
+            }
+            op += a.dst_pitch;
+        }
+    }
+}
+
 }  // namespace
+
+const void *direct_rows_kernel_for(int C)
+{
+    using Fn = void (*)(const KArgs, const CUtensorMap);
+    static const Fn k[3] = {k_direct_rows<1>, k_direct_rows<3>, k_direct_rows<4>};
+    const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
+    return ci < 0 ? nullptr : reinterpret_cast<const void *>(k[ci]);
+}
 
 // Any ratio: op DIRECT_U8 (bilinear or nearest) or DIRECT_NORM (bilinear).
 const void *direct_kernel_for(int op, int mode, int C)

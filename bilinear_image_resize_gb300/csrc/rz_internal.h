@@ -178,5 +178,8 @@ const void *direct_down2_kernel_for(int mode, int C);
 enum DirectOp { DIRECT_U8 = 0, DIRECT_NORM = 1 };
 constexpr int kDirectRun = 4;   // output pixels per thread
 const void *direct_kernel_for(int op, int mode, int C);
+// uint8 bilinear with each thread walking a.TR output rows (vertical
+// upscales); nullptr if none.
+const void *direct_rows_kernel_for(int C);
 
 }  // namespace rz

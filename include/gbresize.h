@@ -261,17 +261,20 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  *                       streaming kernel (the 3x3 filter family; uint8
  *                       bilinear upscales) streams its strip;
  *   RZ_OPT_U8_KERNEL    value 0 (automatic), 1, 2 or 3: which kernel runs
- *                       uint8 bilinear resizes.  0: the exact 2x case with
- *                       direct loads when the layout allows (source base,
- *                       pitch and batch stride multiples of 16 bytes, 8 for
- *                       three channels; output ones of 8, 4 for three
- *                       channels), vertical upscales streamed (each source
- *                       row's horizontal sums computed once, kept in
- *                       registers), other cases in staged tiles; 1: staged
- *                       tiles always; 2: streamed whenever a strip's source
- *                       span fits (not the exact 2x case); 3: direct loads
- *                       for the exact 2x case where the layout allows, staged
- *                       tiles otherwise.  Bit-exact whichever runs.
+ *                       uint8-source resizes (plain, and the normalise
+ *                       epilogue).  0: vertical bilinear upscales streamed
+ *                       (each source row's horizontal sums computed once,
+ *                       kept in registers), everything else with direct
+ *                       loads (each thread reads its own taps; the exact 2x
+ *                       case with vector loads when the source base, pitch
+ *                       and batch stride are multiples of 16 bytes, 8 for
+ *                       three channels, and the output ones of 8, 4 for three
+ *                       channels); 1: staged tiles always; 2: streamed
+ *                       whenever a strip's source span fits (not the exact 2x
+ *                       case or the normalise epilogue); 3: direct loads
+ *                       always (upscales with each thread walking output
+ *                       rows, tile_rows of resize_plan_set_tile per thread).
+ *                       Bit-exact whichever runs.
  * Returns RZ_ERR_ARG for an unknown option or value.
  */
 #define RZ_OPT_STAGES 1

@@ -231,6 +231,21 @@ def test_u8_stream_unit_shapes(rz, tile):
         np.testing.assert_array_equal(got, want, err_msg=str((geom, tile)))
 
 
+@pytest.mark.parametrize("rows", [1, 2, 3, 8, 31, 2160])
+def test_u8_direct_rows_per_thread(rz, rows):
+    # the row-walking direct kernel on upscales: any rows per thread (the
+    # tile override's row count), ragged segments and odd layouts
+    for geom in _STREAM_GEOMS[:4]:
+        img, want = stream_case(rz, geom)
+        got = gpu_u8(rz, img, geom[3], geom[4], rz.RZ_LINEAR, tile=(rows, 64), opts=[(rz.RZ_OPT_U8_KERNEL, 3)])
+        np.testing.assert_array_equal(got, want, err_msg=str((geom, rows)))
+    img, want = stream_case(rz, _STREAM_GEOMS[1])
+    H, W, C = img.shape
+    got = gpu_u8(rz, img, 611, 797, rz.RZ_LINEAR, src_pitch=W * C + 3, src_off=1, dst_pad=5, dst_off=2,
+                 tile=(rows, 64), opts=[(rz.RZ_OPT_U8_KERNEL, 3)])
+    np.testing.assert_array_equal(got, want)
+
+
 def test_u8_stream_and_staged_tiles_agree(rz):
     # both uint8 kernels on the same upscale: identical bytes
     img, want = stream_case(rz, _STREAM_GEOMS[1])
