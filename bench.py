@@ -360,6 +360,10 @@ def gpu_arm(args, rank, local_rank, world):
     if kind == "u8":
         e2e = e2e_u8(rz, plan, frames[0], H, W, OH, OW, C, dev, n=max(10, min(args.steps, 200)))
 
+    # the achievable ceiling for this byte count: torch's device copy of
+    # (read + write) / 2 bytes per step, same ring rotation, graph replays
+    ceiling = copy_ceiling(step_bytes, ring, stream, dev)
+
     # several frames per launch (resize_u8_batch), u8 workloads
     batched = None
     if kind == "u8" and args.batch_frames > 0:
@@ -375,10 +379,38 @@ def gpu_arm(args, rank, local_rank, world):
         "value": value, "ms": ms_max, "launch_ms": launch_ms, "eager_ms_per_step": eager_ms,
         "achieved_gbs": achieved, "peak_gbs": peak, "peak_src": src, "step_bytes": step_bytes,
         "read_bytes": rd, "write_bytes": wr, "ring": ring, "graph_steps": G, "clocks": clocks, "e2e": e2e,
-        "desc": desc, "px": px, "batched": batched,
+        "desc": desc, "px": px, "batched": batched, "copy_ceiling": ceiling,
     }
     plan.destroy()
     return res
+
+
+def copy_ceiling(step_bytes, ring, stream, dev, reps=8):
+    """GB/s of a plain device copy moving the step's byte count (half read,
+    half written), over a ring of buffers, graph-replayed and event-timed:
+    what one launch of this size can reach on this GPU."""
+    import torch
+    n = max(16, step_bytes // 2 // 16 * 16)
+    srcs = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(ring)]
+    dsts = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(ring)]
+    g = torch.cuda.CUDAGraph()
+    k = max(ring, 48 // ring * ring)
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(k):
+            dsts[i % ring].copy_(srcs[i % ring])
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * k)
+    return {"gbs": 2 * n / (us * 1e-6) / 1e9, "us_per_copy": us, "bytes_moved": 2 * n, "what": "torch device copy"}
 
 
 def batched_u8(rz, plan, frames, H, W, OH, OW, C, nf, stream, dev, frame_bytes, launches=48):
@@ -688,6 +720,7 @@ def main():
             "eager_ms_per_step": r["eager_ms_per_step"],
             "clocks": r["clocks"],
             "batched": r["batched"],
+            "copy_ceiling": dict(r["copy_ceiling"], frac=r["achieved_gbs"] / r["copy_ceiling"]["gbs"]),
         }
         print(json.dumps(line), flush=True)
     if world > 1:

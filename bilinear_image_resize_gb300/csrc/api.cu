@@ -382,14 +382,21 @@ int get_stream_tile(rz_plan_s *p, int op, int C, int batch, TileCfg *out, const 
     return RZ_OK;
 }
 
-// The uint8 bilinear resize takes the streaming form for vertical upscales,
-// where each source row feeds several output rows (measured faster there than
-// the direct kernels), or when the option asks for it; not for the exact 2x
-// case.
+// The uint8 bilinear resize takes the streaming form for vertical upscales
+// of at least kStreamMinPixels outputs, where each source row feeds several
+// output rows (measured faster there than the direct kernels), or when the
+// option asks for it; not for the exact 2x case.
+constexpr long long kStreamMinPixels = 1 << 18;   // smaller outputs: the stream's set-up dominates
+
+bool auto_u8_stream(const rz_plan_s &p)
+{
+    return p.OH > p.H && static_cast<long long>(p.OH) * p.OW >= kStreamMinPixels;
+}
+
 bool want_u8_stream(const rz_plan_s &p, bool down2)
 {
     if (p.mode != RZ_LINEAR || down2) return false;
-    return p.opt_u8_kernel == 2 || (p.opt_u8_kernel == 0 && p.OH > p.H);
+    return p.opt_u8_kernel == 2 || (p.opt_u8_kernel == 0 && auto_u8_stream(p));
 }
 
 // Tile and grid for this call: the override if one is set, else the cached
@@ -479,7 +486,7 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
 {
     const int opt = p->opt_u8_kernel;
     if (!((fam == rz::FAM_U8 && (opt == 0 || opt == 3)) || (fam == rz::FAM_NORM && opt != 1))) return false;
-    if (fam == rz::FAM_U8 && opt == 0 && mode == RZ_LINEAR && a.OH > a.H && !is_down2(*p)) return false;
+    if (fam == rz::FAM_U8 && opt == 0 && mode == RZ_LINEAR && auto_u8_stream(*p) && !is_down2(*p)) return false;
     const int C = a.C, batch = a.batch;
     a.xt = p->d_xq;
     a.yt = p->d_yq;
@@ -499,7 +506,7 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
         }
     }
     const long long gpr = (a.OW + rz::kDirectRun - 1) / rz::kDirectRun;
-    if (!fn && fam == rz::FAM_U8 && mode == RZ_LINEAR && a.OH > a.H) {
+    if (!fn && fam == rz::FAM_U8 && mode == RZ_LINEAR && a.OH > a.H && opt == 3) {
         // about 2048 threads per SM, each walking R output rows
         fn = rz::direct_rows_kernel_for(C);
         int sms = 0;

@@ -262,9 +262,10 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  *                       bilinear upscales) streams its strip;
  *   RZ_OPT_U8_KERNEL    value 0 (automatic), 1, 2 or 3: which kernel runs
  *                       uint8-source resizes (plain, and the normalise
- *                       epilogue).  0: vertical bilinear upscales streamed
- *                       (each source row's horizontal sums computed once,
- *                       kept in registers), everything else with direct
+ *                       epilogue).  0: vertical bilinear upscales to at
+ *                       least 2^18 output pixels streamed (each source row's
+ *                       horizontal sums computed once, kept in registers),
+ *                       everything else with direct
  *                       loads (each thread reads its own taps; the exact 2x
  *                       case with vector loads when the source base, pitch
  *                       and batch stride are multiples of 16 bytes, 8 for
