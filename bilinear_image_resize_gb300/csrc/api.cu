@@ -523,8 +523,13 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
         a.TR = std::min(R, a.OH);
         groups = gpr * ((a.OH + a.TR - 1) / a.TR);
     }
+    if (!fn && fam == rz::FAM_NORM) {
+        // a warp per 128 output pixels of a row
+        fn = rz::direct_kernel_for(rz::DIRECT_NORM, mode, C);
+        groups = static_cast<long long>(a.OH) * ((a.OW + 32 * rz::kDirectRun - 1) / (32 * rz::kDirectRun)) * 32;
+    }
     if (!fn) {
-        fn = rz::direct_kernel_for(fam == rz::FAM_NORM ? rz::DIRECT_NORM : rz::DIRECT_U8, mode, C);
+        fn = rz::direct_kernel_for(rz::DIRECT_U8, mode, C);
         groups = gpr * a.OH;
     }
     if (!fn) return false;

@@ -105,16 +105,15 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_direct(const KArgs a, 
     }
 }
 
-// Any ratio, uint8 source: bilinear (exact 11-bit fixed point, the tiled
-// kernel's arithmetic: hsum_u8 per row, then (B0 hT + B1 hB + 2^21) >> 22)
-// or nearest, written as uint8 HWC (OP = DIRECT_U8) or through the normalise
-// epilogue as float32 planes (OP = DIRECT_NORM: y = q * scale[c] + shift[c],
-// CUDA interpolation page §4.2).  A thread takes four consecutive output
-// pixels of one row: their four table entries in two 16-byte loads, their
-// taps from the two source rows through L1 (neighbouring threads share
-// them), 32-bit words where the row layout allows and the taps lie at least
-// 12 bytes before the row's end (so no load passes the row), bytes otherwise.
-template <int OP, int C, int LINEAR>
+// Any ratio, uint8: bilinear (exact 11-bit fixed point, the tiled kernel's
+// arithmetic: hsum_u8 per row, then (B0 hT + B1 hB + 2^21) >> 22) or
+// nearest.  A thread takes four consecutive output pixels of one row: their
+// four table entries in two 16-byte loads, their taps from the two source
+// rows through L1 (neighbouring threads share them), 32-bit words where the
+// row layout allows and the taps lie at least 12 bytes before the row's end
+// (so no load passes the row), bytes otherwise; the four pixels leave as
+// 32-bit words when the output layout allows.
+template <int C, int LINEAR>
 __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const __grid_constant__ CUtensorMap)
 {
     constexpr int RUN = 4;
@@ -173,48 +172,99 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
                     q[k][c] = (B0 * hT[c] + B1 * hB[c] + (1 << 21)) >> 22;
             }
         }
-        if constexpr (OP == DIRECT_U8) {
-            uint8_t *op = a.dst + (long long)b * a.dst_bstride + (long long)dy * a.dst_pitch + (long long)x0 * C;
-            const bool words = npx == RUN && ((reinterpret_cast<uintptr_t>(op)) & 3) == 0;
-            if (words) {
-                uint32_t *o = reinterpret_cast<uint32_t *>(op);
-                if constexpr (C == 1) {
-                    __stcs(o, pack4(q[0][0], q[1][0], q[2][0], q[3][0]));
-                } else if constexpr (C == 3) {
-                    __stcs(o, pack4(q[0][0], q[0][1], q[0][2], q[1][0]));
-                    __stcs(o + 1, pack4(q[1][1], q[1][2], q[2][0], q[2][1]));
-                    __stcs(o + 2, pack4(q[2][2], q[3][0], q[3][1], q[3][2]));
-                } else {
-#pragma unroll
-                    for (int k = 0; k < RUN; k++)
-                        __stcs(o + k, pack4(q[k][0], q[k][1], q[k][2], q[k][3]));
-                }
+        uint8_t *op = a.dst + (long long)b * a.dst_bstride + (long long)dy * a.dst_pitch + (long long)x0 * C;
+        const bool words = npx == RUN && ((reinterpret_cast<uintptr_t>(op)) & 3) == 0;
+        if (words) {
+            uint32_t *o = reinterpret_cast<uint32_t *>(op);
+            if constexpr (C == 1) {
+                __stcs(o, pack4(q[0][0], q[1][0], q[2][0], q[3][0]));
+            } else if constexpr (C == 3) {
+                __stcs(o, pack4(q[0][0], q[0][1], q[0][2], q[1][0]));
+                __stcs(o + 1, pack4(q[1][1], q[1][2], q[2][0], q[2][1]));
+                __stcs(o + 2, pack4(q[2][2], q[3][0], q[3][1], q[3][2]));
             } else {
 #pragma unroll
                 for (int k = 0; k < RUN; k++)
-                    if (k < npx)
-#pragma unroll
-                        for (int c = 0; c < C; c++)
-                            op[k * C + c] = static_cast<uint8_t>(q[k][c]);
+                    __stcs(o + k, pack4(q[k][0], q[k][1], q[k][2], q[k][3]));
             }
         } else {
 #pragma unroll
-            for (int c = 0; c < C; c++) {
-                float *pl = reinterpret_cast<float *>(a.dst + (long long)b * a.dst_bstride + (long long)c * a.dst_plane +
-                                                      (long long)dy * a.dst_pitch) + x0;
-                float f[RUN];
+            for (int k = 0; k < RUN; k++)
+                if (k < npx)
 #pragma unroll
-                for (int k = 0; k < RUN; k++)
-                    f[k] = fmaf(static_cast<float>(q[k][c]), a.scale[c], a.shift[c]);
-                if (npx == RUN && (reinterpret_cast<uintptr_t>(pl) & 15) == 0) {
-                    __stcs(reinterpret_cast<float4 *>(pl), make_float4(f[0], f[1], f[2], f[3]));
-                } else {
+                    for (int c = 0; c < C; c++)
+                        op[k * C + c] = static_cast<uint8_t>(q[k][c]);
+        }
+    }
+}
+
+// Bilinear + normalise, uint8 source, float32 planes out (y = q * scale[c] +
+// shift[c] on the exact uint8 result q, CUDA interpolation page §4.2).  A
+// warp takes 128 consecutive output pixels of one row, lane l the pixels
+// l, l + 32, l + 64, l + 96: one load instruction then reads the taps of 32
+// neighbouring pixels (a short stretch of the source row, few sectors even
+// for strong downscales), and each plane store writes 32 consecutive floats.
+// Taps and load rules as in k_direct.
+template <int C>
+__global__ void __launch_bounds__(kDirectThreads) k_direct_norm(const KArgs a, const __grid_constant__ CUtensorMap)
+{
+    constexpr int RUN = 4;
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int wpr = (a.OW + 32 * RUN - 1) / (32 * RUN);   // warps per output row
+    const int gw = (blockIdx.x * kDirectThreads + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (gw >= a.OH * wpr)
+        return;
+    const int dy = gw / wpr, xb = (gw - dy * wpr) * 32 * RUN;
+    const int row_bytes = a.W * C;
+    int xs[RUN], xw[RUN];
+    bool ok[RUN];
 #pragma unroll
-                    for (int k = 0; k < RUN; k++)
-                        if (k < npx)
-                            __stcs(pl + k, f[k]);
+    for (int k = 0; k < RUN; k++) {
+        const int x = xb + lane + 32 * k;
+        ok[k] = x < a.OW;
+        const int2 e = __ldg(a.xt + min(x, a.OW - 1));
+        xs[k] = e.x;
+        xw[k] = e.y;
+    }
+    const int2 ye = __ldg(a.yt + dy);
+    const int r0 = ye.x, r1 = min(ye.x + 1, a.H - 1);
+    const int B1 = ye.y, B0 = 2048 - B1;
+    const bool words_in = ((reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
+                            static_cast<uintptr_t>(a.src_bstride)) & 3) == 0;
+    for (int b = blockIdx.y; b < a.batch; b += gridDim.y) {
+        const uint8_t *img = a.src + (long long)b * a.src_bstride;
+        const uint8_t *top = img + (long long)r0 * a.src_pitch;
+        const uint8_t *bot = img + (long long)r1 * a.src_pitch;
+        int q[RUN][C];
+#pragma unroll
+        for (int k = 0; k < RUN; k++) {
+            const int o0 = xs[k] * C;
+            int hT[C], hB[C];
+            if (words_in && o0 + 12 <= row_bytes) {
+                const uint32_t aw = static_cast<uint32_t>(2048 - xw[k]) | (static_cast<uint32_t>(xw[k]) << 16);
+                hsum_u8<C>(top, o0, aw, hT);
+                hsum_u8<C>(bot, o0, aw, hB);
+            } else {
+                const int o1 = min(xs[k] + 1, a.W - 1) * C;
+#pragma unroll
+                for (int c = 0; c < C; c++) {
+                    hT[c] = (2048 - xw[k]) * __ldg(top + o0 + c) + xw[k] * __ldg(top + o1 + c);
+                    hB[c] = (2048 - xw[k]) * __ldg(bot + o0 + c) + xw[k] * __ldg(bot + o1 + c);
                 }
             }
+#pragma unroll
+            for (int c = 0; c < C; c++)
+                q[k][c] = (B0 * hT[c] + B1 * hB[c] + (1 << 21)) >> 22;
+        }
+#pragma unroll
+        for (int c = 0; c < C; c++) {
+            float *pl = reinterpret_cast<float *>(a.dst + (long long)b * a.dst_bstride + (long long)c * a.dst_plane +
+                                                  (long long)dy * a.dst_pitch) + xb + lane;
+#pragma unroll
+            for (int k = 0; k < RUN; k++)
+                if (ok[k])
+                    __stcs(pl + 32 * k, fmaf(static_cast<float>(q[k][c]), a.scale[c], a.shift[c]));
         }
     }
 }
@@ -345,10 +395,9 @@ const void *direct_rows_kernel_for(int C)
 const void *direct_kernel_for(int op, int mode, int C)
 {
     using Fn = void (*)(const KArgs, const CUtensorMap);
-    static const Fn u8[2][3] = {{k_direct<DIRECT_U8, 1, 0>, k_direct<DIRECT_U8, 3, 0>, k_direct<DIRECT_U8, 4, 0>},
-                                {k_direct<DIRECT_U8, 1, 1>, k_direct<DIRECT_U8, 3, 1>, k_direct<DIRECT_U8, 4, 1>}};
-    static const Fn norm[3] = {k_direct<DIRECT_NORM, 1, 1>, k_direct<DIRECT_NORM, 3, 1>,
-                               k_direct<DIRECT_NORM, 4, 1>};
+    static const Fn u8[2][3] = {{k_direct<1, 0>, k_direct<3, 0>, k_direct<4, 0>},
+                                {k_direct<1, 1>, k_direct<3, 1>, k_direct<4, 1>}};
+    static const Fn norm[3] = {k_direct_norm<1>, k_direct_norm<3>, k_direct_norm<4>};
     const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
     if (ci < 0)
         return nullptr;
