@@ -524,9 +524,9 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
         groups = gpr * ((a.OH + a.TR - 1) / a.TR);
     }
     if (!fn && fam == rz::FAM_NORM) {
-        // a warp per 128 output pixels of a row
+        // a warp per 32 kNormRun output pixels of a row
         fn = rz::direct_kernel_for(rz::DIRECT_NORM, mode, C);
-        groups = static_cast<long long>(a.OH) * ((a.OW + 32 * rz::kDirectRun - 1) / (32 * rz::kDirectRun)) * 32;
+        groups = static_cast<long long>(a.OH) * ((a.OW + 32 * rz::kNormRun - 1) / (32 * rz::kNormRun)) * 32;
     }
     if (!fn) {
         fn = rz::direct_kernel_for(rz::DIRECT_U8, mode, C);

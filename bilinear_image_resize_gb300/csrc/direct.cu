@@ -200,15 +200,15 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
 
 // Bilinear + normalise, uint8 source, float32 planes out (y = q * scale[c] +
 // shift[c] on the exact uint8 result q, CUDA interpolation page §4.2).  A
-// warp takes 128 consecutive output pixels of one row, lane l the pixels
-// l, l + 32, l + 64, l + 96: one load instruction then reads the taps of 32
+// warp takes 32 kNormRun consecutive output pixels of one row, lane l the
+// pixels l, l + 32, ...: one load instruction then reads the taps of 32
 // neighbouring pixels (a short stretch of the source row, few sectors even
 // for strong downscales), and each plane store writes 32 consecutive floats.
 // Taps and load rules as in k_direct.
 template <int C>
 __global__ void __launch_bounds__(kDirectThreads) k_direct_norm(const KArgs a, const __grid_constant__ CUtensorMap)
 {
-    constexpr int RUN = 4;
+    constexpr int RUN = kNormRun;
     grid_launch_dependents();
     grid_dependency_wait();
     const int wpr = (a.OW + 32 * RUN - 1) / (32 * RUN);   // warps per output row

@@ -177,6 +177,7 @@ const void *direct_down2_kernel_for(int mode, int C);
 // epilogue, float32 planes) for (mode, C); nullptr if none.
 enum DirectOp { DIRECT_U8 = 0, DIRECT_NORM = 1 };
 constexpr int kDirectRun = 4;   // output pixels per thread
+constexpr int kNormRun = 1;     // normalise: output pixels per lane (interleaved by 32)
 const void *direct_kernel_for(int op, int mode, int C);
 // uint8 bilinear with each thread walking a.TR output rows (vertical
 // upscales); nullptr if none.
