@@ -477,7 +477,8 @@ bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15)
 
 // Direct-load kernels (direct.cu) for uint8-source resizes, unless the
 // option asks for staged tiles (1) or streaming (2), and except automatic
-// bilinear vertical upscales (streamed).  Exact 2x (bilinear tables of the
+// bilinear vertical upscales other than exact 2x (streamed).  Exact 2x
+// upscales with the 1-3 weights; exact 2x downscales (bilinear tables of the
 // 2x pattern, or nearest at W = 2 OW, H = 2 OH) with vector loads where the
 // layout allows; vertical bilinear upscales (option 3) with each thread
 // walking rows; everything else one thread per four output pixels.  Returns
@@ -486,8 +487,26 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
 {
     const int opt = p->opt_u8_kernel;
     if (!((fam == rz::FAM_U8 && (opt == 0 || opt == 3)) || (fam == rz::FAM_NORM && opt != 1))) return false;
-    if (fam == rz::FAM_U8 && opt == 0 && mode == RZ_LINEAR && auto_u8_stream(*p) && !is_down2(*p)) return false;
     const int C = a.C, batch = a.batch;
+    if (fam == rz::FAM_U8 && mode == RZ_LINEAR && !p->opt_generic && a.OW == 2 * a.W && a.OH == 2 * a.H) {
+        // exact 2x upscale: the 1-3 weights (direct.cu k_up2_direct), any layout
+        a.xt = p->d_xq;
+        a.yt = p->d_yq;
+        const void *ufn = rz::direct_up2_kernel_for(C);
+        if (ufn) {
+            *rc = RZ_OK;
+            if (!do_launch) return true;
+            const long long groups = static_cast<long long>(a.H) * ((a.W + rz::kUp2Cols - 1) / rz::kUp2Cols);
+            const int gx = static_cast<int>((groups + rz::kDirectThreads - 1) / rz::kDirectThreads);
+            CUtensorMap none;
+            std::memset(&none, 0, sizeof(none));
+            const int e = rz::launch_resize(ufn, a, none, gx, 0, p->opt_pdl != 0, stream, rz::kDirectThreads,
+                                            std::min(batch, 65535));
+            if (e != 0) *rc = cuda_fail(static_cast<cudaError_t>(e));
+            return true;
+        }
+    }
+    if (fam == rz::FAM_U8 && opt == 0 && mode == RZ_LINEAR && auto_u8_stream(*p) && !is_down2(*p)) return false;
     a.xt = p->d_xq;
     a.yt = p->d_yq;
     const void *fn = nullptr;

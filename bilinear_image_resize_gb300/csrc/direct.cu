@@ -198,6 +198,109 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
     }
 }
 
+// Exact 2x bilinear upscale of uint8 (OW = 2 W, OH = 2 H).  Output column
+// X = 2s samples x = s - 1/4 (taps s - 1, s with weights 1/4, 3/4) and
+// X = 2s + 1 samples x = s + 1/4 (taps s, s + 1 with 3/4, 1/4); the same for
+// rows.  The 11-bit weights are then 512 and 1536, so the exact sum
+// (B0 (A0 t0 + A1 t1) + B1 (...) + 2^21) >> 22 equals (V + 8) >> 4 with
+// V = sum of b a t over a, b in {1, 3} (CUDA interpolation page §2.2, §6.2).
+// At the borders the plan folds the outside tap onto the edge pixel with
+// all the weight, which is the same as repeating the edge pixel (§6.1).
+// A thread takes P = 4 source columns s0 .. s0 + 3 of source row r and forms
+// output rows 2r and 2r + 1, columns 2 s0 .. 2 s0 + 7: it reads source rows
+// r - 1, r, r + 1 over columns s0 - 1 .. s0 + 4 (clamped), sums each column
+// vertically (1 and 3 for row 2r, 3 and 1 for row 2r + 1) and then
+// horizontally.  Interior groups read 32-bit words (byte offsets fixed at
+// compile time) when the source layout is 4-byte aligned; edge groups read
+// bytes with clamped columns.
+template <int C>
+__global__ void __launch_bounds__(kDirectThreads) k_up2_direct(const KArgs a, const __grid_constant__ CUtensorMap)
+{
+    constexpr int P = 4;                   // source columns per thread
+    constexpr int NB = (P + 2) * C;        // source bytes per row used: columns s0 - 1 .. s0 + P
+    constexpr int LEAD = (4 - C % 4) % 4;  // (s0 - 1) C - its word boundary, s0 a multiple of 4
+    constexpr int NW = (LEAD + NB + 3) / 4;
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int gpr = (a.W + P - 1) / P;
+    const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
+    if (idx >= a.H * gpr)
+        return;
+    const int r = idx / gpr, s0 = (idx - r * gpr) * P;
+    const int np = min(P, a.W - s0);
+    const int rows[3] = {max(r - 1, 0), r, min(r + 1, a.H - 1)};
+    const bool words_in = ((reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
+                            static_cast<uintptr_t>(a.src_bstride)) & 3) == 0;
+    // interior: the words read, [(s0 - 1) C - LEAD, + 4 NW), lie inside the row
+    const bool inner = words_in && s0 >= 1 && (s0 - 1) * C - LEAD + 4 * NW <= a.W * C;
+    for (int b = blockIdx.y; b < a.batch; b += gridDim.y) {
+        const uint8_t *img = a.src + (long long)b * a.src_bstride;
+        int v[2][NB];   // vertical sums for output rows 2r and 2r + 1, per source byte
+        int t[3][NB];
+#pragma unroll
+        for (int k = 0; k < 3; k++) {
+            const uint8_t *row = img + (long long)rows[k] * a.src_pitch;
+            if (inner) {
+                const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (s0 - 1) * C - LEAD);
+                uint32_t wd[NW];
+#pragma unroll
+                for (int i = 0; i < NW; i++)
+                    wd[i] = __ldg(w + i);
+#pragma unroll
+                for (int i = 0; i < NB; i++)
+                    t[k][i] = (wd[(LEAD + i) / 4] >> (8 * ((LEAD + i) % 4))) & 0xff;
+            } else {
+#pragma unroll
+                for (int i = 0; i < P + 2; i++) {
+                    const int col = clampi(s0 - 1 + i, 0, a.W - 1);
+#pragma unroll
+                    for (int c = 0; c < C; c++)
+                        t[k][i * C + c] = __ldg(row + col * C + c);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NB; i++) {
+            v[0][i] = t[0][i] + 3 * t[1][i];
+            v[1][i] = 3 * t[1][i] + t[2][i];
+        }
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            int q[2 * P][C];
+#pragma unroll
+            for (int sx = 0; sx < P; sx++)
+#pragma unroll
+                for (int c = 0; c < C; c++) {
+                    const int l = v[j][sx * C + c], m = v[j][(sx + 1) * C + c], rr = v[j][(sx + 2) * C + c];
+                    q[2 * sx][c] = (l + 3 * m + 8) >> 4;
+                    q[2 * sx + 1][c] = (3 * m + rr + 8) >> 4;
+                }
+            uint8_t *op = a.dst + (long long)b * a.dst_bstride + (long long)(2 * r + j) * a.dst_pitch +
+                          (long long)(2 * s0) * C;
+            const bool words = np == P && (reinterpret_cast<uintptr_t>(op) & 3) == 0;
+            if (words) {
+                // 2 P C bytes = 8, 24 or 32: whole 32-bit words
+                uint32_t ow[2 * P * C / 4];
+#pragma unroll
+                for (int i = 0; i < 2 * P * C / 4; i++)
+                    ow[i] = pack4(q[(4 * i) / C][(4 * i) % C], q[(4 * i + 1) / C][(4 * i + 1) % C],
+                                  q[(4 * i + 2) / C][(4 * i + 2) % C], q[(4 * i + 3) / C][(4 * i + 3) % C]);
+                uint32_t *o = reinterpret_cast<uint32_t *>(op);
+#pragma unroll
+                for (int i = 0; i < 2 * P * C / 4; i++)
+                    __stcs(o + i, ow[i]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 2 * P; k++)
+                    if (k < 2 * np)
+#pragma unroll
+                        for (int c = 0; c < C; c++)
+                            op[k * C + c] = static_cast<uint8_t>(q[k][c]);
+            }
+        }
+    }
+}
+
 // Bilinear + normalise, uint8 source, float32 planes out (y = q * scale[c] +
 // shift[c] on the exact uint8 result q, CUDA interpolation page §4.2).  A
 // warp takes 32 kNormRun consecutive output pixels of one row, lane l the
@@ -382,6 +485,14 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_rows(const KArgs a, c
 }
 
 }  // namespace
+
+const void *direct_up2_kernel_for(int C)
+{
+    using Fn = void (*)(const KArgs, const CUtensorMap);
+    static const Fn k[3] = {k_up2_direct<1>, k_up2_direct<3>, k_up2_direct<4>};
+    const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
+    return ci < 0 ? nullptr : reinterpret_cast<const void *>(k[ci]);
+}
 
 const void *direct_rows_kernel_for(int C)
 {

@@ -179,6 +179,10 @@ enum DirectOp { DIRECT_U8 = 0, DIRECT_NORM = 1 };
 constexpr int kDirectRun = 4;   // output pixels per thread
 constexpr int kNormRun = 1;     // normalise: output pixels per lane (interleaved by 32)
 const void *direct_kernel_for(int op, int mode, int C);
+// The exact 2x uint8 bilinear upscale (thread per 4 source columns of a
+// source row: 8 x 2 outputs); nullptr if none.
+constexpr int kUp2Cols = 4;
+const void *direct_up2_kernel_for(int C);
 // uint8 bilinear with each thread walking a.TR output rows (vertical
 // upscales); nullptr if none.
 const void *direct_rows_kernel_for(int C);

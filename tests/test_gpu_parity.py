@@ -607,6 +607,37 @@ def test_exact_2x_direct_loads(rz, C):
                 np.testing.assert_array_equal(got, want, err_msg=str((mode, H, W, pad, off)))
 
 
+@pytest.mark.parametrize("C", [1, 3, 4])
+def test_exact_2x_upscale(rz, C):
+    # the 1-3 weight kernel: tiny and odd sizes (edge groups take the byte
+    # path), unaligned layouts, and agreement with the streaming and staged
+    # kernels
+    for (H, W) in [(1, 1), (1, 5), (3, 2), (2, 9), (7, 13), (16, 16), (33, 70), (540, 961), (1080, 1920)]:
+        img = synth.random_u8((H, W, C), seed=H * 11 + W + C)
+        want = oracle.linear_u8(img, 2 * H, 2 * W)
+        for pad, off in [(0, 0), (16, 0), (3, 1), (5, 2)]:
+            got = gpu_u8(rz, img, 2 * H, 2 * W, rz.RZ_LINEAR, src_pitch=W * C + pad, src_off=off, dst_pad=pad,
+                         dst_off=off)
+            np.testing.assert_array_equal(got, want, err_msg=str((H, W, pad, off)))
+    img = synth.random_u8((97, 130, C), seed=5)
+    a = gpu_u8(rz, img, 194, 260, rz.RZ_LINEAR)
+    for k in (1, 2):
+        np.testing.assert_array_equal(a, gpu_u8(rz, img, 194, 260, rz.RZ_LINEAR, opts=[(rz.RZ_OPT_U8_KERNEL, k)]))
+
+
+def test_exact_2x_upscale_batch(rz):
+    N = 3
+    frames = np.stack([synth.random_u8((135, 240, 3), seed=70 + n) for n in range(N)])
+    src = torch.from_numpy(frames).cuda()
+    dst = torch.empty((N, 270, 480, 3), dtype=torch.uint8, device="cuda")
+    with rz.resize_plan_create(135, 240, 270, 480, rz.RZ_LINEAR) as plan:
+        rz.resize_u8_batch(plan, src, dst)
+        torch.cuda.synchronize()
+    got = dst.cpu().numpy()
+    for n in range(N):
+        np.testing.assert_array_equal(got[n], oracle.linear_u8(frames[n], 270, 480))
+
+
 def test_exact_2x_direct_batch_and_pdl_chain(rz):
     # a batch through the direct kernel, then a second resize of its output
     # queued right after it (the dependent launch must wait for the first)
