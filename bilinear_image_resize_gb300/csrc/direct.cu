@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
 // compile time) when the source layout is 4-byte aligned; edge groups read
 // bytes with clamped columns.
 template <int C>
-__global__ void __launch_bounds__(kDirectThreads) k_up2_direct(const KArgs a, const __grid_constant__ CUtensorMap)
+__global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a, const __grid_constant__ CUtensorMap)
 {
     constexpr int P = 4;                   // source columns per thread
     constexpr int NB = (P + 2) * C;        // source bytes per row used: columns s0 - 1 .. s0 + P
