@@ -1,0 +1,57 @@
+"""The closed forms the exact-ratio kernels compute, checked against the oracle.
+
+At an exact 2x downscale every tap weight is 1024, so the fixed-point sum is
+(t0 + t1 + b0 + b1 + 2) >> 2.  At an exact 2x upscale the weights are 512 and
+1536, so the sum is (sum of b * a * t + 8) >> 4 with a, b in {1, 3} (the
+9-3-3-1 filter), the outside tap at a border folded onto the edge pixel by
+the plan being the same as repeating the edge pixel.  These identities are
+what direct.cu relies on; here they are computed in numpy from their own
+definition and compared with the oracle's general formula on random images.
+"""
+import numpy as np
+import pytest
+
+import oracle
+
+
+def down2(img):
+    t = img.astype(np.int64)
+    return ((t[0::2, 0::2] + t[0::2, 1::2] + t[1::2, 0::2] + t[1::2, 1::2] + 2) >> 2).astype(np.uint8)
+
+
+def up2(img):
+    t = img.astype(np.int64)
+    H, W = t.shape[:2]
+    p = np.pad(t, ((1, 1), (1, 1), (0, 0)), mode="edge")   # edge repetition
+    out = np.zeros((2 * H, 2 * W, t.shape[2]), np.int64)
+    for j, (wy0, wy1, dy) in enumerate([(1, 3, 0), (3, 1, 1)]):   # rows (r-1, r) or (r, r+1)
+        for i, (wx0, wx1, dx) in enumerate([(1, 3, 0), (3, 1, 1)]):
+            v = (wy0 * wx0 * p[dy:dy + H, dx:dx + W] + wy0 * wx1 * p[dy:dy + H, dx + 1:dx + 1 + W] +
+                 wy1 * wx0 * p[dy + 1:dy + 1 + H, dx:dx + W] + wy1 * wx1 * p[dy + 1:dy + 1 + H, dx + 1:dx + 1 + W])
+            out[j::2, i::2] = (v + 8) >> 4
+    return out.astype(np.uint8)
+
+
+@pytest.mark.parametrize("C", [1, 3, 4])
+def test_exact_2x_downscale_is_the_four_tap_mean(C):
+    rng = np.random.default_rng(31 + C)
+    for (H, W) in [(2, 2), (2, 18), (6, 34), (30, 46), (64, 62)]:
+        img = rng.integers(0, 256, size=(H, W, C), dtype=np.uint8)
+        np.testing.assert_array_equal(down2(img), oracle.linear_u8(img, H // 2, W // 2))
+
+
+@pytest.mark.parametrize("C", [1, 3, 4])
+def test_exact_2x_upscale_is_the_9331_filter(C):
+    rng = np.random.default_rng(41 + C)
+    for (H, W) in [(1, 1), (1, 5), (3, 2), (2, 9), (7, 13), (16, 16), (33, 70)]:
+        img = rng.integers(0, 256, size=(H, W, C), dtype=np.uint8)
+        np.testing.assert_array_equal(up2(img), oracle.linear_u8(img, 2 * H, 2 * W))
+
+
+def test_the_identities_fail_on_a_planted_error():
+    # a wrong weight pair would not pass: the comparison has teeth
+    rng = np.random.default_rng(5)
+    img = rng.integers(0, 256, size=(9, 11, 3), dtype=np.uint8)
+    t = img.astype(np.int64)
+    wrong = ((t[0::2, 0::2][:4, :5] * 3 + t[1::2, 1::2][:4, :5] + 2) >> 2).astype(np.uint8)
+    assert not np.array_equal(wrong, oracle.linear_u8(img, 4, 5)[:4, :5])
