@@ -206,20 +206,45 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
 // V = sum of b a t over a, b in {1, 3} (CUDA interpolation page §2.2, §6.2).
 // At the borders the plan folds the outside tap onto the edge pixel with
 // all the weight, which is the same as repeating the edge pixel (§6.1).
+//
 // A thread takes P = 4 source columns s0 .. s0 + 3 of source row r and forms
-// output rows 2r and 2r + 1, columns 2 s0 .. 2 s0 + 7: it reads source rows
-// r - 1, r, r + 1 over columns s0 - 1 .. s0 + 4 (clamped), sums each column
-// vertically (1 and 3 for row 2r, 3 and 1 for row 2r + 1) and then
-// horizontally.  Interior groups read 32-bit words (byte offsets fixed at
-// compile time) when the source layout is 4-byte aligned; edge groups read
-// bytes with clamped columns.
+// output rows 2r and 2r + 1, columns 2 s0 .. 2 s0 + 7, from source rows
+// r - 1, r, r + 1 over columns s0 - 1 .. s0 + 4 (clamped).  The bytes of each
+// row sit in NW words (32-bit loads for interior groups on a 4-byte-aligned
+// layout, assembled from clamped byte loads otherwise), byte e of the group
+// at bit 8 (e % 4) of word e / 4.  The arithmetic runs on two bytes at a time
+// in 16-bit lanes: word w splits into lo[w] (bytes 4w, 4w + 2) and hi[w]
+// (bytes 4w + 1, 4w + 3).  The vertical sums (1 3 and 3 1) are lane-wise; a
+// byte's horizontal neighbour C bytes away lies, for a whole lane pair, in one
+// register of the other or the same parity, or across two adjacent ones (one
+// byte permute).  Every lane stays below 2^16 (at most 16 * 255 + 8).
+template <int C>
+struct Up2Layout {
+    static constexpr int P = 4;                    // source columns per thread
+    static constexpr int NB = (P + 2) * C;         // group bytes: columns s0 - 1 .. s0 + P
+    static constexpr int LEAD = (4 - C % 4) % 4;   // bytes before the group in its first word
+    static constexpr int NW = (LEAD + NB + 3) / 4;
+    static constexpr int NWO = 2 * P * C / 4;      // output words per row: 2, 6, 8
+};
+
+// The lane pair {byte e0 + d, byte e0 + 2 + d} of the split words, where the
+// pair register (parity a, word w) holds bytes e0 = 4w + a and e0 + 2.
+template <int NW>
+__device__ __forceinline__ uint32_t lane_pair(const uint32_t (&lo)[NW], const uint32_t (&hi)[NW], int e)
+{
+    const int ec = max(e, 0);
+    const int w = min(ec >> 2, NW - 1), w1 = min(w + 1, NW - 1);
+    const uint32_t *src = (ec & 1) ? hi : lo;
+    if (((ec >> 1) & 1) == 0)
+        return src[w];
+    return __byte_perm(src[w], src[w1], 0x5432);   // upper lane of word w, lower lane of w + 1
+}
+
 template <int C>
 __global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a, const __grid_constant__ CUtensorMap)
 {
-    constexpr int P = 4;                   // source columns per thread
-    constexpr int NB = (P + 2) * C;        // source bytes per row used: columns s0 - 1 .. s0 + P
-    constexpr int LEAD = (4 - C % 4) % 4;  // (s0 - 1) C - its word boundary, s0 a multiple of 4
-    constexpr int NW = (LEAD + NB + 3) / 4;
+    using Lay = Up2Layout<C>;
+    constexpr int P = Lay::P, NB = Lay::NB, LEAD = Lay::LEAD, NW = Lay::NW, NWO = Lay::NWO;
     grid_launch_dependents();
     grid_dependency_wait();
     const int gpr = (a.W + P - 1) / P;
@@ -235,67 +260,83 @@ __global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a,
     const bool inner = words_in && s0 >= 1 && (s0 - 1) * C - LEAD + 4 * NW <= a.W * C;
     for (int b = blockIdx.y; b < a.batch; b += gridDim.y) {
         const uint8_t *img = a.src + (long long)b * a.src_bstride;
-        int v[2][NB];   // vertical sums for output rows 2r and 2r + 1, per source byte
-        int t[3][NB];
+        uint32_t lo[3][NW], hi[3][NW];
 #pragma unroll
         for (int k = 0; k < 3; k++) {
             const uint8_t *row = img + (long long)rows[k] * a.src_pitch;
+            uint32_t wd[NW];
             if (inner) {
                 const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (s0 - 1) * C - LEAD);
-                uint32_t wd[NW];
 #pragma unroll
                 for (int i = 0; i < NW; i++)
                     wd[i] = __ldg(w + i);
-#pragma unroll
-                for (int i = 0; i < NB; i++)
-                    t[k][i] = (wd[(LEAD + i) / 4] >> (8 * ((LEAD + i) % 4))) & 0xff;
             } else {
 #pragma unroll
-                for (int i = 0; i < P + 2; i++) {
-                    const int col = clampi(s0 - 1 + i, 0, a.W - 1);
+                for (int i = 0; i < NW; i++)
+                    wd[i] = 0;
 #pragma unroll
-                    for (int c = 0; c < C; c++)
-                        t[k][i * C + c] = __ldg(row + col * C + c);
+                for (int i = 0; i < NB; i++) {
+                    const int col = clampi(s0 - 1 + i / C, 0, a.W - 1);
+                    wd[(LEAD + i) / 4] |= static_cast<uint32_t>(__ldg(row + col * C + i % C)) << (8 * ((LEAD + i) % 4));
                 }
+            }
+#pragma unroll
+            for (int i = 0; i < NW; i++) {
+                lo[k][i] = wd[i] & 0x00ff00ffu;
+                hi[k][i] = (wd[i] >> 8) & 0x00ff00ffu;
             }
         }
 #pragma unroll
-        for (int i = 0; i < NB; i++) {
-            v[0][i] = t[0][i] + 3 * t[1][i];
-            v[1][i] = 3 * t[1][i] + t[2][i];
-        }
-#pragma unroll
         for (int j = 0; j < 2; j++) {
-            int q[2 * P][C];
+            // vertical sums of output row 2r + j: rows (r - 1, r) weighted 1 3,
+            // or (r, r + 1) weighted 3 1
+            uint32_t vl[NW], vh[NW];
 #pragma unroll
-            for (int sx = 0; sx < P; sx++)
+            for (int i = 0; i < NW; i++) {
+                vl[i] = j == 0 ? lo[0][i] + 3 * lo[1][i] : 3 * lo[1][i] + lo[2][i];
+                vh[i] = j == 0 ? hi[0][i] + 3 * hi[1][i] : 3 * hi[1][i] + hi[2][i];
+            }
+            // horizontal: for every pair register, the even output (left
+            // neighbour 1, itself 3) and the odd output (itself 3, right 1)
+            uint32_t ev[2][NW], od[2][NW];
 #pragma unroll
-                for (int c = 0; c < C; c++) {
-                    const int l = v[j][sx * C + c], m = v[j][(sx + 1) * C + c], rr = v[j][(sx + 2) * C + c];
-                    q[2 * sx][c] = (l + 3 * m + 8) >> 4;
-                    q[2 * sx + 1][c] = (3 * m + rr + 8) >> 4;
+            for (int par = 0; par < 2; par++)
+#pragma unroll
+                for (int i = 0; i < NW; i++) {
+                    const int e0 = 4 * i + par;
+                    const uint32_t m = par ? vh[i] : vl[i];
+                    const uint32_t l = lane_pair<NW>(vl, vh, e0 - C), rr = lane_pair<NW>(vl, vh, e0 + C);
+                    ev[par][i] = ((l + 3 * m + 0x00080008u) >> 4) & 0x00ff00ffu;
+                    od[par][i] = ((3 * m + rr + 0x00080008u) >> 4) & 0x00ff00ffu;
                 }
+            // output byte ob: output column oc = ob / C, channel ob % C, from
+            // group byte e = LEAD + (oc / 2 + 1) C + ob % C, even or odd output
+            uint32_t ow[NWO];
+#pragma unroll
+            for (int wo = 0; wo < NWO; wo++) {
+                uint32_t bytes[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const int ob = 4 * wo + k, oc = ob / C;
+                    const int e = LEAD + (oc / 2 + 1) * C + ob % C;
+                    const uint32_t reg = (oc & 1) ? od[e & 1][e >> 2] : ev[e & 1][e >> 2];
+                    bytes[k] = ((e >> 1) & 1) ? (reg >> 16) : reg;   // low byte of its lane
+                }
+                ow[wo] = __byte_perm(__byte_perm(bytes[0], bytes[1], 0x0040), __byte_perm(bytes[2], bytes[3], 0x0040),
+                                     0x5410);
+            }
             uint8_t *op = a.dst + (long long)b * a.dst_bstride + (long long)(2 * r + j) * a.dst_pitch +
                           (long long)(2 * s0) * C;
-            const bool words = np == P && (reinterpret_cast<uintptr_t>(op) & 3) == 0;
-            if (words) {
-                // 2 P C bytes = 8, 24 or 32: whole 32-bit words
-                uint32_t ow[2 * P * C / 4];
-#pragma unroll
-                for (int i = 0; i < 2 * P * C / 4; i++)
-                    ow[i] = pack4(q[(4 * i) / C][(4 * i) % C], q[(4 * i + 1) / C][(4 * i + 1) % C],
-                                  q[(4 * i + 2) / C][(4 * i + 2) % C], q[(4 * i + 3) / C][(4 * i + 3) % C]);
+            if (np == P && (reinterpret_cast<uintptr_t>(op) & 3) == 0) {
                 uint32_t *o = reinterpret_cast<uint32_t *>(op);
 #pragma unroll
-                for (int i = 0; i < 2 * P * C / 4; i++)
+                for (int i = 0; i < NWO; i++)
                     __stcs(o + i, ow[i]);
             } else {
 #pragma unroll
-                for (int k = 0; k < 2 * P; k++)
-                    if (k < 2 * np)
-#pragma unroll
-                        for (int c = 0; c < C; c++)
-                            op[k * C + c] = static_cast<uint8_t>(q[k][c]);
+                for (int i = 0; i < 2 * P * C; i++)
+                    if (i < 2 * np * C)
+                        op[i] = static_cast<uint8_t>(ow[i / 4] >> (8 * (i % 4)));
             }
         }
     }
