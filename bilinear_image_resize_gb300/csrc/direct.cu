@@ -327,7 +327,16 @@ __global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a,
             }
             uint8_t *op = a.dst + (long long)b * a.dst_bstride + (long long)(2 * r + j) * a.dst_pitch +
                           (long long)(2 * s0) * C;
-            if (np == P && (reinterpret_cast<uintptr_t>(op) & 3) == 0) {
+            const uintptr_t oa = reinterpret_cast<uintptr_t>(op);
+            if (np == P && NWO % 4 == 0 && (oa & 15) == 0) {
+#pragma unroll
+                for (int i = 0; i < NWO; i += 4)
+                    __stcs(reinterpret_cast<uint4 *>(op) + i / 4, make_uint4(ow[i], ow[i + 1], ow[i + 2], ow[i + 3]));
+            } else if (np == P && NWO % 2 == 0 && (oa & 7) == 0) {
+#pragma unroll
+                for (int i = 0; i < NWO; i += 2)
+                    __stcs(reinterpret_cast<uint2 *>(op) + i / 2, make_uint2(ow[i], ow[i + 1]));
+            } else if (np == P && (oa & 3) == 0) {
                 uint32_t *o = reinterpret_cast<uint32_t *>(op);
 #pragma unroll
                 for (int i = 0; i < NWO; i++)
