@@ -298,32 +298,43 @@ __global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a,
             }
             // horizontal: for every pair register, the even output (left
             // neighbour 1, itself 3) and the odd output (itself 3, right 1)
+            // (only registers holding a byte the outputs use: group bytes
+            // LEAD + C .. LEAD + C + P C - 1)
             uint32_t ev[2][NW], od[2][NW];
 #pragma unroll
             for (int par = 0; par < 2; par++)
 #pragma unroll
                 for (int i = 0; i < NW; i++) {
                     const int e0 = 4 * i + par;
+                    const bool used = (e0 >= LEAD + C && e0 < LEAD + C + P * C) ||
+                                      (e0 + 2 >= LEAD + C && e0 + 2 < LEAD + C + P * C);
+                    if (!used) {
+                        ev[par][i] = od[par][i] = 0;
+                        continue;
+                    }
                     const uint32_t m = par ? vh[i] : vl[i];
                     const uint32_t l = lane_pair<NW>(vl, vh, e0 - C), rr = lane_pair<NW>(vl, vh, e0 + C);
                     ev[par][i] = ((l + 3 * m + 0x00080008u) >> 4) & 0x00ff00ffu;
                     od[par][i] = ((3 * m + rr + 0x00080008u) >> 4) & 0x00ff00ffu;
                 }
             // output byte ob: output column oc = ob / C, channel ob % C, from
-            // group byte e = LEAD + (oc / 2 + 1) C + ob % C, even or odd output
+            // group byte e = LEAD + (oc / 2 + 1) C + ob % C, even or odd
+            // output: byte 0 or 2 of its register, picked by byte permutes
             uint32_t ow[NWO];
 #pragma unroll
             for (int wo = 0; wo < NWO; wo++) {
-                uint32_t bytes[4];
+                uint32_t reg[4];
+                uint32_t pos[4];
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
                     const int ob = 4 * wo + k, oc = ob / C;
                     const int e = LEAD + (oc / 2 + 1) * C + ob % C;
-                    const uint32_t reg = (oc & 1) ? od[e & 1][e >> 2] : ev[e & 1][e >> 2];
-                    bytes[k] = ((e >> 1) & 1) ? (reg >> 16) : reg;   // low byte of its lane
+                    reg[k] = (oc & 1) ? od[e & 1][e >> 2] : ev[e & 1][e >> 2];
+                    pos[k] = ((e >> 1) & 1) ? 2u : 0u;
                 }
-                ow[wo] = __byte_perm(__byte_perm(bytes[0], bytes[1], 0x0040), __byte_perm(bytes[2], bytes[3], 0x0040),
-                                     0x5410);
+                const uint32_t lo2 = __byte_perm(reg[0], reg[1], pos[0] | ((4u + pos[1]) << 4));
+                const uint32_t hi2 = __byte_perm(reg[2], reg[3], pos[2] | ((4u + pos[3]) << 4));
+                ow[wo] = __byte_perm(lo2, hi2, 0x5410);
             }
             uint8_t *op = a.dst + (long long)b * a.dst_bstride + (long long)(2 * r + j) * a.dst_pitch +
                           (long long)(2 * s0) * C;
