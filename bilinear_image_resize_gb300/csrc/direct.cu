@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a,
 #pragma unroll
             for (int i = 0; i < NW; i++) {
                 lo[k][i] = wd[i] & 0x00ff00ffu;
-                hi[k][i] = (wd[i] >> 8) & 0x00ff00ffu;
+                hi[k][i] = __byte_perm(wd[i], 0, 0x4341);   // bytes 1, 3 into the lanes' low bytes
             }
         }
 #pragma unroll
@@ -312,10 +312,13 @@ __global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a,
                         ev[par][i] = od[par][i] = 0;
                         continue;
                     }
-                    const uint32_t m = par ? vh[i] : vl[i];
+                    // each lane sum is below 2^12, so after the shift bytes 0
+                    // and 2 hold the two results exactly (the only bytes the
+                    // output permutes take); the other bits need no mask
+                    const uint32_t m3 = 3 * (par ? vh[i] : vl[i]);
                     const uint32_t l = lane_pair<NW>(vl, vh, e0 - C), rr = lane_pair<NW>(vl, vh, e0 + C);
-                    ev[par][i] = ((l + 3 * m + 0x00080008u) >> 4) & 0x00ff00ffu;
-                    od[par][i] = ((3 * m + rr + 0x00080008u) >> 4) & 0x00ff00ffu;
+                    ev[par][i] = (l + m3 + 0x00080008u) >> 4;
+                    od[par][i] = (m3 + rr + 0x00080008u) >> 4;
                 }
             // output byte ob: output column oc = ob / C, channel ob % C, from
             // group byte e = LEAD + (oc / 2 + 1) C + ob % C, even or odd
