@@ -23,7 +23,7 @@ from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_EPI_
 __all__ = [
     "ResizeError", "Plan", "resize_plan_create", "resize_plan_destroy", "resize_plan_status",
     "resize_plan_set_tile", "resize_plan_set_option", "resize_u8", "resize_f32", "resize_u8_batch",
-    "resize_f32_batch", "resize_fused", "resize_u8_host",
+    "resize_f32_batch", "resize_fused", "resize_u8_host", "resize_wait_selftest",
     "resize_axis_table", "resize_strerror", "resize_last_cuda_error", "make_epilogue", "resize_u8_noalloc",
     "RZ_NOALLOC_MAX_DIM",
     "RZ_LINEAR", "RZ_NEAREST", "RZ_U8", "RZ_F32", "RZ_EPI_NORMALIZE_NCHW", "RZ_EPI_FILTER3X3",
@@ -186,6 +186,13 @@ def resize_u8_batch(plan: Plan, src, dst, mode: int | None = None, stream=None) 
 def resize_f32_batch(plan: Plan, src, dst, mode: int | None = None, stream=None) -> None:
     """dst[n] = resize(src[n]) for float32 tensors (N, H, W, C) -> (N, OH, OW, C), one launch."""
     _batch("resize_f32_batch", plan, src, dst, mode, stream)
+
+
+def resize_wait_selftest(dev_status, limit_us: int, stream=None) -> None:
+    """Launch the bounded-wait self-test: dev_status (a one-element int32 CUDA
+    tensor) receives RZ_ERR_TIMEOUT when the wait gives up after limit_us."""
+    _check(_native.load().resize_wait_selftest(dev_status.data_ptr(), limit_us, _stream(stream)),
+           "resize_wait_selftest")
 
 
 def make_epilogue(kind: int, batch: int = 1, src_batch_stride: int = 0, dst_batch_stride: int = 0,

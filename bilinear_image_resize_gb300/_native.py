@@ -66,6 +66,7 @@ SIGNATURES = {
     "resize_u8": (_i, [_p, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
     "resize_f32": (_i, [_p, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
     "resize_u8_batch": (_i, [_p, _p, _sz, _sz, _p, _sz, _sz, _i, _i, _i, _i, _i, _i, _i, _p]),
+    "resize_wait_selftest": (_i, [_p, _i, _p]),
     "resize_f32_batch": (_i, [_p, _p, _sz, _sz, _p, _sz, _sz, _i, _i, _i, _i, _i, _i, _i, _p]),
     "resize_fused": (_i, [_p, _p, _i, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, ctypes.POINTER(RzEpilogue), _p]),
     "resize_u8_host": (_i, [_p, _p, _sz, _p, _sz, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),

@@ -841,6 +841,13 @@ int resize_f32(rz_plan p, const float *src, size_t src_pitch, float *dst, size_t
     return run(p, rz::FAM_F32, src, src_pitch, 0, dst, dst_pitch, 0, H, W, C, out_h, out_w, mode, 1, extra, stream);
 }
 
+int resize_wait_selftest(int *dev_status, int limit_us, void *stream)
+{
+    if (!dev_status || limit_us < 1 || limit_us > 1000000) return RZ_ERR_ARG;
+    const int e = rz::launch_wait_selftest(dev_status, 1000ull * static_cast<unsigned long long>(limit_us), stream);
+    return e != 0 ? cuda_fail(static_cast<cudaError_t>(e)) : RZ_OK;
+}
+
 int resize_u8_batch(rz_plan p, const uint8_t *src, size_t src_pitch, size_t src_batch_stride, uint8_t *dst,
                     size_t dst_pitch, size_t dst_batch_stride, int batch, int H, int W, int C, int out_h, int out_w,
                     int mode, void *stream)

@@ -692,7 +692,26 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a, const __g
     }
 }
 
+// Self-test of the bounded wait: one thread waits on a barrier nothing
+// arrives on; the wait must give up after limit_ns and report the time-out.
+__global__ void k_wait_selftest(int *status, unsigned long long limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0)
+        return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    *status = RZ_OK;
+    mbar_wait_bounded(&bar, 0, status, limit_ns);   // writes RZ_ERR_TIMEOUT when it gives up
+}
+
 }  // namespace
+
+int launch_wait_selftest(int *status, unsigned long long limit_ns, void *stream)
+{
+    k_wait_selftest<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns);
+    return static_cast<int>(cudaGetLastError());
+}
 
 const void *kernel_for(int fam, int mode, int variant, int C)
 {

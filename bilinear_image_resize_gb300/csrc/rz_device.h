@@ -89,19 +89,20 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-// Wait for phase `parity` of the barrier, at most kWaitLimitNs.  Between
+// Wait for phase `parity` of the barrier, at most limit_ns (kWaitLimitNs).  Between
 // attempts the waiting warp sleeps (32 ns, doubling up to 256 ns) so that it
 // leaves the issue slots to the warps computing on the same scheduler.  On
 // time-out the status word (if given) records RZ_ERR_TIMEOUT and false is
 // returned.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status)
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status,
+                                                  uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = global_ns();
     unsigned int nap = 32;
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             if (status)
                 atomicExch(status, RZ_ERR_TIMEOUT);
             return false;

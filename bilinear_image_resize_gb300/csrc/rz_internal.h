@@ -168,6 +168,10 @@ int launch_resize(const void *fn, const KArgs &a, const CUtensorMap &tmap, int g
 // of two rows.
 __host__ __device__ constexpr int down2_px(int C) { return C == 1 ? 8 : (C == 3 ? 4 : 2); }
 
+// One CTA waiting on a barrier nothing completes, at most limit_ns; writes
+// RZ_ERR_TIMEOUT to *status when the wait gives up.  Returns a cudaError_t.
+int launch_wait_selftest(int *status, unsigned long long limit_ns, void *stream);
+
 // Direct-load kernels (direct.cu): a thread per output group, no staging.
 constexpr int kDirectThreads = 256;
 // The exact 2x uint8 downscale (bilinear or nearest) for C channels; nullptr

@@ -221,6 +221,17 @@ RZ_API int resize_u8_host(rz_plan p, const uint8_t *host_src, size_t host_src_pi
  */
 RZ_API int resize_axis_table(int n_in, int n_out, int mode, int32_t *ofs, int32_t *w_q11, float *u);
 
+/*
+ * Self-test of the bounded waits the staged and streaming kernels use on
+ * their shared-memory barriers: launches one CTA whose thread waits on a
+ * barrier that nothing completes, for at most limit_us microseconds
+ * (1..1000000), and writes RZ_ERR_TIMEOUT to *dev_status (caller-owned
+ * device memory; RZ_OK is written first) when the wait gives up.
+ * Asynchronous on `stream`.  It makes failure reporting testable without
+ * faulting or hanging a GPU; the pages have no counterpart.
+ */
+RZ_API int resize_wait_selftest(int *dev_status, int limit_us, void *stream);
+
 /* Human-readable name of a status code (static string). */
 RZ_API const char *resize_strerror(int code);
 

@@ -674,6 +674,26 @@ def test_options_reject_bad_values(rz):
                 rz.resize_plan_set_option(plan, opt, val)
 
 
+def test_bounded_wait_reports_timeout(rz):
+    # the barrier waits in the staged and streaming kernels give up after a
+    # limit and report RZ_ERR_TIMEOUT; here a wait on a barrier nothing
+    # completes must end within its limit, report, and leave the context usable
+    import time
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    rz.resize_wait_selftest(status, 2000)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(status.item()) == rz.RZ_ERR_TIMEOUT
+    assert 0.002 <= elapsed < 1.0
+    for bad in (0, -5, 1000001):
+        with pytest.raises(rz.ResizeError):
+            rz.resize_wait_selftest(status, bad)
+    img = synth.smooth_rgb(96, 64, 3)
+    np.testing.assert_array_equal(gpu_u8(rz, img, 40, 70, rz.RZ_LINEAR), oracle.linear_u8(img, 40, 70))
+
+
 def test_back_to_back_dependent_resizes(rz):
     # a chain where each resize reads the previous one's output, queued with
     # programmatic dependent launches: every link must see its input complete
