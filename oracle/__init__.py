@@ -36,14 +36,18 @@ def _load():
     lib.oracle_weight_q11.restype = _i64
     lib.oracle_nearest_index.argtypes = [_i64, _i64, _i64]
     lib.oracle_nearest_index.restype = _i64
-    for name in ("oracle_linear_u8", "oracle_nearest_u8"):
-        f = getattr(lib, name)
-        f.argtypes = [_p, _i64, _int, _int, _int, _p, _i64, _int, _int]
-        f.restype = None
+    lib.oracle_border_index.argtypes = [_i64, _i64, _int]
+    lib.oracle_border_index.restype = _i64
+    lib.oracle_nearest_u8.argtypes = [_p, _i64, _int, _int, _int, _p, _i64, _int, _int]
+    lib.oracle_nearest_u8.restype = None
+    lib.oracle_linear_u8.argtypes = [_p, _i64, _int, _int, _int, _p, _i64, _int, _int, _int]
+    lib.oracle_linear_u8.restype = None
     lib.oracle_linear_u8_rows.argtypes = [_p, _i64, _int, _int, _int, _p, _i64, _int, _int, _int, _int]
     lib.oracle_linear_u8_rows.restype = None
-    lib.oracle_linear_f32.argtypes = [_p, _i64, _int, _int, _int, _p, _int, _int]
+    lib.oracle_linear_f32.argtypes = [_p, _i64, _int, _int, _int, _p, _int, _int, _int]
     lib.oracle_linear_f32.restype = None
+    lib.oracle_gray_u8.argtypes = [_p, _i64, _int, _int, _int, _int, _p, _i64]
+    lib.oracle_gray_u8.restype = None
     lib.oracle_nearest_f32.argtypes = [_p, _i64, _int, _int, _int, _p, _int, _int]
     lib.oracle_nearest_f32.restype = None
     lib.oracle_normalize_nchw.argtypes = [_p, _int, _int, _int, _p, _p, _p]
@@ -85,13 +89,22 @@ def nearest_index(n_in: int, n_out: int, d: int) -> int:
     return _load().oracle_nearest_index(n_in, n_out, d)
 
 
-def linear_u8(src: np.ndarray, out_h: int, out_w: int) -> np.ndarray:
+# border rules (CUDA interpolation page §6.1)
+BORDER_CLAMP, BORDER_MIRROR, BORDER_WRAP = 0, 1, 2
+
+
+def border_index(k: int, n: int, border: int) -> int:
+    """Index k of an axis of n samples mapped inside by the border rule."""
+    return _load().oracle_border_index(k, n, border)
+
+
+def linear_u8(src: np.ndarray, out_h: int, out_w: int, border: int = BORDER_CLAMP) -> np.ndarray:
     """u8 bilinear resize of an HxW or HxWxC image; returns (out_h, out_w, C) u8."""
     s = _as_hwc(np.asarray(src))
-    assert s.dtype == np.uint8
+    assert s.dtype == np.uint8 and border in (0, 1, 2)
     H, W, C = s.shape
     dst = np.empty((out_h, out_w, C), np.uint8)
-    _load().oracle_linear_u8(_ptr(s), s.strides[0], H, W, C, _ptr(dst), dst.strides[0], out_h, out_w)
+    _load().oracle_linear_u8(_ptr(s), s.strides[0], H, W, C, _ptr(dst), dst.strides[0], out_h, out_w, border)
     return dst
 
 
@@ -116,13 +129,13 @@ def nearest_u8(src: np.ndarray, out_h: int, out_w: int) -> np.ndarray:
     return dst
 
 
-def linear_f32(src: np.ndarray, out_h: int, out_w: int) -> np.ndarray:
+def linear_f32(src: np.ndarray, out_h: int, out_w: int, border: int = BORDER_CLAMP) -> np.ndarray:
     """f32 bilinear resize evaluated in double; returns (out_h, out_w, C) float64."""
     s = _as_hwc(np.asarray(src))
-    assert s.dtype == np.float32
+    assert s.dtype == np.float32 and border in (0, 1, 2)
     H, W, C = s.shape
     dst = np.empty((out_h, out_w, C), np.float64)
-    _load().oracle_linear_f32(_ptr(s), s.strides[0], H, W, C, _ptr(dst), out_h, out_w)
+    _load().oracle_linear_f32(_ptr(s), s.strides[0], H, W, C, _ptr(dst), out_h, out_w, border)
     return dst
 
 
@@ -166,6 +179,26 @@ def linear_f32_filter3x3(src: np.ndarray, out_h: int, out_w: int, w) -> np.ndarr
     return filter3x3(linear_f32(src, out_h, out_w), w)
 
 
-def linear_u8_normalize(src: np.ndarray, out_h: int, out_w: int, mean, std) -> np.ndarray:
+def linear_u8_normalize(src: np.ndarray, out_h: int, out_w: int, mean, std,
+                        border: int = BORDER_CLAMP) -> np.ndarray:
     """The fused op's definition: normalize_nchw(linear_u8(src))."""
-    return normalize_nchw(linear_u8(src, out_h, out_w), mean, std)
+    return normalize_nchw(linear_u8(src, out_h, out_w, border), mean, std)
+
+
+def gray_u8(src: np.ndarray, bgr: bool = False) -> np.ndarray:
+    """Grayscale (H, W) u8 of an HxWxC u8 image, C >= 3 (channel order RGB, or BGR)."""
+    s = _as_hwc(np.asarray(src))
+    assert s.dtype == np.uint8 and s.shape[2] >= 3
+    H, W, C = s.shape
+    dst = np.empty((H, W), np.uint8)
+    _load().oracle_gray_u8(_ptr(s), s.strides[0], H, W, C, int(bool(bgr)), _ptr(dst), dst.strides[0])
+    return dst
+
+
+def gray_resize_u8(src: np.ndarray, out_h: int, out_w: int, linear: bool = True, bgr: bool = False,
+                   border: int = BORDER_CLAMP) -> np.ndarray:
+    """The fused op's definition: resize(gray_u8(src)), shape (out_h, out_w) u8."""
+    g = gray_u8(src, bgr)
+    if linear:
+        return linear_u8(g, out_h, out_w, border)[:, :, 0]
+    return nearest_u8(g, out_h, out_w)[:, :, 0]

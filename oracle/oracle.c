@@ -27,13 +27,18 @@
  *  [TRACKING]  "Performance Optimization of Object Tracking Algorithms in
  *              OpenCV on GPUs" — §4.2 kernel merging and Table 10: a merged
  *              kernel computes exactly the composition of the kernels it
- *              replaces.
+ *              replaces; §3.1.1 "Execution Flow": frames are converted to
+ *              grayscale (cvtColor, the RGB2Gray kernel) before the resize.
  *
  * Readings where the pages leave a step open (each is also listed in the
  * design notes):
  *  - mapping: x = (dx + 1/2) * W_in / W_out - 1/2 with the ratio of the actual
  *    sizes, held as the exact rational ((2dx+1) W_in - W_out) / (2 W_out);
- *  - border: both taps' indices are clamped into [0, n-1] ([INTERP] §6.1);
+ *  - border ([INTERP] §6.1 names clamp, mirror and wrap): each tap's integer
+ *    index is mapped into [0, n-1] by the border rule, the weights stay
+ *    those of the unmapped position; mirror reflects about the edge samples
+ *    (index -1 reads 1, index n reads n-2), wrap repeats the axis with
+ *    period n;
  *  - u8 weights: 11 fractional bits, A1 = round-half-up(2048 u), A0 = 2048-A1,
  *    the same for B on rows; the four products are summed exactly and rounded
  *    half-up once: (sum + 2^21) >> 22 ([INTERP] §6.2 "fixed point");
@@ -41,7 +46,10 @@
  *  - normalise: y = (q / 255 - mean[c]) / std[c] on the rounded u8 resize
  *    result q, written planar (NCHW);
  *  - 3x3 filter: correlation on the resized grid, replicate border on that
- *    grid, weights used as given (no division by 9).
+ *    grid, weights used as given (no division by 9);
+ *  - grayscale ([TRACKING] §3.1.1 gives no weights): the ITU-R BT.601 luma
+ *    weights 0.299 R + 0.587 G + 0.114 B, rounded half-up exactly to u8,
+ *    converted per source pixel before the resize samples it.
  *
  * Pixel (x, y), channel c of an interleaved image lives at byte offset
  * y * pitch + (x * C + c) * sizeof(element).  Pitches are in bytes.
@@ -65,6 +73,37 @@ static int64_t clamp_index(int64_t k, int64_t n)
     if (k > n - 1)
         return n - 1;
     return k;
+}
+
+/*
+ * Border rule of [INTERP] §6.1 for an integer index k on an axis of n samples:
+ *   0  clamp:  the nearest sample inside, k -> min(max(k, 0), n - 1);
+ *   1  mirror: reflection about the first and last sample centres, so the
+ *              extended axis reads 0 1 .. n-1 n-2 .. 1 0 1 .. (period 2n - 2);
+ *              a single sample (n = 1) is read everywhere;
+ *   2  wrap:   the axis repeats, k -> k mod n.
+ */
+static int64_t border_index(int64_t k, int64_t n, int border)
+{
+    if (border == 1) {
+        if (n == 1)
+            return 0;
+        int64_t period = 2 * (n - 1);
+        int64_t m = k % period;
+        if (m < 0)
+            m += period;
+        return m <= n - 1 ? m : period - m;
+    }
+    if (border == 2) {
+        int64_t m = k % n;
+        return m < 0 ? m + n : m;
+    }
+    return clamp_index(k, n);
+}
+
+int64_t oracle_border_index(int64_t k, int64_t n, int border)
+{
+    return border_index(k, n, border);
 }
 
 /*
@@ -96,26 +135,28 @@ int64_t oracle_nearest_index(int64_t n_in, int64_t n_out, int64_t d)
 }
 
 /*
- * u8 bilinear, [INTERP] §2.2 with §6.1 clamp and §6.2 fixed point:
+ * u8 bilinear, [INTERP] §2.2 with a §6.1 border rule and §6.2 fixed point:
  *   dst = ( B0 A0 s(i,j) + B0 A1 s(i+1,j) + B1 A0 s(i,j+1) + B1 A1 s(i+1,j+1)
  *           + 2^21 ) >> 22
- * where s(i, j) is column i, row j, and A/B are the 11-bit weights of u/v.
+ * where s(i, j) is column i, row j (indices mapped by border_index), and A/B
+ * are the 11-bit weights of u/v.
  */
-void oracle_linear_u8_rows(const uint8_t *src, int64_t src_pitch, int H, int W, int C,
-                           uint8_t *dst, int64_t dst_pitch, int OH, int OW, int dy0, int dy1)
+void oracle_linear_u8_border_rows(const uint8_t *src, int64_t src_pitch, int H, int W, int C,
+                                  uint8_t *dst, int64_t dst_pitch, int OH, int OW, int border,
+                                  int dy0, int dy1)
 {
     for (int64_t dy = dy0; dy < dy1 && dy < OH; dy++) {
         int64_t j, rv, dv;
         oracle_linear_coord(H, OH, dy, &j, &rv, &dv);
         int64_t B1 = oracle_weight_q11(rv, dv);
         int64_t B0 = 2048 - B1;
-        int64_t j0 = clamp_index(j, H), j1 = clamp_index(j + 1, H);
+        int64_t j0 = border_index(j, H, border), j1 = border_index(j + 1, H, border);
         for (int64_t dx = 0; dx < OW; dx++) {
             int64_t i, ru, du;
             oracle_linear_coord(W, OW, dx, &i, &ru, &du);
             int64_t A1 = oracle_weight_q11(ru, du);
             int64_t A0 = 2048 - A1;
-            int64_t i0 = clamp_index(i, W), i1 = clamp_index(i + 1, W);
+            int64_t i0 = border_index(i, W, border), i1 = border_index(i + 1, W, border);
             for (int64_t c = 0; c < C; c++) {
                 int64_t s00 = src[j0 * src_pitch + i0 * C + c];
                 int64_t s10 = src[j0 * src_pitch + i1 * C + c];
@@ -128,11 +169,18 @@ void oracle_linear_u8_rows(const uint8_t *src, int64_t src_pitch, int H, int W, 
     }
 }
 
-/* All output rows; the row-range form above lets a caller time a bounded sample. */
-void oracle_linear_u8(const uint8_t *src, int64_t src_pitch, int H, int W, int C,
-                      uint8_t *dst, int64_t dst_pitch, int OH, int OW)
+/* Clamp border, output rows [dy0, dy1): lets a caller time a bounded sample. */
+void oracle_linear_u8_rows(const uint8_t *src, int64_t src_pitch, int H, int W, int C,
+                           uint8_t *dst, int64_t dst_pitch, int OH, int OW, int dy0, int dy1)
 {
-    oracle_linear_u8_rows(src, src_pitch, H, W, C, dst, dst_pitch, OH, OW, 0, OH);
+    oracle_linear_u8_border_rows(src, src_pitch, H, W, C, dst, dst_pitch, OH, OW, 0, dy0, dy1);
+}
+
+/* All output rows, any border rule. */
+void oracle_linear_u8(const uint8_t *src, int64_t src_pitch, int H, int W, int C,
+                      uint8_t *dst, int64_t dst_pitch, int OH, int OW, int border)
+{
+    oracle_linear_u8_border_rows(src, src_pitch, H, W, C, dst, dst_pitch, OH, OW, border, 0, OH);
 }
 
 /* u8 nearest, [INTERP] §2.1 read as OpenCV INTER_NEAREST (floor). */
@@ -158,21 +206,22 @@ static double f32_at(const float *src, int64_t pitch_bytes, int64_t x, int64_t y
 /*
  * f32 bilinear, evaluated in double with the exact u = r / den:
  *   dst = (1-u)(1-v) s(i,j) + u(1-v) s(i+1,j) + (1-u)v s(i,j+1) + uv s(i+1,j+1)
- * [INTERP] §2.2, §6.1.  Output is double, dense, dst[(dy * OW + dx) * C + c].
+ * [INTERP] §2.2, §6.1 (indices mapped by border_index).  Output is double,
+ * dense, dst[(dy * OW + dx) * C + c].
  */
 void oracle_linear_f32(const float *src, int64_t src_pitch, int H, int W, int C,
-                       double *dst, int OH, int OW)
+                       double *dst, int OH, int OW, int border)
 {
     for (int64_t dy = 0; dy < OH; dy++) {
         int64_t j, rv, dv;
         oracle_linear_coord(H, OH, dy, &j, &rv, &dv);
         double v = (double)rv / (double)dv;
-        int64_t j0 = clamp_index(j, H), j1 = clamp_index(j + 1, H);
+        int64_t j0 = border_index(j, H, border), j1 = border_index(j + 1, H, border);
         for (int64_t dx = 0; dx < OW; dx++) {
             int64_t i, ru, du;
             oracle_linear_coord(W, OW, dx, &i, &ru, &du);
             double u = (double)ru / (double)du;
-            int64_t i0 = clamp_index(i, W), i1 = clamp_index(i + 1, W);
+            int64_t i0 = border_index(i, W, border), i1 = border_index(i + 1, W, border);
             for (int64_t c = 0; c < C; c++) {
                 double s00 = f32_at(src, src_pitch, i0, j0, C, c);
                 double s10 = f32_at(src, src_pitch, i1, j0, C, c);
@@ -235,5 +284,24 @@ void oracle_filter3x3(const double *r, int OH, int OW, const double *w, double *
                     sum += w[(a + 1) * 3 + (b + 1)] * r[yy * OW + xx];
                 }
             z[y * OW + x] = sum;
+        }
+}
+
+/*
+ * Grayscale of an interleaved u8 image with C >= 3 channels, [TRACKING]
+ * §3.1.1 (cvtColor to grayscale before the resize).  With (R, G, B) the
+ * channels (0, 1, 2), or (2, 1, 0) when bgr is set, and any fourth channel
+ * ignored:  Y = floor((299 R + 587 G + 114 B + 500) / 1000), which is
+ * 0.299 R + 0.587 G + 0.114 B rounded half-up, exactly.  dst is H x W u8.
+ */
+void oracle_gray_u8(const uint8_t *src, int64_t src_pitch, int H, int W, int C, int bgr,
+                    uint8_t *dst, int64_t dst_pitch)
+{
+    int64_t ir = bgr ? 2 : 0, ib = bgr ? 0 : 2;
+    for (int64_t y = 0; y < H; y++)
+        for (int64_t x = 0; x < W; x++) {
+            const uint8_t *px = src + y * src_pitch + x * C;
+            int64_t sum = 299 * (int64_t)px[ir] + 587 * (int64_t)px[1] + 114 * (int64_t)px[ib];
+            dst[y * dst_pitch + x] = (uint8_t)((sum + 500) / 1000);
         }
 }
