@@ -55,7 +55,15 @@ WORKLOADS = {
     "f32_8192_to_5980_filter3x3": ("f32 8192x8192 -> 5980x5980 bilinear + 3x3 filter", "filt", 8192, 8192, 5980,
                                    5980, 1, "linear", 1),
     "tiny_64x48_to_128x96": ("u8 64x48 -> 128x96 bilinear", "u8", 48, 64, 96, 128, 1, "linear", 1),
+    "4k_to_1080p_gray": ("4K RGB u8 -> gray (BT.601) -> 1080p bilinear, fused (3840x2160x3 -> 1920x1080x1)",
+                         "gray", 2160, 3840, 1080, 1920, 3, "linear", 1),
+    "1080p_to_4k_mirror": ("1080p->4K RGB u8 bilinear upscale, mirror border", "u8", 1080, 1920, 2160, 3840, 3,
+                           "linear", 1),
+    "1080p_to_4k_wrap": ("1080p->4K RGB u8 bilinear upscale, wrap border", "u8", 1080, 1920, 2160, 3840, 3,
+                         "linear", 1),
 }
+# border rule of a workload's plan (RZ_BORDER_*; clamp when absent)
+WORKLOAD_BORDER = {"1080p_to_4k_mirror": 1, "1080p_to_4k_wrap": 2}
 DEFAULT_WORKLOAD = "4k_to_1080p"
 METRIC = "output Gpix/s and achieved HBM GB/s (% of GB300 peak), 4K->1080p RGB u8 bilinear"
 
@@ -85,9 +93,9 @@ def algorithmic_bytes(kind, H, W, OH, OW, C, mode, batch):
     if m == rz.RZ_LINEAR:
         rows |= set(min(int(r) + 1, H - 1) for r in yofs)
     in_es = 4 if kind == "filt" else 1
-    out_es = 1 if kind == "u8" else 4
+    out_es = 1 if kind in ("u8", "gray") else 4
     read = len(rows) * W * C * in_es
-    write = OH * OW * C * out_es
+    write = OH * OW * (1 if kind == "gray" else C) * out_es
     return batch * read, batch * write
 
 
@@ -184,7 +192,7 @@ def make_frames(kind, H, W, C, batch, count, dev):
     import torch
 
     from bilinear_image_resize_gb300 import synth
-    if kind == "u8":
+    if kind in ("u8", "gray"):
         base = synth.smooth_rgb(W, H, 3) if (C == 3 and W >= 1920) else synth.random_u8((H, W, C), seed=3)
         if base.shape != (H, W, C):
             base = synth.random_u8((H, W, C), seed=3)
@@ -205,11 +213,24 @@ def make_outputs(kind, OH, OW, C, batch, count, dev):
     import torch
     if kind == "u8":
         shape, dt = (OH, OW, C), torch.uint8
+    elif kind == "gray":
+        shape, dt = (OH, OW), torch.uint8
     elif kind == "norm":
         shape, dt = (batch, C, OH, OW), torch.float32
     else:
         shape, dt = (OH, OW), torch.float32
     return [torch.empty(shape, dtype=dt, device=dev) for _ in range(count)]
+
+
+def make_epi(rz, synth, kind):
+    """The fused epilogue of a workload kind (None for the plain uint8 resize)."""
+    if kind == "norm":
+        return rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=synth.NORM_MEAN, std=synth.NORM_STD)
+    if kind == "filt":
+        return rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=synth.filter_weights())
+    if kind == "gray":
+        return rz.make_epilogue(rz.RZ_EPI_GRAY_RGB)
+    return None
 
 
 def gpu_arm(args, rank, local_rank, world):
@@ -232,7 +253,7 @@ def gpu_arm(args, rank, local_rank, world):
     ring = max(2, min(64, int(3 * L2_BYTES // (in_bytes + out_bytes)) + 1))
     frames = make_frames(kind, H, W, C, batch, ring, dev)
     outs = make_outputs(kind, OH, OW, C, batch, ring, dev)
-    plan = rz.resize_plan_create(H, W, OH, OW, mode)
+    plan = rz.resize_plan_create(H, W, OH, OW, mode, border=WORKLOAD_BORDER.get(args.workload, 0))
     if args.tile:
         tr, tw = (int(v) for v in args.tile.split("x"))
         fam = {"u8": rz.KIND_U8, "norm": rz.KIND_NORMALIZE, "filt": rz.KIND_FILTER3X3}[kind]
@@ -249,11 +270,7 @@ def gpu_arm(args, rank, local_rank, world):
         rz.resize_plan_set_option(plan, rz.RZ_OPT_PDL, 0)
     if args.u8_kernel:
         rz.resize_plan_set_option(plan, rz.RZ_OPT_U8_KERNEL, args.u8_kernel)
-    epi = None
-    if kind == "norm":
-        epi = rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=synth.NORM_MEAN, std=synth.NORM_STD)
-    elif kind == "filt":
-        epi = rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=synth.filter_weights())
+    epi = make_epi(rz, synth, kind)
 
     def step(i):
         s, d = frames[i % ring], outs[i % ring]
@@ -498,11 +515,17 @@ def oracle_rate(workload, budget_s):
     import oracle
     from bilinear_image_resize_gb300 import synth
     desc, kind, H, W, OH, OW, C, mode, batch = WORKLOADS[workload]
-    if kind == "u8":
+    border = WORKLOAD_BORDER.get(workload, 0)
+    if kind == "gray":
+        img = synth.smooth_rgb(W, H, 3)
+
+        def run(rows):
+            return oracle.gray_resize_u8(img, OH, OW)
+    elif kind == "u8":
         img = synth.smooth_rgb(W, H, 3) if (C == 3 and W >= 1920) else synth.random_u8((H, W, C), seed=3)
         if mode == "linear":
             def run(rows):
-                return oracle.linear_u8_rows(img, OH, OW, 0, rows)
+                return oracle.linear_u8_rows(img, OH, OW, 0, rows, border)
         else:
             def run(rows):
                 return oracle.nearest_u8(img, OH, OW)
@@ -553,16 +576,17 @@ def reference_arm(args):
         steps_px = None
     else:
         # each step: a band of output rows sized so that W + K steps take about a minute
+        border = WORKLOAD_BORDER.get(args.workload, 0)
         t0 = time.perf_counter()
-        oracle.linear_u8_rows(img, OH, OW, 0, OH)
+        oracle.linear_u8_rows(img, OH, OW, 0, OH, border)
         per_frame = time.perf_counter() - t0
         budget = 60.0 / max(1, args.steps + args.warmup)
         rows = int(max(1, min(OH, OH * budget / max(per_frame, 1e-6))))
         for _ in range(args.warmup):
-            oracle.linear_u8_rows(img, OH, OW, 0, rows)
+            oracle.linear_u8_rows(img, OH, OW, 0, rows, border)
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            oracle.linear_u8_rows(img, OH, OW, 0, rows)
+            oracle.linear_u8_rows(img, OH, OW, 0, rows, border)
         total_s = time.perf_counter() - t0
         value = rows * OW * args.steps / total_s / 1e9
         steps_px = rows * OW
@@ -598,12 +622,8 @@ def profile_run(args):
     ring = max(2, min(64, int(3 * L2_BYTES // max(1, in_bytes)) + 1))
     frames = make_frames(kind, H, W, C, batch, ring, dev)
     outs = make_outputs(kind, OH, OW, C, batch, ring, dev)
-    plan = rz.resize_plan_create(H, W, OH, OW, mode)
-    epi = None
-    if kind == "norm":
-        epi = rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=synth.NORM_MEAN, std=synth.NORM_STD)
-    elif kind == "filt":
-        epi = rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=synth.filter_weights())
+    plan = rz.resize_plan_create(H, W, OH, OW, mode, border=WORKLOAD_BORDER.get(args.workload, 0))
+    epi = make_epi(rz, synth, kind)
     nf = args.batch_frames if (kind == "u8" and args.profile_batched) else 0
     if nf:
         # two batches of nf frames in rotation, one resize_u8_batch launch each
@@ -687,7 +707,7 @@ def main():
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "u8" if WORKLOADS[args.workload][1] == "u8" else "f32",
+            "dtype": "u8" if WORKLOADS[args.workload][1] in ("u8", "gray") else "f32",
             "data": "synthetic",
             "config": {
                 "workload": desc,

@@ -14,8 +14,8 @@ from __future__ import annotations
 import ctypes
 
 from . import _native
-from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_EPI_FILTER3X3,
-                      RZ_EPI_NORMALIZE_NCHW, RZ_ERR_ARG, RZ_ERR_CUDA, RZ_ERR_NOMEM, RZ_ERR_TIMEOUT,
+from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_BORDER_CLAMP, RZ_BORDER_MIRROR,
+                      RZ_BORDER_WRAP, RZ_EPI_FILTER3X3, RZ_EPI_GRAY_BGR, RZ_EPI_GRAY_RGB, RZ_EPI_NORMALIZE_NCHW, RZ_ERR_ARG, RZ_ERR_CUDA, RZ_ERR_NOMEM, RZ_ERR_TIMEOUT,
                       RZ_ERR_UNSUPPORTED, RZ_F32, RZ_LINEAR, RZ_MAX_DIM, RZ_NEAREST, RZ_NOALLOC_MAX_DIM, RZ_OK,
                       RZ_OPT_CTAS_PER_SM, RZ_OPT_GENERIC_ONLY, RZ_OPT_GRID_MODE, RZ_OPT_PDL, RZ_OPT_RING_ROWS,
                       RZ_OPT_STAGES, RZ_OPT_U8_KERNEL, RZ_U8, RzEpilogue)
@@ -27,6 +27,8 @@ __all__ = [
     "resize_axis_table", "resize_strerror", "resize_last_cuda_error", "make_epilogue", "resize_u8_noalloc",
     "RZ_NOALLOC_MAX_DIM",
     "RZ_LINEAR", "RZ_NEAREST", "RZ_U8", "RZ_F32", "RZ_EPI_NORMALIZE_NCHW", "RZ_EPI_FILTER3X3",
+    "RZ_EPI_GRAY_RGB", "RZ_EPI_GRAY_BGR", "RZ_BORDER_CLAMP", "RZ_BORDER_MIRROR", "RZ_BORDER_WRAP",
+    "resize_plan_create_border", "resize_axis_table_border",
     "RZ_OK", "RZ_ERR_ARG", "RZ_ERR_UNSUPPORTED", "RZ_ERR_CUDA", "RZ_ERR_NOMEM", "RZ_ERR_TIMEOUT",
     "RZ_MAX_DIM", "KIND_U8", "KIND_F32", "KIND_NORMALIZE", "KIND_FILTER3X3",
     "RZ_OPT_STAGES", "RZ_OPT_GENERIC_ONLY", "RZ_OPT_CTAS_PER_SM", "RZ_OPT_GRID_MODE", "RZ_OPT_PDL",
@@ -61,9 +63,11 @@ def _stream(stream) -> int:
 class Plan:
     """Owns an ``rz_plan`` handle; freed by ``resize_plan_destroy`` or on collection."""
 
-    def __init__(self, handle: int, in_h: int, in_w: int, out_h: int, out_w: int, mode: int):
+    def __init__(self, handle: int, in_h: int, in_w: int, out_h: int, out_w: int, mode: int,
+                 border: int = RZ_BORDER_CLAMP):
         self.handle = handle
         self.in_h, self.in_w, self.out_h, self.out_w, self.mode = in_h, in_w, out_h, out_w, mode
+        self.border = border
 
     def destroy(self) -> None:
         if self.handle:
@@ -85,11 +89,22 @@ class Plan:
         self.destroy()
 
 
-def resize_plan_create(in_h: int, in_w: int, out_h: int, out_w: int, mode: int = RZ_LINEAR, stream=None) -> Plan:
+def resize_plan_create(in_h: int, in_w: int, out_h: int, out_w: int, mode: int = RZ_LINEAR, stream=None,
+                       border: int = RZ_BORDER_CLAMP) -> Plan:
+    if border != RZ_BORDER_CLAMP:
+        return resize_plan_create_border(in_h, in_w, out_h, out_w, mode, border, stream)
     h = ctypes.c_void_p()
     _check(_native.load().resize_plan_create(ctypes.byref(h), in_h, in_w, out_h, out_w, mode, _stream(stream)),
            "resize_plan_create")
     return Plan(h.value, in_h, in_w, out_h, out_w, mode)
+
+
+def resize_plan_create_border(in_h: int, in_w: int, out_h: int, out_w: int, mode: int, border: int,
+                              stream=None) -> Plan:
+    h = ctypes.c_void_p()
+    _check(_native.load().resize_plan_create_border(ctypes.byref(h), in_h, in_w, out_h, out_w, mode, border,
+                                                    _stream(stream)), "resize_plan_create_border")
+    return Plan(h.value, in_h, in_w, out_h, out_w, mode, border)
 
 
 def resize_plan_destroy(plan: Plan) -> None:
@@ -210,18 +225,32 @@ def make_epilogue(kind: int, batch: int = 1, src_batch_stride: int = 0, dst_batc
 
 
 def resize_fused(plan: Plan, src, dst, epilogue: RzEpilogue, stream=None) -> None:
-    """Bilinear resize with a fused epilogue.
+    """Resize with a fused epilogue.
 
     RZ_EPI_NORMALIZE_NCHW: src uint8 (N, H, W, C) or (H, W, C); dst float32
     (N, C, OH, OW) or (C, OH, OW).  RZ_EPI_FILTER3X3: src and dst float32
-    (N, H, W, C) / (H, W, C) / (H, W).  The epilogue's batch and batch strides
+    (N, H, W, C) / (H, W, C) / (H, W).  RZ_EPI_GRAY_RGB / RZ_EPI_GRAY_BGR:
+    src uint8 (N, H, W, C) or (H, W, C) with C = 3 or 4, dst uint8 (N, OH, OW)
+    or (OH, OW), in the plan's mode.  The epilogue's batch and batch strides
     are filled in from the tensors.
     """
     import torch
     e = RzEpilogue.from_buffer_copy(epilogue)
     batched = src.dim() == 4
     s = src if batched else src.unsqueeze(0)
-    if e.kind == RZ_EPI_NORMALIZE_NCHW:
+    mode = RZ_LINEAR
+    if e.kind in (RZ_EPI_GRAY_RGB, RZ_EPI_GRAY_BGR):
+        d = dst if dst.dim() == 3 else dst.unsqueeze(0)
+        N, OH, OW = d.shape
+        C = s.shape[3]
+        if d.stride(2) != 1:
+            raise ValueError("dst rows must be contiguous")
+        dp = d.stride(1)
+        dtype_code = RZ_U8
+        mode = plan.mode
+        if s.dtype != torch.uint8 or d.dtype != torch.uint8:
+            raise ValueError("gray epilogue takes uint8 src and dst")
+    elif e.kind == RZ_EPI_NORMALIZE_NCHW:
         d = dst if dst.dim() == 4 else dst.unsqueeze(0)
         N, C, OH, OW = d.shape
         if d.stride(3) != 1 or d.stride(1) != OH * d.stride(2):
@@ -252,7 +281,7 @@ def resize_fused(plan: Plan, src, dst, epilogue: RzEpilogue, stream=None) -> Non
     e.src_batch_stride = s.stride(0) * s.element_size()
     e.dst_batch_stride = d.stride(0) * d.element_size()
     _check(_native.load().resize_fused(plan.handle, s.data_ptr(), dtype_code, s.stride(1) * s.element_size(),
-                                       d.data_ptr(), dp, H, W, C, OH, OW, RZ_LINEAR, ctypes.byref(e),
+                                       d.data_ptr(), dp, H, W, C, OH, OW, mode, ctypes.byref(e),
                                        _stream(stream)), "resize_fused")
 
 
@@ -279,6 +308,17 @@ def resize_axis_table(n_in: int, n_out: int, mode: int = RZ_LINEAR):
     u = np.zeros(n_out, np.float32)
     _check(_native.load().resize_axis_table(n_in, n_out, mode, ofs.ctypes.data, w.ctypes.data, u.ctypes.data),
            "resize_axis_table")
+    return ofs, w, u
+
+
+def resize_axis_table_border(n_in: int, n_out: int, mode: int, border: int):
+    """resize_axis_table under a border rule."""
+    import numpy as np
+    ofs = np.zeros(n_out, np.int32)
+    w = np.zeros(n_out, np.int32)
+    u = np.zeros(n_out, np.float32)
+    _check(_native.load().resize_axis_table_border(n_in, n_out, mode, border, ofs.ctypes.data, w.ctypes.data,
+                                                   u.ctypes.data), "resize_axis_table_border")
     return ofs, w, u
 
 

@@ -16,6 +16,11 @@ RZ_U8 = 0
 RZ_F32 = 1
 RZ_EPI_NORMALIZE_NCHW = 1
 RZ_EPI_FILTER3X3 = 2
+RZ_EPI_GRAY_RGB = 3
+RZ_EPI_GRAY_BGR = 4
+RZ_BORDER_CLAMP = 0
+RZ_BORDER_MIRROR = 1
+RZ_BORDER_WRAP = 2
 RZ_OK = 0
 RZ_ERR_ARG = 1
 RZ_ERR_UNSUPPORTED = 2
@@ -59,6 +64,7 @@ _i = ctypes.c_int
 # name -> (restype, argtypes); every symbol include/gbresize.h declares
 SIGNATURES = {
     "resize_plan_create": (_i, [ctypes.POINTER(_p), _i, _i, _i, _i, _i, _p]),
+    "resize_plan_create_border": (_i, [ctypes.POINTER(_p), _i, _i, _i, _i, _i, _i, _p]),
     "resize_plan_destroy": (_i, [_p]),
     "resize_plan_status": (_i, [_p, ctypes.POINTER(_i)]),
     "resize_plan_set_tile": (_i, [_p, _i, _i, _i]),
@@ -71,6 +77,7 @@ SIGNATURES = {
     "resize_fused": (_i, [_p, _p, _i, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, ctypes.POINTER(RzEpilogue), _p]),
     "resize_u8_host": (_i, [_p, _p, _sz, _p, _sz, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
     "resize_axis_table": (_i, [_i, _i, _i, _p, _p, _p]),
+    "resize_axis_table_border": (_i, [_i, _i, _i, _i, _p, _p, _p]),
     "resize_strerror": (ctypes.c_char_p, [_i]),
     "resize_last_cuda_error": (_i, []),
     "resize_u8_noalloc": (_i, [_p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),

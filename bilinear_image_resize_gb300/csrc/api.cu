@@ -41,10 +41,20 @@ int64_t floor_div(int64_t a, int64_t b)  // b > 0
 // den = 2 n_out (Volcanic resize page, "Naive resize with linear sampling").
 // ofs = floor(x); the far tap's weight is u = r / den with r = num - ofs*den:
 // as 11-bit fixed point round-half-up(2048 u) (CUDA interpolation page §6.2),
-// as float rounded once from double.  A left tap left of 0, or a left tap at
-// n_in - 1, is folded to one clamped tap with weight 0: both taps would read
-// the same clamped sample (§6.1), so the value is unchanged.
-void axis_linear(int n_in, int n_out, int32_t *ofs, int32_t *q11, float *u)
+// as float rounded once from double.  The sampled position lies in
+// [-1/2, n_in - 1/2], so only ofs = -1 or ofs = n_in - 1 has a tap outside,
+// which the border rule maps (§6.1; the weights stay those of the unmapped
+// position):
+//  - clamp: both taps read the same edge sample, so the entry is folded to
+//    one tap with weight 0 (value unchanged);
+//  - mirror: the outside tap reads the inside neighbour of the edge sample,
+//    so the taps stay adjacent and the entry becomes that adjacent pair with
+//    the weights exchanged (ofs 0 or n_in - 2, weight 2048 - w, u = 1 - u);
+//  - wrap: the outside tap reads the opposite edge sample, so the entry keeps
+//    its weight with ofs = n_in - 1, and the kernels take sample 0 as the
+//    far tap of ofs = n_in - 1.
+// A one-sample axis reads its sample under every rule (folded as clamp).
+void axis_linear(int n_in, int n_out, int border, int32_t *ofs, int32_t *q11, float *u)
 {
     const int64_t den = 2 * static_cast<int64_t>(n_out);
     for (int64_t d = 0; d < n_out; d++) {
@@ -53,7 +63,15 @@ void axis_linear(int n_in, int n_out, int32_t *ofs, int32_t *q11, float *u)
         const int64_t r = num - s * den;
         int64_t w = floor_div(4096 * r + den, 2 * den);
         float uf = static_cast<float>(static_cast<double>(r) / static_cast<double>(den));
-        if (s < 0) {
+        const bool outside = s < 0 || (s >= n_in - 1 && r != 0);
+        const float uflip = static_cast<float>(static_cast<double>(den - r) / static_cast<double>(den));
+        if (outside && border == RZ_BORDER_MIRROR && n_in > 1) {
+            s = s < 0 ? 0 : n_in - 2;
+            w = 2048 - w;
+            uf = uflip;
+        } else if (outside && border == RZ_BORDER_WRAP) {
+            s = n_in - 1;
+        } else if (s < 0) {
             s = 0;
             w = 0;
             uf = 0.0f;
@@ -113,6 +131,7 @@ EncodeTiledFn tensor_encoder()
 
 struct rz_plan_s {
     int H, W, OH, OW, mode, device;
+    int border = RZ_BORDER_CLAMP;   // bilinear taps outside the source (RZ_BORDER_*)
     std::vector<int32_t> xofs, xq, yofs, yq;
     std::vector<float> xu, yu;
     void *dmem = nullptr;
@@ -134,6 +153,7 @@ struct rz_plan_s {
 namespace {
 
 bool valid_mode(int m) { return m == RZ_LINEAR || m == RZ_NEAREST; }
+bool valid_border(int b) { return b == RZ_BORDER_CLAMP || b == RZ_BORDER_MIRROR || b == RZ_BORDER_WRAP; }
 
 // Upper bound on the bytes of one staged source row of the tile column
 // starting at output column dx0: the tap span rounded out to 16 bytes.
@@ -486,27 +506,58 @@ bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15)
 bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do_launch, int *rc)
 {
     const int opt = p->opt_u8_kernel;
-    if (!((fam == rz::FAM_U8 && (opt == 0 || opt == 3)) || (fam == rz::FAM_NORM && opt != 1))) return false;
     const int C = a.C, batch = a.batch;
-    if (fam == rz::FAM_U8 && mode == RZ_LINEAR && !p->opt_generic && a.OW == 2 * a.W && a.OH == 2 * a.H) {
-        // exact 2x upscale: the 1-3 weights (direct.cu k_up2_direct), any layout
+    const bool wrap = p->border == RZ_BORDER_WRAP && mode == RZ_LINEAR;
+    auto launch = [&](const void *fn, long long threads) {
+        *rc = RZ_OK;
+        if (!do_launch) return true;
+        const int gx = static_cast<int>((threads + rz::kDirectThreads - 1) / rz::kDirectThreads);
+        CUtensorMap none;
+        std::memset(&none, 0, sizeof(none));
+        const int e = rz::launch_resize(fn, a, none, gx, 0, p->opt_pdl != 0, stream, rz::kDirectThreads,
+                                        std::min(batch, 65535));
+        if (e != 0) *rc = cuda_fail(static_cast<cudaError_t>(e));
+        return true;
+    };
+    if (fam == rz::FAM_GRAY) {
+        // gray conversion then uint8 resize: a thread per four output pixels;
+        // exact 2x downscales with vector loads where the layout allows
         a.xt = p->d_xq;
         a.yt = p->d_yq;
-        const void *ufn = rz::direct_up2_kernel_for(C);
-        if (ufn) {
-            *rc = RZ_OK;
-            if (!do_launch) return true;
-            const long long groups = static_cast<long long>(a.H) * ((a.W + rz::kUp2Cols - 1) / rz::kUp2Cols);
-            const int gx = static_cast<int>((groups + rz::kDirectThreads - 1) / rz::kDirectThreads);
-            CUtensorMap none;
-            std::memset(&none, 0, sizeof(none));
-            const int e = rz::launch_resize(ufn, a, none, gx, 0, p->opt_pdl != 0, stream, rz::kDirectThreads,
-                                            std::min(batch, 65535));
-            if (e != 0) *rc = cuda_fail(static_cast<cudaError_t>(e));
-            return true;
+        const long long groups = static_cast<long long>(a.OH) * ((a.OW + rz::kDirectRun - 1) / rz::kDirectRun);
+        if (!p->opt_generic && a.W == 2 * a.OW && a.H == 2 * a.OH && (mode == RZ_NEAREST || is_down2(*p))) {
+            const uintptr_t lw = C == 3 ? 8 : 16;
+            const uintptr_t sa = reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
+                                 static_cast<uintptr_t>(a.src_bstride);
+            const uintptr_t da = reinterpret_cast<uintptr_t>(a.dst) | static_cast<uintptr_t>(a.dst_pitch) |
+                                 static_cast<uintptr_t>(a.dst_bstride);
+            const void *dfn = rz::direct_down2_gray_kernel_for(mode, C, a.bgr != 0);
+            if (dfn && sa % lw == 0 && da % 4 == 0) return launch(dfn, groups);
         }
+        const void *gfn = rz::direct_gray_kernel_for(mode, C, wrap);
+        if (!gfn) return false;
+        return launch(gfn, groups);
     }
-    if (fam == rz::FAM_U8 && opt == 0 && mode == RZ_LINEAR && auto_u8_stream(*p) && !is_down2(*p)) return false;
+    if (fam == rz::FAM_F32) {
+        // float32 plans with the wrap rule: a thread per output pixel
+        if (!wrap) return false;
+        const void *ffn = rz::direct_f32_kernel_for(C, true);
+        if (!ffn) return false;
+        a.xt = p->d_xf;
+        a.yt = p->d_yf;
+        return launch(ffn, static_cast<long long>(a.OH) * a.OW);
+    }
+    if (!((fam == rz::FAM_U8 && (opt == 0 || opt == 3)) || (fam == rz::FAM_NORM && opt != 1))) return false;
+    if (fam == rz::FAM_U8 && mode == RZ_LINEAR && !p->opt_generic && a.OW == 2 * a.W && a.OH == 2 * a.H) {
+        // exact 2x upscale: the 1-3 weights (direct.cu k_up2_direct), any
+        // layout, any border rule
+        a.xt = p->d_xq;
+        a.yt = p->d_yq;
+        const void *ufn = rz::direct_up2_kernel_for(C, p->border);
+        if (ufn) return launch(ufn, static_cast<long long>(a.H) * ((a.W + rz::kUp2Cols - 1) / rz::kUp2Cols));
+    }
+    if (fam == rz::FAM_U8 && opt == 0 && mode == RZ_LINEAR && auto_u8_stream(*p) && !is_down2(*p) && !wrap)
+        return false;
     a.xt = p->d_xq;
     a.yt = p->d_yq;
     const void *fn = nullptr;
@@ -525,7 +576,7 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
         }
     }
     const long long gpr = (a.OW + rz::kDirectRun - 1) / rz::kDirectRun;
-    if (!fn && fam == rz::FAM_U8 && mode == RZ_LINEAR && a.OH > a.H && opt == 3) {
+    if (!fn && fam == rz::FAM_U8 && mode == RZ_LINEAR && a.OH > a.H && opt == 3 && !wrap) {
         // about 2048 threads per SM, each walking R output rows
         fn = rz::direct_rows_kernel_for(C);
         int sms = 0;
@@ -544,23 +595,15 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
     }
     if (!fn && fam == rz::FAM_NORM) {
         // a warp per 32 kNormRun output pixels of a row
-        fn = rz::direct_kernel_for(rz::DIRECT_NORM, mode, C);
+        fn = rz::direct_kernel_for(rz::DIRECT_NORM, mode, C, wrap);
         groups = static_cast<long long>(a.OH) * ((a.OW + 32 * rz::kNormRun - 1) / (32 * rz::kNormRun)) * 32;
     }
     if (!fn) {
-        fn = rz::direct_kernel_for(rz::DIRECT_U8, mode, C);
+        fn = rz::direct_kernel_for(rz::DIRECT_U8, mode, C, wrap);
         groups = gpr * a.OH;
     }
     if (!fn) return false;
-    *rc = RZ_OK;
-    if (!do_launch) return true;
-    const int gx = static_cast<int>((groups + rz::kDirectThreads - 1) / rz::kDirectThreads);
-    CUtensorMap none;
-    std::memset(&none, 0, sizeof(none));
-    const int e = rz::launch_resize(fn, a, none, gx, 0, p->opt_pdl != 0, stream, rz::kDirectThreads,
-                                    std::min(batch, 65535));
-    if (e != 0) *rc = cuda_fail(static_cast<cudaError_t>(e));
-    return true;
+    return launch(fn, groups);
 }
 
 // Shared body of every resize entry point.  `planes` > 0 selects the planar
@@ -577,8 +620,9 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     if (!src || !dst) return RZ_ERR_ARG;
     const int in_es = rz::fam_in_es(fam), out_es = rz::fam_out_es(fam);
     const bool nchw = fam == rz::FAM_NORM;
+    const int out_c = (nchw || fam == rz::FAM_GRAY) ? 1 : C;   // interleaved channels of an output row
     const size_t in_row = static_cast<size_t>(W) * C * in_es;
-    const size_t out_row = static_cast<size_t>(OW) * (nchw ? 1 : C) * out_es;
+    const size_t out_row = static_cast<size_t>(OW) * out_c * out_es;
     if (src_pitch < in_row || dst_pitch < out_row) return RZ_ERR_ARG;
     if (in_es == 4 && ((src_pitch & 3) || (reinterpret_cast<uintptr_t>(src) & 3))) return RZ_ERR_ARG;
     if (out_es == 4 && ((dst_pitch & 3) || (reinterpret_cast<uintptr_t>(dst) & 3))) return RZ_ERR_ARG;
@@ -606,7 +650,12 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     a.H = H; a.W = W; a.OH = OH; a.OW = OW; a.C = C;
     a.batch = batch;
     a.status = p->d_status;
+    a.border = p->border;
     if (run_direct(p, fam, a, mode, stream, do_launch, &rc)) return rc;
+    // the staged and streaming kernels take source spans from the tables,
+    // which under the wrap rule are not monotone at the edges
+    if (p->border == RZ_BORDER_WRAP && mode == RZ_LINEAR) return RZ_ERR_UNSUPPORTED;
+    if (fam == rz::FAM_GRAY) return RZ_ERR_UNSUPPORTED;
 
     TileCfg t;
     const void *fn = nullptr;
@@ -618,7 +667,7 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     a.box_bytes = t.box_bytes;
     a.tma_in = aligned16(src) && (src_pitch % 16 == 0) && (in_row % 16 == 0) &&
                (a.src_bstride % 16 == 0);
-    const int strip_bytes = t.TW * (nchw ? 1 : C) * out_es;
+    const int strip_bytes = t.TW * out_c * out_es;
     a.tma_out = aligned16(dst) && (dst_pitch % 16 == 0) && (a.dst_bstride % 16 == 0) &&
                 (a.dst_plane % 16 == 0) && (t.tiles_x == 1 || strip_bytes % 16 == 0);
     const bool fl = (fam == rz::FAM_F32 || fam == rz::FAM_FILT);
@@ -660,9 +709,16 @@ extern "C" {
 
 int resize_axis_table(int n_in, int n_out, int mode, int32_t *ofs, int32_t *w_q11, float *u)
 {
-    if (n_in < 1 || n_out < 0 || n_in > RZ_MAX_DIM || n_out > RZ_MAX_DIM || !valid_mode(mode)) return RZ_ERR_ARG;
+    return resize_axis_table_border(n_in, n_out, mode, RZ_BORDER_CLAMP, ofs, w_q11, u);
+}
+
+int resize_axis_table_border(int n_in, int n_out, int mode, int border, int32_t *ofs, int32_t *w_q11, float *u)
+{
+    if (n_in < 1 || n_out < 0 || n_in > RZ_MAX_DIM || n_out > RZ_MAX_DIM || !valid_mode(mode) ||
+        !valid_border(border))
+        return RZ_ERR_ARG;
     if (mode == RZ_LINEAR) {
-        axis_linear(n_in, n_out, ofs, w_q11, u);
+        axis_linear(n_in, n_out, border, ofs, w_q11, u);
     } else {
         std::vector<int32_t> tmp(static_cast<size_t>(n_out));
         axis_nearest(n_in, n_out, tmp.data());
@@ -673,14 +729,20 @@ int resize_axis_table(int n_in, int n_out, int mode, int32_t *ofs, int32_t *w_q1
 
 int resize_plan_create(rz_plan *out, int in_h, int in_w, int out_h, int out_w, int mode, void *stream)
 {
+    return resize_plan_create_border(out, in_h, in_w, out_h, out_w, mode, RZ_BORDER_CLAMP, stream);
+}
+
+int resize_plan_create_border(rz_plan *out, int in_h, int in_w, int out_h, int out_w, int mode, int border,
+                              void *stream)
+{
     if (!out) return RZ_ERR_ARG;
     *out = nullptr;
     if (in_h < 1 || in_w < 1 || out_h < 0 || out_w < 0 || in_h > RZ_MAX_DIM || in_w > RZ_MAX_DIM ||
-        out_h > RZ_MAX_DIM || out_w > RZ_MAX_DIM || !valid_mode(mode))
+        out_h > RZ_MAX_DIM || out_w > RZ_MAX_DIM || !valid_mode(mode) || !valid_border(border))
         return RZ_ERR_ARG;
     rz_plan_s *p = new (std::nothrow) rz_plan_s();
     if (!p) return RZ_ERR_NOMEM;
-    p->H = in_h; p->W = in_w; p->OH = out_h; p->OW = out_w; p->mode = mode;
+    p->H = in_h; p->W = in_w; p->OH = out_h; p->OW = out_w; p->mode = mode; p->border = border;
     try {
         p->xofs.resize(out_w); p->xq.resize(out_w); p->xu.resize(out_w);
         p->yofs.resize(out_h); p->yq.resize(out_h); p->yu.resize(out_h);
@@ -689,8 +751,8 @@ int resize_plan_create(rz_plan *out, int in_h, int in_w, int out_h, int out_w, i
         return RZ_ERR_NOMEM;
     }
     if (mode == RZ_LINEAR) {
-        axis_linear(in_w, out_w, p->xofs.data(), p->xq.data(), p->xu.data());
-        axis_linear(in_h, out_h, p->yofs.data(), p->yq.data(), p->yu.data());
+        axis_linear(in_w, out_w, border, p->xofs.data(), p->xq.data(), p->xu.data());
+        axis_linear(in_h, out_h, border, p->yofs.data(), p->yq.data(), p->yu.data());
     } else {
         axis_nearest(in_w, out_w, p->xofs.data());
         axis_nearest(in_h, out_h, p->yofs.data());
@@ -778,7 +840,9 @@ int resize_plan_status(rz_plan p, int *status)
 
 int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_cols)
 {
-    if (!p || kind < 0 || kind >= rz::FAM_COUNT || kind == 2 || tile_rows < 0 || tile_cols < 0) return RZ_ERR_ARG;
+    if (!p || kind < 0 || kind >= rz::FAM_COUNT || kind == 2 || kind == rz::FAM_GRAY || tile_rows < 0 ||
+        tile_cols < 0)
+        return RZ_ERR_ARG;
     if ((tile_rows == 0) != (tile_cols == 0)) return RZ_ERR_ARG;
     std::lock_guard<std::mutex> lk(p->mu);
     p->over_tr[kind] = tile_rows;
@@ -869,9 +933,18 @@ int resize_f32_batch(rz_plan p, const float *src, size_t src_pitch, size_t src_b
 int resize_fused(rz_plan p, const void *src, int src_dtype, size_t src_pitch, void *dst, size_t dst_pitch, int H,
                  int W, int C, int out_h, int out_w, int mode, const rz_epilogue *e, void *stream)
 {
-    if (!e || mode != RZ_LINEAR) return RZ_ERR_ARG;
+    if (!e) return RZ_ERR_ARG;
     KArgs extra = {};
     int fam;
+    if (e->kind == RZ_EPI_GRAY_RGB || e->kind == RZ_EPI_GRAY_BGR) {
+        if (src_dtype != RZ_U8 || !valid_mode(mode) || C < 3) return RZ_ERR_ARG;
+        if (C > 4) return RZ_ERR_UNSUPPORTED;
+        fam = rz::FAM_GRAY;
+        extra.bgr = e->kind == RZ_EPI_GRAY_BGR ? 1 : 0;
+        return run(p, fam, src, src_pitch, e->src_batch_stride, dst, dst_pitch, e->dst_batch_stride, H, W, C, out_h,
+                   out_w, mode, e->batch, extra, stream);
+    }
+    if (mode != RZ_LINEAR) return RZ_ERR_ARG;
     if (e->kind == RZ_EPI_NORMALIZE_NCHW) {
         if (src_dtype != RZ_U8) return RZ_ERR_ARG;
         fam = rz::FAM_NORM;

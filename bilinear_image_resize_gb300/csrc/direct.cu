@@ -112,8 +112,11 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_direct(const KArgs a, 
 // rows through L1 (neighbouring threads share them), 32-bit words where the
 // row layout allows and the taps lie at least 12 bytes before the row's end
 // (so no load passes the row), bytes otherwise; the four pixels leave as
-// 32-bit words when the output layout allows.
-template <int C, int LINEAR>
+// 32-bit words when the output layout allows.  WRAP: the plan's border rule
+// is wrap, whose edge entries hold the last sample as the near tap, and the
+// far tap past the last sample is sample 0 (far_tap); the clamp and mirror
+// rules are in the tables alone.
+template <int C, int LINEAR, bool WRAP>
 __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const __grid_constant__ CUtensorMap)
 {
     constexpr int RUN = 4;
@@ -133,7 +136,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
     const int xs[RUN] = {xa.x, xa.z, xb.x, xb.z};   // left tap (nearest: the tap)
     const int xw[RUN] = {xa.y, xa.w, xb.y, xb.w};   // right tap's 11-bit weight
     const int2 ye = __ldg(a.yt + dy);
-    const int r0 = ye.x, r1 = LINEAR ? min(ye.x + 1, a.H - 1) : ye.x;
+    const int r0 = ye.x, r1 = LINEAR ? far_tap<WRAP>(ye.x, a.H) : ye.x;
     const int B1 = ye.y, B0 = 2048 - B1;
     const bool words_in = ((reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
                             static_cast<uintptr_t>(a.src_bstride)) & 3) == 0;
@@ -155,12 +158,13 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
                     q[k][c] = __ldg(top + o0 + c);
             } else {
                 int hT[C], hB[C];
+                // o0 + 12 <= row bytes puts the far tap inside (xs <= W - 2)
                 if (words_in && o0 + 12 <= row_bytes) {
                     const uint32_t aw = static_cast<uint32_t>(2048 - xw[k]) | (static_cast<uint32_t>(xw[k]) << 16);
                     hsum_u8<C>(top, o0, aw, hT);
                     hsum_u8<C>(bot, o0, aw, hB);
                 } else {
-                    const int o1 = min(xs[k] + 1, a.W - 1) * C;
+                    const int o1 = far_tap<WRAP>(xs[k], a.W) * C;
 #pragma unroll
                     for (int c = 0; c < C; c++) {
                         hT[c] = (2048 - xw[k]) * __ldg(top + o0 + c) + xw[k] * __ldg(top + o1 + c);
@@ -204,8 +208,10 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
 // rows.  The 11-bit weights are then 512 and 1536, so the exact sum
 // (B0 (A0 t0 + A1 t1) + B1 (...) + 2^21) >> 22 equals (V + 8) >> 4 with
 // V = sum of b a t over a, b in {1, 3} (CUDA interpolation page §2.2, §6.2).
-// At the borders the plan folds the outside tap onto the edge pixel with
-// all the weight, which is the same as repeating the edge pixel (§6.1).
+// A tap outside the source (source column or row -1 or n) reads the sample
+// the plan's border rule BORDER names (§6.1: clamp, mirror or wrap;
+// border_index); the rule is a template parameter, so the clamp form has no
+// test of it.
 //
 // A thread takes P = 4 source columns s0 .. s0 + 3 of source row r and forms
 // output rows 2r and 2r + 1, columns 2 s0 .. 2 s0 + 7, from source rows
@@ -240,7 +246,7 @@ __device__ __forceinline__ uint32_t lane_pair(const uint32_t (&lo)[NW], const ui
     return __byte_perm(src[w], src[w1], 0x5432);   // upper lane of word w, lower lane of w + 1
 }
 
-template <int C>
+template <int C, int BORDER>
 __global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a, const __grid_constant__ CUtensorMap)
 {
     using Lay = Up2Layout<C>;
@@ -253,7 +259,10 @@ __global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a,
         return;
     const int r = idx / gpr, s0 = (idx - r * gpr) * P;
     const int np = min(P, a.W - s0);
-    const int rows[3] = {max(r - 1, 0), r, min(r + 1, a.H - 1)};
+    // (the clamp form spelled as max / min / clampi: this kernel's register
+    // allocation, and its speed, follow the exact form of these expressions)
+    const int rows[3] = {BORDER == RZ_BORDER_CLAMP ? max(r - 1, 0) : border_index(r - 1, a.H, BORDER), r,
+                         BORDER == RZ_BORDER_CLAMP ? min(r + 1, a.H - 1) : border_index(r + 1, a.H, BORDER)};
     const bool words_in = ((reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
                             static_cast<uintptr_t>(a.src_bstride)) & 3) == 0;
     // interior: the words read, [(s0 - 1) C - LEAD, + 4 NW), lie inside the row
@@ -276,7 +285,8 @@ __global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a,
                     wd[i] = 0;
 #pragma unroll
                 for (int i = 0; i < NB; i++) {
-                    const int col = clampi(s0 - 1 + i / C, 0, a.W - 1);
+                    const int col = BORDER == RZ_BORDER_CLAMP ? clampi(s0 - 1 + i / C, 0, a.W - 1)
+                                                              : border_index(s0 - 1 + i / C, a.W, BORDER);
                     wd[(LEAD + i) / 4] |= static_cast<uint32_t>(__ldg(row + col * C + i % C)) << (8 * ((LEAD + i) % 4));
                 }
             }
@@ -371,8 +381,8 @@ __global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a,
 // pixels l, l + 32, ...: one load instruction then reads the taps of 32
 // neighbouring pixels (a short stretch of the source row, few sectors even
 // for strong downscales), and each plane store writes 32 consecutive floats.
-// Taps and load rules as in k_direct.
-template <int C>
+// Taps, border rules and load rules as in k_direct.
+template <int C, bool WRAP>
 __global__ void __launch_bounds__(kDirectThreads) k_direct_norm(const KArgs a, const __grid_constant__ CUtensorMap)
 {
     constexpr int RUN = kNormRun;
@@ -395,7 +405,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_norm(const KArgs a, c
         xw[k] = e.y;
     }
     const int2 ye = __ldg(a.yt + dy);
-    const int r0 = ye.x, r1 = min(ye.x + 1, a.H - 1);
+    const int r0 = ye.x, r1 = far_tap<WRAP>(ye.x, a.H);
     const int B1 = ye.y, B0 = 2048 - B1;
     const bool words_in = ((reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
                             static_cast<uintptr_t>(a.src_bstride)) & 3) == 0;
@@ -413,7 +423,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_norm(const KArgs a, c
                 hsum_u8<C>(top, o0, aw, hT);
                 hsum_u8<C>(bot, o0, aw, hB);
             } else {
-                const int o1 = min(xs[k] + 1, a.W - 1) * C;
+                const int o1 = far_tap<WRAP>(xs[k], a.W) * C;
 #pragma unroll
                 for (int c = 0; c < C; c++) {
                     hT[c] = (2048 - xw[k]) * __ldg(top + o0 + c) + xw[k] * __ldg(top + o1 + c);
@@ -548,14 +558,281 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_rows(const KArgs a, c
     }
 }
 
+// Bytes o0 .. o0 + 7 of a row as one 64-bit value (byte o0 lowest), from the
+// three aligned 32-bit words that hold them.  The row base is 4-byte aligned
+// and o0 + 12 <= the row's bytes, so every word read lies inside the row.
+__device__ __forceinline__ uint64_t load_8_bytes(const uint8_t *row, int o0)
+{
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (o0 & ~3));
+    const uint32_t w0 = __ldg(w), w1 = __ldg(w + 1), w2 = __ldg(w + 2);
+    const uint32_t sh = 8u * static_cast<uint32_t>(o0 & 3);
+    return static_cast<uint64_t>(__funnelshift_r(w1, w2, sh)) << 32 | __funnelshift_r(w0, w1, sh);
+}
+
+// BT.601 luma of one pixel, rounded half-up exactly: floor((299 R + 587 G +
+// 114 B + 500) / 1000) (the sum is below 2^18).
+__device__ __forceinline__ int gray_of(uint32_t r, uint32_t g, uint32_t b)
+{
+    return static_cast<int>((299u * r + 587u * g + 114u * b + 500u) / 1000u);
+}
+
+// Gray of pixel p (0 or 1) of a pair of C-channel pixels packed in v.
+template <int C>
+__device__ __forceinline__ int gray_in(uint64_t v, int p, int ir, int ib)
+{
+    const int base = 8 * p * C;
+    return gray_of(static_cast<uint32_t>(v >> (base + 8 * ir)) & 255u, static_cast<uint32_t>(v >> (base + 8)) & 255u,
+                   static_cast<uint32_t>(v >> (base + 8 * ib)) & 255u);
+}
+
+template <int C>
+__device__ __forceinline__ int gray_at(const uint8_t *row, int x, int ir, int ib)
+{
+    const uint8_t *px = row + x * C;
+    return gray_of(__ldg(px + ir), __ldg(px + 1), __ldg(px + ib));
+}
+
+// Grayscale conversion fused before the uint8 resize (OpenCV object-tracking
+// page §3.1.1: cvtColor to gray, then resize).  Each tap pixel's gray value
+// (BT.601, rounded half-up) is formed from its C = 3 or 4 channels (R, G, B
+// or B, G, R; a fourth is ignored), then the exact bilinear sum of k_direct
+// (or the nearest tap) is taken over the gray values, so the result equals
+// resizing the converted image.  A thread takes four consecutive output
+// pixels; a tap pair's 2 C bytes come from three aligned words where the
+// row allows (as in k_direct), from bytes otherwise; the four gray outputs
+// leave as one 32-bit word when aligned.
+template <int C, int LINEAR, bool WRAP>
+__global__ void __launch_bounds__(kDirectThreads) k_direct_gray(const KArgs a, const __grid_constant__ CUtensorMap)
+{
+    constexpr int RUN = 4;
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int gpr = (a.OW + RUN - 1) / RUN;
+    const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
+    if (idx >= a.OH * gpr)
+        return;
+    const int dy = idx / gpr, x0 = (idx - dy * gpr) * RUN;
+    const int npx = min(RUN, a.OW - x0);
+    const int row_bytes = a.W * C;
+    const int ir = a.bgr ? 2 : 0, ib = a.bgr ? 0 : 2;
+    const int4 xa = __ldg(reinterpret_cast<const int4 *>(a.xt + x0));
+    const int4 xb = __ldg(reinterpret_cast<const int4 *>(a.xt + x0 + 2));
+    const int xs[RUN] = {xa.x, xa.z, xb.x, xb.z};
+    const int xw[RUN] = {xa.y, xa.w, xb.y, xb.w};
+    const int2 ye = __ldg(a.yt + dy);
+    const int r0 = ye.x, r1 = LINEAR ? far_tap<WRAP>(ye.x, a.H) : ye.x;
+    const int B1 = ye.y, B0 = 2048 - B1;
+    const bool words_in = ((reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
+                            static_cast<uintptr_t>(a.src_bstride)) & 3) == 0;
+    for (int b = blockIdx.y; b < a.batch; b += gridDim.y) {
+        const uint8_t *img = a.src + (long long)b * a.src_bstride;
+        const uint8_t *top = img + (long long)r0 * a.src_pitch;
+        const uint8_t *bot = img + (long long)r1 * a.src_pitch;
+        int q[RUN];
+#pragma unroll
+        for (int k = 0; k < RUN; k++) {
+            if (k >= npx) {
+                q[k] = 0;
+            } else if (!LINEAR) {
+                q[k] = gray_at<C>(top, xs[k], ir, ib);
+            } else {
+                const int o0 = xs[k] * C;
+                int t0, t1, b0, b1;
+                if (words_in && o0 + 12 <= row_bytes) {   // far tap inside: xs <= W - 2
+                    const uint64_t vt = load_8_bytes(top, o0), vb = load_8_bytes(bot, o0);
+                    t0 = gray_in<C>(vt, 0, ir, ib);
+                    t1 = gray_in<C>(vt, 1, ir, ib);
+                    b0 = gray_in<C>(vb, 0, ir, ib);
+                    b1 = gray_in<C>(vb, 1, ir, ib);
+                } else {
+                    const int x1 = far_tap<WRAP>(xs[k], a.W);
+                    t0 = gray_at<C>(top, xs[k], ir, ib);
+                    t1 = gray_at<C>(top, x1, ir, ib);
+                    b0 = gray_at<C>(bot, xs[k], ir, ib);
+                    b1 = gray_at<C>(bot, x1, ir, ib);
+                }
+                const int A1 = xw[k], A0 = 2048 - A1;
+                q[k] = (B0 * (A0 * t0 + A1 * t1) + B1 * (A0 * b0 + A1 * b1) + (1 << 21)) >> 22;
+            }
+        }
+        uint8_t *op = a.dst + (long long)b * a.dst_bstride + (long long)dy * a.dst_pitch + x0;
+        if (npx == RUN && (reinterpret_cast<uintptr_t>(op) & 3) == 0) {
+            __stcs(reinterpret_cast<uint32_t *>(op), pack4(q[0], q[1], q[2], q[3]));
+        } else {
+#pragma unroll
+            for (int k = 0; k < RUN; k++)
+                if (k < npx)
+                    op[k] = static_cast<uint8_t>(q[k]);
+        }
+    }
+}
+
+// Gray of pixel p of a run of C-channel pixels held in words (byte e of the
+// run at bits 8 (e % 4) of word e / 4); p, C and the order compile-time.
+template <int C, bool BGR>
+__device__ __forceinline__ int gray_word_px(const uint32_t *w, int p)
+{
+    constexpr int IR = BGR ? 2 : 0, IB = BGR ? 0 : 2;
+    const int er = p * C + IR, eg = p * C + 1, eb = p * C + IB;
+    return gray_of((w[er >> 2] >> (8 * (er & 3))) & 255u, (w[eg >> 2] >> (8 * (eg & 3))) & 255u,
+                   (w[eb >> 2] >> (8 * (eb & 3))) & 255u);
+}
+
+// Grayscale conversion fused before an exact 2x downscale (W = 2 OW,
+// H = 2 OH): bilinear (rounded mean of the 2 x 2 gray values, the exact sum
+// at weights 1024) or nearest (the upper-left gray value).  A thread takes
+// four output pixels: eight source pixels of each of its two rows in one
+// 24- or 32-byte run (three 8-byte or two 16-byte streaming loads), and
+// stores the four gray bytes as one word.  Requirements, checked by the host:
+// source base, pitch and batch stride multiples of 8 bytes (C = 3) or 16
+// (C = 4); output ones multiples of 4.
+template <int C, int LINEAR, bool BGR>
+__global__ void __launch_bounds__(kDirectThreads) k_down2_gray(const KArgs a, const __grid_constant__ CUtensorMap)
+{
+    constexpr int PX = 4, SB = 2 * PX * C, NW = SB / 4;
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int full = a.OW / PX;
+    const int gpr = full + (a.OW % PX ? 1 : 0);
+    const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
+    if (idx >= a.OH * gpr)
+        return;
+    const int dy = idx / gpr, j = idx - dy * gpr;
+    for (int b = blockIdx.y; b < a.batch; b += gridDim.y) {
+        const uint8_t *top = a.src + (long long)b * a.src_bstride + (long long)(2 * dy) * a.src_pitch;
+        const uint8_t *bot = top + a.src_pitch;
+        uint8_t *out = a.dst + (long long)b * a.dst_bstride + (long long)dy * a.dst_pitch;
+        if (j < full) {
+            uint32_t tw[NW], bw[NW];
+            if constexpr (C == 3) {
+                const uint2 *tp = reinterpret_cast<const uint2 *>(top + SB * j);
+                const uint2 *bp = reinterpret_cast<const uint2 *>(bot + SB * j);
+#pragma unroll
+                for (int k = 0; k < 3; k++) {
+                    const uint2 t = __ldcs(tp + k);
+                    tw[2 * k] = t.x; tw[2 * k + 1] = t.y;
+                    if (LINEAR) {
+                        const uint2 u = __ldcs(bp + k);
+                        bw[2 * k] = u.x; bw[2 * k + 1] = u.y;
+                    }
+                }
+            } else {
+                const uint4 *tp = reinterpret_cast<const uint4 *>(top + SB * j);
+                const uint4 *bp = reinterpret_cast<const uint4 *>(bot + SB * j);
+#pragma unroll
+                for (int k = 0; k < 2; k++) {
+                    const uint4 t = __ldcs(tp + k);
+                    tw[4 * k] = t.x; tw[4 * k + 1] = t.y; tw[4 * k + 2] = t.z; tw[4 * k + 3] = t.w;
+                    if (LINEAR) {
+                        const uint4 u = __ldcs(bp + k);
+                        bw[4 * k] = u.x; bw[4 * k + 1] = u.y; bw[4 * k + 2] = u.z; bw[4 * k + 3] = u.w;
+                    }
+                }
+            }
+            int q[PX];
+#pragma unroll
+            for (int k = 0; k < PX; k++) {
+                q[k] = gray_word_px<C, BGR>(tw, 2 * k);
+                if (LINEAR)
+                    q[k] = (q[k] + gray_word_px<C, BGR>(tw, 2 * k + 1) + gray_word_px<C, BGR>(bw, 2 * k) +
+                            gray_word_px<C, BGR>(bw, 2 * k + 1) + 2) >> 2;
+            }
+            __stcs(reinterpret_cast<uint32_t *>(out + PX * j), pack4(q[0], q[1], q[2], q[3]));
+        } else {
+            // the row's last pixels, fewer than a group: byte by byte
+            constexpr int IR = BGR ? 2 : 0, IB = BGR ? 0 : 2;
+            for (int p = full * PX; p < a.OW; p++) {
+                int g = gray_at<C>(top, 2 * p, IR, IB);
+                if (LINEAR)
+                    g = (g + gray_at<C>(top, 2 * p + 1, IR, IB) + gray_at<C>(bot, 2 * p, IR, IB) +
+                         gray_at<C>(bot, 2 * p + 1, IR, IB) + 2) >> 2;
+                out[p] = static_cast<uint8_t>(g);
+            }
+        }
+    }
+}
+
+// float32 bilinear, a thread per output pixel (all C channels): the lerp form
+// h = t0 + u (t1 - t0) on both rows, then the same across rows with v, with
+// the tables' float weights (CUDA interpolation page §2.2).  Used for plans
+// whose border rule is wrap (WRAP: the far tap past the last sample is
+// sample 0); clamp and mirror are in the tables alone.
+template <int C, bool WRAP>
+__global__ void __launch_bounds__(kDirectThreads) k_direct_f32(const KArgs a, const __grid_constant__ CUtensorMap)
+{
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const long long idx = static_cast<long long>(blockIdx.x) * kDirectThreads + threadIdx.x;
+    if (idx >= static_cast<long long>(a.OH) * a.OW)
+        return;
+    const int dy = static_cast<int>(idx / a.OW), dx = static_cast<int>(idx - static_cast<long long>(dy) * a.OW);
+    const int2 xe = __ldg(a.xt + dx), ye = __ldg(a.yt + dy);
+    const float u = __int_as_float(xe.y), v = __int_as_float(ye.y);
+    const int c0 = xe.x * C, c1 = far_tap<WRAP>(xe.x, a.W) * C;
+    const int y1 = far_tap<WRAP>(ye.x, a.H);
+    for (int b = blockIdx.y; b < a.batch; b += gridDim.y) {
+        const uint8_t *img = a.src + (long long)b * a.src_bstride;
+        const float *top = reinterpret_cast<const float *>(img + (long long)ye.x * a.src_pitch);
+        const float *bot = reinterpret_cast<const float *>(img + (long long)y1 * a.src_pitch);
+        float *op = reinterpret_cast<float *>(a.dst + (long long)b * a.dst_bstride + (long long)dy * a.dst_pitch) +
+                    static_cast<long long>(dx) * C;
+#pragma unroll
+        for (int c = 0; c < C; c++) {
+            const float t0 = __ldg(top + c0 + c), t1 = __ldg(top + c1 + c);
+            const float b0 = __ldg(bot + c0 + c), b1 = __ldg(bot + c1 + c);
+            const float h0 = fmaf(u, t1 - t0, t0), h1 = fmaf(u, b1 - b0, b0);
+            __stcs(op + c, fmaf(v, h1 - h0, h0));
+        }
+    }
+}
+
 }  // namespace
 
-const void *direct_up2_kernel_for(int C)
+const void *direct_gray_kernel_for(int mode, int C, bool wrap)
 {
     using Fn = void (*)(const KArgs, const CUtensorMap);
-    static const Fn k[3] = {k_up2_direct<1>, k_up2_direct<3>, k_up2_direct<4>};
+    static const Fn k[2][2][2] = {{{k_direct_gray<3, 0, false>, k_direct_gray<4, 0, false>},
+                                   {k_direct_gray<3, 0, false>, k_direct_gray<4, 0, false>}},
+                                  {{k_direct_gray<3, 1, false>, k_direct_gray<4, 1, false>},
+                                   {k_direct_gray<3, 1, true>, k_direct_gray<4, 1, true>}}};
+    if (C != 3 && C != 4)
+        return nullptr;
+    const int m = mode == RZ_LINEAR ? 1 : 0;
+    return reinterpret_cast<const void *>(k[m][wrap ? 1 : 0][C == 4 ? 1 : 0]);
+}
+
+const void *direct_down2_gray_kernel_for(int mode, int C, bool bgr)
+{
+    using Fn = void (*)(const KArgs, const CUtensorMap);
+    static const Fn k[2][2][2] = {{{k_down2_gray<3, 0, false>, k_down2_gray<3, 0, true>},
+                                   {k_down2_gray<4, 0, false>, k_down2_gray<4, 0, true>}},
+                                  {{k_down2_gray<3, 1, false>, k_down2_gray<3, 1, true>},
+                                   {k_down2_gray<4, 1, false>, k_down2_gray<4, 1, true>}}};
+    if (C != 3 && C != 4)
+        return nullptr;
+    return reinterpret_cast<const void *>(k[mode == RZ_LINEAR ? 1 : 0][C == 4 ? 1 : 0][bgr ? 1 : 0]);
+}
+
+const void *direct_f32_kernel_for(int C, bool wrap)
+{
+    using Fn = void (*)(const KArgs, const CUtensorMap);
+    static const Fn k[2][3] = {{k_direct_f32<1, false>, k_direct_f32<3, false>, k_direct_f32<4, false>},
+                               {k_direct_f32<1, true>, k_direct_f32<3, true>, k_direct_f32<4, true>}};
     const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
-    return ci < 0 ? nullptr : reinterpret_cast<const void *>(k[ci]);
+    return ci < 0 ? nullptr : reinterpret_cast<const void *>(k[wrap ? 1 : 0][ci]);
+}
+
+const void *direct_up2_kernel_for(int C, int border)
+{
+    using Fn = void (*)(const KArgs, const CUtensorMap);
+    static const Fn k[3][3] = {
+        {k_up2_direct<1, RZ_BORDER_CLAMP>, k_up2_direct<3, RZ_BORDER_CLAMP>, k_up2_direct<4, RZ_BORDER_CLAMP>},
+        {k_up2_direct<1, RZ_BORDER_MIRROR>, k_up2_direct<3, RZ_BORDER_MIRROR>, k_up2_direct<4, RZ_BORDER_MIRROR>},
+        {k_up2_direct<1, RZ_BORDER_WRAP>, k_up2_direct<3, RZ_BORDER_WRAP>, k_up2_direct<4, RZ_BORDER_WRAP>}};
+    const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
+    if (ci < 0 || border < 0 || border > 2)
+        return nullptr;
+    return reinterpret_cast<const void *>(k[border][ci]);
 }
 
 const void *direct_rows_kernel_for(int C)
@@ -567,19 +844,22 @@ const void *direct_rows_kernel_for(int C)
 }
 
 // Any ratio: op DIRECT_U8 (bilinear or nearest) or DIRECT_NORM (bilinear).
-const void *direct_kernel_for(int op, int mode, int C)
+// Nearest taps are always inside, so the wrap form exists for bilinear only.
+const void *direct_kernel_for(int op, int mode, int C, bool wrap)
 {
     using Fn = void (*)(const KArgs, const CUtensorMap);
-    static const Fn u8[2][3] = {{k_direct<1, 0>, k_direct<3, 0>, k_direct<4, 0>},
-                                {k_direct<1, 1>, k_direct<3, 1>, k_direct<4, 1>}};
-    static const Fn norm[3] = {k_direct_norm<1>, k_direct_norm<3>, k_direct_norm<4>};
+    static const Fn u8[3][3] = {{k_direct<1, 0, false>, k_direct<3, 0, false>, k_direct<4, 0, false>},
+                                {k_direct<1, 1, false>, k_direct<3, 1, false>, k_direct<4, 1, false>},
+                                {k_direct<1, 1, true>, k_direct<3, 1, true>, k_direct<4, 1, true>}};
+    static const Fn norm[2][3] = {{k_direct_norm<1, false>, k_direct_norm<3, false>, k_direct_norm<4, false>},
+                                  {k_direct_norm<1, true>, k_direct_norm<3, true>, k_direct_norm<4, true>}};
     const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
     if (ci < 0)
         return nullptr;
     const int m = mode == RZ_LINEAR ? 1 : 0;
     if (op == DIRECT_NORM)
-        return m ? reinterpret_cast<const void *>(norm[ci]) : nullptr;
-    return reinterpret_cast<const void *>(u8[m][ci]);
+        return m ? reinterpret_cast<const void *>(norm[wrap ? 1 : 0][ci]) : nullptr;
+    return reinterpret_cast<const void *>(u8[m ? (wrap ? 2 : 1) : 0][ci]);
 }
 
 const void *direct_down2_kernel_for(int mode, int C)

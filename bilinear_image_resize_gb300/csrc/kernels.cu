@@ -96,10 +96,10 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *pl, int
     const int nrc = g.dy1 - g.dy0;   // output rows of the tile
     int xv = 0;
     if (lane < 2)
-        xv = sample_index<LINEAR>(a.W, a.OW, lane == 0 ? g.dx0 : g.dx1 - 1);
+        xv = sample_index<LINEAR>(a.W, a.OW, lane == 0 ? g.dx0 : g.dx1 - 1, a.border);
     int yv = 0;
     if (lane < nrc)
-        yv = sample_index<LINEAR>(a.H, a.OH, g.dy0 + lane);
+        yv = sample_index<LINEAR>(a.H, a.OH, g.dy0 + lane, a.border);
     const int xs0 = __shfl_sync(0xffffffffu, xv, 0);
     const int xs1r = __shfl_sync(0xffffffffu, xv, 1);
     const int xs1 = LINEAR ? min(xs1r + 1, a.W - 1) : xs1r;
@@ -125,7 +125,7 @@ __device__ void plan_stage(const KArgs &a, const SmemLayout &L, uint8_t *pl, int
         const bool act = k < nrc;
         int r0 = 0x7fffffff, r1 = 0x7fffffff;
         if (act) {
-            r0 = k < 32 ? yv : sample_index<LINEAR>(a.H, a.OH, g.dy0 + k);
+            r0 = k < 32 ? yv : sample_index<LINEAR>(a.H, a.OH, g.dy0 + k, a.border);
             r1 = LINEAR ? min(r0 + 1, a.H - 1) : r0;
         }
         int prev_r1 = __shfl_up_sync(0xffffffffu, r1, 1);

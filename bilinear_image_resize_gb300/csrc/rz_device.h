@@ -189,6 +189,29 @@ __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.p
 
 __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
+// Index k in [-1, n] of an axis of n samples mapped inside by the border
+// rule (CUDA interpolation page §6.1): clamp repeats the edge sample, mirror
+// reflects about it (-1 -> 1, n -> n - 2), wrap repeats the axis (-1 -> n - 1,
+// n -> 0); a one-sample axis reads sample 0.  Indices further out map to a
+// sample inside (callers use them for no output).  Under clamp this is
+// clampi(k, 0, n - 1).
+__device__ __forceinline__ int border_index(int k, int n, int border)
+{
+    if (k < 0)
+        return border == RZ_BORDER_WRAP ? n - 1 : (border == RZ_BORDER_MIRROR ? min(1, n - 1) : 0);
+    if (k >= n)
+        return border == RZ_BORDER_WRAP ? 0 : (border == RZ_BORDER_MIRROR ? max(n - 2, 0) : n - 1);
+    return k;
+}
+
+// The far tap of a bilinear pair whose near tap is k (0 <= k < n): k + 1,
+// or past the last sample sample 0 under the wrap rule, else the last.
+template <bool WRAP>
+__device__ __forceinline__ int far_tap(int k, int n)
+{
+    return k + 1 < n ? k + 1 : (WRAP ? 0 : n - 1);
+}
+
 __device__ __forceinline__ int ceil_log2(int v) { return v <= 1 ? 0 : 32 - __clz(v - 1); }
 
 // floor(num / den) for 0 < den <= 2^17 and |num / den| < 2^17 + 1, exactly:
@@ -208,17 +231,24 @@ __device__ __forceinline__ int floor_div_exact(long long num, int den)
 
 // Source row/column sampled by output index d, exactly as the plan's tables
 // hold it: bilinear floor(((2d+1) n_in - n_out) / (2 n_out)) folded into
-// [0, n_in - 1]; nearest floor(d n_in / n_out) kept below n_in.  The
-// producer needs only these indices (not the weights) to stage a tile, so it
-// derives them without touching global memory.
+// [0, n_in - 1], where under the mirror rule an entry at the last sample with
+// a far tap of non-zero weight is held as the pair (n_in - 2, n_in - 1);
+// nearest floor(d n_in / n_out) kept below n_in.  (Wrap plans never reach
+// the kernels that call this.)  The producer needs only these indices (not
+// the weights) to stage a tile, so it derives them without touching global
+// memory.
 template <int LINEAR>
-__device__ __forceinline__ int sample_index(int n_in, int n_out, int d)
+__device__ __forceinline__ int sample_index(int n_in, int n_out, int d, int border)
 {
     int s;
-    if (LINEAR)
-        s = floor_div_exact((2LL * d + 1) * n_in - n_out, 2 * n_out);
-    else
+    if (LINEAR) {
+        const long long num = (2LL * d + 1) * n_in - n_out;
+        s = floor_div_exact(num, 2 * n_out);
+        if (s >= n_in - 1 && border == RZ_BORDER_MIRROR && n_in > 1 && num != static_cast<long long>(s) * 2 * n_out)
+            return n_in - 2;
+    } else {
         s = floor_div_exact(static_cast<long long>(d) * n_in, n_out);
+    }
     return s < 0 ? 0 : (s > n_in - 1 ? n_in - 1 : s);
 }
 

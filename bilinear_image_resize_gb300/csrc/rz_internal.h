@@ -17,16 +17,17 @@ constexpr int kMaxSmem = 227 * 1024;    // opt-in dynamic shared memory per CTA 
 constexpr int kMaxStages = 4;           // staged-tile ring depth limit
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded mbarrier waits: 1 s
 
-// Kernel families.  The numbering matches resize_plan_set_tile's `kind`.
-enum Family { FAM_U8 = 0, FAM_F32 = 1, FAM_NORM = 3, FAM_FILT = 4, FAM_COUNT = 5 };
+// Kernel families.  The numbering matches resize_plan_set_tile's `kind`
+// (the gray family runs on direct-load kernels only and takes no tile).
+enum Family { FAM_U8 = 0, FAM_F32 = 1, FAM_NORM = 3, FAM_FILT = 4, FAM_GRAY = 5, FAM_COUNT = 6 };
 
 // Compute variants of the uint8 bilinear family.
 enum Variant { VAR_GENERIC = 0, VAR_DOWN2 = 1 };
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ constexpr int fam_in_es(int fam) { return (fam == FAM_U8 || fam == FAM_NORM) ? 1 : 4; }
-__host__ __device__ constexpr int fam_out_es(int fam) { return fam == FAM_U8 ? 1 : 4; }
+__host__ __device__ constexpr int fam_in_es(int fam) { return (fam == FAM_U8 || fam == FAM_NORM || fam == FAM_GRAY) ? 1 : 4; }
+__host__ __device__ constexpr int fam_out_es(int fam) { return (fam == FAM_U8 || fam == FAM_GRAY) ? 1 : 4; }
 __host__ __device__ constexpr int fam_halo(int fam) { return fam == FAM_FILT ? 1 : 0; }
 // Families whose producer also stages the tile's sampling-table entries.
 __host__ __device__ constexpr bool fam_tables_in_stage(int fam) { return fam == FAM_NORM; }
@@ -143,6 +144,8 @@ struct KArgs {
     const int2 *xt;         // per output column {source column, weight}; kTabPad clamped entries either side
     const int2 *yt;         // per output row    {source row, weight}; kTabPad clamped entries either side
     int *status;            // device status word (RZ_OK or RZ_ERR_TIMEOUT)
+    int border;             // RZ_BORDER_*: the plan's rule for taps outside the source
+    int bgr;                // gray epilogue: channels in B, G, R order
     float scale[4], shift[4];  // normalise epilogue: y = q * scale[c] + shift[c]
     float w[9];                // 3x3 epilogue weights, row-major
 };
@@ -182,11 +185,19 @@ const void *direct_down2_kernel_for(int mode, int C);
 enum DirectOp { DIRECT_U8 = 0, DIRECT_NORM = 1 };
 constexpr int kDirectRun = 4;   // output pixels per thread
 constexpr int kNormRun = 1;     // normalise: output pixels per lane (interleaved by 32)
-const void *direct_kernel_for(int op, int mode, int C);
+// WRAP: the plan's border rule is RZ_BORDER_WRAP (a far tap past the last
+// sample reads sample 0).
+const void *direct_kernel_for(int op, int mode, int C, bool wrap = false);
+// Grayscale conversion then uint8 resize, C = 3 or 4 source channels; the
+// exact 2x downscale form (four outputs per thread, vector loads).
+const void *direct_gray_kernel_for(int mode, int C, bool wrap);
+const void *direct_down2_gray_kernel_for(int mode, int C, bool bgr);
+// float32 bilinear, a thread per output pixel (used for WRAP plans).
+const void *direct_f32_kernel_for(int C, bool wrap);
 // The exact 2x uint8 bilinear upscale (thread per 4 source columns of a
 // source row: 8 x 2 outputs); nullptr if none.
 constexpr int kUp2Cols = 4;
-const void *direct_up2_kernel_for(int C);
+const void *direct_up2_kernel_for(int C, int border);
 // uint8 bilinear with each thread walking a.TR output rows (vertical
 // upscales); nullptr if none.
 const void *direct_rows_kernel_for(int C);

@@ -73,6 +73,14 @@ extern "C" {
 
 #define RZ_EPI_NORMALIZE_NCHW 1
 #define RZ_EPI_FILTER3X3 2
+#define RZ_EPI_GRAY_RGB 3
+#define RZ_EPI_GRAY_BGR 4
+
+/* Border rules for taps outside the source (CUDA interpolation page §6.1). */
+#define RZ_BORDER_CLAMP 0   /* the edge sample repeats                          */
+#define RZ_BORDER_MIRROR 1  /* reflection about the edge samples: index -1 reads
+                               sample 1, index n reads sample n-2              */
+#define RZ_BORDER_WRAP 2    /* the image repeats: index -1 reads n-1, n reads 0 */
 
 #define RZ_OK 0
 #define RZ_ERR_ARG 1          /* bad pointer, size, pitch, mode or overlap     */
@@ -109,6 +117,26 @@ typedef struct rz_plan_s *rz_plan;
  * stream).  On success *out receives the plan; on failure *out is NULL.
  */
 RZ_API int resize_plan_create(rz_plan *out, int in_h, int in_w, int out_h, int out_w, int mode, void *stream);
+
+/*
+ * resize_plan_create with a border rule for bilinear taps outside the source
+ * (RZ_BORDER_CLAMP, RZ_BORDER_MIRROR or RZ_BORDER_WRAP; CUDA interpolation
+ * page §6.1).  Each tap's integer index is mapped by the rule; the weights
+ * stay those of the unmapped position.  Only upscaled axes sample outside
+ * (the sampled position lies in [-1/2, n - 1/2]), so the rule changes
+ * nothing on downscales, and nothing for RZ_NEAREST (indices are always
+ * inside).  A one-sample axis reads its sample under every rule.
+ *
+ * Table forms (resize_axis_table_border): under MIRROR the two taps stay
+ * adjacent, so an edge column is stored as that adjacent pair (xofs 0 or
+ * n - 2, a1 = 2048 - the unmapped a1, u = 1 - the unmapped u); under WRAP an
+ * edge column is stored as xofs = n - 1 with its unmapped weight and the far
+ * tap is index 0.  WRAP plans run on the direct-load kernels only: the 3x3
+ * filter epilogue, and RZ_OPT_U8_KERNEL values 1 and 2, return
+ * RZ_ERR_UNSUPPORTED for them.
+ */
+RZ_API int resize_plan_create_border(rz_plan *out, int in_h, int in_w, int out_h, int out_w, int mode, int border,
+                                     void *stream);
 
 /* Free a plan (NULL is accepted).  Synchronises the device first so that no
  * queued kernel still reads the tables. */
@@ -176,6 +204,16 @@ RZ_API int resize_f32_batch(rz_plan p, const float *src, size_t src_pitch, size_
  *   bilinear result on the output grid and clamp keeps rows in [0, out_h-1]
  *   and columns in [0, out_w-1] (replicate border).  Each channel is filtered
  *   on its own.  Batch as above (plane layout is HWC here).
+ * RZ_EPI_GRAY_RGB / RZ_EPI_GRAY_BGR: src uint8 HWC with C = 3 or 4 channels
+ *   (R, G, B in that order, or B, G, R; a fourth channel is ignored), dst
+ *   uint8 single-channel (dst_pitch >= out_w).  The conversion to grayscale
+ *   that precedes the resize in OpenCV's detection preprocessing ("Performance
+ *   Optimization of Object Tracking Algorithms in OpenCV on GPUs", §3.1.1):
+ *   each source pixel's gray value Y = floor((299 R + 587 G + 114 B + 500) /
+ *   1000), i.e. the BT.601 weights 0.299, 0.587, 0.114 rounded half-up
+ *   exactly, then the uint8 resize of the gray image (bilinear or nearest,
+ *   the plan's mode and border), so the result equals resize_u8 of the
+ *   converted image bit for bit.  Batch as above.
  *
  * batch >= 0 (0 is a no-op); batch strides are bytes and must keep the frames
  * from overlapping when batch > 1.
@@ -191,10 +229,10 @@ typedef struct {
 } rz_epilogue;
 
 /*
- * Bilinear resize with an epilogue.  src_dtype is RZ_U8 for
- * RZ_EPI_NORMALIZE_NCHW and RZ_F32 for RZ_EPI_FILTER3X3; mode must be
- * RZ_LINEAR.  Other arguments as resize_u8/resize_f32.  std[c] must be
- * non-zero and finite.
+ * Resize with an epilogue.  src_dtype is RZ_U8 for RZ_EPI_NORMALIZE_NCHW and
+ * the gray kinds, RZ_F32 for RZ_EPI_FILTER3X3; mode must be RZ_LINEAR except
+ * for the gray kinds (either mode).  Other arguments as resize_u8/resize_f32.
+ * std[c] must be non-zero and finite.
  */
 RZ_API int resize_fused(rz_plan p, const void *src, int src_dtype, size_t src_pitch, void *dst, size_t dst_pitch,
                  int H, int W, int C, int out_h, int out_w, int mode, const rz_epilogue *e, void *stream);
@@ -221,6 +259,11 @@ RZ_API int resize_u8_host(rz_plan p, const uint8_t *host_src, size_t host_src_pi
  */
 RZ_API int resize_axis_table(int n_in, int n_out, int mode, int32_t *ofs, int32_t *w_q11, float *u);
 
+/* resize_axis_table under a border rule (the table forms described at
+ * resize_plan_create_border). */
+RZ_API int resize_axis_table_border(int n_in, int n_out, int mode, int border, int32_t *ofs, int32_t *w_q11,
+                                    float *u);
+
 /*
  * Self-test of the bounded waits the staged and streaming kernels use on
  * their shared-memory barriers: launches one CTA whose thread waits on a
@@ -241,7 +284,7 @@ RZ_API int resize_last_cuda_error(void);
 /*
  * Tile override for tuning (0 = automatic): output rows and output columns
  * per CTA for kernel family `kind` (RZ_U8, RZ_F32, or 2 + RZ_EPI_* for the
- * fused kernels) of this plan.  Results do not depend on it; only speed does.
+ * normalise and 3x3 kernels) of this plan.  Results do not depend on it; only speed does.
  * For the streaming kernels (the 3x3 filter family, uint8 bilinear upscales)
  * a tile is one streamed unit: tile_rows output rows of a strip of tile_cols
  * output columns (at most the kernel's widest strip).  A tile that does not

@@ -44,6 +44,9 @@ def _load():
     lib.oracle_linear_u8.restype = None
     lib.oracle_linear_u8_rows.argtypes = [_p, _i64, _int, _int, _int, _p, _i64, _int, _int, _int, _int]
     lib.oracle_linear_u8_rows.restype = None
+    lib.oracle_linear_u8_border_rows.argtypes = [_p, _i64, _int, _int, _int, _p, _i64, _int, _int, _int, _int,
+                                                 _int]
+    lib.oracle_linear_u8_border_rows.restype = None
     lib.oracle_linear_f32.argtypes = [_p, _i64, _int, _int, _int, _p, _int, _int, _int]
     lib.oracle_linear_f32.restype = None
     lib.oracle_gray_u8.argtypes = [_p, _i64, _int, _int, _int, _int, _p, _i64]
@@ -108,15 +111,17 @@ def linear_u8(src: np.ndarray, out_h: int, out_w: int, border: int = BORDER_CLAM
     return dst
 
 
-def linear_u8_rows(src: np.ndarray, out_h: int, out_w: int, dy0: int, dy1: int) -> np.ndarray:
+def linear_u8_rows(src: np.ndarray, out_h: int, out_w: int, dy0: int, dy1: int,
+                   border: int = BORDER_CLAMP) -> np.ndarray:
     """Output rows [dy0, dy1) of the u8 bilinear resize to (out_h, out_w); shape (dy1-dy0, out_w, C)."""
     s = _as_hwc(np.asarray(src))
-    assert s.dtype == np.uint8 and 0 <= dy0 <= dy1 <= out_h
+    assert s.dtype == np.uint8 and 0 <= dy0 <= dy1 <= out_h and border in (0, 1, 2)
     H, W, C = s.shape
     full = np.empty((dy1 - dy0, out_w, C), np.uint8)
     # rows dy0.. land at the start of `full`: shift the destination base back by dy0 rows
     base = full.ctypes.data - dy0 * full.strides[0]
-    _load().oracle_linear_u8_rows(_ptr(s), s.strides[0], H, W, C, base, full.strides[0], out_h, out_w, dy0, dy1)
+    _load().oracle_linear_u8_border_rows(_ptr(s), s.strides[0], H, W, C, base, full.strides[0], out_h, out_w,
+                                         border, dy0, dy1)
     return full
 
 

@@ -90,12 +90,68 @@ def test_nearest_tables_match_floor(lib, geom):
     np.testing.assert_array_equal(ofs, expect)
 
 
+def effective_taps(n_in, ofs, w, border):
+    """{source index: 11-bit weight} an entry reads, as the kernels read it:
+    taps ofs and ofs + 1 (the far tap clamped, or sample 0 under wrap)."""
+    far = ofs + 1 if ofs + 1 < n_in else (0 if border == 2 else n_in - 1)
+    taps = {}
+    for k, wt in ((ofs, 2048 - w), (far, w)):
+        if wt:
+            taps[k] = taps.get(k, 0) + wt
+    return taps
+
+
+@pytest.mark.parametrize("border", [0, 1, 2])
+@pytest.mark.parametrize("geom", GEOMS + [(2, 2), (2, 7), (5, 23), (2, 4096)])
+def test_border_tables_read_the_oracle_taps(lib, geom, border):
+    # every entry, read as the kernels read it, puts the weights of the
+    # oracle's definition (taps i and i + 1 mapped by the border rule, 11-bit
+    # weights of the unmapped position) on the same source samples
+    import bilinear_image_resize_gb300 as rz
+    import oracle
+    n_in, n_out = geom
+    if n_out > 1200:
+        n_out_check = list(range(0, 40)) + list(range(n_out - 40, n_out))
+    else:
+        n_out_check = range(n_out)
+    ofs, q, u = rz.resize_axis_table_border(n_in, n_out, rz.RZ_LINEAR, border)
+    assert np.all((q >= 0) & (q <= 2048)) and np.all((ofs >= 0) & (ofs <= n_in - 1))
+    for d in n_out_check:
+        i, r, den = oracle.linear_coord(n_in, n_out, d)
+        a1 = oracle.weight_q11(r, den)
+        want = {}
+        for k, wt in ((oracle.border_index(i, n_in, border), 2048 - a1),
+                      (oracle.border_index(i + 1, n_in, border), a1)):
+            if wt:
+                want[k] = want.get(k, 0) + wt
+        assert effective_taps(n_in, int(ofs[d]), int(q[d]), border) == want, (d, ofs[d], q[d])
+        # the float weight puts 1 - u and u on the same taps, within a rounding
+        fw = float(u[d])
+        far = int(ofs[d]) + 1 if ofs[d] + 1 < n_in else (0 if border == 2 else n_in - 1)
+        exact = {}
+        for k, wt in ((oracle.border_index(i, n_in, border), 1 - Fraction(r, den)),
+                      (oracle.border_index(i + 1, n_in, border), Fraction(r, den))):
+            exact[k] = exact.get(k, 0) + wt
+        got = {}
+        for k, wt in ((int(ofs[d]), 1 - fw), (far, fw)):
+            got[k] = got.get(k, 0) + wt
+        for k in set(exact) | set(got):
+            assert abs(float(exact.get(k, 0)) - got.get(k, 0)) < 1e-6
+    if border != 2:
+        assert np.all(np.diff(ofs) >= 0)        # spans stay monotone but under wrap
+    if border == 0:
+        np.testing.assert_array_equal(ofs, rz.resize_axis_table(n_in, n_out, rz.RZ_LINEAR)[0])
+
+
 def test_axis_table_rejects_bad_args(lib):
     assert lib.resize_axis_table(0, 5, 1, None, None, None) == 1
     assert lib.resize_axis_table(5, -1, 1, None, None, None) == 1
     assert lib.resize_axis_table(5, 5, 7, None, None, None) == 1
     assert lib.resize_axis_table(65537, 5, 1, None, None, None) == 1
     assert lib.resize_axis_table(5, 0, 1, None, None, None) == 0
+    assert lib.resize_axis_table_border(5, 5, 1, 3, None, None, None) == 1
+    assert lib.resize_axis_table_border(5, 5, 1, -1, None, None, None) == 1
+    assert lib.resize_axis_table_border(5, 9, 1, 2, None, None, None) == 0
 
 
 def test_calls_validate_before_cuda(lib):
@@ -106,6 +162,9 @@ def test_calls_validate_before_cuda(lib):
     assert h.value is None
     assert lib.resize_plan_create(ctypes.byref(h), 5, 5, 5, 5, 9, None) == RZ_ERR_ARG
     assert lib.resize_plan_create(None, 5, 5, 5, 5, 1, None) == RZ_ERR_ARG
+    assert lib.resize_plan_create_border(ctypes.byref(h), 5, 5, 5, 5, 1, 3, None) == RZ_ERR_ARG
+    assert lib.resize_plan_create_border(ctypes.byref(h), 5, 5, 5, 5, 1, -1, None) == RZ_ERR_ARG
+    assert h.value is None
     # null plan
     assert lib.resize_u8(None, 16, 3, 32, 3, 1, 1, 1, 1, 1, 1, None) == RZ_ERR_ARG
     assert lib.resize_f32(None, 16, 12, 32, 12, 1, 1, 3, 1, 1, 1, None) == RZ_ERR_ARG
