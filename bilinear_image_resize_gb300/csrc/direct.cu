@@ -576,13 +576,26 @@ __device__ __forceinline__ int gray_of(uint32_t r, uint32_t g, uint32_t b)
     return static_cast<int>((299u * r + 587u * g + 114u * b + 500u) / 1000u);
 }
 
-// Gray of pixel p (0 or 1) of a pair of C-channel pixels packed in v.
-template <int C>
-__device__ __forceinline__ int gray_in(uint64_t v, int p, int ir, int ib)
+// The same for a pixel whose channels are bytes 0..2 of px (byte 3 ignored),
+// in two byte dot products: the weights split into high and low bytes (299 =
+// 256 + 43, 587 = 2 * 256 + 75, 114 = 114), so the sum is 256 dp4a(px, hi) +
+// dp4a(px, lo) + 500; floor(s / 1000) is the high word of s * 4294968,
+// exact for s < 6.1e6 (4294968 * 1000 - 2^32 = 704).  Weight words for R, G,
+// B in bytes 0, 1, 2; for B, G, R the byte order of each word reverses.
+constexpr uint32_t kGrayLoRGB = 43u | 75u << 8 | 114u << 16, kGrayHiRGB = 1u | 2u << 8;
+constexpr uint32_t kGrayLoBGR = 114u | 75u << 8 | 43u << 16, kGrayHiBGR = 2u << 8 | 1u << 16;
+__device__ __forceinline__ int gray_dp4a(uint32_t px, uint32_t lo, uint32_t hi)
 {
-    const int base = 8 * p * C;
-    return gray_of(static_cast<uint32_t>(v >> (base + 8 * ir)) & 255u, static_cast<uint32_t>(v >> (base + 8)) & 255u,
-                   static_cast<uint32_t>(v >> (base + 8 * ib)) & 255u);
+    const uint32_t s = __dp4a(px, hi, 0u) * 256u + __dp4a(px, lo, 500u);
+    return static_cast<int>(__umulhi(s, 4294968u));
+}
+
+// Gray of pixel p (0 or 1) of a pair of C-channel pixels packed in v (byte
+// 8 p C onwards), with the weight words of the channel order.
+template <int C>
+__device__ __forceinline__ int gray_in(uint64_t v, int p, uint32_t lo, uint32_t hi)
+{
+    return gray_dp4a(static_cast<uint32_t>(v >> (8 * p * C)), lo, hi);
 }
 
 template <int C>
@@ -615,6 +628,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_gray(const KArgs a, c
     const int npx = min(RUN, a.OW - x0);
     const int row_bytes = a.W * C;
     const int ir = a.bgr ? 2 : 0, ib = a.bgr ? 0 : 2;
+    const uint32_t wlo = a.bgr ? kGrayLoBGR : kGrayLoRGB, whi = a.bgr ? kGrayHiBGR : kGrayHiRGB;
     const int4 xa = __ldg(reinterpret_cast<const int4 *>(a.xt + x0));
     const int4 xb = __ldg(reinterpret_cast<const int4 *>(a.xt + x0 + 2));
     const int xs[RUN] = {xa.x, xa.z, xb.x, xb.z};
@@ -640,10 +654,10 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_gray(const KArgs a, c
                 int t0, t1, b0, b1;
                 if (words_in && o0 + 12 <= row_bytes) {   // far tap inside: xs <= W - 2
                     const uint64_t vt = load_8_bytes(top, o0), vb = load_8_bytes(bot, o0);
-                    t0 = gray_in<C>(vt, 0, ir, ib);
-                    t1 = gray_in<C>(vt, 1, ir, ib);
-                    b0 = gray_in<C>(vb, 0, ir, ib);
-                    b1 = gray_in<C>(vb, 1, ir, ib);
+                    t0 = gray_in<C>(vt, 0, wlo, whi);
+                    t1 = gray_in<C>(vt, 1, wlo, whi);
+                    b0 = gray_in<C>(vb, 0, wlo, whi);
+                    b1 = gray_in<C>(vb, 1, wlo, whi);
                 } else {
                     const int x1 = far_tap<WRAP>(xs[k], a.W);
                     t0 = gray_at<C>(top, xs[k], ir, ib);
@@ -667,15 +681,19 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_gray(const KArgs a, c
     }
 }
 
-// Gray of pixel p of a run of C-channel pixels held in words (byte e of the
-// run at bits 8 (e % 4) of word e / 4); p, C and the order compile-time.
-template <int C, bool BGR>
-__device__ __forceinline__ int gray_word_px(const uint32_t *w, int p)
+// Gray of pixel p of a run of NW words of C-channel pixels (byte e of the
+// run at bits 8 (e % 4) of word e / 4); p, C and the order compile-time.  A
+// three-channel pixel is gathered into one word by a byte permute.
+template <int C, bool BGR, int NW>
+__device__ __forceinline__ int gray_word_px(const uint32_t (&w)[NW], int p)
 {
-    constexpr int IR = BGR ? 2 : 0, IB = BGR ? 0 : 2;
-    const int er = p * C + IR, eg = p * C + 1, eb = p * C + IB;
-    return gray_of((w[er >> 2] >> (8 * (er & 3))) & 255u, (w[eg >> 2] >> (8 * (eg & 3))) & 255u,
-                   (w[eb >> 2] >> (8 * (eb & 3))) & 255u);
+    const int e = p * C, i = e >> 2, o = e & 3;
+    uint32_t px;
+    if (C == 4 || o == 0)
+        px = w[i];
+    else
+        px = __byte_perm(w[i], w[min(i + 1, NW - 1)], static_cast<uint32_t>(o | (o + 1) << 4 | (o + 2) << 8));
+    return BGR ? gray_dp4a(px, kGrayLoBGR, kGrayHiBGR) : gray_dp4a(px, kGrayLoRGB, kGrayHiRGB);
 }
 
 // Grayscale conversion fused before an exact 2x downscale (W = 2 OW,
@@ -732,10 +750,10 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_gray(const KArgs a, co
             int q[PX];
 #pragma unroll
             for (int k = 0; k < PX; k++) {
-                q[k] = gray_word_px<C, BGR>(tw, 2 * k);
+                q[k] = gray_word_px<C, BGR, NW>(tw, 2 * k);
                 if (LINEAR)
-                    q[k] = (q[k] + gray_word_px<C, BGR>(tw, 2 * k + 1) + gray_word_px<C, BGR>(bw, 2 * k) +
-                            gray_word_px<C, BGR>(bw, 2 * k + 1) + 2) >> 2;
+                    q[k] = (q[k] + gray_word_px<C, BGR, NW>(tw, 2 * k + 1) + gray_word_px<C, BGR, NW>(bw, 2 * k) +
+                            gray_word_px<C, BGR, NW>(bw, 2 * k + 1) + 2) >> 2;
             }
             __stcs(reinterpret_cast<uint32_t *>(out + PX * j), pack4(q[0], q[1], q[2], q[3]));
         } else {

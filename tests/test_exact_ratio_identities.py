@@ -55,3 +55,18 @@ def test_the_identities_fail_on_a_planted_error():
     t = img.astype(np.int64)
     wrong = ((t[0::2, 0::2][:4, :5] * 3 + t[1::2, 1::2][:4, :5] + 2) >> 2).astype(np.uint8)
     assert not np.array_equal(wrong, oracle.linear_u8(img, 4, 5)[:4, :5])
+
+
+def test_gray_split_weights_and_division_by_1000():
+    # the gray kernels form 299 R + 587 G + 114 B + 500 as
+    # 256 * (R + 2 G) + (43 R + 75 G + 114 B) + 500 (two byte dot products)
+    # and take floor(s / 1000) as the high word of s * 4294968, exact for
+    # every s the sum can reach (at most 255 * 1000 + 500); checked here
+    # over all inputs against the oracle's conversion
+    r, g, b = np.meshgrid(np.arange(256), np.arange(256), np.arange(256), indexing="ij")
+    s = 256 * (r + 2 * g) + (43 * r + 75 * g + 114 * b) + 500
+    y = (s.astype(np.uint64) * np.uint64(4294968)) >> np.uint64(32)
+    rgb = np.stack([r, g, b], -1).astype(np.uint8).reshape(4096, 4096, 3)
+    np.testing.assert_array_equal(y.reshape(4096, 4096).astype(np.uint8), oracle.gray_u8(rgb))
+    t = np.arange(0, 255501, dtype=np.uint64)
+    np.testing.assert_array_equal((t * np.uint64(4294968)) >> np.uint64(32), t // np.uint64(1000))
