@@ -51,6 +51,10 @@ def _load():
     lib.oracle_linear_f32.restype = None
     lib.oracle_gray_u8.argtypes = [_p, _i64, _int, _int, _int, _int, _p, _i64]
     lib.oracle_gray_u8.restype = None
+    lib.oracle_filter_valid.argtypes = [_p, _int, _int, _p, _int, _p]
+    lib.oracle_filter_valid.restype = None
+    lib.oracle_filter_centred.argtypes = [_p, _int, _int, _p, _int, _p]
+    lib.oracle_filter_centred.restype = None
     lib.oracle_nearest_f32.argtypes = [_p, _i64, _int, _int, _int, _p, _int, _int]
     lib.oracle_nearest_f32.restype = None
     lib.oracle_normalize_nchw.argtypes = [_p, _int, _int, _int, _p, _p, _p]
@@ -207,3 +211,39 @@ def gray_resize_u8(src: np.ndarray, out_h: int, out_w: int, linear: bool = True,
     if linear:
         return linear_u8(g, out_h, out_w, border)[:, :, 0]
     return nearest_u8(g, out_h, out_w)[:, :, 0]
+
+
+def filter_valid(img: np.ndarray, w) -> np.ndarray:
+    """K x K correlation over the valid region of a single-channel image, in
+    double; shape (H - K + 1, W - K + 1)."""
+    a = np.ascontiguousarray(np.asarray(img, np.float64))
+    if a.ndim == 3:
+        assert a.shape[2] == 1
+        a = np.ascontiguousarray(a[:, :, 0])
+    wk = np.ascontiguousarray(np.asarray(w, np.float64))
+    K = wk.shape[0]
+    assert wk.shape == (K, K) and a.shape[0] >= K and a.shape[1] >= K
+    H, W = a.shape
+    out = np.empty((H - K + 1, W - K + 1), np.float64)
+    _load().oracle_filter_valid(_ptr(a), H, W, _ptr(wk), K, _ptr(out))
+    return out
+
+
+def filter_centred(r: np.ndarray, w) -> np.ndarray:
+    """Odd K x K replicate-border correlation of a single-channel image, in double."""
+    a = np.ascontiguousarray(np.asarray(r, np.float64))
+    if a.ndim == 3:
+        assert a.shape[2] == 1
+        a = np.ascontiguousarray(a[:, :, 0])
+    wk = np.ascontiguousarray(np.asarray(w, np.float64))
+    K = wk.shape[0]
+    assert wk.shape == (K, K) and K % 2 == 1
+    OH, OW = a.shape
+    z = np.empty((OH, OW), np.float64)
+    _load().oracle_filter_centred(_ptr(a), OH, OW, _ptr(wk), K, _ptr(z))
+    return z
+
+
+def linear_f32_filter(src: np.ndarray, out_h: int, out_w: int, w, border: int = BORDER_CLAMP) -> np.ndarray:
+    """The fused K x K op's definition: filter_centred(linear_f32(src)), all in double."""
+    return filter_centred(linear_f32(src, out_h, out_w, border), w)

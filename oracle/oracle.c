@@ -305,3 +305,45 @@ void oracle_gray_u8(const uint8_t *src, int64_t src_pitch, int H, int W, int C, 
             dst[y * dst_pitch + x] = (uint8_t)((sum + 500) / 1000);
         }
 }
+
+/*
+ * K x K correlation over the valid region, [CONV] §2 (the filter placed with
+ * its first row and column on the output position, each covered input
+ * multiplied by its weight, the products summed; no flip):
+ *   out[y][x] = sum_{r, c in [0, K)} w[r * K + c] * in[y + r][x + c],
+ * 0 <= y <= H - K, 0 <= x <= W - K.  Single channel, dense, double.
+ */
+void oracle_filter_valid(const double *in, int H, int W, const double *w, int K, double *out)
+{
+    int64_t OH = H - K + 1, OW = W - K + 1;
+    for (int64_t y = 0; y < OH; y++)
+        for (int64_t x = 0; x < OW; x++) {
+            double sum = 0.0;
+            for (int64_t r = 0; r < K; r++)
+                for (int64_t c = 0; c < K; c++)
+                    sum += w[r * K + c] * in[(y + r) * W + (x + c)];
+            out[y * OW + x] = sum;
+        }
+}
+
+/*
+ * K x K correlation (K odd) centred on each pixel of a single-channel image
+ * r (OH x OW), rows and columns outside replaced by the nearest edge
+ * row/column: the 3x3 rule of oracle_filter3x3 for any odd K,
+ *   z[y][x] = sum_{a,b in [-K/2, K/2]} w[(a+K/2)*K + (b+K/2)] r[clamp(y+a)][clamp(x+b)].
+ */
+void oracle_filter_centred(const double *r, int OH, int OW, const double *w, int K, double *z)
+{
+    int64_t R = K / 2;
+    for (int64_t y = 0; y < OH; y++)
+        for (int64_t x = 0; x < OW; x++) {
+            double sum = 0.0;
+            for (int64_t a = -R; a <= R; a++)
+                for (int64_t b = -R; b <= R; b++) {
+                    int64_t yy = clamp_index(y + a, OH);
+                    int64_t xx = clamp_index(x + b, OW);
+                    sum += w[(a + R) * K + (b + R)] * r[yy * OW + xx];
+                }
+            z[y * OW + x] = sum;
+        }
+}
