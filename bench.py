@@ -62,8 +62,23 @@ WORKLOADS = {
     "1080p_to_4k_wrap": ("1080p->4K RGB u8 bilinear upscale, wrap border", "u8", 1080, 1920, 2160, 3840, 3,
                          "linear", 1),
 }
+for _k in (5, 7):
+    WORKLOADS[f"f32_8192_to_5980_filter{_k}x{_k}"] = (
+        f"f32 8192x8192 -> 5980x5980 bilinear + {_k}x{_k} filter", "filt", 8192, 8192, 5980, 5980, 1, "linear", 1)
+for _k in (8, 16, 32, 64):
+    WORKLOADS[f"f32_4096_valid_filter{_k}"] = (
+        f"f32 4096x4096 {_k}x{_k} correlation over the valid region (standalone)", "valid", 4096, 4096,
+        4097 - _k, 4097 - _k, 1, "none", 1)
 # border rule of a workload's plan (RZ_BORDER_*; clamp when absent)
 WORKLOAD_BORDER = {"1080p_to_4k_mirror": 1, "1080p_to_4k_wrap": 2}
+# filter width of the filter workloads (3 when absent)
+WORKLOAD_FILTER_K = {f"f32_8192_to_5980_filter{k}x{k}": k for k in (5, 7)}
+WORKLOAD_FILTER_K.update({f"f32_4096_valid_filter{k}": k for k in (8, 16, 32, 64)})
+
+
+def fp32_fma_peak_tflops(sm_mhz=2070.0, sms=152):
+    """FP32 peak from unit counts and clocks: sms x 128 FMA lanes x 2 FLOP x clock."""
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
 DEFAULT_WORKLOAD = "4k_to_1080p"
 METRIC = "output Gpix/s and achieved HBM GB/s (% of GB300 peak), 4K->1080p RGB u8 bilinear"
 
@@ -222,11 +237,14 @@ def make_outputs(kind, OH, OW, C, batch, count, dev):
     return [torch.empty(shape, dtype=dt, device=dev) for _ in range(count)]
 
 
-def make_epi(rz, synth, kind):
+def make_epi(rz, synth, kind, workload=""):
     """The fused epilogue of a workload kind (None for the plain uint8 resize)."""
     if kind == "norm":
         return rz.make_epilogue(rz.RZ_EPI_NORMALIZE_NCHW, mean=synth.NORM_MEAN, std=synth.NORM_STD)
     if kind == "filt":
+        K = WORKLOAD_FILTER_K.get(workload, 3)
+        if K != 3:
+            return rz.make_epilogue(rz.RZ_EPI_FILTER, wk=synth.filter_weights_k(K))
         return rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=synth.filter_weights())
     if kind == "gray":
         return rz.make_epilogue(rz.RZ_EPI_GRAY_RGB)
@@ -270,7 +288,7 @@ def gpu_arm(args, rank, local_rank, world):
         rz.resize_plan_set_option(plan, rz.RZ_OPT_PDL, 0)
     if args.u8_kernel:
         rz.resize_plan_set_option(plan, rz.RZ_OPT_U8_KERNEL, args.u8_kernel)
-    epi = make_epi(rz, synth, kind)
+    epi = make_epi(rz, synth, kind, args.workload)
 
     def step(i):
         s, d = frames[i % ring], outs[i % ring]
@@ -400,6 +418,73 @@ def gpu_arm(args, rank, local_rank, world):
     }
     plan.destroy()
     return res
+
+
+def valid_arm(args, local_rank):
+    """The standalone K x K correlation (filter2d_valid_f32): graph-replayed
+    launches over a ring of inputs larger than L2, event-timed on the
+    launching stream, FLOPs = 2 K^2 per output."""
+    import torch
+
+    import bilinear_image_resize_gb300 as rz
+    from bilinear_image_resize_gb300 import synth
+    desc, kind, H, W, OH, OW, C, _m, batch = WORKLOADS[args.workload]
+    K = WORKLOAD_FILTER_K[args.workload]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    ring = max(2, int(3 * L2_BYTES // (4 * (H * W + OH * OW))) + 1)
+    base = torch.from_numpy(synth.float_gray(W, H, 5)).to(dev)
+    srcs = [base if i == 0 else torch.roll(base, 3 * i, 1) for i in range(ring)]
+    dsts = [torch.empty((OH, OW), dtype=torch.float32, device=dev) for _ in range(ring)]
+    wt = torch.from_numpy(synth.filter_weights_k(K)).to(dev)
+
+    def step(i):
+        rz.filter2d_valid_f32(srcs[i % ring], wt, dsts[i % ring], stream=stream)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize()
+    G = max(1, min(ring * max(1, 24 // ring), args.steps))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(G):
+            step(i)
+    ref0 = dsts[0].clone()
+    with torch.cuda.stream(stream):
+        dsts[0].zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    if not torch.equal(dsts[0], ref0):
+        raise RuntimeError("captured graph did not reproduce the eager result")
+    reps = max(1, args.steps // G)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    ms = ev0.elapsed_time(ev1)
+    time.sleep(0.1)
+    sampler.stop()
+    clocks = sampler.summary(t0 - 0.02, t1 + 0.02)
+    n = reps * G
+    launch_s = ms / 1e3 / n
+    tflops = 2.0 * K * K * OH * OW / launch_s / 1e12
+    peak = fp32_fma_peak_tflops(clocks["sm_max_mhz"] or 2070.0)
+    return {"steps": n, "ms": ms, "launch_ms": launch_s * 1e3, "tflops": tflops, "peak": peak, "clocks": clocks,
+            "value": OH * OW / launch_s / 1e9, "desc": desc, "K": K, "ring": ring, "graph_steps": G}
 
 
 def copy_ceiling(step_bytes, ring, stream, dev, reps=8):
@@ -534,23 +619,38 @@ def oracle_rate(workload, budget_s):
 
         def run(rows):
             return oracle.linear_u8_normalize(frames[0], OH, OW, synth.NORM_MEAN, synth.NORM_STD)
-    else:
+    elif kind == "valid":
         img = synth.float_gray(W, H, 5)
-        w = synth.filter_weights()
+        wk = synth.filter_weights_k(WORKLOAD_FILTER_K[workload])
+        K = wk.shape[0]
 
         def run(rows):
-            return oracle.linear_f32_filter3x3(img, OH, OW, w)
+            # output rows [0, rows) need input rows [0, rows + K - 1)
+            return oracle.filter_valid(img[:rows + K - 1], wk)
+    else:
+        img = synth.float_gray(W, H, 5)
+        K = WORKLOAD_FILTER_K.get(workload, 3)
+        w = synth.filter_weights() if K == 3 else synth.filter_weights_k(K)
+
+        def run(rows):
+            if K == 3:
+                return oracle.linear_f32_filter3x3(img, OH, OW, w)
+            return oracle.linear_f32_filter(img, OH, OW, w)
     t0 = time.perf_counter()
     run(min(OH, 8))
     probe = time.perf_counter() - t0
     rows_full = OH if (kind == "u8" and mode == "linear") else None
+    if kind == "valid":
+        # a band of output rows sized by the probe so the sample fits the budget
+        per_row = max(probe / 8, 1e-6)
+        rows_full = int(max(1, min(OH, budget_s / 3 / per_row)))
     n_px = 0
     calls = 0
     t0 = time.perf_counter()
     while True:
         if rows_full:
             run(rows_full)
-            n_px += OH * OW
+            n_px += rows_full * OW
         else:
             run(None)
             n_px += OH * OW
@@ -623,7 +723,7 @@ def profile_run(args):
     frames = make_frames(kind, H, W, C, batch, ring, dev)
     outs = make_outputs(kind, OH, OW, C, batch, ring, dev)
     plan = rz.resize_plan_create(H, W, OH, OW, mode, border=WORKLOAD_BORDER.get(args.workload, 0))
-    epi = make_epi(rz, synth, kind)
+    epi = make_epi(rz, synth, kind, args.workload)
     nf = args.batch_frames if (kind == "u8" and args.profile_batched) else 0
     if nf:
         # two batches of nf frames in rotation, one resize_u8_batch launch each
@@ -685,6 +785,29 @@ def main():
 
     import __graft_entry__
     __graft_entry__.build()
+
+    if WORKLOADS[args.workload][1] == "valid":
+        r = valid_arm(args, local_rank)
+        if rank == 0:
+            v, calls, dt, _ = oracle_rate(args.workload, args.cpu_budget)
+            line = {
+                "metric": f"output Gpix/s and FP32 TFLOP/s, {r['desc']}", "value": r["value"], "unit": "Gpix/s",
+                "n_gpus": world, "steps": r["steps"], "warmup": args.warmup, "ms_per_step": r["launch_ms"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic",
+                "config": {"workload": r["desc"], "l2": f"ring of {r['ring']} input/output sets > 3x L2",
+                           "launch": f"CUDA graphs of {r['graph_steps']} filter2d_valid_f32 launches, one stream",
+                           "flops_per_step": 2 * r["K"] ** 2 * WORKLOADS[args.workload][4] ** 2},
+                "roofline": {"bound": "alu", "achieved": r["tflops"], "peak": r["peak"], "unit": "TFLOP/s",
+                             "frac": r["tflops"] / r["peak"],
+                             "peak_source": "derived: 152 SMs x 128 FP32 FMA lanes x 2 FLOP x max SM clock",
+                             "traffic": None},
+                "cpu_baseline": {"value": v, "unit": "Gpix/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"{calls} bands of output rows in {dt:.1f} s, single-threaded C oracle"},
+                "e2e": None, "gpu_launches": r["steps"], "clocks": r["clocks"],
+            }
+            print(json.dumps(line), flush=True)
+        return
 
     r = gpu_arm(args, rank, local_rank, world)
 

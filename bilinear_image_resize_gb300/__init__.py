@@ -15,10 +15,10 @@ import ctypes
 
 from . import _native
 from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_BORDER_CLAMP, RZ_BORDER_MIRROR,
-                      RZ_BORDER_WRAP, RZ_EPI_FILTER3X3, RZ_EPI_GRAY_BGR, RZ_EPI_GRAY_RGB, RZ_EPI_NORMALIZE_NCHW, RZ_ERR_ARG, RZ_ERR_CUDA, RZ_ERR_NOMEM, RZ_ERR_TIMEOUT,
+                      RZ_BORDER_WRAP, RZ_EPI_FILTER, RZ_EPI_FILTER3X3, RZ_EPI_GRAY_BGR, RZ_EPI_GRAY_RGB, RZ_EPI_NORMALIZE_NCHW, RZ_ERR_ARG, RZ_ERR_CUDA, RZ_ERR_NOMEM, RZ_ERR_TIMEOUT,
                       RZ_ERR_UNSUPPORTED, RZ_F32, RZ_LINEAR, RZ_MAX_DIM, RZ_NEAREST, RZ_NOALLOC_MAX_DIM, RZ_OK,
                       RZ_OPT_CTAS_PER_SM, RZ_OPT_GENERIC_ONLY, RZ_OPT_GRID_MODE, RZ_OPT_PDL, RZ_OPT_RING_ROWS,
-                      RZ_OPT_STAGES, RZ_OPT_U8_KERNEL, RZ_U8, RzEpilogue)
+                      RZ_OPT_FILTER_KERNEL, RZ_OPT_STAGES, RZ_OPT_U8_KERNEL, RZ_U8, RzEpilogue)
 
 __all__ = [
     "ResizeError", "Plan", "resize_plan_create", "resize_plan_destroy", "resize_plan_status",
@@ -28,7 +28,8 @@ __all__ = [
     "RZ_NOALLOC_MAX_DIM",
     "RZ_LINEAR", "RZ_NEAREST", "RZ_U8", "RZ_F32", "RZ_EPI_NORMALIZE_NCHW", "RZ_EPI_FILTER3X3",
     "RZ_EPI_GRAY_RGB", "RZ_EPI_GRAY_BGR", "RZ_BORDER_CLAMP", "RZ_BORDER_MIRROR", "RZ_BORDER_WRAP",
-    "resize_plan_create_border", "resize_axis_table_border",
+    "resize_plan_create_border", "resize_axis_table_border", "RZ_EPI_FILTER", "RZ_OPT_FILTER_KERNEL",
+    "filter2d_valid_f32",
     "RZ_OK", "RZ_ERR_ARG", "RZ_ERR_UNSUPPORTED", "RZ_ERR_CUDA", "RZ_ERR_NOMEM", "RZ_ERR_TIMEOUT",
     "RZ_MAX_DIM", "KIND_U8", "KIND_F32", "KIND_NORMALIZE", "KIND_FILTER3X3",
     "RZ_OPT_STAGES", "RZ_OPT_GENERIC_ONLY", "RZ_OPT_CTAS_PER_SM", "RZ_OPT_GRID_MODE", "RZ_OPT_PDL",
@@ -134,7 +135,7 @@ def _hwc(t, name):
             raise ValueError(f"{name}: columns must be contiguous")
     elif t.dim() == 3:
         H, W, C = t.shape
-        if t.stride(2) != 1 or t.stride(1) != C:
+        if (C > 1 and t.stride(2) != 1) or t.stride(1) != C:
             raise ValueError(f"{name}: pixels must be packed (stride(1) == C, stride(2) == 1)")
     else:
         raise ValueError(f"{name}: expected HxW or HxWxC, got shape {tuple(t.shape)}")
@@ -178,7 +179,7 @@ def _nhwc(t, name):
     if t.dim() != 4:
         raise ValueError(f"{name}: expected NxHxWxC, got shape {tuple(t.shape)}")
     N, H, W, C = t.shape
-    if t.stride(3) != 1 or t.stride(2) != C:
+    if (C > 1 and t.stride(3) != 1) or t.stride(2) != C:
         raise ValueError(f"{name}: pixels must be packed (stride(2) == C, stride(3) == 1)")
     es = t.element_size()
     return N, H, W, C, t.stride(1) * es, t.stride(0) * es
@@ -211,7 +212,8 @@ def resize_wait_selftest(dev_status, limit_us: int, stream=None) -> None:
 
 
 def make_epilogue(kind: int, batch: int = 1, src_batch_stride: int = 0, dst_batch_stride: int = 0,
-                  mean=(0.0, 0.0, 0.0, 0.0), std=(1.0, 1.0, 1.0, 1.0), w3x3=None) -> RzEpilogue:
+                  mean=(0.0, 0.0, 0.0, 0.0), std=(1.0, 1.0, 1.0, 1.0), w3x3=None, wk=None) -> RzEpilogue:
+    """An rz_epilogue; wk is a K x K weight array (odd K <= 7) for RZ_EPI_FILTER."""
     e = RzEpilogue()
     e.kind, e.batch = kind, batch
     e.src_batch_stride, e.dst_batch_stride = src_batch_stride, dst_batch_stride
@@ -221,6 +223,14 @@ def make_epilogue(kind: int, batch: int = 1, src_batch_stride: int = 0, dst_batc
     if w3x3 is not None:
         for i in range(9):
             e.w3x3[i] = float(w3x3[i])
+    if wk is not None:
+        rows = [list(r) for r in wk]
+        e.ksize = len(rows)
+        flat = [float(v) for r in rows for v in r]
+        if len(flat) != e.ksize * e.ksize or e.ksize > 7:
+            raise ValueError("wk must be a square array of at most 7 x 7 weights")
+        for i, v in enumerate(flat):
+            e.wk[i] = v
     return e
 
 
@@ -259,7 +269,7 @@ def resize_fused(plan: Plan, src, dst, epilogue: RzEpilogue, stream=None) -> Non
         dtype_code = RZ_U8
         if s.dtype != torch.uint8 or d.dtype != torch.float32:
             raise ValueError("normalise epilogue takes uint8 src and float32 dst")
-    elif e.kind == RZ_EPI_FILTER3X3:
+    elif e.kind in (RZ_EPI_FILTER3X3, RZ_EPI_FILTER):
         if not batched and src.dim() == 2:
             s = src.unsqueeze(0).unsqueeze(-1)
             d = dst.unsqueeze(0).unsqueeze(-1)
@@ -275,7 +285,7 @@ def resize_fused(plan: Plan, src, dst, epilogue: RzEpilogue, stream=None) -> Non
     Nb, H, W, Cs = s.shape
     if Nb != N or Cs != C:
         raise ValueError("src and dst batch or channel counts differ")
-    if s.stride(3) != 1 or s.stride(2) != C:
+    if (C > 1 and s.stride(3) != 1) or s.stride(2) != C:
         raise ValueError("src pixels must be packed")
     e.batch = N
     e.src_batch_stride = s.stride(0) * s.element_size()
@@ -283,6 +293,23 @@ def resize_fused(plan: Plan, src, dst, epilogue: RzEpilogue, stream=None) -> Non
     _check(_native.load().resize_fused(plan.handle, s.data_ptr(), dtype_code, s.stride(1) * s.element_size(),
                                        d.data_ptr(), dp, H, W, C, OH, OW, mode, ctypes.byref(e),
                                        _stream(stream)), "resize_fused")
+
+
+def filter2d_valid_f32(src, weights, dst, stream=None) -> None:
+    """dst[:] = the K x K correlation of src over its valid region.
+
+    src: float32 CUDA tensor (H, W) with contiguous rows; weights: float32
+    CUDA tensor (K, K); dst: float32 CUDA tensor (H - K + 1, W - K + 1).
+    """
+    if src.dim() != 2 or dst.dim() != 2 or src.stride(1) != 1 or dst.stride(1) != 1:
+        raise ValueError("src and dst must be 2-D with contiguous rows")
+    K = weights.shape[0]
+    if weights.dim() != 2 or weights.shape[1] != K or not weights.is_contiguous():
+        raise ValueError("weights must be a contiguous K x K tensor")
+    H, W = src.shape
+    _check(_native.load().filter2d_valid_f32(src.data_ptr(), src.stride(0) * 4, H, W, weights.data_ptr(), K,
+                                             dst.data_ptr(), dst.stride(0) * 4, _stream(stream)),
+           "filter2d_valid_f32")
 
 
 def resize_u8_host(plan: Plan, host_src, host_dst, dev_src, dev_dst, stream=None) -> None:

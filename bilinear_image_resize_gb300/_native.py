@@ -18,6 +18,7 @@ RZ_EPI_NORMALIZE_NCHW = 1
 RZ_EPI_FILTER3X3 = 2
 RZ_EPI_GRAY_RGB = 3
 RZ_EPI_GRAY_BGR = 4
+RZ_EPI_FILTER = 5
 RZ_BORDER_CLAMP = 0
 RZ_BORDER_MIRROR = 1
 RZ_BORDER_WRAP = 2
@@ -37,6 +38,7 @@ RZ_OPT_GRID_MODE = 4
 RZ_OPT_PDL = 5
 RZ_OPT_RING_ROWS = 6
 RZ_OPT_U8_KERNEL = 7
+RZ_OPT_FILTER_KERNEL = 8
 
 # kernel families for resize_plan_set_tile
 KIND_U8 = 0
@@ -54,6 +56,8 @@ class RzEpilogue(ctypes.Structure):
         ("mean", ctypes.c_float * 4),
         ("std", ctypes.c_float * 4),
         ("w3x3", ctypes.c_float * 9),
+        ("ksize", ctypes.c_int),
+        ("wk", ctypes.c_float * 49),
     ]
 
 
@@ -76,6 +80,7 @@ SIGNATURES = {
     "resize_f32_batch": (_i, [_p, _p, _sz, _sz, _p, _sz, _sz, _i, _i, _i, _i, _i, _i, _i, _p]),
     "resize_fused": (_i, [_p, _p, _i, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, ctypes.POINTER(RzEpilogue), _p]),
     "resize_u8_host": (_i, [_p, _p, _sz, _p, _sz, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
+    "filter2d_valid_f32": (_i, [_p, _sz, _i, _i, _p, _i, _p, _sz, _p]),
     "resize_axis_table": (_i, [_i, _i, _i, _p, _p, _p]),
     "resize_axis_table_border": (_i, [_i, _i, _i, _i, _p, _p, _p]),
     "resize_strerror": (ctypes.c_char_p, [_i]),

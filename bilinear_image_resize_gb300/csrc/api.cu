@@ -148,6 +148,7 @@ struct rz_plan_s {
     int opt_pdl = 1;           // programmatic dependent launch
     int opt_ring_rows = 0;     // streaming kernels: source rows in the ring (0: automatic)
     int opt_u8_kernel = 0;     // uint8 bilinear: 0 automatic, 1 staged tiles, 2 streaming, 3 direct
+    int opt_filter_kernel = 0; // 3x3 epilogue: 0 automatic, 1 streaming, 2 tile kernel
 };
 
 namespace {
@@ -508,17 +509,39 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
     const int opt = p->opt_u8_kernel;
     const int C = a.C, batch = a.batch;
     const bool wrap = p->border == RZ_BORDER_WRAP && mode == RZ_LINEAR;
-    auto launch = [&](const void *fn, long long threads) {
+    auto launch_grid = [&](const void *fn, long long gx, int block) {
         *rc = RZ_OK;
         if (!do_launch) return true;
-        const int gx = static_cast<int>((threads + rz::kDirectThreads - 1) / rz::kDirectThreads);
         CUtensorMap none;
         std::memset(&none, 0, sizeof(none));
-        const int e = rz::launch_resize(fn, a, none, gx, 0, p->opt_pdl != 0, stream, rz::kDirectThreads,
+        const int e = rz::launch_resize(fn, a, none, static_cast<int>(gx), 0, p->opt_pdl != 0, stream, block,
                                         std::min(batch, 65535));
         if (e != 0) *rc = cuda_fail(static_cast<cudaError_t>(e));
         return true;
     };
+    auto launch = [&](const void *fn, long long threads) {
+        return launch_grid(fn, (threads + rz::kDirectThreads - 1) / rz::kDirectThreads, rz::kDirectThreads);
+    };
+    if (fam == rz::FAM_FILT) {
+        // K x K epilogue: the tile kernel (filter.cu) for K other than 3, for
+        // wrap plans, or when the option asks; else the streaming 3x3 kernel
+        const int fopt = p->opt_filter_kernel;
+        if (a.ksize == 3 && !wrap && fopt != 2) return false;
+        if (fopt == 1) {
+            *rc = RZ_ERR_UNSUPPORTED;
+            return true;
+        }
+        const void *ffn = rz::resize_filter_kernel_for(C, a.ksize, wrap);
+        if (!ffn) {
+            *rc = RZ_ERR_UNSUPPORTED;
+            return true;
+        }
+        a.xt = p->d_xf;
+        a.yt = p->d_yf;
+        const long long tiles = static_cast<long long>((a.OW + rz::kFTW - 1) / rz::kFTW) *
+                                ((a.OH + rz::kFTH - 1) / rz::kFTH);
+        return launch_grid(ffn, tiles, rz::kFilterThreads);
+    }
     if (fam == rz::FAM_GRAY) {
         // gray conversion then uint8 resize: a thread per four output pixels;
         // exact 2x downscales with vector loads where the layout allows
@@ -884,6 +907,10 @@ int resize_plan_set_option(rz_plan p, int option, int value)
         if (value < 0 || value > 3) return RZ_ERR_ARG;
         p->opt_u8_kernel = value;
         break;
+    case RZ_OPT_FILTER_KERNEL:
+        if (value < 0 || value > 2) return RZ_ERR_ARG;
+        p->opt_filter_kernel = value;
+        break;
     default:
         return RZ_ERR_ARG;
     }
@@ -958,12 +985,38 @@ int resize_fused(rz_plan p, const void *src, int src_dtype, size_t src_pitch, vo
     } else if (e->kind == RZ_EPI_FILTER3X3) {
         if (src_dtype != RZ_F32) return RZ_ERR_ARG;
         fam = rz::FAM_FILT;
+        extra.ksize = 3;
         for (int i = 0; i < 9; i++) extra.w[i] = e->w3x3[i];
+    } else if (e->kind == RZ_EPI_FILTER) {
+        if (src_dtype != RZ_F32 || e->ksize < 1 || e->ksize % 2 == 0) return RZ_ERR_ARG;
+        if (e->ksize > 7) return RZ_ERR_UNSUPPORTED;
+        fam = rz::FAM_FILT;
+        extra.ksize = e->ksize;
+        for (int i = 0; i < e->ksize * e->ksize; i++) extra.w[i] = e->wk[i];
     } else {
         return RZ_ERR_ARG;
     }
     return run(p, fam, src, src_pitch, e->src_batch_stride, dst, dst_pitch, e->dst_batch_stride, H, W, C, out_h,
                out_w, mode, e->batch, extra, stream);
+}
+
+int filter2d_valid_f32(const float *src, size_t src_pitch, int H, int W, const float *weights, int K, float *dst,
+                       size_t dst_pitch, void *stream)
+{
+    if (H < 0 || W < 0 || K < 1 || H > RZ_MAX_DIM || W > RZ_MAX_DIM) return RZ_ERR_ARG;
+    if (K > rz::kMaxFilterK) return RZ_ERR_UNSUPPORTED;
+    if (H < K || W < K) return RZ_OK;   // empty output
+    if (!src || !dst || !weights) return RZ_ERR_ARG;
+    const size_t in_row = static_cast<size_t>(W) * 4, out_row = static_cast<size_t>(W - K + 1) * 4;
+    if (src_pitch < in_row || dst_pitch < out_row || (src_pitch & 3) || (dst_pitch & 3) ||
+        (reinterpret_cast<uintptr_t>(src) & 3) || (reinterpret_cast<uintptr_t>(dst) & 3) ||
+        (reinterpret_cast<uintptr_t>(weights) & 3))
+        return RZ_ERR_ARG;
+    if (overlap(src, image_extent(H, src_pitch, in_row), dst, image_extent(H - K + 1, dst_pitch, out_row)))
+        return RZ_ERR_ARG;
+    const int e = rz::launch_filter_valid(src, static_cast<long long>(src_pitch), H, W, weights, K, dst,
+                                          static_cast<long long>(dst_pitch), true, stream);
+    return e != 0 ? cuda_fail(static_cast<cudaError_t>(e)) : RZ_OK;
 }
 
 int resize_u8_host(rz_plan p, const uint8_t *host_src, size_t host_src_pitch, uint8_t *host_dst, size_t host_dst_pitch,

@@ -147,7 +147,8 @@ struct KArgs {
     int border;             // RZ_BORDER_*: the plan's rule for taps outside the source
     int bgr;                // gray epilogue: channels in B, G, R order
     float scale[4], shift[4];  // normalise epilogue: y = q * scale[c] + shift[c]
-    float w[9];                // 3x3 epilogue weights, row-major
+    float w[49];               // K x K epilogue weights (K <= 7), row-major
+    int ksize;                 // K of the filter epilogue (3 for the 3x3 kind)
 };
 
 // Record a cudaError_t for resize_last_cuda_error (this host thread).
@@ -174,6 +175,23 @@ __host__ __device__ constexpr int down2_px(int C) { return C == 1 ? 8 : (C == 3 
 // One CTA waiting on a barrier nothing completes, at most limit_ns; writes
 // RZ_ERR_TIMEOUT to *status when the wait gives up.  Returns a cudaError_t.
 int launch_wait_selftest(int *status, unsigned long long limit_ns, void *stream);
+
+// K x K filters (filter.cu).  Fused: odd K <= 7 after the float32 bilinear
+// resize, output tiles of kFTW x kFTH with a K / 2 halo of resized values in
+// shared memory.  Standalone: the valid-region correlation, 1 <= K <= 64,
+// output tiles of kVTW x kVTH (a warp per two rows, eight columns a lane).
+constexpr int kFilterThreads = 256;
+constexpr int kFTW = 64, kFTH = 32;
+constexpr int kVTW = 256, kVTH = 16;
+constexpr int kMaxFilterK = 64;
+__host__ __device__ constexpr int filter_valid_row_floats(int K) { return kVTW + ((K + 7) & ~7) + 8; }
+__host__ __device__ constexpr int filter_valid_smem(int K)
+{
+    return 4 * ((kVTH + K - 1) * filter_valid_row_floats(K) + K * ((K + 7) & ~7));
+}
+const void *resize_filter_kernel_for(int C, int K, bool wrap);
+int launch_filter_valid(const float *src, long long src_pitch, int H, int W, const float *w, int K, float *dst,
+                        long long dst_pitch, bool pdl, void *stream);
 
 // Direct-load kernels (direct.cu): a thread per output group, no staging.
 constexpr int kDirectThreads = 256;

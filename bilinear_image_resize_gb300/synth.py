@@ -81,6 +81,12 @@ def filter_weights(seed: int = 55) -> np.ndarray:
     return (w / w.sum()).astype(np.float32)
 
 
+def filter_weights_k(K: int, seed: int = 56) -> np.ndarray:
+    """K x K positive weights summing to 1 (float32), the K x K analogue of filter_weights."""
+    w = np.random.default_rng(seed + K).random((K, K))
+    return (w / w.sum()).astype(np.float32)
+
+
 def random_u8(shape, seed: int) -> np.ndarray:
     return np.random.default_rng(seed).integers(0, 256, size=shape, dtype=np.uint8)
 

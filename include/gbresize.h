@@ -75,6 +75,7 @@ extern "C" {
 #define RZ_EPI_FILTER3X3 2
 #define RZ_EPI_GRAY_RGB 3
 #define RZ_EPI_GRAY_BGR 4
+#define RZ_EPI_FILTER 5
 
 /* Border rules for taps outside the source (CUDA interpolation page §6.1). */
 #define RZ_BORDER_CLAMP 0   /* the edge sample repeats                          */
@@ -214,6 +215,11 @@ RZ_API int resize_f32_batch(rz_plan p, const float *src, size_t src_pitch, size_
  *   exactly, then the uint8 resize of the gray image (bilinear or nearest,
  *   the plan's mode and border), so the result equals resize_u8 of the
  *   converted image bit for bit.  Batch as above.
+ * RZ_EPI_FILTER: the 3x3 rule for any odd ksize K in 1..7: src and dst
+ *   float32 HWC, z = sum_{a,b in -K/2..K/2} wk[(a+K/2)*K + (b+K/2)] *
+ *   r[clamp(dy+a)][clamp(dx+b)], each channel on its own, replicate border
+ *   on the output grid.  K = 3 gives RZ_EPI_FILTER3X3's result.  Any border
+ *   rule of the plan (the 3x3 kind under RZ_BORDER_WRAP runs this form too).
  *
  * batch >= 0 (0 is a no-op); batch strides are bytes and must keep the frames
  * from overlapping when batch > 1.
@@ -226,16 +232,35 @@ typedef struct {
     float mean[4];
     float std[4];
     float w3x3[9];
+    int ksize;        /* RZ_EPI_FILTER: K (odd, 1..7) */
+    float wk[49];     /* RZ_EPI_FILTER: K x K weights, row-major */
 } rz_epilogue;
 
 /*
  * Resize with an epilogue.  src_dtype is RZ_U8 for RZ_EPI_NORMALIZE_NCHW and
- * the gray kinds, RZ_F32 for RZ_EPI_FILTER3X3; mode must be RZ_LINEAR except
+ * the gray kinds, RZ_F32 for RZ_EPI_FILTER3X3 and RZ_EPI_FILTER; mode must be RZ_LINEAR except
  * for the gray kinds (either mode).  Other arguments as resize_u8/resize_f32.
  * std[c] must be non-zero and finite.
  */
 RZ_API int resize_fused(rz_plan p, const void *src, int src_dtype, size_t src_pitch, void *dst, size_t dst_pitch,
                  int H, int W, int C, int out_h, int out_w, int mode, const rz_epilogue *e, void *stream);
+
+/*
+ * K x K correlation over the valid region ("OpenCL image convolution" §2):
+ *   dst[y][x] = sum_{r, c in [0, K)} w[r*K + c] * src[y + r][x + c]
+ * for 0 <= y <= H - K, 0 <= x <= W - K (the filter's first row and column on
+ * the output position; no flip).  float32, one channel; src and dst rows at
+ * byte pitches (multiples of 4, src_pitch >= W*4, dst_pitch >= (W-K+1)*4);
+ * weights: DEVICE pointer to K*K floats, row-major, read during the call's
+ * kernel.  1 <= K <= 64 (RZ_ERR_UNSUPPORTED above); H, W <= RZ_MAX_DIM.
+ * H < K or W < K gives an
+ * empty output (RZ_OK, nothing launched).  Asynchronous on `stream`; no
+ * allocation; src and dst must not overlap.  Results are float32 sums in an
+ * order of the kernel's choosing (within K*K float32 roundings of the exact
+ * sum).
+ */
+RZ_API int filter2d_valid_f32(const float *src, size_t src_pitch, int H, int W, const float *weights, int K,
+                              float *dst, size_t dst_pitch, void *stream);
 
 /*
  * End-to-end uint8 resize from HOST memory: copies the image from
@@ -329,7 +354,14 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  *                       case or the normalise epilogue); 3: direct loads
  *                       always (upscales with each thread walking output
  *                       rows, tile_rows of resize_plan_set_tile per thread).
- *                       Bit-exact whichever runs.
+ *                       Bit-exact whichever runs;
+ *   RZ_OPT_FILTER_KERNEL value 0 (automatic), 1 or 2: which kernel runs the
+ *                       3x3 filter epilogue (RZ_EPI_FILTER3X3, or
+ *                       RZ_EPI_FILTER with K = 3).  0: streaming, or the
+ *                       tile kernel under RZ_BORDER_WRAP; 1: streaming
+ *                       (RZ_ERR_UNSUPPORTED under wrap); 2: the tile kernel
+ *                       that serves the other K.  Equal within float32
+ *                       rounding.
  * Returns RZ_ERR_ARG for an unknown option or value.
  */
 #define RZ_OPT_STAGES 1
@@ -339,6 +371,7 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
 #define RZ_OPT_PDL 5
 #define RZ_OPT_RING_ROWS 6
 #define RZ_OPT_U8_KERNEL 7
+#define RZ_OPT_FILTER_KERNEL 8
 RZ_API int resize_plan_set_option(rz_plan p, int option, int value);
 
 /*

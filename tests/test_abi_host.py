@@ -40,10 +40,24 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(_native.SIGNATURES) == set(names)
 
 
-def test_epilogue_struct_layout_matches_header():
+def test_epilogue_struct_layout_matches_header(tmp_path):
+    # the binding's ctypes struct against the C compiler's layout of the header's
+    import shutil
+    import subprocess
     from bilinear_image_resize_gb300 import RzEpilogue
-    # int, int, size_t, size_t, float[4], float[4], float[9] on LP64
-    assert ctypes.sizeof(RzEpilogue) == 4 + 4 + 8 + 8 + 16 + 16 + 36 + 4  # trailing pad to 8
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f[0] for f in RzEpilogue._fields_]
+    prog = tmp_path / "layout.c"
+    prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gbresize.h"\nint main(void){'
+                    'printf("%zu", sizeof(rz_epilogue));' +
+                    "".join(f'printf(" %zu", offsetof(rz_epilogue, {n}));' for n in fields) + "return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(RzEpilogue)
+    assert got[1:] == [getattr(RzEpilogue, n).offset for n in fields]
 
 
 def exact_linear(n_in, n_out):

@@ -185,7 +185,7 @@ def test_normalize_border(rz, border, kernel):
         assert max_abs(got[n], want) <= F32_TOL
 
 
-def test_filter3x3_mirror_and_wrap_rejected(rz):
+def test_filter3x3_mirror_and_wrap(rz):
     H, W, OH, OW = 64, 80, 150, 170
     img = synth.random_f32((H, W), seed=9)
     w = synth.filter_weights()
@@ -196,7 +196,13 @@ def test_filter3x3_mirror_and_wrap_rejected(rz):
         torch.cuda.synchronize()
     want = oracle.filter3x3(oracle.linear_f32(img, OH, OW, MIRROR), w)
     assert max_abs(dst.cpu().numpy(), want) <= F32_TOL
+    # wrap: the tile kernel (the streaming one takes monotone tables only)
     with rz.resize_plan_create(H, W, OH, OW, rz.RZ_LINEAR, border=WRAP) as plan:
+        rz.resize_fused(plan, src, dst, rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=w))
+        torch.cuda.synchronize()
+        want = oracle.filter3x3(oracle.linear_f32(img, OH, OW, WRAP), w)
+        assert max_abs(dst.cpu().numpy(), want) <= F32_TOL
+        rz.resize_plan_set_option(plan, rz.RZ_OPT_FILTER_KERNEL, 1)
         with pytest.raises(rz.ResizeError) as ei:
             rz.resize_fused(plan, src, dst, rz.make_epilogue(rz.RZ_EPI_FILTER3X3, w3x3=w))
         assert ei.value.code == rz.RZ_ERR_UNSUPPORTED
