@@ -179,15 +179,17 @@ int launch_wait_selftest(int *status, unsigned long long limit_ns, void *stream)
 // K x K filters (filter.cu).  Fused: odd K <= 7 after the float32 bilinear
 // resize, output tiles of kFTW x kFTH with a K / 2 halo of resized values in
 // shared memory.  Standalone: the valid-region correlation, 1 <= K <= 64,
-// output tiles of kVTW x kVTH (a warp per two rows, eight columns a lane).
+// output tiles of kVTW columns by two rows per warp (eight columns a lane).
 constexpr int kFilterThreads = 256;
 constexpr int kFTW = 64, kFTH = 32;
-constexpr int kVTW = 256, kVTH = 16;
+constexpr int kVTW = 256;
 constexpr int kMaxFilterK = 64;
+__host__ __device__ constexpr int valid_threads(int K) { return K > 32 ? 512 : 256; }
+__host__ __device__ constexpr int valid_tile_rows(int threads) { return 2 * threads / 32; }
 __host__ __device__ constexpr int filter_valid_row_floats(int K) { return kVTW + ((K + 7) & ~7) + 8; }
-__host__ __device__ constexpr int filter_valid_smem(int K)
+__host__ __device__ constexpr int filter_valid_smem(int K, int threads)
 {
-    return 4 * ((kVTH + K - 1) * filter_valid_row_floats(K) + K * ((K + 7) & ~7));
+    return 4 * ((valid_tile_rows(threads) + K - 1) * filter_valid_row_floats(K) + K * ((K + 7) & ~7));
 }
 const void *resize_filter_kernel_for(int C, int K, bool wrap);
 int launch_filter_valid(const float *src, long long src_pitch, int H, int W, const float *w, int K, float *dst,
