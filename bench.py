@@ -70,6 +70,10 @@ for _k in (8, 16, 32, 64):
         f"f32 4096x4096 {_k}x{_k} correlation over the valid region (standalone)", "valid", 4096, 4096,
         4097 - _k, 4097 - _k, 1, "none", 1)
 # border rule of a workload's plan (RZ_BORDER_*; clamp when absent)
+WORKLOADS["4k_to_1080p_rgba"] = ("4K->1080p RGBA u8 bilinear (exact kernel)", "u8", 2160, 3840, 1080, 1920, 4,
+                                  "linear", 1)
+WORKLOADS["4k_to_1080p_rgba_texture"] = ("4K->1080p RGBA u8 bilinear through the texture unit (hardware filtering, "
+                                          "not bit-exact)", "tex", 2160, 3840, 1080, 1920, 4, "linear", 1)
 WORKLOAD_BORDER = {"1080p_to_4k_mirror": 1, "1080p_to_4k_wrap": 2}
 # filter width of the filter workloads (3 when absent)
 WORKLOAD_FILTER_K = {f"f32_8192_to_5980_filter{k}x{k}": k for k in (5, 7)}
@@ -108,7 +112,7 @@ def algorithmic_bytes(kind, H, W, OH, OW, C, mode, batch):
     if m == rz.RZ_LINEAR:
         rows |= set(min(int(r) + 1, H - 1) for r in yofs)
     in_es = 4 if kind == "filt" else 1
-    out_es = 1 if kind in ("u8", "gray") else 4
+    out_es = 1 if kind in ("u8", "gray", "tex") else 4
     read = len(rows) * W * C * in_es
     write = OH * OW * (1 if kind == "gray" else C) * out_es
     return batch * read, batch * write
@@ -207,7 +211,7 @@ def make_frames(kind, H, W, C, batch, count, dev):
     import torch
 
     from bilinear_image_resize_gb300 import synth
-    if kind in ("u8", "gray"):
+    if kind in ("u8", "gray", "tex"):
         base = synth.smooth_rgb(W, H, 3) if (C == 3 and W >= 1920) else synth.random_u8((H, W, C), seed=3)
         if base.shape != (H, W, C):
             base = synth.random_u8((H, W, C), seed=3)
@@ -226,7 +230,7 @@ def make_frames(kind, H, W, C, batch, count, dev):
 
 def make_outputs(kind, OH, OW, C, batch, count, dev):
     import torch
-    if kind == "u8":
+    if kind in ("u8", "tex"):
         shape, dt = (OH, OW, C), torch.uint8
     elif kind == "gray":
         shape, dt = (OH, OW), torch.uint8
@@ -289,11 +293,14 @@ def gpu_arm(args, rank, local_rank, world):
     if args.u8_kernel:
         rz.resize_plan_set_option(plan, rz.RZ_OPT_U8_KERNEL, args.u8_kernel)
     epi = make_epi(rz, synth, kind, args.workload)
+    textures = [rz.Texture(f) for f in frames] if kind == "tex" else None
 
     def step(i):
         s, d = frames[i % ring], outs[i % ring]
         if kind == "u8":
             rz.resize_u8(plan, s, d, stream=stream)
+        elif kind == "tex":
+            textures[i % ring].resize(d, stream=stream)
         else:
             rz.resize_fused(plan, s, d, epi, stream=stream)
 
@@ -321,6 +328,8 @@ def gpu_arm(args, rank, local_rank, world):
     with torch.cuda.stream(stream):
         if kind == "u8":
             rz.resize_u8(plan, frames[0], ref0, stream=stream)
+        elif kind == "tex":
+            textures[0].resize(ref0, stream=stream)
         else:
             rz.resize_fused(plan, frames[0], ref0, epi, stream=stream)
         outs[0].zero_()
@@ -416,6 +425,8 @@ def gpu_arm(args, rank, local_rank, world):
         "read_bytes": rd, "write_bytes": wr, "ring": ring, "graph_steps": G, "clocks": clocks, "e2e": e2e,
         "desc": desc, "px": px, "batched": batched, "copy_ceiling": ceiling,
     }
+    for t in textures or ():
+        t.destroy()
     plan.destroy()
     return res
 
@@ -606,7 +617,7 @@ def oracle_rate(workload, budget_s):
 
         def run(rows):
             return oracle.gray_resize_u8(img, OH, OW)
-    elif kind == "u8":
+    elif kind in ("u8", "tex"):
         img = synth.smooth_rgb(W, H, 3) if (C == 3 and W >= 1920) else synth.random_u8((H, W, C), seed=3)
         if mode == "linear":
             def run(rows):
@@ -639,7 +650,7 @@ def oracle_rate(workload, budget_s):
     t0 = time.perf_counter()
     run(min(OH, 8))
     probe = time.perf_counter() - t0
-    rows_full = OH if (kind == "u8" and mode == "linear") else None
+    rows_full = OH if (kind in ("u8", "tex") and mode == "linear") else None
     if kind == "valid":
         # a band of output rows sized by the probe so the sample fits the budget
         per_row = max(probe / 8, 1e-6)
@@ -739,9 +750,12 @@ def profile_run(args):
         # two batches of nf frames in rotation, one resize_u8_batch launch each
         sets = [(torch.stack([frames[(b * nf + i) % ring] for i in range(nf)]),
                  torch.empty((nf, OH, OW, C), dtype=torch.uint8, device=dev)) for b in range(2)]
+    textures = [rz.Texture(f) for f in frames] if kind == "tex" else None
     for i in range(args.warmup + args.profile):
         if nf:
             rz.resize_u8_batch(plan, *sets[i % 2])
+        elif kind == "tex":
+            textures[i % ring].resize(outs[i % ring])
         elif kind == "u8":
             rz.resize_u8(plan, frames[i % ring], outs[i % ring])
         else:
@@ -840,7 +854,7 @@ def main():
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "u8" if WORKLOADS[args.workload][1] in ("u8", "gray") else "f32",
+            "dtype": "u8" if WORKLOADS[args.workload][1] in ("u8", "gray", "tex") else "f32",
             "data": "synthetic",
             "config": {
                 "workload": desc,

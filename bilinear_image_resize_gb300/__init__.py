@@ -29,7 +29,7 @@ __all__ = [
     "RZ_LINEAR", "RZ_NEAREST", "RZ_U8", "RZ_F32", "RZ_EPI_NORMALIZE_NCHW", "RZ_EPI_FILTER3X3",
     "RZ_EPI_GRAY_RGB", "RZ_EPI_GRAY_BGR", "RZ_BORDER_CLAMP", "RZ_BORDER_MIRROR", "RZ_BORDER_WRAP",
     "resize_plan_create_border", "resize_axis_table_border", "RZ_EPI_FILTER", "RZ_OPT_FILTER_KERNEL",
-    "filter2d_valid_f32",
+    "filter2d_valid_f32", "Texture", "resize_texture_create",
     "RZ_OK", "RZ_ERR_ARG", "RZ_ERR_UNSUPPORTED", "RZ_ERR_CUDA", "RZ_ERR_NOMEM", "RZ_ERR_TIMEOUT",
     "RZ_MAX_DIM", "KIND_U8", "KIND_F32", "KIND_NORMALIZE", "KIND_FILTER3X3",
     "RZ_OPT_STAGES", "RZ_OPT_GENERIC_ONLY", "RZ_OPT_CTAS_PER_SM", "RZ_OPT_GRID_MODE", "RZ_OPT_PDL",
@@ -310,6 +310,49 @@ def filter2d_valid_f32(src, weights, dst, stream=None) -> None:
     _check(_native.load().filter2d_valid_f32(src.data_ptr(), src.stride(0) * 4, H, W, weights.data_ptr(), K,
                                              dst.data_ptr(), dst.stride(0) * 4, _stream(stream)),
            "filter2d_valid_f32")
+
+
+class Texture:
+    """Owns an ``rz_tex`` handle (a texture object over a uint8 image); the
+    image tensor is kept alive with it."""
+
+    def __init__(self, src):
+        H, W, C, pitch = _hwc(src, "src")
+        h = ctypes.c_void_p()
+        _check(_native.load().resize_texture_create(ctypes.byref(h), src.data_ptr(), pitch, H, W, C),
+               "resize_texture_create")
+        self.handle, self.src, self.C = h.value, src, C
+
+    def resize(self, dst, stream=None) -> None:
+        """dst[:] = the hardware-filtered bilinear resize of the image."""
+        OH, OW, C, pitch = _hwc(dst, "dst")
+        if C != self.C:
+            raise ValueError("dst channels differ from the image's")
+        _check(_native.load().resize_texture_u8(self.handle, dst.data_ptr(), pitch, OH, OW, _stream(stream)),
+               "resize_texture_u8")
+
+    def destroy(self) -> None:
+        if self.handle:
+            h, self.handle = self.handle, None
+            _check(_native.load().resize_texture_destroy(h), "resize_texture_destroy")
+
+    def __del__(self):
+        try:
+            if self.handle:
+                _native.load().resize_texture_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.destroy()
+
+
+def resize_texture_create(src) -> Texture:
+    return Texture(src)
 
 
 def resize_u8_host(plan: Plan, host_src, host_dst, dev_src, dev_dst, stream=None) -> None:

@@ -81,6 +81,9 @@ SIGNATURES = {
     "resize_fused": (_i, [_p, _p, _i, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, ctypes.POINTER(RzEpilogue), _p]),
     "resize_u8_host": (_i, [_p, _p, _sz, _p, _sz, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
     "filter2d_valid_f32": (_i, [_p, _sz, _i, _i, _p, _i, _p, _sz, _p]),
+    "resize_texture_create": (_i, [ctypes.POINTER(_p), _p, _sz, _i, _i, _i]),
+    "resize_texture_u8": (_i, [_p, _p, _sz, _i, _i, _p]),
+    "resize_texture_destroy": (_i, [_p]),
     "resize_axis_table": (_i, [_i, _i, _i, _p, _p, _p]),
     "resize_axis_table_border": (_i, [_i, _i, _i, _i, _p, _p, _p]),
     "resize_strerror": (ctypes.c_char_p, [_i]),

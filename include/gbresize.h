@@ -246,6 +246,29 @@ RZ_API int resize_fused(rz_plan p, const void *src, int src_dtype, size_t src_pi
                  int H, int W, int C, int out_h, int out_w, int mode, const rz_epilogue *e, void *stream);
 
 /*
+ * Hardware-filtered bilinear resize, a comparison path: the texture unit's
+ * linear filtering sampled at (dst + 0.5) * in / out with clamped addressing
+ * ("From Prototype to Performance: Optimizing OpenCV Resize on Volcanic
+ * GPUs", *Naive resize with linear sampling*; CUDA interpolation page §4.1).
+ * Its weights have about 8 fractional bits, so results may differ from
+ * resize_u8 (and the oracle) by a unit or so; resize_u8 is the exact path.
+ *
+ * resize_texture_create binds a texture object to the caller's uint8 image
+ * (device memory, C = 1 or 4 interleaved channels; C = 3 has no texture
+ * format: RZ_ERR_UNSUPPORTED).  The base must be aligned to the device's
+ * texture alignment and src_pitch a multiple of its texture pitch alignment
+ * (cudaDevAttrTextureAlignment / cudaDevAttrTexturePitchAlignment);
+ * otherwise RZ_ERR_ARG.  The image must stay allocated
+ * while the handle lives.  resize_texture_u8 resizes it into dst (out_w * C
+ * bytes per row at dst_pitch), asynchronously on `stream`, no allocation.
+ * resize_texture_destroy synchronises the device and frees the handle.
+ */
+typedef struct rz_tex_s *rz_tex;
+RZ_API int resize_texture_create(rz_tex *out, const uint8_t *src, size_t src_pitch, int H, int W, int C);
+RZ_API int resize_texture_u8(rz_tex t, uint8_t *dst, size_t dst_pitch, int out_h, int out_w, void *stream);
+RZ_API int resize_texture_destroy(rz_tex t);
+
+/*
  * K x K correlation over the valid region ("OpenCL image convolution" §2):
  *   dst[y][x] = sum_{r, c in [0, K)} w[r*K + c] * src[y + r][x + c]
  * for 0 <= y <= H - K, 0 <= x <= W - K (the filter's first row and column on
