@@ -18,7 +18,8 @@ from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_BORD
                       RZ_BORDER_WRAP, RZ_EPI_FILTER, RZ_EPI_FILTER3X3, RZ_EPI_GRAY_BGR, RZ_EPI_GRAY_RGB, RZ_EPI_NORMALIZE_NCHW, RZ_ERR_ARG, RZ_ERR_CUDA, RZ_ERR_NOMEM, RZ_ERR_TIMEOUT,
                       RZ_ERR_UNSUPPORTED, RZ_F32, RZ_LINEAR, RZ_MAX_DIM, RZ_NEAREST, RZ_NOALLOC_MAX_DIM, RZ_OK,
                       RZ_OPT_CTAS_PER_SM, RZ_OPT_GENERIC_ONLY, RZ_OPT_GRID_MODE, RZ_OPT_PDL, RZ_OPT_RING_ROWS,
-                      RZ_OPT_FILTER_KERNEL, RZ_OPT_STAGES, RZ_OPT_U8_KERNEL, RZ_U8, RzEpilogue)
+                      RZ_MULTI_MAX_JOBS, RZ_OPT_FILTER_KERNEL, RZ_OPT_STAGES, RZ_OPT_U8_KERNEL, RZ_U8,
+                      RzEpilogue, RzJob)
 
 __all__ = [
     "ResizeError", "Plan", "resize_plan_create", "resize_plan_destroy", "resize_plan_status",
@@ -29,7 +30,8 @@ __all__ = [
     "RZ_LINEAR", "RZ_NEAREST", "RZ_U8", "RZ_F32", "RZ_EPI_NORMALIZE_NCHW", "RZ_EPI_FILTER3X3",
     "RZ_EPI_GRAY_RGB", "RZ_EPI_GRAY_BGR", "RZ_BORDER_CLAMP", "RZ_BORDER_MIRROR", "RZ_BORDER_WRAP",
     "resize_plan_create_border", "resize_axis_table_border", "RZ_EPI_FILTER", "RZ_OPT_FILTER_KERNEL",
-    "filter2d_valid_f32", "Texture", "resize_texture_create",
+    "filter2d_valid_f32", "Texture", "resize_texture_create", "make_jobs", "resize_u8_multi",
+    "RZ_MULTI_MAX_JOBS",
     "RZ_OK", "RZ_ERR_ARG", "RZ_ERR_UNSUPPORTED", "RZ_ERR_CUDA", "RZ_ERR_NOMEM", "RZ_ERR_TIMEOUT",
     "RZ_MAX_DIM", "KIND_U8", "KIND_F32", "KIND_NORMALIZE", "KIND_FILTER3X3",
     "RZ_OPT_STAGES", "RZ_OPT_GENERIC_ONLY", "RZ_OPT_CTAS_PER_SM", "RZ_OPT_GRID_MODE", "RZ_OPT_PDL",
@@ -310,6 +312,37 @@ def filter2d_valid_f32(src, weights, dst, stream=None) -> None:
     _check(_native.load().filter2d_valid_f32(src.data_ptr(), src.stride(0) * 4, H, W, weights.data_ptr(), K,
                                              dst.data_ptr(), dst.stride(0) * 4, _stream(stream)),
            "filter2d_valid_f32")
+
+
+def make_jobs(srcs, dsts, device=None):
+    """A device array of rz_job descriptors for resize_u8_multi from lists of
+    uint8 HWC (or HW) CUDA tensors; returns (jobs tensor, C)."""
+    import torch
+    if len(srcs) != len(dsts):
+        raise ValueError("srcs and dsts differ in length")
+    arr = (_native.RzJob * max(1, len(srcs)))()
+    C = None
+    for k, (s, d) in enumerate(zip(srcs, dsts)):
+        H, W, cs, sp = _hwc(s, "src")
+        OH, OW, cd, dp = _hwc(d, "dst")
+        if cs != cd or (C is not None and cs != C):
+            raise ValueError("every job must have the same channel count")
+        C = cs
+        arr[k] = _native.RzJob(s.data_ptr(), d.data_ptr(), sp, dp, H, W, OH, OW)
+    raw = bytes(memoryview(arr))[:ctypes.sizeof(_native.RzJob) * len(srcs)]
+    dev = device if device is not None else (srcs[0].device if srcs else "cuda")
+    jobs = torch.frombuffer(bytearray(raw), dtype=torch.uint8).to(dev) if raw else torch.empty(
+        0, dtype=torch.uint8, device=dev)
+    return jobs, (C or 1)
+
+
+def resize_u8_multi(jobs, njobs: int, C: int, mode: int = RZ_LINEAR, status=None, stream=None) -> None:
+    """Launch the jobs of a device job array (make_jobs) in one kernel;
+    status: optional one-element int32 CUDA tensor receiving RZ_ERR_ARG when
+    a job is invalid."""
+    _check(_native.load().resize_u8_multi(jobs.data_ptr() if njobs else None, njobs, C, mode,
+                                          status.data_ptr() if status is not None else None, _stream(stream)),
+           "resize_u8_multi")
 
 
 class Texture:

@@ -65,6 +65,22 @@ _p = ctypes.c_void_p
 _sz = ctypes.c_size_t
 _i = ctypes.c_int
 
+
+class RzJob(ctypes.Structure):
+    _fields_ = [
+        ("src", ctypes.c_void_p),
+        ("dst", ctypes.c_void_p),
+        ("src_pitch", ctypes.c_size_t),
+        ("dst_pitch", ctypes.c_size_t),
+        ("H", ctypes.c_int),
+        ("W", ctypes.c_int),
+        ("out_h", ctypes.c_int),
+        ("out_w", ctypes.c_int),
+    ]
+
+
+RZ_MULTI_MAX_JOBS = 2048
+
 # name -> (restype, argtypes); every symbol include/gbresize.h declares
 SIGNATURES = {
     "resize_plan_create": (_i, [ctypes.POINTER(_p), _i, _i, _i, _i, _i, _p]),
@@ -81,6 +97,7 @@ SIGNATURES = {
     "resize_fused": (_i, [_p, _p, _i, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, ctypes.POINTER(RzEpilogue), _p]),
     "resize_u8_host": (_i, [_p, _p, _sz, _p, _sz, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
     "filter2d_valid_f32": (_i, [_p, _sz, _i, _i, _p, _i, _p, _sz, _p]),
+    "resize_u8_multi": (_i, [_p, _i, _i, _i, _p, _p]),
     "resize_texture_create": (_i, [ctypes.POINTER(_p), _p, _sz, _i, _i, _i]),
     "resize_texture_u8": (_i, [_p, _p, _sz, _i, _i, _p]),
     "resize_texture_destroy": (_i, [_p]),

@@ -1000,6 +1000,16 @@ int resize_fused(rz_plan p, const void *src, int src_dtype, size_t src_pitch, vo
                out_w, mode, e->batch, extra, stream);
 }
 
+int resize_u8_multi(const rz_job *dev_jobs, int njobs, int C, int mode, int *dev_status, void *stream)
+{
+    if (njobs < 0 || njobs > RZ_MULTI_MAX_JOBS || !valid_mode(mode) || C < 1) return RZ_ERR_ARG;
+    if (C != 1 && C != 3 && C != 4) return RZ_ERR_UNSUPPORTED;
+    if (njobs == 0) return RZ_OK;
+    if (!dev_jobs) return RZ_ERR_ARG;
+    const int e = rz::launch_multi(dev_jobs, njobs, C, mode, dev_status, true, stream);
+    return e != 0 ? cuda_fail(static_cast<cudaError_t>(e)) : RZ_OK;
+}
+
 int filter2d_valid_f32(const float *src, size_t src_pitch, int H, int W, const float *weights, int K, float *dst,
                        size_t dst_pitch, void *stream)
 {

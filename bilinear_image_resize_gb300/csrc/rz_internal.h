@@ -195,6 +195,11 @@ const void *resize_filter_kernel_for(int C, int K, bool wrap);
 int launch_filter_valid(const float *src, long long src_pitch, int H, int W, const float *w, int K, float *dst,
                         long long dst_pitch, bool pdl, void *stream);
 
+// Many geometries in one launch (multi.cu): a persistent grid over the jobs'
+// output row segments.  Returns a cudaError_t.
+constexpr int kMultiMaxJobs = RZ_MULTI_MAX_JOBS;
+int launch_multi(const rz_job *jobs, int njobs, int C, int mode, int *status, bool pdl, void *stream);
+
 // Direct-load kernels (direct.cu): a thread per output group, no staging.
 constexpr int kDirectThreads = 256;
 // The exact 2x uint8 downscale (bilinear or nearest) for C channels; nullptr

@@ -246,6 +246,37 @@ RZ_API int resize_fused(rz_plan p, const void *src, int src_dtype, size_t src_pi
                  int H, int W, int C, int out_h, int out_w, int mode, const rz_epilogue *e, void *stream);
 
 /*
+ * Many independent uint8 resizes of different geometries in ONE launch, for
+ * small frames whose own launches would each cost more than their work
+ * (kernel-call overhead: "Performance Optimization of Object Tracking
+ * Algorithms in OpenCV on GPUs" §4.2; batching launches: CUDA interpolation
+ * page §8.1).  Each job resizes src (H x W x C interleaved, src_pitch bytes
+ * per row) into dst (out_h x out_w x C, dst_pitch bytes per row) exactly as
+ * resize_u8 with a clamp-border plan of that geometry does (bit-identical);
+ * no plan is needed: sampling positions and weights are computed in the
+ * kernel.  All jobs share C (1, 3 or 4) and mode.
+ *
+ * dev_jobs: DEVICE array of njobs descriptors (caller-owned, read by the
+ * kernel; fill it once and the launch can be captured and replayed in a
+ * graph).  0 <= njobs <= RZ_MULTI_MAX_JOBS.  A job whose fields are invalid
+ * (null pointers, sizes outside 1..RZ_MAX_DIM for the source or 0..RZ_MAX_DIM
+ * for the output, pitches below the row bytes; an empty output's pointers
+ * and pitches are not checked) is skipped and RZ_ERR_ARG is
+ * written to *dev_status (a caller-owned device int, may be NULL); the other
+ * jobs still run.  Jobs must not overlap one another's outputs or write
+ * their own inputs.  Asynchronous on `stream`; no allocation.
+ */
+typedef struct {
+    const uint8_t *src;
+    uint8_t *dst;
+    size_t src_pitch;
+    size_t dst_pitch;
+    int H, W, out_h, out_w;
+} rz_job;
+#define RZ_MULTI_MAX_JOBS 2048
+RZ_API int resize_u8_multi(const rz_job *dev_jobs, int njobs, int C, int mode, int *dev_status, void *stream);
+
+/*
  * Hardware-filtered bilinear resize, a comparison path: the texture unit's
  * linear filtering sampled at (dst + 0.5) * in / out with clamped addressing
  * ("From Prototype to Performance: Optimizing OpenCV Resize on Volcanic

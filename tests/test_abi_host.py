@@ -40,24 +40,26 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(_native.SIGNATURES) == set(names)
 
 
-def test_epilogue_struct_layout_matches_header(tmp_path):
-    # the binding's ctypes struct against the C compiler's layout of the header's
+@pytest.mark.parametrize("cname, pyname", [("rz_epilogue", "RzEpilogue"), ("rz_job", "RzJob")])
+def test_struct_layouts_match_header(tmp_path, cname, pyname):
+    # the binding's ctypes structs against the C compiler's layout of the header's
     import shutil
     import subprocess
-    from bilinear_image_resize_gb300 import RzEpilogue
+    import bilinear_image_resize_gb300 as rz
+    cls = getattr(rz, pyname)
     cc = shutil.which("gcc") or shutil.which("cc")
     if cc is None:
         pytest.skip("no C compiler")
-    fields = [f[0] for f in RzEpilogue._fields_]
+    fields = [f[0] for f in cls._fields_]
     prog = tmp_path / "layout.c"
     prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gbresize.h"\nint main(void){'
-                    'printf("%zu", sizeof(rz_epilogue));' +
-                    "".join(f'printf(" %zu", offsetof(rz_epilogue, {n}));' for n in fields) + "return 0;}\n")
+                    f'printf("%zu", sizeof({cname}));' +
+                    "".join(f'printf(" %zu", offsetof({cname}, {n}));' for n in fields) + "return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
     got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
-    assert got[0] == ctypes.sizeof(RzEpilogue)
-    assert got[1:] == [getattr(RzEpilogue, n).offset for n in fields]
+    assert got[0] == ctypes.sizeof(cls)
+    assert got[1:] == [getattr(cls, n).offset for n in fields]
 
 
 def exact_linear(n_in, n_out):
