@@ -138,7 +138,7 @@ struct rz_plan_s {
     int2 *d_xq = nullptr, *d_xf = nullptr, *d_yq = nullptr, *d_yf = nullptr;
     int *d_status = nullptr;
     std::mutex mu;
-    struct Entry { int fam, C, batch; TileCfg cfg; };
+    struct Entry { int fam, C, batch, halo; TileCfg cfg; };
     std::vector<Entry> cache;
     int over_tr[rz::FAM_COUNT] = {}, over_tw[rz::FAM_COUNT] = {};
     int opt_stages = 0;        // 0: automatic
@@ -158,9 +158,8 @@ bool valid_border(int b) { return b == RZ_BORDER_CLAMP || b == RZ_BORDER_MIRROR 
 
 // Upper bound on the bytes of one staged source row of the tile column
 // starting at output column dx0: the tap span rounded out to 16 bytes.
-int span_bytes(const rz_plan_s &p, int fam, int C, int dx0, int dx1)
+int span_bytes(const rz_plan_s &p, int fam, int C, int dx0, int dx1, int halo)
 {
-    const int halo = rz::fam_halo(fam);
     const int es = rz::fam_in_es(fam);
     const int cx0 = std::clamp(dx0 - halo, 0, p.OW - 1);
     const int cx1 = std::clamp(dx1 - 1 + halo, 0, p.OW - 1);
@@ -175,11 +174,12 @@ int span_bytes(const rz_plan_s &p, int fam, int C, int dx0, int dx1)
 // for the uint8 bilinear kernels, whose 32-bit tap reads may run up to 11
 // bytes past a span (onto taps of weight 0).  `pad` = false for the exact 2x
 // path, which reads only inside each span.
-int max_slot_bytes(const rz_plan_s &p, int fam, int C, int TW, bool pad = true)
+int max_slot_bytes(const rz_plan_s &p, int fam, int C, int TW, bool pad = true, int halo = -1)
 {
+    if (halo < 0) halo = rz::fam_halo(fam);
     int m = 0;
     for (int dx0 = 0; dx0 < p.OW; dx0 += TW)
-        m = std::max(m, span_bytes(p, fam, C, dx0, std::min(dx0 + TW, p.OW)));
+        m = std::max(m, span_bytes(p, fam, C, dx0, std::min(dx0 + TW, p.OW), halo));
     return m + (pad ? rz::fam_slot_pad(fam) : 0);
 }
 
@@ -327,13 +327,13 @@ constexpr int kStreamMinRows = 16;          // shortest automatic unit (the filt
 // chunks as keep three CTAs per SM (two at least).  Returns
 // RZ_ERR_UNSUPPORTED when the uint8 form does not fit (the caller then uses
 // the staged-tile kernel).
-int get_stream_tile(rz_plan_s *p, int op, int C, int batch, TileCfg *out, const void **fn_out)
+int get_stream_tile(rz_plan_s *p, int op, int C, int batch, TileCfg *out, const void **fn_out, int halo)
 {
-    const void *fn = rz::stream_kernel_for(op, p->mode, C);
+    const void *fn = rz::stream_kernel_for(op, p->mode, C, halo);
     if (!fn) return RZ_ERR_UNSUPPORTED;
     const bool u8 = op == rz::STREAM_U8;
     const int fam = u8 ? rz::FAM_U8 : rz::FAM_FILT;
-    const int widest = u8 ? rz::stream_u8_strip(C) : rz::filter_strip(C);
+    const int widest = u8 ? rz::stream_u8_strip(C) : rz::filter_strip(C, halo);
     TileCfg t;
     int strips = (p->OW + widest - 1) / widest;
     int span = 0;
@@ -341,7 +341,7 @@ int get_stream_tile(rz_plan_s *p, int op, int C, int batch, TileCfg *out, const 
         t.TW = (p->OW + strips - 1) / strips;
         if (u8 && t.TW < p->OW) t.TW = std::min(p->OW, (t.TW + 31) / 32 * 32);   // word-aligned output runs
         if (p->over_tw[fam] > 0) t.TW = std::min({p->over_tw[fam], widest, p->OW});
-        span = max_slot_bytes(*p, fam, C, t.TW, u8);   // a multiple of 16 (+16 of padding for uint8)
+        span = max_slot_bytes(*p, fam, C, t.TW, u8, halo);   // a multiple of 16 (+16 of padding for uint8)
         if (!u8 || span <= 2048) break;
         if (p->over_tw[fam] > 0 || t.TW <= 32) return RZ_ERR_UNSUPPORTED;
         strips++;
@@ -397,7 +397,7 @@ int get_stream_tile(rz_plan_s *p, int op, int C, int batch, TileCfg *out, const 
     const long long units = static_cast<long long>(batch) * t.tiles_x * t.tiles_y;
     if (units > 0x7fffffffLL) return RZ_ERR_UNSUPPORTED;
     t.grid = p->opt_grid_mode == 1 ? static_cast<int>(units) : static_cast<int>(std::min(units, cap));
-    p->cache.push_back({fam, C, batch, t});
+    p->cache.push_back({fam, C, batch, halo, t});
     *out = t;
     *fn_out = fn;
     return RZ_OK;
@@ -422,22 +422,22 @@ bool want_u8_stream(const rz_plan_s &p, bool down2)
 
 // Tile and grid for this call: the override if one is set, else the cached
 // automatic choice.  Returns an RZ_* status.
-int get_tile(rz_plan_s *p, int fam, int C, int batch, TileCfg *out, const void **fn_out)
+int get_tile(rz_plan_s *p, int fam, int C, int batch, TileCfg *out, const void **fn_out, int halo)
 {
     std::lock_guard<std::mutex> lk(p->mu);
     for (const auto &e : p->cache)
-        if (e.fam == fam && e.C == C && e.batch == batch) {
+        if (e.fam == fam && e.C == C && e.batch == batch && e.halo == halo) {
             *out = e.cfg;
             *fn_out = e.cfg.stream ? rz::stream_kernel_for(e.cfg.stream == 2 ? rz::STREAM_U8 : rz::STREAM_FILTER,
-                                                           p->mode, C)
+                                                           p->mode, C, halo)
                                    : rz::kernel_for(fam, p->mode, e.cfg.variant, C);
             return RZ_OK;
         }
-    if (fam == rz::FAM_FILT) return get_stream_tile(p, rz::STREAM_FILTER, C, batch, out, fn_out);
+    if (fam == rz::FAM_FILT) return get_stream_tile(p, rz::STREAM_FILTER, C, batch, out, fn_out, halo);
     const int stages = p->opt_stages > 0 ? p->opt_stages : kDefaultStages;
     const bool down2 = fam == rz::FAM_U8 && !p->opt_generic && is_down2(*p);
     if (fam == rz::FAM_U8 && want_u8_stream(*p, down2)) {
-        const int rc = get_stream_tile(p, rz::STREAM_U8, C, batch, out, fn_out);
+        const int rc = get_stream_tile(p, rz::STREAM_U8, C, batch, out, fn_out, 0);
         if (rc != RZ_ERR_UNSUPPORTED) return rc;   // else the staged-tile kernel below
     }
     TileCfg t;
@@ -469,7 +469,7 @@ int get_tile(rz_plan_s *p, int fam, int C, int batch, TileCfg *out, const void *
     t.grid = p->opt_grid_mode == 1
                  ? static_cast<int>(ntiles)
                  : static_cast<int>(std::min<long long>(ntiles, static_cast<long long>(per_sm) * sms));
-    p->cache.push_back({fam, C, batch, t});
+    p->cache.push_back({fam, C, batch, halo, t});
     *out = t;
     *fn_out = fn;
     return RZ_OK;
@@ -523,10 +523,11 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
         return launch_grid(fn, (threads + rz::kDirectThreads - 1) / rz::kDirectThreads, rz::kDirectThreads);
     };
     if (fam == rz::FAM_FILT) {
-        // K x K epilogue: the tile kernel (filter.cu) for K other than 3, for
-        // wrap plans, or when the option asks; else the streaming 3x3 kernel
+        // K x K epilogue: the streaming kernel for K = 3, 5, 7 (source rows
+        // streamed once, neighbours by shuffle); the tile kernel (filter.cu)
+        // for K = 1, for wrap plans, or when the option asks
         const int fopt = p->opt_filter_kernel;
-        if (a.ksize == 3 && !wrap && fopt != 2) return false;
+        if (a.ksize >= 3 && !wrap && fopt != 2) return false;
         if (fopt == 1) {
             *rc = RZ_ERR_UNSUPPORTED;
             return true;
@@ -682,7 +683,7 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
 
     TileCfg t;
     const void *fn = nullptr;
-    rc = get_tile(p, fam, C, batch, &t, &fn);
+    rc = get_tile(p, fam, C, batch, &t, &fn, fam == rz::FAM_FILT ? a.ksize / 2 : 0);
     if (rc != RZ_OK) return rc;
     a.TR = t.TR; a.TW = t.TW; a.tiles_x = t.tiles_x; a.tiles_y = t.tiles_y;
     a.max_rows = t.max_rows; a.slot_bytes = t.slot_bytes; a.stages = t.stages;

@@ -103,10 +103,11 @@ enum StreamOp { STREAM_FILTER = 0, STREAM_U8 = 1 };
 constexpr int kStreamChunkRows = 8;     // rows per chunk (a power of two)
 constexpr int kStreamRingMax = 128;     // ring rows (chunks x rows per chunk)
 constexpr int kStreamListWindow = 128;  // listed rows the producer keeps (ints)
-// 3x3 filter: resized columns per consumer lane (two for one channel, else
-// one); widest strip = eight consumer warps x (32 x lane columns - 2) outputs
+// K x K filter: resized columns per consumer lane (two for one channel, else
+// one); widest strip = eight consumer warps x (32 x lane columns - 2 K/2)
+// outputs
 __host__ __device__ constexpr int filter_lane_cols(int C) { return C == 1 ? 2 : 1; }
-__host__ __device__ constexpr int filter_strip(int C) { return 8 * (32 * filter_lane_cols(C) - 2); }
+__host__ __device__ constexpr int filter_strip(int C, int R = 1) { return 8 * (32 * filter_lane_cols(C) - 2 * R); }
 // uint8 bilinear: consecutive output pixels per consumer lane; widest strip
 __host__ __device__ constexpr int stream_u8_run(int C) { return C == 4 ? 2 : 4; }
 __host__ __device__ constexpr int stream_u8_strip(int C) { return 8 * 32 * stream_u8_run(C); }
@@ -157,8 +158,9 @@ void record_cuda_error(int e);
 // Kernel entry for (family, mode, variant, C); nullptr if none.
 const void *kernel_for(int fam, int mode, int variant, int C);
 
-// The streaming kernel for (StreamOp, mode, C); nullptr if none.
-const void *stream_kernel_for(int op, int mode, int C);
+// The streaming kernel for (StreamOp, mode, C, filter halo R = K / 2);
+// nullptr if none.
+const void *stream_kernel_for(int op, int mode, int C, int R = 1);
 
 // Launch it on grid x grid_y CTAs of `threads` (asynchronous), optionally as
 // a programmatic dependent launch.  `tmap` describes the source when

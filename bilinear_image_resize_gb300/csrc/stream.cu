@@ -2,11 +2,11 @@
 // down a segment of rows, streaming the source rows it needs through a ring
 // of chunks in shared memory.  Two consumers share the producer:
 //
-//   * the 3x3 filter epilogue on float32 HWC images.  It filters the RESIZED
-//     image: out(y, x) = sum over a, b in {-1, 0, 1} of
-//     w[a+1][b+1] * R(clamp(y + a), clamp(x + b)), where R is the bilinear
-//     resize and the clamp replicates R's border (CUDA interpolation page,
-//     §4.2 fused epilogue; §6.1 replicate border);
+//   * the K x K filter epilogue (K = 3, 5, 7) on float32 HWC images.  It
+//     filters the RESIZED image: out(y, x) = sum over a, b in -K/2 .. K/2 of
+//     w[a+K/2][b+K/2] * Z(clamp(y + a), clamp(x + b)), where Z is the
+//     bilinear resize and the clamp replicates Z's border (CUDA interpolation
+//     page, §4.2 fused epilogue; §6.1 replicate border);
 //   * the uint8 bilinear resize in row-separable form.  The exact horizontal
 //     sum h = A0 t0 + A1 t1 of a source row is formed once per output column
 //     when the row arrives; each output row then needs only the vertical
@@ -16,7 +16,7 @@
 //     rows are shared by several output rows (upscales).
 //
 // Work unit: one strip of TW output columns by TR output rows of one image.
-// A unit computes on rows dy0 - HALO .. dy1 - 1 + HALO (HALO = 1 for the
+// A unit computes on rows dy0 - HALO .. dy1 - 1 + HALO (HALO = K / 2 for the
 // filter, 0 for the plain resize; clamped into the image) and samples the
 // source rows those rows list, each once and in increasing order.
 //
@@ -342,33 +342,35 @@ __device__ __forceinline__ bool walk_unit(const KArgs &a, const UnitGeom &g, con
     return true;
 }
 
-// ------------------------------------------------------------------ consumer: 3x3 filter (float32)
+// ------------------------------------------------------------------ consumer: K x K filter (float32)
 
-// Each warp takes CW output columns; resized column e = lane + 32 i of the
-// warp is dx0 + warp * CW - 1 + e (held at dx1 past the strip: its value only
-// feeds lanes that emit nothing); columns e = 1 .. CW are its outputs.  Per
-// resized row the lane forms its resized values, takes the neighbours' by
-// warp shuffle and adds them into partial sums of the three output rows the
-// row feeds (output row k - 2 completes at row k).
-template <int C, int LINEAR>
+// K = 2R + 1.  Each warp takes CW output columns; resized column e = lane +
+// 32 i of the warp is dx0 + warp * CW - R + e (the true column, clamped to
+// the image, up to R past the strip; held there beyond: those values feed
+// lanes that emit nothing); columns e = R .. R + CW - 1 are its outputs.  Per
+// resized row the lane forms its resized values, takes the neighbours' at
+// distances 1 .. R by warp shuffle and adds them into partial sums of the K
+// output rows the row feeds (output row k - 2R completes at row k).
+template <int C, int LINEAR, int R>
 __device__ __forceinline__ bool consume_filter(const KArgs &a, const UnitGeom &g, const Ring &rg, Cursor &cs)
 {
+    constexpr int K = 2 * R + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int NCOL = filter_lane_cols(C);   // resized columns per lane: lane + 32 i
     const int CW = (a.TW + kConsumers / 32 - 1) / (kConsumers / 32);
     const int NB = rg.NB, BW = rg.BW, BB = rg.BB;
     int b_lo, nbytes;
-    unit_span<4, 1>(a, g, C, LINEAR, b_lo, nbytes);
+    unit_span<4, R>(a, g, C, LINEAR, b_lo, nbytes);
     const int nc = g.dx1 - g.dx0;
     float uw[NCOL];
     int off0[NCOL][C], off1[NCOL][C];   // float offsets of the taps' channels within a staged row
     bool emit[NCOL];
-    const int rel0 = warp * CW - 1 + lane;
+    const int rel0 = warp * CW - R + lane;
 #pragma unroll
     for (int i = 0; i < NCOL; i++) {
         const int e = lane + 32 * i, rel = rel0 + 32 * i;
-        emit[i] = e >= 1 && e <= CW && rel < nc;
-        const int2 xe = a.xt[clampi(g.dx0 + min(rel, nc), 0, a.OW - 1)];
+        emit[i] = e >= R && e < R + CW && rel < nc;
+        const int2 xe = a.xt[clampi(g.dx0 + min(rel, nc + R - 1), 0, a.OW - 1)];
         uw[i] = __int_as_float(xe.y);
         const int x1 = LINEAR ? min(xe.x + 1, a.W - 1) : xe.x;
 #pragma unroll
@@ -383,23 +385,25 @@ __device__ __forceinline__ bool consume_filter(const KArgs &a, const UnitGeom &g
     // of this lane is rel0 + 32 i pixels on (>= 0 where emitted)
     uint8_t *op = a.dst + (long long)g.b * a.dst_bstride + (long long)g.dy0 * a.dst_pitch +
                   (long long)g.dx0 * C * 4;
-    // partial sums of the output rows resized row k contributes to: acc1 for
-    // output row k - 1, acc2 for k - 2; each sums its nine products in the
-    // filter's row-major order
-    float acc1[NCOL][C], acc2[NCOL][C];
+    // partial sums of the output rows resized row k contributes to: acc[j]
+    // for output row k - 1 - j; each sums its K^2 products in the filter's
+    // row-major order
+    float acc[2 * R][NCOL][C];
 #pragma unroll
-    for (int i = 0; i < NCOL; i++)
+    for (int j = 0; j < 2 * R; j++)
 #pragma unroll
-        for (int c = 0; c < C; c++)
-            acc1[i][c] = acc2[i][c] = 0.0f;
-    return walk_unit<1, LINEAR>(a, g, rg, cs, [&](int k, const uint8_t *top8, const uint8_t *bot8, int wbits, int) {
+        for (int i = 0; i < NCOL; i++)
+#pragma unroll
+            for (int c = 0; c < C; c++)
+                acc[j][i][c] = 0.0f;
+    return walk_unit<R, LINEAR>(a, g, rg, cs, [&](int k, const uint8_t *top8, const uint8_t *bot8, int wbits, int) {
         const float *top = reinterpret_cast<const float *>(top8);
         const float *bot = reinterpret_cast<const float *>(bot8);
         const float v = __int_as_float(wbits);
-        const bool store = k >= 2;
+        const bool store = k >= 2 * R;
 #pragma unroll
         for (int c = 0; c < C; c++) {
-            float m[NCOL], l[NCOL], r[NCOL];
+            float m[NCOL];
 #pragma unroll
             for (int i = 0; i < NCOL; i++) {
                 const float t0 = top[off0[i][c]], t1 = top[off1[i][c]];
@@ -408,27 +412,47 @@ __device__ __forceinline__ bool consume_filter(const KArgs &a, const UnitGeom &g
                 const float hB = fmaf(uw[i], b1 - b0, b0);
                 m[i] = fmaf(v, hB - hT, hT);
             }
-            if constexpr (NCOL == 1) {
-                l[0] = __shfl_up_sync(0xffffffffu, m[0], 1);
-                r[0] = __shfl_down_sync(0xffffffffu, m[0], 1);
-            } else {
-                // e = lane and e = lane + 32: the two halves meet between lane
-                // 31's first column and lane 0's second
-                l[0] = __shfl_up_sync(0xffffffffu, m[0], 1);
-                r[0] = __shfl_sync(0xffffffffu, lane == 0 ? m[1] : m[0], (lane + 1) & 31);
-                l[1] = __shfl_sync(0xffffffffu, lane == 31 ? m[0] : m[1], (lane + 31) & 31);
-                r[1] = __shfl_down_sync(0xffffffffu, m[1], 1);
+            // nb[d][i]: resized column e + d - R of this lane's column i
+            float nb[K][NCOL];
+#pragma unroll
+            for (int i = 0; i < NCOL; i++)
+                nb[R][i] = m[i];
+#pragma unroll
+            for (int d = 1; d <= R; d++) {
+                if constexpr (NCOL == 1) {
+                    nb[R - d][0] = __shfl_up_sync(0xffffffffu, m[0], d);
+                    nb[R + d][0] = __shfl_down_sync(0xffffffffu, m[0], d);
+                } else {
+                    // e = lane and e = lane + 32: a neighbour d away lies in
+                    // the other half where the lane index wraps
+                    const float up0 = m[0];
+                    const float up1 = lane >= 32 - d ? m[0] : m[1];
+                    const float dn0 = lane < d ? m[1] : m[0];
+                    const float dn1 = m[1];
+                    nb[R - d][0] = __shfl_sync(0xffffffffu, up0, (lane + 32 - d) & 31);
+                    nb[R - d][1] = __shfl_sync(0xffffffffu, up1, (lane + 32 - d) & 31);
+                    nb[R + d][0] = __shfl_sync(0xffffffffu, dn0, (lane + d) & 31);
+                    nb[R + d][1] = __shfl_sync(0xffffffffu, dn1, (lane + d) & 31);
+                }
             }
 #pragma unroll
             for (int i = 0; i < NCOL; i++) {
-                // this row is row a = -1 of output k, a = 0 of k - 1, a = +1 of k - 2
-                const float a0 = fmaf(a.w[2], r[i], fmaf(a.w[1], m[i], a.w[0] * l[i]));
-                const float a1 = fmaf(a.w[5], r[i], fmaf(a.w[4], m[i], fmaf(a.w[3], l[i], acc1[i][c])));
-                const float a2 = fmaf(a.w[8], r[i], fmaf(a.w[7], m[i], fmaf(a.w[6], l[i], acc2[i][c])));
+                // this row is filter row fr of output k - fr (k counted from
+                // the unit's first computed row); row 2R completes an output
+                float row_sum[K];
+#pragma unroll
+                for (int fr = 0; fr < K; fr++) {
+                    float sacc = fr == 0 ? a.w[fr * K] * nb[0][i] : fmaf(a.w[fr * K], nb[0][i], acc[fr - 1][i][c]);
+#pragma unroll
+                    for (int b = 1; b < K; b++)
+                        sacc = fmaf(a.w[fr * K + b], nb[b][i], sacc);
+                    row_sum[fr] = sacc;
+                }
                 if (store && emit[i])
-                    __stcs(reinterpret_cast<float *>(op) + (rel0 + 32 * i) * C + c, a2);
-                acc2[i][c] = a1;
-                acc1[i][c] = a0;
+                    __stcs(reinterpret_cast<float *>(op) + (rel0 + 32 * i) * C + c, row_sum[2 * R]);
+#pragma unroll
+                for (int j = 0; j < 2 * R; j++)
+                    acc[j][i][c] = row_sum[j];
             }
         }
         if (store)
@@ -533,16 +557,24 @@ __device__ __forceinline__ bool consume_u8(const KArgs &a, const UnitGeom &g, co
 
 // ------------------------------------------------------------------ the kernel
 
-// OP: STREAM_FILTER (float32 + 3x3) or STREAM_U8 (uint8 bilinear).  The
-// uint8 form holds two rows of sums for four pixels per lane and runs two
-// CTAs per SM; the filter runs three.
-template <int OP, int C, int LINEAR>
-__global__ void __launch_bounds__(kThreads, OP == STREAM_U8 ? 2 : 3)
+// OP: STREAM_FILTER (float32 + K x K, K = 2R + 1) or STREAM_U8 (uint8
+// bilinear).  The uint8 form holds two rows of sums for four pixels per lane.
+// CTAs per SM the register budget is set for: 3 for the 3x3 filter, 2 for
+// the uint8 form and the 5x5 and one-channel 7x7 filters, 1 for the 7x7
+// filter on 3 or 4 channels (whose K - 1 rows of partial sums per channel
+// would spill at two).
+__host__ __device__ constexpr int stream_min_ctas(int op, int C, int R)
+{
+    return op == STREAM_U8 ? 2 : (R == 1 ? 3 : (R == 3 && C > 1 ? 1 : 2));
+}
+
+template <int OP, int C, int LINEAR, int R>
+__global__ void __launch_bounds__(kThreads, stream_min_ctas(OP, C, R))
     k_stream(const KArgs a, const __grid_constant__ CUtensorMap tmap)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int ES = OP == STREAM_FILTER ? 4 : 1;
-    constexpr int HALO = OP == STREAM_FILTER ? 1 : 0;
+    constexpr int HALO = OP == STREAM_FILTER ? R : 0;
     Ring rg;
     rg.NCH = a.ring_chunks;
     rg.G = a.chunk_rows;
@@ -579,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, OP == STREAM_U8 ? 2 : 3)
         const UnitGeom g = unit_geom(a, u);
         bool ok;
         if constexpr (OP == STREAM_FILTER)
-            ok = consume_filter<C, LINEAR>(a, g, rg, cs);
+            ok = consume_filter<C, LINEAR, R>(a, g, rg, cs);
         else
             ok = consume_u8<C>(a, g, rg, cs);
         if (!ok)
@@ -590,17 +622,23 @@ __global__ void __launch_bounds__(kThreads, OP == STREAM_U8 ? 2 : 3)
 }  // namespace
 
 // Bilinear only: the fused entry point is bilinear by contract, and the
-// uint8 streaming form is chosen for bilinear resizes.
-const void *stream_kernel_for(int op, int mode, int C)
+// uint8 streaming form is chosen for bilinear resizes.  R: the filter's
+// halo (K = 2R + 1, 1..3); ignored for the uint8 form.
+const void *stream_kernel_for(int op, int mode, int C, int R)
 {
     using Fn = void (*)(const KArgs, const CUtensorMap);
-    static const Fn filt[3] = {k_stream<STREAM_FILTER, 1, 1>, k_stream<STREAM_FILTER, 3, 1>,
-                               k_stream<STREAM_FILTER, 4, 1>};
-    static const Fn u8[3] = {k_stream<STREAM_U8, 1, 1>, k_stream<STREAM_U8, 3, 1>, k_stream<STREAM_U8, 4, 1>};
+    static const Fn filt[3][3] = {
+        {k_stream<STREAM_FILTER, 1, 1, 1>, k_stream<STREAM_FILTER, 3, 1, 1>, k_stream<STREAM_FILTER, 4, 1, 1>},
+        {k_stream<STREAM_FILTER, 1, 1, 2>, k_stream<STREAM_FILTER, 3, 1, 2>, k_stream<STREAM_FILTER, 4, 1, 2>},
+        {k_stream<STREAM_FILTER, 1, 1, 3>, k_stream<STREAM_FILTER, 3, 1, 3>, k_stream<STREAM_FILTER, 4, 1, 3>}};
+    static const Fn u8[3] = {k_stream<STREAM_U8, 1, 1, 0>, k_stream<STREAM_U8, 3, 1, 0>,
+                             k_stream<STREAM_U8, 4, 1, 0>};
     const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
     if (ci < 0 || mode != RZ_LINEAR)
         return nullptr;
-    return reinterpret_cast<const void *>(op == STREAM_FILTER ? filt[ci] : u8[ci]);
+    if (op == STREAM_FILTER)
+        return (R >= 1 && R <= 3) ? reinterpret_cast<const void *>(filt[R - 1][ci]) : nullptr;
+    return reinterpret_cast<const void *>(u8[ci]);
 }
 
 }  // namespace rz

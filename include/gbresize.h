@@ -219,7 +219,7 @@ RZ_API int resize_f32_batch(rz_plan p, const float *src, size_t src_pitch, size_
  *   float32 HWC, z = sum_{a,b in -K/2..K/2} wk[(a+K/2)*K + (b+K/2)] *
  *   r[clamp(dy+a)][clamp(dx+b)], each channel on its own, replicate border
  *   on the output grid.  K = 3 gives RZ_EPI_FILTER3X3's result.  Any border
- *   rule of the plan (the 3x3 kind under RZ_BORDER_WRAP runs this form too).
+ *   rule of the plan.
  *
  * batch >= 0 (0 is a no-op); batch strides are bytes and must keep the frames
  * from overlapping when batch > 1.
@@ -410,12 +410,11 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  *                       rows, tile_rows of resize_plan_set_tile per thread).
  *                       Bit-exact whichever runs;
  *   RZ_OPT_FILTER_KERNEL value 0 (automatic), 1 or 2: which kernel runs the
- *                       3x3 filter epilogue (RZ_EPI_FILTER3X3, or
- *                       RZ_EPI_FILTER with K = 3).  0: streaming, or the
- *                       tile kernel under RZ_BORDER_WRAP; 1: streaming
- *                       (RZ_ERR_UNSUPPORTED under wrap); 2: the tile kernel
- *                       that serves the other K.  Equal within float32
- *                       rounding.
+ *                       filter epilogues (RZ_EPI_FILTER3X3, RZ_EPI_FILTER).
+ *                       0: streaming for K = 3, 5, 7, the tile kernel for
+ *                       K = 1 and under RZ_BORDER_WRAP; 1: streaming
+ *                       (RZ_ERR_UNSUPPORTED for K = 1 or under wrap); 2: the
+ *                       tile kernel.  Equal within float32 rounding.
  * Returns RZ_ERR_ARG for an unknown option or value.
  */
 #define RZ_OPT_STAGES 1

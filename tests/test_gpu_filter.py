@@ -161,11 +161,35 @@ def test_fused_kxk(rz, K, C, border, geom):
 
 
 @pytest.mark.parametrize("kernel", [1, 2])
-def test_fused_3x3_on_both_kernels(rz, kernel):
-    img = synth.random_f32((150, 170, 1), seed=3)
-    w = synth.filter_weights().reshape(3, 3)
-    got = gpu_fused(rz, img, 333, 201, w, opts=[(rz.RZ_OPT_FILTER_KERNEL, kernel)])
-    assert max_abs(got, want_fused(img, 333, 201, w)) <= 1e-4
+@pytest.mark.parametrize("K", [3, 5, 7])
+@pytest.mark.parametrize("C", [1, 3, 4])
+def test_fused_on_both_kernels(rz, kernel, K, C):
+    # the streaming kernel (1) and the tile kernel (2), ragged strips and
+    # segments at several output sizes
+    for (H, W, OH, OW) in [(150, 170, 333, 201), (64, 700, 97, 1500), (300, 40, 130, 19)]:
+        img = synth.random_f32((H, W, C), seed=3 + K)
+        w = synth.filter_weights_k(K)
+        got = gpu_fused(rz, img, OH, OW, w, opts=[(rz.RZ_OPT_FILTER_KERNEL, kernel)])
+        assert max_abs(got, want_fused(img, OH, OW, w)) <= fused_tol(w)
+
+
+@pytest.mark.parametrize("K", [3, 5, 7])
+def test_fused_streaming_tiles_and_rings(rz, K):
+    # explicit strips and ring depths on the streaming kernel
+    img = synth.random_f32((200, 260, 1), seed=K)
+    w = synth.filter_weights_k(K)
+    want = want_fused(img, 310, 390, w)
+    for tile, ring in [((5, 40), 0), ((64, 100), 16), ((1, 17), 2), ((300, 478), 0)]:
+        with rz.resize_plan_create(200, 260, 310, 390, rz.RZ_LINEAR) as plan:
+            rz.resize_plan_set_tile(plan, rz.KIND_FILTER3X3, *tile)
+            if ring:
+                rz.resize_plan_set_option(plan, rz.RZ_OPT_RING_ROWS, ring)
+            src = torch.from_numpy(img).cuda()
+            out = torch.full((310, 390, 1), -99.0, dtype=torch.float32, device="cuda")
+            rz.resize_fused(plan, src, out, rz.make_epilogue(rz.RZ_EPI_FILTER, wk=w))
+            torch.cuda.synchronize()
+            assert rz.resize_plan_status(plan) == rz.RZ_OK
+        assert max_abs(out.cpu().numpy(), want) <= fused_tol(w), (tile, ring)
 
 
 def test_fused_batch(rz):
@@ -202,8 +226,9 @@ def test_fused_argument_checks(rz):
         assert lib.resize_fused(plan.handle, src.data_ptr(), rz.RZ_U8, 32, dst.data_ptr(), 64, 8, 8, 1, 16, 16,
                                 rz.RZ_LINEAR, ctypes.byref(e), st) == rz.RZ_ERR_ARG
         rz.resize_plan_set_option(plan, rz.RZ_OPT_FILTER_KERNEL, 1)
+        e1 = rz.make_epilogue(rz.RZ_EPI_FILTER, wk=np.ones((1, 1)))
         assert lib.resize_fused(plan.handle, src.data_ptr(), rz.RZ_F32, 32, dst.data_ptr(), 64, 8, 8, 1, 16, 16,
-                                rz.RZ_LINEAR, ctypes.byref(e), st) == rz.RZ_ERR_UNSUPPORTED
+                                rz.RZ_LINEAR, ctypes.byref(e1), st) == rz.RZ_ERR_UNSUPPORTED
         with pytest.raises(rz.ResizeError):
             rz.resize_plan_set_option(plan, rz.RZ_OPT_FILTER_KERNEL, 3)
     torch.cuda.synchronize()
