@@ -191,6 +191,22 @@ def test_calls_validate_before_cuda(lib):
     assert lib.resize_plan_status(None, None) == RZ_ERR_ARG
     assert lib.resize_plan_set_tile(None, 0, 1, 1) == RZ_ERR_ARG
     assert lib.resize_plan_destroy(None) == 0
+    # the filter, many-geometry and texture entry points check their
+    # arguments before touching the GPU
+    RZ_ERR_UNSUPPORTED = 2
+    assert lib.filter2d_valid_f32(16, 32, 8, 8, 64, 0, 128, 32, None) == RZ_ERR_ARG
+    assert lib.filter2d_valid_f32(16, 32, 8, 8, 64, 65, 128, 32, None) == RZ_ERR_UNSUPPORTED
+    assert lib.filter2d_valid_f32(16, 32, -1, 8, 64, 3, 128, 32, None) == RZ_ERR_ARG
+    assert lib.filter2d_valid_f32(16, 32, 8, 8, 64, 9, 128, 32, None) == 0          # empty output
+    assert lib.filter2d_valid_f32(None, 32, 8, 8, 64, 3, 128, 32, None) == RZ_ERR_ARG
+    assert lib.resize_u8_multi(16, -1, 3, 1, None, None) == RZ_ERR_ARG
+    assert lib.resize_u8_multi(16, 2049, 3, 1, None, None) == RZ_ERR_ARG
+    assert lib.resize_u8_multi(16, 1, 2, 1, None, None) == RZ_ERR_UNSUPPORTED
+    assert lib.resize_u8_multi(None, 0, 3, 1, None, None) == 0
+    assert lib.resize_texture_create(None, 16, 64, 4, 4, 4) == RZ_ERR_ARG
+    assert lib.resize_texture_create(ctypes.byref(h), None, 64, 4, 4, 4) == RZ_ERR_ARG
+    assert lib.resize_texture_u8(None, 16, 64, 4, 4, None) == RZ_ERR_ARG
+    assert lib.resize_texture_destroy(None) == 0
 
 
 def test_plan_create_without_gpu_reports_cuda_error():
