@@ -97,6 +97,20 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def max_over_ranks(x, dist, device):
+    """The largest of every rank's x (the slowest rank's time), via an
+    all-reduce on `device` (a CUDA device under NCCL, the CPU under gloo)."""
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gpix(px_per_step, steps, world, ms_max):
+    """Whole-job output Gpix/s: every rank's steps over the slowest rank's time."""
+    return px_per_step * steps * world / (ms_max / 1e3) / 1e9
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -386,11 +400,7 @@ def gpu_arm(args, rank, local_rank, world):
     sampler.stop()
     clocks = sampler.summary(t_host0 - 0.02, t_host1 + 0.02)
 
-    ms_max = ms
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist, dev) if dist else ms
 
     # eager (per-call launch) rate, for reference
     with torch.cuda.stream(stream):
@@ -418,7 +428,7 @@ def gpu_arm(args, rank, local_rank, world):
         batched = batched_u8(rz, plan, frames, H, W, OH, OW, C, args.batch_frames, stream, dev, step_bytes)
 
     px = OH * OW * batch
-    value = px * args.steps * world / (ms_max / 1e3) / 1e9
+    value = aggregate_gpix(px, args.steps, world, ms_max)
     launch_ms = ms / args.steps
     achieved = step_bytes / (launch_ms / 1e3) / 1e9
     peaks, src = measured_peaks()

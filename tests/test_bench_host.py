@@ -1,0 +1,60 @@
+"""Host logic of bench.py's multi-process path, on CPU ranks (gloo).
+
+Each rank runs its own replica (no exchange step on the data path); the
+reported time is the slowest rank's, taken by an all-reduce MAX, and the
+value aggregates every rank's work over that time.  Ranks other than 0 do
+no work in the reference (oracle) arm.
+"""
+import io
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+
+import bench
+
+
+def free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    got = bench.max_over_ranks(10.0 + 3 * rank, dist, "cpu")
+    dist.barrier()
+    dist.destroy_process_group()
+    with open(os.path.join(out_dir, f"r{rank}"), "w") as f:
+        f.write(repr(got))
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_max_over_ranks_takes_the_slowest(tmp_path, world):
+    import torch.multiprocessing as mp
+    mp.spawn(_rank_main, args=(world, free_port(), str(tmp_path)), nprocs=world, join=True)
+    for r in range(world):
+        assert float((tmp_path / f"r{r}").read_text()) == 10.0 + 3 * (world - 1)
+
+
+def test_aggregate_counts_every_rank():
+    # 2 ranks x 100 steps x 1 Mpix over 50 ms = 4 Gpix/s
+    assert bench.aggregate_gpix(1_000_000, 100, 2, 50.0) == pytest.approx(4.0)
+    assert bench.aggregate_gpix(1_000_000, 100, 1, 50.0) == pytest.approx(2.0)
+
+
+def test_reference_arm_other_ranks_do_nothing(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+
+    class Args:
+        workload, steps, warmup, cpu_budget = "4k_to_1080p", 1, 0, 0.1
+
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        assert bench.reference_arm(Args()) is None
+    assert buf.getvalue() == ""
