@@ -281,7 +281,7 @@ def resize_fused(plan: Plan, src, dst, epilogue: RzEpilogue, stream=None) -> Non
         dp = d.stride(1) * 4
         dtype_code = RZ_F32
         if s.dtype != torch.float32 or d.dtype != torch.float32:
-            raise ValueError("3x3 epilogue takes float32 src and dst")
+            raise ValueError("filter epilogues take float32 src and dst")
     else:
         raise ValueError(f"unknown epilogue kind {e.kind}")
     Nb, H, W, Cs = s.shape

@@ -100,7 +100,7 @@ void axis_nearest(int n_in, int n_out, int32_t *ofs)
 struct TileCfg {
     int TR = 0, TW = 0, tiles_x = 0, tiles_y = 0, max_rows = 0, slot_bytes = 0, stages = 0, variant = 0;
     int tensor = 0, box_words = 0, box_rows = 0;   // tensor-map staging (one box per chunk)
-    int stream = 0;   // 0: staged-tile kernel; 1: streaming 3x3 filter; 2: streaming uint8 bilinear
+    int stream = 0;   // 0: staged-tile kernel; 1: streaming filter; 2: streaming uint8 bilinear
     int ring_chunks = 0, chunk_rows = 0, chunk_boxes = 0, box_bytes = 0;   // streaming kernels
     size_t smem = 0;
     int grid = 0;
@@ -148,7 +148,7 @@ struct rz_plan_s {
     int opt_pdl = 1;           // programmatic dependent launch
     int opt_ring_rows = 0;     // streaming kernels: source rows in the ring (0: automatic)
     int opt_u8_kernel = 0;     // uint8 bilinear: 0 automatic, 1 staged tiles, 2 streaming, 3 direct
-    int opt_filter_kernel = 0; // 3x3 epilogue: 0 automatic, 1 streaming, 2 tile kernel
+    int opt_filter_kernel = 0; // filter epilogues: 0 automatic, 1 streaming, 2 tile kernel
 };
 
 namespace {
@@ -239,8 +239,8 @@ bool is_down2(const rz_plan_s &p)
 // rows as wide as the output (or the widest power-of-two strip whose staged
 // row stays within 16 KB), narrowed while there are fewer than about twelve
 // tiles per SM (for balance across SMs), then as many output rows per tile as
-// keep the staged ring under 48 KB with that many tiles.  (The 3x3 filter
-// family and uint8 upscales stream strips instead: get_stream_tile.)
+// keep the staged ring under 48 KB with that many tiles.  (The filter family
+// and uint8 upscales stream strips instead: get_stream_tile.)
 TileCfg choose_tile(const rz_plan_s &p, int fam, int C, int batch, int stages, bool down2)
 {
     const int out_es = rz::fam_out_es(fam);

@@ -1,5 +1,5 @@
 // Resize kernels for sm_103a: uint8 and float32 resize and the normalise
-// epilogue (the 3x3 filter epilogue streams strips instead: filter.cu).
+// epilogue (the filter epilogues stream strips instead: stream.cu).
 //
 // Persistent CTAs (as many as fit on the GPU at once) walk the output tiles
 // of TR rows x TW columns in a static round-robin.  Each CTA is warp

@@ -1,5 +1,5 @@
-// Device helpers shared by the resize kernels (kernels.cu) and the 3x3
-// filter kernel (filter.cu): inline PTX for mbarriers, bulk (TMA) copies,
+// Device helpers shared by the kernels (kernels.cu, stream.cu, direct.cu,
+// filter.cu, multi.cu, texture.cu): inline PTX for mbarriers, bulk (TMA) copies,
 // programmatic dependent launch and cache policies, and the exact sampling
 // index the producers derive without touching the tables.  Nothing here is
 // part of the C ABI.

@@ -91,7 +91,7 @@ __host__ __device__ inline SmemLayout smem_layout(int fam, int C, int TR, int TW
     return L;
 }
 
-// Streaming kernels (stream.cu): the 3x3 filter family and the uint8
+// Streaming kernels (stream.cu): the K x K filter family and the uint8
 // bilinear resize in row-separable form.  Units of TW output columns by TR
 // output rows, whose source rows stream through a ring of chunks.  A chunk
 // holds up to chunk_rows rows; each row's span is cut into chunk_boxes blocks

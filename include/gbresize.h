@@ -12,10 +12,17 @@
  *    and neighbour indices clamped into the image (same page, §6.1);
  *  - nearest resize, OpenCV INTER_NEAREST: source index floor(dx * W / OW)
  *    (CUDA interpolation page §2.1, read as OpenCV's floor rule);
- *  - two epilogues fused into the bilinear kernel (CUDA interpolation page
- *    §4.2, operator fusion): per-channel normalisation to float32 planar
- *    (NCHW), and a 3x3 float filter (correlation, replicate border on the
- *    output grid; "OpenCL image convolution", §2).
+ *  - border rules for bilinear taps outside the source: clamp, mirror, wrap
+ *    (same page, §6.1; resize_plan_create_border);
+ *  - epilogues fused into the resize (CUDA interpolation page §4.2, operator
+ *    fusion): per-channel normalisation to float32 planar (NCHW); an odd K x K
+ *    float filter, 3x3 included (correlation, replicate border on the output
+ *    grid; "OpenCL image convolution", §2); grayscale conversion before the
+ *    resize ("Performance Optimization of Object Tracking Algorithms in
+ *    OpenCV on GPUs", §3.1.1);
+ *  - beside the method: the standalone K x K correlation over the valid
+ *    region, many geometries in one launch, a texture-unit comparison path
+ *    and an allocation-free uint8 entry.
  *
  * Numerics:
  *  - uint8 bilinear is exact integer arithmetic: 11-bit weights
@@ -363,12 +370,12 @@ RZ_API int resize_last_cuda_error(void);
 /*
  * Tile override for tuning (0 = automatic): output rows and output columns
  * per CTA for kernel family `kind` (RZ_U8, RZ_F32, or 2 + RZ_EPI_* for the
- * normalise and 3x3 kernels) of this plan.  Results do not depend on it; only speed does.
- * For the streaming kernels (the 3x3 filter family, uint8 bilinear upscales)
+ * normalise and filter kernels) of this plan.  Results do not depend on it; only speed does.
+ * For the streaming kernels (the filter family, uint8 bilinear upscales)
  * a tile is one streamed unit: tile_rows output rows of a strip of tile_cols
  * output columns (at most the kernel's widest strip).  A tile that does not
  * fit in shared memory makes the next call of that family fail with
- * RZ_ERR_ARG (RZ_ERR_UNSUPPORTED for the 3x3 filter family).
+ * RZ_ERR_ARG (RZ_ERR_UNSUPPORTED for the filter family).
  */
 RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_cols);
 
@@ -376,7 +383,7 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  * Tuning and testing options of a plan (results never depend on them):
  *   RZ_OPT_STAGES       value 0 (automatic) or 1..4: source tiles each CTA
  *                       keeps in flight ahead of the one it computes (all
- *                       families but the 3x3 filter, which streams rows);
+ *                       families but the filters, which stream rows);
  *   RZ_OPT_GENERIC_ONLY value 0 or 1: 1 disables the exact-ratio fast path
  *                       (uint8 2x downscale, used only when every table entry
  *                       is the 2x pattern, where it is bit-identical);
@@ -391,7 +398,7 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  *                       memory only after that kernel has completed);
  *   RZ_OPT_RING_ROWS    value 0 (automatic) or 2..128: source rows in the
  *                       shared-memory ring through which each CTA of a
- *                       streaming kernel (the 3x3 filter family; uint8
+ *                       streaming kernel (the filter family; uint8
  *                       bilinear upscales) streams its strip;
  *   RZ_OPT_U8_KERNEL    value 0 (automatic), 1, 2 or 3: which kernel runs
  *                       uint8-source resizes (plain, and the normalise

@@ -717,3 +717,42 @@ def test_back_to_back_dependent_resizes(rz):
     for p in (p1, p2, p3):
         assert rz.resize_plan_status(p) == rz.RZ_OK
         p.destroy()
+
+
+def test_one_plan_on_two_streams_at_once(rz):
+    # the plan's tables are read-only on the device: calls on different
+    # streams may share a plan and run concurrently
+    img_a = synth.smooth_rgb(1920, 1080, 2)
+    img_b = synth.random_u8((1080, 1920, 3), seed=8)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    a = torch.from_numpy(img_a).cuda()
+    b = torch.from_numpy(img_b).cuda()
+    oa = torch.zeros((720, 1280, 3), dtype=torch.uint8, device="cuda")
+    ob = torch.zeros((720, 1280, 3), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    with rz.resize_plan_create(1080, 1920, 720, 1280, rz.RZ_LINEAR) as plan:
+        for _ in range(20):
+            rz.resize_u8(plan, a, oa, stream=sa)
+            rz.resize_u8(plan, b, ob, stream=sb)
+        torch.cuda.synchronize()
+        assert rz.resize_plan_status(plan) == rz.RZ_OK
+    np.testing.assert_array_equal(oa.cpu().numpy(), oracle.linear_u8(img_a, 720, 1280))
+    np.testing.assert_array_equal(ob.cpu().numpy(), oracle.linear_u8(img_b, 720, 1280))
+
+
+def test_plans_on_many_streams(rz):
+    # independent plans of different geometries on their own streams
+    img = synth.random_u8((200, 300, 3), seed=12)
+    src = torch.from_numpy(img).cuda()
+    geoms = [(100, 150), (400, 600), (133, 77), (200, 300), (37, 512)]
+    streams = [torch.cuda.Stream() for _ in geoms]
+    outs = [torch.zeros((h, w, 3), dtype=torch.uint8, device="cuda") for h, w in geoms]
+    plans = [rz.resize_plan_create(200, 300, h, w, rz.RZ_LINEAR) for h, w in geoms]
+    torch.cuda.synchronize()
+    for _ in range(5):
+        for p, o, s in zip(plans, outs, streams):
+            rz.resize_u8(p, src, o, stream=s)
+    torch.cuda.synchronize()
+    for (h, w), o, p in zip(geoms, outs, plans):
+        np.testing.assert_array_equal(o.cpu().numpy(), oracle.linear_u8(img, h, w))
+        p.destroy()
