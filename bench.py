@@ -70,6 +70,8 @@ for _k in (8, 16, 32, 64):
         f"f32 4096x4096 {_k}x{_k} correlation over the valid region (standalone)", "valid", 4096, 4096,
         4097 - _k, 4097 - _k, 1, "none", 1)
 # border rule of a workload's plan (RZ_BORDER_*; clamp when absent)
+WORKLOADS["f32_8192_to_5980"] = ("f32 8192x8192 -> 5980x5980 bilinear (plain resize_f32)", "f32", 8192, 8192, 5980,
+                                  5980, 1, "linear", 1)
 WORKLOADS["4k_to_1080p_rgba"] = ("4K->1080p RGBA u8 bilinear (exact kernel)", "u8", 2160, 3840, 1080, 1920, 4,
                                   "linear", 1)
 WORKLOADS["4k_to_1080p_rgba_texture"] = ("4K->1080p RGBA u8 bilinear through the texture unit (hardware filtering, "
@@ -129,7 +131,7 @@ def algorithmic_bytes(kind, H, W, OH, OW, C, mode, batch):
     rows = set(int(r) for r in yofs)
     if m == rz.RZ_LINEAR:
         rows |= set(min(int(r) + 1, H - 1) for r in yofs)
-    in_es = 4 if kind == "filt" else 1
+    in_es = 4 if kind in ("filt", "f32") else 1
     out_es = 1 if kind in ("u8", "gray", "tex") else 4
     read = len(rows) * W * C * in_es
     write = OH * OW * (1 if kind == "gray" else C) * out_es
@@ -252,6 +254,8 @@ def make_outputs(kind, OH, OW, C, batch, count, dev):
         shape, dt = (OH, OW, C), torch.uint8
     elif kind == "gray":
         shape, dt = (OH, OW), torch.uint8
+    elif kind == "f32":
+        shape, dt = (OH, OW), torch.float32
     elif kind == "norm":
         shape, dt = (batch, C, OH, OW), torch.float32
     else:
@@ -288,7 +292,7 @@ def gpu_arm(args, rank, local_rank, world):
 
     rd, wr = algorithmic_bytes(kind, H, W, OH, OW, C, mode_s, batch)
     step_bytes = rd + wr
-    in_bytes = batch * H * W * C * (4 if kind == "filt" else 1)
+    in_bytes = batch * H * W * C * (4 if kind in ("filt", "f32") else 1)
     out_bytes = wr
     ring = max(2, min(64, int(3 * L2_BYTES // (in_bytes + out_bytes)) + 1))
     frames = make_frames(kind, H, W, C, batch, ring, dev)
@@ -319,6 +323,8 @@ def gpu_arm(args, rank, local_rank, world):
             rz.resize_u8(plan, s, d, stream=stream)
         elif kind == "tex":
             textures[i % ring].resize(d, stream=stream)
+        elif kind == "f32":
+            rz.resize_f32(plan, s, d, stream=stream)
         else:
             rz.resize_fused(plan, s, d, epi, stream=stream)
 
@@ -348,6 +354,8 @@ def gpu_arm(args, rank, local_rank, world):
             rz.resize_u8(plan, frames[0], ref0, stream=stream)
         elif kind == "tex":
             textures[0].resize(ref0, stream=stream)
+        elif kind == "f32":
+            rz.resize_f32(plan, frames[0], ref0, stream=stream)
         else:
             rz.resize_fused(plan, frames[0], ref0, epi, stream=stream)
         outs[0].zero_()
@@ -748,6 +756,11 @@ def oracle_rate(workload, budget_s):
         def run(rows):
             # output rows [0, rows) need input rows [0, rows + K - 1)
             return oracle.filter_valid(img[:rows + K - 1], wk)
+    elif kind == "f32":
+        img = synth.float_gray(W, H, 5)
+
+        def run(rows):
+            return oracle.linear_f32(img, OH, OW)
     else:
         img = synth.float_gray(W, H, 5)
         K = WORKLOAD_FILTER_K.get(workload, 3)
@@ -859,7 +872,7 @@ def profile_run(args):
         torch.cuda.synchronize()
         print(f"profile run: {args.warmup} + {args.profile} launches of {desc}")
         return
-    in_bytes = batch * H * W * C * (4 if kind == "filt" else 1)
+    in_bytes = batch * H * W * C * (4 if kind in ("filt", "f32") else 1)
     ring = max(2, min(64, int(3 * L2_BYTES // max(1, in_bytes)) + 1))
     frames = make_frames(kind, H, W, C, batch, ring, dev)
     outs = make_outputs(kind, OH, OW, C, batch, ring, dev)

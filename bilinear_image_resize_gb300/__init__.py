@@ -18,7 +18,7 @@ from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_BORD
                       RZ_BORDER_WRAP, RZ_EPI_FILTER, RZ_EPI_FILTER3X3, RZ_EPI_GRAY_BGR, RZ_EPI_GRAY_RGB, RZ_EPI_NORMALIZE_NCHW, RZ_ERR_ARG, RZ_ERR_CUDA, RZ_ERR_NOMEM, RZ_ERR_TIMEOUT,
                       RZ_ERR_UNSUPPORTED, RZ_F32, RZ_LINEAR, RZ_MAX_DIM, RZ_NEAREST, RZ_NOALLOC_MAX_DIM, RZ_OK,
                       RZ_OPT_CTAS_PER_SM, RZ_OPT_GENERIC_ONLY, RZ_OPT_GRID_MODE, RZ_OPT_PDL, RZ_OPT_RING_ROWS,
-                      RZ_MULTI_MAX_JOBS, RZ_OPT_FILTER_KERNEL, RZ_OPT_STAGES, RZ_OPT_U8_KERNEL, RZ_U8,
+                      RZ_MULTI_MAX_JOBS, RZ_OPT_F32_KERNEL, RZ_OPT_FILTER_KERNEL, RZ_OPT_STAGES, RZ_OPT_U8_KERNEL, RZ_U8,
                       RzEpilogue, RzJob)
 
 __all__ = [
@@ -29,7 +29,7 @@ __all__ = [
     "RZ_NOALLOC_MAX_DIM",
     "RZ_LINEAR", "RZ_NEAREST", "RZ_U8", "RZ_F32", "RZ_EPI_NORMALIZE_NCHW", "RZ_EPI_FILTER3X3",
     "RZ_EPI_GRAY_RGB", "RZ_EPI_GRAY_BGR", "RZ_BORDER_CLAMP", "RZ_BORDER_MIRROR", "RZ_BORDER_WRAP",
-    "resize_plan_create_border", "resize_axis_table_border", "RZ_EPI_FILTER", "RZ_OPT_FILTER_KERNEL",
+    "resize_plan_create_border", "resize_axis_table_border", "RZ_EPI_FILTER", "RZ_OPT_FILTER_KERNEL", "RZ_OPT_F32_KERNEL",
     "filter2d_valid_f32", "Texture", "resize_texture_create", "make_jobs", "resize_u8_multi",
     "RZ_MULTI_MAX_JOBS",
     "RZ_OK", "RZ_ERR_ARG", "RZ_ERR_UNSUPPORTED", "RZ_ERR_CUDA", "RZ_ERR_NOMEM", "RZ_ERR_TIMEOUT",

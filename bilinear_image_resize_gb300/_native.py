@@ -39,6 +39,7 @@ RZ_OPT_PDL = 5
 RZ_OPT_RING_ROWS = 6
 RZ_OPT_U8_KERNEL = 7
 RZ_OPT_FILTER_KERNEL = 8
+RZ_OPT_F32_KERNEL = 9
 
 # kernel families for resize_plan_set_tile
 KIND_U8 = 0

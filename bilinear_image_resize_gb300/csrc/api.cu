@@ -149,6 +149,7 @@ struct rz_plan_s {
     int opt_ring_rows = 0;     // streaming kernels: source rows in the ring (0: automatic)
     int opt_u8_kernel = 0;     // uint8 bilinear: 0 automatic, 1 staged tiles, 2 streaming, 3 direct
     int opt_filter_kernel = 0; // filter epilogues: 0 automatic, 1 streaming, 2 tile kernel
+    int opt_f32_kernel = 0;    // plain float32 bilinear: 0 automatic (streaming), 1 staged tiles
 };
 
 namespace {
@@ -527,6 +528,7 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
         // streamed once, neighbours by shuffle); the tile kernel (filter.cu)
         // for K = 1, for wrap plans, or when the option asks
         const int fopt = p->opt_filter_kernel;
+        if (a.ksize == 0) return false;   // the plain float32 resize (f32_family)
         if (a.ksize >= 3 && !wrap && fopt != 2) return false;
         if (fopt == 1) {
             *rc = RZ_ERR_UNSUPPORTED;
@@ -630,6 +632,23 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
     return launch(fn, groups);
 }
 
+// The kernel family of a plain float32 resize: bilinear clamp and mirror
+// plans run the streaming filter kernel with K = 1 and weight 1 (each
+// resized value m is stored as 1 * m = m; the source rows stream once, as for
+// the fused filters), unless the option or a float32 tile override asks for
+// the staged tiles; wrap plans take the direct float32 kernel, nearest the
+// staged tiles (and so does a geometry whose source span does not fit a
+// streamed strip: run falls back).
+int f32_family(const rz_plan_s *p, int mode, KArgs &extra)
+{
+    if (!p || mode != RZ_LINEAR || p->border == RZ_BORDER_WRAP || p->opt_f32_kernel != 0 ||
+        p->over_tr[rz::FAM_F32] > 0 || p->over_tw[rz::FAM_F32] > 0)
+        return rz::FAM_F32;
+    extra.ksize = 0;
+    extra.w[0] = 1.0f;
+    return rz::FAM_FILT;
+}
+
 // Shared body of every resize entry point.  `planes` > 0 selects the planar
 // (NCHW) output of the normalise epilogue.
 int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bstride, void *dst, size_t dst_pitch,
@@ -684,6 +703,12 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     TileCfg t;
     const void *fn = nullptr;
     rc = get_tile(p, fam, C, batch, &t, &fn, fam == rz::FAM_FILT ? a.ksize / 2 : 0);
+    if (rc == RZ_ERR_UNSUPPORTED && fam == rz::FAM_FILT && a.ksize == 0) {
+        // a plain float32 resize whose source span does not fit a streamed
+        // strip (very wide rows): the staged tiles take it
+        fam = rz::FAM_F32;
+        rc = get_tile(p, fam, C, batch, &t, &fn, 0);
+    }
     if (rc != RZ_OK) return rc;
     a.TR = t.TR; a.TW = t.TW; a.tiles_x = t.tiles_x; a.tiles_y = t.tiles_y;
     a.max_rows = t.max_rows; a.slot_bytes = t.slot_bytes; a.stages = t.stages;
@@ -912,6 +937,10 @@ int resize_plan_set_option(rz_plan p, int option, int value)
         if (value < 0 || value > 2) return RZ_ERR_ARG;
         p->opt_filter_kernel = value;
         break;
+    case RZ_OPT_F32_KERNEL:
+        if (value < 0 || value > 1) return RZ_ERR_ARG;
+        p->opt_f32_kernel = value;
+        break;
     default:
         return RZ_ERR_ARG;
     }
@@ -930,7 +959,8 @@ int resize_f32(rz_plan p, const float *src, size_t src_pitch, float *dst, size_t
                int out_h, int out_w, int mode, void *stream)
 {
     KArgs extra = {};
-    return run(p, rz::FAM_F32, src, src_pitch, 0, dst, dst_pitch, 0, H, W, C, out_h, out_w, mode, 1, extra, stream);
+    const int fam = f32_family(p, mode, extra);
+    return run(p, fam, src, src_pitch, 0, dst, dst_pitch, 0, H, W, C, out_h, out_w, mode, 1, extra, stream);
 }
 
 int resize_wait_selftest(int *dev_status, int limit_us, void *stream)
@@ -954,7 +984,8 @@ int resize_f32_batch(rz_plan p, const float *src, size_t src_pitch, size_t src_b
                      int mode, void *stream)
 {
     KArgs extra = {};
-    return run(p, rz::FAM_F32, src, src_pitch, src_batch_stride, dst, dst_pitch, dst_batch_stride, H, W, C, out_h,
+    const int fam = f32_family(p, mode, extra);
+    return run(p, fam, src, src_pitch, src_batch_stride, dst, dst_pitch, dst_batch_stride, H, W, C, out_h,
                out_w, mode, batch, extra, stream);
 }
 

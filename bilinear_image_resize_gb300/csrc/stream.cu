@@ -387,10 +387,11 @@ __device__ __forceinline__ bool consume_filter(const KArgs &a, const UnitGeom &g
                   (long long)g.dx0 * C * 4;
     // partial sums of the output rows resized row k contributes to: acc[j]
     // for output row k - 1 - j; each sums its K^2 products in the filter's
-    // row-major order
-    float acc[2 * R][NCOL][C];
+    // row-major order (none for K = 1: the plain resize, weight 1)
+    constexpr int NA = R > 0 ? 2 * R : 1;
+    float acc[NA][NCOL][C];
 #pragma unroll
-    for (int j = 0; j < 2 * R; j++)
+    for (int j = 0; j < NA; j++)
 #pragma unroll
         for (int i = 0; i < NCOL; i++)
 #pragma unroll
@@ -565,7 +566,7 @@ __device__ __forceinline__ bool consume_u8(const KArgs &a, const UnitGeom &g, co
 // would spill at two).
 __host__ __device__ constexpr int stream_min_ctas(int op, int C, int R)
 {
-    return op == STREAM_U8 ? 2 : (R == 1 ? 3 : (R == 3 && C > 1 ? 1 : 2));
+    return op == STREAM_U8 ? 2 : (R <= 1 ? 3 : (R == 3 && C > 1 ? 1 : 2));
 }
 
 template <int OP, int C, int LINEAR, int R>
@@ -623,11 +624,13 @@ __global__ void __launch_bounds__(kThreads, stream_min_ctas(OP, C, R))
 
 // Bilinear only: the fused entry point is bilinear by contract, and the
 // uint8 streaming form is chosen for bilinear resizes.  R: the filter's
-// halo (K = 2R + 1, 1..3); ignored for the uint8 form.
+// halo (K = 2R + 1, 0..3; R = 0 with weight 1 is the plain float32 resize);
+// ignored for the uint8 form.
 const void *stream_kernel_for(int op, int mode, int C, int R)
 {
     using Fn = void (*)(const KArgs, const CUtensorMap);
-    static const Fn filt[3][3] = {
+    static const Fn filt[4][3] = {
+        {k_stream<STREAM_FILTER, 1, 1, 0>, k_stream<STREAM_FILTER, 3, 1, 0>, k_stream<STREAM_FILTER, 4, 1, 0>},
         {k_stream<STREAM_FILTER, 1, 1, 1>, k_stream<STREAM_FILTER, 3, 1, 1>, k_stream<STREAM_FILTER, 4, 1, 1>},
         {k_stream<STREAM_FILTER, 1, 1, 2>, k_stream<STREAM_FILTER, 3, 1, 2>, k_stream<STREAM_FILTER, 4, 1, 2>},
         {k_stream<STREAM_FILTER, 1, 1, 3>, k_stream<STREAM_FILTER, 3, 1, 3>, k_stream<STREAM_FILTER, 4, 1, 3>}};
@@ -637,7 +640,7 @@ const void *stream_kernel_for(int op, int mode, int C, int R)
     if (ci < 0 || mode != RZ_LINEAR)
         return nullptr;
     if (op == STREAM_FILTER)
-        return (R >= 1 && R <= 3) ? reinterpret_cast<const void *>(filt[R - 1][ci]) : nullptr;
+        return (R >= 0 && R <= 3) ? reinterpret_cast<const void *>(filt[R][ci]) : nullptr;
     return reinterpret_cast<const void *>(u8[ci]);
 }
 

@@ -421,7 +421,12 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  *                       0: streaming for K = 3, 5, 7, the tile kernel for
  *                       K = 1 and under RZ_BORDER_WRAP; 1: streaming
  *                       (RZ_ERR_UNSUPPORTED for K = 1 or under wrap); 2: the
- *                       tile kernel.  Equal within float32 rounding.
+ *                       tile kernel.  Equal within float32 rounding;
+ *   RZ_OPT_F32_KERNEL   value 0 (automatic) or 1: which kernel runs the plain
+ *                       float32 bilinear resize under the clamp and mirror
+ *                       rules.  0: the streaming kernel (source rows streamed
+ *                       once through shared memory), unless a float32 tile
+ *                       override is set; 1: staged tiles.  Same arithmetic.
  * Returns RZ_ERR_ARG for an unknown option or value.
  */
 #define RZ_OPT_STAGES 1
@@ -432,6 +437,7 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
 #define RZ_OPT_RING_ROWS 6
 #define RZ_OPT_U8_KERNEL 7
 #define RZ_OPT_FILTER_KERNEL 8
+#define RZ_OPT_F32_KERNEL 9
 RZ_API int resize_plan_set_option(rz_plan p, int option, int value);
 
 /*

@@ -669,7 +669,8 @@ def test_options_reject_bad_values(rz):
         for opt, val in [(rz.RZ_OPT_STAGES, 5), (rz.RZ_OPT_STAGES, -1), (rz.RZ_OPT_GENERIC_ONLY, 2),
                          (rz.RZ_OPT_CTAS_PER_SM, 33), (rz.RZ_OPT_GRID_MODE, 2), (rz.RZ_OPT_PDL, 3),
                          (rz.RZ_OPT_RING_ROWS, 1), (rz.RZ_OPT_RING_ROWS, 129), (rz.RZ_OPT_U8_KERNEL, 4),
-                         (rz.RZ_OPT_U8_KERNEL, -1), (99, 0)]:
+                         (rz.RZ_OPT_U8_KERNEL, -1), (rz.RZ_OPT_F32_KERNEL, 2), (rz.RZ_OPT_F32_KERNEL, -1),
+                         (99, 0)]:
             with pytest.raises(rz.ResizeError):
                 rz.resize_plan_set_option(plan, opt, val)
 
@@ -756,3 +757,32 @@ def test_plans_on_many_streams(rz):
     for (h, w), o, p in zip(geoms, outs, plans):
         np.testing.assert_array_equal(o.cpu().numpy(), oracle.linear_u8(img, h, w))
         p.destroy()
+
+
+@pytest.mark.parametrize("C", [1, 3, 4])
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_f32_streaming_and_staged_kernels(rz, C, kernel):
+    # the plain float32 bilinear resize on the streaming kernel (K = 1
+    # filter, the default) and on staged tiles, over up- and downscales,
+    # ragged strips, padded and unaligned layouts, batches
+    for (H, W, OH, OW) in [(150, 170, 333, 201), (64, 700, 97, 1500), (300, 40, 130, 19), (1, 9, 5, 4),
+                           (512, 512, 373, 600)]:
+        img = synth.random_f32((H, W, C), seed=H + C)
+        for pitch, off in [(None, 0), (W * C + 3, 1)]:
+            src, _keep = device_image(img, pitch, off)
+            out = Canvas(OH, OW, C, torch.float32, 2)
+            with rz.resize_plan_create(H, W, OH, OW, rz.RZ_LINEAR) as plan:
+                rz.resize_plan_set_option(plan, rz.RZ_OPT_F32_KERNEL, kernel)
+                rz.resize_f32(plan, src, out.view)
+                torch.cuda.synchronize()
+                assert rz.resize_plan_status(plan) == rz.RZ_OK
+            out.check_canary()
+            assert max_abs(out.result(), oracle.linear_f32(img, OH, OW)) <= F32_TOL
+    frames = np.stack([synth.random_f32((40, 60, C), seed=n) for n in range(5)])
+    dst = torch.zeros((5, 70, 33, C), dtype=torch.float32, device="cuda")
+    with rz.resize_plan_create(40, 60, 70, 33, rz.RZ_LINEAR, border=1) as plan:
+        rz.resize_plan_set_option(plan, rz.RZ_OPT_F32_KERNEL, kernel)
+        rz.resize_f32_batch(plan, torch.from_numpy(frames).cuda(), dst)
+        torch.cuda.synchronize()
+    for n in range(5):
+        assert max_abs(dst[n].cpu().numpy(), oracle.linear_f32(frames[n], 70, 33, 1)) <= F32_TOL
