@@ -889,6 +889,8 @@ def profile_run(args):
             rz.resize_u8_batch(plan, *sets[i % 2])
         elif kind == "tex":
             textures[i % ring].resize(outs[i % ring])
+        elif kind == "f32":
+            rz.resize_f32(plan, frames[i % ring], outs[i % ring])
         elif kind == "u8":
             rz.resize_u8(plan, frames[i % ring], outs[i % ring])
         else:
