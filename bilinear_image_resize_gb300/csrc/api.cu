@@ -236,6 +236,22 @@ bool is_down2(const rz_plan_s &p)
     return true;
 }
 
+// True when the plan is an exact 3:2 downscale on both axes: output 2m
+// samples 3m + 1/4 (weight 512 on taps 3m, 3m + 1) and 2m + 1 samples
+// 3m + 7/4 (weight 1536 on taps 3m + 1, 3m + 2).
+bool is_down32(const rz_plan_s &p)
+{
+    if (p.mode != RZ_LINEAR || 2 * p.W != 3 * p.OW || 2 * p.H != 3 * p.OH) return false;
+    auto axis_ok = [](const std::vector<int32_t> &ofs, const std::vector<int32_t> &q, int n) {
+        for (int d = 0; d < n; d++) {
+            const int m = d / 2;
+            if (ofs[d] != (d & 1 ? 3 * m + 1 : 3 * m) || q[d] != (d & 1 ? 1536 : 512)) return false;
+        }
+        return true;
+    };
+    return axis_ok(p.xofs, p.xq, p.OW) && axis_ok(p.yofs, p.yq, p.OH);
+}
+
 // Automatic tile choice for persistent CTAs.  Plain resize and normalise:
 // rows as wide as the output (or the widest power-of-two strip whose staged
 // row stays within 16 KB), narrowed while there are fewer than about twelve
@@ -599,6 +615,17 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
             fn = rz::direct_down2_kernel_for(mode, C);
             const int px = rz::down2_px(C);
             groups = static_cast<long long>(a.OH) * ((a.OW + px - 1) / px);
+        }
+    }
+    if (!fn && fam == rz::FAM_U8 && !p->opt_generic && is_down32(*p)) {
+        // exact 3:2 downscale: eight output pixels of one row per thread
+        const uintptr_t sa = reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
+                             static_cast<uintptr_t>(a.src_bstride);
+        const uintptr_t da = reinterpret_cast<uintptr_t>(a.dst) | static_cast<uintptr_t>(a.dst_pitch) |
+                             static_cast<uintptr_t>(a.dst_bstride);
+        if (sa % 4 == 0 && da % 4 == 0) {
+            fn = rz::direct_down32_kernel_for(C);
+            groups = static_cast<long long>(a.OH) * ((a.OW + 7) / 8);
         }
     }
     const long long gpr = (a.OW + rz::kDirectRun - 1) / rz::kDirectRun;

@@ -202,6 +202,85 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
     }
 }
 
+// Exact 3:2 bilinear downscale of uint8 (W = 3 OW / 2, H = 3 OH / 2).  Output
+// column 2m samples x = 3m + 1/4 (taps 3m, 3m + 1 with weights 3/4, 1/4) and
+// 2m + 1 samples 3m + 7/4 (taps 3m + 1, 3m + 2 with 1/4, 3/4), the same for
+// rows, so the 11-bit weights are 1536 and 512 and the exact sum (B0 (A0 t0 +
+// A1 t1) + B1 (...) + 2^21) >> 22 equals (sum of b a t + 8) >> 4 with a, b in
+// {1, 3} (CUDA interpolation page §2.2, §6.2); no tap leaves the image.  A
+// thread forms eight output pixels of one row from the two source rows it
+// samples over twelve source columns: 12 C bytes per row in 3 C aligned
+// words, split into 16-bit lanes (even and odd bytes); the vertical 3-1 sum
+// is lane-wise, and each output byte takes (3 v + v' + 8) >> 4 from two
+// lanes at compile-time positions.  The row's last pixels
+// (fewer than eight) take a byte path.  Requirements, checked by the host:
+// source base, pitch and batch stride multiples of 4; output ones of 4.
+template <int C>
+__global__ void __launch_bounds__(kDirectThreads) k_down32_direct(const KArgs a, const __grid_constant__ CUtensorMap)
+{
+    constexpr int PX = 8;          // output pixels per thread
+    constexpr int NW = 3 * C;      // source words per row: 12 pixels
+    constexpr int NWO = 2 * C;     // output words: 8 pixels
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int full = a.OW / PX;
+    const int gpr = full + (a.OW % PX ? 1 : 0);
+    const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
+    if (idx >= a.OH * gpr)
+        return;
+    const int oy = idx / gpr, j = idx - oy * gpr;
+    // output row 2m + r: the source row weighted 3 is 3m (r = 0) or 3m + 2
+    // (r = 1), the one weighted 1 is 3m + 1
+    const int m = oy >> 1, r = oy & 1;
+    const int ya = 3 * m + 2 * r, yb = 3 * m + 1;
+    for (int b = blockIdx.y; b < a.batch; b += gridDim.y) {
+        const uint8_t *img = a.src + (long long)b * a.src_bstride;
+        const uint8_t *ra = img + (long long)ya * a.src_pitch;
+        const uint8_t *rb = img + (long long)yb * a.src_pitch;
+        uint8_t *o = a.dst + (long long)b * a.dst_bstride + (long long)oy * a.dst_pitch;
+        if (j < full) {
+            // vertical sums 3 a + b in 16-bit lanes (even and odd bytes)
+            uint32_t vl[NW], vh[NW];
+            const uint32_t *wa = reinterpret_cast<const uint32_t *>(ra + 12 * C * j);
+            const uint32_t *wb = reinterpret_cast<const uint32_t *>(rb + 12 * C * j);
+#pragma unroll
+            for (int i = 0; i < NW; i++) {
+                const uint32_t x = __ldcs(wa + i), y = __ldg(wb + i);
+                vl[i] = 3 * (x & 0x00ff00ffu) + (y & 0x00ff00ffu);
+                vh[i] = 3 * ((x >> 8) & 0x00ff00ffu) + ((y >> 8) & 0x00ff00ffu);
+            }
+            // the 16-bit lane of source byte e of the group (below 2^10)
+            auto lane = [&](int e) -> uint32_t {
+                const uint32_t wv = (e & 1) ? vh[e >> 2] : vl[e >> 2];
+                return ((e >> 1) & 1) ? (wv >> 16) : (wv & 0xffffu);
+            };
+            uint32_t *op = reinterpret_cast<uint32_t *>(o + PX * C * j);
+#pragma unroll
+            for (int wo = 0; wo < NWO; wo++) {
+                uint32_t q[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const int ob = 4 * wo + k, oc = ob / C, c = ob % C, i = oc >> 1;
+                    // output 2i: source 3i (3) and 3i + 1 (1); 2i + 1: 3i + 1 (1) and 3i + 2 (3)
+                    const uint32_t x3 = lane(((oc & 1) ? 3 * i + 2 : 3 * i) * C + c);
+                    const uint32_t x1 = lane((3 * i + 1) * C + c);
+                    q[k] = (3 * x3 + x1 + 8) >> 4;
+                }
+                __stcs(op + wo, q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24));
+            }
+        } else {
+            // the row's last pixels, fewer than eight: byte by byte
+            for (int ox = full * PX; ox < a.OW; ox++) {
+                const int i = ox >> 1, s3 = (ox & 1) ? 3 * i + 2 : 3 * i, s1 = 3 * i + 1;
+                for (int c = 0; c < C; c++) {
+                    const int v = 9 * ra[s3 * C + c] + 3 * ra[s1 * C + c] + 3 * rb[s3 * C + c] + rb[s1 * C + c];
+                    o[ox * C + c] = static_cast<uint8_t>((v + 8) >> 4);
+                }
+            }
+        }
+    }
+}
+
 // Exact 2x bilinear upscale of uint8 (OW = 2 W, OH = 2 H).  Output column
 // X = 2s samples x = s - 1/4 (taps s - 1, s with weights 1/4, 3/4) and
 // X = 2s + 1 samples x = s + 1/4 (taps s, s + 1 with 3/4, 1/4); the same for
@@ -851,6 +930,14 @@ const void *direct_up2_kernel_for(int C, int border)
     if (ci < 0 || border < 0 || border > 2)
         return nullptr;
     return reinterpret_cast<const void *>(k[border][ci]);
+}
+
+const void *direct_down32_kernel_for(int C)
+{
+    using Fn = void (*)(const KArgs, const CUtensorMap);
+    static const Fn k[3] = {k_down32_direct<1>, k_down32_direct<3>, k_down32_direct<4>};
+    const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
+    return ci < 0 ? nullptr : reinterpret_cast<const void *>(k[ci]);
 }
 
 const void *direct_rows_kernel_for(int C)

@@ -70,3 +70,30 @@ def test_gray_split_weights_and_division_by_1000():
     np.testing.assert_array_equal(y.reshape(4096, 4096).astype(np.uint8), oracle.gray_u8(rgb))
     t = np.arange(0, 255501, dtype=np.uint64)
     np.testing.assert_array_equal((t * np.uint64(4294968)) >> np.uint64(32), t // np.uint64(1000))
+
+
+def down32(img):
+    # exact 3:2 downscale: output 2m samples x = 3m + 1/4 (taps 3m, 3m+1 at
+    # 3/4, 1/4), output 2m+1 samples 3m + 7/4 (taps 3m+1, 3m+2 at 1/4, 3/4);
+    # the 11-bit weights are 1536 and 512, so the exact sum is the 9-3-3-1
+    # filter (sum of b a t + 8) >> 4
+    t = img.astype(np.int64)
+    H, W = t.shape[:2]
+    wts = [((0, 3), (1, 1)), ((1, 1), (2, 3))]     # (offset, weight) pairs for outputs 2m and 2m+1
+    out = np.zeros((2 * H // 3, 2 * W // 3, t.shape[2]), np.int64)
+    for j, ry in enumerate(wts):
+        for i, rx in enumerate(wts):
+            acc = 0
+            for (oy, wy) in ry:
+                for (ox, wx) in rx:
+                    acc = acc + wy * wx * t[oy::3, ox::3][:H // 3, :W // 3]
+            out[j::2, i::2] = (acc + 8) >> 4
+    return out.astype(np.uint8)
+
+
+@pytest.mark.parametrize("C", [1, 3, 4])
+def test_exact_3_to_2_downscale_is_the_9331_filter(C):
+    rng = np.random.default_rng(41 + C)
+    for (H, W) in [(3, 3), (3, 12), (9, 24), (30, 45), (1080, 1920)]:
+        img = rng.integers(0, 256, size=(H, W, C), dtype=np.uint8)
+        np.testing.assert_array_equal(down32(img), oracle.linear_u8(img, 2 * H // 3, 2 * W // 3))

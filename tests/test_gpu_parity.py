@@ -786,3 +786,25 @@ def test_f32_streaming_and_staged_kernels(rz, C, kernel):
         torch.cuda.synchronize()
     for n in range(5):
         assert max_abs(dst[n].cpu().numpy(), oracle.linear_f32(frames[n], 70, 33, 1)) <= F32_TOL
+
+
+@pytest.mark.parametrize("C", [1, 3, 4])
+def test_exact_3_to_2_downscale(rz, C):
+    # the exact 3:2 kernel (eight outputs by two rows per thread), its ragged
+    # row ends, layouts that send it to the generic kernel, and batches
+    for (H, W) in [(3, 3), (3, 12), (9, 24), (30, 45), (33, 57), (48, 96), (1080, 1920)]:
+        img = synth.random_u8((H, W, C), seed=H + W + C)
+        OH, OW = 2 * H // 3, 2 * W // 3
+        want = oracle.linear_u8(img, OH, OW)
+        np.testing.assert_array_equal(gpu_u8(rz, img, OH, OW, rz.RZ_LINEAR), want)
+        np.testing.assert_array_equal(gpu_u8(rz, img, OH, OW, rz.RZ_LINEAR, src_pitch=W * C + 1, src_off=3,
+                                             dst_pad=1), want)
+        np.testing.assert_array_equal(gpu_u8(rz, img, OH, OW, rz.RZ_LINEAR, opts=[(rz.RZ_OPT_GENERIC_ONLY, 1)]),
+                                      want)
+    frames = np.stack([synth.random_u8((45, 60, C), seed=n) for n in range(7)])
+    dst = torch.zeros((7, 30, 40, C), dtype=torch.uint8, device="cuda")
+    with rz.resize_plan_create(45, 60, 30, 40, rz.RZ_LINEAR) as plan:
+        rz.resize_u8_batch(plan, torch.from_numpy(frames).cuda(), dst)
+        torch.cuda.synchronize()
+    for n in range(7):
+        np.testing.assert_array_equal(dst[n].cpu().numpy(), oracle.linear_u8(frames[n], 30, 40))
