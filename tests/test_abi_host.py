@@ -251,3 +251,18 @@ def test_float_quotient_floor_is_within_one():
             for qv in (lo, q, hi):
                 qf = np.floor(qv).astype(np.int64)
                 assert np.all(np.abs(qf - exact) <= 1), (n_in, n_out)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without libgbresize.so every entry point raises: there is no CPU path
+    to fall back on."""
+    import bilinear_image_resize_gb300 as rz
+    from bilinear_image_resize_gb300 import _native
+    monkeypatch.setattr(_native, "library_path", lambda: str(tmp_path / "libgbresize.so"))
+    monkeypatch.setattr(_native, "_lib", None)
+    with pytest.raises(RuntimeError, match="is missing"):
+        _native.load()
+    with pytest.raises(RuntimeError, match="is missing"):
+        rz.resize_plan_create(16, 16, 8, 8, rz.RZ_LINEAR)
+    with pytest.raises(RuntimeError, match="is missing"):
+        rz.resize_axis_table(16, 8, rz.RZ_LINEAR)
