@@ -299,10 +299,12 @@ __global__ void __launch_bounds__(kDirectThreads) k_down32_direct(const KArgs a,
 // layout, assembled from clamped byte loads otherwise), byte e of the group
 // at bit 8 (e % 4) of word e / 4.  The arithmetic runs on two bytes at a time
 // in 16-bit lanes: word w splits into lo[w] (bytes 4w, 4w + 2) and hi[w]
-// (bytes 4w + 1, 4w + 3).  The vertical sums (1 3 and 3 1) are lane-wise; a
-// byte's horizontal neighbour C bytes away lies, for a whole lane pair, in one
-// register of the other or the same parity, or across two adjacent ones (one
-// byte permute).  Every lane stays below 2^16 (at most 16 * 255 + 8).
+// (bytes 4w + 1, 4w + 3).  The vertical sums (1 3 and 3 1) are lane-wise and
+// scaled by 16, with 32 added, so that the horizontal sum 3 x + x' of two of
+// them is 16 V + 128 and its high byte is the result; a byte's horizontal
+// neighbour C bytes away lies, for a whole lane pair, in one register of the
+// other or the same parity, or across two adjacent ones (one byte permute).
+// Every lane stays below 2^16 (at most 16 * 16 * 255 + 128).
 template <int C>
 struct Up2Layout {
     static constexpr int P = 4;                    // source columns per thread
@@ -325,8 +327,63 @@ __device__ __forceinline__ uint32_t lane_pair(const uint32_t (&lo)[NW], const ui
     return __byte_perm(src[w], src[w1], 0x5432);   // upper lane of word w, lower lane of w + 1
 }
 
+// One 32-bit word from four bytes: byte k is byte pos[k] of reg[k], where
+// equal id[k] name the same register.  All arguments are compile-time
+// constants after unrolling, so the branches fold: a word drawn from one or
+// two registers takes one byte permute, from three two, from four three.
+__device__ __forceinline__ uint32_t gather_bytes(const uint32_t (&reg)[4], const int (&id)[4],
+                                                 const uint32_t (&pos)[4])
+{
+    int slot[4], first[4], nd = 0;
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        slot[k] = -1;
+#pragma unroll
+        for (int j = 0; j < k; j++)
+            if (slot[k] < 0 && id[j] == id[k])
+                slot[k] = slot[j];
+        if (slot[k] < 0) {
+            slot[k] = nd;
+            first[nd] = k;
+            nd++;
+        }
+    }
+    if (nd <= 2) {
+        uint32_t sel = 0;
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            sel |= (pos[k] + 4u * static_cast<uint32_t>(slot[k])) << (4 * k);
+        return __byte_perm(reg[first[0]], nd == 2 ? reg[first[1]] : 0u, sel);
+    }
+    if (nd == 3) {
+        uint32_t s1 = 0, s2 = 0;
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            if (slot[k] < 2) {
+                s1 |= (pos[k] + 4u * static_cast<uint32_t>(slot[k])) << (4 * k);
+                s2 |= static_cast<uint32_t>(k) << (4 * k);
+            } else {
+                s2 |= (4u + pos[k]) << (4 * k);
+            }
+        }
+        return __byte_perm(__byte_perm(reg[first[0]], reg[first[1]], s1), reg[first[2]], s2);
+    }
+    const uint32_t lo2 = __byte_perm(reg[0], reg[1], pos[0] | ((4u + pos[1]) << 4));
+    const uint32_t hi2 = __byte_perm(reg[2], reg[3], pos[2] | ((4u + pos[3]) << 4));
+    return __byte_perm(lo2, hi2, 0x5410);
+}
+
+// CTAs per SM that the register budget of each form is set for: the most at
+// which that form compiles without spills (six for one and three channels,
+// five for three channels under mirror, four for four channels).  The kernel
+// is issue- and latency-bound, so more resident warps shorten it.
 template <int C, int BORDER>
-__global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a, const __grid_constant__ CUtensorMap)
+struct Up2Occupancy {
+    static constexpr int value = C == 4 ? 4 : (C == 3 && BORDER == RZ_BORDER_MIRROR ? 5 : 6);
+};
+
+template <int C, int BORDER>
+__global__ void __launch_bounds__(kDirectThreads, Up2Occupancy<C, BORDER>::value) k_up2_direct(const KArgs a, const __grid_constant__ CUtensorMap)
 {
     using Lay = Up2Layout<C>;
     constexpr int P = Lay::P, NB = Lay::NB, LEAD = Lay::LEAD, NW = Lay::NW, NWO = Lay::NWO;
@@ -377,13 +434,14 @@ __global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a,
         }
 #pragma unroll
         for (int j = 0; j < 2; j++) {
-            // vertical sums of output row 2r + j: rows (r - 1, r) weighted 1 3,
-            // or (r, r + 1) weighted 3 1
+            // vertical sums of output row 2r + j, scaled by 16 and carrying a
+            // quarter of the rounding term: 16 (t + 3 m) + 32 with t the
+            // source row r - 1 (j = 0) or r + 1 (j = 1), m row r
             uint32_t vl[NW], vh[NW];
 #pragma unroll
             for (int i = 0; i < NW; i++) {
-                vl[i] = j == 0 ? lo[0][i] + 3 * lo[1][i] : 3 * lo[1][i] + lo[2][i];
-                vh[i] = j == 0 ? hi[0][i] + 3 * hi[1][i] : 3 * hi[1][i] + hi[2][i];
+                vl[i] = 16 * lo[2 * j][i] + (48 * lo[1][i] + 0x00200020u);
+                vh[i] = 16 * hi[2 * j][i] + (48 * hi[1][i] + 0x00200020u);
             }
             // horizontal: for every pair register, the even output (left
             // neighbour 1, itself 3) and the odd output (itself 3, right 1)
@@ -401,32 +459,33 @@ __global__ void __launch_bounds__(kDirectThreads, 4) k_up2_direct(const KArgs a,
                         ev[par][i] = od[par][i] = 0;
                         continue;
                     }
-                    // each lane sum is below 2^12, so after the shift bytes 0
-                    // and 2 hold the two results exactly (the only bytes the
-                    // output permutes take); the other bits need no mask
+                    // each lane is 16 V + 128 with V the 9-3-3-1 sum, below
+                    // 2^16, so its high byte is (V + 8) >> 4: bytes 1 and 3
+                    // hold the two results (the only bytes the output
+                    // permutes take)
                     const uint32_t m3 = 3 * (par ? vh[i] : vl[i]);
                     const uint32_t l = lane_pair<NW>(vl, vh, e0 - C), rr = lane_pair<NW>(vl, vh, e0 + C);
-                    ev[par][i] = (l + m3 + 0x00080008u) >> 4;
-                    od[par][i] = (m3 + rr + 0x00080008u) >> 4;
+                    ev[par][i] = l + m3;
+                    od[par][i] = m3 + rr;
                 }
             // output byte ob: output column oc = ob / C, channel ob % C, from
             // group byte e = LEAD + (oc / 2 + 1) C + ob % C, even or odd
-            // output: byte 0 or 2 of its register, picked by byte permutes
+            // output: byte 1 or 3 of its register, picked by byte permutes
             uint32_t ow[NWO];
 #pragma unroll
             for (int wo = 0; wo < NWO; wo++) {
                 uint32_t reg[4];
+                int id[4];
                 uint32_t pos[4];
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
                     const int ob = 4 * wo + k, oc = ob / C;
                     const int e = LEAD + (oc / 2 + 1) * C + ob % C;
                     reg[k] = (oc & 1) ? od[e & 1][e >> 2] : ev[e & 1][e >> 2];
-                    pos[k] = ((e >> 1) & 1) ? 2u : 0u;
+                    id[k] = ((oc & 1) * 2 + (e & 1)) * NW + (e >> 2);
+                    pos[k] = ((e >> 1) & 1) ? 3u : 1u;
                 }
-                const uint32_t lo2 = __byte_perm(reg[0], reg[1], pos[0] | ((4u + pos[1]) << 4));
-                const uint32_t hi2 = __byte_perm(reg[2], reg[3], pos[2] | ((4u + pos[3]) << 4));
-                ow[wo] = __byte_perm(lo2, hi2, 0x5410);
+                ow[wo] = gather_bytes(reg, id, pos);
             }
             uint8_t *op = a.dst + (long long)b * a.dst_bstride + (long long)(2 * r + j) * a.dst_pitch +
                           (long long)(2 * s0) * C;
