@@ -20,6 +20,7 @@
 // floor(d n_in / n_out) (§2.1).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "rz_device.h"
@@ -94,7 +95,9 @@ __device__ __forceinline__ int2 entry(int n_in, int n_out, int d, bool linear)
 }
 
 template <int C, int LINEAR>
-__global__ void __launch_bounds__(kMultiThreads) k_multi(const rz_job *__restrict__ jobs, int njobs, int *status)
+// (registers capped for five resident CTAs per SM: a few words spill, and the
+// kernel, latency-bound, still runs faster with the extra warps)
+__global__ void __launch_bounds__(kMultiThreads, 5) k_multi(const rz_job *__restrict__ jobs, int njobs, int *status)
 {
     __shared__ long long pre[kMultiMaxJobs + 1];   // units before job j
     __shared__ long long warp_sum[kMultiThreads / 32];
@@ -248,7 +251,19 @@ int launch_multi(const rz_job *jobs, int njobs, int C, int mode, int *status, bo
     if (e != cudaSuccess)
         return static_cast<int>(e);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(sms * 8), 1, 1);
+    // two rounds of the CTAs that fit at once (each CTA walks an equal share
+    // of the units), the per-SM count asked of the runtime once per form
+    const Fn fn = k[mode == RZ_LINEAR ? 1 : 0][ci];
+    static std::atomic<int> resident[2][3];
+    int per_sm = resident[mode == RZ_LINEAR ? 1 : 0][ci].load(std::memory_order_relaxed);
+    if (per_sm <= 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kMultiThreads, 0);
+        if (e != cudaSuccess)
+            return static_cast<int>(e);
+        per_sm = per_sm > 0 ? per_sm : 1;
+        resident[mode == RZ_LINEAR ? 1 : 0][ci].store(per_sm, std::memory_order_relaxed);
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(sms * 2 * per_sm), 1, 1);
     cfg.blockDim = dim3(kMultiThreads, 1, 1);
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
@@ -256,7 +271,7 @@ int launch_multi(const rz_job *jobs, int njobs, int C, int mode, int *status, bo
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k[mode == RZ_LINEAR ? 1 : 0][ci], jobs, njobs, status);
+    e = cudaLaunchKernelEx(&cfg, fn, jobs, njobs, status);
     return static_cast<int>(e);
 }
 
