@@ -7,8 +7,11 @@
 // launch).  A persistent grid takes the work in units sized to the job: a
 // thread forms four consecutive output columns (a quad) on kMultiRows rows,
 // so a unit is kMultiRows rows of 256 quads for rows of 256 quads or more,
-// else P = 256 / quads-per-row row lanes side by side, each on kMultiRows
-// rows (P apart), so that narrow frames still keep the CTA busy.  Every CTA
+// else P row lanes side by side, each on kMultiRows rows (P apart), so that
+// narrow frames still keep the CTA busy: either P = 256 / quads-per-row whole
+// rows, or, where that leaves more threads idle, eight lanes of 32-quad
+// slices of the row (a 640-pixel row: five slices, every thread busy, where
+// one whole row per unit would idle 96 of the 256).  Every CTA
 // scans the jobs' unit counts into shared memory, then walks units
 // grid-stride, finding each unit's job by a binary search.  The arithmetic
 // is that of the plan-based kernels: sampling
@@ -34,17 +37,23 @@ using namespace dev;
 constexpr int kMultiThreads = 256;
 constexpr int kMultiRows = 8;   // output rows per thread in a unit
 
-// Unit shape of a job: quads per row, row lanes side by side, column units.
+// Unit shape of a job: quads per row lane, row lanes side by side, column
+// units (thread t takes quad cu qw + t % qw of row lane t / qw).
 struct UnitShape {
-    int qpr, P, col_units;
+    int qw, P, col_units;
 };
 
 __device__ __forceinline__ UnitShape unit_shape(const rz_job &j)
 {
     const int qpr = (j.out_w + 3) / 4;
     if (qpr >= kMultiThreads)
-        return {qpr, 1, (qpr + kMultiThreads - 1) / kMultiThreads};
-    return {qpr, kMultiThreads / qpr, 1};
+        return {kMultiThreads, 1, (qpr + kMultiThreads - 1) / kMultiThreads};
+    // whole rows keep P qpr of the 256 threads busy; 32-quad slices keep
+    // qpr / (32 n32) of them busy: the slices when 8 > P n32
+    const int P = kMultiThreads / qpr, n32 = (qpr + 31) / 32;
+    if (8 > P * n32)
+        return {32, kMultiThreads / 32, n32};
+    return {qpr, P, 1};
 }
 
 // An empty output (out_h or out_w 0) reads and writes nothing, so its
@@ -159,9 +168,8 @@ __global__ void __launch_bounds__(kMultiThreads, 5) k_multi(const rz_job *__rest
         const UnitShape sh = unit_shape(J);
         const int rb = static_cast<int>(local / sh.col_units);
         const int cu = static_cast<int>(local - static_cast<long long>(rb) * sh.col_units);
-        const int q = sh.P == 1 ? cu * kMultiThreads + static_cast<int>(threadIdx.x)
-                                : static_cast<int>(threadIdx.x) % sh.qpr;
-        const int p = sh.P == 1 ? 0 : static_cast<int>(threadIdx.x) / sh.qpr;   // row lane
+        const int p = static_cast<int>(threadIdx.x) / sh.qw;   // row lane
+        const int q = cu * sh.qw + static_cast<int>(threadIdx.x) - p * sh.qw;
         const int x0 = 4 * q;
         if (x0 >= J.out_w || p >= sh.P)
             continue;

@@ -47,7 +47,9 @@ def want(img, OH, OW, mode):
 
 
 MIX = [(48, 64, 96, 128), (37, 53, 100, 131), (90, 120, 37, 50), (33, 47, 33, 47), (1, 1, 1, 1), (1, 5, 4, 9),
-       (5, 1, 9, 3), (64, 64, 32, 32), (20, 300, 7, 11), (7, 3, 0, 5), (3, 7, 4, 0), (200, 150, 61, 1030)]
+       (5, 1, 9, 3), (64, 64, 32, 32), (20, 300, 7, 11), (7, 3, 0, 5), (3, 7, 4, 0), (200, 150, 61, 1030),
+       # rows cut into 32-quad slices: whole, ragged last slice, ragged last quad
+       (40, 320, 25, 640), (30, 200, 71, 530), (50, 101, 33, 371)]
 
 
 @pytest.mark.parametrize("C", [1, 3, 4])
