@@ -80,6 +80,26 @@ def test_u8_border_matches_scipy_at_dyadic_ratios(b, geom):
 
 
 @pytest.mark.parametrize("b", BORDERS)
+@pytest.mark.parametrize("geom", [(720, 1280, 224, 224), (1080, 1920, 719, 1279), (37, 53, 23, 41),
+                                  (13, 11, 29, 31), (100, 70, 31, 29), (8, 9, 3, 77)])
+def test_u8_within_weight_quantisation_of_exact_bilinear(b, geom):
+    # at ratios whose weights are not multiples of 2^-11 the u8 result is
+    # pinned by a bound: each 11-bit weight is within 2^-12 of the exact
+    # one, and the weights of an axis sum to one either way, so the weighted
+    # sum moves by at most 255 * (2^-12 + 2^-12) from the exact bilinear
+    # value; the result rounds that sum once
+    from scipy import ndimage
+    H, W, OH, OW = geom
+    img = np.random.default_rng(H + 3 * W + b).integers(0, 256, (H, W, 3), dtype=np.uint8)
+    got = oracle.linear_u8(img, OH, OW, b).astype(np.float64)
+    yy, xx = np.meshgrid(half_pixel(H, OH), half_pixel(W, OW), indexing="ij")
+    bound = 0.5 + 255 * 2 * 2.0 ** -12 + 1e-9
+    for c in range(3):
+        ref = ndimage.map_coordinates(img[:, :, c].astype(np.float64), [yy, xx], order=1, mode=SCIPY_MODE[b])
+        assert np.abs(got[:, :, c] - ref).max() <= bound
+
+
+@pytest.mark.parametrize("b", BORDERS)
 @pytest.mark.parametrize("k", [2, 4])
 def test_u8_border_is_clamp_resize_of_padded_image(b, k):
     # a k-times upscale samples x = d/k + (1-k)/(2k); padding the source by one
