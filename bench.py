@@ -961,7 +961,7 @@ def main():
                 "roofline": {"bound": "hbm", "achieved": r["gbs"], "peak": r["peak"], "unit": "GB/s",
                              "frac": r["gbs"] / r["peak"],
                              "peak_source": f"{r['peak_src']} HBM copy (MEASURED_PEAKS.json hbm_gbs)",
-                             "traffic": None},
+                             "traffic": profile_traffic(args.workload)},
                 "separate_launches": {"ms_per_step": r["ms_separate"],
                                       "value": r["px"] / (r["ms_separate"] / 1e3) / 1e9, "unit": "Gpix/s",
                                       "what": f"the same {r['jobs']} jobs as {r['jobs']} resize_u8 launches "
@@ -988,7 +988,7 @@ def main():
                 "roofline": {"bound": "alu", "achieved": r["tflops"], "peak": r["peak"], "unit": "TFLOP/s",
                              "frac": r["tflops"] / r["peak"],
                              "peak_source": "derived: 152 SMs x 128 FP32 FMA lanes x 2 FLOP x max SM clock",
-                             "traffic": None},
+                             "traffic": profile_traffic(args.workload)},
                 "cpu_baseline": {"value": v, "unit": "Gpix/s", "cores": 1, "kind": "oracle",
                                  "sample": f"{calls} bands of output rows in {dt:.1f} s, single-threaded C oracle"},
                 "e2e": None, "gpu_launches": r["steps"], "clocks": r["clocks"],

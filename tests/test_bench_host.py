@@ -58,3 +58,18 @@ def test_reference_arm_other_ranks_do_nothing(monkeypatch):
     with redirect_stdout(buf):
         assert bench.reference_arm(Args()) is None
     assert buf.getvalue() == ""
+
+
+def test_profile_traffic_only_for_current_sources(tmp_path, monkeypatch):
+    # the roofline's traffic comes from a committed ncu summary, and only
+    # while the kernel's sources hash to the value recorded in it
+    (tmp_path / "profiles").mkdir()
+    current = bench.kernel_sources_hash("multi.cu")
+    summary = ("kernel sources (multi.cu + headers) sha256[:16]: `{}`\n\n"
+               "dram bytes per launch: `123456` (read + write)\n")
+    (tmp_path / "profiles" / "ncu_fresh.md").write_text(summary.format(current))
+    (tmp_path / "profiles" / "ncu_stale.md").write_text(summary.format("0" * 16))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profile_traffic("fresh") == 123456
+    assert bench.profile_traffic("stale") is None
+    assert bench.profile_traffic("absent") is None
