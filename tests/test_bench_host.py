@@ -73,3 +73,26 @@ def test_profile_traffic_only_for_current_sources(tmp_path, monkeypatch):
     assert bench.profile_traffic("fresh") == 123456
     assert bench.profile_traffic("stale") is None
     assert bench.profile_traffic("absent") is None
+
+
+def test_reference_arm_line_carries_the_contract_keys(monkeypatch):
+    # rank 0 of the reference arm times the oracle on the host and prints one
+    # JSON line with the keys the driver reads (the oracle needs no GPU)
+    import json
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+
+    class Args:
+        workload, steps, warmup, cpu_budget = "4k_to_1080p", 1, 3, 0.1
+
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.reference_arm(Args())
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "Gpix/s"
+    assert line["value"] > 0 and line["higher_is_better"] is True and line["steps"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
