@@ -96,3 +96,21 @@ def test_reference_arm_line_carries_the_contract_keys(monkeypatch):
     assert line["value"] > 0 and line["higher_is_better"] is True and line["steps"] == 1
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+@pytest.mark.parametrize("workload, read, write", [
+    ("4k_to_1080p", 2160 * 3840 * 3, 1080 * 1920 * 3),             # every source row is a tap
+    ("4k_to_1080p_nearest", 1080 * 3840 * 3, 1080 * 1920 * 3),     # the even rows only
+    ("1080p_to_4k", 1080 * 1920 * 3, 2160 * 3840 * 3),
+    ("4k_to_1080p_gray", 2160 * 3840 * 3, 1080 * 1920),            # one gray byte out per pixel
+    # 720 -> 224: taps 3.2 rows apart, two distinct rows per output row
+    ("batch64_720p_to_224_norm", 64 * 448 * 1280 * 3, 64 * 3 * 224 * 224 * 4),
+    ("f32_8192_to_5980_filter3x3", 8192 * 8192 * 4, 5980 * 5980 * 4),
+])
+def test_algorithmic_bytes_of_the_workloads(workload, read, write):
+    # the roofline's numerator: source rows the taps read plus the output,
+    # against counts worked out by hand from the geometry
+    desc, kind, H, W, OH, OW, C, mode, batch = bench.WORKLOADS[workload]
+    from bilinear_image_resize_gb300 import _build
+    _build.build()
+    assert bench.algorithmic_bytes(kind, H, W, OH, OW, C, mode, batch) == (read, write)
