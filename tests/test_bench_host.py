@@ -114,3 +114,20 @@ def test_algorithmic_bytes_of_the_workloads(workload, read, write):
     from bilinear_image_resize_gb300 import _build
     _build.build()
     assert bench.algorithmic_bytes(kind, H, W, OH, OW, C, mode, batch) == (read, write)
+
+
+def test_clock_summary_reads_the_timed_window_and_reasons():
+    # nvidia-smi lines (csv, no header, no units) in the sampler's field
+    # order; only samples inside [t0, t1] count, and an "Active" throttle
+    # field is reported by name
+    s = bench.ClockSampler(0)
+
+    def line(sm, hw="Not Active", thermal="Not Active", power="Not Active"):
+        return f"2026/01/01 00:00:00.000, 0, {sm}, 2070, 900.0, 0x0, {hw}, {thermal}, Not Active, {power}"
+
+    s.samples = [(0.5, line(600)), (1.0, line(2070)), (1.1, line(2055, power="Active")), (1.2, line(2070)),
+                 (2.5, line(1000, hw="Active")), (1.3, "garbage")]
+    got = s.summary(0.9, 1.3)
+    assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert s.summary(2.0, 3.0)["reasons"] == ["hw_slowdown"]
+    assert s.summary(5.0, 6.0) == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
