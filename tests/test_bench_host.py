@@ -1,9 +1,14 @@
-"""Host logic of bench.py's multi-process path, on CPU ranks (gloo).
+"""Host logic of bench.py, no GPU needed.
 
-Each rank runs its own replica (no exchange step on the data path); the
-reported time is the slowest rank's, taken by an all-reduce MAX, and the
-value aggregates every rank's work over that time.  Ranks other than 0 do
-no work in the reference (oracle) arm.
+* The multi-process path on CPU ranks (gloo): each rank runs its own
+  replica (no exchange step on the data path); the reported time is the
+  slowest rank's, taken by an all-reduce MAX, and the value aggregates every
+  rank's work over that time.  Ranks other than 0 do no work in the
+  reference (oracle) arm, and rank 0's line carries the contract's keys.
+* The roofline's inputs: algorithmic bytes per launch against hand counts,
+  DRAM traffic only from an ncu summary of the current kernel sources.
+* The clock record: median SM clock inside the timed window, active
+  throttle reasons by name.
 """
 import io
 import os
