@@ -266,3 +266,51 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         rz.resize_plan_create(16, 16, 8, 8, rz.RZ_LINEAR)
     with pytest.raises(RuntimeError, match="is missing"):
         rz.resize_axis_table(16, 8, rz.RZ_LINEAR)
+
+
+def declared_prototypes():
+    """name -> (return type, [parameter types]) of every RZ_API declaration."""
+    with open(os.path.join(ROOT, "include", "gbresize.h")) as f:
+        text = f.read()
+    out = {}
+    for m in re.finditer(r"^RZ_API\s+([\w\s\*]+?)\b(\w+)\s*\(([^)]*)\)\s*;", text, flags=re.M):
+        ret, name, params = m.group(1).strip(), m.group(2), m.group(3).strip()
+        types = []
+        if params and params != "void":
+            for p in params.split(","):
+                p = " ".join(p.split())
+                # drop the parameter's name: the last identifier after the type
+                types.append(re.sub(r"\s*\b\w+$", "", p) if not p.endswith("*") else p)
+        out[name] = (ret, types)
+    return out
+
+
+def _kind_of_c(t):
+    t = t.replace("const ", "").strip()
+    if "*" in t or t in ("rz_plan", "rz_tex"):
+        return "pointer"
+    return {"int": "int", "size_t": "size_t", "char": "char"}[t]
+
+
+def _kind_of_ctypes(t):
+    if t is ctypes.c_void_p or t is ctypes.c_char_p or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+        return "pointer"
+    if t is ctypes.c_int:
+        return "int"
+    if t is ctypes.c_size_t:
+        return "size_t"
+    raise AssertionError(f"unexpected ctypes type {t}")
+
+
+def test_binding_signatures_match_the_header():
+    # every argument the binding passes has the kind (pointer, int, size_t)
+    # the C prototype declares, in the same order, and the return kinds agree
+    from bilinear_image_resize_gb300 import _native
+    protos = declared_prototypes()
+    assert set(protos) == set(_native.SIGNATURES)
+    for name, (ret, params) in protos.items():
+        res, args = _native.SIGNATURES[name]
+        assert len(args) == len(params), (name, params)
+        for i, (c, py) in enumerate(zip(params, args)):
+            assert _kind_of_c(c) == _kind_of_ctypes(py), (name, i, c, py)
+        assert _kind_of_c(ret) == _kind_of_ctypes(res), (name, ret, res)
