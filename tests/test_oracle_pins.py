@@ -97,7 +97,8 @@ def test_identity_with_padded_pitch():
     np.testing.assert_array_equal(oracle.linear_u8(view, 10, 17), np.ascontiguousarray(view))
 
 
-@pytest.mark.parametrize("geom", [(5, 7, 13, 2), (48, 64, 96, 128), (9, 9, 1, 1), (1, 1, 7, 5), (30, 20, 11, 47)])
+@pytest.mark.parametrize("geom", [(5, 7, 13, 2), (48, 64, 96, 128), (9, 9, 1, 1), (1, 1, 7, 5), (30, 20, 11, 47),
+                                  (2, 65536, 3, 65535), (65536, 1, 65535, 2), (1, 65535, 1, 65536)])
 def test_constant_image_stays_constant(geom):
     H, W, OH, OW = geom
     for k in (0, 1, 77, 254, 255):
@@ -127,7 +128,8 @@ def test_exact_2x_ramp_upscale_2d_u8():
     np.testing.assert_array_equal(out, d[:, None] + d[None, :])
 
 
-@pytest.mark.parametrize("geom", [(8192, 5980), (1280, 224), (720, 224), (3, 4096), (97, 13), (13, 97), (64, 128)])
+@pytest.mark.parametrize("geom", [(8192, 5980), (1280, 224), (720, 224), (3, 4096), (97, 13), (13, 97), (64, 128),
+                                  (65536, 65535), (65535, 65536), (65536, 3), (2, 65536)])
 def test_affine_ramp_reproduced_f32(geom):
     # bilinear interpolation reproduces an affine function exactly at the mapped
     # point, clamped into the image: out = a*clamp(x) + b*clamp(y) + c
