@@ -192,3 +192,13 @@ def test_gray_bgr_order_reverses_channels():
     img = np.random.default_rng(2).integers(0, 256, (17, 23, 3), dtype=np.uint8)
     np.testing.assert_array_equal(oracle.gray_u8(img, bgr=True), oracle.gray_u8(img[..., ::-1].copy()))
     assert not np.array_equal(oracle.gray_u8(img, bgr=True), oracle.gray_u8(img))
+
+
+@pytest.mark.parametrize("b", BORDERS)
+def test_row_band_equals_the_whole_resize(b):
+    # the band form the benchmark times computes the same rows as the whole
+    # resize (its rows are independent of one another)
+    img = np.random.default_rng(23).integers(0, 256, (41, 37, 3), dtype=np.uint8)
+    whole = oracle.linear_u8(img, 29, 53, b)
+    for dy0, dy1 in [(0, 29), (0, 1), (5, 17), (28, 29), (10, 10)]:
+        np.testing.assert_array_equal(oracle.linear_u8_rows(img, 29, 53, dy0, dy1, b), whole[dy0:dy1])
