@@ -3,18 +3,23 @@
 One step = one bilinear resize of a 3840x2160 RGB u8 frame to 1920x1080
 through the C ABI (resize_u8), the whole hot path (tables come from the plan,
 built once per geometry, outside the timed region).  The frames are the
-smooth synthetic content (sum of sinusoids + noise) in a ring of 16 device
-frames (498 MB of source + output, over 3x the 129 MB L2), so every step
-reads its input from HBM.  Steps are replayed from CUDA graphs of 96 launches
-(one launch per step, back to back on one stream); K steps are timed with
-CUDA events after W warm-up steps, with a barrier and device synchronise on
-both sides.
+smooth synthetic content (sum of sinusoids + noise) in a ring of distinct
+device input/output sets (14 for this workload, 435 MB, over 3x the 129 MB
+L2), so every step reads its input from HBM.  The K timed steps are one CUDA
+graph of K launches (back to back on one stream; graphs of at most 4096
+launches when K is larger), replayed once between two CUDA events, after W
+warm-up steps, with a barrier and device synchronise on both sides.  A short
+device-side hold queued before the start event keeps host submission latency
+out of the timed region.
 
 Printed (one JSON line): output Gpix/s (`value`), the dominant kernel's
 roofline (algorithmic bytes per launch / average launch duration, against the
-measured HBM copy peak), the end-to-end figure through resize_u8_host from
-page-locked host buffers, the oracle timed on the host cores, and the SM
-clocks sampled during the timed region.
+measured HBM copy peak), a trimmed mean over further timed replays, the
+library's 1:1 copy baseline moving the same bytes, the end-to-end figure
+through resize_u8_host from page-locked host buffers, the oracle timed on the
+host cores (median of three samples, with the host's core count and CPU
+model), and the SM clocks sampled during the timed region and during the
+busy period just before it.
 
 `--impl reference` times the CPU oracle (the only other implementation of the
 method) on the same workload instead, each step a bounded band of output rows.
@@ -39,6 +44,10 @@ sys.path.insert(0, ROOT)
 
 MB = 1e6
 L2_BYTES = 129 * 1024 * 1024
+GRAPH_MAX = 4096        # launches per captured graph
+SETTLE_S = 0.5          # seconds of graph replays right before the timed region
+TRIM_REPLAYS = 11       # extra timed graph replays for the trimmed mean
+HOLD_CYCLES = 2_000_000  # device hold before a start event (about 1 ms at 2 GHz)
 CSRC = os.path.join(ROOT, "bilinear_image_resize_gb300", "csrc")
 
 # name -> (description, kind, H, W, OH, OW, C, mode, batch)
@@ -80,6 +89,10 @@ WORKLOADS["multi_256_mixed"] = ("256 RGB u8 bilinear resizes of 4 mixed small ge
                                  "1280x720->224x224, 320x240->640x480, 800x600->300x300) in one launch",
                                  "multi", 0, 0, 0, 0, 3, "linear", 256)
 MULTI_GEOMS = [(480, 640, 240, 320), (720, 1280, 224, 224), (240, 320, 480, 640), (600, 800, 300, 300)]
+WORKLOADS["1080p_to_540p_and_720p"] = ("1080p RGB u8 -> 960x540 and -> 1280x720 bilinear, both resizes of each frame "
+                                       "in one CUDA graph (two resize_u8 launches per step)", "pair", 1080, 1920,
+                                       0, 0, 3, "linear", 1)
+PAIR_GEOMS = [(540, 960), (720, 1280)]
 WORKLOAD_BORDER = {"1080p_to_4k_mirror": 1, "1080p_to_4k_wrap": 2}
 # filter width of the filter workloads (3 when absent)
 WORKLOAD_FILTER_K = {f"f32_8192_to_5980_filter{k}x{k}": k for k in (5, 7)}
@@ -89,6 +102,47 @@ WORKLOAD_FILTER_K.update({f"f32_4096_valid_filter{k}": k for k in (8, 16, 32, 64
 def fp32_fma_peak_tflops(sm_mhz=2070.0, sms=152):
     """FP32 peak from unit counts and clocks: sms x 128 FMA lanes x 2 FLOP x clock."""
     return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def trimmed_mean(xs, frac=0.1):
+    """Mean after sorting and dropping `frac` of the samples at each end (the
+    Volcanic page's *Measure performance carefully*: discard outliers, then
+    average); at least one sample is kept."""
+    v = sorted(float(x) for x in xs)
+    if not v:
+        raise ValueError("no samples")
+    k = int(len(v) * frac)
+    if 2 * k >= len(v):
+        k = (len(v) - 1) // 2
+    v = v[k:len(v) - k]
+    return sum(v) / len(v)
+
+
+def host_cpu():
+    """Core count and CPU model of this host (lscpu, else /proc/cpuinfo)."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    key = line.split(":", 1)[0].strip().lower()
+                    if key in ("model name", "cpu part") and ":" in line:
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"cpu_count": os.cpu_count(), "model": model or "unknown", "machine": platform.machine()}
+
+
 DEFAULT_WORKLOAD = "4k_to_1080p"
 METRIC = "output Gpix/s and achieved HBM GB/s (% of GB300 peak), 4K->1080p RGB u8 bilinear"
 
@@ -335,9 +389,9 @@ def gpu_arm(args, rank, local_rank, world):
             step(i)
     torch.cuda.synchronize()
 
-    G = min(96, max(1, args.steps))
-    G -= G % ring if G >= ring else 0
-    G = max(G, 1)
+    # the K timed steps as graphs of at most GRAPH_MAX launches: one graph
+    # for any K up to GRAPH_MAX, so the timed region has no gap between graphs
+    G = max(1, min(args.steps, GRAPH_MAX))
 
     def capture(n):
         g = torch.cuda.CUDAGraph()
@@ -380,11 +434,15 @@ def gpu_arm(args, rank, local_rank, world):
     sampler = ClockSampler(visible[local_rank] if local_rank < len(visible) else local_rank)
     sampler.start()
     time.sleep(0.3)
-    # a short busy period before the timed region so clocks settle
-    with torch.cuda.stream(stream):
-        for _ in range(20):
-            g_full.replay()
-    torch.cuda.synchronize()
+    # a busy period right before the timed region (clocks settle; the sampler
+    # records them: the timed region itself is often shorter than its period)
+    t_settle0 = time.time()
+    while time.time() - t_settle0 < SETTLE_S:
+        with torch.cuda.stream(stream):
+            for _ in range(8):
+                g_full.replay()
+        torch.cuda.synchronize()
+    t_settle1 = time.time()
 
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -393,6 +451,7 @@ def gpu_arm(args, rank, local_rank, world):
     torch.cuda.synchronize()
     t_host0 = time.time()
     with torch.cuda.stream(stream):
+        hold_stream(stream)
         ev0.record(stream)
         for _ in range(reps):
             g_full.replay()
@@ -404,9 +463,26 @@ def gpu_arm(args, rank, local_rank, world):
     if dist:
         dist.barrier()
     ms = ev0.elapsed_time(ev1)
+
+    # further timed replays of the first graph, one event pair each, for the
+    # trimmed mean (not part of the contract's timed region)
+    per_launch_us = []
+    for _ in range(TRIM_REPLAYS):
+        with torch.cuda.stream(stream):
+            hold_stream(stream)
+            ev0.record(stream)
+            g_full.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        per_launch_us.append(ev0.elapsed_time(ev1) * 1e3 / G)
     time.sleep(0.1)
     sampler.stop()
     clocks = sampler.summary(t_host0 - 0.02, t_host1 + 0.02)
+    clocks["settle"] = sampler.summary(t_settle0, t_settle1)
+    replays = {"launches_per_replay": G, "replays": len(per_launch_us),
+               "per_launch_us": [round(x, 4) for x in per_launch_us],
+               "trimmed_mean_us": trimmed_mean(per_launch_us), "median_us": statistics.median(per_launch_us),
+               "trim": "10% of the sorted samples dropped at each end"}
 
     ms_max = max_over_ranks(ms, dist, dev) if dist else ms
 
@@ -426,9 +502,9 @@ def gpu_arm(args, rank, local_rank, world):
     if kind == "u8":
         e2e = e2e_u8(rz, plan, frames[0], H, W, OH, OW, C, dev, n=max(10, min(args.steps, 200)))
 
-    # the achievable ceiling for this byte count: torch's device copy of
-    # (read + write) / 2 bytes per step, same ring rotation, graph replays
-    ceiling = copy_ceiling(step_bytes, ring, stream, dev)
+    # the 1:1 copy baseline moving this step's bytes (half read, half
+    # written), timed the same way
+    ceiling = copy_baseline(rz, step_bytes, ring, stream, dev, G)
 
     # several frames per launch (resize_u8_batch), u8 workloads
     batched = None
@@ -445,7 +521,7 @@ def gpu_arm(args, rank, local_rank, world):
         "value": value, "ms": ms_max, "launch_ms": launch_ms, "eager_ms_per_step": eager_ms,
         "achieved_gbs": achieved, "peak_gbs": peak, "peak_src": src, "step_bytes": step_bytes,
         "read_bytes": rd, "write_bytes": wr, "ring": ring, "graph_steps": G, "clocks": clocks, "e2e": e2e,
-        "desc": desc, "px": px, "batched": batched, "copy_ceiling": ceiling,
+        "desc": desc, "px": px, "batched": batched, "copy_ceiling": ceiling, "replays": replays,
     }
     for t in textures or ():
         t.destroy()
@@ -502,6 +578,7 @@ def valid_arm(args, local_rank):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.time()
     with torch.cuda.stream(stream):
+        hold_stream(stream)
         ev0.record(stream)
         for _ in range(reps):
             g.replay()
@@ -573,6 +650,7 @@ def multi_arm(args, local_rank):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
+            hold_stream(stream)
             e0.record(stream)
             for _ in range(reps):
                 g.replay()
@@ -610,32 +688,145 @@ def multi_arm(args, local_rank):
             "steps": reps * 4, "clocks": sampler.summary(t0 - 0.02, t1 + 0.02), "desc": desc, "jobs": N}
 
 
-def copy_ceiling(step_bytes, ring, stream, dev, reps=8):
-    """GB/s of a plain device copy moving the step's byte count (half read,
-    half written), over a ring of buffers, graph-replayed and event-timed:
-    what one launch of this size can reach on this GPU."""
+def pair_arm(args, local_rank):
+    """The two 1080p downscales (to 960x540, exact 2x; to 1280x720, exact
+    3:2) of each frame as one step, K steps captured in one CUDA graph on one
+    stream (2K launches), over a ring of frames larger than L2, timed between
+    events after a device hold."""
+    import numpy as np
     import torch
-    n = max(16, step_bytes // 2 // 16 * 16)
-    srcs = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(ring)]
-    dsts = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(ring)]
-    g = torch.cuda.CUDAGraph()
-    k = max(ring, 48 // ring * ring)
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(k):
-            dsts[i % ring].copy_(srcs[i % ring])
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            g.replay()
+
+    import bilinear_image_resize_gb300 as rz
+    from bilinear_image_resize_gb300 import synth
+    desc, kind, H, W, _OH, _OW, C, _m, _b = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    rd = wr = 0
+    for oh, ow in PAIR_GEOMS:
+        r_, w_ = algorithmic_bytes("u8", H, W, oh, ow, C, "linear", 1)
+        rd, wr = rd + r_, wr + w_
+    per_set = H * W * C + sum(oh * ow * C for oh, ow in PAIR_GEOMS)
+    ring = max(2, int(3 * L2_BYTES // per_set) + 1)
+    base = torch.from_numpy(np.ascontiguousarray(synth.smooth_rgb(W, H, 2))).to(dev)
+    frames = [torch.roll(base, 7 * i, 1).contiguous() for i in range(ring)]
+    outs = [[torch.empty((oh, ow, C), dtype=torch.uint8, device=dev) for oh, ow in PAIR_GEOMS] for _ in range(ring)]
+    plans = [rz.resize_plan_create(H, W, oh, ow, rz.RZ_LINEAR) for oh, ow in PAIR_GEOMS]
+    px = sum(oh * ow for oh, ow in PAIR_GEOMS)
+
+    def step(i):
+        for p_, d_ in zip(plans, outs[i % ring]):
+            rz.resize_u8(p_, frames[i % ring], d_, stream=stream)
+
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize()
+    ref = [d.clone() for d in outs[0]]
+    G = max(1, min(args.steps, GRAPH_MAX))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(G):
+            step(i)
+    with torch.cuda.stream(stream):
+        for d in outs[0]:
+            d.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    if not all(torch.equal(a, b) for a, b in zip(ref, outs[0])):
+        raise RuntimeError("captured graph did not reproduce the eager result")
+    reps = max(1, args.steps // G)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    t_settle0 = time.time()
+    while time.time() - t_settle0 < SETTLE_S:
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+    t_settle1 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        hold_stream(stream)
         e0.record(stream)
         for _ in range(reps):
             g.replay()
         e1.record(stream)
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / (reps * k)
-    return {"gbs": 2 * n / (us * 1e-6) / 1e9, "us_per_copy": us, "bytes_moved": 2 * n, "what": "torch device copy"}
+    t1 = time.time()
+    ms = e0.elapsed_time(e1) / (reps * G)
+    time.sleep(0.1)
+    sampler.stop()
+    clocks = sampler.summary(t0 - 0.02, t1 + 0.02)
+    clocks["settle"] = sampler.summary(t_settle0, t_settle1)
+    peaks, src = measured_peaks()
+    for p_ in plans:
+        p_.destroy()
+    gbs = (rd + wr) / (ms / 1e3) / 1e9
+    return {"ms": ms, "value": px / (ms / 1e3) / 1e9, "gbs": gbs, "peak": float(peaks.get("hbm_gbs", 6800.0)),
+            "peak_src": src, "bytes": rd + wr, "px": px, "steps": reps * G, "clocks": clocks, "desc": desc,
+            "ring": ring, "graph_steps": G}
+
+
+def hold_stream(stream):
+    """Queue a short device-side wait (torch's spin kernel, about 1 ms) on
+    `stream`, so that the host has queued the events and graphs that follow
+    before the device reaches them: host submission latency stays out of the
+    timed region.  A no-op where torch lacks the helper."""
+    import torch
+    if hasattr(torch.cuda, "_sleep"):
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(HOLD_CYCLES)
+
+
+def copy_baseline(rz, step_bytes, ring, stream, dev, launches):
+    """The library's 1:1 copy baseline (resize_copy_baseline: 256-thread
+    CTAs, 16-byte loads and stores, PDL, pre-wait L2 prefetch) moving the
+    step's byte count (half read, half written) over a ring of buffers, timed
+    like the resize (one graph of `launches` launches between events after a
+    device hold); also without the prefetch, and without PDL."""
+    import torch
+    n = max(16, step_bytes // 2 // 16 * 16)
+    srcs = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(ring)]
+    dsts = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(ring)]
+    srcs[0].copy_(torch.randint(0, 256, (n,), dtype=torch.uint8, device=dev))
+    with torch.cuda.stream(stream):
+        rz.resize_copy_baseline(srcs[0], dsts[0], stream=stream)
+    torch.cuda.synchronize()
+    if not torch.equal(srcs[0], dsts[0]):
+        raise RuntimeError("resize_copy_baseline did not copy its source")
+    k = max(launches, ring)
+
+    def timed(flags):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(k):
+                rz.resize_copy_baseline(srcs[i % ring], dsts[i % ring], flags, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        us = []
+        for _ in range(5):
+            with torch.cuda.stream(stream):
+                hold_stream(stream)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us.append(e0.elapsed_time(e1) * 1e3 / k)
+        return statistics.median(us)
+
+    us = timed(rz.RZ_COPY_PDL | rz.RZ_COPY_L2_PREFETCH)
+    us_np = timed(rz.RZ_COPY_PDL)
+    us_plain = timed(0)
+    return {"what": "resize_copy_baseline (1:1 copy kernel: 256-thread CTAs, 16-byte loads and stores, PDL, "
+                    "pre-wait L2 prefetch)", "bytes_moved": 2 * n, "us_per_copy": us,
+            "gbs": 2 * n / (us * 1e-6) / 1e9, "us_per_copy_no_prefetch": us_np, "us_per_copy_no_pdl": us_plain,
+            "launches_per_replay": k, "statistic": "median of 5 graph replays"}
 
 
 def batched_u8(rz, plan, frames, H, W, OH, OW, C, nf, stream, dev, frame_bytes, launches=48):
@@ -742,6 +933,12 @@ def oracle_rate(workload, budget_s):
 
         def run(rows):
             return oracle.linear_u8_normalize(frames[0], OH, OW, synth.NORM_MEAN, synth.NORM_STD)
+    elif kind == "pair":
+        img = synth.smooth_rgb(W, H, 2)
+        OH, OW = 1, sum(oh * ow for oh, ow in PAIR_GEOMS)   # pixels of one step (both outputs)
+
+        def run(rows):
+            return [oracle.linear_u8(img, oh, ow) for oh, ow in PAIR_GEOMS]
     elif kind == "multi":
         imgs = [synth.random_u8((g[0], g[1], C), seed=11 + i) for i, g in enumerate(MULTI_GEOMS)]
         OH, OW = 1, sum(g[2] * g[3] for g in MULTI_GEOMS)   # pixels of one pass over the geometries
@@ -795,6 +992,16 @@ def oracle_rate(workload, budget_s):
     return n_px / dt / 1e9, calls, dt, probe
 
 
+def oracle_sample(workload, budget_s, unit="Gpix/s"):
+    """The oracle's rate as the median of three samples of budget_s / 3 each
+    (single-threaded), with the host's core count and CPU model."""
+    runs = [oracle_rate(workload, budget_s / 3.0) for _ in range(3)]
+    vals = [r[0] for r in runs]
+    return {"value": statistics.median(vals), "unit": unit, "cores": 1, "kind": "oracle",
+            "samples": [round(v, 6) for v in vals], "statistic": "median of 3",
+            "calls": sum(r[1] for r in runs), "seconds": sum(r[2] for r in runs), "host": host_cpu()}
+
+
 def reference_arm(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -831,7 +1038,8 @@ def reference_arm(args):
         "config": {"workload": desc, "sample": f"{steps_px} output pixels (a band of rows) per step"
                    if steps_px else "whole outputs, 10 s", "threads": 1},
         "cpu_baseline": {"value": value, "unit": "Gpix/s", "cores": 1, "kind": "oracle",
-                         "sample": f"bands of {steps_px} output pixels per step, single-threaded C oracle"},
+                         "sample": f"bands of {steps_px} output pixels per step, single-threaded C oracle",
+                         "host": host_cpu()},
         "e2e": {"value": value, "unit": "Gpix/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -948,7 +1156,8 @@ def main():
     if WORKLOADS[args.workload][1] == "multi":
         r = multi_arm(args, local_rank)
         if rank == 0:
-            v, calls, dt, _ = oracle_rate(args.workload, args.cpu_budget)
+            cpu = oracle_sample(args.workload, args.cpu_budget)
+            cpu["sample"] = f"{cpu['calls']} passes over the 4 geometries in {cpu['seconds']:.1f} s, single-threaded"
             line = {
                 "metric": f"output Gpix/s and achieved HBM GB/s, {r['desc']}", "value": r["value"],
                 "unit": "Gpix/s", "n_gpus": world, "steps": r["steps"], "warmup": args.warmup,
@@ -966,9 +1175,32 @@ def main():
                                       "value": r["px"] / (r["ms_separate"] / 1e3) / 1e9, "unit": "Gpix/s",
                                       "what": f"the same {r['jobs']} jobs as {r['jobs']} resize_u8 launches "
                                               "(one plan per geometry), graph-replayed"},
-                "cpu_baseline": {"value": v, "unit": "Gpix/s", "cores": 1, "kind": "oracle",
-                                 "sample": f"{calls} passes over the 4 geometries in {dt:.1f} s, single-threaded"},
+                "cpu_baseline": cpu,
                 "e2e": None, "gpu_launches": r["steps"], "clocks": r["clocks"],
+            }
+            print(json.dumps(line), flush=True)
+        return
+
+    if WORKLOADS[args.workload][1] == "pair":
+        r = pair_arm(args, local_rank)
+        if rank == 0:
+            cpu = oracle_sample(args.workload, args.cpu_budget)
+            cpu["sample"] = (f"{cpu['calls']} steps (both outputs of a frame) in {cpu['seconds']:.1f} s, "
+                             "single-threaded C oracle")
+            line = {
+                "metric": f"output Gpix/s and achieved HBM GB/s, {r['desc']}", "value": r["value"],
+                "unit": "Gpix/s", "n_gpus": world, "steps": r["steps"], "warmup": args.warmup,
+                "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "u8", "data": "synthetic",
+                "config": {"workload": r["desc"], "l2": f"ring of {r['ring']} frames and outputs > 3x L2",
+                           "launch": f"one CUDA graph of {r['graph_steps']} steps (two resize_u8 launches each), "
+                                     "one stream, after a device hold",
+                           "algorithmic_bytes_per_step": r["bytes"]},
+                "roofline": {"bound": "hbm", "achieved": r["gbs"], "peak": r["peak"], "unit": "GB/s",
+                             "frac": r["gbs"] / r["peak"],
+                             "peak_source": f"{r['peak_src']} HBM copy (MEASURED_PEAKS.json hbm_gbs)",
+                             "traffic": None},
+                "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * r["steps"], "clocks": r["clocks"],
             }
             print(json.dumps(line), flush=True)
         return
@@ -976,7 +1208,9 @@ def main():
     if WORKLOADS[args.workload][1] == "valid":
         r = valid_arm(args, local_rank)
         if rank == 0:
-            v, calls, dt, _ = oracle_rate(args.workload, args.cpu_budget)
+            cpu = oracle_sample(args.workload, args.cpu_budget)
+            cpu["sample"] = (f"{cpu['calls']} bands of output rows in {cpu['seconds']:.1f} s, "
+                             "single-threaded C oracle")
             line = {
                 "metric": f"output Gpix/s and FP32 TFLOP/s, {r['desc']}", "value": r["value"], "unit": "Gpix/s",
                 "n_gpus": world, "steps": r["steps"], "warmup": args.warmup, "ms_per_step": r["launch_ms"],
@@ -989,8 +1223,7 @@ def main():
                              "frac": r["tflops"] / r["peak"],
                              "peak_source": "derived: 152 SMs x 128 FP32 FMA lanes x 2 FLOP x max SM clock",
                              "traffic": profile_traffic(args.workload)},
-                "cpu_baseline": {"value": v, "unit": "Gpix/s", "cores": 1, "kind": "oracle",
-                                 "sample": f"{calls} bands of output rows in {dt:.1f} s, single-threaded C oracle"},
+                "cpu_baseline": cpu,
                 "e2e": None, "gpu_launches": r["steps"], "clocks": r["clocks"],
             }
             print(json.dumps(line), flush=True)
@@ -1001,9 +1234,9 @@ def main():
     if rank == 0:
         cpu = None
         if world == 1:
-            v, calls, dt, _ = oracle_rate(args.workload, args.cpu_budget)
-            cpu = {"value": v, "unit": "Gpix/s", "cores": 1, "kind": "oracle",
-                   "sample": f"{calls} whole outputs of this workload in {dt:.1f} s, single-threaded C oracle"}
+            cpu = oracle_sample(args.workload, args.cpu_budget)
+            cpu["sample"] = (f"{cpu['calls']} whole outputs of this workload in {cpu['seconds']:.1f} s, "
+                             "single-threaded C oracle")
         traffic = profile_traffic(args.workload)
         desc = r["desc"]
         line = {
@@ -1023,9 +1256,9 @@ def main():
                 "workload": desc,
                 "l2": f"ring of {r['ring']} distinct input/output sets "
                       f"({r['ring'] * (r['read_bytes'] + r['write_bytes']) / MB:.0f} MB) > 3x L2; every step L2-cold",
-                "launch": f"CUDA graphs of {r['graph_steps']} "
+                "launch": f"the {args.steps} timed steps as CUDA graphs of {r['graph_steps']} "
                           f"{'resize_u8' if WORKLOADS[args.workload][1] == 'u8' else 'resize_fused'} launches "
-                          f"(one frame or batch each), one stream",
+                          f"(one frame or batch each) on one stream, after a device hold",
                 "algorithmic_bytes_per_step": r["step_bytes"],
                 "parallelism": f"{world} independent replica(s)",
                 "tuning": {k: v for k, v in (("tile", args.tile), ("stages", args.stages),
@@ -1050,7 +1283,9 @@ def main():
             "eager_ms_per_step": r["eager_ms_per_step"],
             "clocks": r["clocks"],
             "batched": r["batched"],
-            "copy_ceiling": dict(r["copy_ceiling"], frac=r["achieved_gbs"] / r["copy_ceiling"]["gbs"]),
+            "copy_ceiling": dict(r["copy_ceiling"],
+                                 resize_over_copy_time=(r["launch_ms"] * 1e3) / r["copy_ceiling"]["us_per_copy"]),
+            "replays": r["replays"],
         }
         print(json.dumps(line), flush=True)
     if world > 1:

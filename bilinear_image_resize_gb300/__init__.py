@@ -18,7 +18,7 @@ from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_BORD
                       RZ_BORDER_WRAP, RZ_EPI_FILTER, RZ_EPI_FILTER3X3, RZ_EPI_GRAY_BGR, RZ_EPI_GRAY_RGB, RZ_EPI_NORMALIZE_NCHW, RZ_ERR_ARG, RZ_ERR_CUDA, RZ_ERR_NOMEM, RZ_ERR_TIMEOUT,
                       RZ_ERR_UNSUPPORTED, RZ_F32, RZ_LINEAR, RZ_MAX_DIM, RZ_NEAREST, RZ_NOALLOC_MAX_DIM, RZ_OK,
                       RZ_OPT_CTAS_PER_SM, RZ_OPT_GENERIC_ONLY, RZ_OPT_GRID_MODE, RZ_OPT_PDL, RZ_OPT_RING_ROWS,
-                      RZ_MULTI_MAX_JOBS, RZ_OPT_F32_KERNEL, RZ_OPT_FILTER_KERNEL, RZ_OPT_STAGES, RZ_OPT_U8_KERNEL, RZ_U8,
+                      RZ_MULTI_MAX_JOBS, RZ_OPT_F32_KERNEL, RZ_OPT_FILTER_KERNEL, RZ_OPT_L2_PREFETCH, RZ_COPY_PDL, RZ_COPY_L2_PREFETCH, RZ_OPT_STAGES, RZ_OPT_U8_KERNEL, RZ_U8,
                       RzEpilogue, RzJob)
 
 __all__ = [
@@ -35,7 +35,8 @@ __all__ = [
     "RZ_OK", "RZ_ERR_ARG", "RZ_ERR_UNSUPPORTED", "RZ_ERR_CUDA", "RZ_ERR_NOMEM", "RZ_ERR_TIMEOUT",
     "RZ_MAX_DIM", "KIND_U8", "KIND_F32", "KIND_NORMALIZE", "KIND_FILTER3X3",
     "RZ_OPT_STAGES", "RZ_OPT_GENERIC_ONLY", "RZ_OPT_CTAS_PER_SM", "RZ_OPT_GRID_MODE", "RZ_OPT_PDL",
-    "RZ_OPT_RING_ROWS", "RZ_OPT_U8_KERNEL",
+    "RZ_OPT_RING_ROWS", "RZ_OPT_U8_KERNEL", "RZ_OPT_L2_PREFETCH",
+    "resize_copy_baseline", "RZ_COPY_PDL", "RZ_COPY_L2_PREFETCH",
 ]
 
 
@@ -312,6 +313,21 @@ def filter2d_valid_f32(src, weights, dst, stream=None) -> None:
     _check(_native.load().filter2d_valid_f32(src.data_ptr(), src.stride(0) * 4, H, W, weights.data_ptr(), K,
                                              dst.data_ptr(), dst.stride(0) * 4, _stream(stream)),
            "filter2d_valid_f32")
+
+
+def resize_copy_baseline(src, dst, flags: int = RZ_COPY_PDL | RZ_COPY_L2_PREFETCH, stream=None) -> None:
+    """dst[:] = src, bytes moved by the library's 1:1 copy baseline kernel.
+
+    src, dst: contiguous CUDA tensors of the same byte size (a multiple of
+    16), 16-byte aligned, not overlapping.
+    """
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("src and dst must be contiguous")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("src and dst differ in byte size")
+    _check(_native.load().resize_copy_baseline(src.data_ptr(), dst.data_ptr(), nbytes, flags, _stream(stream)),
+           "resize_copy_baseline")
 
 
 def make_jobs(srcs, dsts, device=None):

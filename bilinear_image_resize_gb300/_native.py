@@ -40,6 +40,10 @@ RZ_OPT_RING_ROWS = 6
 RZ_OPT_U8_KERNEL = 7
 RZ_OPT_FILTER_KERNEL = 8
 RZ_OPT_F32_KERNEL = 9
+RZ_OPT_L2_PREFETCH = 10
+
+RZ_COPY_PDL = 1
+RZ_COPY_L2_PREFETCH = 2
 
 # kernel families for resize_plan_set_tile
 KIND_U8 = 0
@@ -107,6 +111,7 @@ SIGNATURES = {
     "resize_strerror": (ctypes.c_char_p, [_i]),
     "resize_last_cuda_error": (_i, []),
     "resize_u8_noalloc": (_i, [_p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
+    "resize_copy_baseline": (_i, [_p, _p, _sz, _i, _p]),
 }
 
 _lib = None

@@ -150,6 +150,7 @@ struct rz_plan_s {
     int opt_u8_kernel = 0;     // uint8 bilinear: 0 automatic, 1 staged tiles, 2 streaming, 3 direct
     int opt_filter_kernel = 0; // filter epilogues: 0 automatic, 1 streaming, 2 tile kernel
     int opt_f32_kernel = 0;    // plain float32 bilinear: 0 automatic (streaming), 1 staged tiles
+    int opt_l2_prefetch = 1;   // exact-ratio direct kernels: pre-wait L2 prefetch of the source
 };
 
 namespace {
@@ -327,6 +328,31 @@ int ensure_smem_attr(int dev, const void *fn)
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, rz::kMaxSmem);
     if (e != cudaSuccess) return static_cast<int>(e);
     g_attr_done.push_back({dev, fn});
+    return 0;
+}
+
+std::mutex g_occ_mu;
+struct OccEntry { int dev; const void *fn; int block; int ctas; };
+std::vector<OccEntry> g_occ;   // CTAs of a kernel resident at once on a device
+
+// How many CTAs of `fn` (block threads, no dynamic shared memory) the device
+// holds at once: the occupancy calculator's CTAs per SM times the SM count,
+// computed once per (device, kernel, block size).
+int resident_ctas(int dev, const void *fn, int block, int *out)
+{
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    for (const auto &e : g_occ)
+        if (e.dev == dev && e.fn == fn && e.block == block) {
+            *out = e.ctas;
+            return 0;
+        }
+    int per_sm = 0, sms = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, block, 0);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    *out = std::max(1, per_sm * sms);
+    g_occ.push_back({dev, fn, block, *out});
     return 0;
 }
 
@@ -526,18 +552,42 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
     const int opt = p->opt_u8_kernel;
     const int C = a.C, batch = a.batch;
     const bool wrap = p->border == RZ_BORDER_WRAP && mode == RZ_LINEAR;
-    auto launch_grid = [&](const void *fn, long long gx, int block) {
+    // per_image: the kernel takes exactly one image per grid row, so a batch
+    // past 65535 images is split into several launches
+    auto launch_grid = [&](const void *fn, long long gx, int block, bool per_image = false) {
         *rc = RZ_OK;
         if (!do_launch) return true;
         CUtensorMap none;
         std::memset(&none, 0, sizeof(none));
-        const int e = rz::launch_resize(fn, a, none, static_cast<int>(gx), 0, p->opt_pdl != 0, stream, block,
-                                        std::min(batch, 65535));
-        if (e != 0) *rc = cuda_fail(static_cast<cudaError_t>(e));
+        KArgs c = a;
+        c.l2_prefetch = 0;
+        if (a.l2_prefetch) {
+            const int e = resident_ctas(p->device, fn, block, &c.l2_prefetch);
+            if (e != 0) {
+                *rc = cuda_fail(static_cast<cudaError_t>(e));
+                return true;
+            }
+        }
+        for (long long b0 = 0; b0 < batch; b0 += 65535) {
+            const int nb = static_cast<int>(std::min<long long>(batch - b0, 65535));
+            KArgs d = c;
+            if (per_image) {
+                d.src = c.src + b0 * c.src_bstride;
+                d.dst = c.dst + b0 * c.dst_bstride;
+                d.batch = nb;
+            }
+            const int e = rz::launch_resize(fn, d, none, static_cast<int>(gx), 0, p->opt_pdl != 0, stream, block, nb);
+            if (e != 0) {
+                *rc = cuda_fail(static_cast<cudaError_t>(e));
+                return true;
+            }
+            if (!per_image) break;   // the kernel strides over every image itself
+        }
         return true;
     };
-    auto launch = [&](const void *fn, long long threads) {
-        return launch_grid(fn, (threads + rz::kDirectThreads - 1) / rz::kDirectThreads, rz::kDirectThreads);
+    auto launch = [&](const void *fn, long long threads, bool per_image = false) {
+        return launch_grid(fn, (threads + rz::kDirectThreads - 1) / rz::kDirectThreads, rz::kDirectThreads,
+                           per_image);
     };
     if (fam == rz::FAM_FILT) {
         // K x K epilogue: the streaming kernel for K = 3, 5, 7 (source rows
@@ -612,9 +662,9 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
         const uintptr_t da = reinterpret_cast<uintptr_t>(a.dst) | static_cast<uintptr_t>(a.dst_pitch) |
                              static_cast<uintptr_t>(a.dst_bstride);
         if (sa % lw == 0 && da % sw == 0) {
-            fn = rz::direct_down2_kernel_for(mode, C);
+            const void *dfn = rz::direct_down2_kernel_for(mode, C);
             const int px = rz::down2_px(C);
-            groups = static_cast<long long>(a.OH) * ((a.OW + px - 1) / px);
+            if (dfn) return launch(dfn, static_cast<long long>(a.OH) * ((a.OW + px - 1) / px), true);
         }
     }
     if (!fn && fam == rz::FAM_U8 && !p->opt_generic && is_down32(*p)) {
@@ -721,6 +771,7 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     a.batch = batch;
     a.status = p->d_status;
     a.border = p->border;
+    a.l2_prefetch = p->opt_l2_prefetch;
     if (run_direct(p, fam, a, mode, stream, do_launch, &rc)) return rc;
     // the staged and streaming kernels take source spans from the tables,
     // which under the wrap rule are not monotone at the edges
@@ -967,6 +1018,10 @@ int resize_plan_set_option(rz_plan p, int option, int value)
     case RZ_OPT_F32_KERNEL:
         if (value < 0 || value > 1) return RZ_ERR_ARG;
         p->opt_f32_kernel = value;
+        break;
+    case RZ_OPT_L2_PREFETCH:
+        if (value != 0 && value != 1) return RZ_ERR_ARG;
+        p->opt_l2_prefetch = value;
         break;
     default:
         return RZ_ERR_ARG;

@@ -29,80 +29,108 @@ namespace {
 
 using namespace dev;
 
-// Grid: x covers one image's output groups (kDirectThreads per CTA), y walks
-// the images of a batch (strided past 65535 images).  Requirements, checked
-// by the host: W = 2 OW, H = 2 OH; source base, pitch and batch stride
-// multiples of the load width (16 bytes for 1 and 4 channels, 8 for 3);
-// output base, pitch and batch stride multiples of the store width (8, 4).
-// LINEAR = 0 is the exact 2x nearest: every other pixel of every other row
-// (only the upper row is read).
+// The row's last pixels of an exact 2x group kernel (fewer than a group),
+// byte by byte; kept out of line so that the whole-group path compiles to a
+// short straight sequence.
+template <int C, int LINEAR>
+__device__ __noinline__ void down2_row_tail(const uint8_t *top, const uint8_t *bot, uint8_t *out, int p0, int OW)
+{
+    for (int p = p0; p < OW; p++)
+#pragma unroll
+        for (int c = 0; c < C; c++) {
+            const int o = 2 * p * C + c;
+            if (LINEAR) {
+                const int s = top[o] + top[o + C] + bot[o] + bot[o + C] + 2;
+                out[p * C + c] = static_cast<uint8_t>(s >> 2);
+            } else {
+                out[p * C + c] = top[o];
+            }
+        }
+}
+
+// True for the CTAs that prefetch their source span before the dependency
+// wait: the first a.l2_prefetch CTAs in launch order (the host sets it to the
+// CTAs resident at once, 0 for none).  Only those can be resident while the
+// previous kernel still runs; a CTA of a later wave starts after it has
+// finished, when a prefetch just ahead of the CTA's own loads only adds work.
+__device__ __forceinline__ bool first_wave_cta(const KArgs &a)
+{
+    return static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x < a.l2_prefetch;
+}
+
+// One group of the exact 2x downscale: the group's source words of its two
+// rows (LINEAR = 0: the upper row only), the exact sums, one vector store.
+template <int C, int LINEAR>
+__device__ __forceinline__ void down2_one(const uint8_t *top, const uint8_t *bot, uint8_t *out, int j)
+{
+    constexpr int PX = down2_px(C), SB = 2 * PX * C, OB = PX * C;
+    uint32_t tw[SB / 4], bw[SB / 4], o[OB / 4];
+    if constexpr (C == 3) {
+        const uint2 *tp = reinterpret_cast<const uint2 *>(top + SB * j);
+        const uint2 *bp = reinterpret_cast<const uint2 *>(bot + SB * j);
+#pragma unroll
+        for (int k = 0; k < 3; k++) {
+            const uint2 t = __ldcs(tp + k);
+            tw[2 * k] = t.x; tw[2 * k + 1] = t.y;
+            if (LINEAR) {
+                const uint2 u = __ldcs(bp + k);
+                bw[2 * k] = u.x; bw[2 * k + 1] = u.y;
+            }
+        }
+    } else {
+        const uint4 t = __ldcs(reinterpret_cast<const uint4 *>(top + SB * j));
+        tw[0] = t.x; tw[1] = t.y; tw[2] = t.z; tw[3] = t.w;
+        if (LINEAR) {
+            const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(bot + SB * j));
+            bw[0] = u.x; bw[1] = u.y; bw[2] = u.z; bw[3] = u.w;
+        }
+    }
+    if (LINEAR)
+        down2_group<C>(tw, bw, o);
+    else
+        down2_nearest_group<C>(tw, o);
+    if constexpr (C == 3) {
+        uint32_t *op = reinterpret_cast<uint32_t *>(out + OB * j);
+        __stcs(op, o[0]);
+        __stcs(op + 1, o[1]);
+        __stcs(op + 2, o[2]);
+    } else {
+        __stcs(reinterpret_cast<uint2 *>(out + OB * j), make_uint2(o[0], o[1]));
+    }
+}
+
+// Grid: x covers one image's output groups (kDirectThreads per CTA), y the
+// images of a batch, one image per grid row (the host splits batches past
+// 65535 images into several launches).  Requirements, checked by the host: W = 2 OW, H = 2 OH; source
+// base, pitch and batch stride multiples of the load width (16 bytes for 1
+// and 4 channels, 8 for 3); output base, pitch and batch stride multiples of
+// the store width (8, 4).  LINEAR = 0 is the exact 2x nearest: every other
+// pixel of every other row (only the upper row is read).  First-wave CTAs
+// prefetch the source rows they read into L2 before waiting for the previous
+// grid (first_wave_cta).
 template <int C, int LINEAR>
 __global__ void __launch_bounds__(kDirectThreads) k_down2_direct(const KArgs a, const __grid_constant__ CUtensorMap)
 {
-    constexpr int PX = down2_px(C);       // output pixels per group
+    constexpr int PX = down2_px(C);       // output pixels per group: 8, 4, 2
     constexpr int SB = 2 * PX * C;        // source bytes per row and group: 16, 24, 16
-    constexpr int OB = PX * C;            // output bytes per group: 8, 12, 8
     grid_launch_dependents();
-    grid_dependency_wait();
     const int full = a.OW / PX;                // whole groups per row
     const int gpr = full + (a.OW % PX ? 1 : 0);
+    if (first_wave_cta(a))
+        prefetch_items<LINEAR ? 2 : 1>(a.src + (long long)blockIdx.y * a.src_bstride, a.src_pitch,
+                                       (long long)a.W * C, gpr, a.OH, (long long)blockIdx.x * kDirectThreads,
+                                       kDirectThreads, SB, 0, 0, [](int u, int k) { return 2 * u + k; });
+    grid_dependency_wait();
     const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
     if (idx >= a.OH * gpr)
         return;
     const int dy = idx / gpr, j = idx - dy * gpr;
-    for (int b = blockIdx.y; b < a.batch; b += gridDim.y) {
-        const uint8_t *top = a.src + (long long)b * a.src_bstride + (long long)(2 * dy) * a.src_pitch;
-        const uint8_t *bot = top + a.src_pitch;
-        uint8_t *out = a.dst + (long long)b * a.dst_bstride + (long long)dy * a.dst_pitch;
-        if (j < full) {
-            uint32_t tw[SB / 4], bw[SB / 4], o[OB / 4];
-            if constexpr (C == 3) {
-                const uint2 *tp = reinterpret_cast<const uint2 *>(top + SB * j);
-                const uint2 *bp = reinterpret_cast<const uint2 *>(bot + SB * j);
-#pragma unroll
-                for (int k = 0; k < 3; k++) {
-                    const uint2 t = __ldcs(tp + k);
-                    tw[2 * k] = t.x; tw[2 * k + 1] = t.y;
-                    if (LINEAR) {
-                        const uint2 u = __ldcs(bp + k);
-                        bw[2 * k] = u.x; bw[2 * k + 1] = u.y;
-                    }
-                }
-            } else {
-                const uint4 t = __ldcs(reinterpret_cast<const uint4 *>(top + SB * j));
-                tw[0] = t.x; tw[1] = t.y; tw[2] = t.z; tw[3] = t.w;
-                if (LINEAR) {
-                    const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(bot + SB * j));
-                    bw[0] = u.x; bw[1] = u.y; bw[2] = u.z; bw[3] = u.w;
-                }
-            }
-            if (LINEAR)
-                down2_group<C>(tw, bw, o);
-            else
-                down2_nearest_group<C>(tw, o);
-            if constexpr (C == 3) {
-                uint32_t *op = reinterpret_cast<uint32_t *>(out + OB * j);
-                __stcs(op, o[0]);
-                __stcs(op + 1, o[1]);
-                __stcs(op + 2, o[2]);
-            } else {
-                __stcs(reinterpret_cast<uint2 *>(out + OB * j), make_uint2(o[0], o[1]));
-            }
-        } else {
-            // the row's last pixels, fewer than a group: byte by byte
-            for (int p = full * PX; p < a.OW; p++)
-#pragma unroll
-                for (int c = 0; c < C; c++) {
-                    const int o = 2 * p * C + c;
-                    if (LINEAR) {
-                        const int s = top[o] + top[o + C] + bot[o] + bot[o + C] + 2;
-                        out[p * C + c] = static_cast<uint8_t>(s >> 2);
-                    } else {
-                        out[p * C + c] = top[o];
-                    }
-                }
-        }
-    }
+    const uint8_t *top = a.src + (long long)blockIdx.y * a.src_bstride + (long long)(2 * dy) * a.src_pitch;
+    uint8_t *out = a.dst + (long long)blockIdx.y * a.dst_bstride + (long long)dy * a.dst_pitch;
+    if (j < full)
+        down2_one<C, LINEAR>(top, top + a.src_pitch, out, j);
+    else
+        down2_row_tail<C, LINEAR>(top, top + a.src_pitch, out, full * PX, a.OW);
 }
 
 // Any ratio, uint8: bilinear (exact 11-bit fixed point, the tiled kernel's
@@ -222,9 +250,13 @@ __global__ void __launch_bounds__(kDirectThreads) k_down32_direct(const KArgs a,
     constexpr int NW = 3 * C;      // source words per row: 12 pixels
     constexpr int NWO = 2 * C;     // output words: 8 pixels
     grid_launch_dependents();
-    grid_dependency_wait();
     const int full = a.OW / PX;
     const int gpr = full + (a.OW % PX ? 1 : 0);
+    if (first_wave_cta(a))
+        prefetch_items<2>(a.src + (long long)blockIdx.y * a.src_bstride, a.src_pitch, (long long)a.W * C, gpr, a.OH,
+                          (long long)blockIdx.x * kDirectThreads, kDirectThreads, 4 * NW, 0, 0,
+                          [](int u, int k) { return 3 * (u >> 1) + (k ? 1 : 2 * (u & 1)); });
+    grid_dependency_wait();
     const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
     if (idx >= a.OH * gpr)
         return;
@@ -388,8 +420,16 @@ __global__ void __launch_bounds__(kDirectThreads, Up2Occupancy<C, BORDER>::value
     using Lay = Up2Layout<C>;
     constexpr int P = Lay::P, NB = Lay::NB, LEAD = Lay::LEAD, NW = Lay::NW, NWO = Lay::NWO;
     grid_launch_dependents();
-    grid_dependency_wait();
     const int gpr = (a.W + P - 1) / P;
+    if (first_wave_cta(a)) {
+        // source rows r - 1, r, r + 1 (edge rows of the mirror and wrap rules
+        // are left to the loads); the group's words from column s0 - 1
+        const int H = a.H;
+        prefetch_items<3>(a.src + (long long)blockIdx.y * a.src_bstride, a.src_pitch, (long long)a.W * C, gpr, a.H,
+                          (long long)blockIdx.x * kDirectThreads, kDirectThreads, P * C, -C - LEAD, 4 * NW - P * C,
+                          [H](int u, int k) { return min(max(u - 1 + k, 0), H - 1); });
+    }
+    grid_dependency_wait();
     const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
     if (idx >= a.H * gpr)
         return;
@@ -847,9 +887,13 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_gray(const KArgs a, co
 {
     constexpr int PX = 4, SB = 2 * PX * C, NW = SB / 4;
     grid_launch_dependents();
-    grid_dependency_wait();
     const int full = a.OW / PX;
     const int gpr = full + (a.OW % PX ? 1 : 0);
+    if (first_wave_cta(a))
+        prefetch_items<LINEAR ? 2 : 1>(a.src + (long long)blockIdx.y * a.src_bstride, a.src_pitch,
+                                       (long long)a.W * C, gpr, a.OH, (long long)blockIdx.x * kDirectThreads,
+                                       kDirectThreads, SB, 0, 0, [](int u, int k) { return 2 * u + k; });
+    grid_dependency_wait();
     const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
     if (idx >= a.OH * gpr)
         return;

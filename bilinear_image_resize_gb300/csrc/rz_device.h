@@ -167,6 +167,48 @@ __device__ __forceinline__ uint64_t policy_evict_first()
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
+// Ask the memory system to start moving [p, p + bytes) from HBM into L2 (a
+// bulk prefetch, cp.async.bulk.prefetch.L2).  It is a hint: it reads nothing
+// into registers or shared memory and cannot change any result, so a kernel
+// may issue it before griddepcontrol.wait, while the grid it depends on is
+// still running (L2 is the device's point of coherence, so a line that grid
+// writes later is updated there).  The range is shrunk inward to 16-byte
+// bounds, so every prefetched byte lies inside [p, p + bytes).
+__device__ __forceinline__ void l2_prefetch_span(const uint8_t *p, long long bytes)
+{
+    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15);
+    const uintptr_t a1 = (reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(bytes)) & ~static_cast<uintptr_t>(15);
+    if (bytes > 0 && a1 > a0)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a0), "r"(static_cast<uint32_t>(a1 - a0))
+                     : "memory");
+}
+
+// Pre-wait prefetch of the source bytes one CTA of a direct kernel will read.
+// The CTA's work items are [g0, g0 + n) of a grid laid out `per_unit` items
+// per unit (an output row, or a source row for the 2x upscale), `units`
+// units in all; item j of unit u reads bytes [j GB + lead, j GB + lead + GB
+// + extra) of the NR source rows row(u, k), k < NR (row() < 0: none).  Thread
+// t takes the piece (unit u0 + t / NR, row k = t % NR), one bulk prefetch
+// clipped to [0, row_bytes) of that row; pieces past the block's threads are
+// skipped (a hint may cover less).
+template <int NR, class RowFn>
+__device__ __forceinline__ void prefetch_items(const uint8_t *img, long long pitch, long long row_bytes, int per_unit,
+                                               long long units, long long g0, long long n, long long GB, long long lead,
+                                               long long extra, RowFn row)
+{
+    long long g1 = g0 + n;
+    if (g1 > units * per_unit) g1 = units * per_unit;
+    if (g0 >= g1) return;
+    const long long u = g0 / per_unit + static_cast<long long>(threadIdx.x / NR);
+    if (u > (g1 - 1) / per_unit) return;
+    const int k = static_cast<int>(threadIdx.x % NR);
+    const long long jlo = max(g0 - u * per_unit, 0LL), jhi = min(g1 - u * per_unit, static_cast<long long>(per_unit));
+    const long long b0 = max(jlo * GB + lead, 0LL), b1 = min(jhi * GB + lead + extra, row_bytes);
+    const int r = row(static_cast<int>(u), k);
+    if (r < 0 || b1 <= b0) return;
+    l2_prefetch_span(img + static_cast<long long>(r) * pitch + b0, b1 - b0);
+}
+
 // Bulk copy shared -> global (bulk-group completion).
 __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
 {

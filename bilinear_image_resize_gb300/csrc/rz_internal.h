@@ -150,6 +150,7 @@ struct KArgs {
     float scale[4], shift[4];  // normalise epilogue: y = q * scale[c] + shift[c]
     float w[49];               // K x K epilogue weights (K <= 7), row-major
     int ksize;                 // K of the filter epilogue (3 for the 3x3 kind)
+    int l2_prefetch;           // exact-ratio direct kernels: prefetch the CTA's source span into L2 before the dependency wait
 };
 
 // Record a cudaError_t for resize_last_cuda_error (this host thread).

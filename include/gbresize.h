@@ -361,6 +361,25 @@ RZ_API int resize_axis_table_border(int n_in, int n_out, int mode, int border, i
  */
 RZ_API int resize_wait_selftest(int *dev_status, int limit_us, void *stream);
 
+/*
+ * The 1:1 copy baseline (Volcanic page, "From Prototype to Performance:
+ * Optimizing OpenCV Resize on Volcanic GPUs", *Kernel evolution -> Baseline:
+ * simple 1:1 copy behavior*): copies `bytes` bytes from src to dst (device
+ * memory) with no resize arithmetic, in the launch shape of the exact-ratio
+ * resize kernels (256-thread CTAs, one 16-byte load and store per thread),
+ * so that a resize's time can be set against what a launch moving the same
+ * bytes reaches on this GPU.  flags: RZ_COPY_PDL launches it as a
+ * programmatic dependent launch (as the resizes are by default);
+ * RZ_COPY_L2_PREFETCH makes each CTA prefetch its source span into L2 before
+ * waiting for the previous kernel (as RZ_OPT_L2_PREFETCH does for the
+ * resizes).  src and dst 16-byte aligned, bytes a multiple of 16, the ranges
+ * disjoint, unknown flag bits unset: otherwise RZ_ERR_ARG.  bytes = 0 is a
+ * no-op.  Asynchronous on `stream`; no allocation.
+ */
+#define RZ_COPY_PDL 1
+#define RZ_COPY_L2_PREFETCH 2
+RZ_API int resize_copy_baseline(const void *src, void *dst, size_t bytes, int flags, void *stream);
+
 /* Human-readable name of a status code (static string). */
 RZ_API const char *resize_strerror(int code);
 
@@ -426,7 +445,14 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  *                       float32 bilinear resize under the clamp and mirror
  *                       rules.  0: the streaming kernel (source rows streamed
  *                       once through shared memory), unless a float32 tile
- *                       override is set; 1: staged tiles.  Same arithmetic.
+ *                       override is set; 1: staged tiles.  Same arithmetic;
+ *   RZ_OPT_L2_PREFETCH  value 1 (default) or 0: the exact-ratio uint8 kernels
+ *                       (2x down, bilinear, nearest and gray; 3:2 down; 2x
+ *                       up) ask for the source rows each CTA reads to be
+ *                       moved into L2 as soon as the CTA is resident, before
+ *                       it waits for the previous kernel in the stream (with
+ *                       RZ_OPT_PDL, while that kernel finishes).  A prefetch
+ *                       is a hint and changes no result.
  * Returns RZ_ERR_ARG for an unknown option or value.
  */
 #define RZ_OPT_STAGES 1
@@ -438,6 +464,7 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
 #define RZ_OPT_U8_KERNEL 7
 #define RZ_OPT_FILTER_KERNEL 8
 #define RZ_OPT_F32_KERNEL 9
+#define RZ_OPT_L2_PREFETCH 10
 RZ_API int resize_plan_set_option(rz_plan p, int option, int value);
 
 /*
