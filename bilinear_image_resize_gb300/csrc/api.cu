@@ -624,7 +624,7 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
             const uintptr_t da = reinterpret_cast<uintptr_t>(a.dst) | static_cast<uintptr_t>(a.dst_pitch) |
                                  static_cast<uintptr_t>(a.dst_bstride);
             const void *dfn = rz::direct_down2_gray_kernel_for(mode, C, a.bgr != 0);
-            if (dfn && sa % lw == 0 && da % 4 == 0) return launch(dfn, groups);
+            if (dfn && sa % lw == 0 && da % 4 == 0) return launch(dfn, groups, true);
         }
         const void *gfn = rz::direct_gray_kernel_for(mode, C, wrap);
         if (!gfn) return false;
@@ -673,10 +673,8 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
                              static_cast<uintptr_t>(a.src_bstride);
         const uintptr_t da = reinterpret_cast<uintptr_t>(a.dst) | static_cast<uintptr_t>(a.dst_pitch) |
                              static_cast<uintptr_t>(a.dst_bstride);
-        if (sa % 4 == 0 && da % 4 == 0) {
-            fn = rz::direct_down32_kernel_for(C);
-            groups = static_cast<long long>(a.OH) * ((a.OW + 7) / 8);
-        }
+        const void *dfn = rz::direct_down32_kernel_for(C);
+        if (dfn && sa % 4 == 0 && da % 4 == 0) return launch(dfn, static_cast<long long>(a.OH) * ((a.OW + 7) / 8));
     }
     const long long gpr = (a.OW + rz::kDirectRun - 1) / rz::kDirectRun;
     if (!fn && fam == rz::FAM_U8 && mode == RZ_LINEAR && a.OH > a.H && opt == 3 && !wrap) {

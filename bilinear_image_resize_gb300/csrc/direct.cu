@@ -241,7 +241,9 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
 // words, split into 16-bit lanes (even and odd bytes); the vertical 3-1 sum
 // is lane-wise, and each output byte takes (3 v + v' + 8) >> 4 from two
 // lanes at compile-time positions.  The row's last pixels
-// (fewer than eight) take a byte path.  Requirements, checked by the host:
+// (fewer than eight) take a byte path.  (Written as a loop over the images
+// of a batch: without it this kernel compiles to a slower schedule, 4.8
+// against 2.9 us for 1080p -> 720p.)  Requirements, checked by the host:
 // source base, pitch and batch stride multiples of 4; output ones of 4.
 template <int C>
 __global__ void __launch_bounds__(kDirectThreads) k_down32_direct(const KArgs a, const __grid_constant__ CUtensorMap)
@@ -874,12 +876,28 @@ __device__ __forceinline__ int gray_word_px(const uint32_t (&w)[NW], int p)
     return BGR ? gray_dp4a(px, kGrayLoBGR, kGrayHiBGR) : gray_dp4a(px, kGrayLoRGB, kGrayHiRGB);
 }
 
+// The row's last pixels of the exact 2x gray kernel (fewer than a group),
+// byte by byte; out of line, like down2_row_tail.
+template <int C, int LINEAR, bool BGR>
+__device__ __noinline__ void gray_down2_row_tail(const uint8_t *top, const uint8_t *bot, uint8_t *out, int p0, int OW)
+{
+    constexpr int IR = BGR ? 2 : 0, IB = BGR ? 0 : 2;
+    for (int p = p0; p < OW; p++) {
+        int g = gray_at<C>(top, 2 * p, IR, IB);
+        if (LINEAR)
+            g = (g + gray_at<C>(top, 2 * p + 1, IR, IB) + gray_at<C>(bot, 2 * p, IR, IB) +
+                 gray_at<C>(bot, 2 * p + 1, IR, IB) + 2) >> 2;
+        out[p] = static_cast<uint8_t>(g);
+    }
+}
+
 // Grayscale conversion fused before an exact 2x downscale (W = 2 OW,
 // H = 2 OH): bilinear (rounded mean of the 2 x 2 gray values, the exact sum
 // at weights 1024) or nearest (the upper-left gray value).  A thread takes
 // four output pixels: eight source pixels of each of its two rows in one
 // 24- or 32-byte run (three 8-byte or two 16-byte streaming loads), and
-// stores the four gray bytes as one word.  Requirements, checked by the host:
+// stores the four gray bytes as one word.  One image per grid row (the host
+// splits batches past 65535 images).  Requirements, checked by the host:
 // source base, pitch and batch stride multiples of 8 bytes (C = 3) or 16
 // (C = 4); output ones multiples of 4.
 template <int C, int LINEAR, bool BGR>
@@ -898,58 +916,48 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_gray(const KArgs a, co
     if (idx >= a.OH * gpr)
         return;
     const int dy = idx / gpr, j = idx - dy * gpr;
-    for (int b = blockIdx.y; b < a.batch; b += gridDim.y) {
-        const uint8_t *top = a.src + (long long)b * a.src_bstride + (long long)(2 * dy) * a.src_pitch;
-        const uint8_t *bot = top + a.src_pitch;
-        uint8_t *out = a.dst + (long long)b * a.dst_bstride + (long long)dy * a.dst_pitch;
-        if (j < full) {
-            uint32_t tw[NW], bw[NW];
-            if constexpr (C == 3) {
-                const uint2 *tp = reinterpret_cast<const uint2 *>(top + SB * j);
-                const uint2 *bp = reinterpret_cast<const uint2 *>(bot + SB * j);
+    const uint8_t *top = a.src + (long long)blockIdx.y * a.src_bstride + (long long)(2 * dy) * a.src_pitch;
+    const uint8_t *bot = top + a.src_pitch;
+    uint8_t *out = a.dst + (long long)blockIdx.y * a.dst_bstride + (long long)dy * a.dst_pitch;
+    if (j >= full) {
+        gray_down2_row_tail<C, LINEAR, BGR>(top, bot, out, full * PX, a.OW);
+        return;
+    }
+    uint32_t tw[NW], bw[NW];
+    if constexpr (C == 3) {
+        const uint2 *tp = reinterpret_cast<const uint2 *>(top + SB * j);
+        const uint2 *bp = reinterpret_cast<const uint2 *>(bot + SB * j);
 #pragma unroll
-                for (int k = 0; k < 3; k++) {
-                    const uint2 t = __ldcs(tp + k);
-                    tw[2 * k] = t.x; tw[2 * k + 1] = t.y;
-                    if (LINEAR) {
-                        const uint2 u = __ldcs(bp + k);
-                        bw[2 * k] = u.x; bw[2 * k + 1] = u.y;
-                    }
-                }
-            } else {
-                const uint4 *tp = reinterpret_cast<const uint4 *>(top + SB * j);
-                const uint4 *bp = reinterpret_cast<const uint4 *>(bot + SB * j);
-#pragma unroll
-                for (int k = 0; k < 2; k++) {
-                    const uint4 t = __ldcs(tp + k);
-                    tw[4 * k] = t.x; tw[4 * k + 1] = t.y; tw[4 * k + 2] = t.z; tw[4 * k + 3] = t.w;
-                    if (LINEAR) {
-                        const uint4 u = __ldcs(bp + k);
-                        bw[4 * k] = u.x; bw[4 * k + 1] = u.y; bw[4 * k + 2] = u.z; bw[4 * k + 3] = u.w;
-                    }
-                }
+        for (int k = 0; k < 3; k++) {
+            const uint2 t = __ldcs(tp + k);
+            tw[2 * k] = t.x; tw[2 * k + 1] = t.y;
+            if (LINEAR) {
+                const uint2 u = __ldcs(bp + k);
+                bw[2 * k] = u.x; bw[2 * k + 1] = u.y;
             }
-            int q[PX];
+        }
+    } else {
+        const uint4 *tp = reinterpret_cast<const uint4 *>(top + SB * j);
+        const uint4 *bp = reinterpret_cast<const uint4 *>(bot + SB * j);
 #pragma unroll
-            for (int k = 0; k < PX; k++) {
-                q[k] = gray_word_px<C, BGR, NW>(tw, 2 * k);
-                if (LINEAR)
-                    q[k] = (q[k] + gray_word_px<C, BGR, NW>(tw, 2 * k + 1) + gray_word_px<C, BGR, NW>(bw, 2 * k) +
-                            gray_word_px<C, BGR, NW>(bw, 2 * k + 1) + 2) >> 2;
-            }
-            __stcs(reinterpret_cast<uint32_t *>(out + PX * j), pack4(q[0], q[1], q[2], q[3]));
-        } else {
-            // the row's last pixels, fewer than a group: byte by byte
-            constexpr int IR = BGR ? 2 : 0, IB = BGR ? 0 : 2;
-            for (int p = full * PX; p < a.OW; p++) {
-                int g = gray_at<C>(top, 2 * p, IR, IB);
-                if (LINEAR)
-                    g = (g + gray_at<C>(top, 2 * p + 1, IR, IB) + gray_at<C>(bot, 2 * p, IR, IB) +
-                         gray_at<C>(bot, 2 * p + 1, IR, IB) + 2) >> 2;
-                out[p] = static_cast<uint8_t>(g);
+        for (int k = 0; k < 2; k++) {
+            const uint4 t = __ldcs(tp + k);
+            tw[4 * k] = t.x; tw[4 * k + 1] = t.y; tw[4 * k + 2] = t.z; tw[4 * k + 3] = t.w;
+            if (LINEAR) {
+                const uint4 u = __ldcs(bp + k);
+                bw[4 * k] = u.x; bw[4 * k + 1] = u.y; bw[4 * k + 2] = u.z; bw[4 * k + 3] = u.w;
             }
         }
     }
+    int q[PX];
+#pragma unroll
+    for (int k = 0; k < PX; k++) {
+        q[k] = gray_word_px<C, BGR, NW>(tw, 2 * k);
+        if (LINEAR)
+            q[k] = (q[k] + gray_word_px<C, BGR, NW>(tw, 2 * k + 1) + gray_word_px<C, BGR, NW>(bw, 2 * k) +
+                    gray_word_px<C, BGR, NW>(bw, 2 * k + 1) + 2) >> 2;
+    }
+    __stcs(reinterpret_cast<uint32_t *>(out + PX * j), pack4(q[0], q[1], q[2], q[3]));
 }
 
 // float32 bilinear, a thread per output pixel (all C channels): the lerp form
