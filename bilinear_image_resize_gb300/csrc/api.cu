@@ -641,10 +641,33 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
     }
     if (!((fam == rz::FAM_U8 && (opt == 0 || opt == 3)) || (fam == rz::FAM_NORM && opt != 1))) return false;
     if (fam == rz::FAM_U8 && mode == RZ_LINEAR && !p->opt_generic && a.OW == 2 * a.W && a.OH == 2 * a.H) {
-        // exact 2x upscale: the 1-3 weights (direct.cu k_up2_direct), any
-        // layout, any border rule
+        // exact 2x upscale: the 1-3 weights, any layout, any border rule;
+        // three and four channels with pixel lanes, each thread walking
+        // kUp2RowsPerThread source rows (a uint8 tile override's row count
+        // replaces it), one channel in 16-bit lanes of byte pairs
         a.xt = p->d_xq;
         a.yt = p->d_yq;
+        const void *rfn = rz::direct_up2_rows_kernel_for(C, p->border);
+        if (rfn) {
+            // row blocks: as many as one wave of resident threads holds per
+            // column group (rows shared out evenly), or the uint8 tile
+            // override's rows per block
+            const long long gpc = (a.W + 3) / 4;
+            long long nrb;
+            if (p->over_tr[rz::FAM_U8] > 0) {
+                nrb = (a.H + p->over_tr[rz::FAM_U8] - 1) / p->over_tr[rz::FAM_U8];
+            } else {
+                int ctas = 0;
+                const int e = resident_ctas(p->device, rfn, rz::kDirectThreads, &ctas);
+                if (e != 0) {
+                    *rc = cuda_fail(static_cast<cudaError_t>(e));
+                    return true;
+                }
+                nrb = static_cast<long long>(ctas) * rz::kDirectThreads / std::max(1, std::min(batch, 65535)) / gpc;
+            }
+            a.tiles_y = static_cast<int>(std::clamp<long long>(nrb, 1, a.H));
+            return launch(rfn, gpc * a.tiles_y, true);
+        }
         const void *ufn = rz::direct_up2_kernel_for(C, p->border);
         if (ufn) return launch(ufn, static_cast<long long>(a.H) * ((a.W + rz::kUp2Cols - 1) / rz::kUp2Cols));
     }

@@ -555,6 +555,216 @@ __global__ void __launch_bounds__(kDirectThreads, Up2Occupancy<C, BORDER>::value
     }
 }
 
+// ------------------------------------------------------------------ exact 2x upscale, pixel lanes, walking rows
+//
+// The same 9-3-3-1 sum as k_up2_direct for three and four channels, laid out
+// so that a horizontal neighbour is a whole register: each source pixel is
+// unpacked once into two lane words, lo = {c0, c2} and hi = {c1, c3} (16-bit
+// lanes; c3 = 0 for three channels), so the vertical sums
+//   V = 16 t + 48 m + 32   (t the row above or below, m the middle row)
+// and the horizontal ones
+//   even output: 3 V[x] + V[x - 1],   odd output: 3 V[x] + V[x + 1]
+// are one integer multiply-add per lane word; every lane is 16 S + 128 with S
+// the 9-3-3-1 sum (below 2^16), so its high byte is (S + 8) >> 4, the exact
+// result (CUDA interpolation page §2.2, §6.2 at weights 1536 and 512).  A
+// thread takes four source columns of `a.TR` consecutive source rows (two
+// output rows each), keeping the unpacked rows above, at and below the current
+// one in registers, so each row is loaded and unpacked once per thread.
+template <int C>
+struct Up2RowsLayout {
+    static constexpr int P = 4;                    // source columns per thread
+    static constexpr int LEAD = (4 - C % 4) % 4;   // bytes before column s0 - 1 in its word
+    static constexpr int NB = (P + 2) * C;         // bytes of columns s0 - 1 .. s0 + P
+    static constexpr int NW = (LEAD + NB + 3) / 4;
+    static constexpr int NWO = 2 * P * C / 4;      // output words per output row
+};
+
+// Lane word {byte ea, byte eb} of the row's words (eb < 0: {byte ea, 0}),
+// each byte in the low half of a 16-bit lane.
+template <int NW>
+__device__ __forceinline__ uint32_t lane_word(const uint32_t (&w)[NW], int ea, int eb)
+{
+    const int wa = ea >> 2;
+    if (eb < 0)
+        return __byte_perm(w[wa], 0u, 0x4440u | static_cast<uint32_t>(ea & 3));
+    const int wb = eb >> 2;
+    if (wa == wb)
+        return __byte_perm(w[wa], 0u, 0x4040u | static_cast<uint32_t>(ea & 3) | (static_cast<uint32_t>(eb & 3) << 8));
+    return __byte_perm(w[wa], w[wb], static_cast<uint32_t>(ea & 3) | ((4u + (eb & 3)) << 8)) & 0x00ff00ffu;
+}
+
+// Load the words of source columns s0 - 1 .. s0 + P of one row (interior: NW
+// aligned words; at the image's left or right edge, or on layouts that are
+// not 4-byte aligned: bytes, the columns mapped by the border rule) and
+// unpack the P + 2 pixels into lane words.
+template <int C, int BORDER>
+__device__ __forceinline__ void up2_row_lanes(const uint8_t *row, int s0, int W, bool inner, uint32_t (&lo)[6],
+                                              uint32_t (&hi)[6])
+{
+    using L = Up2RowsLayout<C>;
+    uint32_t wd[L::NW];
+    if (inner) {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (s0 - 1) * C - L::LEAD);
+#pragma unroll
+        for (int i = 0; i < L::NW; i++)
+            wd[i] = __ldg(w + i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < L::NW; i++)
+            wd[i] = 0;
+#pragma unroll
+        for (int i = 0; i < L::NB; i++) {
+            const int col = BORDER == RZ_BORDER_CLAMP ? clampi(s0 - 1 + i / C, 0, W - 1)
+                                                      : border_index(s0 - 1 + i / C, W, BORDER);
+            wd[(L::LEAD + i) / 4] |= static_cast<uint32_t>(__ldg(row + col * C + i % C)) << (8 * ((L::LEAD + i) % 4));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 6; k++) {
+        const int e = L::LEAD + k * C;
+        lo[k] = lane_word<L::NW>(wd, e, e + 2);
+        hi[k] = lane_word<L::NW>(wd, e + 1, C == 4 ? e + 3 : -1);
+    }
+}
+
+// Output row 2r (above = row r - 1) or 2r + 1 (above = row r + 1): vertical
+// sums with the middle row's 48 m + 32 (mm), horizontal sums, the result
+// bytes gathered into words and stored.
+template <int C>
+__device__ __forceinline__ void up2_emit_row(const uint32_t (&tlo)[6], const uint32_t (&thi)[6],
+                                             const uint32_t (&mlo)[6], const uint32_t (&mhi)[6], uint8_t *op, int np)
+{
+    using L = Up2RowsLayout<C>;
+    uint32_t vlo[6], vhi[6];
+#pragma unroll
+    for (int k = 0; k < 6; k++) {
+        vlo[k] = 16 * tlo[k] + mlo[k];
+        vhi[k] = 16 * thi[k] + mhi[k];
+    }
+    // output pixel q: centre column k = q / 2 + 1, even (left neighbour) or
+    // odd (right neighbour)
+    uint32_t qlo[2 * 4], qhi[2 * 4];
+#pragma unroll
+    for (int k = 1; k <= 4; k++) {
+        qlo[2 * k - 2] = 3 * vlo[k] + vlo[k - 1];
+        qhi[2 * k - 2] = 3 * vhi[k] + vhi[k - 1];
+        qlo[2 * k - 1] = 3 * vlo[k] + vlo[k + 1];
+        qhi[2 * k - 1] = 3 * vhi[k] + vhi[k + 1];
+    }
+    uint32_t ow[L::NWO];
+#pragma unroll
+    for (int wo = 0; wo < L::NWO; wo++) {
+        uint32_t reg[4];
+        int id[4];
+        uint32_t pos[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const int ob = 4 * wo + k, q = ob / C, c = ob % C;
+            const bool is_hi = (c & 1) != 0;
+            reg[k] = is_hi ? qhi[q] : qlo[q];
+            id[k] = 2 * q + (is_hi ? 1 : 0);
+            pos[k] = c >= 2 ? 3u : 1u;
+        }
+        ow[wo] = gather_bytes(reg, id, pos);
+    }
+    const uintptr_t oa = reinterpret_cast<uintptr_t>(op);
+    if (np == 4 && L::NWO % 4 == 0 && (oa & 15) == 0) {
+#pragma unroll
+        for (int i = 0; i < L::NWO; i += 4)
+            __stcs(reinterpret_cast<uint4 *>(op) + i / 4, make_uint4(ow[i], ow[i + 1], ow[i + 2], ow[i + 3]));
+    } else if (np == 4 && L::NWO % 2 == 0 && (oa & 7) == 0) {
+#pragma unroll
+        for (int i = 0; i < L::NWO; i += 2)
+            __stcs(reinterpret_cast<uint2 *>(op) + i / 2, make_uint2(ow[i], ow[i + 1]));
+    } else if (np == 4 && (oa & 3) == 0) {
+#pragma unroll
+        for (int i = 0; i < L::NWO; i++)
+            __stcs(reinterpret_cast<uint32_t *>(op) + i, ow[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8 * C; i++)
+            if (i < 2 * np * C)
+                op[i] = static_cast<uint8_t>(ow[i / 4] >> (8 * (i % 4)));
+    }
+}
+
+// Grid: x covers one image's (row block, column group) items, column groups
+// fastest; y the images, one per grid row (the host splits batches past
+// 65535).  a.tiles_y = row blocks: block rb takes source rows
+// [rb H / nrb, (rb + 1) H / nrb), so the host can size the grid to one wave
+// of resident CTAs with rows shared out evenly.  Any layout, any border
+// rule.  First-wave CTAs prefetch their source rows into L2 before the
+// dependency wait.
+template <int C, int BORDER>
+__global__ void __launch_bounds__(kDirectThreads) k_up2_rows(const KArgs a, const __grid_constant__ CUtensorMap)
+{
+    using L = Up2RowsLayout<C>;
+    constexpr int P = L::P;
+    grid_launch_dependents();
+    const int gpc = (a.W + P - 1) / P;          // column groups per row block
+    const int nrb = a.tiles_y;
+    auto block_row = [&](int rb) { return static_cast<int>((long long)rb * a.H / nrb); };
+    const uint8_t *img = a.src + (long long)blockIdx.y * a.src_bstride;
+    if (first_wave_cta(a)) {
+        // rows r0 - 1 .. r0 + R of each row block the CTA touches, over its
+        // column span (a piece per row; clamped rows for the edges)
+        const long long g0 = (long long)blockIdx.x * kDirectThreads;
+        const long long g1 = min(g0 + kDirectThreads, (long long)gpc * nrb);
+        if (g0 < g1) {
+            const int rb0 = static_cast<int>(g0 / gpc), rb1 = static_cast<int>((g1 - 1) / gpc);
+            const int per = (a.H + nrb - 1) / nrb + 2;   // rows of the tallest block, with its two neighbours
+            const int piece = threadIdx.x;
+            const int rb = rb0 + piece / per;
+            if (rb <= rb1) {
+                const int row = min(max(block_row(rb) - 1 + piece % per, 0), a.H - 1);
+                const long long jlo = max(g0 - (long long)rb * gpc, 0LL);
+                const long long jhi = min(g1 - (long long)rb * gpc, (long long)gpc);
+                const long long b0 = max(jlo * P * C - C - L::LEAD, 0LL);
+                const long long b1 = min(jhi * P * C + C, (long long)a.W * C);
+                if (b1 > b0)
+                    l2_prefetch_span(img + (long long)row * a.src_pitch + b0, b1 - b0);
+            }
+        }
+    }
+    grid_dependency_wait();
+    const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
+    if (idx >= gpc * nrb)
+        return;
+    const int rb = idx / gpc, j = idx - rb * gpc;
+    const int s0 = j * P, np = min(P, a.W - s0);
+    const int r0 = block_row(rb), r1 = block_row(rb + 1);
+    const bool words_in = ((reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
+                            static_cast<uintptr_t>(a.src_bstride)) & 3) == 0;
+    const bool inner = words_in && s0 >= 1 && (s0 - 1) * C - L::LEAD + 4 * L::NW <= a.W * C;
+    auto row_ptr = [&](int r) {
+        const int rr = BORDER == RZ_BORDER_CLAMP ? clampi(r, 0, a.H - 1) : border_index(r, a.H, BORDER);
+        return img + (long long)rr * a.src_pitch;
+    };
+    uint8_t *out = a.dst + (long long)blockIdx.y * a.dst_bstride + (long long)(2 * s0) * C;
+    // rows k = 0, 1, 2 of the window rotate through the three buffers
+    uint32_t lo[3][6], hi[3][6];
+    up2_row_lanes<C, BORDER>(row_ptr(r0 - 1), s0, a.W, inner, lo[0], hi[0]);
+    up2_row_lanes<C, BORDER>(row_ptr(r0), s0, a.W, inner, lo[1], hi[1]);
+    auto step = [&](const int ia, const int im, const int ib, int r) {
+        up2_row_lanes<C, BORDER>(row_ptr(r + 1), s0, a.W, inner, lo[ib], hi[ib]);
+        uint32_t mlo[6], mhi[6];
+#pragma unroll
+        for (int k = 0; k < 6; k++) {
+            mlo[k] = 48 * lo[im][k] + 0x00200020u;
+            mhi[k] = 48 * hi[im][k] + 0x00200020u;
+        }
+        up2_emit_row<C>(lo[ia], hi[ia], mlo, mhi, out + (long long)(2 * r) * a.dst_pitch, np);
+        up2_emit_row<C>(lo[ib], hi[ib], mlo, mhi, out + (long long)(2 * r + 1) * a.dst_pitch, np);
+    };
+    for (int r = r0; r < r1; r += 3) {
+        step(0, 1, 2, r);
+        if (r + 1 >= r1) break;
+        step(1, 2, 0, r + 1);
+        if (r + 2 >= r1) break;
+        step(2, 0, 1, r + 2);
+    }
+}
+
 // Bilinear + normalise, uint8 source, float32 planes out (y = q * scale[c] +
 // shift[c] on the exact uint8 result q, CUDA interpolation page §4.2).  A
 // warp takes 32 kNormRun consecutive output pixels of one row, lane l the
@@ -1038,6 +1248,18 @@ const void *direct_up2_kernel_for(int C, int border)
         {k_up2_direct<1, RZ_BORDER_MIRROR>, k_up2_direct<3, RZ_BORDER_MIRROR>, k_up2_direct<4, RZ_BORDER_MIRROR>},
         {k_up2_direct<1, RZ_BORDER_WRAP>, k_up2_direct<3, RZ_BORDER_WRAP>, k_up2_direct<4, RZ_BORDER_WRAP>}};
     const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
+    if (ci < 0 || border < 0 || border > 2)
+        return nullptr;
+    return reinterpret_cast<const void *>(k[border][ci]);
+}
+
+const void *direct_up2_rows_kernel_for(int C, int border)
+{
+    using Fn = void (*)(const KArgs, const CUtensorMap);
+    static const Fn k[3][2] = {{k_up2_rows<3, RZ_BORDER_CLAMP>, k_up2_rows<4, RZ_BORDER_CLAMP>},
+                               {k_up2_rows<3, RZ_BORDER_MIRROR>, k_up2_rows<4, RZ_BORDER_MIRROR>},
+                               {k_up2_rows<3, RZ_BORDER_WRAP>, k_up2_rows<4, RZ_BORDER_WRAP>}};
+    const int ci = C == 3 ? 0 : (C == 4 ? 1 : -1);
     if (ci < 0 || border < 0 || border > 2)
         return nullptr;
     return reinterpret_cast<const void *>(k[border][ci]);

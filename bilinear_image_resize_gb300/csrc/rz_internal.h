@@ -226,6 +226,9 @@ const void *direct_f32_kernel_for(int C, bool wrap);
 // source row: 8 x 2 outputs); nullptr if none.
 constexpr int kUp2Cols = 4;
 const void *direct_up2_kernel_for(int C, int border);
+// The exact 2x upscale with pixel lanes, each thread walking a.TR source rows
+// (three and four channels; nullptr otherwise).
+const void *direct_up2_rows_kernel_for(int C, int border);
 // The exact 3:2 uint8 bilinear downscale (thread per 8 outputs of a row from
 // 12 x 2 source pixels); nullptr if none.
 const void *direct_down32_kernel_for(int C);
