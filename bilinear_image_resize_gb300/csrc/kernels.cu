@@ -366,6 +366,10 @@ __device__ void compute_generic(const KArgs &a, const StageView &sv, const TileG
             const int npx = min(RUN, nc - p0);
             int2 xw[RUN];
             if (pair_ok) {
+                // a row's last run may read up to three entries past the
+                // tile's last column (values unused): plan tables keep kTabPad
+                // spare entries after their end, and the no-alloc array's
+                // column table is followed by its row table
                 const int4 v0 = __ldg(reinterpret_cast<const int4 *>(a.xt + g.dx0 + p0));
                 const int4 v1 = __ldg(reinterpret_cast<const int4 *>(a.xt + g.dx0 + p0 + 2));
                 xw[0] = make_int2(v0.x, v0.y);

@@ -32,7 +32,11 @@ constexpr int kNoAllocMaxDim = RZ_NOALLOC_MAX_DIM;
 constexpr int kMaxDevices = 64;
 
 struct NoAllocScratch {
-    int2 xt[kNoAllocMaxDim];   // per output column {source column, 11-bit weight}
+    // per output column {source column, 11-bit weight}; a staged tile's
+    // paired table loads may read up to three entries past xt[out_w - 1],
+    // which at out_w = kNoAllocMaxDim land in yt below (inside this struct;
+    // the values are not used)
+    int2 xt[kNoAllocMaxDim];
     int2 yt[kNoAllocMaxDim];   // per output row    {source row, 11-bit weight}
     int status;                // kernel status word (RZ_OK / RZ_ERR_TIMEOUT)
     int pad[63];
@@ -124,6 +128,12 @@ extern "C" int resize_u8_noalloc(const uint8_t *src, size_t src_pitch, uint8_t *
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(e);
     if (dev < 0 || dev >= kMaxDevices) return RZ_ERR_UNSUPPORTED;
+    // the array's address, the kernel attributes and the SM count are those
+    // of the current device, so the stream must belong to it
+    int stream_dev = dev;
+    e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &stream_dev);
+    if (e != cudaSuccess) return fail(e);
+    if (stream_dev != dev) return RZ_ERR_ARG;
 
     // exact 2x on both axes (W = 2 out_w, H = 2 out_h make x = 2d + 1/2)
     const bool exact2 = linear && W == 2 * out_w && H == 2 * out_h;

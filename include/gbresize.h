@@ -489,6 +489,7 @@ RZ_API int resize_plan_set_option(rz_plan p, int option, int value);
  *     same time) race on the tables and may produce wrong results.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *   - `stream` must belong to the current device (RZ_ERR_ARG otherwise).
  *   - Kernel time-outs are not reported (there is no plan to hold a status).
  */
 #define RZ_NOALLOC_MAX_DIM 8192

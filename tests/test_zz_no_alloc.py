@@ -75,3 +75,39 @@ def test_no_alloc_rejects_sizes_beyond_its_array(rz):
     with pytest.raises(rz.ResizeError) as e:
         rz.resize_u8_noalloc(src, big)
     assert e.value.code == rz.RZ_ERR_UNSUPPORTED
+
+
+# Wide outputs that the no-alloc tile loop cuts into strips: a generic
+# 8192-wide output, an exact 2x whose strips are narrower than the output,
+# and a heavy downscale whose one-strip source span is over 16 KB; every
+# channel count and both modes, two calls in a row, against the plan path.
+@pytest.mark.parametrize("C", [1, 3, 4])
+@pytest.mark.parametrize("geo", [(64, 12000, 32, 8192), (8, 16384, 4, 8192), (4, 65536, 2, 100)])
+def test_no_alloc_wide_outputs_and_strips(rz, C, geo):
+    H, W, OH, OW = geo
+    img = synth.random_u8((H, W, C), seed=W + C)
+    src = torch.from_numpy(img).cuda()
+    for mode in (rz.RZ_LINEAR, rz.RZ_NEAREST):
+        want = with_plan(rz, src, OH, OW, mode)
+        got = torch.full_like(want, 3)
+        rz.resize_u8_noalloc(src, got, mode)
+        rz.resize_u8_noalloc(src, got, mode)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want), (geo, C, mode)
+
+
+def test_no_alloc_rejects_a_stream_of_another_device(rz):
+    # only one device may be present: then a stream of the current device is
+    # accepted and the check cannot be exercised further here
+    src = torch.zeros((16, 16, 3), dtype=torch.uint8, device="cuda")
+    dst = torch.empty((8, 8, 3), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    rz.resize_u8_noalloc(src, dst, stream=s)
+    torch.cuda.synchronize()
+    if torch.cuda.device_count() < 2:
+        return
+    with torch.cuda.device(1):
+        other = torch.cuda.Stream()
+    with pytest.raises(rz.ResizeError) as e:
+        rz.resize_u8_noalloc(src, dst, stream=other)
+    assert e.value.code == rz.RZ_ERR_ARG
