@@ -24,8 +24,14 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompil
               "-I", INCLUDE, "-I", CSRC]
 
 
-def library_path() -> str:
-    return os.path.join(PKG, "libgbresize.so")
+# The bounds-checked variant (libgbresize_checked.so, for tests): these
+# sources compile with -DRZ_CHECK_BOUNDS; the others are the normal build's
+# objects.
+CHECKED_SOURCES = ["kernels.cu", "stream.cu", "direct.cu", "api.cu", "noalloc.cu"]
+
+
+def library_path(checked: bool = False) -> str:
+    return os.path.join(PKG, "libgbresize_checked.so" if checked else "libgbresize.so")
 
 
 def _nvcc() -> str:
@@ -40,17 +46,25 @@ def _stale(out: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
+    """Build libgbresize.so (or, with checked=True, after the normal build,
+    libgbresize_checked.so: the bounds-checked variant)."""
+    if checked:
+        build(force=force, verbose=verbose, extra_flags=extra_flags)
     os.makedirs(BUILD, exist_ok=True)
-    lib = library_path()
+    lib = library_path(checked)
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     if not force and not _stale(lib, srcs + HEADERS + [os.path.abspath(__file__)]):
         return lib
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
+        name = os.path.basename(src)
+        if checked and name not in CHECKED_SOURCES:
+            return os.path.join(BUILD, name + ".o")    # the normal build's object
+        obj = os.path.join(BUILD, name + (".checked.o" if checked else ".o"))
+        flags = [*extra_flags, "-DRZ_CHECK_BOUNDS"] if checked else list(extra_flags)
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         r = subprocess.run(cmd, capture_output=True, text=True)

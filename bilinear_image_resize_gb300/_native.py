@@ -115,6 +115,7 @@ SIGNATURES = {
 }
 
 _lib = None
+_lib_checked = None
 
 
 def load() -> ctypes.CDLL:
@@ -132,4 +133,23 @@ def load() -> ctypes.CDLL:
         f.restype = res
         f.argtypes = args
     _lib = lib
+    return lib
+
+
+def load_checked() -> ctypes.CDLL:
+    """The bounds-checked variant of the library (libgbresize_checked.so, built
+    by _build.build(checked=True)), with the same signatures: a test tool,
+    not used by the package's functions."""
+    global _lib_checked
+    if _lib_checked is not None:
+        return _lib_checked
+    path = library_path(checked=True)
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with _build.build(checked=True)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib_checked = lib
     return lib

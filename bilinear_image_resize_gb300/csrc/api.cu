@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -135,6 +136,7 @@ struct rz_plan_s {
     std::vector<int32_t> xofs, xq, yofs, yq;
     std::vector<float> xu, yu;
     void *dmem = nullptr;
+    size_t dmem_bytes = 0;     // tables and status word, one cudaMalloc block
     int2 *d_xq = nullptr, *d_xf = nullptr, *d_yq = nullptr, *d_yf = nullptr;
     int *d_status = nullptr;
     std::mutex mu;
@@ -793,6 +795,21 @@ int run(rz_plan_s *p, int fam, const void *src, size_t src_pitch, size_t src_bst
     a.status = p->d_status;
     a.border = p->border;
     a.l2_prefetch = p->opt_l2_prefetch;
+    a.src_extent = static_cast<long long>(src_all);
+    a.dst_extent = static_cast<long long>(dst_all);
+    a.tab = static_cast<const uint8_t *>(p->dmem);
+    a.tab_bytes = static_cast<long long>(p->dmem_bytes);
+#ifdef RZ_CHECK_BOUNDS
+    // test hook of the checked build: declare the last RZ_CHECK_SHRINK bytes
+    // of the source and of the output out of range (the buffers themselves
+    // are whole, so an access the kernels should have refused still lands in
+    // valid memory)
+    if (const char *shrink = std::getenv("RZ_CHECK_SHRINK")) {
+        const long long n = std::atoll(shrink);
+        a.src_extent = std::max(0LL, a.src_extent - n);
+        a.dst_extent = std::max(0LL, a.dst_extent - n);
+    }
+#endif
     if (run_direct(p, fam, a, mode, stream, do_launch, &rc)) return rc;
     // the staged and streaming kernels take source spans from the tables,
     // which under the wrap rule are not monotone at the edges
@@ -940,6 +957,7 @@ int resize_plan_create_border(rz_plan *out, int in_h, int in_w, int out_h, int o
     }
     e = cudaMalloc(&p->dmem, total);
     if (e != cudaSuccess) { p->dmem = nullptr; delete p; return cuda_fail(e); }
+    p->dmem_bytes = total;
     uint8_t *d = static_cast<uint8_t *>(p->dmem);
     p->d_xq = reinterpret_cast<int2 *>(d) + kPad;
     p->d_xf = reinterpret_cast<int2 *>(d + off_xf) + kPad;

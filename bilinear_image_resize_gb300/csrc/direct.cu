@@ -40,10 +40,10 @@ __device__ __noinline__ void down2_row_tail(const uint8_t *top, const uint8_t *b
         for (int c = 0; c < C; c++) {
             const int o = 2 * p * C + c;
             if (LINEAR) {
-                const int s = top[o] + top[o + C] + bot[o] + bot[o + C] + 2;
-                out[p * C + c] = static_cast<uint8_t>(s >> 2);
+                const int s = ld_g(top + o) + ld_g(top + o + C) + ld_g(bot + o) + ld_g(bot + o + C) + 2;
+                st_g(out + p * C + c, static_cast<uint8_t>(s >> 2));
             } else {
-                out[p * C + c] = top[o];
+                st_g(out + p * C + c, ld_g(top + o));
             }
         }
 }
@@ -70,18 +70,18 @@ __device__ __forceinline__ void down2_one(const uint8_t *top, const uint8_t *bot
         const uint2 *bp = reinterpret_cast<const uint2 *>(bot + SB * j);
 #pragma unroll
         for (int k = 0; k < 3; k++) {
-            const uint2 t = __ldcs(tp + k);
+            const uint2 t = ld_cs(tp + k);
             tw[2 * k] = t.x; tw[2 * k + 1] = t.y;
             if (LINEAR) {
-                const uint2 u = __ldcs(bp + k);
+                const uint2 u = ld_cs(bp + k);
                 bw[2 * k] = u.x; bw[2 * k + 1] = u.y;
             }
         }
     } else {
-        const uint4 t = __ldcs(reinterpret_cast<const uint4 *>(top + SB * j));
+        const uint4 t = ld_cs(reinterpret_cast<const uint4 *>(top + SB * j));
         tw[0] = t.x; tw[1] = t.y; tw[2] = t.z; tw[3] = t.w;
         if (LINEAR) {
-            const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(bot + SB * j));
+            const uint4 u = ld_cs(reinterpret_cast<const uint4 *>(bot + SB * j));
             bw[0] = u.x; bw[1] = u.y; bw[2] = u.z; bw[3] = u.w;
         }
     }
@@ -91,11 +91,11 @@ __device__ __forceinline__ void down2_one(const uint8_t *top, const uint8_t *bot
         down2_nearest_group<C>(tw, o);
     if constexpr (C == 3) {
         uint32_t *op = reinterpret_cast<uint32_t *>(out + OB * j);
-        __stcs(op, o[0]);
-        __stcs(op + 1, o[1]);
-        __stcs(op + 2, o[2]);
+        st_cs(op, o[0]);
+        st_cs(op + 1, o[1]);
+        st_cs(op + 2, o[2]);
     } else {
-        __stcs(reinterpret_cast<uint2 *>(out + OB * j), make_uint2(o[0], o[1]));
+        st_cs(reinterpret_cast<uint2 *>(out + OB * j), make_uint2(o[0], o[1]));
     }
 }
 
@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_direct(const KArgs a, 
     constexpr int PX = down2_px(C);       // output pixels per group: 8, 4, 2
     constexpr int SB = 2 * PX * C;        // source bytes per row and group: 16, 24, 16
     grid_launch_dependents();
+    bounds_begin(a);
     const int full = a.OW / PX;                // whole groups per row
     const int gpr = full + (a.OW % PX ? 1 : 0);
     if (first_wave_cta(a))
@@ -149,6 +150,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
 {
     constexpr int RUN = 4;
     grid_launch_dependents();
+    bounds_begin(a);
     grid_dependency_wait();
     const int gpr = (a.OW + RUN - 1) / RUN;
     const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
@@ -159,11 +161,11 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
     const int row_bytes = a.W * C;
     // the tables are 16-byte aligned with spare entries past their end, and
     // x0 is a multiple of 4
-    const int4 xa = __ldg(reinterpret_cast<const int4 *>(a.xt + x0));
-    const int4 xb = __ldg(reinterpret_cast<const int4 *>(a.xt + x0 + 2));
+    const int4 xa = ld_nc(reinterpret_cast<const int4 *>(a.xt + x0));
+    const int4 xb = ld_nc(reinterpret_cast<const int4 *>(a.xt + x0 + 2));
     const int xs[RUN] = {xa.x, xa.z, xb.x, xb.z};   // left tap (nearest: the tap)
     const int xw[RUN] = {xa.y, xa.w, xb.y, xb.w};   // right tap's 11-bit weight
-    const int2 ye = __ldg(a.yt + dy);
+    const int2 ye = ld_nc(a.yt + dy);
     const int r0 = ye.x, r1 = LINEAR ? far_tap<WRAP>(ye.x, a.H) : ye.x;
     const int B1 = ye.y, B0 = 2048 - B1;
     const bool words_in = ((reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
             } else if (!LINEAR) {
 #pragma unroll
                 for (int c = 0; c < C; c++)
-                    q[k][c] = __ldg(top + o0 + c);
+                    q[k][c] = ld_nc(top + o0 + c);
             } else {
                 int hT[C], hB[C];
                 // o0 + 12 <= row bytes puts the far tap inside (xs <= W - 2)
@@ -195,8 +197,8 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
                     const int o1 = far_tap<WRAP>(xs[k], a.W) * C;
 #pragma unroll
                     for (int c = 0; c < C; c++) {
-                        hT[c] = (2048 - xw[k]) * __ldg(top + o0 + c) + xw[k] * __ldg(top + o1 + c);
-                        hB[c] = (2048 - xw[k]) * __ldg(bot + o0 + c) + xw[k] * __ldg(bot + o1 + c);
+                        hT[c] = (2048 - xw[k]) * ld_nc(top + o0 + c) + xw[k] * ld_nc(top + o1 + c);
+                        hB[c] = (2048 - xw[k]) * ld_nc(bot + o0 + c) + xw[k] * ld_nc(bot + o1 + c);
                     }
                 }
 #pragma unroll
@@ -209,15 +211,15 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
         if (words) {
             uint32_t *o = reinterpret_cast<uint32_t *>(op);
             if constexpr (C == 1) {
-                __stcs(o, pack4(q[0][0], q[1][0], q[2][0], q[3][0]));
+                st_cs(o, pack4(q[0][0], q[1][0], q[2][0], q[3][0]));
             } else if constexpr (C == 3) {
-                __stcs(o, pack4(q[0][0], q[0][1], q[0][2], q[1][0]));
-                __stcs(o + 1, pack4(q[1][1], q[1][2], q[2][0], q[2][1]));
-                __stcs(o + 2, pack4(q[2][2], q[3][0], q[3][1], q[3][2]));
+                st_cs(o, pack4(q[0][0], q[0][1], q[0][2], q[1][0]));
+                st_cs(o + 1, pack4(q[1][1], q[1][2], q[2][0], q[2][1]));
+                st_cs(o + 2, pack4(q[2][2], q[3][0], q[3][1], q[3][2]));
             } else {
 #pragma unroll
                 for (int k = 0; k < RUN; k++)
-                    __stcs(o + k, pack4(q[k][0], q[k][1], q[k][2], q[k][3]));
+                    st_cs(o + k, pack4(q[k][0], q[k][1], q[k][2], q[k][3]));
             }
         } else {
 #pragma unroll
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
                 if (k < npx)
 #pragma unroll
                     for (int c = 0; c < C; c++)
-                        op[k * C + c] = static_cast<uint8_t>(q[k][c]);
+                        st_g(op + k * C + c, static_cast<uint8_t>(q[k][c]));
         }
     }
 }
@@ -252,6 +254,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_down32_direct(const KArgs a,
     constexpr int NW = 3 * C;      // source words per row: 12 pixels
     constexpr int NWO = 2 * C;     // output words: 8 pixels
     grid_launch_dependents();
+    bounds_begin(a);
     const int full = a.OW / PX;
     const int gpr = full + (a.OW % PX ? 1 : 0);
     if (first_wave_cta(a))
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_down32_direct(const KArgs a,
             const uint32_t *wb = reinterpret_cast<const uint32_t *>(rb + 12 * C * j);
 #pragma unroll
             for (int i = 0; i < NW; i++) {
-                const uint32_t x = __ldcs(wa + i), y = __ldg(wb + i);
+                const uint32_t x = ld_cs(wa + i), y = ld_nc(wb + i);
                 vl[i] = 3 * (x & 0x00ff00ffu) + (y & 0x00ff00ffu);
                 vh[i] = 3 * ((x >> 8) & 0x00ff00ffu) + ((y >> 8) & 0x00ff00ffu);
             }
@@ -300,15 +303,23 @@ __global__ void __launch_bounds__(kDirectThreads) k_down32_direct(const KArgs a,
                     const uint32_t x1 = lane((3 * i + 1) * C + c);
                     q[k] = (3 * x3 + x1 + 8) >> 4;
                 }
-                __stcs(op + wo, q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24));
+                st_cs(op + wo, q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24));
             }
         } else {
             // the row's last pixels, fewer than eight: byte by byte
             for (int ox = full * PX; ox < a.OW; ox++) {
                 const int i = ox >> 1, s3 = (ox & 1) ? 3 * i + 2 : 3 * i, s1 = 3 * i + 1;
                 for (int c = 0; c < C; c++) {
+#ifdef RZ_CHECK_BOUNDS
+                    const int v = 9 * ld_g(ra + s3 * C + c) + 3 * ld_g(ra + s1 * C + c) + 3 * ld_g(rb + s3 * C + c) +
+                                  ld_g(rb + s1 * C + c);
+                    st_g(o + ox * C + c, static_cast<uint8_t>((v + 8) >> 4));
+#else
+                    // (plain accesses here: the wrapper form changes this
+                    // kernel's register allocation and slows its main path)
                     const int v = 9 * ra[s3 * C + c] + 3 * ra[s1 * C + c] + 3 * rb[s3 * C + c] + rb[s1 * C + c];
                     o[ox * C + c] = static_cast<uint8_t>((v + 8) >> 4);
+#endif
                 }
             }
         }
@@ -422,6 +433,7 @@ __global__ void __launch_bounds__(kDirectThreads, Up2Occupancy<C, BORDER>::value
     using Lay = Up2Layout<C>;
     constexpr int P = Lay::P, NB = Lay::NB, LEAD = Lay::LEAD, NW = Lay::NW, NWO = Lay::NWO;
     grid_launch_dependents();
+    bounds_begin(a);
     const int gpr = (a.W + P - 1) / P;
     if (first_wave_cta(a)) {
         // source rows r - 1, r, r + 1 (edge rows of the mirror and wrap rules
@@ -456,7 +468,7 @@ __global__ void __launch_bounds__(kDirectThreads, Up2Occupancy<C, BORDER>::value
                 const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (s0 - 1) * C - LEAD);
 #pragma unroll
                 for (int i = 0; i < NW; i++)
-                    wd[i] = __ldg(w + i);
+                    wd[i] = ld_nc(w + i);
             } else {
 #pragma unroll
                 for (int i = 0; i < NW; i++)
@@ -465,7 +477,7 @@ __global__ void __launch_bounds__(kDirectThreads, Up2Occupancy<C, BORDER>::value
                 for (int i = 0; i < NB; i++) {
                     const int col = BORDER == RZ_BORDER_CLAMP ? clampi(s0 - 1 + i / C, 0, a.W - 1)
                                                               : border_index(s0 - 1 + i / C, a.W, BORDER);
-                    wd[(LEAD + i) / 4] |= static_cast<uint32_t>(__ldg(row + col * C + i % C)) << (8 * ((LEAD + i) % 4));
+                    wd[(LEAD + i) / 4] |= static_cast<uint32_t>(ld_nc(row + col * C + i % C)) << (8 * ((LEAD + i) % 4));
                 }
             }
 #pragma unroll
@@ -535,21 +547,21 @@ __global__ void __launch_bounds__(kDirectThreads, Up2Occupancy<C, BORDER>::value
             if (np == P && NWO % 4 == 0 && (oa & 15) == 0) {
 #pragma unroll
                 for (int i = 0; i < NWO; i += 4)
-                    __stcs(reinterpret_cast<uint4 *>(op) + i / 4, make_uint4(ow[i], ow[i + 1], ow[i + 2], ow[i + 3]));
+                    st_cs(reinterpret_cast<uint4 *>(op) + i / 4, make_uint4(ow[i], ow[i + 1], ow[i + 2], ow[i + 3]));
             } else if (np == P && NWO % 2 == 0 && (oa & 7) == 0) {
 #pragma unroll
                 for (int i = 0; i < NWO; i += 2)
-                    __stcs(reinterpret_cast<uint2 *>(op) + i / 2, make_uint2(ow[i], ow[i + 1]));
+                    st_cs(reinterpret_cast<uint2 *>(op) + i / 2, make_uint2(ow[i], ow[i + 1]));
             } else if (np == P && (oa & 3) == 0) {
                 uint32_t *o = reinterpret_cast<uint32_t *>(op);
 #pragma unroll
                 for (int i = 0; i < NWO; i++)
-                    __stcs(o + i, ow[i]);
+                    st_cs(o + i, ow[i]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 2 * P * C; i++)
                     if (i < 2 * np * C)
-                        op[i] = static_cast<uint8_t>(ow[i / 4] >> (8 * (i % 4)));
+                        st_g(op + i, static_cast<uint8_t>(ow[i / 4] >> (8 * (i % 4))));
             }
         }
     }
@@ -607,7 +619,7 @@ __device__ __forceinline__ void up2_row_lanes(const uint8_t *row, int s0, int W,
         const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (s0 - 1) * C - L::LEAD);
 #pragma unroll
         for (int i = 0; i < L::NW; i++)
-            wd[i] = __ldg(w + i);
+            wd[i] = ld_nc(w + i);
     } else {
 #pragma unroll
         for (int i = 0; i < L::NW; i++)
@@ -616,7 +628,7 @@ __device__ __forceinline__ void up2_row_lanes(const uint8_t *row, int s0, int W,
         for (int i = 0; i < L::NB; i++) {
             const int col = BORDER == RZ_BORDER_CLAMP ? clampi(s0 - 1 + i / C, 0, W - 1)
                                                       : border_index(s0 - 1 + i / C, W, BORDER);
-            wd[(L::LEAD + i) / 4] |= static_cast<uint32_t>(__ldg(row + col * C + i % C)) << (8 * ((L::LEAD + i) % 4));
+            wd[(L::LEAD + i) / 4] |= static_cast<uint32_t>(ld_nc(row + col * C + i % C)) << (8 * ((L::LEAD + i) % 4));
         }
     }
 #pragma unroll
@@ -671,20 +683,20 @@ __device__ __forceinline__ void up2_emit_row(const uint32_t (&tlo)[6], const uin
     if (np == 4 && L::NWO % 4 == 0 && (oa & 15) == 0) {
 #pragma unroll
         for (int i = 0; i < L::NWO; i += 4)
-            __stcs(reinterpret_cast<uint4 *>(op) + i / 4, make_uint4(ow[i], ow[i + 1], ow[i + 2], ow[i + 3]));
+            st_cs(reinterpret_cast<uint4 *>(op) + i / 4, make_uint4(ow[i], ow[i + 1], ow[i + 2], ow[i + 3]));
     } else if (np == 4 && L::NWO % 2 == 0 && (oa & 7) == 0) {
 #pragma unroll
         for (int i = 0; i < L::NWO; i += 2)
-            __stcs(reinterpret_cast<uint2 *>(op) + i / 2, make_uint2(ow[i], ow[i + 1]));
+            st_cs(reinterpret_cast<uint2 *>(op) + i / 2, make_uint2(ow[i], ow[i + 1]));
     } else if (np == 4 && (oa & 3) == 0) {
 #pragma unroll
         for (int i = 0; i < L::NWO; i++)
-            __stcs(reinterpret_cast<uint32_t *>(op) + i, ow[i]);
+            st_cs(reinterpret_cast<uint32_t *>(op) + i, ow[i]);
     } else {
 #pragma unroll
         for (int i = 0; i < 8 * C; i++)
             if (i < 2 * np * C)
-                op[i] = static_cast<uint8_t>(ow[i / 4] >> (8 * (i % 4)));
+                st_g(op + i, static_cast<uint8_t>(ow[i / 4] >> (8 * (i % 4))));
     }
 }
 
@@ -701,6 +713,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_up2_rows(const KArgs a, cons
     using L = Up2RowsLayout<C>;
     constexpr int P = L::P;
     grid_launch_dependents();
+    bounds_begin(a);
     const int gpc = (a.W + P - 1) / P;          // column groups per row block
     const int nrb = a.tiles_y;
     auto block_row = [&](int rb) { return static_cast<int>((long long)rb * a.H / nrb); };
@@ -777,6 +790,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_norm(const KArgs a, c
 {
     constexpr int RUN = kNormRun;
     grid_launch_dependents();
+    bounds_begin(a);
     grid_dependency_wait();
     const int wpr = (a.OW + 32 * RUN - 1) / (32 * RUN);   // warps per output row
     const int gw = (blockIdx.x * kDirectThreads + threadIdx.x) >> 5, lane = threadIdx.x & 31;
@@ -790,11 +804,11 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_norm(const KArgs a, c
     for (int k = 0; k < RUN; k++) {
         const int x = xb + lane + 32 * k;
         ok[k] = x < a.OW;
-        const int2 e = __ldg(a.xt + min(x, a.OW - 1));
+        const int2 e = ld_nc(a.xt + min(x, a.OW - 1));
         xs[k] = e.x;
         xw[k] = e.y;
     }
-    const int2 ye = __ldg(a.yt + dy);
+    const int2 ye = ld_nc(a.yt + dy);
     const int r0 = ye.x, r1 = far_tap<WRAP>(ye.x, a.H);
     const int B1 = ye.y, B0 = 2048 - B1;
     const bool words_in = ((reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
@@ -816,8 +830,8 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_norm(const KArgs a, c
                 const int o1 = far_tap<WRAP>(xs[k], a.W) * C;
 #pragma unroll
                 for (int c = 0; c < C; c++) {
-                    hT[c] = (2048 - xw[k]) * __ldg(top + o0 + c) + xw[k] * __ldg(top + o1 + c);
-                    hB[c] = (2048 - xw[k]) * __ldg(bot + o0 + c) + xw[k] * __ldg(bot + o1 + c);
+                    hT[c] = (2048 - xw[k]) * ld_nc(top + o0 + c) + xw[k] * ld_nc(top + o1 + c);
+                    hB[c] = (2048 - xw[k]) * ld_nc(bot + o0 + c) + xw[k] * ld_nc(bot + o1 + c);
                 }
             }
 #pragma unroll
@@ -831,7 +845,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_norm(const KArgs a, c
 #pragma unroll
             for (int k = 0; k < RUN; k++)
                 if (ok[k])
-                    __stcs(pl + 32 * k, fmaf(static_cast<float>(q[k][c]), a.scale[c], a.shift[c]));
+                    st_cs(pl + 32 * k, fmaf(static_cast<float>(q[k][c]), a.scale[c], a.shift[c]));
         }
     }
 }
@@ -849,6 +863,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_rows(const KArgs a, c
 {
     constexpr int RUN = 4;
     grid_launch_dependents();
+    bounds_begin(a);
     grid_dependency_wait();
     const int gpr = (a.OW + RUN - 1) / RUN;
     const int segs = (a.OH + a.TR - 1) / a.TR;
@@ -859,8 +874,8 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_rows(const KArgs a, c
     const int dy0 = sg * a.TR, dy1 = min(dy0 + a.TR, a.OH);
     const int npx = min(RUN, a.OW - x0);
     const int row_bytes = a.W * C;
-    const int4 xa = __ldg(reinterpret_cast<const int4 *>(a.xt + x0));
-    const int4 xb = __ldg(reinterpret_cast<const int4 *>(a.xt + x0 + 2));
+    const int4 xa = ld_nc(reinterpret_cast<const int4 *>(a.xt + x0));
+    const int4 xb = ld_nc(reinterpret_cast<const int4 *>(a.xt + x0 + 2));
     const int xs[RUN] = {xa.x, xa.z, xb.x, xb.z};
     const int xw[RUN] = {xa.y, xa.w, xb.y, xb.w};
     uint32_t aw[RUN];
@@ -883,7 +898,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_rows(const KArgs a, c
             } else {
 #pragma unroll
                 for (int c = 0; c < C; c++)
-                    h[k][c] = (2048 - xw[k]) * __ldg(row + xs[k] * C + c) + xw[k] * __ldg(row + o1[k] + c);
+                    h[k][c] = (2048 - xw[k]) * ld_nc(row + xs[k] * C + c) + xw[k] * ld_nc(row + o1[k] + c);
             }
         }
     };
@@ -896,7 +911,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_rows(const KArgs a, c
         bool newer1 = false;          // h1 holds the newer row
         int last = -1;                // the newest sampled row
         for (int dy = dy0; dy < dy1; dy++) {
-            const int2 ye = __ldg(a.yt + dy);
+            const int2 ye = ld_nc(a.yt + dy);
             const int r0 = ye.x, r1 = min(ye.x + 1, a.H - 1);
             if (r1 > last) {
                 if (r0 > last) {
@@ -925,15 +940,15 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_rows(const KArgs a, c
             if (words) {
                 uint32_t *o = reinterpret_cast<uint32_t *>(op);
                 if constexpr (C == 1) {
-                    __stcs(o, pack4(q[0][0], q[1][0], q[2][0], q[3][0]));
+                    st_cs(o, pack4(q[0][0], q[1][0], q[2][0], q[3][0]));
                 } else if constexpr (C == 3) {
-                    __stcs(o, pack4(q[0][0], q[0][1], q[0][2], q[1][0]));
-                    __stcs(o + 1, pack4(q[1][1], q[1][2], q[2][0], q[2][1]));
-                    __stcs(o + 2, pack4(q[2][2], q[3][0], q[3][1], q[3][2]));
+                    st_cs(o, pack4(q[0][0], q[0][1], q[0][2], q[1][0]));
+                    st_cs(o + 1, pack4(q[1][1], q[1][2], q[2][0], q[2][1]));
+                    st_cs(o + 2, pack4(q[2][2], q[3][0], q[3][1], q[3][2]));
                 } else {
 #pragma unroll
                     for (int k = 0; k < RUN; k++)
-                        __stcs(o + k, pack4(q[k][0], q[k][1], q[k][2], q[k][3]));
+                        st_cs(o + k, pack4(q[k][0], q[k][1], q[k][2], q[k][3]));
                 }
             } else {
 #pragma unroll
@@ -941,7 +956,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_rows(const KArgs a, c
                     if (k < npx)
 #pragma unroll
                         for (int c = 0; c < C; c++)
-                            op[k * C + c] = static_cast<uint8_t>(q[k][c]);
+                            st_g(op + k * C + c, static_cast<uint8_t>(q[k][c]));
             }
             op += a.dst_pitch;
         }
@@ -954,7 +969,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_rows(const KArgs a, c
 __device__ __forceinline__ uint64_t load_8_bytes(const uint8_t *row, int o0)
 {
     const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (o0 & ~3));
-    const uint32_t w0 = __ldg(w), w1 = __ldg(w + 1), w2 = __ldg(w + 2);
+    const uint32_t w0 = ld_nc(w), w1 = ld_nc(w + 1), w2 = ld_nc(w + 2);
     const uint32_t sh = 8u * static_cast<uint32_t>(o0 & 3);
     return static_cast<uint64_t>(__funnelshift_r(w1, w2, sh)) << 32 | __funnelshift_r(w0, w1, sh);
 }
@@ -992,7 +1007,7 @@ template <int C>
 __device__ __forceinline__ int gray_at(const uint8_t *row, int x, int ir, int ib)
 {
     const uint8_t *px = row + x * C;
-    return gray_of(__ldg(px + ir), __ldg(px + 1), __ldg(px + ib));
+    return gray_of(ld_nc(px + ir), ld_nc(px + 1), ld_nc(px + ib));
 }
 
 // Grayscale conversion fused before the uint8 resize (OpenCV object-tracking
@@ -1009,6 +1024,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_gray(const KArgs a, c
 {
     constexpr int RUN = 4;
     grid_launch_dependents();
+    bounds_begin(a);
     grid_dependency_wait();
     const int gpr = (a.OW + RUN - 1) / RUN;
     const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
@@ -1019,11 +1035,11 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_gray(const KArgs a, c
     const int row_bytes = a.W * C;
     const int ir = a.bgr ? 2 : 0, ib = a.bgr ? 0 : 2;
     const uint32_t wlo = a.bgr ? kGrayLoBGR : kGrayLoRGB, whi = a.bgr ? kGrayHiBGR : kGrayHiRGB;
-    const int4 xa = __ldg(reinterpret_cast<const int4 *>(a.xt + x0));
-    const int4 xb = __ldg(reinterpret_cast<const int4 *>(a.xt + x0 + 2));
+    const int4 xa = ld_nc(reinterpret_cast<const int4 *>(a.xt + x0));
+    const int4 xb = ld_nc(reinterpret_cast<const int4 *>(a.xt + x0 + 2));
     const int xs[RUN] = {xa.x, xa.z, xb.x, xb.z};
     const int xw[RUN] = {xa.y, xa.w, xb.y, xb.w};
-    const int2 ye = __ldg(a.yt + dy);
+    const int2 ye = ld_nc(a.yt + dy);
     const int r0 = ye.x, r1 = LINEAR ? far_tap<WRAP>(ye.x, a.H) : ye.x;
     const int B1 = ye.y, B0 = 2048 - B1;
     const bool words_in = ((reinterpret_cast<uintptr_t>(a.src) | static_cast<uintptr_t>(a.src_pitch) |
@@ -1061,12 +1077,12 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_gray(const KArgs a, c
         }
         uint8_t *op = a.dst + (long long)b * a.dst_bstride + (long long)dy * a.dst_pitch + x0;
         if (npx == RUN && (reinterpret_cast<uintptr_t>(op) & 3) == 0) {
-            __stcs(reinterpret_cast<uint32_t *>(op), pack4(q[0], q[1], q[2], q[3]));
+            st_cs(reinterpret_cast<uint32_t *>(op), pack4(q[0], q[1], q[2], q[3]));
         } else {
 #pragma unroll
             for (int k = 0; k < RUN; k++)
                 if (k < npx)
-                    op[k] = static_cast<uint8_t>(q[k]);
+                    st_g(op + k, static_cast<uint8_t>(q[k]));
         }
     }
 }
@@ -1097,7 +1113,7 @@ __device__ __noinline__ void gray_down2_row_tail(const uint8_t *top, const uint8
         if (LINEAR)
             g = (g + gray_at<C>(top, 2 * p + 1, IR, IB) + gray_at<C>(bot, 2 * p, IR, IB) +
                  gray_at<C>(bot, 2 * p + 1, IR, IB) + 2) >> 2;
-        out[p] = static_cast<uint8_t>(g);
+        st_g(out + p, static_cast<uint8_t>(g));
     }
 }
 
@@ -1115,6 +1131,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_gray(const KArgs a, co
 {
     constexpr int PX = 4, SB = 2 * PX * C, NW = SB / 4;
     grid_launch_dependents();
+    bounds_begin(a);
     const int full = a.OW / PX;
     const int gpr = full + (a.OW % PX ? 1 : 0);
     if (first_wave_cta(a))
@@ -1139,10 +1156,10 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_gray(const KArgs a, co
         const uint2 *bp = reinterpret_cast<const uint2 *>(bot + SB * j);
 #pragma unroll
         for (int k = 0; k < 3; k++) {
-            const uint2 t = __ldcs(tp + k);
+            const uint2 t = ld_cs(tp + k);
             tw[2 * k] = t.x; tw[2 * k + 1] = t.y;
             if (LINEAR) {
-                const uint2 u = __ldcs(bp + k);
+                const uint2 u = ld_cs(bp + k);
                 bw[2 * k] = u.x; bw[2 * k + 1] = u.y;
             }
         }
@@ -1151,10 +1168,10 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_gray(const KArgs a, co
         const uint4 *bp = reinterpret_cast<const uint4 *>(bot + SB * j);
 #pragma unroll
         for (int k = 0; k < 2; k++) {
-            const uint4 t = __ldcs(tp + k);
+            const uint4 t = ld_cs(tp + k);
             tw[4 * k] = t.x; tw[4 * k + 1] = t.y; tw[4 * k + 2] = t.z; tw[4 * k + 3] = t.w;
             if (LINEAR) {
-                const uint4 u = __ldcs(bp + k);
+                const uint4 u = ld_cs(bp + k);
                 bw[4 * k] = u.x; bw[4 * k + 1] = u.y; bw[4 * k + 2] = u.z; bw[4 * k + 3] = u.w;
             }
         }
@@ -1167,7 +1184,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_gray(const KArgs a, co
             q[k] = (q[k] + gray_word_px<C, BGR, NW>(tw, 2 * k + 1) + gray_word_px<C, BGR, NW>(bw, 2 * k) +
                     gray_word_px<C, BGR, NW>(bw, 2 * k + 1) + 2) >> 2;
     }
-    __stcs(reinterpret_cast<uint32_t *>(out + PX * j), pack4(q[0], q[1], q[2], q[3]));
+    st_cs(reinterpret_cast<uint32_t *>(out + PX * j), pack4(q[0], q[1], q[2], q[3]));
 }
 
 // float32 bilinear, a thread per output pixel (all C channels): the lerp form
@@ -1179,12 +1196,13 @@ template <int C, bool WRAP>
 __global__ void __launch_bounds__(kDirectThreads) k_direct_f32(const KArgs a, const __grid_constant__ CUtensorMap)
 {
     grid_launch_dependents();
+    bounds_begin(a);
     grid_dependency_wait();
     const long long idx = static_cast<long long>(blockIdx.x) * kDirectThreads + threadIdx.x;
     if (idx >= static_cast<long long>(a.OH) * a.OW)
         return;
     const int dy = static_cast<int>(idx / a.OW), dx = static_cast<int>(idx - static_cast<long long>(dy) * a.OW);
-    const int2 xe = __ldg(a.xt + dx), ye = __ldg(a.yt + dy);
+    const int2 xe = ld_nc(a.xt + dx), ye = ld_nc(a.yt + dy);
     const float u = __int_as_float(xe.y), v = __int_as_float(ye.y);
     const int c0 = xe.x * C, c1 = far_tap<WRAP>(xe.x, a.W) * C;
     const int y1 = far_tap<WRAP>(ye.x, a.H);
@@ -1196,10 +1214,10 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct_f32(const KArgs a, co
                     static_cast<long long>(dx) * C;
 #pragma unroll
         for (int c = 0; c < C; c++) {
-            const float t0 = __ldg(top + c0 + c), t1 = __ldg(top + c1 + c);
-            const float b0 = __ldg(bot + c0 + c), b1 = __ldg(bot + c1 + c);
+            const float t0 = ld_nc(top + c0 + c), t1 = ld_nc(top + c1 + c);
+            const float b0 = ld_nc(bot + c0 + c), b1 = ld_nc(bot + c1 + c);
             const float h0 = fmaf(u, t1 - t0, t0), h1 = fmaf(u, b1 - b0, b0);
-            __stcs(op + c, fmaf(v, h1 - h0, h0));
+            st_cs(op + c, fmaf(v, h1 - h0, h0));
         }
     }
 }

@@ -216,7 +216,8 @@ __device__ void fetch_stage(const KArgs &a, const SmemLayout &L, const uint8_t *
                 const uint8_t *src = img + (long long)rows[r] * a.src_pitch + b_lo;
                 uint8_t *d = slots + r * a.slot_bytes;
                 for (int k = lane; k < nbytes; k += 32)
-                    d[k] = __ldg(src + k);
+                    if (smem_guard(d + k, 1))
+                        d[k] = ld_nc(src + k);
             }
             __syncwarp();
             mbar_arrive(full);
@@ -251,7 +252,8 @@ __device__ void fetch_stage(const KArgs &a, const SmemLayout &L, const uint8_t *
             const uint8_t *src = img + (long long)rows[r] * a.src_pitch + b_lo;
             uint8_t *d = slots + r * a.slot_bytes;
             for (int k = lane; k < nbytes; k += 32)
-                d[k] = __ldg(src + k);
+                if (smem_guard(d + k, 1))
+                    d[k] = ld_nc(src + k);
         }
         mbar_arrive(full);   // each lane releases its own copies
     }
@@ -291,7 +293,9 @@ __device__ void store_tail(const KArgs &a, const SmemLayout &L, const uint8_t *o
     for (int k = threadIdx.x; k < n; k += kConsumers) {
         const int row = k / tail, j = k - row * tail;
         const int c = row / nr, i = row - c * nr;
-        base[c * a.dst_plane + i * a.dst_pitch + j] = ob[(c * a.TR + i) * L.out_row_bytes + bulk + j];
+        const uint8_t *sp = ob + (c * a.TR + i) * L.out_row_bytes + bulk + j;
+        if (smem_guard(sp, 1))
+            st_g(base + c * a.dst_plane + i * a.dst_pitch + j, *sp);
     }
 }
 
@@ -357,7 +361,7 @@ __device__ void compute_generic(const KArgs &a, const StageView &sv, const TileG
     const int tpr = 1 << lg, rpp = kConsumers >> lg;
     const bool pair_ok = (g.dx0 & 1) == 0;   // 16-byte table loads start on an even column
     for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
-        const int2 yw = __ldg(&a.yt[g.dy0 + rl]);
+        const int2 yw = ld_nc(&a.yt[g.dy0 + rl]);
         const uint8_t *top = sv.slots + sv.map[2 * rl] * sv.slot_bytes;
         const uint8_t *bot = sv.slots + sv.map[2 * rl + 1] * sv.slot_bytes;
         uint8_t *orow = ob_bytes + rl * orow_bytes;
@@ -370,8 +374,8 @@ __device__ void compute_generic(const KArgs &a, const StageView &sv, const TileG
                 // tile's last column (values unused): plan tables keep kTabPad
                 // spare entries after their end, and the no-alloc array's
                 // column table is followed by its row table
-                const int4 v0 = __ldg(reinterpret_cast<const int4 *>(a.xt + g.dx0 + p0));
-                const int4 v1 = __ldg(reinterpret_cast<const int4 *>(a.xt + g.dx0 + p0 + 2));
+                const int4 v0 = ld_nc(reinterpret_cast<const int4 *>(a.xt + g.dx0 + p0));
+                const int4 v1 = ld_nc(reinterpret_cast<const int4 *>(a.xt + g.dx0 + p0 + 2));
                 xw[0] = make_int2(v0.x, v0.y);
                 xw[1] = make_int2(v0.z, v0.w);
                 xw[2] = make_int2(v1.x, v1.y);
@@ -379,7 +383,7 @@ __device__ void compute_generic(const KArgs &a, const StageView &sv, const TileG
             } else {
 #pragma unroll
                 for (int k = 0; k < RUN; k++)
-                    xw[k] = p0 + k < nc ? __ldg(&a.xt[g.dx0 + p0 + k]) : make_int2(0, 0);
+                    xw[k] = p0 + k < nc ? ld_nc(&a.xt[g.dx0 + p0 + k]) : make_int2(0, 0);
             }
             if constexpr (ES == 1) {
                 int q[RUN][C];
@@ -388,9 +392,10 @@ __device__ void compute_generic(const KArgs &a, const StageView &sv, const TileG
                     if (k < npx) {
                         const int o0 = xw[k].x * C - sv.b_lo;
                         if (!LINEAR) {
+                            const bool ok = smem_guard(top + o0, C);
 #pragma unroll
                             for (int c = 0; c < C; c++)
-                                q[k][c] = top[o0 + c];
+                                q[k][c] = ok ? top[o0 + c] : 0;
                         } else {
                             const uint32_t aw = static_cast<uint32_t>(2048 - xw[k].y) |
                                                 (static_cast<uint32_t>(xw[k].y) << 16);
@@ -403,6 +408,8 @@ __device__ void compute_generic(const KArgs &a, const StageView &sv, const TileG
                     }
                 }
                 uint8_t *o = orow + p0 * C;
+                if (!smem_guard(o, npx * C))
+                    continue;
                 if (npx == RUN) {
                     if constexpr (C == 1) {
                         *reinterpret_cast<uint32_t *>(o) = pack4(q[0][0], q[1][0], q[2][0], q[3][0]);
@@ -436,11 +443,19 @@ __device__ void compute_generic(const KArgs &a, const StageView &sv, const TileG
                     if (k < npx) {
                         const int o0 = xw[k].x * C - lo;
                         if (!LINEAR) {
+                            const bool ok = smem_guard(ft + o0, 4 * C);
 #pragma unroll
                             for (int c = 0; c < C; c++)
-                                r[k][c] = ft[o0 + c];
+                                r[k][c] = ok ? ft[o0 + c] : 0.0f;
                         } else {
                             const int o1 = min(xw[k].x + 1, a.W - 1) * C - lo;
+                            if (!(smem_guard(ft + o0, 4 * C) && smem_guard(ft + o1, 4 * C) &&
+                                  smem_guard(fb + o0, 4 * C) && smem_guard(fb + o1, 4 * C))) {
+#pragma unroll
+                                for (int c = 0; c < C; c++)
+                                    r[k][c] = 0.0f;
+                                continue;
+                            }
                             const float u = __int_as_float(xw[k].y);
 #pragma unroll
                             for (int c = 0; c < C; c++) {
@@ -458,6 +473,8 @@ __device__ void compute_generic(const KArgs &a, const StageView &sv, const TileG
                     }
                 }
                 float *o = reinterpret_cast<float *>(orow) + p0 * C;
+                if (!smem_guard(o, 4 * npx * C))
+                    continue;
                 if (npx == RUN) {
                     // RUN * C floats from a 16-byte aligned start: C float4 stores
                     float4 *o4 = reinterpret_cast<float4 *>(o);
@@ -498,6 +515,9 @@ __device__ void compute_down2(const KArgs &a, const StageView &sv, const TileGeo
         const uint8_t *bot = sv.slots + sv.map[2 * rl + 1] * sv.slot_bytes + ofs0;
         uint8_t *orow = ob + rl * orow_bytes;
         for (int j = threadIdx.x & (tpr - 1); j < ngrp; j += tpr) {
+            if (!(smem_guard(top + 4 * SW * j, 4 * SW) && smem_guard(bot + 4 * SW * j, 4 * SW) &&
+                  smem_guard(orow + 2 * SW * j, 2 * SW)))
+                continue;
             uint32_t tw[SW], bw[SW], o[SW / 2];
             if constexpr (C == 3) {
                 const uint2 *tp = reinterpret_cast<const uint2 *>(top + 24 * j);
@@ -527,6 +547,8 @@ __device__ void compute_down2(const KArgs &a, const StageView &sv, const TileGeo
 #pragma unroll
             for (int c = 0; c < C; c++) {
                 const int o = 2 * p * C + c;
+                if (!(smem_guard(top + o, C + 1) && smem_guard(bot + o, C + 1) && smem_guard(orow + p * C + c, 1)))
+                    continue;
                 const int s = top[o] + top[o + C] + bot[o] + bot[o + C] + 2;
                 orow[p * C + c] = static_cast<uint8_t>(s >> 2);
             }
@@ -548,7 +570,7 @@ __device__ void compute_normalize(const KArgs &a, const StageView &sv, const Til
     const int lg = min(8, ceil_log2((nc + U - 1) / U));
     const int tpr = 1 << lg, rpp = kConsumers >> lg;
     for (int rl = threadIdx.x >> lg; rl < nr; rl += rpp) {
-        const int2 yw = sv.ty[rl];
+        const int2 yw = smem_guard(sv.ty + rl, 8) ? sv.ty[rl] : make_int2(0, 0);
         const int B1 = yw.y, B0 = 2048 - B1;
         const uint8_t *top = sv.slots + sv.map[2 * rl] * sv.slot_bytes;
         const uint8_t *bot = sv.slots + sv.map[2 * rl + 1] * sv.slot_bytes;
@@ -557,7 +579,7 @@ __device__ void compute_normalize(const KArgs &a, const StageView &sv, const Til
 #pragma unroll
             for (int k = 0; k < U; k++) {
                 const int cl = c0 + k * tpr;
-                xw[k] = cl < nc ? sv.tx[cl] : make_int2(0, 0);
+                xw[k] = cl < nc && smem_guard(sv.tx + cl, 8) ? sv.tx[cl] : make_int2(0, 0);
             }
 #pragma unroll
             for (int k = 0; k < U; k++) {
@@ -569,7 +591,8 @@ __device__ void compute_normalize(const KArgs &a, const StageView &sv, const Til
                 bilinear_u8_px<C>(top, bot, xw[k].x * C - sv.b_lo, aw, B0, B1, q);
 #pragma unroll
                 for (int c = 0; c < C; c++)
-                    ob[c * plane_el + rl * orow_el + cl] = fmaf(static_cast<float>(q[c]), a.scale[c], a.shift[c]);
+                    if (smem_guard(ob + c * plane_el + rl * orow_el + cl, 4))
+                        ob[c * plane_el + rl * orow_el + cl] = fmaf(static_cast<float>(q[c]), a.scale[c], a.shift[c]);
             }
         }
     }
@@ -603,6 +626,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_resize(const KArgs a, const __g
     __syncthreads();
     // the next launch in the stream may begin its set-up now
     grid_launch_dependents();
+    bounds_begin(a);
 
     if (threadIdx.x >= kConsumers) {
         // ---------------- producer warp

@@ -210,6 +210,10 @@ extern "C" int resize_u8_noalloc(const uint8_t *src, size_t src_pitch, uint8_t *
     a.xt = sc->xt;
     a.yt = sc->yt;
     a.status = &sc->status;
+    a.src_extent = static_cast<long long>(src_bytes);
+    a.dst_extent = static_cast<long long>(dst_bytes);
+    a.tab = reinterpret_cast<const uint8_t *>(sc);
+    a.tab_bytes = static_cast<long long>(sizeof(NoAllocScratch));
     const long long ntiles = static_cast<long long>(a.tiles_x) * a.tiles_y;
     const int grid = static_cast<int>(std::min<long long>(ntiles, static_cast<long long>(per_sm) * sms));
 

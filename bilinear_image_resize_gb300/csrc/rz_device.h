@@ -14,6 +14,179 @@
 namespace rz {
 namespace dev {
 
+// ------------------------------------------------------------------ bounds-checked build
+//
+// Built with -DRZ_CHECK_BOUNDS (a separate library, for tests), every global
+// load and store of the resize kernels goes through the wrappers below, which
+// check the address against the extents the kernel recorded at entry
+// (bounds_begin: source, output, table block) and every shared-memory copy
+// and read window against the CTA's dynamic shared memory.  An access outside
+// them is not made: the thread records RZ_ERR_ARG in the status word (the
+// first error recorded stays) and goes on with a zero value, and a refused
+// bulk copy still completes its barrier's transaction count, so no wait is
+// left hanging.  In the normal build the wrappers are the plain accesses.
+struct BoundsRec {
+    const uint8_t *src, *dst, *tab;
+    long long src_n, dst_n, tab_n;
+    int *status;
+};
+
+#ifdef RZ_CHECK_BOUNDS
+static __shared__ BoundsRec g_bounds;
+
+// Record the kernel's extents (every thread writes the same values).
+__device__ __forceinline__ void bounds_begin(const KArgs &a)
+{
+    g_bounds.src = a.src;
+    g_bounds.dst = a.dst;
+    g_bounds.tab = a.tab;
+    g_bounds.src_n = a.src_extent;
+    g_bounds.dst_n = a.dst_extent;
+    g_bounds.tab_n = a.tab_bytes;
+    g_bounds.status = a.status;
+}
+
+static __device__ __noinline__ void bounds_fault()
+{
+    if (g_bounds.status)
+        atomicCAS(g_bounds.status, RZ_OK, RZ_ERR_ARG);
+}
+
+__device__ __forceinline__ bool in_span(const void *p, long long n, const uint8_t *base, long long extent)
+{
+    const uint8_t *c = static_cast<const uint8_t *>(p);
+    return base != nullptr && n >= 0 && c >= base && c + n <= base + extent;
+}
+
+__device__ __forceinline__ bool read_ok(const void *p, long long n)
+{
+    return in_span(p, n, g_bounds.src, g_bounds.src_n) || in_span(p, n, g_bounds.tab, g_bounds.tab_n);
+}
+
+__device__ __forceinline__ bool write_ok(const void *p, long long n) { return in_span(p, n, g_bounds.dst, g_bounds.dst_n); }
+
+extern __shared__ __align__(16) uint8_t rz_dynamic_smem[];
+
+__device__ __forceinline__ bool smem_ok(const void *p, long long n)
+{
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    return in_span(p, n, rz_dynamic_smem, dyn);
+}
+
+// Check a shared-memory window [p, p + n) a thread is about to read or write.
+#define RZ_SMEM_CHECK(p, n)                                                   \
+    do {                                                                      \
+        if (!::rz::dev::smem_ok((p), (n))) ::rz::dev::bounds_fault();        \
+    } while (0)
+#else
+__device__ __forceinline__ void bounds_begin(const KArgs &) {}
+#define RZ_SMEM_CHECK(p, n) \
+    do {                    \
+    } while (0)
+#endif
+
+// True when [p, p + n) may be read: the CTA's dynamic shared memory for a
+// shared address, the source or the tables otherwise (always in the normal
+// build); a false result is recorded in the checked build.
+__device__ __forceinline__ bool read_guard(const void *p, long long n)
+{
+#ifdef RZ_CHECK_BOUNDS
+    if (!(__isShared(p) ? smem_ok(p, n) : read_ok(p, n))) {
+        bounds_fault();
+        return false;
+    }
+#else
+    (void)p;
+    (void)n;
+#endif
+    return true;
+}
+
+// True when [p, p + n) lies in the CTA's dynamic shared memory (always in the
+// normal build); in the checked build a false result is recorded.  Callers
+// make the access only when it returns true.
+__device__ __forceinline__ bool smem_guard(const void *p, long long n)
+{
+#ifdef RZ_CHECK_BOUNDS
+    if (!smem_ok(p, n)) {
+        bounds_fault();
+        return false;
+    }
+#else
+    (void)p;
+    (void)n;
+#endif
+    return true;
+}
+
+// A float from shared memory (0 and recorded when outside the CTA's dynamic
+// shared memory, in the checked build).
+__device__ __forceinline__ float lds_f(const float *p) { return smem_guard(p, 4) ? *p : 0.0f; }
+
+// Global loads and stores of the resize kernels (checked in the checked
+// build): ld_nc = ld.global.nc (__ldg), ld_cs / st_cs = streaming (__ldcs /
+// __stcs), ld_g / st_g = plain.
+template <class T>
+__device__ __forceinline__ T ld_nc(const T *p)
+{
+#ifdef RZ_CHECK_BOUNDS
+    if (!read_ok(p, sizeof(T))) {
+        bounds_fault();
+        return T{};
+    }
+#endif
+    return __ldg(p);
+}
+
+template <class T>
+__device__ __forceinline__ T ld_cs(const T *p)
+{
+#ifdef RZ_CHECK_BOUNDS
+    if (!read_ok(p, sizeof(T))) {
+        bounds_fault();
+        return T{};
+    }
+#endif
+    return __ldcs(p);
+}
+
+template <class T>
+__device__ __forceinline__ T ld_g(const T *p)
+{
+#ifdef RZ_CHECK_BOUNDS
+    if (!read_ok(p, sizeof(T))) {
+        bounds_fault();
+        return T{};
+    }
+#endif
+    return *p;
+}
+
+template <class T>
+__device__ __forceinline__ void st_cs(T *p, T v)
+{
+#ifdef RZ_CHECK_BOUNDS
+    if (!write_ok(p, sizeof(T))) {
+        bounds_fault();
+        return;
+    }
+#endif
+    __stcs(p, v);
+}
+
+template <class T>
+__device__ __forceinline__ void st_g(T *p, T v)
+{
+#ifdef RZ_CHECK_BOUNDS
+    if (!write_ok(p, sizeof(T))) {
+        bounds_fault();
+        return;
+    }
+#endif
+    *p = v;
+}
+
 // ------------------------------------------------------------------ PTX helpers
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -46,6 +219,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Complete `bytes` of the barrier's expected transaction count without a
+// copy (the checked build's stand-in for a refused bulk copy).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
 }
 
 // Barrier among the consumer warps only (the producer warp never joins it).
@@ -120,6 +301,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 __device__ __forceinline__ void bulk_load_hint(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar,
                                                uint64_t policy)
 {
+#ifdef RZ_CHECK_BOUNDS
+    if (!read_ok(gsrc, bytes) || !smem_ok(sdst, bytes)) {
+        bounds_fault();
+        mbar_complete_tx(bar, bytes);
+        return;
+    }
+#endif
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
         "%4;" ::"r"(smem_addr(sdst)),
@@ -132,8 +320,19 @@ __device__ __forceinline__ void bulk_load_hint(void *sdst, const void *gsrc, uin
 // 8-byte words and `word` is even, so the copy starts on a 16-byte boundary;
 // parts of the box outside the image are zero-filled, not read.
 __device__ __forceinline__ void tensor_load_3d(void *sdst, const CUtensorMap *map, int word, int row, int image,
-                                               uint64_t *bar, uint64_t policy)
+                                               uint64_t *bar, uint64_t policy, uint32_t box_bytes)
 {
+#ifdef RZ_CHECK_BOUNDS
+    // (the tensor map keeps the global side inside the image: parts of the
+    // box outside it are zero-filled)
+    if (!smem_ok(sdst, box_bytes)) {
+        bounds_fault();
+        mbar_complete_tx(bar, box_bytes);
+        return;
+    }
+#else
+    (void)box_bytes;
+#endif
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
         "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(sdst)),
@@ -145,6 +344,13 @@ __device__ __forceinline__ void tensor_load_3d(void *sdst, const CUtensorMap *ma
 // (for the sampling tables, which every tile row reads again).
 __device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar)
 {
+#ifdef RZ_CHECK_BOUNDS
+    if (!read_ok(gsrc, bytes) || !smem_ok(sdst, bytes)) {
+        bounds_fault();
+        mbar_complete_tx(bar, bytes);
+        return;
+    }
+#endif
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_addr(sdst)),
@@ -178,6 +384,12 @@ __device__ __forceinline__ void l2_prefetch_span(const uint8_t *p, long long byt
 {
     const uintptr_t a0 = (reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15);
     const uintptr_t a1 = (reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(bytes)) & ~static_cast<uintptr_t>(15);
+#ifdef RZ_CHECK_BOUNDS
+    if (bytes > 0 && a1 > a0 && !read_ok(reinterpret_cast<const void *>(a0), static_cast<long long>(a1 - a0))) {
+        bounds_fault();
+        return;
+    }
+#endif
     if (bytes > 0 && a1 > a0)
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a0), "r"(static_cast<uint32_t>(a1 - a0))
                      : "memory");
@@ -212,6 +424,12 @@ __device__ __forceinline__ void prefetch_items(const uint8_t *img, long long pit
 // Bulk copy shared -> global (bulk-group completion).
 __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
 {
+#ifdef RZ_CHECK_BOUNDS
+    if (!write_ok(gdst, bytes) || !smem_ok(ssrc, bytes)) {
+        bounds_fault();
+        return;
+    }
+#endif
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(ssrc)),
                  "r"(bytes)
                  : "memory");
@@ -303,6 +521,12 @@ __device__ __forceinline__ int sample_index(int n_in, int n_out, int d, int bord
 template <int C>
 __device__ __forceinline__ void hsum_u8(const uint8_t *row, int o0, uint32_t aw, int (&h)[C])
 {
+    if (!read_guard(row + (C == 4 ? o0 : (o0 & ~3)), C == 3 ? 12 : 8)) {
+#pragma unroll
+        for (int c = 0; c < C; c++)
+            h[c] = 0;
+        return;
+    }
     if constexpr (C == 4) {
         const uint32_t t0 = *reinterpret_cast<const uint32_t *>(row + o0);
         const uint32_t t1 = *reinterpret_cast<const uint32_t *>(row + o0 + 4);

@@ -13,7 +13,19 @@ namespace rz {
 
 constexpr int kConsumers = 256;         // compute threads per CTA (warps 0..7)
 constexpr int kThreads = kConsumers + 32;  // plus one producer warp that stages tiles
-constexpr int kMaxSmem = 227 * 1024;    // opt-in dynamic shared memory per CTA on sm_103a
+// Bounds-checked build (compiled with -DRZ_CHECK_BOUNDS into a separate
+// library, for tests): the kernels check their global and shared-memory
+// accesses against the extents in KArgs and record RZ_ERR_ARG in the status
+// word instead of making an access outside them.
+#ifdef RZ_CHECK_BOUNDS
+constexpr bool kCheckBounds = true;
+#else
+constexpr bool kCheckBounds = false;
+#endif
+
+// opt-in dynamic shared memory per CTA on sm_103a (the checked build keeps
+// 256 bytes back for its static per-CTA bounds record)
+constexpr int kMaxSmem = 227 * 1024 - (kCheckBounds ? 256 : 0);
 constexpr int kMaxStages = 4;           // staged-tile ring depth limit
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded mbarrier waits: 1 s
 
@@ -151,6 +163,11 @@ struct KArgs {
     float w[49];               // K x K epilogue weights (K <= 7), row-major
     int ksize;                 // K of the filter epilogue (3 for the 3x3 kind)
     int l2_prefetch;           // exact-ratio direct kernels: prefetch the CTA's source span into L2 before the dependency wait
+    // extents for the bounds-checked build: bytes readable from src, bytes
+    // writable from dst, the table block [tab, tab + tab_bytes)
+    long long src_extent, dst_extent;
+    const uint8_t *tab;
+    long long tab_bytes;
 };
 
 // Record a cudaError_t for resize_last_cuda_error (this host thread).

@@ -172,7 +172,8 @@ __device__ void stream_producer(const KArgs &a, const CUtensorMap *tmap, const R
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&rg.full[slot], static_cast<uint32_t>(NB * G * BW));
                     for (int k = 0; k < NB; k++)
-                        tensor_load_3d(cb + k * BB, tmap, (b_lo + k * BW) / 8, first, g.b, &rg.full[slot], policy);
+                        tensor_load_3d(cb + k * BB, tmap, (b_lo + k * BW) / 8, first, g.b, &rg.full[slot], policy,
+                                       static_cast<uint32_t>(G * BW));
                 }
             } else if (a.tma_in) {
                 if (lane == 0)
@@ -193,7 +194,8 @@ __device__ void stream_producer(const KArgs &a, const CUtensorMap *tmap, const R
                         img + (long long)window[(p0 + i) & (kStreamListWindow - 1)] * a.src_pitch + b_lo;
                     for (int o = lane; o < nbytes; o += 32) {
                         const int k = o / BW;
-                        cb[k * BB + i * BW + (o - k * BW)] = __ldg(src + o);
+                        if (smem_guard(cb + k * BB + i * BW + (o - k * BW), 1))
+                            cb[k * BB + i * BW + (o - k * BW)] = ld_nc(src + o);
                     }
                 }
                 mbar_arrive(&rg.full[slot]);   // 32 arrivals: each lane releases its own copies
@@ -407,8 +409,8 @@ __device__ __forceinline__ bool consume_filter(const KArgs &a, const UnitGeom &g
             float m[NCOL];
 #pragma unroll
             for (int i = 0; i < NCOL; i++) {
-                const float t0 = top[off0[i][c]], t1 = top[off1[i][c]];
-                const float b0 = bot[off0[i][c]], b1 = bot[off1[i][c]];
+                const float t0 = lds_f(top + off0[i][c]), t1 = lds_f(top + off1[i][c]);
+                const float b0 = lds_f(bot + off0[i][c]), b1 = lds_f(bot + off1[i][c]);
                 const float hT = fmaf(uw[i], t1 - t0, t0);
                 const float hB = fmaf(uw[i], b1 - b0, b0);
                 m[i] = fmaf(v, hB - hT, hT);
@@ -450,7 +452,7 @@ __device__ __forceinline__ bool consume_filter(const KArgs &a, const UnitGeom &g
                     row_sum[fr] = sacc;
                 }
                 if (store && emit[i])
-                    __stcs(reinterpret_cast<float *>(op) + (rel0 + 32 * i) * C + c, row_sum[2 * R]);
+                    st_cs(reinterpret_cast<float *>(op) + (rel0 + 32 * i) * C + c, row_sum[2 * R]);
 #pragma unroll
                 for (int j = 0; j < 2 * R; j++)
                     acc[j][i][c] = row_sum[j];
@@ -534,15 +536,15 @@ __device__ __forceinline__ bool consume_u8(const KArgs &a, const UnitGeom &g, co
         if (words) {
             uint32_t *o = reinterpret_cast<uint32_t *>(op);
             if constexpr (C == 1) {
-                o[0] = pack4(q[0][0], q[1][0], q[2][0], q[3][0]);
+                st_g(o, pack4(q[0][0], q[1][0], q[2][0], q[3][0]));
             } else if constexpr (C == 3) {
-                o[0] = pack4(q[0][0], q[0][1], q[0][2], q[1][0]);
-                o[1] = pack4(q[1][1], q[1][2], q[2][0], q[2][1]);
-                o[2] = pack4(q[2][2], q[3][0], q[3][1], q[3][2]);
+                st_g(o, pack4(q[0][0], q[0][1], q[0][2], q[1][0]));
+                st_g(o + 1, pack4(q[1][1], q[1][2], q[2][0], q[2][1]));
+                st_g(o + 2, pack4(q[2][2], q[3][0], q[3][1], q[3][2]));
             } else {
 #pragma unroll
                 for (int k = 0; k < RUN; k++)
-                    o[k] = pack4(q[k][0], q[k][1], q[k][2], q[k][3]);
+                    st_g(o + k, pack4(q[k][0], q[k][1], q[k][2], q[k][3]));
             }
         } else {
 #pragma unroll
@@ -550,7 +552,7 @@ __device__ __forceinline__ bool consume_u8(const KArgs &a, const UnitGeom &g, co
                 if (k < npx)
 #pragma unroll
                     for (int c = 0; c < C; c++)
-                        op[k * C + c] = static_cast<uint8_t>(q[k][c]);
+                        st_g(op + k * C + c, static_cast<uint8_t>(q[k][c]));
         }
         op += a.dst_pitch;
     });
@@ -599,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, stream_min_ctas(OP, C, R))
     }
     __syncthreads();
     grid_launch_dependents();
+    bounds_begin(a);
     // every thread reads global memory below: wait for the grids this launch
     // depends on
     grid_dependency_wait();
