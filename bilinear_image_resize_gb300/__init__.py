@@ -18,7 +18,7 @@ from ._native import (KIND_F32, KIND_FILTER3X3, KIND_NORMALIZE, KIND_U8, RZ_BORD
                       RZ_BORDER_WRAP, RZ_EPI_FILTER, RZ_EPI_FILTER3X3, RZ_EPI_GRAY_BGR, RZ_EPI_GRAY_RGB, RZ_EPI_NORMALIZE_NCHW, RZ_ERR_ARG, RZ_ERR_CUDA, RZ_ERR_NOMEM, RZ_ERR_TIMEOUT,
                       RZ_ERR_UNSUPPORTED, RZ_F32, RZ_LINEAR, RZ_MAX_DIM, RZ_NEAREST, RZ_NOALLOC_MAX_DIM, RZ_OK,
                       RZ_OPT_CTAS_PER_SM, RZ_OPT_GENERIC_ONLY, RZ_OPT_GRID_MODE, RZ_OPT_PDL, RZ_OPT_RING_ROWS,
-                      RZ_MULTI_MAX_JOBS, RZ_OPT_F32_KERNEL, RZ_OPT_FILTER_KERNEL, RZ_OPT_L2_PREFETCH, RZ_COPY_PDL, RZ_COPY_L2_PREFETCH, RZ_OPT_STAGES, RZ_OPT_U8_KERNEL, RZ_U8,
+                      RZ_MULTI_MAX_JOBS, RZ_OPT_F32_KERNEL, RZ_OPT_FILTER_KERNEL, RZ_OPT_L2_PREFETCH, RZ_COPY_PDL, RZ_COPY_L2_PREFETCH, RZ_FILTER_AUTO, RZ_FILTER_FP32, RZ_FILTER_TENSOR, RZ_OPT_STAGES, RZ_OPT_U8_KERNEL, RZ_U8,
                       RzEpilogue, RzJob)
 
 __all__ = [
@@ -37,6 +37,7 @@ __all__ = [
     "RZ_OPT_STAGES", "RZ_OPT_GENERIC_ONLY", "RZ_OPT_CTAS_PER_SM", "RZ_OPT_GRID_MODE", "RZ_OPT_PDL",
     "RZ_OPT_RING_ROWS", "RZ_OPT_U8_KERNEL", "RZ_OPT_L2_PREFETCH",
     "resize_copy_baseline", "RZ_COPY_PDL", "RZ_COPY_L2_PREFETCH",
+    "RZ_FILTER_AUTO", "RZ_FILTER_FP32", "RZ_FILTER_TENSOR",
 ]
 
 
@@ -298,11 +299,13 @@ def resize_fused(plan: Plan, src, dst, epilogue: RzEpilogue, stream=None) -> Non
                                        _stream(stream)), "resize_fused")
 
 
-def filter2d_valid_f32(src, weights, dst, stream=None) -> None:
+def filter2d_valid_f32(src, weights, dst, stream=None, kernel: int = RZ_FILTER_AUTO, status=None) -> None:
     """dst[:] = the K x K correlation of src over its valid region.
 
     src: float32 CUDA tensor (H, W) with contiguous rows; weights: float32
     CUDA tensor (K, K); dst: float32 CUDA tensor (H - K + 1, W - K + 1).
+    kernel: RZ_FILTER_AUTO, RZ_FILTER_FP32 or RZ_FILTER_TENSOR; status:
+    optional int32 CUDA tensor for the tensor-core kernel's time-outs.
     """
     if src.dim() != 2 or dst.dim() != 2 or src.stride(1) != 1 or dst.stride(1) != 1:
         raise ValueError("src and dst must be 2-D with contiguous rows")
@@ -310,8 +313,9 @@ def filter2d_valid_f32(src, weights, dst, stream=None) -> None:
     if weights.dim() != 2 or weights.shape[1] != K or not weights.is_contiguous():
         raise ValueError("weights must be a contiguous K x K tensor")
     H, W = src.shape
-    _check(_native.load().filter2d_valid_f32(src.data_ptr(), src.stride(0) * 4, H, W, weights.data_ptr(), K,
-                                             dst.data_ptr(), dst.stride(0) * 4, _stream(stream)),
+    _check(_native.load().filter2d_valid_f32_ex(src.data_ptr(), src.stride(0) * 4, H, W, weights.data_ptr(), K,
+                                                dst.data_ptr(), dst.stride(0) * 4, kernel,
+                                                status.data_ptr() if status is not None else None, _stream(stream)),
            "filter2d_valid_f32")
 
 

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build_obj")
-SOURCES = ["kernels.cu", "stream.cu", "direct.cu", "filter.cu", "texture.cu", "multi.cu", "api.cu", "noalloc.cu", "baseline_copy.cu"]
+SOURCES = ["kernels.cu", "stream.cu", "direct.cu", "filter.cu", "texture.cu", "multi.cu", "api.cu", "noalloc.cu", "baseline_copy.cu", "filter_tc.cu"]
 HEADERS = [os.path.join(CSRC, "rz_internal.h"), os.path.join(CSRC, "rz_device.h"), os.path.join(INCLUDE, "gbresize.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

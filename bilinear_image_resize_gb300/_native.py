@@ -42,6 +42,10 @@ RZ_OPT_FILTER_KERNEL = 8
 RZ_OPT_F32_KERNEL = 9
 RZ_OPT_L2_PREFETCH = 10
 
+RZ_FILTER_AUTO = 0
+RZ_FILTER_FP32 = 1
+RZ_FILTER_TENSOR = 2
+
 RZ_COPY_PDL = 1
 RZ_COPY_L2_PREFETCH = 2
 
@@ -102,6 +106,7 @@ SIGNATURES = {
     "resize_fused": (_i, [_p, _p, _i, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, ctypes.POINTER(RzEpilogue), _p]),
     "resize_u8_host": (_i, [_p, _p, _sz, _p, _sz, _p, _sz, _p, _sz, _i, _i, _i, _i, _i, _i, _p]),
     "filter2d_valid_f32": (_i, [_p, _sz, _i, _i, _p, _i, _p, _sz, _p]),
+    "filter2d_valid_f32_ex": (_i, [_p, _sz, _i, _i, _p, _i, _p, _sz, _i, _p, _p]),
     "resize_u8_multi": (_i, [_p, _i, _i, _i, _p, _p]),
     "resize_texture_create": (_i, [ctypes.POINTER(_p), _p, _sz, _i, _i, _i]),
     "resize_texture_u8": (_i, [_p, _p, _sz, _i, _i, _p]),

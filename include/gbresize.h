@@ -324,6 +324,26 @@ RZ_API int filter2d_valid_f32(const float *src, size_t src_pitch, int H, int W, 
                               float *dst, size_t dst_pitch, void *stream);
 
 /*
+ * filter2d_valid_f32 with the kernel chosen by the caller (for tests and
+ * measurements; filter2d_valid_f32 is kernel = RZ_FILTER_AUTO, dev_status =
+ * NULL).  RZ_FILTER_FP32: the FP32 FMA kernel (any layout of the arguments
+ * above).  RZ_FILTER_TENSOR: the tensor-core kernel (tcgen05 MMAs on TF32
+ * operands, each float split into a TF32 high part and the remainder, three
+ * products per tap pair summed in float32: the float32 result within the
+ * bound stated above); it needs src 16-byte aligned and src_pitch a multiple
+ * of 16, and 16 <= K (RZ_ERR_UNSUPPORTED otherwise).  RZ_FILTER_AUTO: the tensor cores
+ * for K >= 48 where their layout conditions hold, FP32 otherwise.
+ * dev_status: optional caller-owned device int; the tensor-core kernel's
+ * bounded waits (1 s) write RZ_ERR_TIMEOUT there when one gives up (the
+ * word is not cleared by the call).  Unknown kernel values: RZ_ERR_ARG.
+ */
+#define RZ_FILTER_AUTO 0
+#define RZ_FILTER_FP32 1
+#define RZ_FILTER_TENSOR 2
+RZ_API int filter2d_valid_f32_ex(const float *src, size_t src_pitch, int H, int W, const float *weights, int K,
+                                 float *dst, size_t dst_pitch, int kernel, int *dev_status, void *stream);
+
+/*
  * End-to-end uint8 resize from HOST memory: copies the image from
  * host_src (pitch host_src_pitch) into the caller's device buffer dev_src
  * (pitch dev_src_pitch), resizes it into dev_dst (pitch dev_dst_pitch) and
