@@ -104,6 +104,19 @@ def fp32_fma_peak_tflops(sm_mhz=2070.0, sms=152):
     return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
+FILTER_TC_MIN_K = 48           # the library's automatic choice: tensor cores from this width
+TF32_OVER_BF16 = 1.1 / 2.25    # nominal dense TF32 / BF16 tensor rates
+
+
+def filter_tc_flops(K, OH, OW):
+    """FLOPs the tensor-core correlation executes per launch: 128 x 32 output
+    tiles, per filter row 3 MMAs (hi*hi, hi*lo, lo*hi) per 8-wide K step over
+    K_T = 32 ceil((32 + K - 1) / 32) Toeplitz columns, 2 x 128 x 32 x 8 each."""
+    tiles = ((OW + 31) // 32) * ((OH + 127) // 128)
+    chunks = (32 + K - 1 + 31) // 32
+    return tiles * K * 3 * (4 * chunks) * 2 * 128 * 32 * 8
+
+
 def trimmed_mean(xs, frac=0.1):
     """Mean after sorting and dropping `frac` of the samples at each end (the
     Volcanic page's *Measure performance carefully*: discard outliers, then
@@ -593,8 +606,12 @@ def valid_arm(args, local_rank):
     launch_s = ms / 1e3 / n
     tflops = 2.0 * K * K * OH * OW / launch_s / 1e12
     peak = fp32_fma_peak_tflops(clocks["sm_max_mhz"] or 2070.0)
+    tensor = K >= FILTER_TC_MIN_K
+    peaks, src = measured_peaks()
     return {"steps": n, "ms": ms, "launch_ms": launch_s * 1e3, "tflops": tflops, "peak": peak, "clocks": clocks,
-            "value": OH * OW / launch_s / 1e9, "desc": desc, "K": K, "ring": ring, "graph_steps": G}
+            "value": OH * OW / launch_s / 1e9, "desc": desc, "K": K, "ring": ring, "graph_steps": G,
+            "tensor": tensor, "tc_tflops": filter_tc_flops(K, OH, OW) / launch_s / 1e12 if tensor else None,
+            "tf32_peak": float(peaks.get("bf16_tflops", 1900.0)) * TF32_OVER_BF16, "peak_src": src}
 
 
 def multi_arm(args, local_rank):
@@ -1219,10 +1236,20 @@ def main():
                 "config": {"workload": r["desc"], "l2": f"ring of {r['ring']} input/output sets > 3x L2",
                            "launch": f"CUDA graphs of {r['graph_steps']} filter2d_valid_f32 launches, one stream",
                            "flops_per_step": 2 * r["K"] ** 2 * WORKLOADS[args.workload][4] ** 2},
-                "roofline": {"bound": "alu", "achieved": r["tflops"], "peak": r["peak"], "unit": "TFLOP/s",
-                             "frac": r["tflops"] / r["peak"],
-                             "peak_source": "derived: 152 SMs x 128 FP32 FMA lanes x 2 FLOP x max SM clock",
-                             "traffic": profile_traffic(args.workload)},
+                "roofline": ({"bound": "tensor", "achieved": r["tc_tflops"], "peak": r["tf32_peak"],
+                              "unit": "TFLOP/s", "frac": r["tc_tflops"] / r["tf32_peak"],
+                              "peak_source": f"{r['peak_src']} bf16 (MEASURED_PEAKS.json bf16_tflops) x nominal "
+                                             "TF32/BF16 ratio 1.1/2.25",
+                              "flops": "executed by the tensor-core kernel (3 TF32 products per tap pair over "
+                                       "Toeplitz tiles)",
+                              "traffic": profile_traffic(args.workload)} if r["tensor"] else
+                             {"bound": "alu", "achieved": r["tflops"], "peak": r["peak"], "unit": "TFLOP/s",
+                              "frac": r["tflops"] / r["peak"],
+                              "peak_source": "derived: 152 SMs x 128 FP32 FMA lanes x 2 FLOP x max SM clock",
+                              "traffic": profile_traffic(args.workload)}),
+                "useful": {"tflops": r["tflops"], "fp32_fma_peak": r["peak"], "frac_of_fp32_fma_peak":
+                           r["tflops"] / r["peak"], "flops": "2 K^2 per output",
+                           "kernel": "tensor cores (k_filter_tc)" if r["tensor"] else "FP32 FMA (k_filter_valid)"},
                 "cpu_baseline": cpu,
                 "e2e": None, "gpu_launches": r["steps"], "clocks": r["clocks"],
             }

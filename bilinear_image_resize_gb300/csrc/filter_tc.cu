@@ -22,10 +22,12 @@
 //
 // One CTA per output tile (512 threads; the staged tile, its lo part, two
 // Toeplitz buffers and the filter take 214 KB of shared memory): thread 0
-// loads the input tile by TMA; all threads split it, then for each filter
-// row build T_r (hi and lo) in one of two buffers while the MMAs of the
-// previous row run; thread 0 issues the row's 3 * 4 ch MMAs (M = 128, N = 32,
-// K = 8) and commits them to that buffer's mbarrier.  The 128 x 32 float32
+// loads the input tile by TMA and all threads split it; then warps 0..14
+// build T_r (hi and lo) for each filter row into one of two buffers and
+// signal it on the buffer's `full` mbarrier, while one lane of warp 15
+// issues each row's 3 * 4 ch MMAs (M = 128, N = 32, K = 8) as soon as its
+// tile is ready and commits them to the buffer's `empty` mbarrier, which
+// hands the buffer back to the builders (no CTA-wide barrier in the loop).  The 128 x 32 float32
 // accumulator lives in tensor memory (32 columns) and leaves through
 // tcgen05.ld (warp w reads lanes 32w .. 32w + 31).  Every wait is bounded
 // (1 s; RZ_ERR_TIMEOUT in the optional status word) and tensor memory is
@@ -58,6 +60,7 @@ constexpr int kTcMaxK = 64;
 constexpr int kTcMinK = 16;                   // below, the FP32 bound of a K x K sum is tighter than three TF32 products hold
 constexpr int kTcSmem = kOffW + kTcMaxK * kTcMaxK * 4 + 1024;   // + slack for 1024-byte alignment
 constexpr int kTcThreads = 512;
+constexpr int kTcBuilders = kTcThreads - 32;    // warps 0..14 build Toeplitz tiles; warp 15 lane 0 issues MMAs
 constexpr unsigned long long kTcWaitNs = 1000000000ull;
 
 struct TcArgs {
@@ -126,6 +129,19 @@ __device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uin
                  : "memory");
 }
 
+// True on every builder thread when v holds on all of them (a barrier among
+// the builders with an AND reduction).
+__device__ __forceinline__ bool builders_all(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, %2, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"(static_cast<uint32_t>(v)), "n"(kTcBuilders)
+                 : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
 
 __global__ void __launch_bounds__(kTcThreads, 1) k_filter_tc(const TcArgs p, const __grid_constant__ CUtensorMap map)
@@ -134,9 +150,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_filter_tc(const TcArgs p, con
     const uint32_t raw = sa(smem_raw);
     const uint32_t sb = (raw + 1023u) & ~1023u;     // 1024-byte aligned base (128-byte swizzle atoms)
     uint8_t *base = smem_raw + (sb - raw);
-    const uint32_t bar_tma = sb + kOffBar, bar_mma = sb + kOffBar + 8;   // bar_mma + 8 b: buffer b
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + kOffBar + 32);
-    int *n_commit = reinterpret_cast<int *>(base + kOffBar + 40);
+    // barriers: the input tile; buffer b built (full + 8 b); buffer b's MMAs done (empty + 8 b)
+    const uint32_t bar_tma = sb + kOffBar, bar_full = sb + kOffBar + 8, bar_empty = sb + kOffBar + 24;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + kOffBar + 40);
+    int *n_commit = reinterpret_cast<int *>(base + kOffBar + 44);
     float *wsm = reinterpret_cast<float *>(base + kOffW);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int x0 = (blockIdx.x % p.tiles_x) * kTcCols, y0 = (blockIdx.x / p.tiles_x) * kTcRows;
@@ -145,8 +162,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_filter_tc(const TcArgs p, con
 
     if (threadIdx.x == 0) {
         bar_init(bar_tma, 1);
-        bar_init(bar_mma, 1);
-        bar_init(bar_mma + 8, 1);
+        bar_init(bar_full, 1);
+        bar_init(bar_full + 8, 1);
+        bar_init(bar_empty, 1);
+        bar_init(bar_empty + 8, 1);
         *n_commit = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -156,18 +175,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_filter_tc(const TcArgs p, con
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // this thread's 16-byte units of every Toeplitz tile (the same for every
-    // filter row): unit (row n, chunk c, unit q) sits at c * kTcChunkB + n *
-    // 128 + (q ^ (n & 7)) * 16 (the 128-byte swizzle) and holds filter
-    // columns d = 32 c + 4 q - n + e, e < 4
-    constexpr int kUnits = (kTcCols * kTcMaxChunks * 8 + kTcThreads - 1) / kTcThreads;
+    // this builder thread's 16-byte units of every Toeplitz tile (the same
+    // for every filter row): unit (row n, chunk c, unit q) sits at c *
+    // kTcChunkB + n * 128 + (q ^ (n & 7)) * 16 (the 128-byte swizzle) and
+    // holds filter columns d = 32 c + 4 q - n + e, e < 4
+    constexpr int kUnits = (kTcCols * kTcMaxChunks * 8 + kTcBuilders - 1) / kTcBuilders;
     int uoff[kUnits], ud[kUnits];
     const int units = kTcCols * CH * 8;
 #pragma unroll
     for (int k = 0; k < kUnits; k++) {
-        const int u = threadIdx.x + k * kTcThreads;
+        const int u = threadIdx.x + k * kTcBuilders;
         const int n = u / (CH * 8), rem = u - n * CH * 8, c = rem >> 3, q = rem & 7;
-        uoff[k] = u < units ? c * kTcChunkB + n * 128 + ((q ^ (n & 7)) << 4) : -1;
+        uoff[k] = (threadIdx.x < kTcBuilders && u < units) ? c * kTcChunkB + n * 128 + ((q ^ (n & 7)) << 4) : -1;
         ud[k] = c * 32 + q * 4 - n;
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -203,45 +222,62 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_filter_tc(const TcArgs p, con
         }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
-    __syncthreads();
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;   // one decision for the whole CTA
 
-    for (int r = 0; r < K; r++) {
-        const int buf = r & 1;
-        if (r >= 2 && ok)
-            ok = bar_wait(bar_mma + 8 * buf, ((r >> 1) - 1) & 1, p.status);   // buffer free again
-        uint8_t *bh = base + kOffB + buf * kBufB, *bl = bh + kTcMaxChunks * kTcChunkB;
-        const float *wr = wsm + r * K;
+    if (threadIdx.x < kTcBuilders) {
+        // builders: Toeplitz tile of filter row r into buffer r & 1 once the
+        // MMAs of row r - 2 have released it; one arrival per tile
+        for (int r = 0; r < K && ok; r++) {
+            const int buf = r & 1;
+            const bool freed = r < 2 || bar_wait(bar_empty + 8 * buf, ((r >> 1) - 1) & 1, p.status);
+            ok = builders_all(freed);   // the same decision in every builder: the named barriers stay matched
+            if (!ok)
+                break;
+            uint8_t *bh = base + kOffB + buf * kBufB, *bl = bh + kTcMaxChunks * kTcChunkB;
+            const float *wr = wsm + r * K;
 #pragma unroll
-        for (int k = 0; k < kUnits; k++) {
-            if (uoff[k] < 0)
-                continue;
-            float v[4];
+            for (int k = 0; k < kUnits; k++) {
+                if (uoff[k] < 0)
+                    continue;
+                float v[4];
 #pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int d = ud[k] + e;
-                v[e] = (d >= 0 && d < K) ? wr[d] : 0.0f;
+                for (int e = 0; e < 4; e++) {
+                    const int d = ud[k] + e;
+                    v[e] = (d >= 0 && d < K) ? wr[d] : 0.0f;
+                }
+                const float4 h = make_float4(tf32_hi(v[0]), tf32_hi(v[1]), tf32_hi(v[2]), tf32_hi(v[3]));
+                *reinterpret_cast<float4 *>(bh + uoff[k]) = h;
+                *reinterpret_cast<float4 *>(bl + uoff[k]) =
+                    make_float4(v[0] - h.x, v[1] - h.y, v[2] - h.z, v[3] - h.w);
             }
-            const float4 h = make_float4(tf32_hi(v[0]), tf32_hi(v[1]), tf32_hi(v[2]), tf32_hi(v[3]));
-            *reinterpret_cast<float4 *>(bh + uoff[k]) = h;
-            *reinterpret_cast<float4 *>(bl + uoff[k]) = make_float4(v[0] - h.x, v[1] - h.y, v[2] - h.z, v[3] - h.w);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("bar.sync 1, %0;" ::"n"(kTcBuilders) : "memory");
+            if (threadIdx.x == 0)
+                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_full + 8 * buf) : "memory");
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
-        if (threadIdx.x == 0 && ok) {
+    } else if (threadIdx.x == kTcBuilders) {
+        // the issuer: the row's 3 x 4 CH MMAs as soon as its tile is built;
+        // descriptors advance by adding (byte offset >> 4) to the start field
+        const uint64_t a_hi = smem_desc(sb + kOffA), a_lo = smem_desc(sb + kOffALo);
+        for (int r = 0; r < K && ok; r++) {
+            const int buf = r & 1;
+            ok = bar_wait(bar_full + 8 * buf, (r >> 1) & 1, p.status);
+            if (!ok)
+                break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t bhs = sb + kOffB + buf * kBufB, bls = bhs + kTcMaxChunks * kTcChunkB;
+            const uint64_t b_hi = smem_desc(sb + kOffB + buf * kBufB);
+            const uint64_t b_lo = b_hi + ((kTcMaxChunks * kTcChunkB) >> 4);
+#pragma unroll 4
             for (int s = 0; s < 4 * CH; s++) {
-                const int c = s >> 2;
-                const uint32_t koff = (s & 3) * 32;                        // 8 TF32 along K
-                const uint32_t aoff = c * kTcChunkA + r * 128 + koff;      // A_r: r rows down the tile
-                const uint64_t ah = smem_desc(sb + kOffA + aoff), al = smem_desc(sb + kOffALo + aoff);
-                const uint64_t bhd = smem_desc(bhs + c * kTcChunkB + koff), bld = smem_desc(bls + c * kTcChunkB + koff);
-                mma_tf32(tmem, ah, bhd, (r > 0 || s > 0) ? 1u : 0u);
-                mma_tf32(tmem, ah, bld, 1u);
-                mma_tf32(tmem, al, bhd, 1u);
+                const uint32_t koff = (s & 3) * 32;                                   // 8 TF32 along K
+                const uint64_t da = (static_cast<uint32_t>((s >> 2) * kTcChunkA) + r * 128 + koff) >> 4;
+                const uint64_t db = (static_cast<uint32_t>((s >> 2) * kTcChunkB) + koff) >> 4;
+                mma_tf32(tmem, a_hi + da, b_hi + db, (r > 0 || s > 0) ? 1u : 0u);
+                mma_tf32(tmem, a_hi + da, b_lo + db, 1u);
+                mma_tf32(tmem, a_lo + da, b_hi + db, 1u);
             }
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                             bar_mma + 8 * buf)
+                             bar_empty + 8 * buf)
                          : "memory");
             *n_commit = r + 1;
         }
@@ -249,7 +285,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_filter_tc(const TcArgs p, con
     __syncthreads();
     // the last commit completes after every MMA issued before it
     const int last = *n_commit - 1;
-    bool done = last >= 0 && bar_wait(bar_mma + 8 * (last & 1), (last >> 1) & 1, p.status);
+    bool done = last == K - 1 && bar_wait(bar_empty + 8 * (last & 1), (last >> 1) & 1, p.status);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (warp < 4) {
         uint32_t v[32];

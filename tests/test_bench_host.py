@@ -136,3 +136,33 @@ def test_clock_summary_reads_the_timed_window_and_reasons():
     assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
     assert s.summary(2.0, 3.0)["reasons"] == ["hw_slowdown"]
     assert s.summary(5.0, 6.0) == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_trimmed_mean_drops_a_tenth_at_each_end():
+    # the Volcanic page's procedure: sort, drop 10% of the samples at each
+    # end, average the rest
+    xs = [5.0, 1.0, 100.0, 2.0, 3.0, 4.0, 6.0, 7.0, 8.0, 9.0]   # 10 samples: drop one at each end
+    assert bench.trimmed_mean(xs) == sum(range(2, 10)) / 8
+    assert bench.trimmed_mean([3.0]) == 3.0
+    assert bench.trimmed_mean([1.0, 2.0]) == 1.5                  # nothing to drop
+    assert bench.trimmed_mean([1.0, 2.0, 30.0], frac=0.4) == 2.0  # keeps the middle one
+    ys = list(range(100))
+    assert bench.trimmed_mean(ys) == sum(range(10, 90)) / 80
+    with pytest.raises(ValueError):
+        bench.trimmed_mean([])
+
+
+def test_host_cpu_reports_cores_and_model():
+    h = bench.host_cpu()
+    assert h["cpu_count"] == os.cpu_count()
+    assert isinstance(h["model"], str) and h["model"]
+
+
+def test_filter_tc_flops_hand_count():
+    # K = 64 on 4096^2: 127 x 32 tiles of 128 x 32 outputs, 3 chunks of 32
+    # Toeplitz columns (32 + 63 = 95 <= 96), per filter row 3 products x 12
+    # steps of 2 x 128 x 32 x 8 FLOPs
+    assert bench.filter_tc_flops(64, 4033, 4033) == 127 * 32 * 64 * 3 * 12 * 2 * 128 * 32 * 8
+    # K = 16: 32 + 15 = 47 -> 2 chunks
+    assert bench.filter_tc_flops(16, 4081, 4081) == 128 * 32 * 16 * 3 * 8 * 2 * 128 * 32 * 8
+    assert bench.FILTER_TC_MIN_K == 48
