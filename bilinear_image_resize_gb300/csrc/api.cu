@@ -683,6 +683,8 @@ bool run_direct(rz_plan_s *p, int fam, KArgs &a, int mode, void *stream, bool do
                 }
                 nrb = static_cast<long long>(ctas) * rz::kDirectThreads / std::max(1, std::min(batch, 65535)) / gpc;
             }
+            // (the kernel forms rb H / nrb in 32 bits: nrb H < 2^32)
+            nrb = std::min<long long>(nrb, 0xFFFFFFFFLL / a.H);
             a.tiles_y = static_cast<int>(std::clamp<long long>(nrb, 1, a.H));
             return launch(rfn, gpc * a.tiles_y, true);
         }

@@ -716,31 +716,34 @@ __global__ void __launch_bounds__(kDirectThreads) k_up2_rows(const KArgs a, cons
     bounds_begin(a);
     const int gpc = (a.W + P - 1) / P;          // column groups per row block
     const int nrb = a.tiles_y;
-    auto block_row = [&](int rb) { return static_cast<int>((long long)rb * a.H / nrb); };
+    // first row of block rb: rb H / nrb (the host keeps nrb H < 2^32)
+    auto block_row = [&](int rb) {
+        return static_cast<int>(static_cast<unsigned>(rb) * static_cast<unsigned>(a.H) / static_cast<unsigned>(nrb));
+    };
     const uint8_t *img = a.src + (long long)blockIdx.y * a.src_bstride;
+    const int g0 = blockIdx.x * kDirectThreads;   // the CTA's first item (gpc * nrb < 2^31)
     if (first_wave_cta(a)) {
-        // rows r0 - 1 .. r0 + R of each row block the CTA touches, over its
-        // column span (a piece per row; clamped rows for the edges)
-        const long long g0 = (long long)blockIdx.x * kDirectThreads;
-        const long long g1 = min(g0 + kDirectThreads, (long long)gpc * nrb);
-        if (g0 < g1) {
-            const int rb0 = static_cast<int>(g0 / gpc), rb1 = static_cast<int>((g1 - 1) / gpc);
-            const int per = (a.H + nrb - 1) / nrb + 2;   // rows of the tallest block, with its two neighbours
-            const int piece = threadIdx.x;
-            const int rb = rb0 + piece / per;
-            if (rb <= rb1) {
-                const int row = min(max(block_row(rb) - 1 + piece % per, 0), a.H - 1);
-                const long long jlo = max(g0 - (long long)rb * gpc, 0LL);
-                const long long jhi = min(g1 - (long long)rb * gpc, (long long)gpc);
-                const long long b0 = max(jlo * P * C - C - L::LEAD, 0LL);
-                const long long b1 = min(jhi * P * C + C, (long long)a.W * C);
+        // rows r0 - 1 .. r1 of each row block the CTA touches (at most two:
+        // a CTA's 256 items span one boundary when gpc >= 256), over its column
+        // span: one piece per row, taken by the threads that issue them
+        const int rb0 = g0 / gpc;
+        const int per = (a.H + nrb - 1) / nrb + 2;   // rows of the tallest block, with its two neighbours
+        const int piece = threadIdx.x;
+        if (piece < 2 * per) {
+            const int g1 = min(g0 + kDirectThreads, gpc * nrb);
+            const int rb = rb0 + (piece >= per ? 1 : 0);
+            if (g0 < g1 && rb <= (g1 - 1) / gpc) {
+                const int row = min(max(block_row(rb) - 1 + (piece >= per ? piece - per : piece), 0), a.H - 1);
+                const int jlo = max(g0 - rb * gpc, 0), jhi = min(g1 - rb * gpc, gpc);
+                const long long b0 = max((long long)jlo * P * C - C - L::LEAD, 0LL);
+                const long long b1 = min((long long)jhi * P * C + C, (long long)a.W * C);
                 if (b1 > b0)
                     l2_prefetch_span(img + (long long)row * a.src_pitch + b0, b1 - b0);
             }
         }
     }
     grid_dependency_wait();
-    const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
+    const int idx = g0 + threadIdx.x;
     if (idx >= gpc * nrb)
         return;
     const int rb = idx / gpc, j = idx - rb * gpc;
@@ -753,21 +756,27 @@ __global__ void __launch_bounds__(kDirectThreads) k_up2_rows(const KArgs a, cons
         const int rr = BORDER == RZ_BORDER_CLAMP ? clampi(r, 0, a.H - 1) : border_index(r, a.H, BORDER);
         return img + (long long)rr * a.src_pitch;
     };
-    uint8_t *out = a.dst + (long long)blockIdx.y * a.dst_bstride + (long long)(2 * s0) * C;
+    // output rows 2r and 2r + 1 of the current step; the source row below
+    // (r + 1) advances by the pitch, mapped by the border rule past the end
+    uint8_t *out = a.dst + (long long)blockIdx.y * a.dst_bstride + (long long)(2 * s0) * C +
+                   (long long)(2 * r0) * a.dst_pitch;
+    const uint8_t *below = img + (long long)(r0 + 1) * a.src_pitch;
     // rows k = 0, 1, 2 of the window rotate through the three buffers
     uint32_t lo[3][6], hi[3][6];
     up2_row_lanes<C, BORDER>(row_ptr(r0 - 1), s0, a.W, inner, lo[0], hi[0]);
     up2_row_lanes<C, BORDER>(row_ptr(r0), s0, a.W, inner, lo[1], hi[1]);
     auto step = [&](const int ia, const int im, const int ib, int r) {
-        up2_row_lanes<C, BORDER>(row_ptr(r + 1), s0, a.W, inner, lo[ib], hi[ib]);
+        up2_row_lanes<C, BORDER>(r + 1 < a.H ? below : row_ptr(r + 1), s0, a.W, inner, lo[ib], hi[ib]);
+        below += a.src_pitch;
         uint32_t mlo[6], mhi[6];
 #pragma unroll
         for (int k = 0; k < 6; k++) {
             mlo[k] = 48 * lo[im][k] + 0x00200020u;
             mhi[k] = 48 * hi[im][k] + 0x00200020u;
         }
-        up2_emit_row<C>(lo[ia], hi[ia], mlo, mhi, out + (long long)(2 * r) * a.dst_pitch, np);
-        up2_emit_row<C>(lo[ib], hi[ib], mlo, mhi, out + (long long)(2 * r + 1) * a.dst_pitch, np);
+        up2_emit_row<C>(lo[ia], hi[ia], mlo, mhi, out, np);
+        up2_emit_row<C>(lo[ib], hi[ib], mlo, mhi, out + a.dst_pitch, np);
+        out += 2 * a.dst_pitch;
     };
     for (int r = r0; r < r1; r += 3) {
         step(0, 1, 2, r);
