@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_direct(const KArgs a, 
     const int gpr = full + (a.OW % PX ? 1 : 0);
     if (first_wave_cta(a))
         prefetch_items<LINEAR ? 2 : 1>(a.src + (long long)blockIdx.y * a.src_bstride, a.src_pitch,
-                                       (long long)a.W * C, gpr, a.OH, (long long)blockIdx.x * kDirectThreads,
+                                       (long long)a.W * C, gpr, a.OH, static_cast<int>(blockIdx.x) * kDirectThreads,
                                        kDirectThreads, SB, 0, 0, [](int u, int k) { return 2 * u + k; });
     grid_dependency_wait();
     const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_down32_direct(const KArgs a,
     const int gpr = full + (a.OW % PX ? 1 : 0);
     if (first_wave_cta(a))
         prefetch_items<2>(a.src + (long long)blockIdx.y * a.src_bstride, a.src_pitch, (long long)a.W * C, gpr, a.OH,
-                          (long long)blockIdx.x * kDirectThreads, kDirectThreads, 4 * NW, 0, 0,
+                          static_cast<int>(blockIdx.x) * kDirectThreads, kDirectThreads, 4 * NW, 0, 0,
                           [](int u, int k) { return 3 * (u >> 1) + (k ? 1 : 2 * (u & 1)); });
     grid_dependency_wait();
     const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(kDirectThreads, Up2Occupancy<C, BORDER>::value
         // are left to the loads); the group's words from column s0 - 1
         const int H = a.H;
         prefetch_items<3>(a.src + (long long)blockIdx.y * a.src_bstride, a.src_pitch, (long long)a.W * C, gpr, a.H,
-                          (long long)blockIdx.x * kDirectThreads, kDirectThreads, P * C, -C - LEAD, 4 * NW - P * C,
+                          static_cast<int>(blockIdx.x) * kDirectThreads, kDirectThreads, P * C, -C - LEAD, 4 * NW - P * C,
                           [H](int u, int k) { return min(max(u - 1 + k, 0), H - 1); });
     }
     grid_dependency_wait();
@@ -1145,7 +1145,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_gray(const KArgs a, co
     const int gpr = full + (a.OW % PX ? 1 : 0);
     if (first_wave_cta(a))
         prefetch_items<LINEAR ? 2 : 1>(a.src + (long long)blockIdx.y * a.src_bstride, a.src_pitch,
-                                       (long long)a.W * C, gpr, a.OH, (long long)blockIdx.x * kDirectThreads,
+                                       (long long)a.W * C, gpr, a.OH, static_cast<int>(blockIdx.x) * kDirectThreads,
                                        kDirectThreads, SB, 0, 0, [](int u, int k) { return 2 * u + k; });
     grid_dependency_wait();
     const int idx = blockIdx.x * kDirectThreads + threadIdx.x;

@@ -398,25 +398,24 @@ __device__ __forceinline__ void l2_prefetch_span(const uint8_t *p, long long byt
 // Pre-wait prefetch of the source bytes one CTA of a direct kernel will read.
 // The CTA's work items are [g0, g0 + n) of a grid laid out `per_unit` items
 // per unit (an output row, or a source row for the 2x upscale), `units`
-// units in all; item j of unit u reads bytes [j GB + lead, j GB + lead + GB
-// + extra) of the NR source rows row(u, k), k < NR (row() < 0: none).  Thread
-// t takes the piece (unit u0 + t / NR, row k = t % NR), one bulk prefetch
-// clipped to [0, row_bytes) of that row; pieces past the block's threads are
-// skipped (a hint may cover less).
+// units in all (units * per_unit < 2^31); item j of unit u reads bytes
+// [j GB + lead, j GB + lead + GB + extra) of the NR source rows row(u, k),
+// k < NR (row() < 0: none).  Thread t takes the piece (unit u0 + t / NR,
+// row k = t % NR), one bulk prefetch clipped to [0, row_bytes) of that row;
+// pieces past the block's threads are skipped (a hint may cover less).
 template <int NR, class RowFn>
 __device__ __forceinline__ void prefetch_items(const uint8_t *img, long long pitch, long long row_bytes, int per_unit,
-                                               long long units, long long g0, long long n, long long GB, long long lead,
-                                               long long extra, RowFn row)
+                                               int units, int g0, int n, int GB, int lead, int extra, RowFn row)
 {
-    long long g1 = g0 + n;
-    if (g1 > units * per_unit) g1 = units * per_unit;
+    const int g1 = min(g0 + n, units * per_unit);
     if (g0 >= g1) return;
-    const long long u = g0 / per_unit + static_cast<long long>(threadIdx.x / NR);
+    const int u = g0 / per_unit + static_cast<int>(threadIdx.x) / NR;
     if (u > (g1 - 1) / per_unit) return;
-    const int k = static_cast<int>(threadIdx.x % NR);
-    const long long jlo = max(g0 - u * per_unit, 0LL), jhi = min(g1 - u * per_unit, static_cast<long long>(per_unit));
-    const long long b0 = max(jlo * GB + lead, 0LL), b1 = min(jhi * GB + lead + extra, row_bytes);
-    const int r = row(static_cast<int>(u), k);
+    const int k = static_cast<int>(threadIdx.x) % NR;
+    const int jlo = max(g0 - u * per_unit, 0), jhi = min(g1 - u * per_unit, per_unit);
+    const long long b0 = max(static_cast<long long>(jlo) * GB + lead, 0LL);
+    const long long b1 = min(static_cast<long long>(jhi) * GB + lead + extra, row_bytes);
+    const int r = row(u, k);
     if (r < 0 || b1 <= b0) return;
     l2_prefetch_span(img + static_cast<long long>(r) * pitch + b0, b1 - b0);
 }
