@@ -29,25 +29,6 @@ namespace {
 
 using namespace dev;
 
-// The row's last pixels of an exact 2x group kernel (fewer than a group),
-// byte by byte; kept out of line so that the whole-group path compiles to a
-// short straight sequence.
-template <int C, int LINEAR>
-__device__ __noinline__ void down2_row_tail(const uint8_t *top, const uint8_t *bot, uint8_t *out, int p0, int OW)
-{
-    for (int p = p0; p < OW; p++)
-#pragma unroll
-        for (int c = 0; c < C; c++) {
-            const int o = 2 * p * C + c;
-            if (LINEAR) {
-                const int s = ld_g(top + o) + ld_g(top + o + C) + ld_g(bot + o) + ld_g(bot + o + C) + 2;
-                st_g(out + p * C + c, static_cast<uint8_t>(s >> 2));
-            } else {
-                st_g(out + p * C + c, ld_g(top + o));
-            }
-        }
-}
-
 // True for the CTAs that prefetch their source span before the dependency
 // wait: the first a.l2_prefetch CTAs in launch order (the host sets it to the
 // CTAs resident at once, 0 for none).  Only those can be resident while the
@@ -56,47 +37,6 @@ __device__ __noinline__ void down2_row_tail(const uint8_t *top, const uint8_t *b
 __device__ __forceinline__ bool first_wave_cta(const KArgs &a)
 {
     return static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x < a.l2_prefetch;
-}
-
-// One group of the exact 2x downscale: the group's source words of its two
-// rows (LINEAR = 0: the upper row only), the exact sums, one vector store.
-template <int C, int LINEAR>
-__device__ __forceinline__ void down2_one(const uint8_t *top, const uint8_t *bot, uint8_t *out, int j)
-{
-    constexpr int PX = down2_px(C), SB = 2 * PX * C, OB = PX * C;
-    uint32_t tw[SB / 4], bw[SB / 4], o[OB / 4];
-    if constexpr (C == 3) {
-        const uint2 *tp = reinterpret_cast<const uint2 *>(top + SB * j);
-        const uint2 *bp = reinterpret_cast<const uint2 *>(bot + SB * j);
-#pragma unroll
-        for (int k = 0; k < 3; k++) {
-            const uint2 t = ld_cs(tp + k);
-            tw[2 * k] = t.x; tw[2 * k + 1] = t.y;
-            if (LINEAR) {
-                const uint2 u = ld_cs(bp + k);
-                bw[2 * k] = u.x; bw[2 * k + 1] = u.y;
-            }
-        }
-    } else {
-        const uint4 t = ld_cs(reinterpret_cast<const uint4 *>(top + SB * j));
-        tw[0] = t.x; tw[1] = t.y; tw[2] = t.z; tw[3] = t.w;
-        if (LINEAR) {
-            const uint4 u = ld_cs(reinterpret_cast<const uint4 *>(bot + SB * j));
-            bw[0] = u.x; bw[1] = u.y; bw[2] = u.z; bw[3] = u.w;
-        }
-    }
-    if (LINEAR)
-        down2_group<C>(tw, bw, o);
-    else
-        down2_nearest_group<C>(tw, o);
-    if constexpr (C == 3) {
-        uint32_t *op = reinterpret_cast<uint32_t *>(out + OB * j);
-        st_cs(op, o[0]);
-        st_cs(op + 1, o[1]);
-        st_cs(op + 2, o[2]);
-    } else {
-        st_cs(reinterpret_cast<uint2 *>(out + OB * j), make_uint2(o[0], o[1]));
-    }
 }
 
 // Grid: x covers one image's output groups (kDirectThreads per CTA), y the
@@ -372,52 +312,6 @@ __device__ __forceinline__ uint32_t lane_pair(const uint32_t (&lo)[NW], const ui
     return __byte_perm(src[w], src[w1], 0x5432);   // upper lane of word w, lower lane of w + 1
 }
 
-// One 32-bit word from four bytes: byte k is byte pos[k] of reg[k], where
-// equal id[k] name the same register.  All arguments are compile-time
-// constants after unrolling, so the branches fold: a word drawn from one or
-// two registers takes one byte permute, from three two, from four three.
-__device__ __forceinline__ uint32_t gather_bytes(const uint32_t (&reg)[4], const int (&id)[4],
-                                                 const uint32_t (&pos)[4])
-{
-    int slot[4], first[4], nd = 0;
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        slot[k] = -1;
-#pragma unroll
-        for (int j = 0; j < k; j++)
-            if (slot[k] < 0 && id[j] == id[k])
-                slot[k] = slot[j];
-        if (slot[k] < 0) {
-            slot[k] = nd;
-            first[nd] = k;
-            nd++;
-        }
-    }
-    if (nd <= 2) {
-        uint32_t sel = 0;
-#pragma unroll
-        for (int k = 0; k < 4; k++)
-            sel |= (pos[k] + 4u * static_cast<uint32_t>(slot[k])) << (4 * k);
-        return __byte_perm(reg[first[0]], nd == 2 ? reg[first[1]] : 0u, sel);
-    }
-    if (nd == 3) {
-        uint32_t s1 = 0, s2 = 0;
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            if (slot[k] < 2) {
-                s1 |= (pos[k] + 4u * static_cast<uint32_t>(slot[k])) << (4 * k);
-                s2 |= static_cast<uint32_t>(k) << (4 * k);
-            } else {
-                s2 |= (4u + pos[k]) << (4 * k);
-            }
-        }
-        return __byte_perm(__byte_perm(reg[first[0]], reg[first[1]], s1), reg[first[2]], s2);
-    }
-    const uint32_t lo2 = __byte_perm(reg[0], reg[1], pos[0] | ((4u + pos[1]) << 4));
-    const uint32_t hi2 = __byte_perm(reg[2], reg[3], pos[2] | ((4u + pos[3]) << 4));
-    return __byte_perm(lo2, hi2, 0x5410);
-}
-
 // CTAs per SM that the register budget of each form is set for: the most at
 // which that form compiles without spills (six for one and three channels,
 // five for three channels under mirror, four for four channels).  The kernel
@@ -569,137 +463,9 @@ __global__ void __launch_bounds__(kDirectThreads, Up2Occupancy<C, BORDER>::value
 
 // ------------------------------------------------------------------ exact 2x upscale, pixel lanes, walking rows
 //
-// The same 9-3-3-1 sum as k_up2_direct for three and four channels, laid out
-// so that a horizontal neighbour is a whole register: each source pixel is
-// unpacked once into two lane words, lo = {c0, c2} and hi = {c1, c3} (16-bit
-// lanes; c3 = 0 for three channels), so the vertical sums
-//   V = 16 t + 48 m + 32   (t the row above or below, m the middle row)
-// and the horizontal ones
-//   even output: 3 V[x] + V[x - 1],   odd output: 3 V[x] + V[x + 1]
-// are one integer multiply-add per lane word; every lane is 16 S + 128 with S
-// the 9-3-3-1 sum (below 2^16), so its high byte is (S + 8) >> 4, the exact
-// result (CUDA interpolation page §2.2, §6.2 at weights 1536 and 512).  A
-// thread takes four source columns of `a.TR` consecutive source rows (two
-// output rows each), keeping the unpacked rows above, at and below the current
-// one in registers, so each row is loaded and unpacked once per thread.
-template <int C>
-struct Up2RowsLayout {
-    static constexpr int P = 4;                    // source columns per thread
-    static constexpr int LEAD = (4 - C % 4) % 4;   // bytes before column s0 - 1 in its word
-    static constexpr int NB = (P + 2) * C;         // bytes of columns s0 - 1 .. s0 + P
-    static constexpr int NW = (LEAD + NB + 3) / 4;
-    static constexpr int NWO = 2 * P * C / 4;      // output words per output row
-};
-
-// Lane word {byte ea, byte eb} of the row's words (eb < 0: {byte ea, 0}),
-// each byte in the low half of a 16-bit lane.
-template <int NW>
-__device__ __forceinline__ uint32_t lane_word(const uint32_t (&w)[NW], int ea, int eb)
-{
-    const int wa = ea >> 2;
-    if (eb < 0)
-        return __byte_perm(w[wa], 0u, 0x4440u | static_cast<uint32_t>(ea & 3));
-    const int wb = eb >> 2;
-    if (wa == wb)
-        return __byte_perm(w[wa], 0u, 0x4040u | static_cast<uint32_t>(ea & 3) | (static_cast<uint32_t>(eb & 3) << 8));
-    return __byte_perm(w[wa], w[wb], static_cast<uint32_t>(ea & 3) | ((4u + (eb & 3)) << 8)) & 0x00ff00ffu;
-}
-
-// Load the words of source columns s0 - 1 .. s0 + P of one row (interior: NW
-// aligned words; at the image's left or right edge, or on layouts that are
-// not 4-byte aligned: bytes, the columns mapped by the border rule) and
-// unpack the P + 2 pixels into lane words.
-template <int C, int BORDER>
-__device__ __forceinline__ void up2_row_lanes(const uint8_t *row, int s0, int W, bool inner, uint32_t (&lo)[6],
-                                              uint32_t (&hi)[6])
-{
-    using L = Up2RowsLayout<C>;
-    uint32_t wd[L::NW];
-    if (inner) {
-        const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (s0 - 1) * C - L::LEAD);
-#pragma unroll
-        for (int i = 0; i < L::NW; i++)
-            wd[i] = ld_nc(w + i);
-    } else {
-#pragma unroll
-        for (int i = 0; i < L::NW; i++)
-            wd[i] = 0;
-#pragma unroll
-        for (int i = 0; i < L::NB; i++) {
-            const int col = BORDER == RZ_BORDER_CLAMP ? clampi(s0 - 1 + i / C, 0, W - 1)
-                                                      : border_index(s0 - 1 + i / C, W, BORDER);
-            wd[(L::LEAD + i) / 4] |= static_cast<uint32_t>(ld_nc(row + col * C + i % C)) << (8 * ((L::LEAD + i) % 4));
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < 6; k++) {
-        const int e = L::LEAD + k * C;
-        lo[k] = lane_word<L::NW>(wd, e, e + 2);
-        hi[k] = lane_word<L::NW>(wd, e + 1, C == 4 ? e + 3 : -1);
-    }
-}
-
-// Output row 2r (above = row r - 1) or 2r + 1 (above = row r + 1): vertical
-// sums with the middle row's 48 m + 32 (mm), horizontal sums, the result
-// bytes gathered into words and stored.
-template <int C>
-__device__ __forceinline__ void up2_emit_row(const uint32_t (&tlo)[6], const uint32_t (&thi)[6],
-                                             const uint32_t (&mlo)[6], const uint32_t (&mhi)[6], uint8_t *op, int np)
-{
-    using L = Up2RowsLayout<C>;
-    uint32_t vlo[6], vhi[6];
-#pragma unroll
-    for (int k = 0; k < 6; k++) {
-        vlo[k] = 16 * tlo[k] + mlo[k];
-        vhi[k] = 16 * thi[k] + mhi[k];
-    }
-    // output pixel q: centre column k = q / 2 + 1, even (left neighbour) or
-    // odd (right neighbour)
-    uint32_t qlo[2 * 4], qhi[2 * 4];
-#pragma unroll
-    for (int k = 1; k <= 4; k++) {
-        qlo[2 * k - 2] = 3 * vlo[k] + vlo[k - 1];
-        qhi[2 * k - 2] = 3 * vhi[k] + vhi[k - 1];
-        qlo[2 * k - 1] = 3 * vlo[k] + vlo[k + 1];
-        qhi[2 * k - 1] = 3 * vhi[k] + vhi[k + 1];
-    }
-    uint32_t ow[L::NWO];
-#pragma unroll
-    for (int wo = 0; wo < L::NWO; wo++) {
-        uint32_t reg[4];
-        int id[4];
-        uint32_t pos[4];
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int ob = 4 * wo + k, q = ob / C, c = ob % C;
-            const bool is_hi = (c & 1) != 0;
-            reg[k] = is_hi ? qhi[q] : qlo[q];
-            id[k] = 2 * q + (is_hi ? 1 : 0);
-            pos[k] = c >= 2 ? 3u : 1u;
-        }
-        ow[wo] = gather_bytes(reg, id, pos);
-    }
-    const uintptr_t oa = reinterpret_cast<uintptr_t>(op);
-    if (np == 4 && L::NWO % 4 == 0 && (oa & 15) == 0) {
-#pragma unroll
-        for (int i = 0; i < L::NWO; i += 4)
-            st_cs(reinterpret_cast<uint4 *>(op) + i / 4, make_uint4(ow[i], ow[i + 1], ow[i + 2], ow[i + 3]));
-    } else if (np == 4 && L::NWO % 2 == 0 && (oa & 7) == 0) {
-#pragma unroll
-        for (int i = 0; i < L::NWO; i += 2)
-            st_cs(reinterpret_cast<uint2 *>(op) + i / 2, make_uint2(ow[i], ow[i + 1]));
-    } else if (np == 4 && (oa & 3) == 0) {
-#pragma unroll
-        for (int i = 0; i < L::NWO; i++)
-            st_cs(reinterpret_cast<uint32_t *>(op) + i, ow[i]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8 * C; i++)
-            if (i < 2 * np * C)
-                st_g(op + i, static_cast<uint8_t>(ow[i / 4] >> (8 * (i % 4))));
-    }
-}
-
+// (the lane-word helpers up2_row_lanes / up2_emit_row are in rz_device.h,
+// shared with the many-geometry launch)
+//
 // Grid: x covers one image's (row block, column group) items, column groups
 // fastest; y the images, one per grid row (the host splits batches past
 // 65535).  a.tiles_y = row blocks: block rb takes source rows

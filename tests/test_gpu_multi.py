@@ -4,7 +4,11 @@ Every job's output must equal the oracle's resize of its own image bit for
 bit (and so resize_u8 with a plan of that geometry), whatever the mix: up-
 and downscales, identity, one-pixel and empty outputs, padded pitches,
 unaligned starts, both modes, every channel count; invalid jobs are skipped
-and flagged while the others still run.
+and flagged while the others still run.  Exact 2x bilinear jobs take their
+own forms inside the launch (the 2 x 2 mean; the 9-3-3-1 upscale on pixel
+lanes), so their ragged groups, one-pixel images, wide rows, row runs that
+end inside a unit, and the layouts that send them back to the generic form
+are checked as well.
 """
 import numpy as np
 import pytest
@@ -67,6 +71,22 @@ def test_multi_padded_and_unaligned(rz, C):
     assert st == rz.RZ_OK
     for img, g, (H, W, OH, OW) in zip(imgs, got, MIX[:6]):
         np.testing.assert_array_equal(g, want(img, OH, OW, 1))
+
+
+# exact 2x down- and upscales: ragged last groups, one-row and one-column
+# images, rows of 256 groups and more, row counts that end inside a unit
+EXACT2X = [(26, 42, 13, 21), (2, 2, 1, 1), (2, 14, 1, 7), (18, 2, 9, 1), (64, 2080, 32, 1040), (22, 18, 11, 9),
+           (40, 34, 20, 17), (13, 21, 26, 42), (1, 1, 2, 2), (1, 7, 2, 14), (9, 1, 18, 2), (4, 4, 8, 8),
+           (30, 1100, 60, 2200), (7, 6, 14, 12), (17, 1025, 34, 2050)]
+
+
+@pytest.mark.parametrize("C", [1, 3, 4])
+@pytest.mark.parametrize("pad,off", [(0, 0), (8, 0), (3, 1), (4, 4)])
+def test_multi_exact_2x_forms(rz, C, pad, off):
+    imgs, got, st = run_jobs(rz, EXACT2X, C, 1, seed=C + pad + off, pad=pad, off=off)
+    assert st == rz.RZ_OK
+    for img, g, (H, W, OH, OW) in zip(imgs, got, EXACT2X):
+        np.testing.assert_array_equal(g, want(img, OH, OW, 1), err_msg=str((H, W, OH, OW)))
 
 
 def test_multi_many_jobs(rz):
