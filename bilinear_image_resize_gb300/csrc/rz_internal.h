@@ -115,10 +115,10 @@ enum StreamOp { STREAM_FILTER = 0, STREAM_U8 = 1 };
 constexpr int kStreamChunkRows = 8;     // rows per chunk (a power of two)
 constexpr int kStreamRingMax = 128;     // ring rows (chunks x rows per chunk)
 constexpr int kStreamListWindow = 128;  // listed rows the producer keeps (ints)
-// K x K filter: resized columns per consumer lane (two for one channel, else
+// K x K filter: resized columns per consumer lane (four for one channel, else
 // one); widest strip = eight consumer warps x (32 x lane columns - 2 K/2)
 // outputs
-__host__ __device__ constexpr int filter_lane_cols(int C) { return C == 1 ? 2 : 1; }
+__host__ __device__ constexpr int filter_lane_cols(int C) { return C == 1 ? 4 : 1; }
 __host__ __device__ constexpr int filter_strip(int C, int R = 1) { return 8 * (32 * filter_lane_cols(C) - 2 * R); }
 // uint8 bilinear: consecutive output pixels per consumer lane; widest strip
 __host__ __device__ constexpr int stream_u8_run(int C) { return C == 4 ? 2 : 4; }

@@ -422,20 +422,15 @@ __device__ __forceinline__ bool consume_filter(const KArgs &a, const UnitGeom &g
                 nb[R][i] = m[i];
 #pragma unroll
             for (int d = 1; d <= R; d++) {
-                if constexpr (NCOL == 1) {
-                    nb[R - d][0] = __shfl_up_sync(0xffffffffu, m[0], d);
-                    nb[R + d][0] = __shfl_down_sync(0xffffffffu, m[0], d);
-                } else {
-                    // e = lane and e = lane + 32: a neighbour d away lies in
-                    // the other half where the lane index wraps
-                    const float up0 = m[0];
-                    const float up1 = lane >= 32 - d ? m[0] : m[1];
-                    const float dn0 = lane < d ? m[1] : m[0];
-                    const float dn1 = m[1];
-                    nb[R - d][0] = __shfl_sync(0xffffffffu, up0, (lane + 32 - d) & 31);
-                    nb[R - d][1] = __shfl_sync(0xffffffffu, up1, (lane + 32 - d) & 31);
-                    nb[R + d][0] = __shfl_sync(0xffffffffu, dn0, (lane + d) & 31);
-                    nb[R + d][1] = __shfl_sync(0xffffffffu, dn1, (lane + d) & 31);
+                // column e - d of slot i comes from lane - d, its slot i (slot
+                // i - 1 where the lane index wraps); e + d from lane + d, slot
+                // i (i + 1 where it wraps): the sender picks
+#pragma unroll
+                for (int i = 0; i < NCOL; i++) {
+                    const float upv = (i > 0 && lane >= 32 - d) ? m[i - 1] : m[i];
+                    const float dnv = (i + 1 < NCOL && lane < d) ? m[i + 1] : m[i];
+                    nb[R - d][i] = __shfl_sync(0xffffffffu, upv, (lane + 32 - d) & 31);
+                    nb[R + d][i] = __shfl_sync(0xffffffffu, dnv, (lane + d) & 31);
                 }
             }
 #pragma unroll

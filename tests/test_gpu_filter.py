@@ -192,6 +192,27 @@ def test_fused_streaming_tiles_and_rings(rz, K):
         assert max_abs(out.cpu().numpy(), want) <= fused_tol(w), (tile, ring)
 
 
+@pytest.mark.parametrize("K", [3, 5, 7])
+def test_fused_widest_strips(rz, K):
+    # one-channel strips as wide as the kernel takes (every lane's four
+    # column slots in use, neighbours taken across the slot boundaries), and
+    # a strip width one column short of it
+    img = synth.random_f32((64, 1400, 1), seed=40 + K)
+    w = synth.filter_weights_k(K)
+    want = want_fused(img, 70, 1290, w)
+    widest = 8 * (32 * 4 - 2 * (K // 2))
+    for tile in [(16, 4096), (9, widest - 1), None]:
+        with rz.resize_plan_create(64, 1400, 70, 1290, rz.RZ_LINEAR) as plan:
+            if tile:
+                rz.resize_plan_set_tile(plan, rz.KIND_FILTER3X3, *tile)
+            src = torch.from_numpy(img).cuda()
+            out = torch.full((70, 1290, 1), -99.0, dtype=torch.float32, device="cuda")
+            rz.resize_fused(plan, src, out, rz.make_epilogue(rz.RZ_EPI_FILTER, wk=w))
+            torch.cuda.synchronize()
+            assert rz.resize_plan_status(plan) == rz.RZ_OK
+        assert max_abs(out.cpu().numpy(), want) <= fused_tol(w), tile
+
+
 def test_fused_batch(rz):
     N, H, W, OH, OW = 3, 40, 50, 77, 33
     frames = np.stack([synth.random_f32((H, W, 3), seed=n) for n in range(N)])
