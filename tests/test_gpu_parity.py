@@ -84,6 +84,23 @@ def check_f32(rz, img, OH, OW, mode, **kw):
 
 # ------------------------------------------------------------------ the five workloads, full size
 
+@pytest.mark.parametrize("C", [1, 3, 4])
+@pytest.mark.parametrize("geom", [(24, 48, 16, 32), (33, 45, 22, 30), (9, 3, 6, 2), (150, 603, 100, 402),
+                                  (3, 1563, 2, 1042)])
+def test_exact_three_halves_downscale(rz, C, geom):
+    # the exact 3:2 kernel (lane words for three and four channels): whole
+    # eight-pixel groups, ragged row ends and rows of the tail alone, every
+    # channel count; 4-byte aligned layouts take the kernel, an odd start the
+    # generic one
+    H, W, OH, OW = geom
+    img = synth.random_u8((H, W, C), seed=H + W + C)
+    sp = W * C + (-W * C) % 4
+    dp = (-OW * C) % 4
+    for kw in ({"src_pitch": sp, "dst_pad": dp}, {"src_pitch": sp + 8, "dst_pad": dp + 8},
+               {"src_off": 1, "dst_off": 3}):
+        check_u8(rz, img, OH, OW, rz.RZ_LINEAR, **kw)
+
+
 def test_tiny_gray_64x48(rz):
     img = synth.tiny_gray()
     check_u8(rz, img, 96, 128, rz.RZ_LINEAR)
