@@ -848,13 +848,14 @@ def copy_baseline(rz, step_bytes, ring, stream, dev, launches):
 
 def batched_u8(rz, plan, frames, H, W, OH, OW, C, nf, stream, dev, frame_bytes, launches=48):
     """Frames per second when `nf` frames go through one resize_u8_batch
-    launch: two distinct batches in rotation (each larger than L2 for 4K
-    frames), graph-replayed launches timed with events on the launching
-    stream, after a check that frame 0 of a batched launch equals the
-    single-frame call's output."""
+    launch: distinct batches in rotation, as many as make together more than
+    three times L2 (two at least), graph-replayed launches timed with events
+    on the launching stream after a device hold, after a check that frame 0
+    of a batched launch equals the single-frame call's output."""
     import torch
+    nsets = max(2, -(-3 * L2_BYTES // (nf * frame_bytes)))
     sets = []
-    for b in range(2):
+    for b in range(nsets):
         src = torch.stack([frames[(b * nf + i) % len(frames)] for i in range(nf)])
         sets.append((src, torch.empty((nf, OH, OW, C), dtype=torch.uint8, device=dev)))
     one = torch.empty((OH, OW, C), dtype=torch.uint8, device=dev)
@@ -865,11 +866,11 @@ def batched_u8(rz, plan, frames, H, W, OH, OW, C, nf, stream, dev, frame_bytes, 
     torch.cuda.synchronize()
     if not torch.equal(sets[0][1][0], one):
         raise RuntimeError("batched launch did not reproduce the single-frame result")
-    n = 8
+    n = max(8, nsets)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for i in range(n):
-            src, dst = sets[i % 2]
+            src, dst = sets[i % nsets]
             rz.resize_u8_batch(plan, src, dst, stream=stream)
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -878,6 +879,7 @@ def batched_u8(rz, plan, frames, H, W, OH, OW, C, nf, stream, dev, frame_bytes, 
     reps = max(1, launches // n)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        hold_stream(stream)
         e0.record(stream)
         for _ in range(reps):
             g.replay()
@@ -890,7 +892,7 @@ def batched_u8(rz, plan, frames, H, W, OH, OW, C, nf, stream, dev, frame_bytes, 
     return {"frames_per_launch": nf, "value": nf * OH * OW / (ms / 1e3) / 1e9, "unit": "Gpix/s",
             "ms_per_launch": ms, "launches": reps * n, "entry": "resize_u8_batch",
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak},
-            "l2": f"two batches of {nf} frames in rotation, {nf * frame_bytes / MB:.0f} MB each"}
+            "l2": f"{nsets} batches of {nf} frames in rotation, {nf * frame_bytes / MB:.0f} MB each"}
 
 
 def e2e_u8(rz, plan, dev_frame, H, W, OH, OW, C, dev, n):
