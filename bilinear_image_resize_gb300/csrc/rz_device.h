@@ -895,5 +895,104 @@ __device__ __forceinline__ void up2_emit_row(const uint32_t (&tlo)[6], const uin
     }
 }
 
+// ------------------------------------------------------------------ exact 3:2 downscale
+
+// One group of the exact 3:2 downscale (W = 3 OW / 2, H = 3 OH / 2): output
+// pixels 8 j .. 8 j + 7 of one row from source pixels 12 j .. 12 j + 11 of
+// its two source rows, ra weighted 3 and rb weighted 1 (each output weights
+// its two source columns 3 and 1 the same way), so the exact bilinear sum is
+// (sum of b a t + 8) >> 4 with a, b in {1, 3}.  ra, rb and o 4-byte aligned.
+template <int C>
+__device__ __forceinline__ void down32_group(const uint8_t *ra, const uint8_t *rb, uint8_t *o, int j)
+{
+    constexpr int PX = 8;          // output pixels
+    constexpr int NW = 3 * C;      // source words per row: 12 pixels
+    constexpr int NWO = 2 * C;     // output words: 8 pixels
+    if constexpr (C >= 3) {
+        // vertical sums 3 a + b in 16-bit lanes of even and odd bytes,
+        // regrouped into pixel lane words {c0, c2} and {c1, c3 or 0}; a
+        // lane word's horizontal 9-3-3-1 sum is then two multiply-adds
+        // for two channels: 48 V[x3] + 16 V[x1] + 128 = 16 S + 128 (S at
+        // most 16 * 255), whose high byte is (S + 8) >> 4
+        const uint32_t *wa = reinterpret_cast<const uint32_t *>(ra + 12 * C * j);
+        const uint32_t *wb = reinterpret_cast<const uint32_t *>(rb + 12 * C * j);
+        uint32_t ve[NW], vo[NW];
+#pragma unroll
+        for (int i = 0; i < NW; i++) {
+            const uint32_t x = ld_cs(wa + i), y = ld_nc(wb + i);
+            ve[i] = 3 * (x & 0x00ff00ffu) + (y & 0x00ff00ffu);
+            vo[i] = 3 * __byte_perm(x, 0u, 0x4341u) + __byte_perm(y, 0u, 0x4341u);
+        }
+        // {lane of source byte e1, lane of e2 (0 for e2 < 0)}
+        auto lanes = [&](int e1, int e2) -> uint32_t {
+            const uint32_t a = (e1 & 1) ? vo[e1 >> 2] : ve[e1 >> 2];
+            const uint32_t s1 = ((e1 >> 1) & 1) ? 0x32u : 0x10u;
+            if (e2 < 0)
+                return __byte_perm(a, 0u, s1 | 0x4400u);
+            const uint32_t b = (e2 & 1) ? vo[e2 >> 2] : ve[e2 >> 2];
+            const bool same = (e1 & 1) == (e2 & 1) && (e1 >> 2) == (e2 >> 2);
+            const uint32_t s2 = ((e2 >> 1) & 1) ? (same ? 0x32u : 0x76u) : (same ? 0x10u : 0x54u);
+            return __byte_perm(a, same ? 0u : b, s1 | (s2 << 8));
+        };
+        uint32_t ol[PX], oh[PX];
+#pragma unroll
+        for (int i = 0; i < PX / 2; i++) {
+            const int p3 = 3 * i, p1 = 3 * i + 1, p2 = 3 * i + 2;
+            const uint32_t ml = 16 * lanes(p1 * C, p1 * C + 2) + 0x00800080u;
+            const uint32_t mh = 16 * lanes(p1 * C + 1, C == 4 ? p1 * C + 3 : -1) + 0x00800080u;
+            ol[2 * i] = 48 * lanes(p3 * C, p3 * C + 2) + ml;
+            oh[2 * i] = 48 * lanes(p3 * C + 1, C == 4 ? p3 * C + 3 : -1) + mh;
+            ol[2 * i + 1] = 48 * lanes(p2 * C, p2 * C + 2) + ml;
+            oh[2 * i + 1] = 48 * lanes(p2 * C + 1, C == 4 ? p2 * C + 3 : -1) + mh;
+        }
+        uint32_t *op = reinterpret_cast<uint32_t *>(o + PX * C * j);
+#pragma unroll
+        for (int wo = 0; wo < NWO; wo++) {
+            // output byte q C + c: byte 1 (c = 0, 1) or 3 (c = 2, 3) of
+            // ol[q] (c even) or oh[q] (c odd)
+            uint32_t reg[4], pos[4];
+            int id[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const int ob = 4 * wo + k, q = ob / C, c = ob % C;
+                reg[k] = (c & 1) ? oh[q] : ol[q];
+                id[k] = 2 * q + (c & 1);
+                pos[k] = c >= 2 ? 3u : 1u;
+            }
+            st_cs(op + wo, gather_bytes(reg, id, pos));
+        }
+    } else {
+        // vertical sums 3 a + b in 16-bit lanes (even and odd bytes)
+        uint32_t vl[NW], vh[NW];
+        const uint32_t *wa = reinterpret_cast<const uint32_t *>(ra + 12 * C * j);
+        const uint32_t *wb = reinterpret_cast<const uint32_t *>(rb + 12 * C * j);
+#pragma unroll
+        for (int i = 0; i < NW; i++) {
+            const uint32_t x = ld_cs(wa + i), y = ld_nc(wb + i);
+            vl[i] = 3 * (x & 0x00ff00ffu) + (y & 0x00ff00ffu);
+            vh[i] = 3 * ((x >> 8) & 0x00ff00ffu) + ((y >> 8) & 0x00ff00ffu);
+        }
+        // the 16-bit lane of source byte e of the group (below 2^10)
+        auto lane = [&](int e) -> uint32_t {
+            const uint32_t wv = (e & 1) ? vh[e >> 2] : vl[e >> 2];
+            return ((e >> 1) & 1) ? (wv >> 16) : (wv & 0xffffu);
+        };
+        uint32_t *op = reinterpret_cast<uint32_t *>(o + PX * C * j);
+#pragma unroll
+        for (int wo = 0; wo < NWO; wo++) {
+            uint32_t q[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const int ob = 4 * wo + k, oc = ob / C, c = ob % C, i = oc >> 1;
+                // output 2i: source 3i (3) and 3i + 1 (1); 2i + 1: 3i + 1 (1) and 3i + 2 (3)
+                const uint32_t x3 = lane(((oc & 1) ? 3 * i + 2 : 3 * i) * C + c);
+                const uint32_t x1 = lane((3 * i + 1) * C + c);
+                q[k] = (3 * x3 + x1 + 8) >> 4;
+            }
+            st_cs(op + wo, q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24));
+        }
+    }
+}
+
 }  // namespace dev
 }  // namespace rz

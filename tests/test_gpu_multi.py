@@ -89,6 +89,33 @@ def test_multi_exact_2x_forms(rz, C, pad, off):
         np.testing.assert_array_equal(g, want(img, OH, OW, 1), err_msg=str((H, W, OH, OW)))
 
 
+# exact 3:2 downscales (the generic form: weights 1536 and 512 from the
+# stepped positions), including cfg2's 1080p -> 720p
+EXACT32 = [(24, 48, 16, 32), (33, 45, 22, 30), (9, 3, 6, 2), (150, 603, 100, 402), (3, 1563, 2, 1042),
+           (1080, 1920, 720, 1280)]
+
+
+@pytest.mark.parametrize("C", [1, 3, 4])
+@pytest.mark.parametrize("pad,off", [(0, 0), (4, 0), (3, 1)])
+def test_multi_exact_three_halves_form(rz, C, pad, off):
+    imgs, got, st = run_jobs(rz, EXACT32, C, 1, seed=3 * C + pad + off, pad=pad, off=off)
+    assert st == rz.RZ_OK
+    for img, g, (H, W, OH, OW) in zip(imgs, got, EXACT32):
+        np.testing.assert_array_equal(g, want(img, OH, OW, 1), err_msg=str((H, W, OH, OW)))
+
+
+@pytest.mark.parametrize("n", [64, 256])
+def test_multi_long_row_runs(rz, n):
+    # the benchmark's mix of geometries (every form: 2x down, 2x up, and two
+    # generic ratios) at a quarter of its job count and at its full count
+    geoms = [[(480, 640, 240, 320), (720, 1280, 224, 224), (240, 320, 480, 640), (600, 800, 300, 300)][k % 4]
+             for k in range(n)]
+    imgs, got, st = run_jobs(rz, geoms, 3, 1, seed=n)
+    assert st == rz.RZ_OK
+    for img, g, (H, W, OH, OW) in zip(imgs, got, geoms):
+        np.testing.assert_array_equal(g, want(img, OH, OW, 1))
+
+
 def test_multi_many_jobs(rz):
     rng = np.random.default_rng(9)
     geoms = [tuple(int(v) for v in rng.integers(1, 40, 4)) for _ in range(600)]
