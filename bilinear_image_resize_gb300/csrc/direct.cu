@@ -283,13 +283,13 @@ __device__ __forceinline__ uint32_t lane_pair(const uint32_t (&lo)[NW], const ui
     return __byte_perm(src[w], src[w1], 0x5432);   // upper lane of word w, lower lane of w + 1
 }
 
-// CTAs per SM that the register budget of each form is set for: the most at
-// which that form compiles without spills (six for one and three channels,
-// five for three channels under mirror, four for four channels).  The kernel
-// is issue- and latency-bound, so more resident warps shorten it.
+// CTAs per SM that the register budget is set for: six, the most at which
+// the one-channel form (the only one launched: three and four channels take
+// k_up2_rows) compiles without spills under every border rule.  The kernel is
+// issue- and latency-bound, so more resident warps shorten it.
 template <int C, int BORDER>
 struct Up2Occupancy {
-    static constexpr int value = C == 4 ? 4 : (C == 3 && BORDER == RZ_BORDER_MIRROR ? 5 : 6);
+    static constexpr int value = 6;
 };
 
 template <int C, int BORDER>
@@ -1007,14 +1007,12 @@ const void *direct_f32_kernel_for(int C, bool wrap)
 const void *direct_up2_kernel_for(int C, int border)
 {
     using Fn = void (*)(const KArgs, const CUtensorMap);
-    static const Fn k[3][3] = {
-        {k_up2_direct<1, RZ_BORDER_CLAMP>, k_up2_direct<3, RZ_BORDER_CLAMP>, k_up2_direct<4, RZ_BORDER_CLAMP>},
-        {k_up2_direct<1, RZ_BORDER_MIRROR>, k_up2_direct<3, RZ_BORDER_MIRROR>, k_up2_direct<4, RZ_BORDER_MIRROR>},
-        {k_up2_direct<1, RZ_BORDER_WRAP>, k_up2_direct<3, RZ_BORDER_WRAP>, k_up2_direct<4, RZ_BORDER_WRAP>}};
-    const int ci = (C == 1) ? 0 : (C == 3 ? 1 : (C == 4 ? 2 : -1));
-    if (ci < 0 || border < 0 || border > 2)
+    // one channel only: three and four channels take k_up2_rows
+    static const Fn k[3] = {k_up2_direct<1, RZ_BORDER_CLAMP>, k_up2_direct<1, RZ_BORDER_MIRROR>,
+                            k_up2_direct<1, RZ_BORDER_WRAP>};
+    if (C != 1 || border < 0 || border > 2)
         return nullptr;
-    return reinterpret_cast<const void *>(k[border][ci]);
+    return reinterpret_cast<const void *>(k[border]);
 }
 
 const void *direct_up2_rows_kernel_for(int C, int border)
