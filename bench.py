@@ -85,6 +85,10 @@ WORKLOADS["4k_to_1080p_rgba"] = ("4K->1080p RGBA u8 bilinear (exact kernel)", "u
                                   "linear", 1)
 WORKLOADS["4k_to_1080p_rgba_texture"] = ("4K->1080p RGBA u8 bilinear through the texture unit (hardware filtering, "
                                           "not bit-exact)", "tex", 2160, 3840, 1080, 1920, 4, "linear", 1)
+WORKLOADS["4k_to_1366x768"] = ("4K->1366x768 RGB u8 bilinear (no exact ratio: the any-ratio direct kernel)", "u8",
+                                2160, 3840, 768, 1366, 3, "linear", 1)
+WORKLOADS["720p_to_1080p"] = ("1280x720->1920x1080 RGB u8 bilinear upscale (1.5x: the row-separable streaming kernel)",
+                              "u8", 720, 1280, 1080, 1920, 3, "linear", 1)
 WORKLOADS["multi_256_mixed"] = ("256 RGB u8 bilinear resizes of 4 mixed small geometries (640x480->320x240, "
                                  "1280x720->224x224, 320x240->640x480, 800x600->300x300) in one launch",
                                  "multi", 0, 0, 0, 0, 3, "linear", 256)

@@ -375,7 +375,7 @@ int resident_ctas(int dev, const void *fn, int block, int *out)
 }
 
 constexpr int kStreamCtaSmem = 74 * 1024;   // three streaming CTAs per SM
-constexpr int kStreamMinRows = 16;          // shortest automatic unit (the filter's halo adds 2 rows)
+constexpr int kStreamMinRows = 8;           // shortest automatic unit (the filter's halo adds 2 rows)
 
 // Units, ring and grid of a streaming kernel (stream.cu).  Units are strips
 // of up to the kernel's widest strip (filter_strip / stream_u8_strip),

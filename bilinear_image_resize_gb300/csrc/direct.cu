@@ -91,8 +91,29 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
     constexpr int RUN = 4;
     grid_launch_dependents();
     bounds_begin(a);
-    grid_dependency_wait();
     const int gpr = (a.OW + RUN - 1) / RUN;
+    if (first_wave_cta(a)) {
+        // the CTA's source spans into L2 before the dependency wait: one
+        // piece per (output row, tap row) of its items, the columns from the
+        // plan's tables (written when the plan was made, never by a kernel, so
+        // they may be read before the wait)
+        const int g0 = blockIdx.x * kDirectThreads, g1 = min(g0 + kDirectThreads, a.OH * gpr);
+        const int d0 = g0 / gpr, nr = (g1 - 1) / gpr - d0 + 1;
+        const int piece = threadIdx.x;
+        if (g0 < g1 && piece < 2 * nr && (LINEAR || (piece & 1) == 0)) {
+            const int dy = d0 + (piece >> 1);
+            const int jlo = max(g0 - dy * gpr, 0), jhi = min(g1 - dy * gpr, gpr);
+            const int y0 = ld_nc(a.yt + dy).x;
+            const int r = (piece & 1) ? far_tap<WRAP>(y0, a.H) : y0;
+            const int xlo = ld_nc(a.xt + jlo * RUN).x, xhi = ld_nc(a.xt + min(jhi * RUN, a.OW) - 1).x;
+            const long long b0 = static_cast<long long>(xlo) * C;
+            const long long b1 = min(static_cast<long long>(xhi + 2) * C, static_cast<long long>(a.W) * C);
+            if (b1 > b0)
+                l2_prefetch_span(a.src + (long long)blockIdx.y * a.src_bstride + (long long)r * a.src_pitch + b0,
+                                 b1 - b0);
+        }
+    }
+    grid_dependency_wait();
     const int idx = blockIdx.x * kDirectThreads + threadIdx.x;
     if (idx >= a.OH * gpr)
         return;

@@ -468,7 +468,8 @@ RZ_API int resize_plan_set_tile(rz_plan p, int kind, int tile_rows, int tile_col
  *                       override is set; 1: staged tiles.  Same arithmetic;
  *   RZ_OPT_L2_PREFETCH  value 1 (default) or 0: the exact-ratio uint8 kernels
  *                       (2x down, bilinear, nearest and gray; 3:2 down; 2x
- *                       up) ask for the source rows each CTA reads to be
+ *                       up) and the any-ratio direct-load one ask for the
+ *                       source rows each CTA reads to be
  *                       moved into L2 as soon as the CTA is resident, before
  *                       it waits for the previous kernel in the stream (with
  *                       RZ_OPT_PDL, while that kernel finishes).  A prefetch

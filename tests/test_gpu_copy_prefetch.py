@@ -89,12 +89,17 @@ def _run(rz, img, OH, OW, mode, prefetch, border=0, epi=None):
 
 # (H, W, OH, OW, C, mode, border): the exact 2x down (bilinear, nearest),
 # 3:2 down and 2x up kernels (layouts that take their vector paths), every
-# channel count, the border rules of the upscale, odd sizes
+# channel count, the border rules of the upscale, odd sizes; then the any-ratio
+# direct kernel (spans from the plan's tables: wide and narrow rows, CTAs
+# that cover several output rows, both modes, the wrap rule's far tap)
 EXACT_CASES = [
     (2160, 3840, 1080, 1920, 3, 1, 0), (2160, 3840, 1080, 1920, 3, 0, 0), (540, 976, 270, 488, 1, 1, 0),
     (540, 968, 270, 484, 4, 0, 0), (1080, 1920, 720, 1280, 3, 1, 0), (333, 1047, 222, 698, 4, 1, 0),
     (90, 132, 60, 88, 1, 1, 0), (1080, 1920, 2160, 3840, 3, 1, 0), (77, 131, 154, 262, 4, 1, 1),
     (77, 131, 154, 262, 1, 1, 2), (61, 50, 122, 100, 3, 1, 1),
+    (2160, 3840, 768, 1366, 3, 1, 0), (1080, 1920, 600, 1000, 4, 1, 0), (720, 1280, 224, 224, 3, 1, 0),
+    (300, 500, 77, 31, 1, 1, 0), (1080, 1920, 600, 1000, 3, 0, 0), (303, 405, 101, 135, 3, 1, 2),
+    (303, 405, 101, 135, 4, 1, 1),
 ]
 
 
