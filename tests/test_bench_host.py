@@ -111,6 +111,9 @@ def test_reference_arm_line_carries_the_contract_keys(monkeypatch):
     # 720 -> 224: taps 3.2 rows apart, two distinct rows per output row
     ("batch64_720p_to_224_norm", 64 * 448 * 1280 * 3, 64 * 3 * 224 * 224 * 4),
     ("f32_8192_to_5980_filter3x3", 8192 * 8192 * 4, 5980 * 5980 * 4),
+    # 2160 -> 768: taps 2.8 rows apart, two distinct rows per output row
+    ("4k_to_1366x768", 2 * 768 * 3840 * 3, 768 * 1366 * 3),
+    ("720p_to_1080p", 720 * 1280 * 3, 1080 * 1920 * 3),             # an upscale taps every row
 ])
 def test_algorithmic_bytes_of_the_workloads(workload, read, write):
     # the roofline's numerator: source rows the taps read plus the output,
