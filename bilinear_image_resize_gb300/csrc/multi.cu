@@ -226,7 +226,7 @@ __device__ __forceinline__ void multi_down2(const rz_job &J, int g, int y0, int 
 }
 
 // Exact 2x upscale form: source columns 4 g .. 4 g + 3 of source rows
-// r0 .. r0 + kMultiRows / 2 - 1 (those below H), output rows 2 r0 ..; the
+// r0 .. r0 + kUp2Rows - 1 (those below H), output rows 2 r0 ..; the
 // unpacked rows above, at and below the current one kept in registers.
 template <int C>
 __device__ __forceinline__ void multi_up2(const rz_job &J, int g, int r0)
