@@ -84,7 +84,8 @@ __global__ void __launch_bounds__(kDirectThreads) k_down2_direct(const KArgs a, 
 // 32-bit words when the output layout allows.  WRAP: the plan's border rule
 // is wrap, whose edge entries hold the last sample as the near tap, and the
 // far tap past the last sample is sample 0 (far_tap); the clamp and mirror
-// rules are in the tables alone.
+// rules are in the tables alone.  First-wave CTAs prefetch the source spans
+// of their items into L2 before the dependency wait (first_wave_cta).
 template <int C, int LINEAR, bool WRAP>
 __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const __grid_constant__ CUtensorMap)
 {
@@ -200,11 +201,11 @@ __global__ void __launch_bounds__(kDirectThreads) k_direct(const KArgs a, const 
 // A1 t1) + B1 (...) + 2^21) >> 22 equals (sum of b a t + 8) >> 4 with a, b in
 // {1, 3} (CUDA interpolation page §2.2, §6.2); no tap leaves the image.  A
 // thread forms eight output pixels of one row from the two source rows it
-// samples over twelve source columns: 12 C bytes per row in 3 C aligned
-// words, split into 16-bit lanes (even and odd bytes); the vertical 3-1 sum
-// is lane-wise, and each output byte takes (3 v + v' + 8) >> 4 from two
-// lanes at compile-time positions.  The row's last pixels
-// (fewer than eight) take a byte path.  (Written as a loop over the images
+// samples over twelve source columns, 12 C bytes per row in 3 C aligned
+// words (down32_group: the vertical 3-1 sums lane-wise in 16-bit lanes, then
+// for three and four channels regrouped into pixel lane words so that the
+// horizontal sums take two channels per multiply-add).  The row's last
+// pixels (fewer than eight) take a byte path.  (Written as a loop over the images
 // of a batch: without it this kernel compiles to a slower schedule, 4.8
 // against 2.9 us for 1080p -> 720p.)  Requirements, checked by the host:
 // source base, pitch and batch stride multiples of 4; output ones of 4.
